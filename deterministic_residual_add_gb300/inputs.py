@@ -1,0 +1,160 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests and the oracle's.
+
+This module only draws numbers: it holds none of the method's arithmetic.
+Every tensor is made on the CPU with torch's CPU generator, in fp32, scaled
+by a standard deviation and shifted by a mean, then narrowed to bf16 by
+torch's own round-to-nearest-even cast.  The distributions follow the
+ROCm/aiter issue #5151 page ("Steps to Reproduce": randn(...) * std, weight
+randn * 0.05 + 1.0, per-step deltas from generators seeded 1000 + step); the
+bits do not match the page's, whose numbers came from a GPU generator.
+
+Workloads (n_rows x hidden, distributions as N(mean, std)):
+
+  tiny            64 x 1024   x N(0,1)     residual N(0,1)  weight N(1,0.1)  seed 0
+  2048x4096     2048 x 4096   x N(0,1)     residual N(0,4)  weight N(1,0.1)  seed 1
+  4096x8192     4096 x 8192   x N(0,1)     residual N(0,4)  weight N(1,0.1)  seed 2
+  chain4096     4096 x 4096   residual0 N(0,1) and weight N(1,0.1) from seed 3;
+                              x_k N(0,0.05) from seed 1000 + k, k = 0..71
+  quant2048x16384 2048 x 16384 x N(0,1)    residual N(0,4)  weight N(1,0.1)  seed 4
+
+Within one workload the draws come from one generator in the order
+x, residual, weight.  eps is 1e-6 everywhere.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+EPS = 1e-6
+
+
+def normal_bf16(gen: torch.Generator, shape, mean: float, std: float) -> torch.Tensor:
+    """N(mean, std) drawn in fp32 on the CPU, cast to bf16."""
+    t = torch.randn(shape, generator=gen, dtype=torch.float32)
+    return (t * std + mean).to(torch.bfloat16)
+
+
+def generator(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    n_rows: int
+    hidden: int
+    x_std: float
+    residual_std: float
+    seed: int
+    weight_mean: float = 1.0
+    weight_std: float = 0.1
+    eps: float = EPS
+    quant: bool = False
+
+    def make(self, n_rows: int | None = None):
+        """Return dict(x, residual, weight, eps) as CPU bf16 tensors.
+
+        n_rows < self.n_rows draws the full-size tensors' leading rows
+        (same bits as the full workload's first rows)."""
+        g = generator(self.seed)
+        x = normal_bf16(g, (self.n_rows, self.hidden), 0.0, self.x_std)
+        r = normal_bf16(g, (self.n_rows, self.hidden), 0.0, self.residual_std)
+        w = normal_bf16(g, (self.hidden,), self.weight_mean, self.weight_std)
+        if n_rows is not None:
+            x, r = x[:n_rows].contiguous(), r[:n_rows].contiguous()
+        return {"x": x, "residual": r, "weight": w, "eps": self.eps}
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 64, 1024, 1.0, 1.0, seed=0),
+    "2048x4096": Workload("2048x4096", 2048, 4096, 1.0, 4.0, seed=1),
+    "4096x8192": Workload("4096x8192", 4096, 8192, 1.0, 4.0, seed=2),
+    "quant2048x16384": Workload("quant2048x16384", 2048, 16384, 1.0, 4.0, seed=4, quant=True),
+}
+
+
+@dataclass(frozen=True)
+class Chain:
+    """Chained calls: residual_out of call k is the residual of call k + 1."""
+    name: str = "chain4096"
+    n_rows: int = 4096
+    hidden: int = 4096
+    depth: int = 72
+    residual0_std: float = 1.0
+    x_std: float = 0.05
+    seed: int = 3
+    delta_seed0: int = 1000
+    weight_mean: float = 1.0
+    weight_std: float = 0.1
+    eps: float = EPS
+
+    def initial(self):
+        """(residual_0, weight) as CPU bf16 tensors."""
+        g = generator(self.seed)
+        r0 = normal_bf16(g, (self.n_rows, self.hidden), 0.0, self.residual0_std)
+        w = normal_bf16(g, (self.hidden,), self.weight_mean, self.weight_std)
+        return r0, w
+
+    def delta(self, k: int) -> torch.Tensor:
+        """x_k for call k, from its own generator seeded delta_seed0 + k."""
+        return normal_bf16(generator(self.delta_seed0 + k), (self.n_rows, self.hidden),
+                           0.0, self.x_std)
+
+
+CHAIN4096 = Chain()
+
+# The page's own reproducer settings ("Steps to Reproduce", part 2): m = 256
+# rows, hidden 4096, initial state N(0,1) and weight N(1,0.05) from seed 1,
+# deltas N(0,0.5) from seeds 1000 + step, 72 calls.
+P3_CHAIN = Chain(name="p3chain", n_rows=256, hidden=4096, depth=72, residual0_std=1.0,
+                 x_std=0.5, seed=1, delta_seed0=1000, weight_mean=1.0, weight_std=0.05)
+
+
+def p3_rounding_probe_inputs():
+    """The page's part 1: three (m, x std, residual std) settings drawn in order
+    from one generator seeded 0, weight N(1, 0.05) each time, hidden 4096."""
+    g = generator(0)
+    cases = []
+    for m, xs, rs in [(512, 1.0, 1.0), (512, 1.0, 30.0), (4096, 3.0, 3.0)]:
+        x = normal_bf16(g, (m, 4096), 0.0, xs)
+        r = normal_bf16(g, (m, 4096), 0.0, rs)
+        w = normal_bf16(g, (4096,), 1.0, 0.05)
+        cases.append({"m": m, "x_std": xs, "residual_std": rs, "x": x, "residual": r,
+                      "weight": w, "eps": EPS})
+    return cases
+
+
+# Rounding edge patterns as bf16 bit pairs (x, residual).  With x = 1.0
+# (0x3F80) and a residual of 2^-8 the fp32 sum has exactly half a bf16 ulp
+# below the cut; the four pairs hit: tie with even kept bit, tie with odd
+# kept bit, just below half, just above half.
+EDGE_PAIRS = [
+    (0x3F80, 0x3B80),  # 1.0 + 2^-8           -> 0x3F808000 (tie, even)
+    (0x3F81, 0x3B80),  # (1 + 2^-7) + 2^-8    -> 0x3F818000 (tie, odd)
+    (0x3F80, 0x3B7F),  # 1.0 + (2^-8 - 2^-16) -> 0x3F807F80 (below half)
+    (0x3F80, 0x3B81),  # 1.0 + (2^-8 + 2^-15) -> 0x3F808100 (above half)
+]
+
+
+def edge_rows(n_rows: int = 16, hidden: int = 1024, seed: int = 0):
+    """Rows whose elements cycle through EDGE_PAIRS and their negatives.
+
+    Element (i, j) takes pattern (i + j) mod 8; patterns 4..7 are 0..3 with
+    both signs flipped.  Weight N(1, 0.1) from `seed`."""
+    pats = [(x, r) for x, r in EDGE_PAIRS] + [(x | 0x8000, r | 0x8000) for x, r in EDGE_PAIRS]
+    xs = np.array([p[0] for p in pats], dtype=np.uint16)
+    rs = np.array([p[1] for p in pats], dtype=np.uint16)
+    idx = (np.arange(n_rows)[:, None] + np.arange(hidden)[None, :]) % len(pats)
+    x = torch.from_numpy(xs[idx].view(np.int16).copy()).view(torch.bfloat16)
+    r = torch.from_numpy(rs[idx].view(np.int16).copy()).view(torch.bfloat16)
+    w = normal_bf16(generator(seed), (hidden,), 1.0, 0.1)
+    return {"x": x.contiguous(), "residual": r.contiguous(), "weight": w, "eps": EPS}
+
+
+def bits(t: torch.Tensor) -> torch.Tensor:
+    """bf16 tensor -> int16 view of its bits (no arithmetic)."""
+    return t.view(torch.int16)

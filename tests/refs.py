@@ -1,0 +1,246 @@
+"""Independent references for the tests: fp64 closed forms, exact rational
+rounding, ULP helpers and the page's bias metric.
+
+None of this is the oracle; it exists to pin the oracle (and, through it,
+the CUDA path) to something other than itself.
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+from pathlib import Path
+
+import numpy as np
+import torch
+
+GOLDEN = Path(__file__).resolve().parent / "golden"
+
+
+def load_golden(name: str) -> dict:
+    vals = {}
+    for line in (GOLDEN / name).read_text().splitlines():
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        k, v = (s.strip() for s in line.split("=", 1))
+        vals[k] = float(v)
+    return vals
+
+
+# ---------------------------------------------------------------- bit views
+def u16(t) -> np.ndarray:
+    """bf16 tensor / uint16-compatible array -> numpy uint16 bit patterns."""
+    if isinstance(t, torch.Tensor):
+        t = t.detach().cpu().contiguous()
+        if t.dtype == torch.bfloat16:
+            t = t.view(torch.int16)
+        return t.numpy().view(np.uint16)
+    a = np.asarray(t)
+    return a.view(np.uint16) if a.dtype == np.int16 else a.astype(np.uint16, copy=False)
+
+
+def bf16_value(b) -> np.ndarray:
+    """bf16 bit patterns -> float64 values (exact)."""
+    b = u16(b)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def f32_bits(v) -> np.ndarray:
+    return np.asarray(v, dtype=np.float32).view(np.uint32)
+
+
+def ulp_bf16(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values around |v|: 2^(floor(log2|v|) - 7), never below
+    the subnormal spacing 2^-133."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    u = np.exp2(e - 7)
+    return np.where(a > 0, np.maximum(u, 2.0 ** -133), 2.0 ** -133)
+
+
+# ------------------------------------------------------- fp64 closed forms
+def add_rmsnorm_f64(x, residual, weight, eps: float):
+    """The page's reference() evaluated in fp64 with no intermediate rounding
+    except eps, taken as the fp32 value the kernels receive."""
+    acc = bf16_value(x) + bf16_value(residual)
+    var = np.mean(acc * acc, axis=-1, keepdims=True)
+    inv = 1.0 / np.sqrt(var + float(np.float32(eps)))
+    y = acc * inv * bf16_value(weight)
+    return y, acc
+
+
+def quant_f64(y64: np.ndarray):
+    amax = np.max(np.abs(y64), axis=-1)
+    scale = amax / 127.0
+    safe = np.where(scale > 0, scale, 1.0)
+    q = np.clip(np.rint(y64 / safe[..., None]), -127, 127)
+    q = np.where(scale[..., None] > 0, q, 0)
+    return q.astype(np.int64), scale
+
+
+# ------------------------------------------------ exact rational rounding
+def rn32(q: Fraction) -> np.float32:
+    """Round a rational to the nearest fp32 value, ties to even, with
+    subnormals and overflow to infinity (IEEE 754 binary32)."""
+    if q == 0:
+        return np.float32(0.0)
+    neg = q < 0
+    a = -q if neg else q
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    quantum_exp = max(e, -126) - 23
+    scaled = a / (Fraction(2) ** quantum_exp)
+    m = scaled.numerator // scaled.denominator
+    rem = scaled - m
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and m % 2 == 1):
+        m += 1
+    val = Fraction(m) * Fraction(2) ** quantum_exp
+    if val >= Fraction(2) ** 128:
+        r = np.float32(np.inf)
+    else:
+        r = np.float32(float(val))  # exact: val is an fp32 value
+        assert Fraction(float(r)) == val
+    return np.float32(-r) if neg else r
+
+
+def frac(v) -> Fraction:
+    return Fraction(float(v))
+
+
+def sqrt_rn32(v) -> np.float32:
+    """Correctly rounded fp32 square root of a non-negative rational (or fp32
+    value), computed with integer square roots (no floating point)."""
+    q = v if isinstance(v, Fraction) else frac(v)
+    assert q >= 0
+    if q == 0:
+        return np.float32(0.0)
+    k = 400
+    num = q.numerator << (2 * k)
+    s = math.isqrt(num // q.denominator)
+    # sqrt(q) lies in [s, s+1) / 2^k.  The square root of a binary32 value is
+    # never a midpoint between two binary32 values, and 2^-400 resolution is
+    # far below half an ulp of any binary32 result.
+    lo = rn32(Fraction(s, 1 << k))
+    hi = rn32(Fraction(s + 1, 1 << k))
+    assert lo == hi, "sqrt too close to a rounding boundary for this resolution"
+    return lo
+
+
+def rne_bf16_exact(v: np.float32) -> int:
+    """Nearest bf16 to an fp32 value, ties to even, decided with rationals."""
+    f = frac(v)
+    if f == 0:
+        return int(np.float32(v).view(np.uint32)) >> 16
+    neg = f < 0
+    a = -f if neg else f
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    quantum_exp = max(e, -126) - 7
+    scaled = a / (Fraction(2) ** quantum_exp)
+    m = scaled.numerator // scaled.denominator
+    rem = scaled - m
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and m % 2 == 1):
+        m += 1
+    val = Fraction(m) * Fraction(2) ** quantum_exp
+    if val >= Fraction(2) ** 128:
+        bits = 0x7F80
+    else:
+        bits = int(np.float32(float(val)).view(np.uint32)) >> 16
+    return bits | (0x8000 if neg else 0)
+
+
+def row_exact(x_bits, r_bits, w_bits, eps: float, *, mul_order: str = "left",
+              mean_op: str = "div", inv_op: str = "recip_of_sqrt", quant: bool = False,
+              quant_op: str = "div"):
+    """One row of the method with every operation rounded by rn32.
+
+    Defaults are the readings the oracle states: pairwise tree over the
+    zero-padded row, mean = S / hidden, inv = 1 / sqrt(mean + eps) with both
+    operations rounded, y = (acc * inv) * w.  The keyword options evaluate
+    the alternative readings (mul_order="right": acc * (inv * w);
+    mean_op="recip": S * (1 / hidden); inv_op="rsqrt": 1/sqrt rounded once;
+    quant_op="recip": y * (1 / scale))
+    so a test can show an input tells the readings apart.
+
+    Returns dict(ro, out, y, S, inv) and, with quant, also q and scale."""
+    xs = [frac(bf16_value(np.uint16(b))) for b in x_bits]
+    rs = [frac(bf16_value(np.uint16(b))) for b in r_bits]
+    ws = [frac(bf16_value(np.uint16(b))) for b in w_bits]
+    h = len(xs)
+    acc = [rn32(a + b) for a, b in zip(xs, rs)]
+    sq = [rn32(frac(a) * frac(a)) for a in acc]
+    p = 1
+    while p < h:
+        p *= 2
+    level = [frac(s) for s in sq] + [Fraction(0)] * (p - h)
+    while len(level) > 1:
+        level = [frac(rn32(level[i] + level[i + 1])) for i in range(0, len(level), 2)]
+    S = rn32(level[0])
+    if mean_op == "div":
+        mean = rn32(frac(S) / h)
+    else:
+        mean = rn32(frac(S) * frac(rn32(Fraction(1, h))))
+    v = rn32(frac(mean) + frac(np.float32(eps)))
+    if inv_op == "recip_of_sqrt":
+        inv = rn32(Fraction(1) / frac(sqrt_rn32(v)))
+    else:
+        inv = sqrt_rn32(Fraction(1) / frac(v))
+    if mul_order == "left":
+        ys = [rn32(frac(rn32(frac(a) * frac(inv))) * w) for a, w in zip(acc, ws)]
+    else:
+        ys = [rn32(frac(a) * frac(rn32(frac(inv) * w))) for a, w in zip(acc, ws)]
+    res = {"ro": [rne_bf16_exact(a) for a in acc], "out": [rne_bf16_exact(y) for y in ys],
+           "y": ys, "S": S, "inv": inv}
+    if quant:
+        amax = max((abs(frac(y)) for y in ys), default=Fraction(0))
+        scale = rn32(amax / 127)
+        qs = []
+        for y in ys:
+            if scale == 0:
+                qs.append(0)
+                continue
+            if quant_op == "div":
+                t = frac(rn32(frac(y) / frac(scale)))
+            else:
+                t = frac(rn32(frac(y) * frac(rn32(Fraction(1) / frac(scale)))))
+            n = math.floor(t)
+            rem = t - n
+            if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+                n += 1
+            qs.append(max(-127, min(127, n)))
+        res["q"], res["scale"] = qs, scale
+    return res
+
+
+# ------------------------------------------------------------- metrics
+def magnitude_bias(got_bits, exp_bits) -> float:
+    """The page's magnitude_bias(): mean over e != 0 of (|g| - |e|) / |e|;
+    negative means shrunk toward zero."""
+    g, e = bf16_value(got_bits), bf16_value(exp_bits)
+    nz = e != 0
+    return float(((np.abs(g[nz]) - np.abs(e[nz])) / np.abs(e[nz])).mean())
+
+
+def magnitude_bias_values(got_bits, exp_values: np.ndarray) -> float:
+    """Same metric against real-valued expectations (e.g. fp64 or fp32 acc)."""
+    g = bf16_value(got_bits)
+    e = np.asarray(exp_values, dtype=np.float64)
+    nz = e != 0
+    return float(((np.abs(g[nz]) - np.abs(e[nz])) / np.abs(e[nz])).mean())
+
+
+def rms(v: np.ndarray) -> float:
+    v = np.asarray(v, dtype=np.float64)
+    return float(np.sqrt(np.mean(v * v)))
+
+
+def cos_sim(a: np.ndarray, b: np.ndarray) -> float:
+    a = np.asarray(a, dtype=np.float64).ravel()
+    b = np.asarray(b, dtype=np.float64).ravel()
+    return float(a @ b / math.sqrt((a @ a) * (b @ b)))

@@ -1,0 +1,63 @@
+"""Each plausible slip planted in a copy of the oracle's C source must fail
+at least one pin of tests/pins.py.  The copies are built into a temporary
+directory; the real oracle source is never touched."""
+import pytest
+
+import oracle
+import pins
+
+S = oracle.SOURCE.read_text()
+
+MUTANTS = {
+    "add_becomes_subtract": (
+        "acc[i] = oracle_bf16_to_f32(x[i]) + oracle_bf16_to_f32(residual[i]);",
+        "acc[i] = oracle_bf16_to_f32(x[i]) - oracle_bf16_to_f32(residual[i]);"),
+    "eps_dropped": ("float var_eps = mean + eps;", "float var_eps = mean;"),
+    "mean_over_padded_length": ("float mean = sum_sq / (float)hidden;",
+                                "float mean = sum_sq / (float)padded;"),
+    "mean_by_reciprocal": ("float mean = sum_sq / (float)hidden;",
+                           "float mean = sum_sq * (1.0f / (float)hidden);"),
+    "weight_index_reversed": ("y[i] = normed * oracle_bf16_to_f32(weight[i]);",
+                              "y[i] = normed * oracle_bf16_to_f32(weight[hidden - 1 - i]);"),
+    "last_square_dropped": ("sq[i] = acc[i] * acc[i];",
+                            "sq[i] = (i + 1 < hidden) ? acc[i] * acc[i] : 0.0f;"),
+    "sequential_sum": ("float sum_sq = pairwise_pow2(sq, padded);",
+                       "float sum_sq = 0.0f; for (int64_t k = 0; k < padded; ++k) sum_sq += sq[k];"),
+    "multiply_reassociated": (
+        "float normed = acc[i] * inv_rms;\n        y[i] = normed * oracle_bf16_to_f32(weight[i]);",
+        "y[i] = acc[i] * (inv_rms * oracle_bf16_to_f32(weight[i]));"),
+    "rsqrt_rounded_once": ("float inv_rms = 1.0f / root;",
+                           "inv_rms_unused: ; float inv_rms = (float)(1.0 / sqrt((double)var_eps)); (void)root;"),
+    "ties_toward_zero": ("return (lo & 1u) ? (uint16_t)(lo + 1u) : lo;", "return lo;"),
+    "ties_to_odd": ("return (lo & 1u) ? (uint16_t)(lo + 1u) : lo;",
+                    "return (lo & 1u) ? lo : (uint16_t)(lo + 1u);"),
+    "ties_away_in_rne": ("if (discarded > 0x8000u)", "if (discarded >= 0x8000u)"),
+    "widen_wrong_shift": ("return f32_from_bits((uint32_t)b << 16);",
+                          "return f32_from_bits((uint32_t)b << 15);"),
+    "out_store_truncates": ("out[base + i] = store_bf16(y[i], store_mode);",
+                            "out[base + i] = store_bf16(y[i], ORACLE_STORE_TRUNC);"),
+    "residual_out_from_x": ("residual_out[i] = store_bf16(acc[i], store_mode);",
+                            "residual_out[i] = store_bf16(oracle_bf16_to_f32(x[i]), store_mode);"),
+    "quant_scale_128": ("float s = amax / 127.0f;", "float s = amax / 128.0f;"),
+    "quant_truncating_round": ("q = round_half_even_to_int(y[i] / s);", "q = (int32_t)(y[i] / s);"),
+    "quant_by_reciprocal": ("q = round_half_even_to_int(y[i] / s);",
+                            "q = round_half_even_to_int(y[i] * (1.0f / s));"),
+    "quant_amax_without_abs": ("amax = fmaxf(amax, fabsf(y[i]));", "amax = fmaxf(amax, y[i]);"),
+}
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    assert S.count(old) == 1, f"mutation site for {name} not found exactly once"
+    src = tmp_path / f"{name}.c"
+    src.write_text(S.replace(old, new))
+    lib = oracle.Oracle(oracle.compile_source(src, tmp_path / f"lib{name}.so"))
+    caught = []
+    for pin in pins.FAST_PINS:
+        try:
+            pin(lib)
+        except Exception:  # noqa: BLE001 - any failure of a pin counts
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin"
