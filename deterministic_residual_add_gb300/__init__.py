@@ -1,0 +1,253 @@
+"""Deterministic fused residual-add + RMSNorm forward for GB300 (sm_103a).
+
+Thin Python binding of the C ABI in include/dradd.h (libdradd.so): it only
+marshals arguments (tensor pointers, sizes, the current CUDA stream) and
+turns status codes into exceptions.  Every step of the computation runs in
+the CUDA kernels of the library; there is no Python or CPU fallback, and
+every call fails loudly if the library cannot be loaded.
+
+    from deterministic_residual_add_gb300 import add_rmsnorm_fwd
+    out, residual_out = add_rmsnorm_fwd(x, residual, weight, eps)
+
+The operation is rmsnorm2d_fwd_with_add as defined on the ROCm/aiter issue
+#5151 page ("Steps to Reproduce", reference()), with round-to-nearest-even
+bf16 stores and a reduction order that never depends on the launch.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from pathlib import Path
+
+__all__ = [
+    "add_rmsnorm_fwd", "add_rmsnorm_quant_fwd", "add_rmsnorm_fwd_with_config",
+    "add_rmsnorm_quant_fwd_with_config", "LaunchConfig", "DraddError", "resolve_config",
+    "device_status", "bf16_convert_range", "status_string", "abi_version", "lib", "library_path",
+    "VARIANT_AUTO", "VARIANT_ROWS", "VARIANT_STAGED", "MAX_HIDDEN",
+]
+
+PKG = Path(__file__).resolve().parent
+LIB_PATH = PKG / "libdradd.so"
+MAX_HIDDEN = 32768
+VARIANT_AUTO, VARIANT_ROWS, VARIANT_STAGED = 0, 1, 2
+
+STATUS_NAMES = {
+    0: "OK", 1: "NULL_PTR", 2: "BAD_SHAPE", 3: "UNSUPPORTED_HIDDEN", 4: "MISALIGNED",
+    5: "BAD_EPS", 6: "ALIAS", 7: "CUDA", 8: "TIMEOUT", 9: "BAD_CONFIG",
+}
+
+
+class DraddError(RuntimeError):
+    """A non-zero status from libdradd."""
+
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+class _LaunchCfg(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "variant", "threads_per_row", "rows_per_cta", "grid_ctas", "stages", "fault_inject",
+        "wait_limit_us", "reserved")]
+
+
+@dataclass
+class LaunchConfig:
+    """Mirror of dradd_launch_cfg; 0 = automatic.  Never changes results."""
+    variant: int = 0
+    threads_per_row: int = 0
+    rows_per_cta: int = 0
+    grid_ctas: int = 0
+    stages: int = 0
+    fault_inject: int = 0
+    wait_limit_us: int = 0
+
+    def _c(self) -> _LaunchCfg:
+        return _LaunchCfg(self.variant, self.threads_per_row, self.rows_per_cta, self.grid_ctas,
+                          self.stages, self.fault_inject, self.wait_limit_us, 0)
+
+    @staticmethod
+    def _from_c(c: _LaunchCfg) -> "LaunchConfig":
+        return LaunchConfig(c.variant, c.threads_per_row, c.rows_per_cta, c.grid_ctas, c.stages,
+                            c.fault_inject, c.wait_limit_us)
+
+
+_lib = None
+_vp, _i64, _f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float
+
+
+def library_path() -> Path:
+    return LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libdradd.so (built by deterministic_residual_add_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not LIB_PATH.exists():
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -m deterministic_residual_add_gb300.build` (needs nvcc)")
+    L = ctypes.CDLL(str(LIB_PATH))
+    bf16_args = [_vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp]
+    quant_args = [_vp, _vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp]
+    cfgp = ctypes.POINTER(_LaunchCfg)
+    for name, args in [("add_rmsnorm_fwd", bf16_args),
+                       ("add_rmsnorm_quant_fwd", quant_args),
+                       ("add_rmsnorm_fwd_with_config", bf16_args + [cfgp]),
+                       ("add_rmsnorm_quant_fwd_with_config", quant_args + [cfgp]),
+                       ("dradd_resolve_config", [_i64, _i64, ctypes.c_int, ctypes.c_int, cfgp]),
+                       ("dradd_device_status", [_vp, ctypes.c_int]),
+                       ("dradd_bf16_convert_range", [_vp, ctypes.c_uint64, _i64, ctypes.c_int, _vp])]:
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    L.dradd_status_string.argtypes = [ctypes.c_int]
+    L.dradd_status_string.restype = ctypes.c_char_p
+    L.dradd_abi_version.argtypes = []
+    L.dradd_abi_version.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().dradd_status_string(int(status)).decode()
+
+
+def abi_version() -> int:
+    return int(lib().dradd_abi_version())
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise DraddError(status, where)
+
+
+# ----------------------------------------------------------- tensor marshalling
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream, device) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _bf16_ptr(t, name: str, n: int | None = None) -> int:
+    torch = _torch()
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"{name} must hold bf16 (got {t.dtype})")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if n is not None and t.numel() != n:
+        raise ValueError(f"{name} has {t.numel()} elements, expected {n}")
+    return t.data_ptr()
+
+
+def _shape(x, hidden):
+    hidden = int(x.shape[-1]) if hidden is None else int(hidden)
+    n_rows = x.numel() // hidden if hidden > 0 else 0
+    return n_rows, hidden
+
+
+def add_rmsnorm_fwd(x, residual, weight, eps: float = 1e-6, *, out=None, residual_out=None,
+                    stream=None, config: LaunchConfig | None = None):
+    """out, residual_out = rmsnorm2d_fwd_with_add(x, residual, weight, eps).
+
+    x, residual: CUDA bf16 tensors [..., hidden]; weight: [hidden].  out and
+    residual_out are allocated like x unless given (residual_out may be
+    `residual` itself, out may be `x`).  Enqueued on `stream` (default: the
+    current stream of x's device)."""
+    torch = _torch()
+    n_rows, hidden = _shape(x, None)
+    n = n_rows * hidden
+    if out is None:
+        out = torch.empty_like(x)
+    if residual_out is None:
+        residual_out = torch.empty_like(x)
+    args = (_bf16_ptr(out, "out", n), _bf16_ptr(residual_out, "residual_out", n),
+            _bf16_ptr(x, "x", n), _bf16_ptr(residual, "residual", n),
+            _bf16_ptr(weight, "weight", hidden), float(eps), n_rows, hidden,
+            _stream_handle(stream, x.device))
+    with torch.cuda.device(x.device):
+        if config is None:
+            _check(lib().add_rmsnorm_fwd(*args), "add_rmsnorm_fwd")
+        else:
+            c = config._c()
+            _check(lib().add_rmsnorm_fwd_with_config(*args, ctypes.byref(c)),
+                   "add_rmsnorm_fwd_with_config")
+    return out, residual_out
+
+
+def add_rmsnorm_quant_fwd(x, residual, weight, eps: float = 1e-6, *, out_q=None, scale=None,
+                          residual_out=None, stream=None, config: LaunchConfig | None = None):
+    """out_q (int8), scale (fp32 per row), residual_out (bf16) of the quant variant."""
+    torch = _torch()
+    n_rows, hidden = _shape(x, None)
+    n = n_rows * hidden
+    if out_q is None:
+        out_q = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    if scale is None:
+        scale = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    if residual_out is None:
+        residual_out = torch.empty_like(x)
+    if out_q.dtype != torch.int8 or not out_q.is_cuda or not out_q.is_contiguous() or out_q.numel() != n:
+        raise ValueError("out_q must be a contiguous CUDA int8 tensor shaped like x")
+    if (scale.dtype != torch.float32 or not scale.is_cuda or not scale.is_contiguous()
+            or scale.numel() != n_rows):
+        raise ValueError("scale must be a contiguous CUDA float32 tensor with one entry per row")
+    args = (out_q.data_ptr(), scale.data_ptr(), _bf16_ptr(residual_out, "residual_out", n),
+            _bf16_ptr(x, "x", n), _bf16_ptr(residual, "residual", n),
+            _bf16_ptr(weight, "weight", hidden), float(eps), n_rows, hidden,
+            _stream_handle(stream, x.device))
+    with torch.cuda.device(x.device):
+        if config is None:
+            _check(lib().add_rmsnorm_quant_fwd(*args), "add_rmsnorm_quant_fwd")
+        else:
+            c = config._c()
+            _check(lib().add_rmsnorm_quant_fwd_with_config(*args, ctypes.byref(c)),
+                   "add_rmsnorm_quant_fwd_with_config")
+    return out_q, scale, residual_out
+
+
+def add_rmsnorm_fwd_with_config(x, residual, weight, eps, config: LaunchConfig, **kw):
+    return add_rmsnorm_fwd(x, residual, weight, eps, config=config, **kw)
+
+
+def add_rmsnorm_quant_fwd_with_config(x, residual, weight, eps, config: LaunchConfig, **kw):
+    return add_rmsnorm_quant_fwd(x, residual, weight, eps, config=config, **kw)
+
+
+def resolve_config(n_rows: int, hidden: int, quant: bool = False, sm_count: int = 152,
+                   config: LaunchConfig | None = None) -> LaunchConfig:
+    """The configuration the library would launch for this shape (no GPU
+    work when sm_count > 0)."""
+    c = (config or LaunchConfig())._c()
+    _check(lib().dradd_resolve_config(int(n_rows), int(hidden), int(bool(quant)), int(sm_count),
+                                      ctypes.byref(c)), "dradd_resolve_config")
+    return LaunchConfig._from_c(c)
+
+
+def device_status(stream=None, clear: bool = True, device=None) -> int:
+    """Synchronise the stream and return the device status (0 or TIMEOUT=8)."""
+    torch = _torch()
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(device):
+        return int(lib().dradd_device_status(_stream_handle(stream, device), int(clear)))
+
+
+def bf16_convert_range(out, first: int, count: int, method: int = 0, stream=None):
+    """Test hook: device conversion of fp32 patterns first..first+count-1."""
+    torch = _torch()
+    _check(lib().dradd_bf16_convert_range(_bf16_ptr(out, "out"), int(first), int(count), int(method),
+                                          _stream_handle(stream, out.device)),
+           "dradd_bf16_convert_range")
+    return out

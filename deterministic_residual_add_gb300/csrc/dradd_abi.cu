@@ -1,0 +1,405 @@
+// dradd_abi.cu -- the C entry points declared in include/dradd.h: argument
+// validation, launch-configuration choice, and dispatch to the kernels.
+//
+// Nothing here changes a result bit: the configuration only decides how rows
+// and blocks are spread over threads, CTAs and SMs, and the kernels combine
+// the partial sums in the same canonical pairwise order for every choice.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "dradd.h"
+#include "dradd_internal.h"
+
+namespace {
+
+using dradd::Params;
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;  // 1 s
+
+// Shared-memory and thread limits used to size grids and stages.  Defaults
+// are GB300's; with a live device they come from the device.
+struct DeviceLimits {
+    int sm_count = 152;
+    int smem_per_block_optin = 232448;  // 227 KiB
+    int smem_per_sm = 233472;           // 228 KiB
+    int max_threads_per_sm = 2048;
+    int max_blocks_per_sm = 32;
+};
+
+std::atomic<int> g_limits_ready[kMaxDevices];
+DeviceLimits g_limits[kMaxDevices];
+
+dradd_status query_limits(DeviceLimits* out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return DRADD_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices && g_limits_ready[dev].load(std::memory_order_acquire)) {
+        *out = g_limits[dev];
+        return DRADD_OK;
+    }
+    DeviceLimits L;
+    if (cudaDeviceGetAttribute(&L.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&L.smem_per_block_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&L.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&L.max_threads_per_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&L.max_blocks_per_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev) !=
+            cudaSuccess)
+        return DRADD_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices) {
+        g_limits[dev] = L;  // identical values if two threads race here
+        g_limits_ready[dev].store(1, std::memory_order_release);
+    }
+    *out = L;
+    return DRADD_OK;
+}
+
+bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
+
+int64_t next_pow2(int64_t v)
+{
+    int64_t p = 1;
+    while (p < v)
+        p *= 2;
+    return p;
+}
+
+// Byte ranges of the buffers of one call, for the overlap rules.
+struct Range {
+    uintptr_t lo = 0, hi = 0;  // [lo, hi)
+    bool overlaps(const Range& o) const { return lo < o.hi && o.lo < hi; }
+    bool same(const Range& o) const { return lo == o.lo && hi == o.hi; }
+};
+
+Range range_of(const void* p, int64_t bytes)
+{
+    Range r;
+    r.lo = reinterpret_cast<uintptr_t>(p);
+    r.hi = r.lo + static_cast<uintptr_t>(bytes);
+    return r;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape, pointers, eps and overlaps.  out/out_q/scale: whichever the variant
+// writes (the others NULL).  Returns DRADD_OK with *noop set for n_rows == 0.
+dradd_status validate(bool quant, const void* out, const void* out_q, const void* scale,
+                      const void* residual_out, const void* x, const void* residual, const void* weight,
+                      float eps, int64_t n_rows, int64_t hidden, bool* noop)
+{
+    *noop = false;
+    if (n_rows < 0 || hidden <= 0)
+        return DRADD_ERR_BAD_SHAPE;
+    if (hidden % 8 != 0 || hidden > DRADD_MAX_HIDDEN)
+        return DRADD_ERR_UNSUPPORTED_HIDDEN;
+    if (n_rows > (INT64_MAX / 4) / hidden)
+        return DRADD_ERR_BAD_SHAPE;
+    if (n_rows == 0) {
+        *noop = true;
+        return DRADD_OK;
+    }
+    const void* primary_out = quant ? out_q : out;
+    if (!primary_out || !residual_out || !x || !residual || !weight || (quant && !scale))
+        return DRADD_ERR_NULL_PTR;
+    if (!aligned(primary_out, 16) || !aligned(residual_out, 16) || !aligned(x, 16) ||
+        !aligned(residual, 16) || !aligned(weight, 16) || (quant && !aligned(scale, 4)))
+        return DRADD_ERR_MISALIGNED;
+    if (!std::isfinite(eps) || eps < 0.0f)
+        return DRADD_ERR_BAD_EPS;
+
+    const int64_t elems = n_rows * hidden;
+    const Range rx = range_of(x, elems * 2), rr = range_of(residual, elems * 2);
+    const Range rw = range_of(weight, hidden * 2);
+    const Range rro = range_of(residual_out, elems * 2);
+    const Range inputs[3] = {rx, rr, rw};
+    Range outs[3];
+    int n_out = 0;
+    outs[n_out++] = rro;
+    if (quant) {
+        outs[n_out++] = range_of(out_q, elems);
+        outs[n_out++] = range_of(scale, n_rows * 4);
+    } else {
+        outs[n_out++] = range_of(out, elems * 2);
+    }
+    for (int a = 0; a < n_out; ++a)
+        for (int b = a + 1; b < n_out; ++b)
+            if (outs[a].overlaps(outs[b]))
+                return DRADD_ERR_ALIAS;
+    // An output may coincide exactly with x or residual (each element is read
+    // by the thread that later writes it, before it writes it); any other
+    // overlap with an input is rejected.
+    for (int a = 0; a < n_out; ++a) {
+        const bool bf16_out = a == 0 || !quant;
+        for (int b = 0; b < 3; ++b) {
+            if (!outs[a].overlaps(inputs[b]))
+                continue;
+            if (bf16_out && b < 2 && outs[a].same(inputs[b]))
+                continue;
+            return DRADD_ERR_ALIAS;
+        }
+    }
+    return DRADD_OK;
+}
+
+// Fill the automatic fields of *cfg and check the explicit ones.
+dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, const DeviceLimits& L,
+                     dradd_launch_cfg* cfg)
+{
+    (void)quant;
+    if (n_rows < 0 || hidden <= 0)
+        return DRADD_ERR_BAD_SHAPE;
+    if (hidden % 8 != 0 || hidden > DRADD_MAX_HIDDEN)
+        return DRADD_ERR_UNSUPPORTED_HIDDEN;
+    const int64_t P = next_pow2(hidden);
+    const int64_t blocks = P / 8;
+
+    if (cfg->variant == DRADD_VARIANT_AUTO)
+        cfg->variant = hidden > 8192 ? DRADD_VARIANT_STAGED : DRADD_VARIANT_ROWS;
+    if (cfg->variant != DRADD_VARIANT_ROWS && cfg->variant != DRADD_VARIANT_STAGED)
+        return DRADD_ERR_BAD_CONFIG;
+    const bool staged = cfg->variant == DRADD_VARIANT_STAGED;
+
+    if (cfg->threads_per_row == 0) {
+        int64_t T = blocks < 512 ? blocks : 512;
+        while (blocks / T > 8)
+            T *= 2;
+        cfg->threads_per_row = static_cast<int>(T);
+    }
+    const int T = cfg->threads_per_row;
+    if (!is_pow2(T) || T > 1024 || blocks % T != 0)
+        return DRADD_ERR_BAD_CONFIG;
+    const int64_t K = blocks / T;
+    if (K != 1 && K != 2 && K != 4 && K != 8)
+        return DRADD_ERR_BAD_CONFIG;
+    if (staged && T < 32)
+        return DRADD_ERR_BAD_CONFIG;
+
+    if (cfg->rows_per_cta == 0)
+        cfg->rows_per_cta = staged ? 1 : (T < 128 ? static_cast<int>(128 / T) : 1);
+    const int R = cfg->rows_per_cta;
+    if (R < 1 || static_cast<int64_t>(T) * R > dradd::max_threads_for(static_cast<int>(K)) ||
+        (T * R) % 32 != 0 || (staged && R != 1))
+        return DRADD_ERR_BAD_CONFIG;
+
+    const int threads = T * R;
+    int ctas_per_sm = L.max_threads_per_sm / threads;
+    if (ctas_per_sm > L.max_blocks_per_sm)
+        ctas_per_sm = L.max_blocks_per_sm;
+    if (staged) {
+        const int64_t stage_bytes = 4 * hidden;
+        const int64_t static_smem = static_cast<int64_t>(dradd::staged_static_smem(static_cast<int>(K)));
+        const int64_t avail = L.smem_per_block_optin - static_smem - 8 * 8;
+        if (cfg->stages == 0) {
+            int64_t S = avail / stage_bytes;
+            cfg->stages = static_cast<int>(S > 4 ? 4 : S);
+        }
+        const int S = cfg->stages;
+        if (S < 1 || S > 8 || S * stage_bytes > avail)
+            return DRADD_ERR_BAD_CONFIG;
+        const int64_t per_cta = S * stage_bytes + static_smem + 8 * S + 1024;  // 1 KiB reserved per CTA
+        const int64_t by_smem = L.smem_per_sm / per_cta;
+        if (by_smem < ctas_per_sm)
+            ctas_per_sm = static_cast<int>(by_smem);
+        if (ctas_per_sm < 1)
+            return DRADD_ERR_BAD_CONFIG;
+    } else if (cfg->stages != 0 || cfg->fault_inject != 0) {
+        return DRADD_ERR_BAD_CONFIG;
+    }
+    if (cfg->wait_limit_us < 0)
+        return DRADD_ERR_BAD_CONFIG;
+
+    if (cfg->grid_ctas == 0) {
+        const int64_t groups = (n_rows + R - 1) / R;
+        int64_t grid;
+        if (staged)
+            grid = static_cast<int64_t>(L.sm_count) * ctas_per_sm;
+        else
+            grid = groups;
+        if (grid > groups)
+            grid = groups;
+        if (grid > 0x7FFFFFFF)
+            grid = 0x7FFFFFFF;
+        if (grid < 1)
+            grid = 1;
+        cfg->grid_ctas = static_cast<int>(grid);
+    }
+    if (cfg->grid_ctas < 1)
+        return DRADD_ERR_BAD_CONFIG;
+    return DRADD_OK;
+}
+
+dradd_status run(bool quant, dradd_bf16* out, int8_t* out_q, float* scale, dradd_bf16* residual_out,
+                 const dradd_bf16* x, const dradd_bf16* residual, const dradd_bf16* weight, float eps,
+                 int64_t n_rows, int64_t hidden, cudaStream_t stream, const dradd_launch_cfg* user_cfg)
+{
+    bool noop = false;
+    dradd_status st = validate(quant, out, out_q, scale, residual_out, x, residual, weight, eps, n_rows,
+                               hidden, &noop);
+    if (st != DRADD_OK || noop)
+        return st;
+    DeviceLimits L;
+    st = query_limits(&L);
+    if (st != DRADD_OK)
+        return st;
+    dradd_launch_cfg cfg = {};
+    if (user_cfg)
+        cfg = *user_cfg;
+    const bool auto_grid = cfg.grid_ctas == 0;
+    st = resolve(n_rows, hidden, quant, L, &cfg);
+    if (st != DRADD_OK)
+        return st;
+    const int K = static_cast<int>(next_pow2(hidden) / 8 / cfg.threads_per_row);
+    const size_t dyn = cfg.variant == DRADD_VARIANT_STAGED
+                           ? static_cast<size_t>(cfg.stages) * 4 * static_cast<size_t>(hidden) +
+                                 8 * static_cast<size_t>(cfg.stages)
+                           : 0;
+    if (auto_grid && cfg.variant == DRADD_VARIANT_STAGED) {
+        // persistent grid: as many CTAs as fit on the device at once
+        int per_sm = 0;
+        if (dradd::staged_occupancy(K, quant, cfg.threads_per_row, dyn, &per_sm) != cudaSuccess)
+            return DRADD_ERR_CUDA;
+        int64_t grid = static_cast<int64_t>(L.sm_count) * (per_sm > 0 ? per_sm : 1);
+        if (grid > n_rows)
+            grid = n_rows;
+        cfg.grid_ctas = static_cast<int>(grid);
+    }
+
+    Params p = {};
+    p.out = out;
+    p.out_q = out_q;
+    p.scale = scale;
+    p.residual_out = residual_out;
+    p.x = x;
+    p.residual = residual;
+    p.weight = weight;
+    p.eps = eps;
+    p.hidden = static_cast<int>(hidden);
+    p.n_rows = n_rows;
+    p.threads_per_row = cfg.threads_per_row;
+    p.rows_per_cta = cfg.rows_per_cta;
+    p.stages = cfg.stages;
+    p.fault_inject = cfg.fault_inject;
+    p.wait_limit_ns = cfg.wait_limit_us > 0 ? static_cast<uint64_t>(cfg.wait_limit_us) * 1000ull
+                                            : kDefaultWaitLimitNs;
+    cudaError_t e;
+    if (cfg.variant == DRADD_VARIANT_STAGED) {
+        e = dradd::launch_staged(p, K, quant, cfg.grid_ctas, cfg.threads_per_row, dyn, stream);
+    } else {
+        e = dradd::launch_rows(p, K, quant, cfg.grid_ctas, cfg.threads_per_row * cfg.rows_per_cta, stream);
+    }
+    return e == cudaSuccess ? DRADD_OK : DRADD_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+dradd_status add_rmsnorm_fwd(dradd_bf16* out, dradd_bf16* residual_out, const dradd_bf16* x,
+                             const dradd_bf16* residual, const dradd_bf16* weight, float eps,
+                             int64_t n_rows, int64_t hidden, cudaStream_t stream)
+{
+    return run(false, out, nullptr, nullptr, residual_out, x, residual, weight, eps, n_rows, hidden,
+               stream, nullptr);
+}
+
+dradd_status add_rmsnorm_quant_fwd(int8_t* out_q, float* scale, dradd_bf16* residual_out,
+                                   const dradd_bf16* x, const dradd_bf16* residual,
+                                   const dradd_bf16* weight, float eps, int64_t n_rows,
+                                   int64_t hidden, cudaStream_t stream)
+{
+    return run(true, nullptr, out_q, scale, residual_out, x, residual, weight, eps, n_rows, hidden,
+               stream, nullptr);
+}
+
+dradd_status add_rmsnorm_fwd_with_config(dradd_bf16* out, dradd_bf16* residual_out,
+                                         const dradd_bf16* x, const dradd_bf16* residual,
+                                         const dradd_bf16* weight, float eps, int64_t n_rows,
+                                         int64_t hidden, cudaStream_t stream,
+                                         const dradd_launch_cfg* cfg)
+{
+    if (!cfg)
+        return DRADD_ERR_NULL_PTR;
+    return run(false, out, nullptr, nullptr, residual_out, x, residual, weight, eps, n_rows, hidden,
+               stream, cfg);
+}
+
+dradd_status add_rmsnorm_quant_fwd_with_config(int8_t* out_q, float* scale, dradd_bf16* residual_out,
+                                               const dradd_bf16* x, const dradd_bf16* residual,
+                                               const dradd_bf16* weight, float eps, int64_t n_rows,
+                                               int64_t hidden, cudaStream_t stream,
+                                               const dradd_launch_cfg* cfg)
+{
+    if (!cfg)
+        return DRADD_ERR_NULL_PTR;
+    return run(true, nullptr, out_q, scale, residual_out, x, residual, weight, eps, n_rows, hidden,
+               stream, cfg);
+}
+
+dradd_status dradd_resolve_config(int64_t n_rows, int64_t hidden, int quant, int sm_count,
+                                  dradd_launch_cfg* cfg)
+{
+    if (!cfg)
+        return DRADD_ERR_NULL_PTR;
+    DeviceLimits L;
+    if (sm_count > 0) {
+        L.sm_count = sm_count;
+    } else {
+        const dradd_status st = query_limits(&L);
+        if (st != DRADD_OK)
+            return st;
+    }
+    return resolve(n_rows, hidden, quant != 0, L, cfg);
+}
+
+dradd_status dradd_device_status(cudaStream_t stream, int clear)
+{
+    unsigned word = 0;
+    if (dradd::read_device_status(&word, clear != 0, stream) != cudaSuccess)
+        return DRADD_ERR_CUDA;
+    return word ? DRADD_ERR_TIMEOUT : DRADD_OK;
+}
+
+dradd_status dradd_bf16_convert_range(dradd_bf16* out, uint64_t first, int64_t count, int method,
+                                      cudaStream_t stream)
+{
+    if (count < 0)
+        return DRADD_ERR_BAD_SHAPE;
+    if (count == 0)
+        return DRADD_OK;
+    if (!out)
+        return DRADD_ERR_NULL_PTR;
+    if (!aligned(out, 2))
+        return DRADD_ERR_MISALIGNED;
+    if (method < 0 || method > 2)
+        return DRADD_ERR_BAD_CONFIG;
+    return dradd::launch_convert(out, first, count, method, stream) == cudaSuccess ? DRADD_OK
+                                                                                  : DRADD_ERR_CUDA;
+}
+
+const char* dradd_status_string(dradd_status status)
+{
+    switch (status) {
+    case DRADD_OK: return "DRADD_OK";
+    case DRADD_ERR_NULL_PTR: return "DRADD_ERR_NULL_PTR: a required pointer is NULL";
+    case DRADD_ERR_BAD_SHAPE: return "DRADD_ERR_BAD_SHAPE: n_rows < 0 or hidden <= 0 (or too large)";
+    case DRADD_ERR_UNSUPPORTED_HIDDEN:
+        return "DRADD_ERR_UNSUPPORTED_HIDDEN: hidden must be a multiple of 8 and <= 32768";
+    case DRADD_ERR_MISALIGNED: return "DRADD_ERR_MISALIGNED: pointers must be 16-byte aligned";
+    case DRADD_ERR_BAD_EPS: return "DRADD_ERR_BAD_EPS: eps must be finite and >= 0";
+    case DRADD_ERR_ALIAS: return "DRADD_ERR_ALIAS: buffers overlap other than as allowed";
+    case DRADD_ERR_CUDA: return "DRADD_ERR_CUDA: a CUDA runtime call failed";
+    case DRADD_ERR_TIMEOUT: return "DRADD_ERR_TIMEOUT: a kernel's bounded wait expired";
+    case DRADD_ERR_BAD_CONFIG: return "DRADD_ERR_BAD_CONFIG: invalid launch configuration";
+    default: return "DRADD_ERR_UNKNOWN";
+    }
+}
+
+int dradd_abi_version(void) { return DRADD_ABI_VERSION; }
+
+}  // extern "C"

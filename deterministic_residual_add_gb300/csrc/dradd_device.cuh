@@ -1,0 +1,272 @@
+// dradd_device.cuh -- device helpers for the residual-add + RMSNorm kernels:
+// bf16 widening and round-to-nearest-even narrowing, the canonical pairwise
+// reduction pieces, and thin wrappers over the PTX for mbarriers and bulk
+// asynchronous copies (TMA engine).
+//
+// Every floating-point step uses an explicit round-to-nearest intrinsic
+// (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn) so that no multiply-add is
+// ever contracted and each operation is exactly one IEEE fp32 rounding.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#ifndef DRADD_RNE_HW_CVT
+#define DRADD_RNE_HW_CVT 1
+#endif
+
+namespace dradd {
+
+// ------------------------------------------------------------ bf16 <-> fp32
+// A bf16 value is the top half of an fp32 word, so widening is exact.  A
+// 32-bit word holds two bf16 values, the lower-addressed element in the low
+// half.
+__device__ __forceinline__ float bf16_lo(uint32_t pair) { return __uint_as_float(pair << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t pair) { return __uint_as_float(pair & 0xFFFF0000u); }
+
+// Round-half-even by integer arithmetic: adding 0x7FFF plus the lowest kept
+// bit carries into the kept half exactly when the discarded half is above
+// 0x8000, or equal to it with an odd kept half.  NaN keeps its sign and
+// becomes the quiet NaN 0x7FC0.
+__device__ __forceinline__ uint32_t rne_bits_int(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u)
+        return ((u >> 16) & 0x8000u) | 0x7FC0u;
+    return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+// The hardware conversion: cvt.rn.bf16x2.f32 rounds both operands to
+// nearest-even (subnormals kept) and packs them, first operand in the high
+// half.  Equal to rne_bits_int on every non-NaN input (checked exhaustively
+// by the test suite); NaN becomes a NaN.
+__device__ __forceinline__ uint32_t pack_rne_cvt(float lo, float hi)
+{
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t pack_rne_int(float lo, float hi)
+{
+    return rne_bits_int(lo) | (rne_bits_int(hi) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_rne(float lo, float hi)
+{
+#if DRADD_RNE_HW_CVT
+    return pack_rne_cvt(lo, hi);
+#else
+    return pack_rne_int(lo, hi);
+#endif
+}
+
+// 8 consecutive bf16 elements = one 16-byte vector.
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8])
+{
+    f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
+    f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+    f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
+    f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+}
+
+__device__ __forceinline__ uint4 pack8_rne(const float (&f)[8])
+{
+    uint4 u;
+    u.x = pack_rne(f[0], f[1]);
+    u.y = pack_rne(f[2], f[3]);
+    u.z = pack_rne(f[4], f[5]);
+    u.w = pack_rne(f[6], f[7]);
+    return u;
+}
+
+// acc = fp32(x) + fp32(residual), element by element.
+__device__ __forceinline__ void add8(const uint4& xv, const uint4& rv, float (&acc)[8])
+{
+    float xf[8], rf[8];
+    unpack8(xv, xf);
+    unpack8(rv, rf);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        acc[e] = __fadd_rn(xf[e], rf[e]);
+}
+
+// The lowest three levels of the pairwise tree: squares of one aligned
+// 8-element block, summed as ((s0+s1)+(s2+s3)) + ((s4+s5)+(s6+s7)).
+__device__ __forceinline__ float fold8_squares(const float (&a)[8])
+{
+    float s[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        s[e] = __fmul_rn(a[e], a[e]);
+    const float l0 = __fadd_rn(s[0], s[1]), l1 = __fadd_rn(s[2], s[3]);
+    const float l2 = __fadd_rn(s[4], s[5]), l3 = __fadd_rn(s[6], s[7]);
+    return __fadd_rn(__fadd_rn(l0, l1), __fadd_rn(l2, l3));
+}
+
+// Pairwise fold of K partial sums held by one thread (K a power of two,
+// adjacent pairs first).  Used for the top levels of the tree, where the
+// K subtrees of a thread are adjacent aligned blocks of T * 8 elements.
+template <int K>
+__device__ __forceinline__ float fold_k(float (&p)[K])
+{
+#pragma unroll
+    for (int width = 1; width < K; width *= 2) {
+#pragma unroll
+        for (int j = 0; j < K; j += 2 * width)
+            p[j] = __fadd_rn(p[j], p[j + width]);
+    }
+    return p[0];
+}
+
+// One level-by-level butterfly over `width` lanes (a power of two <= 32):
+// after the step with offset d every lane holds the sum of its aligned
+// 2d-lane group, formed as (lower d-group) + (upper d-group).  fp32
+// addition is commutative, so both partners hold the same bits.
+__device__ __forceinline__ float butterfly_sum(float v, int width)
+{
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        if (d < width)
+            v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, d));
+    }
+    return v;
+}
+
+__device__ __forceinline__ float butterfly_max(float v, int width)
+{
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        if (d < width)
+            v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, d));
+    }
+    return v;
+}
+
+// inv = 1 / sqrt(S / hidden + eps), each operation rounded once.
+__device__ __forceinline__ float inv_rms(float sum_sq, int hidden, float eps)
+{
+    const float mean = __fdiv_rn(sum_sq, static_cast<float>(hidden));
+    const float v = __fadd_rn(mean, eps);
+    return __fdiv_rn(1.0f, __fsqrt_rn(v));
+}
+
+// Round to the nearest integer, ties to even, saturate; NaN -> 0
+// (cvt.rni.s32.f32), then clamp to the symmetric int8 range.
+__device__ __forceinline__ int32_t quantize_one(float y, float scale)
+{
+    if (scale == 0.0f)
+        return 0;
+    int32_t q = __float2int_rn(__fdiv_rn(y, scale));
+    q = q > 127 ? 127 : q;
+    q = q < -127 ? -127 : q;
+    return q;
+}
+
+__device__ __forceinline__ uint2 pack8_i8(const int32_t (&q)[8])
+{
+    uint2 u;
+    u.x = (uint32_t(q[0]) & 0xFFu) | ((uint32_t(q[1]) & 0xFFu) << 8) |
+          ((uint32_t(q[2]) & 0xFFu) << 16) | ((uint32_t(q[3]) & 0xFFu) << 24);
+    u.y = (uint32_t(q[4]) & 0xFFu) | ((uint32_t(q[5]) & 0xFFu) << 8) |
+          ((uint32_t(q[6]) & 0xFFu) << 16) | ((uint32_t(q[7]) & 0xFFu) << 24);
+    return u;
+}
+
+// ------------------------------------------------------ mbarrier and bulk copy
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// Makes the initialised barriers visible to the asynchronous proxy.
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's earlier shared-memory accesses before later
+// asynchronous-proxy (bulk copy) accesses to shared memory.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of `bar` with the given parity to complete, giving up
+// after `limit_ns` nanoseconds or 2^26 polls, whichever comes first.
+// Returns false on giving up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1; i < (1u << 26); ++i) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((i & 63u) == 0 && global_timer_ns() - t0 > limit_ns)
+            return false;
+    }
+    return false;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing `bytes`
+// transaction bytes on `bar`.  Both addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst_smem, const void* src_gmem,
+                                              uint32_t bytes, uint64_t* bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// ------------------------------------------------------------ global access
+// Streaming (read-once / write-once) 16-byte accesses.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }
+__device__ __forceinline__ void st_stream(uint2* p, const uint2& v) { __stcs(p, v); }
+
+}  // namespace dradd

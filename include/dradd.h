@@ -1,0 +1,215 @@
+/*
+ * dradd.h -- C ABI of libdradd: deterministic fused residual-add + RMSNorm
+ * forward for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the one named rmsnorm2d_fwd_with_add on the ROCm/aiter
+ * issue #5151 page ("rmsnorm2d_fwd_with_add truncates fp32->bf16 on gfx942,
+ * biasing residual_out and compounding across layers"), section "Steps to
+ * Reproduce", function reference():
+ *
+ *     acc          = fp32(x) + fp32(residual)                  (per element)
+ *     residual_out = bf16(acc)
+ *     out          = bf16((acc * rsqrt(mean(acc^2) + eps)) * fp32(weight))
+ *
+ * with both bf16 stores rounded to nearest, ties to even (the page's fix,
+ * sections "Problem Description" and "Notes"), never truncated.
+ *
+ * Every result is a fixed function of the inputs; it does not depend on the
+ * launch configuration, the variant chosen, the GPU's SM count or the run:
+ *   - acc, acc^2, the mean, the sum of eps, the square root, the reciprocal
+ *     and both products are single IEEE fp32 operations rounded to nearest
+ *     (no fused multiply-add, no flush to zero);
+ *   - mean(acc^2) = S / hidden, where S is the pairwise sum of the squares:
+ *     the row is padded with +0 to P = the next power of two >= hidden, and
+ *     the sum of a block is the rounded sum of its lower and upper halves;
+ *   - rsqrt(v) = 1 / sqrt(v), both correctly rounded;
+ *   - the products run left to right: (acc * inv) * weight.
+ *
+ * Conventions shared by every entry point:
+ *   - bf16 values are passed as their 16-bit patterns (dradd_bf16).
+ *   - x, residual, out, residual_out: row-major, n_rows x hidden, contiguous
+ *     (row stride = hidden elements).  weight: hidden elements, shared by
+ *     all rows.
+ *   - All pointers are DEVICE pointers (cudaMalloc'd or otherwise addressable
+ *     by the current device).  The caller allocates and owns every buffer;
+ *     the library allocates no device memory and keeps no per-call state.
+ *   - Every array pointer must be 16-byte aligned (scale: 4-byte aligned).
+ *   - 1 <= hidden <= DRADD_MAX_HIDDEN and hidden % 8 == 0.  n_rows >= 0;
+ *     n_rows == 0 is a successful no-op (pointers are not inspected).
+ *   - eps must be finite and >= 0; it is used as the given fp32 value.
+ *   - Aliasing: an output may be exactly the same buffer as x or as residual
+ *     (e.g. residual_out == residual for an in-place residual update).  Any
+ *     other overlap between buffers is rejected with DRADD_ERR_ALIAS.
+ *   - The call enqueues work on `stream` (0 = the legacy default stream of
+ *     the current device) and returns without synchronising.  Results are
+ *     valid once the stream has reached that point.  Launch failures are
+ *     returned as DRADD_ERR_CUDA at enqueue time.
+ *   - Argument errors are detected on the host before any GPU work and leave
+ *     every buffer untouched.
+ *   - Calls that run at the same time on different streams share nothing
+ *     except the device status word read by dradd_device_status().
+ */
+#ifndef DRADD_H
+#define DRADD_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DRADD_ABI_VERSION 1
+#define DRADD_MAX_HIDDEN 32768
+
+typedef uint16_t dradd_bf16;  /* raw bf16 bit pattern */
+typedef int dradd_status;
+
+enum {
+    DRADD_OK = 0,
+    DRADD_ERR_NULL_PTR = 1,           /* a required pointer is NULL                  */
+    DRADD_ERR_BAD_SHAPE = 2,          /* n_rows < 0 or hidden <= 0                    */
+    DRADD_ERR_UNSUPPORTED_HIDDEN = 3, /* hidden % 8 != 0 or hidden > DRADD_MAX_HIDDEN */
+    DRADD_ERR_MISALIGNED = 4,         /* a pointer is not 16-byte (scale: 4) aligned  */
+    DRADD_ERR_BAD_EPS = 5,            /* eps is NaN, infinite or negative             */
+    DRADD_ERR_ALIAS = 6,              /* buffers overlap other than as allowed         */
+    DRADD_ERR_CUDA = 7,               /* a CUDA runtime call failed                    */
+    DRADD_ERR_TIMEOUT = 8,            /* a kernel's bounded wait expired (device)      */
+    DRADD_ERR_BAD_CONFIG = 9          /* an explicit launch configuration is invalid   */
+};
+
+/*
+ * add_rmsnorm_fwd -- residual-add + RMSNorm forward with bf16 out.
+ * Page: ROCm/aiter issue #5151, "Steps to Reproduce", reference(); the
+ * argument set mirrors the page's call rmsnorm2d_fwd_with_add(out, x,
+ * residual, residual_out, weight, eps).
+ *
+ *   out           [n_rows x hidden] bf16, written: bf16_rne((acc*inv)*weight)
+ *   residual_out  [n_rows x hidden] bf16, written: bf16_rne(acc)
+ *   x, residual   [n_rows x hidden] bf16, read
+ *   weight        [hidden] bf16, read
+ *   eps           added to mean(acc^2) before the square root
+ *   stream        CUDA stream to enqueue on
+ * Returns DRADD_OK or one of the errors above.
+ */
+dradd_status add_rmsnorm_fwd(dradd_bf16* out, dradd_bf16* residual_out,
+                             const dradd_bf16* x, const dradd_bf16* residual,
+                             const dradd_bf16* weight, float eps,
+                             int64_t n_rows, int64_t hidden, cudaStream_t stream);
+
+/*
+ * add_rmsnorm_quant_fwd -- the same forward with the normalised row emitted
+ * as per-row symmetric int8 instead of bf16.  Page: ROCm/aiter issue #5151,
+ * section "Cost of fixing": the quantised configurations take `out` through
+ * a scaled cast (int8 here) rather than the bf16 store; residual_out is the
+ * same bf16 store as in add_rmsnorm_fwd (bit-identical).
+ *
+ * With y = (acc * inv) * weight in fp32 (the value add_rmsnorm_fwd rounds):
+ *   amax       = max over the row of |y|              (exact)
+ *   scale[r]   = amax / 127                           (fp32, rounded once)
+ *   out_q[r,i] = clamp(rint(y_i / scale[r]), -127, 127), rint ties to even,
+ *                the quotient a correctly rounded fp32 division;
+ *                scale[r] == 0 gives out_q[r,:] = 0.
+ *
+ *   out_q         [n_rows x hidden] int8, written (16-byte aligned)
+ *   scale         [n_rows] fp32, written (4-byte aligned); q * scale ~ y
+ *   residual_out  [n_rows x hidden] bf16, written
+ *   other arguments as in add_rmsnorm_fwd.
+ */
+dradd_status add_rmsnorm_quant_fwd(int8_t* out_q, float* scale, dradd_bf16* residual_out,
+                                   const dradd_bf16* x, const dradd_bf16* residual,
+                                   const dradd_bf16* weight, float eps,
+                                   int64_t n_rows, int64_t hidden, cudaStream_t stream);
+
+/*
+ * Explicit launch configuration.  It selects how the work is laid out on the
+ * GPU and never changes a single output bit (that is what the invariance
+ * tests check).  Zero in a field means "choose automatically".
+ *
+ *   variant          DRADD_VARIANT_ROWS: each group of threads_per_row
+ *                    threads loads its row with 16-byte vector loads into
+ *                    registers; DRADD_VARIANT_STAGED: rows are staged into
+ *                    shared memory by bulk asynchronous copies (TMA engine)
+ *                    several rows ahead of the compute.
+ *   threads_per_row  power of two T with T * K * 8 == P (P = next power of
+ *                    two >= hidden) for some K in {1, 2, 4, 8}: thread t of
+ *                    a row owns the 8-element blocks t, t + T, ..., t + (K-1)T.
+ *   rows_per_cta     rows processed side by side by one CTA (ROWS only);
+ *                    threads_per_row * rows_per_cta <= 1024 and a multiple
+ *                    of 32.
+ *   grid_ctas        number of CTAs; each loops over rows with a stride of
+ *                    grid_ctas * rows_per_cta.
+ *   stages           STAGED only: rows in flight per CTA (1..8), limited by
+ *                    shared memory (2 * hidden * 2 bytes per stage).
+ *   fault_inject     test hook, STAGED only: 1 withholds every CTA's first
+ *                    copy so that its bounded wait expires; the kernel then
+ *                    records DRADD_ERR_TIMEOUT in the device status word,
+ *                    waits for its other copies and returns.  Outputs are
+ *                    then unspecified.
+ *   wait_limit_us    STAGED only: bound on each wait for a staged row, in
+ *                    microseconds (0 = 1,000,000).
+ */
+enum { DRADD_VARIANT_AUTO = 0, DRADD_VARIANT_ROWS = 1, DRADD_VARIANT_STAGED = 2 };
+
+typedef struct dradd_launch_cfg {
+    int variant;
+    int threads_per_row;
+    int rows_per_cta;
+    int grid_ctas;
+    int stages;
+    int fault_inject;
+    int wait_limit_us;
+    int reserved;
+} dradd_launch_cfg;
+
+dradd_status add_rmsnorm_fwd_with_config(dradd_bf16* out, dradd_bf16* residual_out,
+                                         const dradd_bf16* x, const dradd_bf16* residual,
+                                         const dradd_bf16* weight, float eps,
+                                         int64_t n_rows, int64_t hidden, cudaStream_t stream,
+                                         const dradd_launch_cfg* cfg);
+
+dradd_status add_rmsnorm_quant_fwd_with_config(int8_t* out_q, float* scale,
+                                               dradd_bf16* residual_out,
+                                               const dradd_bf16* x, const dradd_bf16* residual,
+                                               const dradd_bf16* weight, float eps,
+                                               int64_t n_rows, int64_t hidden,
+                                               cudaStream_t stream,
+                                               const dradd_launch_cfg* cfg);
+
+/*
+ * dradd_resolve_config -- fill the automatic choices of *cfg for a call of
+ * the given shape, as the entry points would, and validate the explicit
+ * ones.  grid_ctas is filled from `sm_count` (pass 0 to query the current
+ * device).  Does no GPU work when sm_count > 0.
+ */
+dradd_status dradd_resolve_config(int64_t n_rows, int64_t hidden, int quant, int sm_count,
+                                  dradd_launch_cfg* cfg);
+
+/*
+ * dradd_device_status -- synchronise `stream`, then return DRADD_OK or the
+ * error a kernel recorded on the current device since the last clear
+ * (DRADD_ERR_TIMEOUT).  clear != 0 resets the word afterwards.
+ */
+dradd_status dradd_device_status(cudaStream_t stream, int clear);
+
+/*
+ * dradd_bf16_convert_range -- test hook: convert the `count` fp32 bit
+ * patterns first, first+1, ... (mod 2^32) to bf16 on the device, with
+ * method 0 = the conversion the kernels use, 1 = integer round-half-even
+ * bit arithmetic, 2 = the hardware cvt.rn.bf16x2.f32 instruction.
+ * `out` is a device array of `count` dradd_bf16 (2-byte aligned).
+ */
+dradd_status dradd_bf16_convert_range(dradd_bf16* out, uint64_t first, int64_t count,
+                                      int method, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* dradd_status_string(dradd_status status);
+
+/* DRADD_ABI_VERSION of the loaded library. */
+int dradd_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DRADD_H */

@@ -1,0 +1,170 @@
+"""The C ABI on the host, without a GPU: the library loads, exports every
+function include/dradd.h declares, and its host logic (argument checks,
+configuration choice) behaves as documented.  Every call made here returns
+before any CUDA runtime call; nothing is launched."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+import deterministic_residual_add_gb300 as dr
+from deterministic_residual_add_gb300 import build as drbuild
+
+ROOT = Path(__file__).resolve().parents[1]
+HEADERS = sorted((ROOT / "include").glob("*.h"))
+
+
+@pytest.fixture(scope="module")
+def L():
+    drbuild.build()
+    return dr.lib()
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", h.read_text(), flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_headers_declare_the_entry_points():
+    names = declared_functions()
+    for n in ("add_rmsnorm_fwd", "add_rmsnorm_quant_fwd", "add_rmsnorm_fwd_with_config",
+              "add_rmsnorm_quant_fwd_with_config", "dradd_resolve_config", "dradd_device_status",
+              "dradd_bf16_convert_range", "dradd_status_string", "dradd_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"libdradd.so does not export {name}"
+
+
+def test_abi_version_and_status_strings(L):
+    assert dr.abi_version() == 1
+    for code, name in dr.STATUS_NAMES.items():
+        assert name in dr.status_string(code)
+    assert "UNKNOWN" in dr.status_string(1234)
+
+
+# Fake, 256-byte aligned "device" addresses far apart: validation reads only
+# the values of the pointers, never the memory.
+MB = 1 << 20
+BASE = 1 << 40
+X, RES, W, OUT, RO, Q, SC = (BASE + i * 256 * MB for i in range(7))
+
+
+def call_bf16(L, out=OUT, ro=RO, x=X, res=RES, w=W, eps=1e-6, n=4, h=1024):
+    return L.add_rmsnorm_fwd(out, ro, x, res, w, eps, n, h, None)
+
+
+def call_quant(L, q=Q, sc=SC, ro=RO, x=X, res=RES, w=W, eps=1e-6, n=4, h=1024):
+    return L.add_rmsnorm_quant_fwd(q, sc, ro, x, res, w, eps, n, h, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n=-1), 2), (dict(h=0), 2), (dict(h=-8), 2),
+    (dict(h=12), 3), (dict(h=32776), 3), (dict(h=1001), 3),
+    (dict(n=1 << 62), 2),
+    (dict(out=0), 1), (dict(ro=0), 1), (dict(x=0), 1), (dict(res=0), 1), (dict(w=0), 1),
+    (dict(out=OUT + 8), 4), (dict(x=X + 2), 4), (dict(w=W + 4), 4),
+    (dict(eps=float("nan")), 5), (dict(eps=float("inf")), 5), (dict(eps=-1e-6), 5),
+    (dict(ro=OUT), 6),                 # both outputs the same buffer
+    (dict(out=X + 1024), 6),           # partial overlap with x
+    (dict(ro=W), 6),                   # output over the weight
+    (dict(ro=RES + 16), 6),            # shifted alias of residual
+])
+def test_bf16_argument_errors(L, kw, code):
+    assert call_bf16(L, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), 1), (dict(sc=0), 1), (dict(sc=SC + 2), 4), (dict(q=Q + 8), 4),
+    (dict(q=X), 6),                    # int8 out over the bf16 input
+    (dict(sc=RO + 64), 6),             # scale inside residual_out
+    (dict(h=24, n=0), 0),
+])
+def test_quant_argument_errors(L, kw, code):
+    assert call_quant(L, **kw) == code
+
+
+def test_zero_rows_is_a_noop(L):
+    # n_rows == 0 succeeds before the pointers are looked at
+    assert call_bf16(L, n=0, out=0, ro=0, x=0, res=0, w=0) == 0
+    assert call_quant(L, n=0, q=0, sc=0, ro=0, x=0, res=0, w=0) == 0
+
+
+def test_config_pointer_required(L):
+    assert L.add_rmsnorm_fwd_with_config(OUT, RO, X, RES, W, 1e-6, 4, 1024, None, None) == 1
+
+
+def test_convert_hook_argument_errors(L):
+    assert L.dradd_bf16_convert_range(None, 0, 16, 0, None) == 1
+    assert L.dradd_bf16_convert_range(OUT, 0, -1, 0, None) == 2
+    assert L.dradd_bf16_convert_range(OUT + 1, 0, 16, 0, None) == 4
+    assert L.dradd_bf16_convert_range(OUT, 0, 16, 3, None) == 9
+    assert L.dradd_bf16_convert_range(OUT, 0, 0, 0, None) == 0
+
+
+# --------------------------------------------------------- configuration choice
+def test_auto_config_covers_every_supported_hidden(L):
+    for h in range(8, dr.MAX_HIDDEN + 1, 8):
+        c = dr.resolve_config(4096, h, sm_count=152)
+        P = 1 << (h - 1).bit_length()
+        T, R = c.threads_per_row, c.rows_per_cta
+        K = P // 8 // T
+        assert T * K * 8 == P and K in (1, 2, 4, 8)
+        assert (T * R) % 32 == 0 and T * R <= (1024 if K <= 2 else 512)
+        assert c.variant == (dr.VARIANT_STAGED if h > 8192 else dr.VARIANT_ROWS)
+        if c.variant == dr.VARIANT_STAGED:
+            assert 1 <= c.stages <= 8 and c.stages * 4 * h <= 232448
+        assert c.grid_ctas >= 1
+
+
+def test_auto_grid(L):
+    c = dr.resolve_config(4096, 4096, sm_count=152)
+    assert (c.variant, c.threads_per_row, c.rows_per_cta) == (dr.VARIANT_ROWS, 512, 1)
+    assert c.grid_ctas == 4096
+    c = dr.resolve_config(2048, 16384, quant=True, sm_count=152)
+    assert c.variant == dr.VARIANT_STAGED and c.stages == 3
+    assert c.grid_ctas % 152 == 0 or c.grid_ctas == 2048
+    c = dr.resolve_config(3, 64, sm_count=152)
+    assert c.threads_per_row == 8 and c.rows_per_cta == 16 and c.grid_ctas == 1
+
+
+@pytest.mark.parametrize("cfg", [
+    dict(variant=3),
+    dict(threads_per_row=384),              # not a power of two
+    dict(threads_per_row=2048),
+    dict(threads_per_row=64),               # K = 16 for P = 8192
+    dict(threads_per_row=512, rows_per_cta=3),
+    dict(threads_per_row=16, rows_per_cta=1),  # 16 threads is not whole warps
+    dict(variant=2, threads_per_row=16),    # staged needs whole warps per row
+    dict(variant=2, rows_per_cta=2),
+    dict(variant=2, stages=9),
+    dict(variant=1, stages=2),
+    dict(variant=1, fault_inject=1),
+    dict(grid_ctas=-1),
+    dict(wait_limit_us=-5),
+])
+def test_bad_configs_rejected(L, cfg):
+    with pytest.raises(dr.DraddError) as e:
+        dr.resolve_config(4096, 8192, sm_count=152, config=dr.LaunchConfig(**cfg))
+    assert e.value.status == 9
+
+
+def test_staged_stages_limited_by_shared_memory(L):
+    with pytest.raises(dr.DraddError):
+        dr.resolve_config(16, 32768, sm_count=152, config=dr.LaunchConfig(variant=2, stages=2))
+    c = dr.resolve_config(16, 32768, sm_count=152, config=dr.LaunchConfig(variant=2))
+    assert c.stages == 1
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        dr.add_rmsnorm_fwd(x, x.clone(), torch.ones(64, dtype=torch.bfloat16), 1e-6,
+                           out=x.clone(), residual_out=x.clone())
