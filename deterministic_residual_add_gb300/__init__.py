@@ -48,7 +48,7 @@ class DraddError(RuntimeError):
 class _LaunchCfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "variant", "threads_per_row", "rows_per_cta", "grid_ctas", "stages", "fault_inject",
-        "wait_limit_us", "reserved")]
+        "wait_limit_us", "serialize")]
 
 
 @dataclass
@@ -61,15 +61,16 @@ class LaunchConfig:
     stages: int = 0
     fault_inject: int = 0
     wait_limit_us: int = 0
+    serialize: int = 0
 
     def _c(self) -> _LaunchCfg:
         return _LaunchCfg(self.variant, self.threads_per_row, self.rows_per_cta, self.grid_ctas,
-                          self.stages, self.fault_inject, self.wait_limit_us, 0)
+                          self.stages, self.fault_inject, self.wait_limit_us, self.serialize)
 
     @staticmethod
     def _from_c(c: _LaunchCfg) -> "LaunchConfig":
         return LaunchConfig(c.variant, c.threads_per_row, c.rows_per_cta, c.grid_ctas, c.stages,
-                            c.fault_inject, c.wait_limit_us)
+                            c.fault_inject, c.wait_limit_us, c.serialize)
 
 
 _lib = None

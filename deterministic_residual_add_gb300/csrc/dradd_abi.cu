@@ -159,14 +159,35 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, const DeviceLim
     const int64_t P = next_pow2(hidden);
     const int64_t blocks = P / 8;
 
-    if (cfg->variant == DRADD_VARIANT_AUTO)
-        cfg->variant = hidden > 8192 ? DRADD_VARIANT_STAGED : DRADD_VARIANT_ROWS;
+    // Automatic choice, from timings on GB300 (back-to-back launches over
+    // buffers larger than L2): rows of up to 256 elements go several to a
+    // CTA in registers; longer rows are staged through shared memory with
+    // about 96-128 KiB of rows in flight per SM.
+    const bool auto_variant = cfg->variant == DRADD_VARIANT_AUTO;
+    if (auto_variant)
+        cfg->variant = hidden > 256 ? DRADD_VARIANT_STAGED : DRADD_VARIANT_ROWS;
     if (cfg->variant != DRADD_VARIANT_ROWS && cfg->variant != DRADD_VARIANT_STAGED)
         return DRADD_ERR_BAD_CONFIG;
     const bool staged = cfg->variant == DRADD_VARIANT_STAGED;
 
+    int auto_stages = 2;
     if (cfg->threads_per_row == 0) {
-        int64_t T = blocks < 512 ? blocks : 512;
+        int64_t T;
+        if (!staged) {
+            T = blocks < 512 ? blocks : 512;
+        } else if (P <= 4096) {
+            T = blocks;                       // K = 1: 32..512 threads
+            auto_stages = P <= 2048 ? 4 : 2;
+        } else if (P <= 8192) {
+            T = 512;                          // K = 2
+            auto_stages = 4;
+        } else if (P <= 16384) {
+            T = 1024;                         // K = 2
+            auto_stages = 2;
+        } else {
+            T = 512;                          // K = 8
+            auto_stages = 1;
+        }
         while (blocks / T > 8)
             T *= 2;
         cfg->threads_per_row = static_cast<int>(T);
@@ -197,7 +218,7 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, const DeviceLim
         const int64_t avail = L.smem_per_block_optin - static_smem - 8 * 8;
         if (cfg->stages == 0) {
             int64_t S = avail / stage_bytes;
-            cfg->stages = static_cast<int>(S > 4 ? 4 : S);
+            cfg->stages = static_cast<int>(S > auto_stages ? auto_stages : S);
         }
         const int S = cfg->stages;
         if (S < 1 || S > 8 || S * stage_bytes > avail)
@@ -211,7 +232,7 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, const DeviceLim
     } else if (cfg->stages != 0 || cfg->fault_inject != 0) {
         return DRADD_ERR_BAD_CONFIG;
     }
-    if (cfg->wait_limit_us < 0)
+    if (cfg->wait_limit_us < 0 || (cfg->serialize != 0 && cfg->serialize != 1))
         return DRADD_ERR_BAD_CONFIG;
 
     if (cfg->grid_ctas == 0) {
@@ -289,9 +310,11 @@ dradd_status run(bool quant, dradd_bf16* out, int8_t* out_q, float* scale, dradd
                                             : kDefaultWaitLimitNs;
     cudaError_t e;
     if (cfg.variant == DRADD_VARIANT_STAGED) {
-        e = dradd::launch_staged(p, K, quant, cfg.grid_ctas, cfg.threads_per_row, dyn, stream);
+        e = dradd::launch_staged(p, K, quant, cfg.grid_ctas, cfg.threads_per_row, dyn, cfg.serialize != 0,
+                                 stream);
     } else {
-        e = dradd::launch_rows(p, K, quant, cfg.grid_ctas, cfg.threads_per_row * cfg.rows_per_cta, stream);
+        e = dradd::launch_rows(p, K, quant, cfg.grid_ctas, cfg.threads_per_row * cfg.rows_per_cta,
+                               cfg.serialize != 0, stream);
     }
     return e == cudaSuccess ? DRADD_OK : DRADD_ERR_CUDA;
 }

@@ -151,13 +151,44 @@ __device__ __forceinline__ float inv_rms(float sum_sq, int hidden, float eps)
     return __fdiv_rn(1.0f, __fsqrt_rn(v));
 }
 
-// Round to the nearest integer, ties to even, saturate; NaN -> 0
-// (cvt.rni.s32.f32), then clamp to the symmetric int8 range.
-__device__ __forceinline__ int32_t quantize_one(float y, float scale)
+// q = clamp(rint(RN(y / scale)), -127, 127) with rint ties to even, where
+// RN(y / scale) is the correctly rounded fp32 quotient; scale == 0 gives 0.
+//
+// Fast path, for a normal finite scale (every row with amax >= 127 * 2^-126):
+// with c = RN(1 / scale) and q0 = RN(y * c), both rounding errors are
+// relative and at most 2^-24, and |y / scale| <= amax / RN(amax / 127)
+// <= 127 / (1 - 2^-24), so |q0 - y/scale| <= 2^-23 * 127.00001 and
+// |RN(y/scale) - y/scale| <= 2^-24 * 127.00001: q0 and RN(y / scale) are
+// less than 2.3e-5 < 2^-15 apart.  When q0 is at least 2^-15 away from the
+// nearest half-integer, no half-integer lies between the two and both round
+// to the same integer, rint(q0).  Otherwise (about 2^-14 of all values) the
+// quotient is computed exactly with a correctly rounded division.
+struct QuantScale {
+    float scale;
+    float recip;  // RN(1 / scale)
+    bool fast;
+};
+
+__device__ __forceinline__ QuantScale make_quant_scale(float scale)
 {
-    if (scale == 0.0f)
+    QuantScale s;
+    s.scale = scale;
+    s.fast = scale >= 0x1p-126f && scale <= 3.40282347e38f;
+    s.recip = s.fast ? __frcp_rn(scale) : 0.0f;
+    return s;
+}
+
+__device__ __forceinline__ int32_t quantize_one(float y, const QuantScale& s)
+{
+    if (s.scale == 0.0f)
         return 0;
-    int32_t q = __float2int_rn(__fdiv_rn(y, scale));
+    int32_t q;
+    const float q0 = __fmul_rn(y, s.recip);
+    const float t = rintf(q0);
+    if (s.fast && fabsf(__fsub_rn(q0, t)) <= 0.5f - 0x1p-15f)
+        q = static_cast<int32_t>(t);
+    else
+        q = __float2int_rn(__fdiv_rn(y, s.scale));  // NaN -> 0, saturating
     q = q > 127 ? 127 : q;
     q = q < -127 ? -127 : q;
     return q;
@@ -261,6 +292,22 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst_smem, const void* src_gm
         " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst_smem)),
         "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// ---------------------------------------------- programmatic dependent launch
+// Blocks until every grid this one depends on in the stream has completed
+// and its memory is visible; a no-op when the grid was launched without
+// programmatic stream serialization.  Called before any global access.
+__device__ __forceinline__ void wait_prior_grids()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next grid in the stream be scheduled now; its CTAs then start as
+// SMs free up and block in wait_prior_grids() until this grid is done.
+__device__ __forceinline__ void allow_next_grid()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ------------------------------------------------------------ global access

@@ -37,9 +37,10 @@ constexpr int max_threads_for(int K) { return K <= 2 ? 1024 : 512; }
 #endif
 constexpr int min_blocks_for(int K) { return K == 1 ? DRADD_MINB1 : K == 2 ? DRADD_MINB2 : 1; }
 
-cudaError_t launch_rows(const Params& p, int K, bool quant, int grid, int threads, cudaStream_t stream);
+cudaError_t launch_rows(const Params& p, int K, bool quant, int grid, int threads, bool serialize,
+                        cudaStream_t stream);
 cudaError_t launch_staged(const Params& p, int K, bool quant, int grid, int threads, size_t dyn_smem,
-                          cudaStream_t stream);
+                          bool serialize, cudaStream_t stream);
 size_t staged_static_smem(int K);
 cudaError_t staged_occupancy(int K, bool quant, int threads, size_t dyn_smem, int* blocks_per_sm);
 cudaError_t launch_convert(uint16_t* out, uint64_t first, int64_t count, int method, cudaStream_t stream);

@@ -119,6 +119,7 @@ __device__ __forceinline__ void finish_row(const Params& p, float (&acc)[K][8], 
             m = butterfly_max(red_max[lane & ((T >> 5) - 1)], T >> 5);
         }
         const float scale = __fdiv_rn(m, 127.0f);
+        const QuantScale qs = make_quant_scale(scale);
         if (active) {
             if (t == 0)
                 p.scale[row] = scale;
@@ -130,7 +131,7 @@ __device__ __forceinline__ void finish_row(const Params& p, float (&acc)[K][8], 
                     int32_t q[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        q[e] = quantize_one(acc[j][e], scale);
+                        q[e] = quantize_one(acc[j][e], qs);
                     st_stream(qrow + b, pack8_i8(q));
                 }
             }
@@ -191,6 +192,8 @@ __global__ void __launch_bounds__(max_threads_for(K), min_blocks_for(K)) rows_ke
     const int warps_per_row = T > 32 ? T >> 5 : 1;
     const int nblocks = p.hidden >> 3;
 
+    wait_prior_grids();
+    allow_next_grid();
     uint4 w[K];
     load_weights<K>(p, w, t, T, nblocks);
 
@@ -252,6 +255,8 @@ __global__ void __launch_bounds__(max_threads_for(K), min_blocks_for(K)) staged_
         fence_mbar_init();
     }
     __syncthreads();
+    wait_prior_grids();
+    allow_next_grid();
 
     const uint64_t policy = l2_policy_evict_first();
     auto issue = [&](int s, int64_t row) {
@@ -410,21 +415,37 @@ cudaError_t ensure_smem_attr(KernelFn fn, int K, bool quant, int dev)
 
 }  // namespace
 
-cudaError_t launch_rows(const Params& p, int K, bool quant, int grid, int threads, cudaStream_t stream)
+// Launch with programmatic stream serialization unless `serialize`: the
+// kernel may then be scheduled while the previous kernel in the stream is
+// still draining, and waits for it (griddepcontrol.wait) before touching
+// global memory.
+cudaError_t launch(KernelFn fn, const Params& p, int grid, int threads, size_t dyn_smem, bool serialize,
+                   cudaStream_t stream)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = dyn_smem;
+    cfg.stream = stream;
+    cfg.attrs = serialize ? nullptr : attr;
+    cfg.numAttrs = serialize ? 0 : 1;
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+cudaError_t launch_rows(const Params& p, int K, bool quant, int grid, int threads, bool serialize,
+                        cudaStream_t stream)
 {
     KernelFn fn = rows_fn(K, quant);
     if (!fn)
         return cudaErrorInvalidValue;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(static_cast<unsigned>(threads));
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, fn, p);
+    return launch(fn, p, grid, threads, 0, serialize, stream);
 }
 
 cudaError_t launch_staged(const Params& p, int K, bool quant, int grid, int threads, size_t dyn_smem,
-                          cudaStream_t stream)
+                          bool serialize, cudaStream_t stream)
 {
     KernelFn fn = staged_fn(K, quant);
     if (!fn)
@@ -436,12 +457,7 @@ cudaError_t launch_staged(const Params& p, int K, bool quant, int grid, int thre
     e = ensure_smem_attr(fn, K, quant, dev);
     if (e != cudaSuccess)
         return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(static_cast<unsigned>(threads));
-    cfg.dynamicSmemBytes = dyn_smem;
-    cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, fn, p);
+    return launch(fn, p, grid, threads, dyn_smem, serialize, stream);
 }
 
 cudaError_t staged_occupancy(int K, bool quant, int threads, size_t dyn_smem, int* blocks_per_sm)

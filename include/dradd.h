@@ -148,6 +148,11 @@ dradd_status add_rmsnorm_quant_fwd(int8_t* out_q, float* scale, dradd_bf16* resi
  *                    then unspecified.
  *   wait_limit_us    STAGED only: bound on each wait for a staged row, in
  *                    microseconds (0 = 1,000,000).
+ *   serialize        0: launch with programmatic stream serialization, so the
+ *                    kernel's CTAs may be scheduled while the previous kernel
+ *                    in the stream drains; they wait for it to complete (and
+ *                    its writes to be visible) before any global memory
+ *                    access.  1: plain launch.
  */
 enum { DRADD_VARIANT_AUTO = 0, DRADD_VARIANT_ROWS = 1, DRADD_VARIANT_STAGED = 2 };
 
@@ -159,7 +164,7 @@ typedef struct dradd_launch_cfg {
     int stages;
     int fault_inject;
     int wait_limit_us;
-    int reserved;
+    int serialize;
 } dradd_launch_cfg;
 
 dradd_status add_rmsnorm_fwd_with_config(dradd_bf16* out, dradd_bf16* residual_out,

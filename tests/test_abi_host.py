@@ -117,7 +117,7 @@ def test_auto_config_covers_every_supported_hidden(L):
         K = P // 8 // T
         assert T * K * 8 == P and K in (1, 2, 4, 8)
         assert (T * R) % 32 == 0 and T * R <= (1024 if K <= 2 else 512)
-        assert c.variant == (dr.VARIANT_STAGED if h > 8192 else dr.VARIANT_ROWS)
+        assert c.variant == (dr.VARIANT_STAGED if h > 256 else dr.VARIANT_ROWS)
         if c.variant == dr.VARIANT_STAGED:
             assert 1 <= c.stages <= 8 and c.stages * 4 * h <= 232448
         assert c.grid_ctas >= 1
@@ -125,11 +125,13 @@ def test_auto_config_covers_every_supported_hidden(L):
 
 def test_auto_grid(L):
     c = dr.resolve_config(4096, 4096, sm_count=152)
-    assert (c.variant, c.threads_per_row, c.rows_per_cta) == (dr.VARIANT_ROWS, 512, 1)
-    assert c.grid_ctas == 4096
+    assert (c.variant, c.threads_per_row, c.rows_per_cta, c.stages) == (dr.VARIANT_STAGED, 512, 1, 2)
+    assert c.grid_ctas % 152 == 0
     c = dr.resolve_config(2048, 16384, quant=True, sm_count=152)
-    assert c.variant == dr.VARIANT_STAGED and c.stages == 3
+    assert (c.variant, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 1024, 2)
     assert c.grid_ctas % 152 == 0 or c.grid_ctas == 2048
+    c = dr.resolve_config(4096, 8192, sm_count=152)
+    assert (c.variant, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 512, 4)
     c = dr.resolve_config(3, 64, sm_count=152)
     assert c.threads_per_row == 8 and c.rows_per_cta == 16 and c.grid_ctas == 1
 
@@ -160,6 +162,8 @@ def test_staged_stages_limited_by_shared_memory(L):
         dr.resolve_config(16, 32768, sm_count=152, config=dr.LaunchConfig(variant=2, stages=2))
     c = dr.resolve_config(16, 32768, sm_count=152, config=dr.LaunchConfig(variant=2))
     assert c.stages == 1
+    c = dr.resolve_config(16, 32768, sm_count=152)
+    assert c.stages == 1 and c.threads_per_row == 512
 
 
 def test_binding_refuses_cpu_tensors():
