@@ -1,12 +1,13 @@
-"""Throughput of the fused residual-add + RMSNorm forward (bf16) at
-n_rows = 4096, hidden = 4096 on GB300, through the C ABI of libdradd.
+"""Throughput of the fused residual-add + RMSNorm forward on GB300, through
+the C ABI of libdradd.
 
-One step = one add_rmsnorm_fwd call over one 4096 x 4096 batch (x and
-residual read, residual_out and out written: 8 bytes per element plus the
-weight once).  Inputs follow the chained-depth workload's distributions
-(x ~ N(0, 0.05), residual ~ N(0, 1), weight ~ N(1, 0.1)).  Timed steps run
-back to back over 4 rotating buffer sets (512 MiB, four times the L2), so
-every step streams from HBM.
+Default workload: add_rmsnorm_fwd at n_rows = 4096, hidden = 4096, bf16 in
+and out.  One step = one call over one 4096 x 4096 batch (x and residual
+read, residual_out and out written: 8 bytes per element, plus the weight
+once).  Inputs follow the chained-depth workload's distributions (x ~
+N(0, 0.05), residual ~ N(0, 1), weight ~ N(1, 0.1)).  Timed steps run back
+to back over 4 rotating buffer sets (512 MiB, four times the L2), so every
+step streams from HBM.  Other workloads (--workload) exist for profiling.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -18,6 +19,8 @@ data path), and rank 0 reports the whole-job rate over the slowest rank.
 from __future__ import annotations
 
 import argparse
+import ctypes
+import hashlib
 import json
 import os
 import re
@@ -36,26 +39,36 @@ import deterministic_residual_add_gb300 as dr  # noqa: E402
 from deterministic_residual_add_gb300 import inputs  # noqa: E402
 
 METRIC = "add+RMSNorm GB/s and % of HBM peak at 4096×4096 bf16; bit-exact vs oracle"
-N_ROWS, HIDDEN = 4096, 4096
 N_SETS = 4
 KERNEL_SOURCES = ["csrc/dradd_kernels.cu", "csrc/dradd_device.cuh"]
 TRAFFIC_FILE = ROOT / "profiles" / "add_rmsnorm_fwd_4096x4096_ncu.md"
 
+# name -> (n_rows, hidden, int8 out, input recipe).  The first is the
+# headline workload; the others are for profiling and context.
+WORKLOADS = {
+    "4096x4096": (4096, 4096, False, "chain4096"),
+    "2048x4096": (2048, 4096, False, "2048x4096"),
+    "4096x8192": (4096, 8192, False, "4096x8192"),
+    "2048x16384": (2048, 16384, False, "quant2048x16384"),
+    "quant2048x16384": (2048, 16384, True, "quant2048x16384"),
+    "quant4096x4096": (4096, 4096, True, "chain4096"),
+}
 
-def algorithmic_bytes(n_rows: int, hidden: int) -> int:
-    """x, residual read + residual_out, out written (2 bytes each) + weight."""
+
+def algorithmic_bytes(n_rows: int, hidden: int, quant: bool = False) -> int:
+    """x, residual read + residual_out written (2 bytes each), out written
+    (2 bytes bf16, or 1 byte int8 plus a 4-byte scale per row), weight once."""
+    if quant:
+        return 7 * n_rows * hidden + 4 * n_rows + 2 * hidden
     return 8 * n_rows * hidden + 2 * hidden
 
 
 def measured_peaks() -> dict:
     p = ROOT / "MEASURED_PEAKS.json"
-    if p.exists():
-        return json.loads(p.read_text())
-    return {}
+    return json.loads(p.read_text()) if p.exists() else {}
 
 
 def kernel_source_hash() -> str:
-    import hashlib
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
         h.update((ROOT / "deterministic_residual_add_gb300" / rel).read_bytes())
@@ -63,8 +76,8 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic():
-    """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source."""
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
     if not TRAFFIC_FILE.exists():
         return None
     text = TRAFFIC_FILE.read_text()
@@ -77,6 +90,7 @@ def recorded_traffic():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples every 200 ms."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -138,12 +152,10 @@ def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
     if world > 1:
         import torch.distributed as tdist
-        torch.cuda.set_device(local)
         tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(local)
     return world, rank, local
 
 
@@ -162,34 +174,59 @@ def max_over_ranks(v: float, world: int) -> float:
     return float(t.item())
 
 
-# -------------------------------------------------------------- our kernel
-class RawCall:
-    """Precomputed C-ABI call: add_rmsnorm_fwd(out, ro, x, r, w, eps, n, h, stream)."""
+# ---------------------------------------------------------------- workload
+def workload_inputs(name: str):
+    """(one x per buffer set, residual, weight) as CPU bf16 tensors."""
+    n, h, quant, recipe = WORKLOADS[name]
+    if recipe == "chain4096":
+        ch = inputs.CHAIN4096
+        r0, w = ch.initial()
+        return [ch.delta(k) for k in range(N_SETS)], r0, w
+    c = inputs.WORKLOADS[recipe].make(n_rows=n)
+    xs = [c["x"]] + [inputs.normal_bf16(inputs.generator(1000 + k), (n, h), 0.0, 1.0)
+                     for k in range(1, N_SETS)]
+    return xs, c["residual"], c["weight"]
 
-    def __init__(self, sets, w, stream):
-        import ctypes
-        self.fn = dr.lib().add_rmsnorm_fwd
-        self.args = [(s["out"].data_ptr(), s["ro"].data_ptr(), s["x"].data_ptr(), s["r"].data_ptr(),
-                      w.data_ptr(), ctypes.c_float(inputs.EPS), N_ROWS, HIDDEN, stream.cuda_stream)
-                     for s in sets]
+
+def make_sets(device, name: str):
+    """N_SETS independent buffer sets; set 0 holds the workload's own first
+    draw (used by the parity spot check)."""
+    n, h, quant, _ = WORKLOADS[name]
+    xs, r0, w = workload_inputs(name)
+    sets = []
+    for x_cpu in xs:
+        x = x_cpu.to(device)
+        s = {"x": x, "r": r0.to(device), "out": torch.empty_like(x), "ro": torch.empty_like(x)}
+        if quant:
+            s["q"] = torch.empty(n, h, dtype=torch.int8, device=device)
+            s["scale"] = torch.empty(n, dtype=torch.float32, device=device)
+        sets.append(s)
+    return sets, w.to(device), (xs[0], r0, w)
+
+
+class RawCall:
+    """Precomputed C-ABI calls, one per buffer set:
+    add_rmsnorm_fwd(out, residual_out, x, residual, weight, eps, n, h, stream)
+    or add_rmsnorm_quant_fwd(out_q, scale, residual_out, x, ...)."""
+
+    def __init__(self, sets, w, stream, n_rows, hidden, quant):
+        L = dr.lib()
+        self.fn = L.add_rmsnorm_quant_fwd if quant else L.add_rmsnorm_fwd
+        self.name = "add_rmsnorm_quant_fwd" if quant else "add_rmsnorm_fwd"
+        eps = ctypes.c_float(inputs.EPS)
+        if quant:
+            self.args = [(s["q"].data_ptr(), s["scale"].data_ptr(), s["ro"].data_ptr(),
+                          s["x"].data_ptr(), s["r"].data_ptr(), w.data_ptr(), eps, n_rows, hidden,
+                          stream.cuda_stream) for s in sets]
+        else:
+            self.args = [(s["out"].data_ptr(), s["ro"].data_ptr(), s["x"].data_ptr(),
+                          s["r"].data_ptr(), w.data_ptr(), eps, n_rows, hidden, stream.cuda_stream)
+                         for s in sets]
 
     def __call__(self, i: int):
         st = self.fn(*self.args[i % len(self.args)])
         if st != 0:
-            raise dr.DraddError(st, "add_rmsnorm_fwd")
-
-
-def make_sets(device):
-    """N_SETS independent (x, residual, out, residual_out) buffers: x_k from
-    the chained workload's generator k, residual_0 in every set."""
-    ch = inputs.CHAIN4096
-    r0, w = ch.initial()
-    sets = []
-    for k in range(N_SETS):
-        x = ch.delta(k).to(device)
-        sets.append({"x": x, "r": r0.to(device), "out": torch.empty_like(x),
-                     "ro": torch.empty_like(x)})
-    return sets, w.to(device), r0
+            raise dr.DraddError(st, self.name)
 
 
 GRAPH_CHUNK = 256  # launches per captured graph (a multiple of N_SETS)
@@ -232,27 +269,36 @@ def time_device(call, steps, warmup, stream, world, use_graph):
     return start.elapsed_time(end)  # ms
 
 
-def time_e2e(steps, device, stream, w_dev):
+def time_e2e(steps, device, stream, name):
     """Public API with host data: per step, copy x and residual (and weight)
-    from pinned host memory, run the op, read out and residual_out back."""
-    ch = inputs.CHAIN4096
-    r0, w = ch.initial()
-    x_h = ch.delta(0).pin_memory()
-    r_h = r0.pin_memory()
-    w_h = w.pin_memory()
-    out_h = torch.empty_like(x_h).pin_memory()
+    from pinned host memory, run the op, read its outputs back."""
+    n, h, quant, _ = WORKLOADS[name]
+    xs, r0, w = workload_inputs(name)
+    x_h, r_h, w_h = xs[0].pin_memory(), r0.pin_memory(), w.pin_memory()
+    x_d, r_d = torch.empty_like(x_h, device=device), torch.empty_like(r_h, device=device)
+    wd = torch.empty_like(w_h, device=device)
+    ro_d = torch.empty_like(x_d)
     ro_h = torch.empty_like(x_h).pin_memory()
-    x_d, r_d, wd = torch.empty_like(x_h, device=device), torch.empty_like(r_h, device=device), \
-        torch.empty_like(w_h, device=device)
-    out_d, ro_d = torch.empty_like(x_d), torch.empty_like(x_d)
+    if quant:
+        q_d = torch.empty(n, h, dtype=torch.int8, device=device)
+        s_d = torch.empty(n, dtype=torch.float32, device=device)
+        outs = [(q_d, torch.empty(n, h, dtype=torch.int8).pin_memory()),
+                (s_d, torch.empty(n, dtype=torch.float32).pin_memory()), (ro_d, ro_h)]
+    else:
+        out_d = torch.empty_like(x_d)
+        outs = [(out_d, torch.empty_like(x_h).pin_memory()), (ro_d, ro_h)]
 
     def step():
         x_d.copy_(x_h, non_blocking=True)
         r_d.copy_(r_h, non_blocking=True)
         wd.copy_(w_h, non_blocking=True)
-        dr.add_rmsnorm_fwd(x_d, r_d, wd, inputs.EPS, out=out_d, residual_out=ro_d, stream=stream)
-        out_h.copy_(out_d, non_blocking=True)
-        ro_h.copy_(ro_d, non_blocking=True)
+        if quant:
+            dr.add_rmsnorm_quant_fwd(x_d, r_d, wd, inputs.EPS, out_q=q_d, scale=s_d,
+                                     residual_out=ro_d, stream=stream)
+        else:
+            dr.add_rmsnorm_fwd(x_d, r_d, wd, inputs.EPS, out=out_d, residual_out=ro_d, stream=stream)
+        for dev_t, host_t in outs:
+            host_t.copy_(dev_t, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(2):
@@ -264,97 +310,106 @@ def time_e2e(steps, device, stream, w_dev):
         stream.synchronize()
         dt = time.perf_counter() - t0
     bi = (x_h.numel() + r_h.numel() + w_h.numel()) * 2
-    bo = (out_h.numel() + ro_h.numel()) * 2
+    bo = sum(h_t.numel() * h_t.element_size() for _, h_t in outs)
     return dt, bi, bo
 
 
-def cpu_baseline(seconds: float, gpu_sets=None):
+def cpu_baseline(seconds: float, name: str, first_inputs, gpu_set0=None):
     """The CPU oracle (single thread) on leading rows of the same workload,
     for about `seconds`; also checks those rows against the GPU's output."""
     import numpy as np
     import oracle
     o = oracle.lib()
-    ch = inputs.CHAIN4096
-    r0, w = ch.initial()
-    x0 = ch.delta(0)
+    n, h, quant, _ = WORKLOADS[name]
+    x0, r0, w = first_inputs
+    fn = o.add_rmsnorm_quant_fwd if quant else o.add_rmsnorm_fwd
     chunk = 64
     rows = 0
-    t0 = time.perf_counter()
     first = None
+    t0 = time.perf_counter()
     while True:
-        lo = rows % N_ROWS
-        hi = min(N_ROWS, lo + chunk)
-        res = o.add_rmsnorm_fwd(x0[lo:hi], r0[lo:hi], w, inputs.EPS)
+        lo = rows % n
+        hi = min(n, lo + chunk)
+        res = fn(x0[lo:hi], r0[lo:hi], w, inputs.EPS)
         if first is None:
             first = res
         rows += hi - lo
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    out = {"value": algorithmic_bytes(rows, HIDDEN) / dt / 1e9, "unit": "GB/s", "cores": 1,
+    out = {"value": algorithmic_bytes(rows, h, quant) / dt / 1e9, "unit": "GB/s", "cores": 1,
            "kind": "oracle",
-           "sample": f"{rows} rows of the 4096x4096 workload ({rows * HIDDEN} elements) in "
+           "sample": f"{rows} rows of the {n}x{h} workload ({rows * h} elements) in "
                      f"{dt:.1f} s, single thread",
            "seconds": round(dt, 3)}
-    if gpu_sets is not None:
-        s = gpu_sets[0]
-        got_out = s["out"][:chunk].view(torch.int16).cpu().numpy().view(np.uint16)
-        got_ro = s["ro"][:chunk].view(torch.int16).cpu().numpy().view(np.uint16)
+    if gpu_set0 is not None:
+        def host(t):
+            t = t[:chunk].cpu()
+            if t.dtype == torch.bfloat16:
+                t = t.view(torch.int16)
+            return t.numpy()
+        keys = ["q", "scale", "ro"] if quant else ["out", "ro"]
+        got = [host(gpu_set0[k]) for k in keys]
         out["parity_rows_checked"] = chunk
-        out["parity_bit_exact"] = bool(np.array_equal(got_out, first[0]) and np.array_equal(got_ro, first[1]))
+        out["parity_bit_exact"] = bool(all(
+            np.array_equal(np.ascontiguousarray(g).view(np.uint8), np.ascontiguousarray(e).view(np.uint8))
+            for g, e in zip(got, first)))
     return out
 
 
 def run_ours(args):
     world, rank, local = dist_setup()
     device = torch.device("cuda", local)
+    n_rows, hidden, quant, _ = WORKLOADS[args.workload]
     dr.lib()
     stream = torch.cuda.Stream(device)
-    sets, w_dev, _ = make_sets(device)
+    sets, w_dev, first_inputs = make_sets(device, args.workload)
     torch.cuda.synchronize()
-    call = RawCall(sets, w_dev, stream)
+    call = RawCall(sets, w_dev, stream, n_rows, hidden, quant)
     with torch.cuda.stream(stream):
         sampler = ClockSampler(local)
         with sampler:
             ms = time_device(call, args.steps, args.warmup, stream, world, args.graph)
     ms = max_over_ranks(ms, world)
-    bytes_step = algorithmic_bytes(N_ROWS, HIDDEN)
+    bytes_step = algorithmic_bytes(n_rows, hidden, quant)
     ms_per_step = ms / args.steps
     value = world * bytes_step * args.steps / (ms / 1e3) / 1e9
     per_launch_gbs = bytes_step / (ms_per_step / 1e3) / 1e9
-    peaks = measured_peaks()
-    peak = peaks.get("hbm_gbs")
+    peak = measured_peaks().get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
     if not peak:
         peak = 6800.0
 
-    e2e_steps = max(3, min(args.steps, args.e2e_steps))
     e2e = None
     if not args.no_e2e:
-        dt, bi, bo = time_e2e(e2e_steps, device, stream, w_dev)
+        e2e_steps = max(3, min(args.steps, args.e2e_steps))
+        dt, bi, bo = time_e2e(e2e_steps, device, stream, args.workload)
         dt = max_over_ranks(dt, world)
-        e2e = {"value": world * bytes_step * e2e_steps / dt / 1e9, "unit": "GB/s",
+        e2e = {"value": round(world * bytes_step * e2e_steps / dt / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
-               "ms_per_step": dt / e2e_steps * 1e3}
+               "ms_per_step": round(dt / e2e_steps * 1e3, 4)}
 
-    cfg = dr.resolve_config(N_ROWS, HIDDEN, sm_count=torch.cuda.get_device_properties(device).multi_processor_count)
+    cfg = dr.resolve_config(n_rows, hidden, quant=quant,
+                            sm_count=torch.cuda.get_device_properties(device).multi_processor_count)
+    op = "add_rmsnorm_quant_fwd" if quant else "add_rmsnorm_fwd"
+    io = "bf16 in, int8 + fp32 scale + bf16 residual_out out" if quant else "bf16 in/out"
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": "add_rmsnorm_fwd 4096x4096 bf16 in/out (chained-depth inputs)",
-                   "n_rows": N_ROWS, "hidden": HIDDEN, "io_dtype": "bf16",
-                   "l2": f"{N_SETS} rotating buffer sets ({N_SETS * 128} MiB) > L2",
+        "config": {"workload": f"{op} {n_rows}x{hidden} {io}", "n_rows": n_rows, "hidden": hidden,
+                   "io_dtype": "bf16",
+                   "l2": f"{N_SETS} rotating buffer sets ({N_SETS * bytes_step // 2**20} MiB) > L2",
                    "launch": {"variant": "rows" if cfg.variant == 1 else "staged",
                               "threads_per_row": cfg.threads_per_row, "rows_per_cta": cfg.rows_per_cta,
-                              "grid_ctas": cfg.grid_ctas},
+                              "stages": cfg.stages},
                    "cuda_graph": bool(args.graph), "parallelism": f"replicas x{world}"},
-        "rows_per_s": round(world * N_ROWS * args.steps / (ms / 1e3), 1),
+        "rows_per_s": round(world * n_rows * args.steps / (ms / 1e3), 1),
         "roofline": {"bound": "hbm", "achieved": round(per_launch_gbs, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(per_launch_gbs / peak, 4),
                      "peak_source": f"{peak_src} hbm_gbs",
-                     "traffic": recorded_traffic(),
+                     "traffic": recorded_traffic() if args.workload == "4096x4096" else None,
                      "algorithmic_bytes_per_launch": bytes_step},
         "gpu_launches": args.steps,
         "e2e": e2e,
@@ -362,7 +417,7 @@ def run_ours(args):
     if rank == 0:
         line["clocks"] = sampler.summary()
         if not args.no_cpu:
-            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds, sets)
+            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds, args.workload, first_inputs, sets[0])
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as tdist
@@ -370,39 +425,39 @@ def run_ours(args):
 
 
 def run_reference(args):
-    """The oracle on the host, on the same metric, unit and workload: each
-    step runs a bounded sample of rows of the 4096 x 4096 batch."""
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    """The oracle on the host cores, on the same metric, unit and workload:
+    each step runs a bounded sample of rows of the batch."""
+    if int(os.environ.get("RANK", "0")) != 0:
         return
     import oracle
     o = oracle.lib()
-    ch = inputs.CHAIN4096
-    r0, w = ch.initial()
-    x0 = ch.delta(0)
+    n, h, quant, _ = WORKLOADS[args.workload]
+    xs, r0, w = workload_inputs(args.workload)
+    x0 = xs[0]
+    fn = o.add_rmsnorm_quant_fwd if quant else o.add_rmsnorm_fwd
     t0 = time.perf_counter()
-    o.add_rmsnorm_fwd(x0[:16], r0[:16], w, inputs.EPS)
+    fn(x0[:16], r0[:16], w, inputs.EPS)
     t_row = max(1e-6, (time.perf_counter() - t0) / 16)
     total = args.warmup + args.steps
-    rows = int(max(1, min(N_ROWS, args.reference_seconds / total / t_row)))
-    for i in range(args.warmup):
-        o.add_rmsnorm_fwd(x0[:rows], r0[:rows], w, inputs.EPS)
+    rows = int(max(1, min(n, args.reference_seconds / total / t_row)))
+    for _ in range(args.warmup):
+        fn(x0[:rows], r0[:rows], w, inputs.EPS)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        lo = (i * rows) % (N_ROWS - rows + 1)
-        o.add_rmsnorm_fwd(x0[lo:lo + rows], r0[lo:lo + rows], w, inputs.EPS)
+        lo = (i * rows) % (n - rows + 1)
+        fn(x0[lo:lo + rows], r0[lo:lo + rows], w, inputs.EPS)
     dt = time.perf_counter() - t0
-    value = algorithmic_bytes(rows, HIDDEN) * args.steps / dt / 1e9
+    value = algorithmic_bytes(rows, h, quant) * args.steps / dt / 1e9
+    op = "add_rmsnorm_quant_fwd" if quant else "add_rmsnorm_fwd"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": "add_rmsnorm_fwd 4096x4096 bf16 in/out (chained-depth inputs)",
-                   "n_rows": N_ROWS, "hidden": HIDDEN, "io_dtype": "bf16",
-                   "rows_per_step": rows},
+        "config": {"workload": f"{op} {n}x{h} (CPU oracle)", "n_rows": n, "hidden": h,
+                   "io_dtype": "bf16", "rows_per_step": rows},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{rows} rows of 4096 per step, single thread"},
+                         "sample": f"{rows} of {n} rows per step, single thread"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -416,7 +471,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--graph", type=int, default=1, help="replay the timed steps as a CUDA graph")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="4096x4096")
+    ap.add_argument("--graph", type=int, default=1, help="replay the timed steps from CUDA graphs")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

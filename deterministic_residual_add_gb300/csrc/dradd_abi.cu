@@ -151,7 +151,6 @@ dradd_status validate(bool quant, const void* out, const void* out_q, const void
 dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, const DeviceLimits& L,
                      dradd_launch_cfg* cfg)
 {
-    (void)quant;
     if (n_rows < 0 || hidden <= 0)
         return DRADD_ERR_BAD_SHAPE;
     if (hidden % 8 != 0 || hidden > DRADD_MAX_HIDDEN)
@@ -159,10 +158,18 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, const DeviceLim
     const int64_t P = next_pow2(hidden);
     const int64_t blocks = P / 8;
 
-    // Automatic choice, from timings on GB300 (back-to-back launches over
-    // buffers larger than L2): rows of up to 256 elements go several to a
-    // CTA in registers; longer rows are staged through shared memory with
-    // about 96-128 KiB of rows in flight per SM.
+    // Automatic choice, measured on GB300 (back-to-back launches over buffers
+    // larger than L2, median of interleaved rounds).  Rows of up to 256
+    // elements go several to a CTA in registers; longer rows are staged
+    // through shared memory, mostly with K = 4 blocks of 8 per thread:
+    //   P      T     K  stages
+    //   512    32    2  4
+    //   1024   64    2  1
+    //   2048   64    4  3
+    //   4096   128   4  1 (bf16, >= 24 rows per SM), else 2
+    //   8192   1024  1  2
+    //   16384  512   4  2
+    //   32768  512   8  1
     const bool auto_variant = cfg->variant == DRADD_VARIANT_AUTO;
     if (auto_variant)
         cfg->variant = hidden > 256 ? DRADD_VARIANT_STAGED : DRADD_VARIANT_ROWS;
@@ -175,19 +182,27 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, const DeviceLim
         int64_t T;
         if (!staged) {
             T = blocks < 512 ? blocks : 512;
-        } else if (P <= 4096) {
-            T = blocks;                       // K = 1: 32..512 threads
-            auto_stages = P <= 2048 ? 4 : 2;
-        } else if (P <= 8192) {
-            T = 512;                          // K = 2
+        } else if (P <= 512) {
+            T = blocks / 2 < 32 ? 32 : blocks / 2;
             auto_stages = 4;
-        } else if (P <= 16384) {
-            T = 1024;                         // K = 2
+        } else if (P == 1024) {
+            T = 64;
+            auto_stages = 1;
+        } else if (P == 2048) {
+            T = 64;
+            auto_stages = 3;
+        } else if (P == 4096) {
+            T = 128;
+            auto_stages = (!quant && n_rows >= 24 * static_cast<int64_t>(L.sm_count)) ? 1 : 2;
+        } else if (P == 8192) {
+            T = 1024;
             auto_stages = 2;
         } else {
-            T = 512;                          // K = 8
-            auto_stages = 1;
+            T = 512;
+            auto_stages = P == 16384 ? 2 : 1;
         }
+        if (T > blocks)
+            T = blocks;
         while (blocks / T > 8)
             T *= 2;
         cfg->threads_per_row = static_cast<int>(T);
@@ -301,6 +316,7 @@ dradd_status run(bool quant, dradd_bf16* out, int8_t* out_q, float* scale, dradd
     p.weight = weight;
     p.eps = eps;
     p.hidden = static_cast<int>(hidden);
+    p.inv_hidden = is_pow2(hidden) ? 1.0f / static_cast<float>(hidden) : 0.0f;
     p.n_rows = n_rows;
     p.threads_per_row = cfg.threads_per_row;
     p.rows_per_cta = cfg.rows_per_cta;

@@ -144,11 +144,16 @@ __device__ __forceinline__ float butterfly_max(float v, int width)
 }
 
 // inv = 1 / sqrt(S / hidden + eps), each operation rounded once.
-__device__ __forceinline__ float inv_rms(float sum_sq, int hidden, float eps)
+// inv_hidden is 1 / hidden when hidden is a power of two (else 0): S / hidden
+// and S * 2^-k are then the same real number, so rounding the product gives
+// the correctly rounded quotient bit for bit.  1 / sqrt(v) is the correctly
+// rounded reciprocal of the correctly rounded square root.
+__device__ __forceinline__ float inv_rms(float sum_sq, int hidden, float inv_hidden, float eps)
 {
-    const float mean = __fdiv_rn(sum_sq, static_cast<float>(hidden));
+    const float mean = inv_hidden != 0.0f ? __fmul_rn(sum_sq, inv_hidden)
+                                          : __fdiv_rn(sum_sq, static_cast<float>(hidden));
     const float v = __fadd_rn(mean, eps);
-    return __fdiv_rn(1.0f, __fsqrt_rn(v));
+    return __frcp_rn(__fsqrt_rn(v));
 }
 
 // q = clamp(rint(RN(y / scale)), -127, 127) with rint ties to even, where
@@ -161,8 +166,9 @@ __device__ __forceinline__ float inv_rms(float sum_sq, int hidden, float eps)
 // |RN(y/scale) - y/scale| <= 2^-24 * 127.00001: q0 and RN(y / scale) are
 // less than 2.3e-5 < 2^-15 apart.  When q0 is at least 2^-15 away from the
 // nearest half-integer, no half-integer lies between the two and both round
-// to the same integer, rint(q0).  Otherwise (about 2^-14 of all values) the
-// quotient is computed exactly with a correctly rounded division.
+// to the same integer, rint(q0).  Otherwise (for about 2^-14 of all values,
+// so for about one 8-value block in 1,000) the block's quotients are computed
+// exactly with a correctly rounded division.
 struct QuantScale {
     float scale;
     float recip;  // RN(1 / scale)
@@ -178,29 +184,55 @@ __device__ __forceinline__ QuantScale make_quant_scale(float scale)
     return s;
 }
 
-__device__ __forceinline__ int32_t quantize_one(float y, const QuantScale& s)
+// The reference path for one element: correctly rounded quotient, then
+// rint ties to even (cvt.rni; NaN -> 0, saturating), then the clamp.
+__device__ __forceinline__ int32_t quantize_exact(float y, float scale)
 {
-    if (s.scale == 0.0f)
+    if (scale == 0.0f)
         return 0;
-    int32_t q;
-    const float q0 = __fmul_rn(y, s.recip);
-    const float t = rintf(q0);
-    if (s.fast && fabsf(__fsub_rn(q0, t)) <= 0.5f - 0x1p-15f)
-        q = static_cast<int32_t>(t);
-    else
-        q = __float2int_rn(__fdiv_rn(y, s.scale));  // NaN -> 0, saturating
+    int32_t q = __float2int_rn(__fdiv_rn(y, scale));
     q = q > 127 ? 127 : q;
     q = q < -127 ? -127 : q;
     return q;
 }
 
-__device__ __forceinline__ uint2 pack8_i8(const int32_t (&q)[8])
+// Low bytes of four ints packed into one word, first in the lowest byte.
+__device__ __forceinline__ uint32_t pack4_low_bytes(int32_t a, int32_t b, int32_t c, int32_t d)
 {
+    const uint32_t ab = __byte_perm(static_cast<uint32_t>(a), static_cast<uint32_t>(b), 0x0040);
+    const uint32_t cd = __byte_perm(static_cast<uint32_t>(c), static_cast<uint32_t>(d), 0x0040);
+    return __byte_perm(ab, cd, 0x5410);
+}
+
+// Eight int8 codes for eight consecutive y values.  Fast path: q0 = y * c;
+// adding 1.5 * 2^23 rounds |q0| < 2^22 to an integer, ties to even, held in
+// the low mantissa bits, so m - 1.5 * 2^23 is rint(q0) exactly and the bit
+// pattern of m minus that of 1.5 * 2^23 is the same integer.  |q0| <= 127.0001
+// here, so no clamp is needed.  If any of the eight lies within 2^-15 of a
+// half-integer (or the scale is not a normal number) the block is redone with
+// quantize_exact.
+__device__ __forceinline__ uint2 quantize8(const float (&y)[8], const QuantScale& s)
+{
+    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+    constexpr int32_t kRoundBits = 0x4B400000;
+    int32_t q[8];
+    bool near_tie = !s.fast;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float q0 = __fmul_rn(y[e], s.recip);
+        const float m = __fadd_rn(q0, kRound);
+        const float t = __fsub_rn(m, kRound);
+        near_tie |= !(fabsf(__fsub_rn(q0, t)) <= 0.5f - 0x1p-15f);
+        q[e] = __float_as_int(m) - kRoundBits;
+    }
+    if (near_tie) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            q[e] = quantize_exact(y[e], s.scale);
+    }
     uint2 u;
-    u.x = (uint32_t(q[0]) & 0xFFu) | ((uint32_t(q[1]) & 0xFFu) << 8) |
-          ((uint32_t(q[2]) & 0xFFu) << 16) | ((uint32_t(q[3]) & 0xFFu) << 24);
-    u.y = (uint32_t(q[4]) & 0xFFu) | ((uint32_t(q[5]) & 0xFFu) << 8) |
-          ((uint32_t(q[6]) & 0xFFu) << 16) | ((uint32_t(q[7]) & 0xFFu) << 24);
+    u.x = pack4_low_bytes(q[0], q[1], q[2], q[3]);
+    u.y = pack4_low_bytes(q[4], q[5], q[6], q[7]);
     return u;
 }
 

@@ -18,6 +18,7 @@ struct Params {
     const uint16_t* weight;
     float eps;
     int hidden;
+    float inv_hidden;         // 1 / hidden if hidden is a power of two, else 0
     int64_t n_rows;
     int threads_per_row;      // T
     int rows_per_cta;         // rows kernel only
@@ -29,13 +30,20 @@ struct Params {
 // Largest CTA for K blocks per thread: the register budget of the bigger
 // tiles (K * 8 accumulators per thread) needs the smaller CTA.
 constexpr int max_threads_for(int K) { return K <= 2 ? 1024 : 512; }
-#ifndef DRADD_MINB1
-#define DRADD_MINB1 1
-#endif
-#ifndef DRADD_MINB2
-#define DRADD_MINB2 1
-#endif
-constexpr int min_blocks_for(int K) { return K == 1 ? DRADD_MINB1 : K == 2 ? DRADD_MINB2 : 1; }
+
+// Resident CTAs per SM the staged kernel with T threads and K blocks per
+// thread is compiled for: the register budget per thread is about 40 for
+// K = 1 (three 512-thread CTAs per SM), 64 for K = 2, 128 for K = 4 and 255
+// for K = 8, capped at 2048 threads and 32 CTAs per SM.
+constexpr int staged_reg_target(int K) { return K == 1 ? 40 : K == 2 ? 64 : K == 4 ? 128 : 255; }
+constexpr int staged_min_blocks(int T, int K)
+{
+    int by_regs = 65536 / (T * staged_reg_target(K));
+    int by_threads = 2048 / T;
+    int b = by_regs < by_threads ? by_regs : by_threads;
+    b = b > 32 ? 32 : b;
+    return b < 1 ? 1 : b;
+}
 
 cudaError_t launch_rows(const Params& p, int K, bool quant, int grid, int threads, bool serialize,
                         cudaStream_t stream);

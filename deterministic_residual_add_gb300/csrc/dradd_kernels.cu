@@ -127,13 +127,8 @@ __device__ __forceinline__ void finish_row(const Params& p, float (&acc)[K][8], 
 #pragma unroll
             for (int j = 0; j < K; ++j) {
                 const int b = t + j * T;
-                if (b < nblocks) {
-                    int32_t q[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        q[e] = quantize_one(acc[j][e], qs);
-                    st_stream(qrow + b, pack8_i8(q));
-                }
+                if (b < nblocks)
+                    st_stream(qrow + b, quantize8(acc[j], qs));
             }
         }
     }
@@ -179,7 +174,7 @@ __device__ __forceinline__ void add_and_store_residual(const Params& p, const ui
 
 // ---------------------------------------------------------------- rows_kernel
 template <int K, bool QUANT>
-__global__ void __launch_bounds__(max_threads_for(K), min_blocks_for(K)) rows_kernel(const Params p)
+__global__ void __launch_bounds__(max_threads_for(K)) rows_kernel(const Params p)
 {
     __shared__ float s_sum[2][32 * K];
     __shared__ float s_max[2][32];
@@ -224,7 +219,7 @@ __global__ void __launch_bounds__(max_threads_for(K), min_blocks_for(K)) rows_ke
         if (T > 32)
             __syncthreads();
         gather_warps<K>(part, T, lane, red);
-        const float inv = inv_rms(fold_k<K>(part), p.hidden, p.eps);
+        const float inv = inv_rms(fold_k<K>(part), p.hidden, p.inv_hidden, p.eps);
         finish_row<K, QUANT>(p, acc, w, inv, row, active, t, T, lane, warp_in_row, nblocks,
                              &s_max[buf][r_local * warps_per_row]);
         buf ^= 1;
@@ -232,13 +227,16 @@ __global__ void __launch_bounds__(max_threads_for(K), min_blocks_for(K)) rows_ke
 }
 
 // -------------------------------------------------------------- staged_kernel
-template <int K, bool QUANT>
-__global__ void __launch_bounds__(max_threads_for(K), min_blocks_for(K)) staged_kernel(const Params p)
+// T (threads per row = threads per CTA) is a compile-time constant so that
+// every (T, K) pair gets its own register budget (staged_min_blocks) and the
+// reduction widths fold away.
+template <int T, int K, bool QUANT>
+__global__ void __launch_bounds__(T, staged_min_blocks(T, K)) staged_kernel(const Params p)
 {
+    static_assert(T >= 32 && T <= 1024 && (T & (T - 1)) == 0, "T: a power of two, 32..1024");
     extern __shared__ __align__(128) unsigned char stage_mem[];
     __shared__ float s_sum[2][32 * K];
     __shared__ float s_max[2][32];
-    const int T = p.threads_per_row;  // == blockDim.x, >= 32
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp_in_row = tid >> 5;
@@ -280,26 +278,16 @@ __global__ void __launch_bounds__(max_threads_for(K), min_blocks_for(K)) staged_
     load_weights<K>(p, w, tid, T, nblocks);
 
     int buf = 0;
+    // Iteration i of this CTA uses stage s = i mod stages and waits for phase
+    // parity floor(i / stages) mod 2; both are kept incrementally.
     int64_t i = 0;
+    int s = 0;
+    uint32_t parity = 0;
     for (int64_t row = blockIdx.x; row < p.n_rows; row += stride, ++i) {
-        const int s = static_cast<int>(i % stages);
-        const uint32_t parity = static_cast<uint32_t>((i / stages) & 1);
+        // A thread whose wait gives up goes on with whatever the stage holds
+        // (outputs are unspecified after a timeout); the CTA learns of it at
+        // the barrier below and stops there, before refilling any stage.
         const bool ok = mbar_wait_bounded(&bars[s], parity, p.wait_limit_ns);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) {
-                atomicOr(&g_device_status, kDeviceStatusTimeout);
-                // Copies already issued must land before shared memory is released.
-                for (int64_t i2 = i; i2 < i + stages; ++i2) {
-                    if (blockIdx.x + i2 * stride >= p.n_rows)
-                        break;
-                    if (p.fault_inject && i2 == 0)
-                        continue;
-                    mbar_wait_bounded(&bars[i2 % stages], static_cast<uint32_t>((i2 / stages) & 1),
-                                      p.wait_limit_ns);
-                }
-            }
-            return;
-        }
         const unsigned char* sbase = stage_mem + static_cast<size_t>(s) * stage_bytes;
         const uint4* xs = reinterpret_cast<const uint4*>(sbase);
         const uint4* rs = reinterpret_cast<const uint4*>(sbase + row_bytes);
@@ -317,7 +305,27 @@ __global__ void __launch_bounds__(max_threads_for(K), min_blocks_for(K)) staged_
 
         float* red = &s_sum[buf][0];
         lanes_then_publish<K>(part, T, lane, warp_in_row, red);
-        __syncthreads();  // every thread has read stage s: refill it
+        // Every thread has read stage s (so it can be refilled) and published
+        // its warp's partial sums; any expired wait ends the CTA here.
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(&g_device_status, kDeviceStatusTimeout);
+                // Copies already issued must land before shared memory is released.
+                int s2 = s;
+                uint32_t parity2 = parity;
+                for (int64_t i2 = i; i2 < i + stages; ++i2) {
+                    if (blockIdx.x + i2 * stride >= p.n_rows)
+                        break;
+                    if (!(p.fault_inject && i2 == 0))
+                        mbar_wait_bounded(&bars[s2], parity2, p.wait_limit_ns);
+                    if (++s2 == stages) {
+                        s2 = 0;
+                        parity2 ^= 1u;
+                    }
+                }
+            }
+            return;
+        }
         if (tid == 0) {
             const int64_t next = row + static_cast<int64_t>(stages) * stride;
             if (next < p.n_rows) {
@@ -326,10 +334,14 @@ __global__ void __launch_bounds__(max_threads_for(K), min_blocks_for(K)) staged_
             }
         }
         gather_warps<K>(part, T, lane, red);
-        const float inv = inv_rms(fold_k<K>(part), p.hidden, p.eps);
+        const float inv = inv_rms(fold_k<K>(part), p.hidden, p.inv_hidden, p.eps);
         finish_row<K, QUANT>(p, acc, w, inv, row, true, tid, T, lane, warp_in_row, nblocks,
                              &s_max[buf][0]);
         buf ^= 1;
+        if (++s == stages) {
+            s = 0;
+            parity ^= 1u;
+        }
     }
 }
 
@@ -367,33 +379,68 @@ KernelFn rows_fn(int K, bool quant)
     }
 }
 
-KernelFn staged_fn(int K, bool quant)
+// Staged kernels exist for T = 32..1024 and K in {1, 2, 4, 8} with
+// T <= max_threads_for(K); index = (log2(T) - 5) * 8 + log2(K) * 2 + quant.
+constexpr int kStagedKernels = 6 * 8;
+
+template <int T, int K>
+constexpr bool staged_exists() { return T <= max_threads_for(K); }
+
+template <int T, int K>
+KernelFn staged_pick(bool quant)
+{
+    if constexpr (staged_exists<T, K>())
+        return quant ? staged_kernel<T, K, true> : staged_kernel<T, K, false>;
+    else
+        return nullptr;
+}
+
+template <int T>
+KernelFn staged_by_k(int K, bool quant)
 {
     switch (K) {
-    case 1: return quant ? staged_kernel<1, true> : staged_kernel<1, false>;
-    case 2: return quant ? staged_kernel<2, true> : staged_kernel<2, false>;
-    case 4: return quant ? staged_kernel<4, true> : staged_kernel<4, false>;
-    case 8: return quant ? staged_kernel<8, true> : staged_kernel<8, false>;
+    case 1: return staged_pick<T, 1>(quant);
+    case 2: return staged_pick<T, 2>(quant);
+    case 4: return staged_pick<T, 4>(quant);
+    case 8: return staged_pick<T, 8>(quant);
     default: return nullptr;
     }
 }
 
-constexpr int kMaxDevices = 64;
-// Per device: bit k set once staged kernel k has been allowed its full
-// dynamic shared memory.
-std::atomic<uint32_t> g_smem_attr_done[kMaxDevices];
-
-int kernel_index(int K, bool quant)
+KernelFn staged_fn(int T, int K, bool quant)
 {
-    const int kk = K == 1 ? 0 : K == 2 ? 1 : K == 4 ? 2 : 3;
-    return kk * 2 + (quant ? 1 : 0);
+    switch (T) {
+    case 32: return staged_by_k<32>(K, quant);
+    case 64: return staged_by_k<64>(K, quant);
+    case 128: return staged_by_k<128>(K, quant);
+    case 256: return staged_by_k<256>(K, quant);
+    case 512: return staged_by_k<512>(K, quant);
+    case 1024: return staged_by_k<1024>(K, quant);
+    default: return nullptr;
+    }
 }
+
+int log2i(int v)
+{
+    int l = 0;
+    while ((1 << l) < v)
+        ++l;
+    return l;
+}
+
+int staged_index(int T, int K, bool quant) { return (log2i(T) - 5) * 8 + log2i(K) * 2 + (quant ? 1 : 0); }
+
+constexpr int kMaxDevices = 64;
+// Per device: bit k set once staged kernel k (staged_index) has been allowed
+// its full dynamic shared memory.
+std::atomic<uint64_t> g_smem_attr_done[kMaxDevices];
+static_assert(kStagedKernels <= 64, "one bit per staged kernel");
 
 // Allow staged kernel `fn` the device's full opt-in dynamic shared memory
 // (once per device and kernel).
-cudaError_t ensure_smem_attr(KernelFn fn, int K, bool quant, int dev)
+cudaError_t ensure_smem_attr(KernelFn fn, int index, int dev)
 {
-    const uint32_t bit = 1u << kernel_index(K, quant);
+    const uint64_t bit = 1ull << index;
     if (dev >= 0 && dev < kMaxDevices && (g_smem_attr_done[dev].load(std::memory_order_acquire) & bit))
         return cudaSuccess;
     int optin = 0;
@@ -447,14 +494,14 @@ cudaError_t launch_rows(const Params& p, int K, bool quant, int grid, int thread
 cudaError_t launch_staged(const Params& p, int K, bool quant, int grid, int threads, size_t dyn_smem,
                           bool serialize, cudaStream_t stream)
 {
-    KernelFn fn = staged_fn(K, quant);
+    KernelFn fn = staged_fn(threads, K, quant);
     if (!fn)
         return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    e = ensure_smem_attr(fn, K, quant, dev);
+    e = ensure_smem_attr(fn, staged_index(threads, K, quant), dev);
     if (e != cudaSuccess)
         return e;
     return launch(fn, p, grid, threads, dyn_smem, serialize, stream);
@@ -462,14 +509,14 @@ cudaError_t launch_staged(const Params& p, int K, bool quant, int grid, int thre
 
 cudaError_t staged_occupancy(int K, bool quant, int threads, size_t dyn_smem, int* blocks_per_sm)
 {
-    KernelFn fn = staged_fn(K, quant);
+    KernelFn fn = staged_fn(threads, K, quant);
     if (!fn)
         return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    e = ensure_smem_attr(fn, K, quant, dev);
+    e = ensure_smem_attr(fn, staged_index(threads, K, quant), dev);
     if (e != cudaSuccess)
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, threads, dyn_smem);
