@@ -43,24 +43,32 @@ N_SETS = 4
 KERNEL_SOURCES = ["csrc/dradd_kernels.cu", "csrc/dradd_device.cuh"]
 TRAFFIC_FILE = ROOT / "profiles" / "add_rmsnorm_fwd_4096x4096_ncu.md"
 
-# name -> (n_rows, hidden, int8 out, input recipe).  The first is the
-# headline workload; the others are for profiling and context.
+# name -> (n_rows, hidden, op, input recipe).  The first is the headline
+# workload; the others are for profiling and context.  op is one of
+# add_rmsnorm, add_rmsnorm_quant, rmsnorm, rmsnorm_quant, residual_add.
 WORKLOADS = {
-    "4096x4096": (4096, 4096, False, "chain4096"),
-    "2048x4096": (2048, 4096, False, "2048x4096"),
-    "4096x8192": (4096, 8192, False, "4096x8192"),
-    "2048x16384": (2048, 16384, False, "quant2048x16384"),
-    "quant2048x16384": (2048, 16384, True, "quant2048x16384"),
-    "quant4096x4096": (4096, 4096, True, "chain4096"),
+    "4096x4096": (4096, 4096, "add_rmsnorm", "chain4096"),
+    "2048x4096": (2048, 4096, "add_rmsnorm", "2048x4096"),
+    "4096x8192": (4096, 8192, "add_rmsnorm", "4096x8192"),
+    "2048x16384": (2048, 16384, "add_rmsnorm", "quant2048x16384"),
+    "quant2048x16384": (2048, 16384, "add_rmsnorm_quant", "quant2048x16384"),
+    "quant4096x4096": (4096, 4096, "add_rmsnorm_quant", "chain4096"),
+    "rmsnorm4096x4096": (4096, 4096, "rmsnorm", "chain4096"),
+    "rmsnorm_quant4096x4096": (4096, 4096, "rmsnorm_quant", "chain4096"),
+    "residual_add4096x4096": (4096, 4096, "residual_add", "chain4096"),
 }
 
 
-def algorithmic_bytes(n_rows: int, hidden: int, quant: bool = False) -> int:
-    """x, residual read + residual_out written (2 bytes each), out written
-    (2 bytes bf16, or 1 byte int8 plus a 4-byte scale per row), weight once."""
-    if quant:
-        return 7 * n_rows * hidden + 4 * n_rows + 2 * hidden
-    return 8 * n_rows * hidden + 2 * hidden
+def algorithmic_bytes(n_rows: int, hidden: int, op: str = "add_rmsnorm") -> int:
+    """Bytes the op must move: bf16 reads of x (and residual), bf16 writes of
+    residual_out (add forms) and out (2 bytes) or int8 out (1 byte) plus a
+    4-byte scale per row, and the weight once (norm forms)."""
+    e = n_rows * hidden
+    return {"add_rmsnorm": 8 * e + 2 * hidden,
+            "add_rmsnorm_quant": 7 * e + 4 * n_rows + 2 * hidden,
+            "rmsnorm": 4 * e + 2 * hidden,
+            "rmsnorm_quant": 3 * e + 4 * n_rows + 2 * hidden,
+            "residual_add": 6 * e}[op]
 
 
 def measured_peaks() -> dict:
@@ -177,7 +185,7 @@ def max_over_ranks(v: float, world: int) -> float:
 # ---------------------------------------------------------------- workload
 def workload_inputs(name: str):
     """(one x per buffer set, residual, weight) as CPU bf16 tensors."""
-    n, h, quant, recipe = WORKLOADS[name]
+    n, h, _, recipe = WORKLOADS[name]
     if recipe == "chain4096":
         ch = inputs.CHAIN4096
         r0, w = ch.initial()
@@ -191,13 +199,13 @@ def workload_inputs(name: str):
 def make_sets(device, name: str):
     """N_SETS independent buffer sets; set 0 holds the workload's own first
     draw (used by the parity spot check)."""
-    n, h, quant, _ = WORKLOADS[name]
+    n, h, op, _ = WORKLOADS[name]
     xs, r0, w = workload_inputs(name)
     sets = []
     for x_cpu in xs:
         x = x_cpu.to(device)
         s = {"x": x, "r": r0.to(device), "out": torch.empty_like(x), "ro": torch.empty_like(x)}
-        if quant:
+        if op.endswith("quant"):
             s["q"] = torch.empty(n, h, dtype=torch.int8, device=device)
             s["scale"] = torch.empty(n, dtype=torch.float32, device=device)
         sets.append(s)
@@ -205,23 +213,33 @@ def make_sets(device, name: str):
 
 
 class RawCall:
-    """Precomputed C-ABI calls, one per buffer set:
-    add_rmsnorm_fwd(out, residual_out, x, residual, weight, eps, n, h, stream)
-    or add_rmsnorm_quant_fwd(out_q, scale, residual_out, x, ...)."""
+    """Precomputed C-ABI calls, one per buffer set, of the workload's op:
+    add_rmsnorm_fwd(out, residual_out, x, residual, weight, eps, n, h, stream),
+    add_rmsnorm_quant_fwd(out_q, scale, residual_out, x, residual, ...),
+    rmsnorm_fwd(out, x, weight, ...), rmsnorm_quant_fwd(out_q, scale, x, ...)
+    or residual_add_fwd(residual_out, x, residual, n, h, stream)."""
 
-    def __init__(self, sets, w, stream, n_rows, hidden, quant):
+    def __init__(self, sets, w, stream, n_rows, hidden, op):
         L = dr.lib()
-        self.fn = L.add_rmsnorm_quant_fwd if quant else L.add_rmsnorm_fwd
-        self.name = "add_rmsnorm_quant_fwd" if quant else "add_rmsnorm_fwd"
+        self.name = op + "_fwd"
+        self.fn = getattr(L, self.name)
         eps = ctypes.c_float(inputs.EPS)
-        if quant:
-            self.args = [(s["q"].data_ptr(), s["scale"].data_ptr(), s["ro"].data_ptr(),
-                          s["x"].data_ptr(), s["r"].data_ptr(), w.data_ptr(), eps, n_rows, hidden,
-                          stream.cuda_stream) for s in sets]
-        else:
-            self.args = [(s["out"].data_ptr(), s["ro"].data_ptr(), s["x"].data_ptr(),
-                          s["r"].data_ptr(), w.data_ptr(), eps, n_rows, hidden, stream.cuda_stream)
-                         for s in sets]
+        st = stream.cuda_stream
+        wp = w.data_ptr()
+
+        def args(s):
+            x, r, ro = s["x"].data_ptr(), s["r"].data_ptr(), s["ro"].data_ptr()
+            if op == "add_rmsnorm":
+                return (s["out"].data_ptr(), ro, x, r, wp, eps, n_rows, hidden, st)
+            if op == "add_rmsnorm_quant":
+                return (s["q"].data_ptr(), s["scale"].data_ptr(), ro, x, r, wp, eps, n_rows, hidden, st)
+            if op == "rmsnorm":
+                return (s["out"].data_ptr(), x, wp, eps, n_rows, hidden, st)
+            if op == "rmsnorm_quant":
+                return (s["q"].data_ptr(), s["scale"].data_ptr(), x, wp, eps, n_rows, hidden, st)
+            return (ro, x, r, n_rows, hidden, st)
+
+        self.args = [args(s) for s in sets]
 
     def __call__(self, i: int):
         st = self.fn(*self.args[i % len(self.args)])
@@ -269,48 +287,33 @@ def time_device(call, steps, warmup, stream, world, use_graph):
     return start.elapsed_time(end)  # ms
 
 
-def time_e2e(steps, device, stream, name):
-    """Public API with host data: per step, copy x and residual (and weight)
-    from pinned host memory, run the op, read its outputs back."""
-    n, h, quant, _ = WORKLOADS[name]
+def time_e2e(steps, device, stream, name, chunk_rows=1024):
+    """Public API with host data: per step, the inputs (x, residual, weight)
+    go from pinned host memory to the device and the outputs come back, with
+    the copies overlapped with the kernels chunk by chunk (host.HostPipeline)."""
+    from deterministic_residual_add_gb300.host import HostPipeline
+    n, h, op, _ = WORKLOADS[name]
+    quant = op == "add_rmsnorm_quant"
     xs, r0, w = workload_inputs(name)
     x_h, r_h, w_h = xs[0].pin_memory(), r0.pin_memory(), w.pin_memory()
-    x_d, r_d = torch.empty_like(x_h, device=device), torch.empty_like(r_h, device=device)
-    wd = torch.empty_like(w_h, device=device)
-    ro_d = torch.empty_like(x_d)
     ro_h = torch.empty_like(x_h).pin_memory()
     if quant:
-        q_d = torch.empty(n, h, dtype=torch.int8, device=device)
-        s_d = torch.empty(n, dtype=torch.float32, device=device)
-        outs = [(q_d, torch.empty(n, h, dtype=torch.int8).pin_memory()),
-                (s_d, torch.empty(n, dtype=torch.float32).pin_memory()), (ro_d, ro_h)]
+        outs = (torch.empty(n, h, dtype=torch.int8).pin_memory(),
+                torch.empty(n, dtype=torch.float32).pin_memory(), ro_h)
     else:
-        out_d = torch.empty_like(x_d)
-        outs = [(out_d, torch.empty_like(x_h).pin_memory()), (ro_d, ro_h)]
-
-    def step():
-        x_d.copy_(x_h, non_blocking=True)
-        r_d.copy_(r_h, non_blocking=True)
-        wd.copy_(w_h, non_blocking=True)
-        if quant:
-            dr.add_rmsnorm_quant_fwd(x_d, r_d, wd, inputs.EPS, out_q=q_d, scale=s_d,
-                                     residual_out=ro_d, stream=stream)
-        else:
-            dr.add_rmsnorm_fwd(x_d, r_d, wd, inputs.EPS, out=out_d, residual_out=ro_d, stream=stream)
-        for dev_t, host_t in outs:
-            host_t.copy_(dev_t, non_blocking=True)
-
+        outs = (torch.empty_like(x_h).pin_memory(), ro_h)
+    pipe = HostPipeline(n, h, device, chunk_rows=chunk_rows, quant=quant)
     with torch.cuda.stream(stream):
         for _ in range(2):
-            step()
+            pipe(x_h, r_h, w_h, inputs.EPS, outs)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(steps):
-            step()
-        stream.synchronize()
+            pipe(x_h, r_h, w_h, inputs.EPS, outs)
+        torch.cuda.synchronize()
         dt = time.perf_counter() - t0
     bi = (x_h.numel() + r_h.numel() + w_h.numel()) * 2
-    bo = sum(h_t.numel() * h_t.element_size() for _, h_t in outs)
+    bo = sum(t.numel() * t.element_size() for t in outs)
     return dt, bi, bo
 
 
@@ -320,9 +323,14 @@ def cpu_baseline(seconds: float, name: str, first_inputs, gpu_set0=None):
     import numpy as np
     import oracle
     o = oracle.lib()
-    n, h, quant, _ = WORKLOADS[name]
+    n, h, op, _ = WORKLOADS[name]
     x0, r0, w = first_inputs
-    fn = o.add_rmsnorm_quant_fwd if quant else o.add_rmsnorm_fwd
+    fns = {"add_rmsnorm": lambda x, r: o.add_rmsnorm_fwd(x, r, w, inputs.EPS),
+           "add_rmsnorm_quant": lambda x, r: o.add_rmsnorm_quant_fwd(x, r, w, inputs.EPS),
+           "rmsnorm": lambda x, r: (o.rmsnorm_fwd(x, w, inputs.EPS),),
+           "rmsnorm_quant": lambda x, r: o.rmsnorm_quant_fwd(x, w, inputs.EPS),
+           "residual_add": lambda x, r: (o.residual_add_fwd(x, r),)}
+    fn = fns[op]
     chunk = 64
     rows = 0
     first = None
@@ -330,14 +338,14 @@ def cpu_baseline(seconds: float, name: str, first_inputs, gpu_set0=None):
     while True:
         lo = rows % n
         hi = min(n, lo + chunk)
-        res = fn(x0[lo:hi], r0[lo:hi], w, inputs.EPS)
+        res = fn(x0[lo:hi], r0[lo:hi])
         if first is None:
             first = res
         rows += hi - lo
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    out = {"value": algorithmic_bytes(rows, h, quant) / dt / 1e9, "unit": "GB/s", "cores": 1,
+    out = {"value": algorithmic_bytes(rows, h, op) / dt / 1e9, "unit": "GB/s", "cores": 1,
            "kind": "oracle",
            "sample": f"{rows} rows of the {n}x{h} workload ({rows * h} elements) in "
                      f"{dt:.1f} s, single thread",
@@ -348,7 +356,8 @@ def cpu_baseline(seconds: float, name: str, first_inputs, gpu_set0=None):
             if t.dtype == torch.bfloat16:
                 t = t.view(torch.int16)
             return t.numpy()
-        keys = ["q", "scale", "ro"] if quant else ["out", "ro"]
+        keys = {"add_rmsnorm": ["out", "ro"], "add_rmsnorm_quant": ["q", "scale", "ro"],
+                "rmsnorm": ["out"], "rmsnorm_quant": ["q", "scale"], "residual_add": ["ro"]}[op]
         got = [host(gpu_set0[k]) for k in keys]
         out["parity_rows_checked"] = chunk
         out["parity_bit_exact"] = bool(all(
@@ -360,18 +369,19 @@ def cpu_baseline(seconds: float, name: str, first_inputs, gpu_set0=None):
 def run_ours(args):
     world, rank, local = dist_setup()
     device = torch.device("cuda", local)
-    n_rows, hidden, quant, _ = WORKLOADS[args.workload]
+    n_rows, hidden, op, _ = WORKLOADS[args.workload]
+    quant = op.endswith("quant")
     dr.lib()
     stream = torch.cuda.Stream(device)
     sets, w_dev, first_inputs = make_sets(device, args.workload)
     torch.cuda.synchronize()
-    call = RawCall(sets, w_dev, stream, n_rows, hidden, quant)
+    call = RawCall(sets, w_dev, stream, n_rows, hidden, op)
     with torch.cuda.stream(stream):
         sampler = ClockSampler(local)
         with sampler:
             ms = time_device(call, args.steps, args.warmup, stream, world, args.graph)
     ms = max_over_ranks(ms, world)
-    bytes_step = algorithmic_bytes(n_rows, hidden, quant)
+    bytes_step = algorithmic_bytes(n_rows, hidden, op)
     ms_per_step = ms / args.steps
     value = world * bytes_step * args.steps / (ms / 1e3) / 1e9
     per_launch_gbs = bytes_step / (ms_per_step / 1e3) / 1e9
@@ -381,29 +391,35 @@ def run_ours(args):
         peak = 6800.0
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and op.startswith("add_rmsnorm"):
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
         dt, bi, bo = time_e2e(e2e_steps, device, stream, args.workload)
         dt = max_over_ranks(dt, world)
         e2e = {"value": round(world * bytes_step * e2e_steps / dt / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
-               "ms_per_step": round(dt / e2e_steps * 1e3, 4)}
+               "ms_per_step": round(dt / e2e_steps * 1e3, 4),
+               "pipeline": "1024-row chunks, upload / kernel / download on 3 streams"}
 
-    cfg = dr.resolve_config(n_rows, hidden, quant=quant,
-                            sm_count=torch.cuda.get_device_properties(device).multi_processor_count)
-    op = "add_rmsnorm_quant_fwd" if quant else "add_rmsnorm_fwd"
-    io = "bf16 in, int8 + fp32 scale + bf16 residual_out out" if quant else "bf16 in/out"
+    sm_count = torch.cuda.get_device_properties(device).multi_processor_count
+    if op == "residual_add":
+        launch = {"variant": "elementwise"}
+    else:
+        cfg = dr.resolve_config(n_rows, hidden, quant=quant, sm_count=sm_count, add=op.startswith("add"))
+        launch = {"variant": "rows" if cfg.variant == 1 else "staged",
+                  "threads_per_row": cfg.threads_per_row, "rows_per_cta": cfg.rows_per_cta,
+                  "stages": cfg.stages}
+    io = {"add_rmsnorm": "bf16 in/out", "add_rmsnorm_quant": "bf16 in, int8 + fp32 scale + bf16 residual_out out",
+          "rmsnorm": "bf16 in/out", "rmsnorm_quant": "bf16 in, int8 + fp32 scale out",
+          "residual_add": "bf16 in/out"}[op]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"{op} {n_rows}x{hidden} {io}", "n_rows": n_rows, "hidden": hidden,
+        "config": {"workload": f"{op}_fwd {n_rows}x{hidden} {io}", "n_rows": n_rows, "hidden": hidden,
                    "io_dtype": "bf16",
                    "l2": f"{N_SETS} rotating buffer sets ({N_SETS * bytes_step // 2**20} MiB) > L2",
-                   "launch": {"variant": "rows" if cfg.variant == 1 else "staged",
-                              "threads_per_row": cfg.threads_per_row, "rows_per_cta": cfg.rows_per_cta,
-                              "stages": cfg.stages},
+                   "launch": launch,
                    "cuda_graph": bool(args.graph), "parallelism": f"replicas x{world}"},
         "rows_per_s": round(world * n_rows * args.steps / (ms / 1e3), 1),
         "roofline": {"bound": "hbm", "achieved": round(per_launch_gbs, 2), "peak": peak,
@@ -431,30 +447,34 @@ def run_reference(args):
         return
     import oracle
     o = oracle.lib()
-    n, h, quant, _ = WORKLOADS[args.workload]
+    n, h, op, _ = WORKLOADS[args.workload]
     xs, r0, w = workload_inputs(args.workload)
     x0 = xs[0]
-    fn = o.add_rmsnorm_quant_fwd if quant else o.add_rmsnorm_fwd
+    fns = {"add_rmsnorm": lambda x, r: o.add_rmsnorm_fwd(x, r, w, inputs.EPS),
+           "add_rmsnorm_quant": lambda x, r: o.add_rmsnorm_quant_fwd(x, r, w, inputs.EPS),
+           "rmsnorm": lambda x, r: o.rmsnorm_fwd(x, w, inputs.EPS),
+           "rmsnorm_quant": lambda x, r: o.rmsnorm_quant_fwd(x, w, inputs.EPS),
+           "residual_add": lambda x, r: o.residual_add_fwd(x, r)}
+    fn = fns[op]
     t0 = time.perf_counter()
-    fn(x0[:16], r0[:16], w, inputs.EPS)
+    fn(x0[:16], r0[:16])
     t_row = max(1e-6, (time.perf_counter() - t0) / 16)
     total = args.warmup + args.steps
     rows = int(max(1, min(n, args.reference_seconds / total / t_row)))
     for _ in range(args.warmup):
-        fn(x0[:rows], r0[:rows], w, inputs.EPS)
+        fn(x0[:rows], r0[:rows])
     t0 = time.perf_counter()
     for i in range(args.steps):
         lo = (i * rows) % (n - rows + 1)
-        fn(x0[lo:lo + rows], r0[lo:lo + rows], w, inputs.EPS)
+        fn(x0[lo:lo + rows], r0[lo:lo + rows])
     dt = time.perf_counter() - t0
-    value = algorithmic_bytes(rows, h, quant) * args.steps / dt / 1e9
-    op = "add_rmsnorm_quant_fwd" if quant else "add_rmsnorm_fwd"
+    value = algorithmic_bytes(rows, h, op) * args.steps / dt / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"{op} {n}x{h} (CPU oracle)", "n_rows": n, "hidden": h,
+        "config": {"workload": f"{op}_fwd {n}x{h} (CPU oracle)", "n_rows": n, "hidden": h,
                    "io_dtype": "bf16", "rows_per_step": rows},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{rows} of {n} rows per step, single thread"},

@@ -21,7 +21,8 @@ from pathlib import Path
 
 __all__ = [
     "add_rmsnorm_fwd", "add_rmsnorm_quant_fwd", "add_rmsnorm_fwd_with_config",
-    "add_rmsnorm_quant_fwd_with_config", "LaunchConfig", "DraddError", "resolve_config",
+    "add_rmsnorm_quant_fwd_with_config", "rmsnorm_fwd", "rmsnorm_quant_fwd", "residual_add_fwd",
+    "LaunchConfig", "DraddError", "resolve_config",
     "device_status", "bf16_convert_range", "status_string", "abi_version", "lib", "library_path",
     "VARIANT_AUTO", "VARIANT_ROWS", "VARIANT_STAGED", "MAX_HIDDEN",
 ]
@@ -30,6 +31,7 @@ PKG = Path(__file__).resolve().parent
 LIB_PATH = PKG / "libdradd.so"
 MAX_HIDDEN = 32768
 VARIANT_AUTO, VARIANT_ROWS, VARIANT_STAGED = 0, 1, 2
+OP_ADD_RMSNORM, OP_ADD_RMSNORM_QUANT, OP_RMSNORM, OP_RMSNORM_QUANT = 0, 1, 2, 3
 
 STATUS_NAMES = {
     0: "OK", 1: "NULL_PTR", 2: "BAD_SHAPE", 3: "UNSUPPORTED_HIDDEN", 4: "MISALIGNED",
@@ -98,6 +100,11 @@ def lib() -> ctypes.CDLL:
                        ("add_rmsnorm_quant_fwd", quant_args),
                        ("add_rmsnorm_fwd_with_config", bf16_args + [cfgp]),
                        ("add_rmsnorm_quant_fwd_with_config", quant_args + [cfgp]),
+                       ("rmsnorm_fwd", [_vp, _vp, _vp, _f32, _i64, _i64, _vp]),
+                       ("rmsnorm_quant_fwd", [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp]),
+                       ("rmsnorm_fwd_with_config", [_vp, _vp, _vp, _f32, _i64, _i64, _vp, cfgp]),
+                       ("rmsnorm_quant_fwd_with_config", [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp, cfgp]),
+                       ("residual_add_fwd", [_vp, _vp, _vp, _i64, _i64, _vp]),
                        ("dradd_resolve_config", [_i64, _i64, ctypes.c_int, ctypes.c_int, cfgp]),
                        ("dradd_device_status", [_vp, ctypes.c_int]),
                        ("dradd_bf16_convert_range", [_vp, ctypes.c_uint64, _i64, ctypes.c_int, _vp])]:
@@ -188,6 +195,15 @@ def add_rmsnorm_fwd(x, residual, weight, eps: float = 1e-6, *, out=None, residua
     return out, residual_out
 
 
+def _check_quant_outs(out_q, scale, n, n_rows):
+    torch = _torch()
+    if out_q.dtype != torch.int8 or not out_q.is_cuda or not out_q.is_contiguous() or out_q.numel() != n:
+        raise ValueError("out_q must be a contiguous CUDA int8 tensor shaped like x")
+    if (scale.dtype != torch.float32 or not scale.is_cuda or not scale.is_contiguous()
+            or scale.numel() != n_rows):
+        raise ValueError("scale must be a contiguous CUDA float32 tensor with one entry per row")
+
+
 def add_rmsnorm_quant_fwd(x, residual, weight, eps: float = 1e-6, *, out_q=None, scale=None,
                           residual_out=None, stream=None, config: LaunchConfig | None = None):
     """out_q (int8), scale (fp32 per row), residual_out (bf16) of the quant variant."""
@@ -200,11 +216,7 @@ def add_rmsnorm_quant_fwd(x, residual, weight, eps: float = 1e-6, *, out_q=None,
         scale = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
     if residual_out is None:
         residual_out = torch.empty_like(x)
-    if out_q.dtype != torch.int8 or not out_q.is_cuda or not out_q.is_contiguous() or out_q.numel() != n:
-        raise ValueError("out_q must be a contiguous CUDA int8 tensor shaped like x")
-    if (scale.dtype != torch.float32 or not scale.is_cuda or not scale.is_contiguous()
-            or scale.numel() != n_rows):
-        raise ValueError("scale must be a contiguous CUDA float32 tensor with one entry per row")
+    _check_quant_outs(out_q, scale, n, n_rows)
     args = (out_q.data_ptr(), scale.data_ptr(), _bf16_ptr(residual_out, "residual_out", n),
             _bf16_ptr(x, "x", n), _bf16_ptr(residual, "residual", n),
             _bf16_ptr(weight, "weight", hidden), float(eps), n_rows, hidden,
@@ -228,13 +240,70 @@ def add_rmsnorm_quant_fwd_with_config(x, residual, weight, eps, config: LaunchCo
 
 
 def resolve_config(n_rows: int, hidden: int, quant: bool = False, sm_count: int = 152,
-                   config: LaunchConfig | None = None) -> LaunchConfig:
+                   config: LaunchConfig | None = None, add: bool = True) -> LaunchConfig:
     """The configuration the library would launch for this shape (no GPU
-    work when sm_count > 0)."""
+    work when sm_count > 0); add=False for plain RMSNorm."""
+    op = (OP_ADD_RMSNORM if add else OP_RMSNORM) + (1 if quant else 0)
     c = (config or LaunchConfig())._c()
-    _check(lib().dradd_resolve_config(int(n_rows), int(hidden), int(bool(quant)), int(sm_count),
-                                      ctypes.byref(c)), "dradd_resolve_config")
+    _check(lib().dradd_resolve_config(int(n_rows), int(hidden), op, int(sm_count), ctypes.byref(c)),
+           "dradd_resolve_config")
     return LaunchConfig._from_c(c)
+
+
+def rmsnorm_fwd(x, weight, eps: float = 1e-6, *, out=None, stream=None,
+                config: LaunchConfig | None = None):
+    """Plain RMSNorm (no residual): out = bf16_rne((x * inv) * weight)."""
+    torch = _torch()
+    n_rows, hidden = _shape(x, None)
+    n = n_rows * hidden
+    if out is None:
+        out = torch.empty_like(x)
+    args = (_bf16_ptr(out, "out", n), _bf16_ptr(x, "x", n), _bf16_ptr(weight, "weight", hidden),
+            float(eps), n_rows, hidden, _stream_handle(stream, x.device))
+    with torch.cuda.device(x.device):
+        if config is None:
+            _check(lib().rmsnorm_fwd(*args), "rmsnorm_fwd")
+        else:
+            c = config._c()
+            _check(lib().rmsnorm_fwd_with_config(*args, ctypes.byref(c)), "rmsnorm_fwd_with_config")
+    return out
+
+
+def rmsnorm_quant_fwd(x, weight, eps: float = 1e-6, *, out_q=None, scale=None, stream=None,
+                      config: LaunchConfig | None = None):
+    """Plain RMSNorm with per-row symmetric int8 out: (out_q, scale)."""
+    torch = _torch()
+    n_rows, hidden = _shape(x, None)
+    n = n_rows * hidden
+    if out_q is None:
+        out_q = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    if scale is None:
+        scale = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    _check_quant_outs(out_q, scale, n, n_rows)
+    args = (out_q.data_ptr(), scale.data_ptr(), _bf16_ptr(x, "x", n), _bf16_ptr(weight, "weight", hidden),
+            float(eps), n_rows, hidden, _stream_handle(stream, x.device))
+    with torch.cuda.device(x.device):
+        if config is None:
+            _check(lib().rmsnorm_quant_fwd(*args), "rmsnorm_quant_fwd")
+        else:
+            c = config._c()
+            _check(lib().rmsnorm_quant_fwd_with_config(*args, ctypes.byref(c)),
+                   "rmsnorm_quant_fwd_with_config")
+    return out_q, scale
+
+
+def residual_add_fwd(x, residual, *, residual_out=None, stream=None):
+    """residual_out = bf16_rne(fp32(x) + fp32(residual))."""
+    torch = _torch()
+    n_rows, hidden = _shape(x, None)
+    n = n_rows * hidden
+    if residual_out is None:
+        residual_out = torch.empty_like(x)
+    args = (_bf16_ptr(residual_out, "residual_out", n), _bf16_ptr(x, "x", n),
+            _bf16_ptr(residual, "residual", n), n_rows, hidden, _stream_handle(stream, x.device))
+    with torch.cuda.device(x.device):
+        _check(lib().residual_add_fwd(*args), "residual_add_fwd")
+    return residual_out
 
 
 def device_status(stream=None, clear: bool = True, device=None) -> int:

@@ -87,9 +87,32 @@ Range range_of(const void* p, int64_t bytes)
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Outputs must not overlap one another.  A bf16 output may coincide exactly
+// with x or residual (inputs 0 and 2: each element is read by the thread that
+// later writes it, before it writes it); any other overlap with an input is
+// rejected.
+dradd_status check_overlaps(const Range* inputs, int n_in, const Range* outs, const bool* bf16_out, int n_out)
+{
+    for (int a = 0; a < n_out; ++a)
+        for (int b = a + 1; b < n_out; ++b)
+            if (outs[a].overlaps(outs[b]))
+                return DRADD_ERR_ALIAS;
+    for (int a = 0; a < n_out; ++a) {
+        for (int b = 0; b < n_in; ++b) {
+            if (!outs[a].overlaps(inputs[b]))
+                continue;
+            if (bf16_out[a] && b != 1 && outs[a].same(inputs[b]))
+                continue;
+            return DRADD_ERR_ALIAS;
+        }
+    }
+    return DRADD_OK;
+}
+
 // Shape, pointers, eps and overlaps.  out/out_q/scale: whichever the variant
 // writes (the others NULL).  Returns DRADD_OK with *noop set for n_rows == 0.
-dradd_status validate(bool quant, const void* out, const void* out_q, const void* scale,
+// add = false (plain RMSNorm): residual and residual_out are not used.
+dradd_status validate(bool quant, bool add, const void* out, const void* out_q, const void* scale,
                       const void* residual_out, const void* x, const void* residual, const void* weight,
                       float eps, int64_t n_rows, int64_t hidden, bool* noop)
 {
@@ -105,50 +128,41 @@ dradd_status validate(bool quant, const void* out, const void* out_q, const void
         return DRADD_OK;
     }
     const void* primary_out = quant ? out_q : out;
-    if (!primary_out || !residual_out || !x || !residual || !weight || (quant && !scale))
+    if (!primary_out || !x || !weight || (quant && !scale) || (add && (!residual_out || !residual)))
         return DRADD_ERR_NULL_PTR;
-    if (!aligned(primary_out, 16) || !aligned(residual_out, 16) || !aligned(x, 16) ||
-        !aligned(residual, 16) || !aligned(weight, 16) || (quant && !aligned(scale, 4)))
+    if (!aligned(primary_out, 16) || !aligned(x, 16) || !aligned(weight, 16) ||
+        (quant && !aligned(scale, 4)) || (add && (!aligned(residual_out, 16) || !aligned(residual, 16))))
         return DRADD_ERR_MISALIGNED;
     if (!std::isfinite(eps) || eps < 0.0f)
         return DRADD_ERR_BAD_EPS;
 
     const int64_t elems = n_rows * hidden;
-    const Range rx = range_of(x, elems * 2), rr = range_of(residual, elems * 2);
-    const Range rw = range_of(weight, hidden * 2);
-    const Range rro = range_of(residual_out, elems * 2);
-    const Range inputs[3] = {rx, rr, rw};
+    // inputs: x, weight[, residual]; outputs: the bf16 ones first.
+    Range inputs[3];
+    int n_in = 0;
+    inputs[n_in++] = range_of(x, elems * 2);
+    inputs[n_in++] = range_of(weight, hidden * 2);
+    if (add)
+        inputs[n_in++] = range_of(residual, elems * 2);
     Range outs[3];
+    bool bf16_out[3] = {false, false, false};
     int n_out = 0;
-    outs[n_out++] = rro;
+    if (add) {
+        bf16_out[n_out] = true;
+        outs[n_out++] = range_of(residual_out, elems * 2);
+    }
     if (quant) {
         outs[n_out++] = range_of(out_q, elems);
         outs[n_out++] = range_of(scale, n_rows * 4);
     } else {
+        bf16_out[n_out] = true;
         outs[n_out++] = range_of(out, elems * 2);
     }
-    for (int a = 0; a < n_out; ++a)
-        for (int b = a + 1; b < n_out; ++b)
-            if (outs[a].overlaps(outs[b]))
-                return DRADD_ERR_ALIAS;
-    // An output may coincide exactly with x or residual (each element is read
-    // by the thread that later writes it, before it writes it); any other
-    // overlap with an input is rejected.
-    for (int a = 0; a < n_out; ++a) {
-        const bool bf16_out = a == 0 || !quant;
-        for (int b = 0; b < 3; ++b) {
-            if (!outs[a].overlaps(inputs[b]))
-                continue;
-            if (bf16_out && b < 2 && outs[a].same(inputs[b]))
-                continue;
-            return DRADD_ERR_ALIAS;
-        }
-    }
-    return DRADD_OK;
+    return check_overlaps(inputs, n_in, outs, bf16_out, n_out);
 }
 
 // Fill the automatic fields of *cfg and check the explicit ones.
-dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, const DeviceLimits& L,
+dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const DeviceLimits& L,
                      dradd_launch_cfg* cfg)
 {
     if (n_rows < 0 || hidden <= 0)
@@ -162,14 +176,14 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, const DeviceLim
     // larger than L2, median of interleaved rounds).  Rows of up to 256
     // elements go several to a CTA in registers; longer rows are staged
     // through shared memory, mostly with K = 4 blocks of 8 per thread:
-    //   P      T     K  stages
-    //   512    32    2  4
-    //   1024   64    2  1
-    //   2048   64    4  3
-    //   4096   128   4  1 (bf16, >= 24 rows per SM), else 2
-    //   8192   1024  1  2
-    //   16384  512   4  2
-    //   32768  512   8  1
+    //   P      T     K  stages (residual-add forms)   stages (plain RMSNorm)
+    //   512    32    2  4                             4
+    //   1024   64    2  1                             2
+    //   2048   64    4  3                             2
+    //   4096   128   4  1 (bf16, >= 24 rows/SM) else 2  3 (bf16), 1 (int8)
+    //   8192   1024  1  2                             T = 512, K = 2: 3
+    //   16384  512   4  2                             4
+    //   32768  512   8  1                             2
     const bool auto_variant = cfg->variant == DRADD_VARIANT_AUTO;
     if (auto_variant)
         cfg->variant = hidden > 256 ? DRADD_VARIANT_STAGED : DRADD_VARIANT_ROWS;
@@ -187,19 +201,22 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, const DeviceLim
             auto_stages = 4;
         } else if (P == 1024) {
             T = 64;
-            auto_stages = 1;
+            auto_stages = add ? 1 : 2;
         } else if (P == 2048) {
             T = 64;
-            auto_stages = 3;
+            auto_stages = add ? 3 : 2;
         } else if (P == 4096) {
             T = 128;
-            auto_stages = (!quant && n_rows >= 24 * static_cast<int64_t>(L.sm_count)) ? 1 : 2;
+            if (add)
+                auto_stages = (!quant && n_rows >= 24 * static_cast<int64_t>(L.sm_count)) ? 1 : 2;
+            else
+                auto_stages = quant ? 1 : 3;
         } else if (P == 8192) {
-            T = 1024;
-            auto_stages = 2;
+            T = add ? 1024 : 512;
+            auto_stages = add ? 2 : 3;
         } else {
             T = 512;
-            auto_stages = P == 16384 ? 2 : 1;
+            auto_stages = P == 16384 ? (add ? 2 : 4) : (add ? 1 : 2);
         }
         if (T > blocks)
             T = blocks;
@@ -228,7 +245,7 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, const DeviceLim
     if (ctas_per_sm > L.max_blocks_per_sm)
         ctas_per_sm = L.max_blocks_per_sm;
     if (staged) {
-        const int64_t stage_bytes = 4 * hidden;
+        const int64_t stage_bytes = (add ? 4 : 2) * hidden;
         const int64_t static_smem = static_cast<int64_t>(dradd::staged_static_smem(static_cast<int>(K)));
         const int64_t avail = L.smem_per_block_optin - static_smem - 8 * 8;
         if (cfg->stages == 0) {
@@ -270,12 +287,13 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, const DeviceLim
     return DRADD_OK;
 }
 
-dradd_status run(bool quant, dradd_bf16* out, int8_t* out_q, float* scale, dradd_bf16* residual_out,
-                 const dradd_bf16* x, const dradd_bf16* residual, const dradd_bf16* weight, float eps,
-                 int64_t n_rows, int64_t hidden, cudaStream_t stream, const dradd_launch_cfg* user_cfg)
+dradd_status run(bool quant, bool add, dradd_bf16* out, int8_t* out_q, float* scale,
+                 dradd_bf16* residual_out, const dradd_bf16* x, const dradd_bf16* residual,
+                 const dradd_bf16* weight, float eps, int64_t n_rows, int64_t hidden, cudaStream_t stream,
+                 const dradd_launch_cfg* user_cfg)
 {
     bool noop = false;
-    dradd_status st = validate(quant, out, out_q, scale, residual_out, x, residual, weight, eps, n_rows,
+    dradd_status st = validate(quant, add, out, out_q, scale, residual_out, x, residual, weight, eps, n_rows,
                                hidden, &noop);
     if (st != DRADD_OK || noop)
         return st;
@@ -287,18 +305,18 @@ dradd_status run(bool quant, dradd_bf16* out, int8_t* out_q, float* scale, dradd
     if (user_cfg)
         cfg = *user_cfg;
     const bool auto_grid = cfg.grid_ctas == 0;
-    st = resolve(n_rows, hidden, quant, L, &cfg);
+    st = resolve(n_rows, hidden, quant, add, L, &cfg);
     if (st != DRADD_OK)
         return st;
     const int K = static_cast<int>(next_pow2(hidden) / 8 / cfg.threads_per_row);
     const size_t dyn = cfg.variant == DRADD_VARIANT_STAGED
-                           ? static_cast<size_t>(cfg.stages) * 4 * static_cast<size_t>(hidden) +
+                           ? static_cast<size_t>(cfg.stages) * (add ? 4 : 2) * static_cast<size_t>(hidden) +
                                  8 * static_cast<size_t>(cfg.stages)
                            : 0;
     if (auto_grid && cfg.variant == DRADD_VARIANT_STAGED) {
         // persistent grid: as many CTAs as fit on the device at once
         int per_sm = 0;
-        if (dradd::staged_occupancy(K, quant, cfg.threads_per_row, dyn, &per_sm) != cudaSuccess)
+        if (dradd::staged_occupancy(K, quant, add, cfg.threads_per_row, dyn, &per_sm) != cudaSuccess)
             return DRADD_ERR_CUDA;
         int64_t grid = static_cast<int64_t>(L.sm_count) * (per_sm > 0 ? per_sm : 1);
         if (grid > n_rows)
@@ -324,12 +342,14 @@ dradd_status run(bool quant, dradd_bf16* out, int8_t* out_q, float* scale, dradd
     p.fault_inject = cfg.fault_inject;
     p.wait_limit_ns = cfg.wait_limit_us > 0 ? static_cast<uint64_t>(cfg.wait_limit_us) * 1000ull
                                             : kDefaultWaitLimitNs;
+    if (dradd::device_status_ptr(&p.status) != cudaSuccess)
+        return DRADD_ERR_CUDA;
     cudaError_t e;
     if (cfg.variant == DRADD_VARIANT_STAGED) {
-        e = dradd::launch_staged(p, K, quant, cfg.grid_ctas, cfg.threads_per_row, dyn, cfg.serialize != 0,
-                                 stream);
+        e = dradd::launch_staged(p, K, quant, add, cfg.grid_ctas, cfg.threads_per_row, dyn,
+                                 cfg.serialize != 0, stream);
     } else {
-        e = dradd::launch_rows(p, K, quant, cfg.grid_ctas, cfg.threads_per_row * cfg.rows_per_cta,
+        e = dradd::launch_rows(p, K, quant, add, cfg.grid_ctas, cfg.threads_per_row * cfg.rows_per_cta,
                                cfg.serialize != 0, stream);
     }
     return e == cudaSuccess ? DRADD_OK : DRADD_ERR_CUDA;
@@ -343,7 +363,7 @@ dradd_status add_rmsnorm_fwd(dradd_bf16* out, dradd_bf16* residual_out, const dr
                              const dradd_bf16* residual, const dradd_bf16* weight, float eps,
                              int64_t n_rows, int64_t hidden, cudaStream_t stream)
 {
-    return run(false, out, nullptr, nullptr, residual_out, x, residual, weight, eps, n_rows, hidden,
+    return run(false, true, out, nullptr, nullptr, residual_out, x, residual, weight, eps, n_rows, hidden,
                stream, nullptr);
 }
 
@@ -352,7 +372,7 @@ dradd_status add_rmsnorm_quant_fwd(int8_t* out_q, float* scale, dradd_bf16* resi
                                    const dradd_bf16* weight, float eps, int64_t n_rows,
                                    int64_t hidden, cudaStream_t stream)
 {
-    return run(true, nullptr, out_q, scale, residual_out, x, residual, weight, eps, n_rows, hidden,
+    return run(true, true, nullptr, out_q, scale, residual_out, x, residual, weight, eps, n_rows, hidden,
                stream, nullptr);
 }
 
@@ -364,7 +384,7 @@ dradd_status add_rmsnorm_fwd_with_config(dradd_bf16* out, dradd_bf16* residual_o
 {
     if (!cfg)
         return DRADD_ERR_NULL_PTR;
-    return run(false, out, nullptr, nullptr, residual_out, x, residual, weight, eps, n_rows, hidden,
+    return run(false, true, out, nullptr, nullptr, residual_out, x, residual, weight, eps, n_rows, hidden,
                stream, cfg);
 }
 
@@ -376,15 +396,17 @@ dradd_status add_rmsnorm_quant_fwd_with_config(int8_t* out_q, float* scale, drad
 {
     if (!cfg)
         return DRADD_ERR_NULL_PTR;
-    return run(true, nullptr, out_q, scale, residual_out, x, residual, weight, eps, n_rows, hidden,
+    return run(true, true, nullptr, out_q, scale, residual_out, x, residual, weight, eps, n_rows, hidden,
                stream, cfg);
 }
 
-dradd_status dradd_resolve_config(int64_t n_rows, int64_t hidden, int quant, int sm_count,
+dradd_status dradd_resolve_config(int64_t n_rows, int64_t hidden, int op, int sm_count,
                                   dradd_launch_cfg* cfg)
 {
     if (!cfg)
         return DRADD_ERR_NULL_PTR;
+    if (op < DRADD_OP_ADD_RMSNORM || op > DRADD_OP_RMSNORM_QUANT)
+        return DRADD_ERR_BAD_CONFIG;
     DeviceLimits L;
     if (sm_count > 0) {
         L.sm_count = sm_count;
@@ -393,7 +415,76 @@ dradd_status dradd_resolve_config(int64_t n_rows, int64_t hidden, int quant, int
         if (st != DRADD_OK)
             return st;
     }
-    return resolve(n_rows, hidden, quant != 0, L, cfg);
+    const bool quant = op == DRADD_OP_ADD_RMSNORM_QUANT || op == DRADD_OP_RMSNORM_QUANT;
+    const bool add = op == DRADD_OP_ADD_RMSNORM || op == DRADD_OP_ADD_RMSNORM_QUANT;
+    return resolve(n_rows, hidden, quant, add, L, cfg);
+}
+
+dradd_status rmsnorm_fwd(dradd_bf16* out, const dradd_bf16* x, const dradd_bf16* weight, float eps,
+                         int64_t n_rows, int64_t hidden, cudaStream_t stream)
+{
+    return run(false, false, out, nullptr, nullptr, nullptr, x, nullptr, weight, eps, n_rows, hidden, stream,
+               nullptr);
+}
+
+dradd_status rmsnorm_quant_fwd(int8_t* out_q, float* scale, const dradd_bf16* x, const dradd_bf16* weight,
+                               float eps, int64_t n_rows, int64_t hidden, cudaStream_t stream)
+{
+    return run(true, false, nullptr, out_q, scale, nullptr, x, nullptr, weight, eps, n_rows, hidden, stream,
+               nullptr);
+}
+
+dradd_status rmsnorm_fwd_with_config(dradd_bf16* out, const dradd_bf16* x, const dradd_bf16* weight,
+                                     float eps, int64_t n_rows, int64_t hidden, cudaStream_t stream,
+                                     const dradd_launch_cfg* cfg)
+{
+    if (!cfg)
+        return DRADD_ERR_NULL_PTR;
+    return run(false, false, out, nullptr, nullptr, nullptr, x, nullptr, weight, eps, n_rows, hidden, stream,
+               cfg);
+}
+
+dradd_status rmsnorm_quant_fwd_with_config(int8_t* out_q, float* scale, const dradd_bf16* x,
+                                           const dradd_bf16* weight, float eps, int64_t n_rows,
+                                           int64_t hidden, cudaStream_t stream, const dradd_launch_cfg* cfg)
+{
+    if (!cfg)
+        return DRADD_ERR_NULL_PTR;
+    return run(true, false, nullptr, out_q, scale, nullptr, x, nullptr, weight, eps, n_rows, hidden, stream,
+               cfg);
+}
+
+dradd_status residual_add_fwd(dradd_bf16* residual_out, const dradd_bf16* x, const dradd_bf16* residual,
+                              int64_t n_rows, int64_t hidden, cudaStream_t stream)
+{
+    if (n_rows < 0 || hidden <= 0)
+        return DRADD_ERR_BAD_SHAPE;
+    if (hidden % 8 != 0 || hidden > DRADD_MAX_HIDDEN)
+        return DRADD_ERR_UNSUPPORTED_HIDDEN;
+    if (n_rows > (INT64_MAX / 4) / hidden)
+        return DRADD_ERR_BAD_SHAPE;
+    if (n_rows == 0)
+        return DRADD_OK;
+    if (!residual_out || !x || !residual)
+        return DRADD_ERR_NULL_PTR;
+    if (!aligned(residual_out, 16) || !aligned(x, 16) || !aligned(residual, 16))
+        return DRADD_ERR_MISALIGNED;
+    const int64_t elems = n_rows * hidden;
+    // inputs in the order check_overlaps expects: x, (weight slot, empty), residual
+    const Range inputs[3] = {range_of(x, elems * 2), Range{}, range_of(residual, elems * 2)};
+    const Range outs[1] = {range_of(residual_out, elems * 2)};
+    const bool bf16_out[1] = {true};
+    dradd_status st = check_overlaps(inputs, 3, outs, bf16_out, 1);
+    if (st != DRADD_OK)
+        return st;
+    DeviceLimits L;
+    st = query_limits(&L);
+    if (st != DRADD_OK)
+        return st;
+    return dradd::launch_residual_add(residual_out, x, residual, elems / 8, L.sm_count, false, stream) ==
+                   cudaSuccess
+               ? DRADD_OK
+               : DRADD_ERR_CUDA;
 }
 
 dradd_status dradd_device_status(cudaStream_t stream, int clear)

@@ -160,14 +160,14 @@ __device__ __forceinline__ float inv_rms(float sum_sq, int hidden, float inv_hid
 // RN(y / scale) is the correctly rounded fp32 quotient; scale == 0 gives 0.
 //
 // Fast path, for a normal finite scale (every row with amax >= 127 * 2^-126):
-// with c = RN(1 / scale) and q0 = RN(y * c), both rounding errors are
-// relative and at most 2^-24, and |y / scale| <= amax / RN(amax / 127)
-// <= 127 / (1 - 2^-24), so |q0 - y/scale| <= 2^-23 * 127.00001 and
-// |RN(y/scale) - y/scale| <= 2^-24 * 127.00001: q0 and RN(y / scale) are
-// less than 2.3e-5 < 2^-15 apart.  When q0 is at least 2^-15 away from the
-// nearest half-integer, no half-integer lies between the two and both round
-// to the same integer, rint(q0).  Otherwise (for about 2^-14 of all values,
-// so for about one 8-value block in 1,000) the block's quotients are computed
+// with c = RN(1 / scale) and z = y * c exactly, the relative error of c is
+// at most 2^-24 and |y / scale| <= amax / RN(amax / 127) <= 127 / (1 - 2^-24),
+// so |z - y/scale| <= 2^-24 * 127.00001; also |RN(y/scale) - y/scale| <=
+// 2^-24 * 127.00001: z and RN(y / scale) are less than 1.6e-5 apart.  When z
+// is at least 2^-15 - 2^-25 away from the nearest half-integer, no
+// half-integer lies between the two and both round to the same integer,
+// rint(z) (see quantize8).  Otherwise (for about 2^-14 of all values, so for
+// about one 8-value block in 1,000) the block's quotients are computed
 // exactly with a correctly rounded division.
 struct QuantScale {
     float scale;
@@ -196,43 +196,45 @@ __device__ __forceinline__ int32_t quantize_exact(float y, float scale)
     return q;
 }
 
-// Low bytes of four ints packed into one word, first in the lowest byte.
-__device__ __forceinline__ uint32_t pack4_low_bytes(int32_t a, int32_t b, int32_t c, int32_t d)
+// Low bytes of four words packed into one word, first in the lowest byte.
+__device__ __forceinline__ uint32_t pack4_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
-    const uint32_t ab = __byte_perm(static_cast<uint32_t>(a), static_cast<uint32_t>(b), 0x0040);
-    const uint32_t cd = __byte_perm(static_cast<uint32_t>(c), static_cast<uint32_t>(d), 0x0040);
+    const uint32_t ab = __byte_perm(a, b, 0x0040);
+    const uint32_t cd = __byte_perm(c, d, 0x0040);
     return __byte_perm(ab, cd, 0x5410);
 }
 
-// Eight int8 codes for eight consecutive y values.  Fast path: q0 = y * c;
-// adding 1.5 * 2^23 rounds |q0| < 2^22 to an integer, ties to even, held in
-// the low mantissa bits, so m - 1.5 * 2^23 is rint(q0) exactly and the bit
-// pattern of m minus that of 1.5 * 2^23 is the same integer.  |q0| <= 127.0001
-// here, so no clamp is needed.  If any of the eight lies within 2^-15 of a
-// half-integer (or the scale is not a normal number) the block is redone with
-// quantize_exact.
+// Eight int8 codes for eight consecutive y values.  Fast path: with z the
+// exact product y * c, m = fma(y, c, 1.5 * 2^23) rounds z (|z| < 2^22) to an
+// integer, ties to even, held in m's low mantissa bits: t = m - 1.5 * 2^23
+// is rint(z) exactly, and the low byte of m's bit pattern is the low byte of
+// that integer (the constant's own low byte is zero), i.e. the int8 code.
+// d = fma(y, c, -t) is z - t rounded once (error below 2^-25 near a half),
+// and |z - RN(y / scale)| <= 2^-24 * 127.00001 * 2 < 1.6e-5; so when
+// |d| <= 0.5 - 2^-15, no half-integer lies between z and RN(y / scale) and
+// rint(z) = rint(RN(y / scale)).  |z| <= 127.0001 here, so no clamp is
+// needed.  If any of the eight is nearer a half-integer (or the scale is not
+// a normal number) the block is redone with quantize_exact.
 __device__ __forceinline__ uint2 quantize8(const float (&y)[8], const QuantScale& s)
 {
     constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-    constexpr int32_t kRoundBits = 0x4B400000;
-    int32_t q[8];
+    uint32_t bits[8];
     bool near_tie = !s.fast;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-        const float q0 = __fmul_rn(y[e], s.recip);
-        const float m = __fadd_rn(q0, kRound);
+        const float m = __fmaf_rn(y[e], s.recip, kRound);
         const float t = __fsub_rn(m, kRound);
-        near_tie |= !(fabsf(__fsub_rn(q0, t)) <= 0.5f - 0x1p-15f);
-        q[e] = __float_as_int(m) - kRoundBits;
+        near_tie |= !(fabsf(__fmaf_rn(y[e], s.recip, -t)) <= 0.5f - 0x1p-15f);
+        bits[e] = __float_as_uint(m);
     }
     if (near_tie) {
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-            q[e] = quantize_exact(y[e], s.scale);
+            bits[e] = static_cast<uint32_t>(quantize_exact(y[e], s.scale));
     }
     uint2 u;
-    u.x = pack4_low_bytes(q[0], q[1], q[2], q[3]);
-    u.y = pack4_low_bytes(q[4], q[5], q[6], q[7]);
+    u.x = pack4_low_bytes(bits[0], bits[1], bits[2], bits[3]);
+    u.y = pack4_low_bytes(bits[4], bits[5], bits[6], bits[7]);
     return u;
 }
 

@@ -25,7 +25,12 @@ struct Params {
     int stages;               // staged kernel only
     int fault_inject;         // staged kernel only
     uint64_t wait_limit_ns;   // staged kernel only
+    unsigned* status;         // device status word (set on an expired wait)
 };
+
+constexpr unsigned kDeviceStatusTimeout = 1u;
+
+using KernelFn = void (*)(Params);
 
 // Largest CTA for K blocks per thread: the register budget of the bigger
 // tiles (K * 8 accumulators per thread) needs the smaller CTA.
@@ -45,13 +50,20 @@ constexpr int staged_min_blocks(int T, int K)
     return b < 1 ? 1 : b;
 }
 
-cudaError_t launch_rows(const Params& p, int K, bool quant, int grid, int threads, bool serialize,
+// add = true: residual-add + RMSNorm (reads x and residual, writes
+// residual_out); false: plain RMSNorm of x.
+cudaError_t launch_rows(const Params& p, int K, bool quant, bool add, int grid, int threads, bool serialize,
                         cudaStream_t stream);
-cudaError_t launch_staged(const Params& p, int K, bool quant, int grid, int threads, size_t dyn_smem,
-                          bool serialize, cudaStream_t stream);
+cudaError_t launch_staged(const Params& p, int K, bool quant, bool add, int grid, int threads,
+                          size_t dyn_smem, bool serialize, cudaStream_t stream);
+cudaError_t staged_occupancy(int K, bool quant, bool add, int threads, size_t dyn_smem, int* blocks_per_sm);
 size_t staged_static_smem(int K);
-cudaError_t staged_occupancy(int K, bool quant, int threads, size_t dyn_smem, int* blocks_per_sm);
+KernelFn staged_fn_add(int T, int K, bool quant);
+KernelFn staged_fn_norm(int T, int K, bool quant);
+cudaError_t launch_residual_add(uint16_t* residual_out, const uint16_t* x, const uint16_t* residual,
+                                int64_t n_vec, int sm_count, bool serialize, cudaStream_t stream);
 cudaError_t launch_convert(uint16_t* out, uint64_t first, int64_t count, int method, cudaStream_t stream);
 cudaError_t read_device_status(unsigned* status, bool clear, cudaStream_t stream);
+cudaError_t device_status_ptr(unsigned** ptr);
 
 }  // namespace dradd

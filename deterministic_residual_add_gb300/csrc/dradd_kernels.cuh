@@ -1,0 +1,396 @@
+// dradd_kernels.cuh -- the kernel templates for the fused residual-add +
+// RMSNorm forward (bf16 out and per-row int8 out) and for plain RMSNorm, on
+// sm_103a.  Instantiated by the dradd_*.cu translation units.
+//
+// The operation (ROCm/aiter issue #5151, "Steps to Reproduce", reference()):
+//   acc = fp32(x) + fp32(residual); residual_out = bf16_rne(acc);
+//   out = bf16_rne((acc * (1 / sqrt(S / hidden + eps))) * fp32(weight)),
+// where S is the canonical pairwise sum of acc^2 over the row zero-padded to
+// P = next power of two >= hidden.  With ADD = false the residual is absent:
+// acc = fp32(x) (exact) and there is no residual_out (plain RMSNorm).
+//
+// Work layout shared by both kernels.  A row is split into 8-element blocks
+// (one 16-byte vector each), P / 8 of them counting the padding.  The T
+// threads of a row own K = P / (8 T) blocks each, thread t holding blocks
+// t, t + T, ..., t + (K - 1) T, so consecutive threads touch consecutive
+// 16-byte vectors (fully coalesced for every K).  The canonical tree then
+// factors exactly:
+//   levels 1-3   inside each 8-block, in registers            (fold8_squares)
+//   next log2 T  across the T threads for each j: lanes by xor butterfly,
+//                then warps through shared memory and a second butterfly
+//   top log2 K   across the K subtrees a thread holds          (fold_k)
+// Each stage adds adjacent aligned blocks, lower + upper, so the sum equals
+// the tree over the padded row whatever T, K, rows per CTA or grid are; the
+// padding blocks contribute +0 and adding +0 to a sum of squares is exact.
+//
+// Kernels:
+//   rows_kernel    rows are loaded straight into registers with streaming
+//                  16-byte loads; a CTA handles rows_per_cta rows side by side
+//                  and loops over the rows with a grid stride.
+//   staged_kernel  persistent CTAs stage whole rows of x (and residual) into
+//                  shared memory with 1-D bulk asynchronous copies (TMA
+//                  engine), `stages` rows ahead of the compute; the copy for
+//                  row i + stages is issued as soon as row i has been read.
+//                  Every wait on a copy is bounded: past the limit the CTA
+//                  records a timeout in the device status word, waits (again
+//                  bounded) for its other copies and returns.
+#pragma once
+
+#include "dradd_device.cuh"
+#include "dradd_internal.h"
+
+namespace dradd {
+
+// ------------------------------------------------------------------ helpers
+// Sum of one row across its T threads for each of the K subtrees: lanes
+// first, then (T > 32) each warp's lane 0 publishes its sums in `red` (W * K
+// floats for this row); the caller puts a CTA-wide barrier between this and
+// gather_warps.
+template <int K>
+__device__ __forceinline__ void lanes_then_publish(float (&part)[K], int T, int lane, int warp_in_row,
+                                                   float* red)
+{
+    const int width = T < 32 ? T : 32;
+#pragma unroll
+    for (int j = 0; j < K; ++j)
+        part[j] = butterfly_sum(part[j], width);
+    if (T > 32 && lane == 0) {
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+            red[warp_in_row * K + j] = part[j];
+    }
+}
+
+template <int K>
+__device__ __forceinline__ void gather_warps(float (&part)[K], int T, int lane, const float* red)
+{
+    if (T <= 32)
+        return;
+    const int W = T >> 5;
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        const float v = red[(lane & (W - 1)) * K + j];
+        part[j] = butterfly_sum(v, W);
+    }
+}
+
+// Row epilogue after inv is known: bf16 store, or the int8 quant (which
+// needs its own CTA-wide max).  Called by every thread of the CTA.
+template <int K, bool QUANT>
+__device__ __forceinline__ void finish_row(const Params& p, float (&acc)[K][8], const uint4 (&w)[K],
+                                           float inv, int64_t row, bool active, int t, int T, int lane,
+                                           int warp_in_row, int nblocks, float* red_max)
+{
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        float wf[8];
+        unpack8(w[j], wf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            acc[j][e] = __fmul_rn(__fmul_rn(acc[j][e], inv), wf[e]);
+    }
+    if constexpr (!QUANT) {
+        if (active) {
+            uint4* orow = reinterpret_cast<uint4*>(p.out + row * p.hidden);
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const int b = t + j * T;
+                if (b < nblocks)
+                    st_stream(orow + b, pack8_rne(acc[j]));
+            }
+        }
+    } else {
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                m = fmaxf(m, fabsf(acc[j][e]));
+        }
+        m = butterfly_max(m, T < 32 ? T : 32);
+        if (T > 32) {
+            if (lane == 0)
+                red_max[warp_in_row] = m;
+            __syncthreads();
+            m = butterfly_max(red_max[lane & ((T >> 5) - 1)], T >> 5);
+        }
+        const float scale = __fdiv_rn(m, 127.0f);
+        const QuantScale qs = make_quant_scale(scale);
+        if (active) {
+            if (t == 0)
+                p.scale[row] = scale;
+            uint2* qrow = reinterpret_cast<uint2*>(p.out_q + row * p.hidden);
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const int b = t + j * T;
+                if (b < nblocks)
+                    st_stream(qrow + b, quantize8(acc[j], qs));
+            }
+        }
+    }
+}
+
+// The weight blocks a thread needs, kept as packed bf16 (4 registers per
+// 8 weights) for the whole life of the CTA.
+template <int K>
+__device__ __forceinline__ void load_weights(const Params& p, uint4 (&w)[K], int t, int T, int nblocks)
+{
+    const uint4* wrow = reinterpret_cast<const uint4*>(p.weight);
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        const int b = t + j * T;
+        w[j] = b < nblocks ? __ldg(wrow + b) : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// acc for K blocks from already loaded vectors (x + residual with ADD, x
+// alone otherwise); with ADD residual_out is stored in the same pass.
+// Returns the per-block partial sums of squares.
+template <int K, bool ADD>
+__device__ __forceinline__ void row_accumulate(const Params& p, const uint4 (&xv)[K], const uint4 (&rv)[K],
+                                               float (&acc)[K][8], float (&part)[K], int64_t row,
+                                               bool active, int t, int T, int nblocks)
+{
+    uint4* rorow = ADD ? reinterpret_cast<uint4*>(p.residual_out + row * p.hidden) : nullptr;
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        const int b = t + j * T;
+        if (active && b < nblocks) {
+            if constexpr (ADD) {
+                add8(xv[j], rv[j], acc[j]);
+                st_stream(rorow + b, pack8_rne(acc[j]));
+            } else {
+                unpack8(xv[j], acc[j]);
+            }
+            part[j] = fold8_squares(acc[j]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[j][e] = 0.0f;
+            part[j] = 0.0f;
+        }
+    }
+}
+
+__device__ __forceinline__ void record_timeout(const Params& p)
+{
+    atomicOr(p.status, kDeviceStatusTimeout);
+}
+
+// ---------------------------------------------------------------- rows_kernel
+template <int K, bool QUANT, bool ADD>
+__global__ void __launch_bounds__(max_threads_for(K)) rows_kernel(const Params p)
+{
+    __shared__ float s_sum[2][32 * K];
+    __shared__ float s_max[2][32];
+    const int T = p.threads_per_row;
+    const int tid = threadIdx.x;
+    const int r_local = tid / T;
+    const int t = tid - r_local * T;
+    const int lane = tid & 31;
+    const int warp_in_row = t >> 5;
+    const int warps_per_row = T > 32 ? T >> 5 : 1;
+    const int nblocks = p.hidden >> 3;
+
+    wait_prior_grids();
+    allow_next_grid();
+    uint4 w[K];
+    load_weights<K>(p, w, t, T, nblocks);
+
+    const int64_t rows_per_step = static_cast<int64_t>(gridDim.x) * p.rows_per_cta;
+    int buf = 0;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * p.rows_per_cta; base < p.n_rows;
+         base += rows_per_step) {
+        const int64_t row = base + r_local;
+        const bool active = row < p.n_rows;
+        uint4 xv[K], rv[K];
+        if (active) {
+            const uint4* xrow = reinterpret_cast<const uint4*>(p.x + row * p.hidden);
+            const uint4* rrow = ADD ? reinterpret_cast<const uint4*>(p.residual + row * p.hidden) : nullptr;
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const int b = t + j * T;
+                if (b < nblocks) {
+                    xv[j] = ld_stream(xrow + b);
+                    if constexpr (ADD)
+                        rv[j] = ld_stream(rrow + b);
+                }
+            }
+        }
+        float acc[K][8], part[K];
+        row_accumulate<K, ADD>(p, xv, rv, acc, part, row, active, t, T, nblocks);
+
+        float* red = &s_sum[buf][r_local * warps_per_row * K];
+        lanes_then_publish<K>(part, T, lane, warp_in_row, red);
+        if (T > 32)
+            __syncthreads();
+        gather_warps<K>(part, T, lane, red);
+        const float inv = inv_rms(fold_k<K>(part), p.hidden, p.inv_hidden, p.eps);
+        finish_row<K, QUANT>(p, acc, w, inv, row, active, t, T, lane, warp_in_row, nblocks,
+                             &s_max[buf][r_local * warps_per_row]);
+        buf ^= 1;
+    }
+}
+
+// -------------------------------------------------------------- staged_kernel
+// T (threads per row = threads per CTA) is a compile-time constant so that
+// every (T, K) pair gets its own register budget (staged_min_blocks) and the
+// reduction widths fold away.  A stage holds one row of x, then (with ADD)
+// one row of residual.
+template <int T, int K, bool QUANT, bool ADD>
+__global__ void __launch_bounds__(T, staged_min_blocks(T, K)) staged_kernel(const Params p)
+{
+    static_assert(T >= 32 && T <= 1024 && (T & (T - 1)) == 0, "T: a power of two, 32..1024");
+    extern __shared__ __align__(128) unsigned char stage_mem[];
+    __shared__ float s_sum[2][32 * K];
+    __shared__ float s_max[2][32];
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp_in_row = tid >> 5;
+    const int nblocks = p.hidden >> 3;
+    const int stages = p.stages;
+    const uint32_t row_bytes = static_cast<uint32_t>(p.hidden) * 2u;
+    const uint32_t stage_bytes = (ADD ? 2u : 1u) * row_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stage_mem + static_cast<size_t>(stages) * stage_bytes);
+    const int64_t stride = gridDim.x;
+
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s)
+            mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    wait_prior_grids();
+    allow_next_grid();
+
+    const uint64_t policy = l2_policy_evict_first();
+    auto issue = [&](int s, int64_t row) {
+        unsigned char* dst = stage_mem + static_cast<size_t>(s) * stage_bytes;
+        mbar_arrive_expect_tx(&bars[s], stage_bytes);
+        bulk_copy_g2s(dst, p.x + row * p.hidden, row_bytes, &bars[s], policy);
+        if constexpr (ADD)
+            bulk_copy_g2s(dst + row_bytes, p.residual + row * p.hidden, row_bytes, &bars[s], policy);
+    };
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) {
+            const int64_t row = blockIdx.x + s * stride;
+            if (row >= p.n_rows)
+                break;
+            if (p.fault_inject && s == 0)
+                continue;  // test hook: this copy never comes, so its wait expires
+            issue(s, row);
+        }
+    }
+
+    uint4 w[K];
+    load_weights<K>(p, w, tid, T, nblocks);
+
+    int buf = 0;
+    // Iteration i of this CTA uses stage s = i mod stages and waits for phase
+    // parity floor(i / stages) mod 2; both are kept incrementally.
+    int64_t i = 0;
+    int s = 0;
+    uint32_t parity = 0;
+    for (int64_t row = blockIdx.x; row < p.n_rows; row += stride, ++i) {
+        // A thread whose wait gives up goes on with whatever the stage holds
+        // (outputs are unspecified after a timeout); the CTA learns of it at
+        // the barrier below and stops there, before refilling any stage.
+        const bool ok = mbar_wait_bounded(&bars[s], parity, p.wait_limit_ns);
+        const unsigned char* sbase = stage_mem + static_cast<size_t>(s) * stage_bytes;
+        const uint4* xs = reinterpret_cast<const uint4*>(sbase);
+        const uint4* rs = reinterpret_cast<const uint4*>(sbase + row_bytes);
+        uint4 xv[K], rv[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const int b = tid + j * T;
+            if (b < nblocks) {
+                xv[j] = xs[b];
+                if constexpr (ADD)
+                    rv[j] = rs[b];
+            }
+        }
+        float acc[K][8], part[K];
+        row_accumulate<K, ADD>(p, xv, rv, acc, part, row, true, tid, T, nblocks);
+
+        float* red = &s_sum[buf][0];
+        lanes_then_publish<K>(part, T, lane, warp_in_row, red);
+        // Every thread has read stage s (so it can be refilled) and published
+        // its warp's partial sums; any expired wait ends the CTA here.
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                record_timeout(p);
+                // Copies already issued must land before shared memory is released.
+                int s2 = s;
+                uint32_t parity2 = parity;
+                for (int64_t i2 = i; i2 < i + stages; ++i2) {
+                    if (blockIdx.x + i2 * stride >= p.n_rows)
+                        break;
+                    if (!(p.fault_inject && i2 == 0))
+                        mbar_wait_bounded(&bars[s2], parity2, p.wait_limit_ns);
+                    if (++s2 == stages) {
+                        s2 = 0;
+                        parity2 ^= 1u;
+                    }
+                }
+            }
+            return;
+        }
+        if (tid == 0) {
+            const int64_t next = row + static_cast<int64_t>(stages) * stride;
+            if (next < p.n_rows) {
+                fence_proxy_async_smem();
+                issue(s, next);
+            }
+        }
+        gather_warps<K>(part, T, lane, red);
+        const float inv = inv_rms(fold_k<K>(part), p.hidden, p.inv_hidden, p.eps);
+        finish_row<K, QUANT>(p, acc, w, inv, row, true, tid, T, lane, warp_in_row, nblocks,
+                             &s_max[buf][0]);
+        buf ^= 1;
+        if (++s == stages) {
+            s = 0;
+            parity ^= 1u;
+        }
+    }
+}
+
+// ------------------------------------------------------- staged kernel table
+// Staged kernels exist for T = 32..1024 and K in {1, 2, 4, 8} with
+// T <= max_threads_for(K).
+
+template <int T, int K, bool ADD>
+KernelFn staged_pick(bool quant)
+{
+    if constexpr (T <= max_threads_for(K))
+        return quant ? staged_kernel<T, K, true, ADD> : staged_kernel<T, K, false, ADD>;
+    else
+        return nullptr;
+}
+
+template <int T, bool ADD>
+KernelFn staged_by_k(int K, bool quant)
+{
+    switch (K) {
+    case 1: return staged_pick<T, 1, ADD>(quant);
+    case 2: return staged_pick<T, 2, ADD>(quant);
+    case 4: return staged_pick<T, 4, ADD>(quant);
+    case 8: return staged_pick<T, 8, ADD>(quant);
+    default: return nullptr;
+    }
+}
+
+template <bool ADD>
+KernelFn staged_table(int T, int K, bool quant)
+{
+    switch (T) {
+    case 32: return staged_by_k<32, ADD>(K, quant);
+    case 64: return staged_by_k<64, ADD>(K, quant);
+    case 128: return staged_by_k<128, ADD>(K, quant);
+    case 256: return staged_by_k<256, ADD>(K, quant);
+    case 512: return staged_by_k<512, ADD>(K, quant);
+    case 1024: return staged_by_k<1024, ADD>(K, quant);
+    default: return nullptr;
+    }
+}
+
+}  // namespace dradd

@@ -183,12 +183,72 @@ dradd_status add_rmsnorm_quant_fwd_with_config(int8_t* out_q, float* scale,
 
 /*
  * dradd_resolve_config -- fill the automatic choices of *cfg for a call of
- * the given shape, as the entry points would, and validate the explicit
- * ones.  grid_ctas is filled from `sm_count` (pass 0 to query the current
- * device).  Does no GPU work when sm_count > 0.
+ * the given shape and operation, as the entry points would, and validate
+ * the explicit ones.  `op` is one of DRADD_OP_* (0 and 1 are the bf16 and
+ * int8 residual-add forms, 2 and 3 plain RMSNorm).  grid_ctas is filled from
+ * `sm_count` (pass 0 to query the current device); for the staged variant
+ * the entry points size the grid with the CUDA occupancy calculator instead.
+ * Does no GPU work when sm_count > 0.
  */
-dradd_status dradd_resolve_config(int64_t n_rows, int64_t hidden, int quant, int sm_count,
+enum {
+    DRADD_OP_ADD_RMSNORM = 0,
+    DRADD_OP_ADD_RMSNORM_QUANT = 1,
+    DRADD_OP_RMSNORM = 2,
+    DRADD_OP_RMSNORM_QUANT = 3
+};
+
+dradd_status dradd_resolve_config(int64_t n_rows, int64_t hidden, int op, int sm_count,
                                   dradd_launch_cfg* cfg);
+
+/*
+ * rmsnorm_fwd -- plain RMSNorm forward, the residual-free half of the page's
+ * reference() (ROCm/aiter issue #5151, "Steps to Reproduce"): acc = fp32(x)
+ * (exact), then exactly the normalisation of add_rmsnorm_fwd:
+ *   out = bf16_rne((acc * (1 / sqrt(S / hidden + eps))) * fp32(weight))
+ * with the same pairwise tree, the same rounding steps and the same launch
+ * invariance.  There is no residual and no residual_out.
+ *
+ *   out     [n_rows x hidden] bf16, written (may be exactly x)
+ *   x       [n_rows x hidden] bf16, read
+ *   weight  [hidden] bf16, read
+ * Conventions, errors and aliasing as for add_rmsnorm_fwd.
+ */
+dradd_status rmsnorm_fwd(dradd_bf16* out, const dradd_bf16* x, const dradd_bf16* weight, float eps,
+                         int64_t n_rows, int64_t hidden, cudaStream_t stream);
+
+/*
+ * rmsnorm_quant_fwd -- plain RMSNorm with the per-row symmetric int8 output
+ * of add_rmsnorm_quant_fwd (same amax, scale and rounding rules).
+ *   out_q [n_rows x hidden] int8, scale [n_rows] fp32, written.
+ */
+dradd_status rmsnorm_quant_fwd(int8_t* out_q, float* scale, const dradd_bf16* x,
+                               const dradd_bf16* weight, float eps, int64_t n_rows, int64_t hidden,
+                               cudaStream_t stream);
+
+dradd_status rmsnorm_fwd_with_config(dradd_bf16* out, const dradd_bf16* x, const dradd_bf16* weight,
+                                     float eps, int64_t n_rows, int64_t hidden, cudaStream_t stream,
+                                     const dradd_launch_cfg* cfg);
+
+dradd_status rmsnorm_quant_fwd_with_config(int8_t* out_q, float* scale, const dradd_bf16* x,
+                                           const dradd_bf16* weight, float eps, int64_t n_rows,
+                                           int64_t hidden, cudaStream_t stream,
+                                           const dradd_launch_cfg* cfg);
+
+/*
+ * residual_add_fwd -- the residual update alone, the other half of the
+ * page's reference(): residual_out = bf16_rne(fp32(x) + fp32(residual)),
+ * element by element, bit-identical to add_rmsnorm_fwd's residual_out (the
+ * store the page is about: "Problem Description", "Cost of fixing").
+ *
+ *   residual_out  [n_rows x hidden] bf16, written (may be exactly x or
+ *                 residual)
+ *   x, residual   [n_rows x hidden] bf16, read
+ * Shape, alignment and aliasing rules as for add_rmsnorm_fwd (no weight,
+ * no eps).
+ */
+dradd_status residual_add_fwd(dradd_bf16* residual_out, const dradd_bf16* x,
+                              const dradd_bf16* residual, int64_t n_rows, int64_t hidden,
+                              cudaStream_t stream);
 
 /*
  * dradd_device_status -- synchronise `stream`, then return DRADD_OK or the

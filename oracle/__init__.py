@@ -119,6 +119,13 @@ class Oracle:
         L.oracle_add_rmsnorm_quant_fwd.argtypes = [
             _i8p, _f32p, _u16p, _u16p, _u16p, _u16p, ctypes.c_float, _i64, _i64, ctypes.c_int,
             _f32p, _f32p]
+        L.oracle_rmsnorm_fwd.restype = ctypes.c_int
+        L.oracle_rmsnorm_fwd.argtypes = [_u16p, _u16p, _u16p, ctypes.c_float, _i64, _i64, ctypes.c_int,
+                                         _f32p, _f32p]
+        L.oracle_rmsnorm_quant_fwd.restype = ctypes.c_int
+        L.oracle_rmsnorm_quant_fwd.argtypes = [_i8p, _f32p, _u16p, _u16p, ctypes.c_float, _i64, _i64]
+        L.oracle_residual_add_fwd.restype = ctypes.c_int
+        L.oracle_residual_add_fwd.argtypes = [_u16p, _u16p, _u16p, _i64, ctypes.c_int]
         L.oracle_abi_version.restype = ctypes.c_int
 
     # ---- conversions -------------------------------------------------
@@ -214,6 +221,64 @@ class Oracle:
         if return_terms:
             return q, scale, ro, ss, inv
         return q, scale, ro
+
+
+    def rmsnorm_fwd(self, x, weight, eps: float, store_mode: str = "rne", threads: int = 1,
+                    return_terms: bool = False):
+        """Plain RMSNorm: out (uint16 array shaped like x)."""
+        x, weight = _as_u16(x), _as_u16(weight)
+        hidden = x.shape[-1]
+        n_rows = x.size // hidden if hidden else 0
+        assert weight.size == hidden
+        out = np.empty_like(x)
+        ss = np.empty(n_rows, dtype=np.float32)
+        inv = np.empty(n_rows, dtype=np.float32)
+        x2, o2 = x.reshape(n_rows, hidden), out.reshape(n_rows, hidden)
+        mode = STORE_MODES[store_mode]
+
+        def run(lo: int, hi: int) -> int:
+            if hi <= lo:
+                return 0
+            return self._L.oracle_rmsnorm_fwd(
+                _ptr(o2[lo:hi], _u16p), _ptr(x2[lo:hi], _u16p), _ptr(weight, _u16p), ctypes.c_float(eps),
+                hi - lo, hidden, mode, _ptr(ss[lo:hi], _f32p), _ptr(inv[lo:hi], _f32p))
+
+        for rc in _split_rows(run, n_rows, threads):
+            if rc != 0:
+                raise RuntimeError(f"oracle_rmsnorm_fwd failed with {rc}")
+        return (out, ss, inv) if return_terms else out
+
+    def rmsnorm_quant_fwd(self, x, weight, eps: float, threads: int = 1):
+        """Plain RMSNorm, int8 out: (out_q, scale)."""
+        x, weight = _as_u16(x), _as_u16(weight)
+        hidden = x.shape[-1]
+        n_rows = x.size // hidden if hidden else 0
+        q = np.empty(x.shape, dtype=np.int8)
+        scale = np.empty(n_rows, dtype=np.float32)
+        x2, q2 = x.reshape(n_rows, hidden), q.reshape(n_rows, hidden)
+
+        def run(lo: int, hi: int) -> int:
+            if hi <= lo:
+                return 0
+            return self._L.oracle_rmsnorm_quant_fwd(
+                _ptr(q2[lo:hi], _i8p), _ptr(scale[lo:hi], _f32p), _ptr(x2[lo:hi], _u16p),
+                _ptr(weight, _u16p), ctypes.c_float(eps), hi - lo, hidden)
+
+        for rc in _split_rows(run, n_rows, threads):
+            if rc != 0:
+                raise RuntimeError(f"oracle_rmsnorm_quant_fwd failed with {rc}")
+        return q, scale
+
+    def residual_add_fwd(self, x, residual, store_mode: str = "rne"):
+        """The residual update alone: residual_out (uint16, shaped like x)."""
+        x, residual = _as_u16(x), _as_u16(residual)
+        assert residual.shape == x.shape
+        ro = np.empty_like(x)
+        rc = self._L.oracle_residual_add_fwd(_ptr(ro, _u16p), _ptr(x, _u16p), _ptr(residual, _u16p),
+                                             x.size, STORE_MODES[store_mode])
+        if rc != 0:
+            raise RuntimeError(f"oracle_residual_add_fwd failed with {rc}")
+        return ro
 
 
 def _split_rows(run, n_rows: int, threads: int):

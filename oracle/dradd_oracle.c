@@ -1,6 +1,7 @@
 /*
  * dradd_oracle.c -- plain, slow, single-threaded CPU oracle for the fused
- * residual-add + RMSNorm forward and its int8-quant variant.
+ * residual-add + RMSNorm forward and its int8-quant variant, and for its two
+ * halves: plain RMSNorm (no residual) and the residual update alone.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
  * calls this file: only tests, the smoke check and the bench's CPU-baseline
@@ -182,7 +183,8 @@ float oracle_pairwise_sum(const float* v, int64_t n)
 
 /* One row of the method.  acc and sq are caller scratch of length hidden and
  * next_pow2(hidden) (zero-filled past hidden).  y receives the fp32 value
- * before the store. */
+ * before the store.  With residual == NULL (plain RMSNorm) acc is x alone and
+ * residual_out is not written. */
 static void add_rmsnorm_row(float* y, uint16_t* residual_out, float* acc, float* sq,
                             const uint16_t* x, const uint16_t* residual,
                             const uint16_t* weight, float eps, int64_t hidden,
@@ -190,8 +192,12 @@ static void add_rmsnorm_row(float* y, uint16_t* residual_out, float* acc, float*
                             float* sum_sq_out, float* inv_rms_out)
 {
     for (int64_t i = 0; i < hidden; ++i) {
-        acc[i] = oracle_bf16_to_f32(x[i]) + oracle_bf16_to_f32(residual[i]);
-        residual_out[i] = store_bf16(acc[i], store_mode);
+        if (residual) {
+            acc[i] = oracle_bf16_to_f32(x[i]) + oracle_bf16_to_f32(residual[i]);
+            residual_out[i] = store_bf16(acc[i], store_mode);
+        } else {
+            acc[i] = oracle_bf16_to_f32(x[i]);
+        }
         sq[i] = acc[i] * acc[i];
     }
     float sum_sq = pairwise_pow2(sq, padded);
@@ -259,6 +265,27 @@ static int32_t round_half_even_to_int(float v)
     return (int32_t)rintf(v);
 }
 
+/* Per-row symmetric int8 codes of the fp32 row y: amax = max |y|,
+ * scale = amax / 127, q = clamp(rint(y / scale), -127, 127); scale == 0
+ * gives q = 0. */
+static void quantize_row(int8_t* q_out, float* scale_out, const float* y, int64_t hidden)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < hidden; ++i)
+        amax = fmaxf(amax, fabsf(y[i]));
+    float s = amax / 127.0f;
+    *scale_out = s;
+    for (int64_t i = 0; i < hidden; ++i) {
+        int32_t q = 0;
+        if (s != 0.0f) {
+            q = round_half_even_to_int(y[i] / s);
+            if (q > 127) q = 127;
+            if (q < -127) q = -127;
+        }
+        q_out[i] = (int8_t)q;
+    }
+}
+
 /* residual-add + RMSNorm forward with per-row symmetric int8 out.
  * out_q: n_rows x hidden int8; scale: n_rows fp32 (q * scale ~ y). */
 int oracle_add_rmsnorm_quant_fwd(int8_t* out_q, float* scale, uint16_t* residual_out,
@@ -287,22 +314,83 @@ int oracle_add_rmsnorm_quant_fwd(int8_t* out_q, float* scale, uint16_t* residual
                         weight, eps, hidden, padded, store_mode,
                         row_sum_sq ? row_sum_sq + r : NULL,
                         row_inv_rms ? row_inv_rms + r : NULL);
-        float amax = 0.0f;
-        for (int64_t i = 0; i < hidden; ++i)
-            amax = fmaxf(amax, fabsf(y[i]));
-        float s = amax / 127.0f;
-        scale[r] = s;
-        for (int64_t i = 0; i < hidden; ++i) {
-            int32_t q = 0;
-            if (s != 0.0f) {
-                q = round_half_even_to_int(y[i] / s);
-                if (q > 127) q = 127;
-                if (q < -127) q = -127;
-            }
-            out_q[base + i] = (int8_t)q;
-        }
+        quantize_row(out_q + base, scale + r, y, hidden);
     }
     free(acc); free(sq); free(y);
+    return ORACLE_OK;
+}
+
+/* Plain RMSNorm: the row function without a residual.  Same layout as
+ * oracle_add_rmsnorm_fwd, minus residual and residual_out. */
+int oracle_rmsnorm_fwd(uint16_t* out, const uint16_t* x, const uint16_t* weight, float eps,
+                       int64_t n_rows, int64_t hidden, int store_mode,
+                       float* row_sum_sq, float* row_inv_rms)
+{
+    if (n_rows < 0 || hidden <= 0)
+        return ORACLE_ERR_ARG;
+    if (n_rows == 0)
+        return ORACLE_OK;
+    if (!out || !x || !weight)
+        return ORACLE_ERR_ARG;
+    int64_t padded = next_pow2(hidden);
+    float* acc = (float*)malloc((size_t)hidden * sizeof(float));
+    float* sq = (float*)calloc((size_t)padded, sizeof(float));
+    float* y = (float*)malloc((size_t)hidden * sizeof(float));
+    if (!acc || !sq || !y) {
+        free(acc); free(sq); free(y);
+        return ORACLE_ERR_NOMEM;
+    }
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t base = r * hidden;
+        add_rmsnorm_row(y, NULL, acc, sq, x + base, NULL, weight, eps, hidden, padded, store_mode,
+                        row_sum_sq ? row_sum_sq + r : NULL,
+                        row_inv_rms ? row_inv_rms + r : NULL);
+        for (int64_t i = 0; i < hidden; ++i)
+            out[base + i] = store_bf16(y[i], store_mode);
+    }
+    free(acc); free(sq); free(y);
+    return ORACLE_OK;
+}
+
+/* Plain RMSNorm with the per-row symmetric int8 output. */
+int oracle_rmsnorm_quant_fwd(int8_t* out_q, float* scale, const uint16_t* x, const uint16_t* weight,
+                             float eps, int64_t n_rows, int64_t hidden)
+{
+    if (n_rows < 0 || hidden <= 0)
+        return ORACLE_ERR_ARG;
+    if (n_rows == 0)
+        return ORACLE_OK;
+    if (!out_q || !scale || !x || !weight)
+        return ORACLE_ERR_ARG;
+    int64_t padded = next_pow2(hidden);
+    float* acc = (float*)malloc((size_t)hidden * sizeof(float));
+    float* sq = (float*)calloc((size_t)padded, sizeof(float));
+    float* y = (float*)malloc((size_t)hidden * sizeof(float));
+    if (!acc || !sq || !y) {
+        free(acc); free(sq); free(y);
+        return ORACLE_ERR_NOMEM;
+    }
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t base = r * hidden;
+        add_rmsnorm_row(y, NULL, acc, sq, x + base, NULL, weight, eps, hidden, padded,
+                        ORACLE_STORE_RNE, NULL, NULL);
+        quantize_row(out_q + base, scale + r, y, hidden);
+    }
+    free(acc); free(sq); free(y);
+    return ORACLE_OK;
+}
+
+/* The residual update alone: residual_out = store(fp32(x) + fp32(residual))
+ * for n elements. */
+int oracle_residual_add_fwd(uint16_t* residual_out, const uint16_t* x, const uint16_t* residual,
+                            int64_t n, int store_mode)
+{
+    if (n < 0 || (n > 0 && (!residual_out || !x || !residual)))
+        return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i) {
+        float acc = oracle_bf16_to_f32(x[i]) + oracle_bf16_to_f32(residual[i]);
+        residual_out[i] = store_bf16(acc, store_mode);
+    }
     return ORACLE_OK;
 }
 

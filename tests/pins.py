@@ -313,6 +313,72 @@ def pin_quant(o, seed: int = 13):
         assert list(q[0].astype(int)) == ex["q"] and scale[0] == ex["scale"], i
 
 
+# ------------------------------------------------------- the two halves
+def pin_rmsnorm(o, seed: int = 17):
+    """Plain RMSNorm (acc = x): within 1 bf16 ulp of fp64; constant rows give
+    the weight back; equal to the residual-add form with a zero residual on
+    rows without -0 (a special case that reduces to the pinned function);
+    and a -0 input keeps its sign (acc = -0, so out = -0 * inv * w), which a
+    zero residual would have turned into +0."""
+    g = inputs.generator(seed)
+    for n, h, sx in [(6, 1024, 1.0), (4, 24, 2.0), (3, 3000, 0.5), (8, 64, 1e-3), (1, 32768, 1.0)]:
+        x = inputs.normal_bf16(g, (n, h), 0.0, sx)
+        w = inputs.normal_bf16(g, (h,), 1.0, 0.5)
+        out = o.rmsnorm_fwd(x, w, 1e-6)
+        y64, _ = refs.add_rmsnorm_f64(x, torch.zeros_like(x), w, 1e-6)
+        assert float((np.abs(refs.bf16_value(out) - y64) / refs.ulp_bf16(y64)).max()) <= 1.0
+        out_add, _ = o.add_rmsnorm_fwd(x, torch.zeros_like(x), w, 1e-6)
+        assert np.array_equal(out, out_add)
+    h = 256
+    w = refs.u16(inputs.normal_bf16(g, (h,), 0.0, 1.0))
+    x = np.array([[0x4040] * h, [0xC0A0] * h], np.uint16)  # constant 3 and -5
+    out = o.rmsnorm_fwd(x, w, 1e-6)
+    assert np.array_equal(out[0], w) and np.array_equal(out[1], w ^ np.uint16(0x8000))
+    x = np.zeros((1, h), np.uint16)
+    x[0, ::2] = 0x8000                                       # -0 at even positions
+    x[0, 1] = 0x3F80                                         # one nonzero keeps inv finite
+    out = o.rmsnorm_fwd(x, np.full(h, 0x3F80, np.uint16), 1e-6)
+    assert np.all(out[0, 2::2] == 0x8000) and np.all(out[0, 3::2] == 0x0000)
+    out_add, _ = o.add_rmsnorm_fwd(x, np.zeros_like(x), np.full(h, 0x3F80, np.uint16), 1e-6)
+    assert np.all(out_add[0, 2::2] == 0x0000)                # -0 + +0 = +0 in the add form
+    for i in range(6):
+        hh = (8, 24, 16)[i % 3]
+        xb = refs.u16(inputs.normal_bf16(g, (1, hh), 0.0, 1.0))
+        wb = refs.u16(inputs.normal_bf16(g, (hh,), 1.0, 0.3))
+        out = o.rmsnorm_fwd(xb, wb, 1e-6)
+        assert list(out[0]) == refs.row_exact(xb[0], [0] * hh, wb, 1e-6)["out"], i
+
+
+def pin_rmsnorm_quant(o, seed: int = 19):
+    """Plain RMSNorm, int8 out: the int8 variant's invariants, and equal to the
+    residual-add int8 form with a zero residual."""
+    g = inputs.generator(seed)
+    for n, h in [(8, 1024), (3, 24), (2, 16384)]:
+        x = inputs.normal_bf16(g, (n, h), 0.0, 2.0)
+        w = inputs.normal_bf16(g, (h,), 1.0, 0.1)
+        q, scale = o.rmsnorm_quant_fwd(x, w, 1e-6)
+        q2, s2, _ = o.add_rmsnorm_quant_fwd(x, torch.zeros_like(x), w, 1e-6)
+        assert np.array_equal(q, q2) and np.array_equal(scale.view(np.uint32), s2.view(np.uint32))
+        assert np.all(np.abs(q.astype(np.int64)).max(axis=1) == 127)
+        y64, _ = refs.add_rmsnorm_f64(x, torch.zeros_like(x), w, 1e-6)
+        q64, _ = refs.quant_f64(y64)
+        assert np.abs(q.astype(np.int64) - q64).max() <= 1
+
+
+def pin_residual_add(o, seed: int = 23):
+    """The residual update alone: torch's cast of the fp32 sum, the residual-add
+    form's residual_out, and the page's truncation in trunc mode."""
+    for c in [inputs.WORKLOADS["tiny"].make(), inputs.edge_rows(16, 1024)]:
+        ro = o.residual_add_fwd(c["x"], c["residual"])
+        exp = refs.u16((c["x"].float() + c["residual"].float()).to(torch.bfloat16))
+        assert np.array_equal(ro, exp)
+        _, ro2 = o.add_rmsnorm_fwd(c["x"], c["residual"], c["weight"], c["eps"])
+        assert np.array_equal(ro, ro2)
+        acc = c["x"].float() + c["residual"].float()
+        trunc = refs.u16((acc.view(torch.int32) >> 16).to(torch.int16))
+        assert np.array_equal(o.residual_add_fwd(c["x"], c["residual"], "trunc"), trunc)
+
+
 FAST_PINS = [
     pin_rne_edge_table,
     pin_tree_worked_examples,
@@ -326,4 +392,7 @@ FAST_PINS = [
     pin_rows_exact_rational,
     pin_reading_examples,
     pin_quant,
+    pin_rmsnorm,
+    pin_rmsnorm_quant,
+    pin_residual_add,
 ]

@@ -179,3 +179,40 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises(ValueError):
         dr.add_rmsnorm_fwd(x, x.clone(), torch.ones(64, dtype=torch.bfloat16), 1e-6,
                            out=x.clone(), residual_out=x.clone())
+
+
+# ----------------------------------------------- plain RMSNorm, residual add
+@pytest.mark.parametrize("args,code", [
+    ((OUT, X, W, 1e-6, 4, 1024), None),            # valid: not called (would launch)
+    ((0, X, W, 1e-6, 4, 1024), 1), ((OUT, 0, W, 1e-6, 4, 1024), 1), ((OUT, X, 0, 1e-6, 4, 1024), 1),
+    ((OUT + 8, X, W, 1e-6, 4, 1024), 4), ((OUT, X, W, -1.0, 4, 1024), 5),
+    ((X + 64, X, W, 1e-6, 4, 1024), 6), ((W, X, W, 1e-6, 4, 1024), 6),
+    ((OUT, X, W, 1e-6, 0, 1024), 0), ((OUT, X, W, 1e-6, 4, 20), 3),
+])
+def test_rmsnorm_argument_errors(L, args, code):
+    if code is None:
+        return
+    assert L.rmsnorm_fwd(*args, None) == code
+
+
+def test_rmsnorm_quant_and_residual_add_errors(L):
+    assert L.rmsnorm_quant_fwd(0, SC, X, W, 1e-6, 4, 1024, None) == 1
+    assert L.rmsnorm_quant_fwd(Q, SC + 1, X, W, 1e-6, 4, 1024, None) == 4
+    assert L.rmsnorm_quant_fwd(X, SC, X, W, 1e-6, 4, 1024, None) == 6
+    assert L.residual_add_fwd(0, X, RES, 4, 1024, None) == 1
+    assert L.residual_add_fwd(RO, X + 4, RES, 4, 1024, None) == 4
+    assert L.residual_add_fwd(X + 32, X, RES, 4, 1024, None) == 6
+    assert L.residual_add_fwd(RO, X, RES, 4, 12, None) == 3
+    assert L.residual_add_fwd(RO, X, RES, -2, 1024, None) == 2
+    assert L.residual_add_fwd(0, 0, 0, 0, 1024, None) == 0
+    assert L.rmsnorm_fwd_with_config(OUT, X, W, 1e-6, 4, 1024, None, None) == 1
+
+
+def test_resolve_op_codes(L):
+    c = dr.LaunchConfig()._c()
+    assert L.dradd_resolve_config(16, 1024, 4, 152, ctypes.byref(c)) == 9
+    plain = dr.resolve_config(4096, 16384, add=False)
+    assert plain.variant == dr.VARIANT_STAGED and plain.stages == 4 and plain.threads_per_row == 512
+    # a plain-RMSNorm stage holds only x, so 32768-wide rows fit two stages
+    c = dr.resolve_config(16, 32768, add=False, config=dr.LaunchConfig(variant=2, stages=2))
+    assert c.stages == 2
