@@ -40,7 +40,7 @@ from deterministic_residual_add_gb300 import inputs  # noqa: E402
 
 METRIC = "add+RMSNorm GB/s and % of HBM peak at 4096×4096 bf16; bit-exact vs oracle"
 N_SETS = 4
-KERNEL_SOURCES = ["csrc/dradd_kernels.cu", "csrc/dradd_device.cuh"]
+KERNEL_SOURCES = ["csrc/dradd_kernels.cuh", "csrc/dradd_device.cuh"]
 TRAFFIC_FILE = ROOT / "profiles" / "add_rmsnorm_fwd_4096x4096_ncu.md"
 
 # name -> (n_rows, hidden, op, input recipe).  The first is the headline
