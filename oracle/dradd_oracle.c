@@ -286,6 +286,96 @@ static void quantize_row(int8_t* q_out, float* scale_out, const float* y, int64_
     }
 }
 
+/* ---- fp8 e4m3 (OCP "e4m3fn": 1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits; no infinities; S.1111.111 is NaN; the largest finite
+ * magnitude is 448 = 1.75 * 2^8; subnormals are m * 2^-9). */
+#define E4M3_MAX 448.0f
+
+/* Magnitude of the e4m3 code c (0 <= c <= 0x7E). */
+static double e4m3_magnitude(unsigned c)
+{
+    unsigned e = (c >> 3) & 0xFu, m = c & 7u;
+    if (e == 0)
+        return ldexp((double)m, -9);
+    return ldexp(1.0 + m / 8.0, (int)e - 7);
+}
+
+/* Round to the nearest e4m3 value, ties to the even code (last mantissa bit
+ * 0); magnitudes above 448 saturate to 448 ("satfinite"); NaN gives 0x7F
+ * with the sign kept.  Found by comparing |f| with the finite magnitudes in
+ * order (the codes 0x00..0x7E increase with their magnitude). */
+uint8_t oracle_e4m3_rne(float f)
+{
+    uint8_t sign = (uint8_t)((bits_from_f32(f) >> 24) & 0x80u);
+    if (isnan(f))
+        return (uint8_t)(sign | 0x7Fu);
+    double a = fabs((double)f);
+    if (a >= (double)E4M3_MAX)
+        return (uint8_t)(sign | 0x7Eu);
+    unsigned lo = 0;  /* largest code with magnitude <= a */
+    while (lo < 0x7Eu && e4m3_magnitude(lo + 1) <= a)
+        ++lo;
+    double d_lo = a - e4m3_magnitude(lo), d_hi = e4m3_magnitude(lo + 1) - a;
+    unsigned c = lo;
+    if (d_hi < d_lo || (d_hi == d_lo && (lo & 1u)))
+        c = lo + 1;
+    return (uint8_t)(sign | c);
+}
+
+/* Per-row symmetric e4m3 codes of the fp32 row y: amax = max |y|,
+ * scale = amax / 448, q = e4m3_rne(y / scale); scale == 0 gives q = 0. */
+static void quantize_row_e4m3(uint8_t* q_out, float* scale_out, const float* y, int64_t hidden)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < hidden; ++i)
+        amax = fmaxf(amax, fabsf(y[i]));
+    float s = amax / E4M3_MAX;
+    *scale_out = s;
+    for (int64_t i = 0; i < hidden; ++i)
+        q_out[i] = s != 0.0f ? oracle_e4m3_rne(y[i] / s) : 0;
+}
+
+/* residual-add + RMSNorm forward with per-row e4m3 out (x, residual ==
+ * NULL: plain RMSNorm, residual_out not written). */
+int oracle_rmsnorm_e4m3_fwd(uint8_t* out_q, float* scale, uint16_t* residual_out,
+                            const uint16_t* x, const uint16_t* residual,
+                            const uint16_t* weight, float eps, int64_t n_rows, int64_t hidden)
+{
+    if (n_rows < 0 || hidden <= 0)
+        return ORACLE_ERR_ARG;
+    if (n_rows == 0)
+        return ORACLE_OK;
+    if (!out_q || !scale || !x || !weight || (residual && !residual_out))
+        return ORACLE_ERR_ARG;
+    int64_t padded = next_pow2(hidden);
+    float* acc = (float*)malloc((size_t)hidden * sizeof(float));
+    float* sq = (float*)calloc((size_t)padded, sizeof(float));
+    float* y = (float*)malloc((size_t)hidden * sizeof(float));
+    if (!acc || !sq || !y) {
+        free(acc); free(sq); free(y);
+        return ORACLE_ERR_NOMEM;
+    }
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t base = r * hidden;
+        add_rmsnorm_row(y, residual ? residual_out + base : NULL, acc, sq, x + base,
+                        residual ? residual + base : NULL, weight, eps, hidden, padded,
+                        ORACLE_STORE_RNE, NULL, NULL);
+        quantize_row_e4m3(out_q + base, scale + r, y, hidden);
+    }
+    free(acc); free(sq); free(y);
+    return ORACLE_OK;
+}
+
+/* Convert n fp32 values to e4m3 codes (for the conversion checks). */
+int oracle_e4m3_convert_array(uint8_t* dst, const float* src, int64_t n)
+{
+    if ((!dst || !src) && n > 0)
+        return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = oracle_e4m3_rne(src[i]);
+    return ORACLE_OK;
+}
+
 /* residual-add + RMSNorm forward with per-row symmetric int8 out.
  * out_q: n_rows x hidden int8; scale: n_rows fp32 (q * scale ~ y). */
 int oracle_add_rmsnorm_quant_fwd(int8_t* out_q, float* scale, uint16_t* residual_out,

@@ -251,6 +251,8 @@ EXAMPLE_RSQRT = [  # 1 / sqrt(v) in two rounded steps  vs  one correctly rounded
     0x4003, 0x3D42, 0x403B, 0x3DE2, 0x407C, 0x3EC0, 0x3EA8, 0x4015]
 EXAMPLE_QUANT_DIV = [  # q = rint(y / scale)  vs  rint(y * (1 / scale)), weight 1
     0xBFFB, 0x401F, 0x3FC5, 0xBF9F, 0xBD80, 0xBF5C, 0x3F54, 0x3CBE]
+EXAMPLE_FP8_DIV = [  # e4m3(y / scale)  vs  e4m3(y * (1 / scale)), plain RMSNorm, weight 1
+    0xBCA9, 0xBC7B, 0xBFBB, 0x3FAE, 0x3F09, 0xC028, 0x3EBA, 0x3C74]
 
 
 def pin_reading_examples(o):
@@ -274,6 +276,12 @@ def pin_reading_examples(o):
     x = np.array([xb], np.uint16)
     q, scale, _ = o.add_rmsnorm_quant_fwd(x, np.zeros_like(x), np.array(wb, np.uint16), 1e-6)
     assert list(q[0].astype(int)) == stated["q"] and scale[0] == stated["scale"]
+    xb = EXAMPLE_FP8_DIV
+    stated, sc = refs.e4m3_row_exact(xb, None, [0x3F80] * 8, 1e-6)
+    other, _ = refs.e4m3_row_exact(xb, None, [0x3F80] * 8, 1e-6, quant_op="recip")
+    assert stated != other
+    q, scale = o.rmsnorm_fp8_fwd(np.array([xb], np.uint16), np.full(8, 0x3F80, np.uint16), 1e-6)
+    assert list(q[0]) == stated and scale[0] == sc
 
 
 # ------------------------------------------------------------------ quant
@@ -379,6 +387,72 @@ def pin_residual_add(o, seed: int = 23):
         assert np.array_equal(o.residual_add_fwd(c["x"], c["residual"], "trunc"), trunc)
 
 
+# ---------------------------------------------------------------- fp8 e4m3
+def pin_e4m3_encoder(o, seed: int = 29):
+    """The e4m3 encoder: hand-derived codes (ties to the even code, the
+    subnormal range, saturation at 448), every finite code decodes and
+    re-encodes to itself, and agreement with torch's cast to float8_e4m3fn on
+    values clamped to the finite range (torch rounds to nearest even there)."""
+    table = [(1.0, 0x38), (448.0, 0x7E), (500.0, 0x7E), (1e30, 0x7E), (-448.0, 0xFE),
+             (2.0 ** -9, 0x01), (2.0 ** -10, 0x00), (1.5 * 2.0 ** -10, 0x01), (3 * 2.0 ** -10, 0x02),
+             (1.0625, 0x38), (1.1875, 0x3A), (432.0, 0x7E), (240.0, 0x77), (-0.0, 0x80),
+             (0.0, 0x00), (2.0 ** -6, 0x08), (7 * 2.0 ** -9, 0x07), (15 * 2.0 ** -10, 0x08)]
+    for f, code in table:
+        assert o.e4m3_scalar(f) == code, (f, hex(code), hex(o.e4m3_scalar(f)))
+    for c in list(range(0x7F)) + [c | 0x80 for c in range(0x7F)]:
+        v = -0.0 if c == 0x80 else float(refs.e4m3_value(c))
+        assert o.e4m3_scalar(v) == c, hex(c)
+    rng = np.random.default_rng(seed)
+    f = np.concatenate([rng.standard_normal(1 << 18).astype(np.float32) * 50,
+                        (rng.standard_normal(1 << 16) * 2.0 ** -8).astype(np.float32),
+                        np.array([refs.e4m3_value(c) for c in range(0x7F)], dtype=np.float64).astype(np.float32)
+                        * np.float32(1.0625)])
+    f = np.clip(f, -448.0, 448.0).astype(np.float32)
+    got = o.e4m3_convert(f)
+    exp = torch.from_numpy(f.copy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    bad = np.nonzero(got != exp)[0]
+    assert bad.size == 0, (bad.size, float(f[bad[0]]), hex(got[bad[0]]), hex(exp[bad[0]]))
+
+
+def pin_fp8_rows(o, seed: int = 31):
+    """Per-row e4m3 out: 448 reached on every nonzero row, dequantisation
+    within half an e4m3 step of the fp64 value (plus the fp32 path's error),
+    equal to the exact-rational evaluation on small rows, zero rows give
+    scale 0 and code 0, and the residual form's residual_out is the bf16
+    variant's."""
+    g = inputs.generator(seed)
+    vals = np.array([float(refs.e4m3_value(c)) for c in range(0x7F)] + [float("nan")])
+    for n, h, with_res in [(8, 1024, True), (4, 24, False), (2, 16384, True), (6, 3000, False)]:
+        x = inputs.normal_bf16(g, (n, h), 0.0, 1.0)
+        r = inputs.normal_bf16(g, (n, h), 0.0, 2.0) if with_res else None
+        w = inputs.normal_bf16(g, (h,), 1.0, 0.1)
+        res = o.rmsnorm_fp8_fwd(x, w, 1e-6, residual=r)
+        q, scale = res[0], res[1]
+        if with_res:
+            _, ro_b = o.add_rmsnorm_fwd(x, r, w, 1e-6)
+            assert np.array_equal(res[2], ro_b)
+        assert np.all((q & 0x7F).max(axis=1) == 0x7E)
+        mag = vals[q & 0x7F] * np.where(q & 0x80, -1.0, 1.0)
+        y64, _ = refs.add_rmsnorm_f64(x, r if with_res else torch.zeros_like(x), w, 1e-6)
+        deq = mag * scale.astype(np.float64)[:, None]
+        # half an e4m3 step at the value's binade (2^-4 relative), or half the
+        # subnormal step 2^-10 times the scale
+        step = np.maximum(np.abs(mag) * 2.0 ** -4, 2.0 ** -10) * scale.astype(np.float64)[:, None]
+        assert np.all(np.abs(deq - y64) <= step + np.abs(y64) * 2.0 ** -20)
+    z = np.zeros((2, 64), np.uint16)
+    q, scale = o.rmsnorm_fp8_fwd(z, np.full(64, 0x3F80, np.uint16), 1e-6)
+    assert np.all(q == 0) and np.all(scale == 0)
+    for i in range(6):
+        hh = (8, 16)[i % 2]
+        xb = refs.u16(inputs.normal_bf16(g, (1, hh), 0.0, 1.0))
+        rb = refs.u16(inputs.normal_bf16(g, (1, hh), 0.0, 1.0))
+        wb = refs.u16(inputs.normal_bf16(g, (hh,), 1.0, 0.3))
+        plain = i % 3 == 0
+        res = o.rmsnorm_fp8_fwd(xb, wb, 1e-6, residual=None if plain else rb)
+        codes, sc = refs.e4m3_row_exact(xb[0], None if plain else rb[0], wb, 1e-6)
+        assert list(res[0][0]) == codes and res[1][0] == sc, i
+
+
 FAST_PINS = [
     pin_rne_edge_table,
     pin_tree_worked_examples,
@@ -395,4 +469,6 @@ FAST_PINS = [
     pin_rmsnorm,
     pin_rmsnorm_quant,
     pin_residual_add,
+    pin_e4m3_encoder,
+    pin_fp8_rows,
 ]

@@ -218,6 +218,69 @@ def row_exact(x_bits, r_bits, w_bits, eps: float, *, mul_order: str = "left",
     return res
 
 
+# ---------------------------------------------------------------- e4m3
+def e4m3_value(code: int) -> Fraction:
+    """Exact value of an e4m3 (e4m3fn) code; NaN codes are not accepted."""
+    sign = -1 if code & 0x80 else 1
+    e, m = (code >> 3) & 0xF, code & 7
+    assert not (e == 15 and m == 7), "NaN"
+    mag = Fraction(m, 8) * Fraction(1, 2 ** 6) if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+    return sign * mag
+
+
+def e4m3_rne_exact(q: Fraction) -> int:
+    """Nearest e4m3 code to a rational, ties to the even code, saturating at
+    448; the sign of zero follows the sign of q."""
+    neg = q < 0
+    a = -q if neg else q
+    if a >= 448:
+        return 0x7E | (0x80 if neg else 0)
+    best = min(range(0x7F), key=lambda c: (abs(e4m3_value(c) - a), c & 1))
+    return best | (0x80 if neg else 0)
+
+
+def e4m3_row_exact(x_bits, r_bits, w_bits, eps: float, quant_op: str = "div"):
+    """Exact-rational e4m3 quantisation of one row (residual None: plain):
+    scale = RN32(amax / 448), q = e4m3 of RN32(y / scale) (quant_op="recip":
+    of RN32(y * RN32(1 / scale)), the alternative reading)."""
+    xs = list(x_bits)
+    rs = list(r_bits) if r_bits is not None else [0] * len(xs)
+    ys = row_exact(xs, rs, w_bits, eps)["y"] if r_bits is not None else _plain_row_y(xs, w_bits, eps)
+    amax = max((abs(frac(y)) for y in ys), default=Fraction(0))
+    scale = rn32(amax / 448)
+    if scale == 0:
+        return [0] * len(ys), scale
+    codes = []
+    for y in ys:
+        if quant_op == "div":
+            t = rn32(frac(y) / frac(scale))
+        else:
+            t = rn32(frac(y) * frac(rn32(Fraction(1) / frac(scale))))
+        c = e4m3_rne_exact(frac(t))
+        if frac(t) == 0 and np.float32(t).view(np.uint32) >> 31:
+            c |= 0x80
+        codes.append(c)
+    return codes, scale
+
+
+def _plain_row_y(x_bits, w_bits, eps):
+    """fp32 y of plain RMSNorm (acc = x exactly) by exact rational steps."""
+    acc = [np.float32(bf16_value(np.uint16(b))) for b in x_bits]
+    h = len(acc)
+    sq = [rn32(frac(a) * frac(a)) for a in acc]
+    p = 1
+    while p < h:
+        p *= 2
+    level = [frac(s) for s in sq] + [Fraction(0)] * (p - h)
+    while len(level) > 1:
+        level = [frac(rn32(level[i] + level[i + 1])) for i in range(0, len(level), 2)]
+    S = rn32(level[0])
+    v = rn32(frac(rn32(frac(S) / h)) + frac(np.float32(eps)))
+    inv = rn32(Fraction(1) / frac(sqrt_rn32(v)))
+    ws = [frac(bf16_value(np.uint16(b))) for b in w_bits]
+    return [rn32(frac(rn32(frac(a) * frac(inv))) * w) for a, w in zip(acc, ws)]
+
+
 # ------------------------------------------------------------- metrics
 def magnitude_bias(got_bits, exp_bits) -> float:
     """The page's magnitude_bias(): mean over e != 0 of (|g| - |e|) / |e|;

@@ -50,6 +50,12 @@ MUTANTS = {
         "float acc = oracle_bf16_to_f32(x[i]) - oracle_bf16_to_f32(residual[i]);"),
     "residual_add_truncates": ("residual_out[i] = store_bf16(acc, store_mode);",
                                "residual_out[i] = store_bf16(acc, ORACLE_STORE_TRUNC);"),
+    "e4m3_scale_480": ("float s = amax / E4M3_MAX;", "float s = amax / 480.0f;"),
+    "e4m3_ties_to_odd": ("if (d_hi < d_lo || (d_hi == d_lo && (lo & 1u)))",
+                         "if (d_hi < d_lo || (d_hi == d_lo && !(lo & 1u)))"),
+    "e4m3_no_saturation": ("if (a >= (double)E4M3_MAX)", "if (a >= 1e30)"),
+    "e4m3_quotient_by_reciprocal": ("q_out[i] = s != 0.0f ? oracle_e4m3_rne(y[i] / s) : 0;",
+                                    "q_out[i] = s != 0.0f ? oracle_e4m3_rne(y[i] * (1.0f / s)) : 0;"),
 }
 
 
