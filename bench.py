@@ -45,7 +45,8 @@ TRAFFIC_FILE = ROOT / "profiles" / "add_rmsnorm_fwd_4096x4096_ncu.md"
 
 # name -> (n_rows, hidden, op, input recipe).  The first is the headline
 # workload; the others are for profiling and context.  op is one of
-# add_rmsnorm, add_rmsnorm_quant, rmsnorm, rmsnorm_quant, residual_add.
+# add_rmsnorm, add_rmsnorm_quant, add_rmsnorm_fp8, rmsnorm, rmsnorm_quant,
+# rmsnorm_fp8, residual_add.
 WORKLOADS = {
     "4096x4096": (4096, 4096, "add_rmsnorm", "chain4096"),
     "2048x4096": (2048, 4096, "add_rmsnorm", "2048x4096"),
@@ -56,6 +57,9 @@ WORKLOADS = {
     "rmsnorm4096x4096": (4096, 4096, "rmsnorm", "chain4096"),
     "rmsnorm_quant4096x4096": (4096, 4096, "rmsnorm_quant", "chain4096"),
     "residual_add4096x4096": (4096, 4096, "residual_add", "chain4096"),
+    "fp8_2048x16384": (2048, 16384, "add_rmsnorm_fp8", "quant2048x16384"),
+    "fp8_4096x4096": (4096, 4096, "add_rmsnorm_fp8", "chain4096"),
+    "rmsnorm_fp8_4096x4096": (4096, 4096, "rmsnorm_fp8", "chain4096"),
 }
 
 
@@ -66,8 +70,10 @@ def algorithmic_bytes(n_rows: int, hidden: int, op: str = "add_rmsnorm") -> int:
     e = n_rows * hidden
     return {"add_rmsnorm": 8 * e + 2 * hidden,
             "add_rmsnorm_quant": 7 * e + 4 * n_rows + 2 * hidden,
+            "add_rmsnorm_fp8": 7 * e + 4 * n_rows + 2 * hidden,
             "rmsnorm": 4 * e + 2 * hidden,
             "rmsnorm_quant": 3 * e + 4 * n_rows + 2 * hidden,
+            "rmsnorm_fp8": 3 * e + 4 * n_rows + 2 * hidden,
             "residual_add": 6 * e}[op]
 
 
@@ -205,7 +211,7 @@ def make_sets(device, name: str):
     for x_cpu in xs:
         x = x_cpu.to(device)
         s = {"x": x, "r": r0.to(device), "out": torch.empty_like(x), "ro": torch.empty_like(x)}
-        if op.endswith("quant"):
+        if op.endswith("quant") or op.endswith("fp8"):
             s["q"] = torch.empty(n, h, dtype=torch.int8, device=device)
             s["scale"] = torch.empty(n, dtype=torch.float32, device=device)
         sets.append(s)
@@ -231,11 +237,11 @@ class RawCall:
             x, r, ro = s["x"].data_ptr(), s["r"].data_ptr(), s["ro"].data_ptr()
             if op == "add_rmsnorm":
                 return (s["out"].data_ptr(), ro, x, r, wp, eps, n_rows, hidden, st)
-            if op == "add_rmsnorm_quant":
+            if op in ("add_rmsnorm_quant", "add_rmsnorm_fp8"):
                 return (s["q"].data_ptr(), s["scale"].data_ptr(), ro, x, r, wp, eps, n_rows, hidden, st)
             if op == "rmsnorm":
                 return (s["out"].data_ptr(), x, wp, eps, n_rows, hidden, st)
-            if op == "rmsnorm_quant":
+            if op in ("rmsnorm_quant", "rmsnorm_fp8"):
                 return (s["q"].data_ptr(), s["scale"].data_ptr(), x, wp, eps, n_rows, hidden, st)
             return (ro, x, r, n_rows, hidden, st)
 
@@ -329,7 +335,9 @@ def cpu_baseline(seconds: float, name: str, first_inputs, gpu_set0=None):
            "add_rmsnorm_quant": lambda x, r: o.add_rmsnorm_quant_fwd(x, r, w, inputs.EPS),
            "rmsnorm": lambda x, r: (o.rmsnorm_fwd(x, w, inputs.EPS),),
            "rmsnorm_quant": lambda x, r: o.rmsnorm_quant_fwd(x, w, inputs.EPS),
-           "residual_add": lambda x, r: (o.residual_add_fwd(x, r),)}
+           "residual_add": lambda x, r: (o.residual_add_fwd(x, r),),
+           "add_rmsnorm_fp8": lambda x, r: o.rmsnorm_fp8_fwd(x, w, inputs.EPS, residual=r),
+           "rmsnorm_fp8": lambda x, r: o.rmsnorm_fp8_fwd(x, w, inputs.EPS)}
     fn = fns[op]
     chunk = 64
     rows = 0
@@ -357,7 +365,8 @@ def cpu_baseline(seconds: float, name: str, first_inputs, gpu_set0=None):
                 t = t.view(torch.int16)
             return t.numpy()
         keys = {"add_rmsnorm": ["out", "ro"], "add_rmsnorm_quant": ["q", "scale", "ro"],
-                "rmsnorm": ["out"], "rmsnorm_quant": ["q", "scale"], "residual_add": ["ro"]}[op]
+                "rmsnorm": ["out"], "rmsnorm_quant": ["q", "scale"], "residual_add": ["ro"],
+                "add_rmsnorm_fp8": ["q", "scale", "ro"], "rmsnorm_fp8": ["q", "scale"]}[op]
         got = [host(gpu_set0[k]) for k in keys]
         out["parity_rows_checked"] = chunk
         out["parity_bit_exact"] = bool(all(
@@ -370,7 +379,7 @@ def run_ours(args):
     world, rank, local = dist_setup()
     device = torch.device("cuda", local)
     n_rows, hidden, op, _ = WORKLOADS[args.workload]
-    quant = op.endswith("quant")
+    quant = op.endswith("quant") or op.endswith("fp8")
     dr.lib()
     stream = torch.cuda.Stream(device)
     sets, w_dev, first_inputs = make_sets(device, args.workload)
@@ -391,7 +400,7 @@ def run_ours(args):
         peak = 6800.0
 
     e2e = None
-    if not args.no_e2e and op.startswith("add_rmsnorm"):
+    if not args.no_e2e and op in ("add_rmsnorm", "add_rmsnorm_quant"):
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
         dt, bi, bo = time_e2e(e2e_steps, device, stream, args.workload)
         dt = max_over_ranks(dt, world)
@@ -404,13 +413,16 @@ def run_ours(args):
     if op == "residual_add":
         launch = {"variant": "elementwise"}
     else:
-        cfg = dr.resolve_config(n_rows, hidden, quant=quant, sm_count=sm_count, add=op.startswith("add"))
+        cfg = dr.resolve_config(n_rows, hidden, quant=quant, sm_count=sm_count, add=op.startswith("add"),
+                                fp8=op.endswith("fp8"))
         launch = {"variant": "rows" if cfg.variant == 1 else "staged",
                   "threads_per_row": cfg.threads_per_row, "rows_per_cta": cfg.rows_per_cta,
                   "stages": cfg.stages}
     io = {"add_rmsnorm": "bf16 in/out", "add_rmsnorm_quant": "bf16 in, int8 + fp32 scale + bf16 residual_out out",
           "rmsnorm": "bf16 in/out", "rmsnorm_quant": "bf16 in, int8 + fp32 scale out",
-          "residual_add": "bf16 in/out"}[op]
+          "residual_add": "bf16 in/out",
+          "add_rmsnorm_fp8": "bf16 in, e4m3 + fp32 scale + bf16 residual_out out",
+          "rmsnorm_fp8": "bf16 in, e4m3 + fp32 scale out"}[op]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
@@ -454,7 +466,9 @@ def run_reference(args):
            "add_rmsnorm_quant": lambda x, r: o.add_rmsnorm_quant_fwd(x, r, w, inputs.EPS),
            "rmsnorm": lambda x, r: o.rmsnorm_fwd(x, w, inputs.EPS),
            "rmsnorm_quant": lambda x, r: o.rmsnorm_quant_fwd(x, w, inputs.EPS),
-           "residual_add": lambda x, r: o.residual_add_fwd(x, r)}
+           "residual_add": lambda x, r: o.residual_add_fwd(x, r),
+           "add_rmsnorm_fp8": lambda x, r: o.rmsnorm_fp8_fwd(x, w, inputs.EPS, residual=r),
+           "rmsnorm_fp8": lambda x, r: o.rmsnorm_fp8_fwd(x, w, inputs.EPS)}
     fn = fns[op]
     t0 = time.perf_counter()
     fn(x0[:16], r0[:16])

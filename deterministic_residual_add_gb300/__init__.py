@@ -22,6 +22,7 @@ from pathlib import Path
 __all__ = [
     "add_rmsnorm_fwd", "add_rmsnorm_quant_fwd", "add_rmsnorm_fwd_with_config",
     "add_rmsnorm_quant_fwd_with_config", "rmsnorm_fwd", "rmsnorm_quant_fwd", "residual_add_fwd",
+    "add_rmsnorm_fp8_fwd", "rmsnorm_fp8_fwd",
     "LaunchConfig", "DraddError", "resolve_config",
     "device_status", "bf16_convert_range", "status_string", "abi_version", "lib", "library_path",
     "VARIANT_AUTO", "VARIANT_ROWS", "VARIANT_STAGED", "MAX_HIDDEN",
@@ -32,6 +33,7 @@ LIB_PATH = PKG / "libdradd.so"
 MAX_HIDDEN = 32768
 VARIANT_AUTO, VARIANT_ROWS, VARIANT_STAGED = 0, 1, 2
 OP_ADD_RMSNORM, OP_ADD_RMSNORM_QUANT, OP_RMSNORM, OP_RMSNORM_QUANT = 0, 1, 2, 3
+OP_ADD_RMSNORM_FP8, OP_RMSNORM_FP8 = 4, 5
 
 STATUS_NAMES = {
     0: "OK", 1: "NULL_PTR", 2: "BAD_SHAPE", 3: "UNSUPPORTED_HIDDEN", 4: "MISALIGNED",
@@ -105,6 +107,10 @@ def lib() -> ctypes.CDLL:
                        ("rmsnorm_fwd_with_config", [_vp, _vp, _vp, _f32, _i64, _i64, _vp, cfgp]),
                        ("rmsnorm_quant_fwd_with_config", [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp, cfgp]),
                        ("residual_add_fwd", [_vp, _vp, _vp, _i64, _i64, _vp]),
+                       ("add_rmsnorm_fp8_fwd", quant_args),
+                       ("add_rmsnorm_fp8_fwd_with_config", quant_args + [cfgp]),
+                       ("rmsnorm_fp8_fwd", [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp]),
+                       ("rmsnorm_fp8_fwd_with_config", [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp, cfgp]),
                        ("dradd_resolve_config", [_i64, _i64, ctypes.c_int, ctypes.c_int, cfgp]),
                        ("dradd_device_status", [_vp, ctypes.c_int]),
                        ("dradd_bf16_convert_range", [_vp, ctypes.c_uint64, _i64, ctypes.c_int, _vp])]:
@@ -240,10 +246,14 @@ def add_rmsnorm_quant_fwd_with_config(x, residual, weight, eps, config: LaunchCo
 
 
 def resolve_config(n_rows: int, hidden: int, quant: bool = False, sm_count: int = 152,
-                   config: LaunchConfig | None = None, add: bool = True) -> LaunchConfig:
+                   config: LaunchConfig | None = None, add: bool = True, fp8: bool = False) -> LaunchConfig:
     """The configuration the library would launch for this shape (no GPU
-    work when sm_count > 0); add=False for plain RMSNorm."""
-    op = (OP_ADD_RMSNORM if add else OP_RMSNORM) + (1 if quant else 0)
+    work when sm_count > 0); add=False for plain RMSNorm, fp8=True for the
+    e4m3 output."""
+    if fp8:
+        op = OP_ADD_RMSNORM_FP8 if add else OP_RMSNORM_FP8
+    else:
+        op = (OP_ADD_RMSNORM if add else OP_RMSNORM) + (1 if quant else 0)
     c = (config or LaunchConfig())._c()
     _check(lib().dradd_resolve_config(int(n_rows), int(hidden), op, int(sm_count), ctypes.byref(c)),
            "dradd_resolve_config")
@@ -289,6 +299,61 @@ def rmsnorm_quant_fwd(x, weight, eps: float = 1e-6, *, out_q=None, scale=None, s
             c = config._c()
             _check(lib().rmsnorm_quant_fwd_with_config(*args, ctypes.byref(c)),
                    "rmsnorm_quant_fwd_with_config")
+    return out_q, scale
+
+
+def _fp8_outs(x, out_q, scale):
+    torch = _torch()
+    if out_q is None:
+        out_q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    if out_q.dtype != torch.uint8:
+        raise ValueError("out_q must hold uint8 e4m3 codes")
+    return out_q, scale
+
+
+def add_rmsnorm_fp8_fwd(x, residual, weight, eps: float = 1e-6, *, out_q=None, scale=None,
+                        residual_out=None, stream=None, config: LaunchConfig | None = None):
+    """Residual-add + RMSNorm with per-row e4m3 out: (out_q uint8 codes,
+    scale, residual_out)."""
+    torch = _torch()
+    n_rows, hidden = _shape(x, None)
+    n = n_rows * hidden
+    out_q, scale = _fp8_outs(x, out_q, scale)
+    if residual_out is None:
+        residual_out = torch.empty_like(x)
+    _check_quant_outs(out_q.view(torch.int8), scale, n, n_rows)
+    args = (out_q.data_ptr(), scale.data_ptr(), _bf16_ptr(residual_out, "residual_out", n),
+            _bf16_ptr(x, "x", n), _bf16_ptr(residual, "residual", n),
+            _bf16_ptr(weight, "weight", hidden), float(eps), n_rows, hidden,
+            _stream_handle(stream, x.device))
+    with torch.cuda.device(x.device):
+        if config is None:
+            _check(lib().add_rmsnorm_fp8_fwd(*args), "add_rmsnorm_fp8_fwd")
+        else:
+            c = config._c()
+            _check(lib().add_rmsnorm_fp8_fwd_with_config(*args, ctypes.byref(c)),
+                   "add_rmsnorm_fp8_fwd_with_config")
+    return out_q, scale, residual_out
+
+
+def rmsnorm_fp8_fwd(x, weight, eps: float = 1e-6, *, out_q=None, scale=None, stream=None,
+                    config: LaunchConfig | None = None):
+    """Plain RMSNorm with per-row e4m3 out: (out_q uint8 codes, scale)."""
+    torch = _torch()
+    n_rows, hidden = _shape(x, None)
+    n = n_rows * hidden
+    out_q, scale = _fp8_outs(x, out_q, scale)
+    _check_quant_outs(out_q.view(torch.int8), scale, n, n_rows)
+    args = (out_q.data_ptr(), scale.data_ptr(), _bf16_ptr(x, "x", n), _bf16_ptr(weight, "weight", hidden),
+            float(eps), n_rows, hidden, _stream_handle(stream, x.device))
+    with torch.cuda.device(x.device):
+        if config is None:
+            _check(lib().rmsnorm_fp8_fwd(*args), "rmsnorm_fp8_fwd")
+        else:
+            c = config._c()
+            _check(lib().rmsnorm_fp8_fwd_with_config(*args, ctypes.byref(c)), "rmsnorm_fp8_fwd_with_config")
     return out_q, scale
 
 

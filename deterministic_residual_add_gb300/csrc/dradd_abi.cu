@@ -287,11 +287,14 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     return DRADD_OK;
 }
 
-dradd_status run(bool quant, bool add, dradd_bf16* out, int8_t* out_q, float* scale,
+// out_kind: dradd::kOutBf16 (writes out), kOutInt8 or kOutE4m3 (writes the
+// 1-byte codes to out_q and the per-row scale).
+dradd_status run(int out_kind, bool add, dradd_bf16* out, int8_t* out_q, float* scale,
                  dradd_bf16* residual_out, const dradd_bf16* x, const dradd_bf16* residual,
                  const dradd_bf16* weight, float eps, int64_t n_rows, int64_t hidden, cudaStream_t stream,
                  const dradd_launch_cfg* user_cfg)
 {
+    const bool quant = out_kind != dradd::kOutBf16;
     bool noop = false;
     dradd_status st = validate(quant, add, out, out_q, scale, residual_out, x, residual, weight, eps, n_rows,
                                hidden, &noop);
@@ -316,7 +319,7 @@ dradd_status run(bool quant, bool add, dradd_bf16* out, int8_t* out_q, float* sc
     if (auto_grid && cfg.variant == DRADD_VARIANT_STAGED) {
         // persistent grid: as many CTAs as fit on the device at once
         int per_sm = 0;
-        if (dradd::staged_occupancy(K, quant, add, cfg.threads_per_row, dyn, &per_sm) != cudaSuccess)
+        if (dradd::staged_occupancy(K, out_kind, add, cfg.threads_per_row, dyn, &per_sm) != cudaSuccess)
             return DRADD_ERR_CUDA;
         int64_t grid = static_cast<int64_t>(L.sm_count) * (per_sm > 0 ? per_sm : 1);
         if (grid > n_rows)
@@ -346,10 +349,10 @@ dradd_status run(bool quant, bool add, dradd_bf16* out, int8_t* out_q, float* sc
         return DRADD_ERR_CUDA;
     cudaError_t e;
     if (cfg.variant == DRADD_VARIANT_STAGED) {
-        e = dradd::launch_staged(p, K, quant, add, cfg.grid_ctas, cfg.threads_per_row, dyn,
+        e = dradd::launch_staged(p, K, out_kind, add, cfg.grid_ctas, cfg.threads_per_row, dyn,
                                  cfg.serialize != 0, stream);
     } else {
-        e = dradd::launch_rows(p, K, quant, add, cfg.grid_ctas, cfg.threads_per_row * cfg.rows_per_cta,
+        e = dradd::launch_rows(p, K, out_kind, add, cfg.grid_ctas, cfg.threads_per_row * cfg.rows_per_cta,
                                cfg.serialize != 0, stream);
     }
     return e == cudaSuccess ? DRADD_OK : DRADD_ERR_CUDA;
@@ -363,7 +366,7 @@ dradd_status add_rmsnorm_fwd(dradd_bf16* out, dradd_bf16* residual_out, const dr
                              const dradd_bf16* residual, const dradd_bf16* weight, float eps,
                              int64_t n_rows, int64_t hidden, cudaStream_t stream)
 {
-    return run(false, true, out, nullptr, nullptr, residual_out, x, residual, weight, eps, n_rows, hidden,
+    return run(dradd::kOutBf16, true, out, nullptr, nullptr, residual_out, x, residual, weight, eps, n_rows, hidden,
                stream, nullptr);
 }
 
@@ -372,7 +375,7 @@ dradd_status add_rmsnorm_quant_fwd(int8_t* out_q, float* scale, dradd_bf16* resi
                                    const dradd_bf16* weight, float eps, int64_t n_rows,
                                    int64_t hidden, cudaStream_t stream)
 {
-    return run(true, true, nullptr, out_q, scale, residual_out, x, residual, weight, eps, n_rows, hidden,
+    return run(dradd::kOutInt8, true, nullptr, out_q, scale, residual_out, x, residual, weight, eps, n_rows, hidden,
                stream, nullptr);
 }
 
@@ -384,7 +387,7 @@ dradd_status add_rmsnorm_fwd_with_config(dradd_bf16* out, dradd_bf16* residual_o
 {
     if (!cfg)
         return DRADD_ERR_NULL_PTR;
-    return run(false, true, out, nullptr, nullptr, residual_out, x, residual, weight, eps, n_rows, hidden,
+    return run(dradd::kOutBf16, true, out, nullptr, nullptr, residual_out, x, residual, weight, eps, n_rows, hidden,
                stream, cfg);
 }
 
@@ -396,7 +399,7 @@ dradd_status add_rmsnorm_quant_fwd_with_config(int8_t* out_q, float* scale, drad
 {
     if (!cfg)
         return DRADD_ERR_NULL_PTR;
-    return run(true, true, nullptr, out_q, scale, residual_out, x, residual, weight, eps, n_rows, hidden,
+    return run(dradd::kOutInt8, true, nullptr, out_q, scale, residual_out, x, residual, weight, eps, n_rows, hidden,
                stream, cfg);
 }
 
@@ -405,7 +408,7 @@ dradd_status dradd_resolve_config(int64_t n_rows, int64_t hidden, int op, int sm
 {
     if (!cfg)
         return DRADD_ERR_NULL_PTR;
-    if (op < DRADD_OP_ADD_RMSNORM || op > DRADD_OP_RMSNORM_QUANT)
+    if (op < DRADD_OP_ADD_RMSNORM || op > DRADD_OP_RMSNORM_FP8)
         return DRADD_ERR_BAD_CONFIG;
     DeviceLimits L;
     if (sm_count > 0) {
@@ -415,22 +418,60 @@ dradd_status dradd_resolve_config(int64_t n_rows, int64_t hidden, int op, int sm
         if (st != DRADD_OK)
             return st;
     }
-    const bool quant = op == DRADD_OP_ADD_RMSNORM_QUANT || op == DRADD_OP_RMSNORM_QUANT;
-    const bool add = op == DRADD_OP_ADD_RMSNORM || op == DRADD_OP_ADD_RMSNORM_QUANT;
+    const bool quant = op != DRADD_OP_ADD_RMSNORM && op != DRADD_OP_RMSNORM;
+    const bool add = op == DRADD_OP_ADD_RMSNORM || op == DRADD_OP_ADD_RMSNORM_QUANT ||
+                     op == DRADD_OP_ADD_RMSNORM_FP8;
     return resolve(n_rows, hidden, quant, add, L, cfg);
+}
+
+dradd_status add_rmsnorm_fp8_fwd(uint8_t* out_q, float* scale, dradd_bf16* residual_out,
+                                 const dradd_bf16* x, const dradd_bf16* residual, const dradd_bf16* weight,
+                                 float eps, int64_t n_rows, int64_t hidden, cudaStream_t stream)
+{
+    return run(dradd::kOutE4m3, true, nullptr, reinterpret_cast<int8_t*>(out_q), scale, residual_out, x,
+               residual, weight, eps, n_rows, hidden, stream, nullptr);
+}
+
+dradd_status add_rmsnorm_fp8_fwd_with_config(uint8_t* out_q, float* scale, dradd_bf16* residual_out,
+                                             const dradd_bf16* x, const dradd_bf16* residual,
+                                             const dradd_bf16* weight, float eps, int64_t n_rows,
+                                             int64_t hidden, cudaStream_t stream,
+                                             const dradd_launch_cfg* cfg)
+{
+    if (!cfg)
+        return DRADD_ERR_NULL_PTR;
+    return run(dradd::kOutE4m3, true, nullptr, reinterpret_cast<int8_t*>(out_q), scale, residual_out, x,
+               residual, weight, eps, n_rows, hidden, stream, cfg);
+}
+
+dradd_status rmsnorm_fp8_fwd(uint8_t* out_q, float* scale, const dradd_bf16* x, const dradd_bf16* weight,
+                             float eps, int64_t n_rows, int64_t hidden, cudaStream_t stream)
+{
+    return run(dradd::kOutE4m3, false, nullptr, reinterpret_cast<int8_t*>(out_q), scale, nullptr, x, nullptr,
+               weight, eps, n_rows, hidden, stream, nullptr);
+}
+
+dradd_status rmsnorm_fp8_fwd_with_config(uint8_t* out_q, float* scale, const dradd_bf16* x,
+                                         const dradd_bf16* weight, float eps, int64_t n_rows, int64_t hidden,
+                                         cudaStream_t stream, const dradd_launch_cfg* cfg)
+{
+    if (!cfg)
+        return DRADD_ERR_NULL_PTR;
+    return run(dradd::kOutE4m3, false, nullptr, reinterpret_cast<int8_t*>(out_q), scale, nullptr, x, nullptr,
+               weight, eps, n_rows, hidden, stream, cfg);
 }
 
 dradd_status rmsnorm_fwd(dradd_bf16* out, const dradd_bf16* x, const dradd_bf16* weight, float eps,
                          int64_t n_rows, int64_t hidden, cudaStream_t stream)
 {
-    return run(false, false, out, nullptr, nullptr, nullptr, x, nullptr, weight, eps, n_rows, hidden, stream,
+    return run(dradd::kOutBf16, false, out, nullptr, nullptr, nullptr, x, nullptr, weight, eps, n_rows, hidden, stream,
                nullptr);
 }
 
 dradd_status rmsnorm_quant_fwd(int8_t* out_q, float* scale, const dradd_bf16* x, const dradd_bf16* weight,
                                float eps, int64_t n_rows, int64_t hidden, cudaStream_t stream)
 {
-    return run(true, false, nullptr, out_q, scale, nullptr, x, nullptr, weight, eps, n_rows, hidden, stream,
+    return run(dradd::kOutInt8, false, nullptr, out_q, scale, nullptr, x, nullptr, weight, eps, n_rows, hidden, stream,
                nullptr);
 }
 
@@ -440,7 +481,7 @@ dradd_status rmsnorm_fwd_with_config(dradd_bf16* out, const dradd_bf16* x, const
 {
     if (!cfg)
         return DRADD_ERR_NULL_PTR;
-    return run(false, false, out, nullptr, nullptr, nullptr, x, nullptr, weight, eps, n_rows, hidden, stream,
+    return run(dradd::kOutBf16, false, out, nullptr, nullptr, nullptr, x, nullptr, weight, eps, n_rows, hidden, stream,
                cfg);
 }
 
@@ -450,7 +491,7 @@ dradd_status rmsnorm_quant_fwd_with_config(int8_t* out_q, float* scale, const dr
 {
     if (!cfg)
         return DRADD_ERR_NULL_PTR;
-    return run(true, false, nullptr, out_q, scale, nullptr, x, nullptr, weight, eps, n_rows, hidden, stream,
+    return run(dradd::kOutInt8, false, nullptr, out_q, scale, nullptr, x, nullptr, weight, eps, n_rows, hidden, stream,
                cfg);
 }
 
@@ -506,7 +547,7 @@ dradd_status dradd_bf16_convert_range(dradd_bf16* out, uint64_t first, int64_t c
         return DRADD_ERR_NULL_PTR;
     if (!aligned(out, 2))
         return DRADD_ERR_MISALIGNED;
-    if (method < 0 || method > 2)
+    if (method < 0 || method > 3)
         return DRADD_ERR_BAD_CONFIG;
     return dradd::launch_convert(out, first, count, method, stream) == cudaSuccess ? DRADD_OK
                                                                                   : DRADD_ERR_CUDA;

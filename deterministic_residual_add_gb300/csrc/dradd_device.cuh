@@ -238,6 +238,73 @@ __device__ __forceinline__ uint2 quantize8(const float (&y)[8], const QuantScale
     return u;
 }
 
+// ------------------------------------------------------------ fp8 e4m3 codes
+// cvt.rn.satfinite.e4m3x2.f32 rounds two fp32 values to nearest-even e4m3
+// (OCP e4m3fn: subnormals kept, magnitudes past 448 saturate to 448, NaN to
+// NaN) and packs them, the first operand in the high byte.  Equal to the
+// oracle's encoder on every non-NaN fp32 input (checked exhaustively by the
+// test suite).
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
+{
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Per-row e4m3 scale: scale = RN(amax / 448) and the two multipliers that
+// bracket 1 / scale, c_lo = RN(RN(1/scale) * (1 - 2^-20)) and c_hi likewise
+// with 1 + 2^-20.
+struct E4m3Scale {
+    float scale;
+    float c_lo, c_hi;
+    bool fast;
+};
+
+__device__ __forceinline__ E4m3Scale make_e4m3_scale(float scale)
+{
+    E4m3Scale s;
+    s.scale = scale;
+    s.fast = scale >= 0x1p-126f && scale <= 3.40282347e38f;
+    const float c = s.fast ? __frcp_rn(scale) : 0.0f;
+    s.c_lo = __fmul_rn(c, 1.0f - 0x1p-20f);
+    s.c_hi = __fmul_rn(c, 1.0f + 0x1p-20f);
+    return s;
+}
+
+// Eight e4m3 codes for eight consecutive y values: e4m3(RN(y / scale)).
+// Fast path: with every rounding relative and at most 2^-24, for y >= 0
+// RN(y * c_lo) <= y/scale * (1 - 2^-20 + 3 * 2^-24) < y/scale * (1 - 2^-24)
+// <= RN(y / scale), and likewise RN(y / scale) <= RN(y * c_hi) (mirrored for
+// y < 0; values too small for a relative bound are below half the smallest
+// e4m3 step and give code 0 at both ends).  Rounding to e4m3 is monotone, so when
+// both ends give the same code, RN(y / scale) gives it too.  A block where
+// any pair of ends differs (a quotient within about 2^-20 of an e4m3
+// rounding boundary), or a scale that is not a normal number, is redone with
+// the correctly rounded division; scale == 0 gives code 0.
+__device__ __forceinline__ uint2 quantize8_e4m3(const float (&y)[8], const E4m3Scale& s)
+{
+    uint32_t lo[4], hi[4];
+    bool boundary = !s.fast;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        lo[p] = e4m3x2(__fmul_rn(y[2 * p], s.c_lo), __fmul_rn(y[2 * p + 1], s.c_lo));
+        hi[p] = e4m3x2(__fmul_rn(y[2 * p], s.c_hi), __fmul_rn(y[2 * p + 1], s.c_hi));
+        boundary |= lo[p] != hi[p];
+    }
+    if (boundary) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            lo[p] = s.scale == 0.0f
+                        ? 0u
+                        : e4m3x2(__fdiv_rn(y[2 * p], s.scale), __fdiv_rn(y[2 * p + 1], s.scale));
+        }
+    }
+    uint2 u;
+    u.x = lo[0] | (lo[1] << 16);
+    u.y = lo[2] | (lo[3] << 16);
+    return u;
+}
+
 // ------------------------------------------------------ mbarrier and bulk copy
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {

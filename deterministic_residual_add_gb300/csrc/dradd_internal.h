@@ -10,7 +10,7 @@ namespace dradd {
 
 struct Params {
     uint16_t* out;            // bf16 out (bf16 variant)
-    int8_t* out_q;            // int8 out (quant variant)
+    int8_t* out_q;            // int8 or e4m3 codes (quantised variants)
     float* scale;             // per-row scale (quant variant)
     uint16_t* residual_out;
     const uint16_t* x;
@@ -29,6 +29,9 @@ struct Params {
 };
 
 constexpr unsigned kDeviceStatusTimeout = 1u;
+
+// What a normalised row is stored as.
+enum OutKind : int { kOutBf16 = 0, kOutInt8 = 1, kOutE4m3 = 2 };
 
 using KernelFn = void (*)(Params);
 
@@ -52,14 +55,19 @@ constexpr int staged_min_blocks(int T, int K)
 
 // add = true: residual-add + RMSNorm (reads x and residual, writes
 // residual_out); false: plain RMSNorm of x.
-cudaError_t launch_rows(const Params& p, int K, bool quant, bool add, int grid, int threads, bool serialize,
+cudaError_t launch_rows(const Params& p, int K, int out, bool add, int grid, int threads, bool serialize,
                         cudaStream_t stream);
-cudaError_t launch_staged(const Params& p, int K, bool quant, bool add, int grid, int threads,
+cudaError_t launch_staged(const Params& p, int K, int out, bool add, int grid, int threads,
                           size_t dyn_smem, bool serialize, cudaStream_t stream);
-cudaError_t staged_occupancy(int K, bool quant, bool add, int threads, size_t dyn_smem, int* blocks_per_sm);
+cudaError_t staged_occupancy(int K, int out, bool add, int threads, size_t dyn_smem, int* blocks_per_sm);
 size_t staged_static_smem(int K);
-KernelFn staged_fn_add(int T, int K, bool quant);
-KernelFn staged_fn_norm(int T, int K, bool quant);
+// One function per (mode, output kind), each in its own translation unit.
+KernelFn staged_fn_add_bf16(int T, int K);
+KernelFn staged_fn_add_int8(int T, int K);
+KernelFn staged_fn_add_e4m3(int T, int K);
+KernelFn staged_fn_norm_bf16(int T, int K);
+KernelFn staged_fn_norm_int8(int T, int K);
+KernelFn staged_fn_norm_e4m3(int T, int K);
 cudaError_t launch_residual_add(uint16_t* residual_out, const uint16_t* x, const uint16_t* residual,
                                 int64_t n_vec, int sm_count, bool serialize, cudaStream_t stream);
 cudaError_t launch_convert(uint16_t* out, uint64_t first, int64_t count, int method, cudaStream_t stream);

@@ -1,8 +1,8 @@
 // dradd_kernels.cu -- the rows kernels, the residual-add kernel, the
 // conversion test kernel, the device status word and every launcher.  The
-// staged kernels are instantiated in dradd_staged_add.cu and
-// dradd_staged_norm.cu (one translation unit per mode, compiled in
-// parallel) and reached through staged_fn_add / staged_fn_norm.
+// staged kernels are instantiated in dradd_staged_<mode>_<out>.cu (one
+// translation unit per mode and output kind, compiled in parallel) and
+// reached through staged_fn_<mode>_<out>.
 #include <atomic>
 
 #include "dradd_kernels.cuh"
@@ -60,6 +60,8 @@ __global__ void convert_kernel(uint16_t* out, uint64_t first, int64_t count, int
             b = rne_bits_int(f);
         else if (method == 2)
             b = pack_rne_cvt(f, f) & 0xFFFFu;
+        else if (method == 3)
+            b = e4m3x2(f, f) & 0xFFu;
         else
             b = pack_rne(f, f) & 0xFFFFu;
         out[i] = static_cast<uint16_t>(b);
@@ -69,24 +71,36 @@ __global__ void convert_kernel(uint16_t* out, uint64_t first, int64_t count, int
 // ------------------------------------------------------------------ launchers
 namespace {
 
-KernelFn rows_fn(int K, bool quant, bool add)
+KernelFn rows_fn(int K, int out, bool add)
 {
-#define DRADD_ROWS(KK)                                                                   \
-    return add ? (quant ? rows_kernel<KK, true, true> : rows_kernel<KK, false, true>)    \
-               : (quant ? rows_kernel<KK, true, false> : rows_kernel<KK, false, false>)
+#define DRADD_ROWS_OUT(KK, OO) \
+    return add ? rows_kernel<KK, OO, true> : rows_kernel<KK, OO, false>
+#define DRADD_ROWS(KK)                                                  \
+    switch (out) {                                                      \
+    case kOutBf16: DRADD_ROWS_OUT(KK, kOutBf16);                        \
+    case kOutInt8: DRADD_ROWS_OUT(KK, kOutInt8);                        \
+    case kOutE4m3: DRADD_ROWS_OUT(KK, kOutE4m3);                        \
+    default: return nullptr;                                            \
+    }
     switch (K) {
-    case 1: DRADD_ROWS(1);
-    case 2: DRADD_ROWS(2);
-    case 4: DRADD_ROWS(4);
-    case 8: DRADD_ROWS(8);
+    case 1: DRADD_ROWS(1)
+    case 2: DRADD_ROWS(2)
+    case 4: DRADD_ROWS(4)
+    case 8: DRADD_ROWS(8)
     default: return nullptr;
     }
 #undef DRADD_ROWS
+#undef DRADD_ROWS_OUT
 }
 
-KernelFn staged_fn(int T, int K, bool quant, bool add)
+KernelFn staged_fn(int T, int K, int out, bool add)
 {
-    return add ? staged_fn_add(T, K, quant) : staged_fn_norm(T, K, quant);
+    switch (out) {
+    case kOutBf16: return add ? staged_fn_add_bf16(T, K) : staged_fn_norm_bf16(T, K);
+    case kOutInt8: return add ? staged_fn_add_int8(T, K) : staged_fn_norm_int8(T, K);
+    case kOutE4m3: return add ? staged_fn_add_e4m3(T, K) : staged_fn_norm_e4m3(T, K);
+    default: return nullptr;
+    }
 }
 
 int log2i(int v)
@@ -97,16 +111,16 @@ int log2i(int v)
     return l;
 }
 
-// One bit per staged kernel: (add, T = 32..1024, K = 1..8, quant).
-int staged_index(int T, int K, bool quant, bool add)
+// One bit per staged kernel: (add, out = 0..2, T = 32..1024, K = 1..8).
+int staged_index(int T, int K, int out, bool add)
 {
-    return (add ? 48 : 0) + (log2i(T) - 5) * 8 + log2i(K) * 2 + (quant ? 1 : 0);
+    return ((add ? 3 : 0) + out) * 24 + (log2i(T) - 5) * 4 + log2i(K);
 }
 
 constexpr int kMaxDevices = 64;
 // Per device: bit k of word k / 64 set once staged kernel k has been allowed
-// its full dynamic shared memory.
-std::atomic<uint64_t> g_smem_attr_done[kMaxDevices][2];
+// its full dynamic shared memory (6 x 24 kernels).
+std::atomic<uint64_t> g_smem_attr_done[kMaxDevices][3];
 std::atomic<unsigned*> g_status_ptr[kMaxDevices];
 
 cudaError_t ensure_smem_attr(KernelFn fn, int index, int dev)
@@ -178,41 +192,41 @@ static cudaError_t launch(void (*fn)(Args...), int grid, int threads, size_t dyn
     return cudaLaunchKernelEx(&cfg, fn, args...);
 }
 
-cudaError_t launch_rows(const Params& p, int K, bool quant, bool add, int grid, int threads, bool serialize,
+cudaError_t launch_rows(const Params& p, int K, int out, bool add, int grid, int threads, bool serialize,
                         cudaStream_t stream)
 {
-    KernelFn fn = rows_fn(K, quant, add);
+    KernelFn fn = rows_fn(K, out, add);
     if (!fn)
         return cudaErrorInvalidValue;
     return launch(fn, grid, threads, 0, serialize, stream, p);
 }
 
-cudaError_t launch_staged(const Params& p, int K, bool quant, bool add, int grid, int threads,
+cudaError_t launch_staged(const Params& p, int K, int out, bool add, int grid, int threads,
                           size_t dyn_smem, bool serialize, cudaStream_t stream)
 {
-    KernelFn fn = staged_fn(threads, K, quant, add);
+    KernelFn fn = staged_fn(threads, K, out, add);
     if (!fn)
         return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    e = ensure_smem_attr(fn, staged_index(threads, K, quant, add), dev);
+    e = ensure_smem_attr(fn, staged_index(threads, K, out, add), dev);
     if (e != cudaSuccess)
         return e;
     return launch(fn, grid, threads, dyn_smem, serialize, stream, p);
 }
 
-cudaError_t staged_occupancy(int K, bool quant, bool add, int threads, size_t dyn_smem, int* blocks_per_sm)
+cudaError_t staged_occupancy(int K, int out, bool add, int threads, size_t dyn_smem, int* blocks_per_sm)
 {
-    KernelFn fn = staged_fn(threads, K, quant, add);
+    KernelFn fn = staged_fn(threads, K, out, add);
     if (!fn)
         return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    e = ensure_smem_attr(fn, staged_index(threads, K, quant, add), dev);
+    e = ensure_smem_attr(fn, staged_index(threads, K, out, add), dev);
     if (e != cudaSuccess)
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, threads, dyn_smem);

@@ -74,9 +74,10 @@ __device__ __forceinline__ void gather_warps(float (&part)[K], int T, int lane, 
     }
 }
 
-// Row epilogue after inv is known: bf16 store, or the int8 quant (which
-// needs its own CTA-wide max).  Called by every thread of the CTA.
-template <int K, bool QUANT>
+// Row epilogue after inv is known: bf16 store, or the per-row int8 / e4m3
+// codes (which need their own CTA-wide max).  Called by every thread of the
+// CTA.
+template <int K, int OUT>
 __device__ __forceinline__ void finish_row(const Params& p, float (&acc)[K][8], const uint4 (&w)[K],
                                            float inv, int64_t row, bool active, int t, int T, int lane,
                                            int warp_in_row, int nblocks, float* red_max)
@@ -89,7 +90,7 @@ __device__ __forceinline__ void finish_row(const Params& p, float (&acc)[K][8], 
         for (int e = 0; e < 8; ++e)
             acc[j][e] = __fmul_rn(__fmul_rn(acc[j][e], inv), wf[e]);
     }
-    if constexpr (!QUANT) {
+    if constexpr (OUT == kOutBf16) {
         if (active) {
             uint4* orow = reinterpret_cast<uint4*>(p.out + row * p.hidden);
 #pragma unroll
@@ -114,17 +115,27 @@ __device__ __forceinline__ void finish_row(const Params& p, float (&acc)[K][8], 
             __syncthreads();
             m = butterfly_max(red_max[lane & ((T >> 5) - 1)], T >> 5);
         }
-        const float scale = __fdiv_rn(m, 127.0f);
-        const QuantScale qs = make_quant_scale(scale);
+        const float scale = __fdiv_rn(m, OUT == kOutInt8 ? 127.0f : 448.0f);
         if (active) {
             if (t == 0)
                 p.scale[row] = scale;
             uint2* qrow = reinterpret_cast<uint2*>(p.out_q + row * p.hidden);
+            if constexpr (OUT == kOutInt8) {
+                const QuantScale qs = make_quant_scale(scale);
 #pragma unroll
-            for (int j = 0; j < K; ++j) {
-                const int b = t + j * T;
-                if (b < nblocks)
-                    st_stream(qrow + b, quantize8(acc[j], qs));
+                for (int j = 0; j < K; ++j) {
+                    const int b = t + j * T;
+                    if (b < nblocks)
+                        st_stream(qrow + b, quantize8(acc[j], qs));
+                }
+            } else {
+                const E4m3Scale qs = make_e4m3_scale(scale);
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    const int b = t + j * T;
+                    if (b < nblocks)
+                        st_stream(qrow + b, quantize8_e4m3(acc[j], qs));
+                }
             }
         }
     }
@@ -178,7 +189,7 @@ __device__ __forceinline__ void record_timeout(const Params& p)
 }
 
 // ---------------------------------------------------------------- rows_kernel
-template <int K, bool QUANT, bool ADD>
+template <int K, int OUT, bool ADD>
 __global__ void __launch_bounds__(max_threads_for(K)) rows_kernel(const Params p)
 {
     __shared__ float s_sum[2][32 * K];
@@ -226,7 +237,7 @@ __global__ void __launch_bounds__(max_threads_for(K)) rows_kernel(const Params p
             __syncthreads();
         gather_warps<K>(part, T, lane, red);
         const float inv = inv_rms(fold_k<K>(part), p.hidden, p.inv_hidden, p.eps);
-        finish_row<K, QUANT>(p, acc, w, inv, row, active, t, T, lane, warp_in_row, nblocks,
+        finish_row<K, OUT>(p, acc, w, inv, row, active, t, T, lane, warp_in_row, nblocks,
                              &s_max[buf][r_local * warps_per_row]);
         buf ^= 1;
     }
@@ -237,7 +248,7 @@ __global__ void __launch_bounds__(max_threads_for(K)) rows_kernel(const Params p
 // every (T, K) pair gets its own register budget (staged_min_blocks) and the
 // reduction widths fold away.  A stage holds one row of x, then (with ADD)
 // one row of residual.
-template <int T, int K, bool QUANT, bool ADD>
+template <int T, int K, int OUT, bool ADD>
 __global__ void __launch_bounds__(T, staged_min_blocks(T, K)) staged_kernel(const Params p)
 {
     static_assert(T >= 32 && T <= 1024 && (T & (T - 1)) == 0, "T: a power of two, 32..1024");
@@ -344,7 +355,7 @@ __global__ void __launch_bounds__(T, staged_min_blocks(T, K)) staged_kernel(cons
         }
         gather_warps<K>(part, T, lane, red);
         const float inv = inv_rms(fold_k<K>(part), p.hidden, p.inv_hidden, p.eps);
-        finish_row<K, QUANT>(p, acc, w, inv, row, true, tid, T, lane, warp_in_row, nblocks,
+        finish_row<K, OUT>(p, acc, w, inv, row, true, tid, T, lane, warp_in_row, nblocks,
                              &s_max[buf][0]);
         buf ^= 1;
         if (++s == stages) {
@@ -356,39 +367,38 @@ __global__ void __launch_bounds__(T, staged_min_blocks(T, K)) staged_kernel(cons
 
 // ------------------------------------------------------- staged kernel table
 // Staged kernels exist for T = 32..1024 and K in {1, 2, 4, 8} with
-// T <= max_threads_for(K).
-
-template <int T, int K, bool ADD>
-KernelFn staged_pick(bool quant)
+// T <= max_threads_for(K); each translation unit instantiates one (OUT, ADD).
+template <int T, int K, int OUT, bool ADD>
+KernelFn staged_pick()
 {
     if constexpr (T <= max_threads_for(K))
-        return quant ? staged_kernel<T, K, true, ADD> : staged_kernel<T, K, false, ADD>;
+        return staged_kernel<T, K, OUT, ADD>;
     else
         return nullptr;
 }
 
-template <int T, bool ADD>
-KernelFn staged_by_k(int K, bool quant)
+template <int T, int OUT, bool ADD>
+KernelFn staged_by_k(int K)
 {
     switch (K) {
-    case 1: return staged_pick<T, 1, ADD>(quant);
-    case 2: return staged_pick<T, 2, ADD>(quant);
-    case 4: return staged_pick<T, 4, ADD>(quant);
-    case 8: return staged_pick<T, 8, ADD>(quant);
+    case 1: return staged_pick<T, 1, OUT, ADD>();
+    case 2: return staged_pick<T, 2, OUT, ADD>();
+    case 4: return staged_pick<T, 4, OUT, ADD>();
+    case 8: return staged_pick<T, 8, OUT, ADD>();
     default: return nullptr;
     }
 }
 
-template <bool ADD>
-KernelFn staged_table(int T, int K, bool quant)
+template <int OUT, bool ADD>
+KernelFn staged_table(int T, int K)
 {
     switch (T) {
-    case 32: return staged_by_k<32, ADD>(K, quant);
-    case 64: return staged_by_k<64, ADD>(K, quant);
-    case 128: return staged_by_k<128, ADD>(K, quant);
-    case 256: return staged_by_k<256, ADD>(K, quant);
-    case 512: return staged_by_k<512, ADD>(K, quant);
-    case 1024: return staged_by_k<1024, ADD>(K, quant);
+    case 32: return staged_by_k<32, OUT, ADD>(K);
+    case 64: return staged_by_k<64, OUT, ADD>(K);
+    case 128: return staged_by_k<128, OUT, ADD>(K);
+    case 256: return staged_by_k<256, OUT, ADD>(K);
+    case 512: return staged_by_k<512, OUT, ADD>(K);
+    case 1024: return staged_by_k<1024, OUT, ADD>(K);
     default: return nullptr;
     }
 }

@@ -1,0 +1,10 @@
+// dradd_staged_norm_bf16.cu -- staged kernels of the plain RMSNorm (no residual)
+// forward with bf16 out; one translation unit per (mode, output) so
+// that the build compiles them in parallel.
+#include "dradd_kernels.cuh"
+
+namespace dradd {
+
+KernelFn staged_fn_norm_bf16(int T, int K) { return staged_table<kOutBf16, false>(T, K); }
+
+}  // namespace dradd

@@ -185,7 +185,7 @@ dradd_status add_rmsnorm_quant_fwd_with_config(int8_t* out_q, float* scale,
  * dradd_resolve_config -- fill the automatic choices of *cfg for a call of
  * the given shape and operation, as the entry points would, and validate
  * the explicit ones.  `op` is one of DRADD_OP_* (0 and 1 are the bf16 and
- * int8 residual-add forms, 2 and 3 plain RMSNorm).  grid_ctas is filled from
+ * int8 residual-add forms, 2 and 3 plain RMSNorm, 4 and 5 the fp8 forms).  grid_ctas is filled from
  * `sm_count` (pass 0 to query the current device); for the staged variant
  * the entry points size the grid with the CUDA occupancy calculator instead.
  * Does no GPU work when sm_count > 0.
@@ -194,7 +194,9 @@ enum {
     DRADD_OP_ADD_RMSNORM = 0,
     DRADD_OP_ADD_RMSNORM_QUANT = 1,
     DRADD_OP_RMSNORM = 2,
-    DRADD_OP_RMSNORM_QUANT = 3
+    DRADD_OP_RMSNORM_QUANT = 3,
+    DRADD_OP_ADD_RMSNORM_FP8 = 4,
+    DRADD_OP_RMSNORM_FP8 = 5
 };
 
 dradd_status dradd_resolve_config(int64_t n_rows, int64_t hidden, int op, int sm_count,
@@ -235,6 +237,44 @@ dradd_status rmsnorm_quant_fwd_with_config(int8_t* out_q, float* scale, const dr
                                            const dradd_launch_cfg* cfg);
 
 /*
+ * add_rmsnorm_fp8_fwd -- the residual-add + RMSNorm forward with the
+ * normalised row emitted as per-row scaled fp8 e4m3 codes (OCP "e4m3fn":
+ * 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no infinities,
+ * largest finite 448).  Page: ROCm/aiter issue #5151, "Cost of fixing": the
+ * quantised configurations take out through a scaled cast to int8, fp8 or
+ * fp4 instead of the bf16 store.  With y as in add_rmsnorm_quant_fwd:
+ *   amax       = max over the row of |y|                 (exact)
+ *   scale[r]   = amax / 448                              (fp32, rounded once)
+ *   out_q[r,i] = e4m3(y_i / scale[r]): the quotient a correctly rounded fp32
+ *                division, then rounded to the nearest e4m3 value, ties to
+ *                the even code, magnitudes past 448 saturating to 448;
+ *                scale[r] == 0 gives code 0.
+ *   out_q         [n_rows x hidden] e4m3 codes (uint8), written (16-byte
+ *                 aligned); code * scale ~ y
+ *   scale, residual_out and the other arguments as in add_rmsnorm_quant_fwd.
+ */
+dradd_status add_rmsnorm_fp8_fwd(uint8_t* out_q, float* scale, dradd_bf16* residual_out,
+                                 const dradd_bf16* x, const dradd_bf16* residual,
+                                 const dradd_bf16* weight, float eps, int64_t n_rows,
+                                 int64_t hidden, cudaStream_t stream);
+
+dradd_status add_rmsnorm_fp8_fwd_with_config(uint8_t* out_q, float* scale, dradd_bf16* residual_out,
+                                             const dradd_bf16* x, const dradd_bf16* residual,
+                                             const dradd_bf16* weight, float eps, int64_t n_rows,
+                                             int64_t hidden, cudaStream_t stream,
+                                             const dradd_launch_cfg* cfg);
+
+/* rmsnorm_fp8_fwd -- plain RMSNorm (no residual) with the same e4m3 output. */
+dradd_status rmsnorm_fp8_fwd(uint8_t* out_q, float* scale, const dradd_bf16* x,
+                             const dradd_bf16* weight, float eps, int64_t n_rows, int64_t hidden,
+                             cudaStream_t stream);
+
+dradd_status rmsnorm_fp8_fwd_with_config(uint8_t* out_q, float* scale, const dradd_bf16* x,
+                                         const dradd_bf16* weight, float eps, int64_t n_rows,
+                                         int64_t hidden, cudaStream_t stream,
+                                         const dradd_launch_cfg* cfg);
+
+/*
  * residual_add_fwd -- the residual update alone, the other half of the
  * page's reference(): residual_out = bf16_rne(fp32(x) + fp32(residual)),
  * element by element, bit-identical to add_rmsnorm_fwd's residual_out (the
@@ -259,10 +299,11 @@ dradd_status dradd_device_status(cudaStream_t stream, int clear);
 
 /*
  * dradd_bf16_convert_range -- test hook: convert the `count` fp32 bit
- * patterns first, first+1, ... (mod 2^32) to bf16 on the device, with
- * method 0 = the conversion the kernels use, 1 = integer round-half-even
- * bit arithmetic, 2 = the hardware cvt.rn.bf16x2.f32 instruction.
- * `out` is a device array of `count` dradd_bf16 (2-byte aligned).
+ * patterns first, first+1, ... (mod 2^32) on the device, with method
+ * 0 = the bf16 conversion the kernels use, 1 = integer round-half-even bit
+ * arithmetic to bf16, 2 = the hardware cvt.rn.bf16x2.f32 instruction,
+ * 3 = the e4m3 conversion the fp8 kernels use (code in the low byte).
+ * `out` is a device array of `count` 16-bit words (2-byte aligned).
  */
 dradd_status dradd_bf16_convert_range(dradd_bf16* out, uint64_t first, int64_t count,
                                       int method, cudaStream_t stream);

@@ -300,10 +300,23 @@ static double e4m3_magnitude(unsigned c)
     return ldexp(1.0 + m / 8.0, (int)e - 7);
 }
 
+/* Magnitudes of the finite codes 0x00..0x7E, which increase with the code. */
+static double e4m3_table[0x7F];
+static int e4m3_table_ready;
+
+static void e4m3_fill_table(void)
+{
+    if (e4m3_table_ready)
+        return;
+    for (unsigned c = 0; c < 0x7Fu; ++c)
+        e4m3_table[c] = e4m3_magnitude(c);
+    e4m3_table_ready = 1;  /* every caller writes the same values */
+}
+
 /* Round to the nearest e4m3 value, ties to the even code (last mantissa bit
  * 0); magnitudes above 448 saturate to 448 ("satfinite"); NaN gives 0x7F
- * with the sign kept.  Found by comparing |f| with the finite magnitudes in
- * order (the codes 0x00..0x7E increase with their magnitude). */
+ * with the sign kept.  |f| is placed between two consecutive finite
+ * magnitudes by binary search and the nearer one is taken. */
 uint8_t oracle_e4m3_rne(float f)
 {
     uint8_t sign = (uint8_t)((bits_from_f32(f) >> 24) & 0x80u);
@@ -312,10 +325,16 @@ uint8_t oracle_e4m3_rne(float f)
     double a = fabs((double)f);
     if (a >= (double)E4M3_MAX)
         return (uint8_t)(sign | 0x7Eu);
-    unsigned lo = 0;  /* largest code with magnitude <= a */
-    while (lo < 0x7Eu && e4m3_magnitude(lo + 1) <= a)
-        ++lo;
-    double d_lo = a - e4m3_magnitude(lo), d_hi = e4m3_magnitude(lo + 1) - a;
+    e4m3_fill_table();
+    unsigned lo = 0, hi = 0x7Eu;  /* largest code with magnitude <= a lies in [lo, hi) */
+    while (hi - lo > 1) {
+        unsigned mid = (lo + hi) / 2;
+        if (e4m3_table[mid] <= a)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    double d_lo = a - e4m3_table[lo], d_hi = e4m3_table[lo + 1] - a;
     unsigned c = lo;
     if (d_hi < d_lo || (d_hi == d_lo && (lo & 1u)))
         c = lo + 1;

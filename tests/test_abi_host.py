@@ -104,7 +104,7 @@ def test_convert_hook_argument_errors(L):
     assert L.dradd_bf16_convert_range(None, 0, 16, 0, None) == 1
     assert L.dradd_bf16_convert_range(OUT, 0, -1, 0, None) == 2
     assert L.dradd_bf16_convert_range(OUT + 1, 0, 16, 0, None) == 4
-    assert L.dradd_bf16_convert_range(OUT, 0, 16, 3, None) == 9
+    assert L.dradd_bf16_convert_range(OUT, 0, 16, 4, None) == 9
     assert L.dradd_bf16_convert_range(OUT, 0, 0, 0, None) == 0
 
 
@@ -210,9 +210,23 @@ def test_rmsnorm_quant_and_residual_add_errors(L):
 
 def test_resolve_op_codes(L):
     c = dr.LaunchConfig()._c()
-    assert L.dradd_resolve_config(16, 1024, 4, 152, ctypes.byref(c)) == 9
+    assert L.dradd_resolve_config(16, 1024, 6, 152, ctypes.byref(c)) == 9
     plain = dr.resolve_config(4096, 16384, add=False)
     assert plain.variant == dr.VARIANT_STAGED and plain.stages == 4 and plain.threads_per_row == 512
     # a plain-RMSNorm stage holds only x, so 32768-wide rows fit two stages
     c = dr.resolve_config(16, 32768, add=False, config=dr.LaunchConfig(variant=2, stages=2))
     assert c.stages == 2
+
+
+def test_fp8_argument_errors(L):
+    assert L.add_rmsnorm_fp8_fwd(0, SC, RO, X, RES, W, 1e-6, 4, 1024, None) == 1
+    assert L.add_rmsnorm_fp8_fwd(Q + 4, SC, RO, X, RES, W, 1e-6, 4, 1024, None) == 4
+    assert L.add_rmsnorm_fp8_fwd(Q, SC, RO, X, RES, W, float("nan"), 4, 1024, None) == 5
+    assert L.add_rmsnorm_fp8_fwd(RES, SC, RO, X, RES, W, 1e-6, 4, 1024, None) == 6
+    assert L.rmsnorm_fp8_fwd(Q, 0, X, W, 1e-6, 4, 1024, None) == 1
+    assert L.rmsnorm_fp8_fwd(Q, SC, X, W, 1e-6, 0, 1024, None) == 0
+    assert L.rmsnorm_fp8_fwd_with_config(Q, SC, X, W, 1e-6, 4, 1024, None, None) == 1
+    c = dr.resolve_config(4096, 4096, add=True, fp8=True)
+    assert c.variant == dr.VARIANT_STAGED and c.stages == 2
+    c = dr.resolve_config(4096, 4096, add=False, fp8=True)
+    assert c.stages == 1

@@ -53,7 +53,9 @@ MUTANTS = {
     "e4m3_scale_480": ("float s = amax / E4M3_MAX;", "float s = amax / 480.0f;"),
     "e4m3_ties_to_odd": ("if (d_hi < d_lo || (d_hi == d_lo && (lo & 1u)))",
                          "if (d_hi < d_lo || (d_hi == d_lo && !(lo & 1u)))"),
-    "e4m3_no_saturation": ("if (a >= (double)E4M3_MAX)", "if (a >= 1e30)"),
+    "e4m3_subnormal_exponent": ("return ldexp((double)m, -9);", "return ldexp((double)m, -10);"),
+    "e4m3_exponent_bias_8": ("return ldexp(1.0 + m / 8.0, (int)e - 7);",
+                             "return ldexp(1.0 + m / 8.0, (int)e - 8);"),
     "e4m3_quotient_by_reciprocal": ("q_out[i] = s != 0.0f ? oracle_e4m3_rne(y[i] / s) : 0;",
                                     "q_out[i] = s != 0.0f ? oracle_e4m3_rne(y[i] * (1.0f / s)) : 0;"),
 }
