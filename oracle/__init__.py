@@ -134,6 +134,13 @@ class Oracle:
         L.oracle_rmsnorm_e4m3_fwd.restype = ctypes.c_int
         L.oracle_rmsnorm_e4m3_fwd.argtypes = [_u8p, _f32p, _u16p, _u16p, _u16p, _u16p, ctypes.c_float,
                                               _i64, _i64]
+        L.oracle_e2m1_rne.restype = ctypes.c_uint8
+        L.oracle_e2m1_rne.argtypes = [ctypes.c_float]
+        L.oracle_e2m1_convert_array.restype = ctypes.c_int
+        L.oracle_e2m1_convert_array.argtypes = [_u8p, _f32p, _i64]
+        L.oracle_rmsnorm_e2m1_fwd.restype = ctypes.c_int
+        L.oracle_rmsnorm_e2m1_fwd.argtypes = [_u8p, _f32p, _u16p, _u16p, _u16p, _u16p, ctypes.c_float,
+                                              _i64, _i64]
         L.oracle_abi_version.restype = ctypes.c_int
 
     # ---- conversions -------------------------------------------------
@@ -324,6 +331,44 @@ class Oracle:
         for rc in _split_rows(run, n_rows, threads):
             if rc != 0:
                 raise RuntimeError(f"oracle_rmsnorm_e4m3_fwd failed with {rc}")
+        return (q, scale) if r is None else (q, scale, ro)
+
+
+    def e2m1_scalar(self, f: float) -> int:
+        return int(self._L.oracle_e2m1_rne(ctypes.c_float(f)))
+
+    def e2m1_convert(self, f32: np.ndarray) -> np.ndarray:
+        src = np.ascontiguousarray(f32, dtype=np.float32)
+        dst = np.empty(src.shape, dtype=np.uint8)
+        assert self._L.oracle_e2m1_convert_array(_ptr(dst, _u8p), _ptr(src, _f32p), src.size) == 0
+        return dst
+
+    def rmsnorm_fp4_fwd(self, x, weight, eps: float, residual=None, threads: int = 1):
+        """Per-row e2m1 out, two codes per byte: (out_q [n, h/2] uint8, scale)
+        for plain RMSNorm, or (out_q, scale, residual_out) with a residual."""
+        x, weight = _as_u16(x), _as_u16(weight)
+        hidden = x.shape[-1]
+        n_rows = x.size // hidden if hidden else 0
+        r = _as_u16(residual) if residual is not None else None
+        q = np.empty((n_rows, hidden // 2), dtype=np.uint8)
+        scale = np.empty(n_rows, dtype=np.float32)
+        ro = np.empty_like(x) if r is not None else None
+        x2 = x.reshape(n_rows, hidden)
+        r2 = r.reshape(n_rows, hidden) if r is not None else None
+        ro2 = ro.reshape(n_rows, hidden) if r is not None else None
+
+        def run(lo: int, hi: int) -> int:
+            if hi <= lo:
+                return 0
+            return self._L.oracle_rmsnorm_e2m1_fwd(
+                _ptr(q[lo:hi], _u8p), _ptr(scale[lo:hi], _f32p),
+                _ptr(ro2[lo:hi] if r is not None else None, _u16p), _ptr(x2[lo:hi], _u16p),
+                _ptr(r2[lo:hi] if r is not None else None, _u16p), _ptr(weight, _u16p),
+                ctypes.c_float(eps), hi - lo, hidden)
+
+        for rc in _split_rows(run, n_rows, threads):
+            if rc != 0:
+                raise RuntimeError(f"oracle_rmsnorm_e2m1_fwd failed with {rc}")
         return (q, scale) if r is None else (q, scale, ro)
 
 

@@ -1,7 +1,8 @@
 /*
  * dradd_oracle.c -- plain, slow, single-threaded CPU oracle for the fused
- * residual-add + RMSNorm forward and its int8-quant variant, and for its two
- * halves: plain RMSNorm (no residual) and the residual update alone.
+ * residual-add + RMSNorm forward and its quantised variants (int8, fp8 e4m3,
+ * fp4 e2m1), and for its two halves: plain RMSNorm (no residual) and the
+ * residual update alone.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
  * calls this file: only tests, the smoke check and the bench's CPU-baseline
@@ -392,6 +393,92 @@ int oracle_e4m3_convert_array(uint8_t* dst, const float* src, int64_t n)
         return ORACLE_ERR_ARG;
     for (int64_t i = 0; i < n; ++i)
         dst[i] = oracle_e4m3_rne(src[i]);
+    return ORACLE_OK;
+}
+
+/* ---- fp4 e2m1 (1 sign, 2 exponent bits with bias 1, 1 mantissa bit; the
+ * magnitudes of codes 0..7 are 0, 0.5, 1, 1.5, 2, 3, 4, 6; no infinities or
+ * NaN).  Two codes per byte: the even element in the low nibble. */
+#define E2M1_MAX 6.0f
+
+static const double e2m1_magnitudes[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+/* Nearest e2m1 code, ties to the even code, magnitudes past 6 saturating to
+ * 6; the sign bit (bit 3) follows the sign of f; NaN gives 0 (the format has
+ * no NaN; outside this library's use). */
+uint8_t oracle_e2m1_rne(float f)
+{
+    if (isnan(f))
+        return 0;
+    uint8_t sign = (uint8_t)((bits_from_f32(f) >> 28) & 0x8u);
+    double a = fabs((double)f);
+    if (a >= (double)E2M1_MAX)
+        return (uint8_t)(sign | 7u);
+    unsigned lo = 0;
+    while (lo < 7u && e2m1_magnitudes[lo + 1] <= a)
+        ++lo;
+    double d_lo = a - e2m1_magnitudes[lo], d_hi = e2m1_magnitudes[lo + 1] - a;
+    unsigned c = lo;
+    if (d_hi < d_lo || (d_hi == d_lo && (lo & 1u)))
+        c = lo + 1;
+    return (uint8_t)(sign | c);
+}
+
+/* Per-row symmetric e2m1 codes of y, packed two per byte:
+ * scale = amax / 6, code = e2m1_rne(y / scale); scale == 0 gives code 0. */
+static void quantize_row_e2m1(uint8_t* q_out, float* scale_out, const float* y, int64_t hidden)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < hidden; ++i)
+        amax = fmaxf(amax, fabsf(y[i]));
+    float s = amax / E2M1_MAX;
+    *scale_out = s;
+    for (int64_t i = 0; i < hidden; i += 2) {
+        uint8_t c0 = s != 0.0f ? oracle_e2m1_rne(y[i] / s) : 0;
+        uint8_t c1 = s != 0.0f ? oracle_e2m1_rne(y[i + 1] / s) : 0;
+        q_out[i / 2] = (uint8_t)(c0 | (c1 << 4));
+    }
+}
+
+/* Residual-add + RMSNorm (or plain, residual == NULL) with per-row e2m1
+ * out: out_q holds n_rows x hidden / 2 bytes.  hidden must be even. */
+int oracle_rmsnorm_e2m1_fwd(uint8_t* out_q, float* scale, uint16_t* residual_out,
+                            const uint16_t* x, const uint16_t* residual,
+                            const uint16_t* weight, float eps, int64_t n_rows, int64_t hidden)
+{
+    if (n_rows < 0 || hidden <= 0 || hidden % 2)
+        return ORACLE_ERR_ARG;
+    if (n_rows == 0)
+        return ORACLE_OK;
+    if (!out_q || !scale || !x || !weight || (residual && !residual_out))
+        return ORACLE_ERR_ARG;
+    int64_t padded = next_pow2(hidden);
+    float* acc = (float*)malloc((size_t)hidden * sizeof(float));
+    float* sq = (float*)calloc((size_t)padded, sizeof(float));
+    float* y = (float*)malloc((size_t)hidden * sizeof(float));
+    if (!acc || !sq || !y) {
+        free(acc); free(sq); free(y);
+        return ORACLE_ERR_NOMEM;
+    }
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t base = r * hidden;
+        add_rmsnorm_row(y, residual ? residual_out + base : NULL, acc, sq, x + base,
+                        residual ? residual + base : NULL, weight, eps, hidden, padded,
+                        ORACLE_STORE_RNE, NULL, NULL);
+        quantize_row_e2m1(out_q + base / 2, scale + r, y, hidden);
+    }
+    free(acc); free(sq); free(y);
+    return ORACLE_OK;
+}
+
+/* Convert n fp32 values to e2m1 codes, one per byte (for the conversion
+ * checks). */
+int oracle_e2m1_convert_array(uint8_t* dst, const float* src, int64_t n)
+{
+    if ((!dst || !src) && n > 0)
+        return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = oracle_e2m1_rne(src[i]);
     return ORACLE_OK;
 }
 

@@ -453,6 +453,65 @@ def pin_fp8_rows(o, seed: int = 31):
         assert list(res[0][0]) == codes and res[1][0] == sc, i
 
 
+# ---------------------------------------------------------------- fp4 e2m1
+def pin_e2m1_encoder(o):
+    """Every interval and every tie of the eight e2m1 magnitudes, by hand:
+    ties go to the even code; past 6 saturates; the sign is bit 3."""
+    table = [(0.0, 0x0), (0.2, 0x0), (0.25, 0x0), (0.3, 0x1), (0.5, 0x1), (0.75, 0x2), (0.8, 0x2),
+             (1.0, 0x2), (1.25, 0x2), (1.3, 0x3), (1.5, 0x3), (1.75, 0x4), (2.0, 0x4), (2.5, 0x4),
+             (2.6, 0x5), (3.0, 0x5), (3.5, 0x6), (4.0, 0x6), (5.0, 0x6), (5.1, 0x7), (6.0, 0x7),
+             (7.0, 0x7), (1e30, 0x7), (-0.0, 0x8), (-0.75, 0xA), (-6.0, 0xF), (-100.0, 0xF)]
+    for f, code in table:
+        assert o.e2m1_scalar(f) == code, (f, code, o.e2m1_scalar(f))
+    for c in range(16):
+        v = float(refs.E2M1[c & 7]) * (-1.0 if c & 8 else 1.0)
+        if c == 8:
+            v = -0.0
+        assert o.e2m1_scalar(v) == c, c
+    f = np.linspace(-7, 7, 20001, dtype=np.float32)
+    got = o.e2m1_convert(f)
+    exp = np.array([refs.e2m1_rne_exact(refs.frac(v), bool(np.float32(v).view(np.uint32) >> 31)) for v in f])
+    assert np.array_equal(got, exp)
+
+
+def pin_fp4_rows(o, seed: int = 37):
+    """Per-row e2m1 out: 6 reached on every nonzero row, dequantisation within
+    half an e2m1 step of fp64 (plus the fp32 path's error), exact-rational
+    rows, zero rows, and residual_out equal to the bf16 variant's."""
+    g = inputs.generator(seed)
+    mags = np.array([float(v) for v in refs.E2M1])
+    for n, h, with_res in [(8, 1024, True), (4, 24, False), (2, 16384, True)]:
+        x = inputs.normal_bf16(g, (n, h), 0.0, 1.0)
+        r = inputs.normal_bf16(g, (n, h), 0.0, 2.0) if with_res else None
+        w = inputs.normal_bf16(g, (h,), 1.0, 0.1)
+        res = o.rmsnorm_fp4_fwd(x, w, 1e-6, residual=r)
+        codes = refs.unpack_fp4(res[0])
+        scale = res[1].astype(np.float64)
+        if with_res:
+            _, ro_b = o.add_rmsnorm_fwd(x, r, w, 1e-6)
+            assert np.array_equal(res[2], ro_b)
+        assert np.all((codes & 7).max(axis=1) == 7)
+        val = mags[codes & 7] * np.where(codes & 8, -1.0, 1.0) * scale[:, None]
+        y64, _ = refs.add_rmsnorm_f64(x, r if with_res else torch.zeros_like(x), w, 1e-6)
+        # e2m1 steps are 0.5 up to 2, 1 up to 4 and 2 up to 6: half the step
+        # of the interval holding the larger of the value and its code
+        m = np.maximum(np.abs(val), np.abs(y64)) / scale[:, None]
+        half = np.where(m > 4, 1.0, np.where(m > 2, 0.5, 0.25))
+        assert np.all(np.abs(val - y64) <= half * scale[:, None] * (1 + 1e-6) + np.abs(y64) * 2.0 ** -20)
+    z = np.zeros((2, 64), np.uint16)
+    q, scale = o.rmsnorm_fp4_fwd(z, np.full(64, 0x3F80, np.uint16), 1e-6)
+    assert np.all(q == 0) and np.all(scale == 0)
+    for i in range(6):
+        hh = (8, 16)[i % 2]
+        xb = refs.u16(inputs.normal_bf16(g, (1, hh), 0.0, 1.0))
+        rb = refs.u16(inputs.normal_bf16(g, (1, hh), 0.0, 1.0))
+        wb = refs.u16(inputs.normal_bf16(g, (hh,), 1.0, 0.3))
+        plain = i % 3 == 0
+        res = o.rmsnorm_fp4_fwd(xb, wb, 1e-6, residual=None if plain else rb)
+        codes, sc = refs.fp4_row_exact(xb[0], None if plain else rb[0], wb, 1e-6)
+        assert list(refs.unpack_fp4(res[0])[0]) == codes and res[1][0] == sc, i
+
+
 FAST_PINS = [
     pin_rne_edge_table,
     pin_tree_worked_examples,
@@ -471,4 +530,6 @@ FAST_PINS = [
     pin_residual_add,
     pin_e4m3_encoder,
     pin_fp8_rows,
+    pin_e2m1_encoder,
+    pin_fp4_rows,
 ]

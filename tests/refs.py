@@ -263,6 +263,43 @@ def e4m3_row_exact(x_bits, r_bits, w_bits, eps: float, quant_op: str = "div"):
     return codes, scale
 
 
+E2M1 = [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2), Fraction(2), Fraction(3),
+        Fraction(4), Fraction(6)]
+
+
+def e2m1_rne_exact(q: Fraction, negative_zero: bool = False) -> int:
+    """Nearest e2m1 code to a rational, ties to the even code, saturating at
+    6; bit 3 is the sign."""
+    neg = q < 0 or (q == 0 and negative_zero)
+    a = abs(q)
+    code = 7 if a >= 6 else min(range(8), key=lambda c: (abs(E2M1[c] - a), c & 1))
+    return code | (8 if neg else 0)
+
+
+def fp4_row_exact(x_bits, r_bits, w_bits, eps: float):
+    """Exact-rational e2m1 codes (one per element, unpacked) and scale of one
+    row: scale = RN32(amax / 6), code = e2m1 of RN32(y / scale)."""
+    xs = list(x_bits)
+    ys = row_exact(xs, list(r_bits), w_bits, eps)["y"] if r_bits is not None else _plain_row_y(xs, w_bits, eps)
+    amax = max((abs(frac(y)) for y in ys), default=Fraction(0))
+    scale = rn32(amax / 6)
+    if scale == 0:
+        return [0] * len(ys), scale
+    codes = []
+    for y in ys:
+        t = rn32(frac(y) / frac(scale))
+        codes.append(e2m1_rne_exact(frac(t), bool(np.float32(t).view(np.uint32) >> 31)))
+    return codes, scale
+
+
+def unpack_fp4(q: np.ndarray) -> np.ndarray:
+    """[..., h/2] bytes -> [..., h] codes (even element in the low nibble)."""
+    out = np.empty(q.shape[:-1] + (q.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = q & 0xF
+    out[..., 1::2] = q >> 4
+    return out
+
+
 def _plain_row_y(x_bits, w_bits, eps):
     """fp32 y of plain RMSNorm (acc = x exactly) by exact rational steps."""
     acc = [np.float32(bf16_value(np.uint16(b))) for b in x_bits]

@@ -56,6 +56,10 @@ MUTANTS = {
     "e4m3_subnormal_exponent": ("return ldexp((double)m, -9);", "return ldexp((double)m, -10);"),
     "e4m3_exponent_bias_8": ("return ldexp(1.0 + m / 8.0, (int)e - 7);",
                              "return ldexp(1.0 + m / 8.0, (int)e - 8);"),
+    "e2m1_scale_4": ("float s = amax / E2M1_MAX;", "float s = amax / 4.0f;"),
+    "e2m1_ties_to_odd": ("if (d_hi < d_lo || (d_hi == d_lo && (lo & 1u)))\n        c = lo + 1;\n    return (uint8_t)(sign | c);\n}\n\n/* Per-row symmetric e2m1",
+                         "if (d_hi < d_lo || (d_hi == d_lo && !(lo & 1u)))\n        c = lo + 1;\n    return (uint8_t)(sign | c);\n}\n\n/* Per-row symmetric e2m1"),
+    "e2m1_nibbles_swapped": ("q_out[i / 2] = (uint8_t)(c0 | (c1 << 4));", "q_out[i / 2] = (uint8_t)(c1 | (c0 << 4));"),
     "e4m3_quotient_by_reciprocal": ("q_out[i] = s != 0.0f ? oracle_e4m3_rne(y[i] / s) : 0;",
                                     "q_out[i] = s != 0.0f ? oracle_e4m3_rne(y[i] * (1.0f / s)) : 0;"),
 }
