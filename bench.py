@@ -45,8 +45,8 @@ TRAFFIC_FILE = ROOT / "profiles" / "add_rmsnorm_fwd_4096x4096_ncu.md"
 
 # name -> (n_rows, hidden, op, input recipe).  The first is the headline
 # workload; the others are for profiling and context.  op is one of
-# add_rmsnorm, add_rmsnorm_quant, add_rmsnorm_fp8, rmsnorm, rmsnorm_quant,
-# rmsnorm_fp8, residual_add.
+# add_rmsnorm, add_rmsnorm_quant, add_rmsnorm_fp8, add_rmsnorm_fp4, rmsnorm,
+# rmsnorm_quant, rmsnorm_fp8, residual_add.
 WORKLOADS = {
     "4096x4096": (4096, 4096, "add_rmsnorm", "chain4096"),
     "2048x4096": (2048, 4096, "add_rmsnorm", "2048x4096"),
@@ -60,6 +60,8 @@ WORKLOADS = {
     "fp8_2048x16384": (2048, 16384, "add_rmsnorm_fp8", "quant2048x16384"),
     "fp8_4096x4096": (4096, 4096, "add_rmsnorm_fp8", "chain4096"),
     "rmsnorm_fp8_4096x4096": (4096, 4096, "rmsnorm_fp8", "chain4096"),
+    "fp4_2048x16384": (2048, 16384, "add_rmsnorm_fp4", "quant2048x16384"),
+    "fp4_4096x4096": (4096, 4096, "add_rmsnorm_fp4", "chain4096"),
 }
 
 
@@ -68,13 +70,14 @@ def algorithmic_bytes(n_rows: int, hidden: int, op: str = "add_rmsnorm") -> int:
     residual_out (add forms) and out (2 bytes) or int8 out (1 byte) plus a
     4-byte scale per row, and the weight once (norm forms)."""
     e = n_rows * hidden
-    return {"add_rmsnorm": 8 * e + 2 * hidden,
+    return int({"add_rmsnorm": 8 * e + 2 * hidden,
             "add_rmsnorm_quant": 7 * e + 4 * n_rows + 2 * hidden,
             "add_rmsnorm_fp8": 7 * e + 4 * n_rows + 2 * hidden,
+            "add_rmsnorm_fp4": 6.5 * e + 4 * n_rows + 2 * hidden,
             "rmsnorm": 4 * e + 2 * hidden,
             "rmsnorm_quant": 3 * e + 4 * n_rows + 2 * hidden,
             "rmsnorm_fp8": 3 * e + 4 * n_rows + 2 * hidden,
-            "residual_add": 6 * e}[op]
+            "residual_add": 6 * e}[op])
 
 
 def measured_peaks() -> dict:
@@ -211,8 +214,8 @@ def make_sets(device, name: str):
     for x_cpu in xs:
         x = x_cpu.to(device)
         s = {"x": x, "r": r0.to(device), "out": torch.empty_like(x), "ro": torch.empty_like(x)}
-        if op.endswith("quant") or op.endswith("fp8"):
-            s["q"] = torch.empty(n, h, dtype=torch.int8, device=device)
+        if op.endswith("quant") or op.endswith("fp8") or op.endswith("fp4"):
+            s["q"] = torch.empty(n, h // 2 if op.endswith("fp4") else h, dtype=torch.int8, device=device)
             s["scale"] = torch.empty(n, dtype=torch.float32, device=device)
         sets.append(s)
     return sets, w.to(device), (xs[0], r0, w)
@@ -237,7 +240,7 @@ class RawCall:
             x, r, ro = s["x"].data_ptr(), s["r"].data_ptr(), s["ro"].data_ptr()
             if op == "add_rmsnorm":
                 return (s["out"].data_ptr(), ro, x, r, wp, eps, n_rows, hidden, st)
-            if op in ("add_rmsnorm_quant", "add_rmsnorm_fp8"):
+            if op in ("add_rmsnorm_quant", "add_rmsnorm_fp8", "add_rmsnorm_fp4"):
                 return (s["q"].data_ptr(), s["scale"].data_ptr(), ro, x, r, wp, eps, n_rows, hidden, st)
             if op == "rmsnorm":
                 return (s["out"].data_ptr(), x, wp, eps, n_rows, hidden, st)
@@ -337,7 +340,8 @@ def cpu_baseline(seconds: float, name: str, first_inputs, gpu_set0=None):
            "rmsnorm_quant": lambda x, r: o.rmsnorm_quant_fwd(x, w, inputs.EPS),
            "residual_add": lambda x, r: (o.residual_add_fwd(x, r),),
            "add_rmsnorm_fp8": lambda x, r: o.rmsnorm_fp8_fwd(x, w, inputs.EPS, residual=r),
-           "rmsnorm_fp8": lambda x, r: o.rmsnorm_fp8_fwd(x, w, inputs.EPS)}
+           "rmsnorm_fp8": lambda x, r: o.rmsnorm_fp8_fwd(x, w, inputs.EPS),
+           "add_rmsnorm_fp4": lambda x, r: o.rmsnorm_fp4_fwd(x, w, inputs.EPS, residual=r)}
     fn = fns[op]
     chunk = 64
     rows = 0
@@ -366,7 +370,8 @@ def cpu_baseline(seconds: float, name: str, first_inputs, gpu_set0=None):
             return t.numpy()
         keys = {"add_rmsnorm": ["out", "ro"], "add_rmsnorm_quant": ["q", "scale", "ro"],
                 "rmsnorm": ["out"], "rmsnorm_quant": ["q", "scale"], "residual_add": ["ro"],
-                "add_rmsnorm_fp8": ["q", "scale", "ro"], "rmsnorm_fp8": ["q", "scale"]}[op]
+                "add_rmsnorm_fp8": ["q", "scale", "ro"], "rmsnorm_fp8": ["q", "scale"],
+                "add_rmsnorm_fp4": ["q", "scale", "ro"]}[op]
         got = [host(gpu_set0[k]) for k in keys]
         out["parity_rows_checked"] = chunk
         out["parity_bit_exact"] = bool(all(
@@ -379,7 +384,7 @@ def run_ours(args):
     world, rank, local = dist_setup()
     device = torch.device("cuda", local)
     n_rows, hidden, op, _ = WORKLOADS[args.workload]
-    quant = op.endswith("quant") or op.endswith("fp8")
+    quant = op.endswith("quant") or op.endswith("fp8") or op.endswith("fp4")
     dr.lib()
     stream = torch.cuda.Stream(device)
     sets, w_dev, first_inputs = make_sets(device, args.workload)
@@ -414,7 +419,7 @@ def run_ours(args):
         launch = {"variant": "elementwise"}
     else:
         cfg = dr.resolve_config(n_rows, hidden, quant=quant, sm_count=sm_count, add=op.startswith("add"),
-                                fp8=op.endswith("fp8"))
+                                fp8=op.endswith("fp8"), fp4=op.endswith("fp4"))
         launch = {"variant": "rows" if cfg.variant == 1 else "staged",
                   "threads_per_row": cfg.threads_per_row, "rows_per_cta": cfg.rows_per_cta,
                   "stages": cfg.stages}
@@ -422,7 +427,8 @@ def run_ours(args):
           "rmsnorm": "bf16 in/out", "rmsnorm_quant": "bf16 in, int8 + fp32 scale out",
           "residual_add": "bf16 in/out",
           "add_rmsnorm_fp8": "bf16 in, e4m3 + fp32 scale + bf16 residual_out out",
-          "rmsnorm_fp8": "bf16 in, e4m3 + fp32 scale out"}[op]
+          "rmsnorm_fp8": "bf16 in, e4m3 + fp32 scale out",
+          "add_rmsnorm_fp4": "bf16 in, packed e2m1 + fp32 scale + bf16 residual_out out"}[op]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
@@ -468,7 +474,8 @@ def run_reference(args):
            "rmsnorm_quant": lambda x, r: o.rmsnorm_quant_fwd(x, w, inputs.EPS),
            "residual_add": lambda x, r: o.residual_add_fwd(x, r),
            "add_rmsnorm_fp8": lambda x, r: o.rmsnorm_fp8_fwd(x, w, inputs.EPS, residual=r),
-           "rmsnorm_fp8": lambda x, r: o.rmsnorm_fp8_fwd(x, w, inputs.EPS)}
+           "rmsnorm_fp8": lambda x, r: o.rmsnorm_fp8_fwd(x, w, inputs.EPS),
+           "add_rmsnorm_fp4": lambda x, r: o.rmsnorm_fp4_fwd(x, w, inputs.EPS, residual=r)}
     fn = fns[op]
     t0 = time.perf_counter()
     fn(x0[:16], r0[:16])

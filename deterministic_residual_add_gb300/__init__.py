@@ -22,7 +22,7 @@ from pathlib import Path
 __all__ = [
     "add_rmsnorm_fwd", "add_rmsnorm_quant_fwd", "add_rmsnorm_fwd_with_config",
     "add_rmsnorm_quant_fwd_with_config", "rmsnorm_fwd", "rmsnorm_quant_fwd", "residual_add_fwd",
-    "add_rmsnorm_fp8_fwd", "rmsnorm_fp8_fwd",
+    "add_rmsnorm_fp8_fwd", "rmsnorm_fp8_fwd", "add_rmsnorm_fp4_fwd", "rmsnorm_fp4_fwd",
     "LaunchConfig", "DraddError", "resolve_config",
     "device_status", "bf16_convert_range", "status_string", "abi_version", "lib", "library_path",
     "VARIANT_AUTO", "VARIANT_ROWS", "VARIANT_STAGED", "MAX_HIDDEN",
@@ -34,6 +34,7 @@ MAX_HIDDEN = 32768
 VARIANT_AUTO, VARIANT_ROWS, VARIANT_STAGED = 0, 1, 2
 OP_ADD_RMSNORM, OP_ADD_RMSNORM_QUANT, OP_RMSNORM, OP_RMSNORM_QUANT = 0, 1, 2, 3
 OP_ADD_RMSNORM_FP8, OP_RMSNORM_FP8 = 4, 5
+OP_ADD_RMSNORM_FP4, OP_RMSNORM_FP4 = 6, 7
 
 STATUS_NAMES = {
     0: "OK", 1: "NULL_PTR", 2: "BAD_SHAPE", 3: "UNSUPPORTED_HIDDEN", 4: "MISALIGNED",
@@ -111,6 +112,10 @@ def lib() -> ctypes.CDLL:
                        ("add_rmsnorm_fp8_fwd_with_config", quant_args + [cfgp]),
                        ("rmsnorm_fp8_fwd", [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp]),
                        ("rmsnorm_fp8_fwd_with_config", [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp, cfgp]),
+                       ("add_rmsnorm_fp4_fwd", quant_args),
+                       ("add_rmsnorm_fp4_fwd_with_config", quant_args + [cfgp]),
+                       ("rmsnorm_fp4_fwd", [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp]),
+                       ("rmsnorm_fp4_fwd_with_config", [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp, cfgp]),
                        ("dradd_resolve_config", [_i64, _i64, ctypes.c_int, ctypes.c_int, cfgp]),
                        ("dradd_device_status", [_vp, ctypes.c_int]),
                        ("dradd_bf16_convert_range", [_vp, ctypes.c_uint64, _i64, ctypes.c_int, _vp])]:
@@ -246,11 +251,14 @@ def add_rmsnorm_quant_fwd_with_config(x, residual, weight, eps, config: LaunchCo
 
 
 def resolve_config(n_rows: int, hidden: int, quant: bool = False, sm_count: int = 152,
-                   config: LaunchConfig | None = None, add: bool = True, fp8: bool = False) -> LaunchConfig:
+                   config: LaunchConfig | None = None, add: bool = True, fp8: bool = False,
+                   fp4: bool = False) -> LaunchConfig:
     """The configuration the library would launch for this shape (no GPU
-    work when sm_count > 0); add=False for plain RMSNorm, fp8=True for the
-    e4m3 output."""
-    if fp8:
+    work when sm_count > 0); add=False for plain RMSNorm, fp8=True / fp4=True
+    for the e4m3 / e2m1 output."""
+    if fp4:
+        op = OP_ADD_RMSNORM_FP4 if add else OP_RMSNORM_FP4
+    elif fp8:
         op = OP_ADD_RMSNORM_FP8 if add else OP_RMSNORM_FP8
     else:
         op = (OP_ADD_RMSNORM if add else OP_RMSNORM) + (1 if quant else 0)
@@ -354,6 +362,64 @@ def rmsnorm_fp8_fwd(x, weight, eps: float = 1e-6, *, out_q=None, scale=None, str
         else:
             c = config._c()
             _check(lib().rmsnorm_fp8_fwd_with_config(*args, ctypes.byref(c)), "rmsnorm_fp8_fwd_with_config")
+    return out_q, scale
+
+
+def _fp4_outs(x, out_q, scale):
+    torch = _torch()
+    if out_q is None:
+        out_q = torch.empty(x.shape[:-1] + (x.shape[-1] // 2,), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    if (out_q.dtype != torch.uint8 or not out_q.is_cuda or not out_q.is_contiguous()
+            or out_q.numel() * 2 != x.numel()):
+        raise ValueError("out_q must be a contiguous CUDA uint8 tensor of hidden / 2 bytes per row")
+    if (scale.dtype != torch.float32 or not scale.is_cuda or not scale.is_contiguous()
+            or scale.numel() * x.shape[-1] != x.numel()):
+        raise ValueError("scale must be a contiguous CUDA float32 tensor with one entry per row")
+    return out_q, scale
+
+
+def add_rmsnorm_fp4_fwd(x, residual, weight, eps: float = 1e-6, *, out_q=None, scale=None,
+                        residual_out=None, stream=None, config: LaunchConfig | None = None):
+    """Residual-add + RMSNorm with per-row e2m1 out: (out_q [..., h/2] uint8,
+    two codes per byte with the even element in the low nibble; scale;
+    residual_out)."""
+    torch = _torch()
+    n_rows, hidden = _shape(x, None)
+    n = n_rows * hidden
+    out_q, scale = _fp4_outs(x, out_q, scale)
+    if residual_out is None:
+        residual_out = torch.empty_like(x)
+    args = (out_q.data_ptr(), scale.data_ptr(), _bf16_ptr(residual_out, "residual_out", n),
+            _bf16_ptr(x, "x", n), _bf16_ptr(residual, "residual", n),
+            _bf16_ptr(weight, "weight", hidden), float(eps), n_rows, hidden,
+            _stream_handle(stream, x.device))
+    with torch.cuda.device(x.device):
+        if config is None:
+            _check(lib().add_rmsnorm_fp4_fwd(*args), "add_rmsnorm_fp4_fwd")
+        else:
+            c = config._c()
+            _check(lib().add_rmsnorm_fp4_fwd_with_config(*args, ctypes.byref(c)),
+                   "add_rmsnorm_fp4_fwd_with_config")
+    return out_q, scale, residual_out
+
+
+def rmsnorm_fp4_fwd(x, weight, eps: float = 1e-6, *, out_q=None, scale=None, stream=None,
+                    config: LaunchConfig | None = None):
+    """Plain RMSNorm with per-row e2m1 out: (out_q [..., h/2] uint8, scale)."""
+    torch = _torch()
+    n_rows, hidden = _shape(x, None)
+    n = n_rows * hidden
+    out_q, scale = _fp4_outs(x, out_q, scale)
+    args = (out_q.data_ptr(), scale.data_ptr(), _bf16_ptr(x, "x", n), _bf16_ptr(weight, "weight", hidden),
+            float(eps), n_rows, hidden, _stream_handle(stream, x.device))
+    with torch.cuda.device(x.device):
+        if config is None:
+            _check(lib().rmsnorm_fp4_fwd(*args), "rmsnorm_fp4_fwd")
+        else:
+            c = config._c()
+            _check(lib().rmsnorm_fp4_fwd_with_config(*args, ctypes.byref(c)), "rmsnorm_fp4_fwd_with_config")
     return out_q, scale
 
 

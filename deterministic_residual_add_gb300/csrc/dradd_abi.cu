@@ -112,10 +112,13 @@ dradd_status check_overlaps(const Range* inputs, int n_in, const Range* outs, co
 // Shape, pointers, eps and overlaps.  out/out_q/scale: whichever the variant
 // writes (the others NULL).  Returns DRADD_OK with *noop set for n_rows == 0.
 // add = false (plain RMSNorm): residual and residual_out are not used.
-dradd_status validate(bool quant, bool add, const void* out, const void* out_q, const void* scale,
+// out_kind: dradd::kOutBf16 writes out; the others write 1-byte codes to
+// out_q (two e2m1 codes per byte) and a per-row scale.
+dradd_status validate(int out_kind, bool add, const void* out, const void* out_q, const void* scale,
                       const void* residual_out, const void* x, const void* residual, const void* weight,
                       float eps, int64_t n_rows, int64_t hidden, bool* noop)
 {
+    const bool quant = out_kind != dradd::kOutBf16;
     *noop = false;
     if (n_rows < 0 || hidden <= 0)
         return DRADD_ERR_BAD_SHAPE;
@@ -152,7 +155,7 @@ dradd_status validate(bool quant, bool add, const void* out, const void* out_q, 
         outs[n_out++] = range_of(residual_out, elems * 2);
     }
     if (quant) {
-        outs[n_out++] = range_of(out_q, elems);
+        outs[n_out++] = range_of(out_q, out_kind == dradd::kOutE2m1 ? elems / 2 : elems);
         outs[n_out++] = range_of(scale, n_rows * 4);
     } else {
         bf16_out[n_out] = true;
@@ -296,7 +299,7 @@ dradd_status run(int out_kind, bool add, dradd_bf16* out, int8_t* out_q, float* 
 {
     const bool quant = out_kind != dradd::kOutBf16;
     bool noop = false;
-    dradd_status st = validate(quant, add, out, out_q, scale, residual_out, x, residual, weight, eps, n_rows,
+    dradd_status st = validate(out_kind, add, out, out_q, scale, residual_out, x, residual, weight, eps, n_rows,
                                hidden, &noop);
     if (st != DRADD_OK || noop)
         return st;
@@ -408,7 +411,7 @@ dradd_status dradd_resolve_config(int64_t n_rows, int64_t hidden, int op, int sm
 {
     if (!cfg)
         return DRADD_ERR_NULL_PTR;
-    if (op < DRADD_OP_ADD_RMSNORM || op > DRADD_OP_RMSNORM_FP8)
+    if (op < DRADD_OP_ADD_RMSNORM || op > DRADD_OP_RMSNORM_FP4)
         return DRADD_ERR_BAD_CONFIG;
     DeviceLimits L;
     if (sm_count > 0) {
@@ -420,7 +423,7 @@ dradd_status dradd_resolve_config(int64_t n_rows, int64_t hidden, int op, int sm
     }
     const bool quant = op != DRADD_OP_ADD_RMSNORM && op != DRADD_OP_RMSNORM;
     const bool add = op == DRADD_OP_ADD_RMSNORM || op == DRADD_OP_ADD_RMSNORM_QUANT ||
-                     op == DRADD_OP_ADD_RMSNORM_FP8;
+                     op == DRADD_OP_ADD_RMSNORM_FP8 || op == DRADD_OP_ADD_RMSNORM_FP4;
     return resolve(n_rows, hidden, quant, add, L, cfg);
 }
 
@@ -442,6 +445,43 @@ dradd_status add_rmsnorm_fp8_fwd_with_config(uint8_t* out_q, float* scale, dradd
         return DRADD_ERR_NULL_PTR;
     return run(dradd::kOutE4m3, true, nullptr, reinterpret_cast<int8_t*>(out_q), scale, residual_out, x,
                residual, weight, eps, n_rows, hidden, stream, cfg);
+}
+
+dradd_status add_rmsnorm_fp4_fwd(uint8_t* out_q, float* scale, dradd_bf16* residual_out,
+                                 const dradd_bf16* x, const dradd_bf16* residual, const dradd_bf16* weight,
+                                 float eps, int64_t n_rows, int64_t hidden, cudaStream_t stream)
+{
+    return run(dradd::kOutE2m1, true, nullptr, reinterpret_cast<int8_t*>(out_q), scale, residual_out, x,
+               residual, weight, eps, n_rows, hidden, stream, nullptr);
+}
+
+dradd_status add_rmsnorm_fp4_fwd_with_config(uint8_t* out_q, float* scale, dradd_bf16* residual_out,
+                                             const dradd_bf16* x, const dradd_bf16* residual,
+                                             const dradd_bf16* weight, float eps, int64_t n_rows,
+                                             int64_t hidden, cudaStream_t stream,
+                                             const dradd_launch_cfg* cfg)
+{
+    if (!cfg)
+        return DRADD_ERR_NULL_PTR;
+    return run(dradd::kOutE2m1, true, nullptr, reinterpret_cast<int8_t*>(out_q), scale, residual_out, x,
+               residual, weight, eps, n_rows, hidden, stream, cfg);
+}
+
+dradd_status rmsnorm_fp4_fwd(uint8_t* out_q, float* scale, const dradd_bf16* x, const dradd_bf16* weight,
+                             float eps, int64_t n_rows, int64_t hidden, cudaStream_t stream)
+{
+    return run(dradd::kOutE2m1, false, nullptr, reinterpret_cast<int8_t*>(out_q), scale, nullptr, x, nullptr,
+               weight, eps, n_rows, hidden, stream, nullptr);
+}
+
+dradd_status rmsnorm_fp4_fwd_with_config(uint8_t* out_q, float* scale, const dradd_bf16* x,
+                                         const dradd_bf16* weight, float eps, int64_t n_rows, int64_t hidden,
+                                         cudaStream_t stream, const dradd_launch_cfg* cfg)
+{
+    if (!cfg)
+        return DRADD_ERR_NULL_PTR;
+    return run(dradd::kOutE2m1, false, nullptr, reinterpret_cast<int8_t*>(out_q), scale, nullptr, x, nullptr,
+               weight, eps, n_rows, hidden, stream, cfg);
 }
 
 dradd_status rmsnorm_fp8_fwd(uint8_t* out_q, float* scale, const dradd_bf16* x, const dradd_bf16* weight,
@@ -547,7 +587,7 @@ dradd_status dradd_bf16_convert_range(dradd_bf16* out, uint64_t first, int64_t c
         return DRADD_ERR_NULL_PTR;
     if (!aligned(out, 2))
         return DRADD_ERR_MISALIGNED;
-    if (method < 0 || method > 3)
+    if (method < 0 || method > 4)
         return DRADD_ERR_BAD_CONFIG;
     return dradd::launch_convert(out, first, count, method, stream) == cudaSuccess ? DRADD_OK
                                                                                   : DRADD_ERR_CUDA;

@@ -251,9 +251,9 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
     return d;
 }
 
-// Per-row e4m3 scale: scale = RN(amax / 448) and the two multipliers that
-// bracket 1 / scale, c_lo = RN(RN(1/scale) * (1 - 2^-20)) and c_hi likewise
-// with 1 + 2^-20.
+// Per-row fp8 / fp4 scale (scale = RN(amax / 448) or RN(amax / 6)) and the
+// two multipliers that bracket 1 / scale, c_lo = RN(RN(1/scale) * (1 - 2^-20))
+// and c_hi likewise with 1 + 2^-20.
 struct E4m3Scale {
     float scale;
     float c_lo, c_hi;
@@ -303,6 +303,48 @@ __device__ __forceinline__ uint2 quantize8_e4m3(const float (&y)[8], const E4m3S
     u.x = lo[0] | (lo[1] << 16);
     u.y = lo[2] | (lo[3] << 16);
     return u;
+}
+
+// ------------------------------------------------------------ fp4 e2m1 codes
+// cvt.rn.satfinite.e2m1x2.f32 rounds two fp32 values to nearest-even e2m1
+// (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; past 6 saturates) and packs them
+// into one byte, the first operand in the high nibble.  Equal to the
+// oracle's encoder on every non-NaN fp32 input (checked exhaustively by the
+// test suite).
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi)
+{
+    uint16_t d;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u16.u8 %0, t;\n\t}"
+        : "=h"(d)
+        : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Eight e2m1 codes (four bytes, even elements in the low nibbles) for eight
+// consecutive y values: e2m1(RN(y / scale)), by the same bracket as
+// quantize8_e4m3 (rounding to e2m1 is monotone too); `s` is built by
+// make_e4m3_scale from scale = RN(amax / 6).
+__device__ __forceinline__ uint32_t quantize8_e2m1(const float (&y)[8], const E4m3Scale& s)
+{
+    uint32_t lo[4], hi[4];
+    bool boundary = !s.fast;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        lo[p] = e2m1x2(__fmul_rn(y[2 * p], s.c_lo), __fmul_rn(y[2 * p + 1], s.c_lo));
+        hi[p] = e2m1x2(__fmul_rn(y[2 * p], s.c_hi), __fmul_rn(y[2 * p + 1], s.c_hi));
+        boundary |= lo[p] != hi[p];
+    }
+    if (boundary) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            lo[p] = s.scale == 0.0f
+                        ? 0u
+                        : e2m1x2(__fdiv_rn(y[2 * p], s.scale), __fdiv_rn(y[2 * p + 1], s.scale));
+        }
+    }
+    return lo[0] | (lo[1] << 8) | (lo[2] << 16) | (lo[3] << 24);
 }
 
 // ------------------------------------------------------ mbarrier and bulk copy

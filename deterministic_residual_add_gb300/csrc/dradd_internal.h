@@ -10,7 +10,7 @@ namespace dradd {
 
 struct Params {
     uint16_t* out;            // bf16 out (bf16 variant)
-    int8_t* out_q;            // int8 or e4m3 codes (quantised variants)
+    int8_t* out_q;            // int8, e4m3 or packed e2m1 codes (quantised variants)
     float* scale;             // per-row scale (quant variant)
     uint16_t* residual_out;
     const uint16_t* x;
@@ -31,7 +31,7 @@ struct Params {
 constexpr unsigned kDeviceStatusTimeout = 1u;
 
 // What a normalised row is stored as.
-enum OutKind : int { kOutBf16 = 0, kOutInt8 = 1, kOutE4m3 = 2 };
+enum OutKind : int { kOutBf16 = 0, kOutInt8 = 1, kOutE4m3 = 2, kOutE2m1 = 3 };
 
 using KernelFn = void (*)(Params);
 
@@ -65,9 +65,11 @@ size_t staged_static_smem(int K);
 KernelFn staged_fn_add_bf16(int T, int K);
 KernelFn staged_fn_add_int8(int T, int K);
 KernelFn staged_fn_add_e4m3(int T, int K);
+KernelFn staged_fn_add_e2m1(int T, int K);
 KernelFn staged_fn_norm_bf16(int T, int K);
 KernelFn staged_fn_norm_int8(int T, int K);
 KernelFn staged_fn_norm_e4m3(int T, int K);
+KernelFn staged_fn_norm_e2m1(int T, int K);
 cudaError_t launch_residual_add(uint16_t* residual_out, const uint16_t* x, const uint16_t* residual,
                                 int64_t n_vec, int sm_count, bool serialize, cudaStream_t stream);
 cudaError_t launch_convert(uint16_t* out, uint64_t first, int64_t count, int method, cudaStream_t stream);

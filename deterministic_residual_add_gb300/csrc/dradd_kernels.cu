@@ -62,6 +62,8 @@ __global__ void convert_kernel(uint16_t* out, uint64_t first, int64_t count, int
             b = pack_rne_cvt(f, f) & 0xFFFFu;
         else if (method == 3)
             b = e4m3x2(f, f) & 0xFFu;
+        else if (method == 4)
+            b = e2m1x2(f, f) & 0xFu;
         else
             b = pack_rne(f, f) & 0xFFFFu;
         out[i] = static_cast<uint16_t>(b);
@@ -80,6 +82,7 @@ KernelFn rows_fn(int K, int out, bool add)
     case kOutBf16: DRADD_ROWS_OUT(KK, kOutBf16);                        \
     case kOutInt8: DRADD_ROWS_OUT(KK, kOutInt8);                        \
     case kOutE4m3: DRADD_ROWS_OUT(KK, kOutE4m3);                        \
+    case kOutE2m1: DRADD_ROWS_OUT(KK, kOutE2m1);                        \
     default: return nullptr;                                            \
     }
     switch (K) {
@@ -99,6 +102,7 @@ KernelFn staged_fn(int T, int K, int out, bool add)
     case kOutBf16: return add ? staged_fn_add_bf16(T, K) : staged_fn_norm_bf16(T, K);
     case kOutInt8: return add ? staged_fn_add_int8(T, K) : staged_fn_norm_int8(T, K);
     case kOutE4m3: return add ? staged_fn_add_e4m3(T, K) : staged_fn_norm_e4m3(T, K);
+    case kOutE2m1: return add ? staged_fn_add_e2m1(T, K) : staged_fn_norm_e2m1(T, K);
     default: return nullptr;
     }
 }
@@ -111,15 +115,15 @@ int log2i(int v)
     return l;
 }
 
-// One bit per staged kernel: (add, out = 0..2, T = 32..1024, K = 1..8).
+// One bit per staged kernel: (add, out = 0..3, T = 32..1024, K = 1..8).
 int staged_index(int T, int K, int out, bool add)
 {
-    return ((add ? 3 : 0) + out) * 24 + (log2i(T) - 5) * 4 + log2i(K);
+    return ((add ? 4 : 0) + out) * 24 + (log2i(T) - 5) * 4 + log2i(K);
 }
 
 constexpr int kMaxDevices = 64;
 // Per device: bit k of word k / 64 set once staged kernel k has been allowed
-// its full dynamic shared memory (6 x 24 kernels).
+// its full dynamic shared memory (8 x 24 kernels).
 std::atomic<uint64_t> g_smem_attr_done[kMaxDevices][3];
 std::atomic<unsigned*> g_status_ptr[kMaxDevices];
 

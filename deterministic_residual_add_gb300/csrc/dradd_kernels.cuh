@@ -115,12 +115,22 @@ __device__ __forceinline__ void finish_row(const Params& p, float (&acc)[K][8], 
             __syncthreads();
             m = butterfly_max(red_max[lane & ((T >> 5) - 1)], T >> 5);
         }
-        const float scale = __fdiv_rn(m, OUT == kOutInt8 ? 127.0f : 448.0f);
+        const float scale = __fdiv_rn(m, OUT == kOutInt8 ? 127.0f : OUT == kOutE4m3 ? 448.0f : 6.0f);
         if (active) {
             if (t == 0)
                 p.scale[row] = scale;
             uint2* qrow = reinterpret_cast<uint2*>(p.out_q + row * p.hidden);
-            if constexpr (OUT == kOutInt8) {
+            if constexpr (OUT == kOutE2m1) {
+                // two codes per byte: a row is hidden / 2 bytes, a block 4 bytes
+                uint32_t* prow = reinterpret_cast<uint32_t*>(p.out_q + row * (p.hidden / 2));
+                const E4m3Scale qs = make_e4m3_scale(scale);
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    const int b = t + j * T;
+                    if (b < nblocks)
+                        __stcs(prow + b, quantize8_e2m1(acc[j], qs));
+                }
+            } else if constexpr (OUT == kOutInt8) {
                 const QuantScale qs = make_quant_scale(scale);
 #pragma unroll
                 for (int j = 0; j < K; ++j) {

@@ -185,7 +185,8 @@ dradd_status add_rmsnorm_quant_fwd_with_config(int8_t* out_q, float* scale,
  * dradd_resolve_config -- fill the automatic choices of *cfg for a call of
  * the given shape and operation, as the entry points would, and validate
  * the explicit ones.  `op` is one of DRADD_OP_* (0 and 1 are the bf16 and
- * int8 residual-add forms, 2 and 3 plain RMSNorm, 4 and 5 the fp8 forms).  grid_ctas is filled from
+ * int8 residual-add forms, 2 and 3 plain RMSNorm, 4 and 5 the fp8 forms,
+ * 6 and 7 the fp4 forms).  grid_ctas is filled from
  * `sm_count` (pass 0 to query the current device); for the staged variant
  * the entry points size the grid with the CUDA occupancy calculator instead.
  * Does no GPU work when sm_count > 0.
@@ -196,7 +197,9 @@ enum {
     DRADD_OP_RMSNORM = 2,
     DRADD_OP_RMSNORM_QUANT = 3,
     DRADD_OP_ADD_RMSNORM_FP8 = 4,
-    DRADD_OP_RMSNORM_FP8 = 5
+    DRADD_OP_RMSNORM_FP8 = 5,
+    DRADD_OP_ADD_RMSNORM_FP4 = 6,
+    DRADD_OP_RMSNORM_FP4 = 7
 };
 
 dradd_status dradd_resolve_config(int64_t n_rows, int64_t hidden, int op, int sm_count,
@@ -275,6 +278,42 @@ dradd_status rmsnorm_fp8_fwd_with_config(uint8_t* out_q, float* scale, const dra
                                          const dradd_launch_cfg* cfg);
 
 /*
+ * add_rmsnorm_fp4_fwd -- the residual-add + RMSNorm forward with the
+ * normalised row emitted as per-row scaled fp4 e2m1 codes (1 sign, 2
+ * exponent bits with bias 1, 1 mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2,
+ * 3, 4, 6), the fp4 scaled cast of the page's "Cost of fixing":
+ *   scale[r]   = amax / 6                                (fp32, rounded once)
+ *   code       = e2m1(y_i / scale[r]): the correctly rounded fp32 quotient
+ *                rounded to the nearest e2m1 value, ties to the even code,
+ *                magnitudes past 6 saturating to 6; scale[r] == 0 gives 0.
+ *   out_q         [n_rows x hidden / 2] bytes, written (16-byte aligned):
+ *                 byte j of a row holds element 2j in its low nibble and
+ *                 element 2j + 1 in its high nibble; bit 3 of a code is the
+ *                 sign.
+ *   scale, residual_out and the other arguments as in add_rmsnorm_quant_fwd.
+ */
+dradd_status add_rmsnorm_fp4_fwd(uint8_t* out_q, float* scale, dradd_bf16* residual_out,
+                                 const dradd_bf16* x, const dradd_bf16* residual,
+                                 const dradd_bf16* weight, float eps, int64_t n_rows,
+                                 int64_t hidden, cudaStream_t stream);
+
+dradd_status add_rmsnorm_fp4_fwd_with_config(uint8_t* out_q, float* scale, dradd_bf16* residual_out,
+                                             const dradd_bf16* x, const dradd_bf16* residual,
+                                             const dradd_bf16* weight, float eps, int64_t n_rows,
+                                             int64_t hidden, cudaStream_t stream,
+                                             const dradd_launch_cfg* cfg);
+
+/* rmsnorm_fp4_fwd -- plain RMSNorm (no residual) with the same e2m1 output. */
+dradd_status rmsnorm_fp4_fwd(uint8_t* out_q, float* scale, const dradd_bf16* x,
+                             const dradd_bf16* weight, float eps, int64_t n_rows, int64_t hidden,
+                             cudaStream_t stream);
+
+dradd_status rmsnorm_fp4_fwd_with_config(uint8_t* out_q, float* scale, const dradd_bf16* x,
+                                         const dradd_bf16* weight, float eps, int64_t n_rows,
+                                         int64_t hidden, cudaStream_t stream,
+                                         const dradd_launch_cfg* cfg);
+
+/*
  * residual_add_fwd -- the residual update alone, the other half of the
  * page's reference(): residual_out = bf16_rne(fp32(x) + fp32(residual)),
  * element by element, bit-identical to add_rmsnorm_fwd's residual_out (the
@@ -302,7 +341,8 @@ dradd_status dradd_device_status(cudaStream_t stream, int clear);
  * patterns first, first+1, ... (mod 2^32) on the device, with method
  * 0 = the bf16 conversion the kernels use, 1 = integer round-half-even bit
  * arithmetic to bf16, 2 = the hardware cvt.rn.bf16x2.f32 instruction,
- * 3 = the e4m3 conversion the fp8 kernels use (code in the low byte).
+ * 3 = the e4m3 conversion the fp8 kernels use (code in the low byte),
+ * 4 = the e2m1 conversion the fp4 kernels use (code in the low nibble).
  * `out` is a device array of `count` 16-bit words (2-byte aligned).
  */
 dradd_status dradd_bf16_convert_range(dradd_bf16* out, uint64_t first, int64_t count,

@@ -104,7 +104,7 @@ def test_convert_hook_argument_errors(L):
     assert L.dradd_bf16_convert_range(None, 0, 16, 0, None) == 1
     assert L.dradd_bf16_convert_range(OUT, 0, -1, 0, None) == 2
     assert L.dradd_bf16_convert_range(OUT + 1, 0, 16, 0, None) == 4
-    assert L.dradd_bf16_convert_range(OUT, 0, 16, 4, None) == 9
+    assert L.dradd_bf16_convert_range(OUT, 0, 16, 5, None) == 9
     assert L.dradd_bf16_convert_range(OUT, 0, 0, 0, None) == 0
 
 
@@ -210,7 +210,7 @@ def test_rmsnorm_quant_and_residual_add_errors(L):
 
 def test_resolve_op_codes(L):
     c = dr.LaunchConfig()._c()
-    assert L.dradd_resolve_config(16, 1024, 6, 152, ctypes.byref(c)) == 9
+    assert L.dradd_resolve_config(16, 1024, 8, 152, ctypes.byref(c)) == 9
     plain = dr.resolve_config(4096, 16384, add=False)
     assert plain.variant == dr.VARIANT_STAGED and plain.stages == 4 and plain.threads_per_row == 512
     # a plain-RMSNorm stage holds only x, so 32768-wide rows fit two stages
@@ -230,3 +230,14 @@ def test_fp8_argument_errors(L):
     assert c.variant == dr.VARIANT_STAGED and c.stages == 2
     c = dr.resolve_config(4096, 4096, add=False, fp8=True)
     assert c.stages == 1
+
+
+def test_fp4_argument_errors(L):
+    assert L.add_rmsnorm_fp4_fwd(0, SC, RO, X, RES, W, 1e-6, 4, 1024, None) == 1
+    assert L.add_rmsnorm_fp4_fwd(Q + 8, SC, RO, X, RES, W, 1e-6, 4, 1024, None) == 4
+    # 4 x 1024 codes take 2048 bytes: starting 2032 bytes before residual_out overlaps it
+    assert L.add_rmsnorm_fp4_fwd(RO - 2032, SC, RO, X, RES, W, 1e-6, 4, 1024, None) == 6
+    assert L.rmsnorm_fp4_fwd(Q, SC, X, W, 1e-6, 0, 1024, None) == 0
+    assert L.rmsnorm_fp4_fwd_with_config(Q, SC, X, W, 1e-6, 4, 1024, None, None) == 1
+    c = dr.resolve_config(2048, 16384, add=True, fp4=True)
+    assert c.variant == dr.VARIANT_STAGED and c.threads_per_row == 512
