@@ -158,3 +158,20 @@ def edge_rows(n_rows: int = 16, hidden: int = 1024, seed: int = 0):
 def bits(t: torch.Tensor) -> torch.Tensor:
     """bf16 tensor -> int16 view of its bits (no arithmetic)."""
     return t.view(torch.int16)
+
+
+def hashed_bf16_rows(rows: torch.Tensor, hidden: int, salt: int) -> torch.Tensor:
+    """bf16 bit patterns (as int16) for the given row indices, a fixed hash of
+    (row, column, salt) on whatever device `rows` lives on: random sign,
+    exponent 2^-4..2^3, 7 random mantissa bits.  Any subset of rows of a
+    huge tensor can be rebuilt exactly without materialising the rest, so
+    inputs past 2^31 elements can be made on the device and checked on
+    sampled rows.  Every intermediate stays below 2^63."""
+    cols = torch.arange(hidden, device=rows.device, dtype=torch.int64)
+    hsh = (rows.to(torch.int64)[:, None] * 131 + cols[None, :] * 7 + salt * 977) * 739982445
+    hsh = hsh & 0xFFFFFFFF
+    hsh = hsh ^ (hsh >> 13)
+    mant = hsh & 0x7F
+    expo = 0x7B + ((hsh >> 7) & 0x7)
+    sign = ((hsh >> 10) & 1) << 15
+    return (sign | (expo << 7) | mant).to(torch.int16)
