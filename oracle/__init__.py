@@ -141,6 +141,10 @@ class Oracle:
         L.oracle_rmsnorm_e2m1_fwd.restype = ctypes.c_int
         L.oracle_rmsnorm_e2m1_fwd.argtypes = [_u8p, _f32p, _u16p, _u16p, _u16p, _u16p, ctypes.c_float,
                                               _i64, _i64]
+        L.oracle_qk_rmsnorm_fwd.restype = ctypes.c_int
+        L.oracle_qk_rmsnorm_fwd.argtypes = [ctypes.c_void_p, _f32p, _u16p, _u16p, _u16p, _u16p, _u16p,
+                                            _u16p, _u16p, ctypes.c_float, ctypes.c_float, _i64, _i64,
+                                            _i64, _i64, _i64]
         L.oracle_abi_version.restype = ctypes.c_int
 
     # ---- conversions -------------------------------------------------
@@ -370,6 +374,35 @@ class Oracle:
             if rc != 0:
                 raise RuntimeError(f"oracle_rmsnorm_e2m1_fwd failed with {rc}")
         return (q, scale) if r is None else (q, scale, ro)
+
+    def qk_rmsnorm_fwd(self, q, q_weight, k, k_weight, q_eps: float, k_eps: float,
+                       group_size: int = 0, q_residual=None):
+        """Fused q/k RMSNorm: returns a dict with q_out (bf16 bit patterns,
+        shaped like q, when group_size == 0; else e4m3 codes, uint8), q_scale
+        ([n_q, q_hidden / group_size] fp32, or None), q_residual_out (with a
+        q residual, else None) and k_out (bf16 bit patterns shaped like k).
+        q or k may have zero rows."""
+        q, qw, k, kw = _as_u16(q), _as_u16(q_weight), _as_u16(k), _as_u16(k_weight)
+        hq, hk = q.shape[-1], k.shape[-1]
+        nq = q.size // hq if hq else 0
+        nk = k.size // hk if hk else 0
+        qr = _as_u16(q_residual) if q_residual is not None else None
+        if group_size:
+            q_out = np.empty(q.shape, dtype=np.uint8)
+            q_scale = np.empty((nq, hq // group_size), dtype=np.float32)
+        else:
+            q_out = np.empty(q.shape, dtype=np.uint16)
+            q_scale = None
+        qro = np.empty_like(q) if qr is not None else None
+        k_out = np.empty_like(k)
+        rc = self._L.oracle_qk_rmsnorm_fwd(
+            q_out.ctypes.data_as(ctypes.c_void_p), _ptr(q_scale, _f32p), _ptr(qro, _u16p),
+            _ptr(k_out, _u16p), _ptr(q, _u16p), _ptr(qr, _u16p), _ptr(qw, _u16p), _ptr(k, _u16p),
+            _ptr(kw, _u16p), ctypes.c_float(q_eps), ctypes.c_float(k_eps), nq, hq, nk, hk,
+            int(group_size))
+        if rc != 0:
+            raise RuntimeError(f"oracle_qk_rmsnorm_fwd failed with {rc}")
+        return {"q_out": q_out, "q_scale": q_scale, "q_residual_out": qro, "k_out": k_out}
 
 
 def _split_rows(run, n_rows: int, threads: int):

@@ -1,8 +1,8 @@
 /*
  * dradd_oracle.c -- plain, slow, single-threaded CPU oracle for the fused
  * residual-add + RMSNorm forward and its quantised variants (int8, fp8 e4m3,
- * fp4 e2m1), and for its two halves: plain RMSNorm (no residual) and the
- * residual update alone.
+ * fp4 e2m1), for its two halves (plain RMSNorm, no residual; the residual
+ * update alone) and for the fused q/k RMSNorm with per-group e4m3 out.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
  * calls this file: only tests, the smoke check and the bench's CPU-baseline
@@ -586,6 +586,85 @@ int oracle_residual_add_fwd(uint16_t* residual_out, const uint16_t* x, const uin
     for (int64_t i = 0; i < n; ++i) {
         float acc = oracle_bf16_to_f32(x[i]) + oracle_bf16_to_f32(residual[i]);
         residual_out[i] = store_bf16(acc, store_mode);
+    }
+    return ORACLE_OK;
+}
+
+/* ---- fused q/k RMSNorm with per-group e4m3 out.
+ * The page (section "Notes") names a second kernel whose bf16 residual
+ * stores were not audited: the fused q/k RMSNorm + group quant kernel.  It
+ * prints no formula for it; the reading taken here is the plainest one that
+ * the name and the rest of the page support:
+ *   - two independent sets of rows normalised in one call, "q" (n_q_rows x
+ *     q_hidden, weight q_weight, eps q_eps) and "k" (n_k_rows x k_hidden,
+ *     weight k_weight, eps k_eps); a per-head norm is the same call with
+ *     rows = tokens x heads and hidden = head size;
+ *   - each row is the row function above: q with an optional residual add
+ *     (q_residual != NULL; q_residual_out gets the round-to-nearest-even
+ *     bf16 of the fp32 sum), k plain;
+ *   - "group quant": q's fp32 output is cut into consecutive groups of
+ *     group_size elements, each quantised to e4m3 exactly as a row of the
+ *     per-row e4m3 output (scale = amax / 448 over the group, code =
+ *     e4m3_rne(y / scale)); q_scale holds n_q_rows x (q_hidden / group_size)
+ *     scales, row-major.  group_size == 0 stores q as bf16 (round to nearest
+ *     even) instead, with q_scale unused;
+ *   - k's output is always bf16, rounded to nearest even.
+ * q_out is uint16_t bf16 bit patterns when group_size == 0, else uint8_t
+ * e4m3 codes.  Either row count may be 0. */
+static int qk_rows(void* q_out, float* q_scale, uint16_t* residual_out, const uint16_t* x,
+                   const uint16_t* residual, const uint16_t* weight, float eps, int64_t n_rows,
+                   int64_t hidden, int64_t group_size)
+{
+    int64_t padded = next_pow2(hidden);
+    float* acc = (float*)malloc((size_t)hidden * sizeof(float));
+    float* sq = (float*)calloc((size_t)padded, sizeof(float));
+    float* y = (float*)malloc((size_t)hidden * sizeof(float));
+    if (!acc || !sq || !y) {
+        free(acc); free(sq); free(y);
+        return ORACLE_ERR_NOMEM;
+    }
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int64_t base = r * hidden;
+        add_rmsnorm_row(y, residual ? residual_out + base : NULL, acc, sq, x + base,
+                        residual ? residual + base : NULL, weight, eps, hidden, padded,
+                        ORACLE_STORE_RNE, NULL, NULL);
+        if (group_size == 0) {
+            uint16_t* o = (uint16_t*)q_out + base;
+            for (int64_t i = 0; i < hidden; ++i)
+                o[i] = store_bf16(y[i], ORACLE_STORE_RNE);
+        } else {
+            int64_t groups = hidden / group_size;
+            for (int64_t g = 0; g < groups; ++g)
+                quantize_row_e4m3((uint8_t*)q_out + base + g * group_size,
+                                  q_scale + r * groups + g, y + g * group_size, group_size);
+        }
+    }
+    free(acc); free(sq); free(y);
+    return ORACLE_OK;
+}
+
+int oracle_qk_rmsnorm_fwd(void* q_out, float* q_scale, uint16_t* q_residual_out, uint16_t* k_out,
+                          const uint16_t* q, const uint16_t* q_residual, const uint16_t* q_weight,
+                          const uint16_t* k, const uint16_t* k_weight, float q_eps, float k_eps,
+                          int64_t n_q_rows, int64_t q_hidden, int64_t n_k_rows, int64_t k_hidden,
+                          int64_t group_size)
+{
+    if (n_q_rows < 0 || n_k_rows < 0 || group_size < 0)
+        return ORACLE_ERR_ARG;
+    if (n_q_rows > 0) {
+        if (q_hidden <= 0 || !q_out || !q || !q_weight || (q_residual && !q_residual_out))
+            return ORACLE_ERR_ARG;
+        if (group_size > 0 && (q_hidden % group_size != 0 || !q_scale))
+            return ORACLE_ERR_ARG;
+        int rc = qk_rows(q_out, q_scale, q_residual_out, q, q_residual, q_weight, q_eps, n_q_rows,
+                         q_hidden, group_size);
+        if (rc != ORACLE_OK)
+            return rc;
+    }
+    if (n_k_rows > 0) {
+        if (k_hidden <= 0 || !k_out || !k || !k_weight)
+            return ORACLE_ERR_ARG;
+        return qk_rows(k_out, NULL, NULL, k, NULL, k_weight, k_eps, n_k_rows, k_hidden, 0);
     }
     return ORACLE_OK;
 }

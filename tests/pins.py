@@ -512,6 +512,79 @@ def pin_fp4_rows(o, seed: int = 37):
         assert list(refs.unpack_fp4(res[0])[0]) == codes and res[1][0] == sc, i
 
 
+# ------------------------------------------------------ fused q/k RMSNorm
+def pin_qk_rows(o, seed: int = 41):
+    """Fused q/k RMSNorm with per-group e4m3 out.  Against the exact-rational
+    evaluation on small rows (each group its own scale; k plain bf16 with
+    its own weight and eps); 448 reached in every nonzero group; every
+    group dequantised within half an e4m3 step of fp64; group size =
+    q_hidden gives the per-row e4m3 output, group size 0 the bf16 output of
+    the residual-add (or plain) RMSNorm; zero groups give scale 0, code 0;
+    either side may be empty."""
+    g = inputs.generator(seed)
+    vals = np.array([float(refs.e4m3_value(c)) for c in range(0x7F)] + [float("nan")])
+    for i, (hq, hk, gs, with_res) in enumerate([(16, 8, 8, True), (32, 16, 8, False), (24, 8, 8, True),
+                                                (64, 24, 16, True), (32, 32, 32, False)]):
+        qb = refs.u16(inputs.normal_bf16(g, (2, hq), 0.0, 1.0))
+        rb = refs.u16(inputs.normal_bf16(g, (2, hq), 0.0, 3.0)) if with_res else None
+        qw = refs.u16(inputs.normal_bf16(g, (hq,), 1.0, 0.3))
+        kb = refs.u16(inputs.normal_bf16(g, (3, hk), 0.5, 2.0))
+        kw = refs.u16(inputs.normal_bf16(g, (hk,), 1.0, 0.3))
+        q_eps, k_eps = 1e-6, 0.25
+        res = o.qk_rmsnorm_fwd(qb, qw, kb, kw, q_eps, k_eps, group_size=gs, q_residual=rb)
+        for r in range(2):
+            codes, scales = refs.e4m3_group_exact(qb[r], None if rb is None else rb[r], qw, q_eps, gs)
+            assert list(res["q_out"][r]) == codes, (i, r)
+            assert [np.float32(s) for s in res["q_scale"][r]] == [np.float32(s) for s in scales], (i, r)
+            if with_res:
+                ro = refs.row_exact(qb[r], rb[r], qw, q_eps)["ro"]
+                assert list(res["q_residual_out"][r]) == ro, (i, r)
+        for r in range(3):
+            assert list(res["k_out"][r]) == refs.plain_bf16_exact(kb[r], kw, k_eps), (i, r)
+
+    for n, hq, gs, with_res in [(6, 1536, 128, True), (5, 4096, 64, False), (4, 200, 8, True)]:
+        q = inputs.normal_bf16(g, (n, hq), 0.0, 1.0)
+        r = inputs.normal_bf16(g, (n, hq), 0.0, 2.0) if with_res else None
+        qw = inputs.normal_bf16(g, (hq,), 1.0, 0.1)
+        k = inputs.normal_bf16(g, (n, 512), 0.0, 1.0)
+        kw = inputs.normal_bf16(g, (512,), 1.0, 0.1)
+        res = o.qk_rmsnorm_fwd(q, qw, k, kw, 1e-6, 1e-5, group_size=gs, q_residual=r)
+        codes = res["q_out"].reshape(n, hq // gs, gs)
+        assert np.all((codes & 0x7F).max(axis=2) == 0x7E)
+        y64, _ = refs.add_rmsnorm_f64(q, r if with_res else torch.zeros_like(q), qw, 1e-6)
+        mag = vals[codes & 0x7F] * np.where(codes & 0x80, -1.0, 1.0)
+        sc = res["q_scale"].astype(np.float64)[:, :, None]
+        deq = (mag * sc).reshape(n, hq)
+        step = (np.maximum(np.abs(mag) * 2.0 ** -4, 2.0 ** -10) * sc).reshape(n, hq)
+        assert np.all(np.abs(deq - y64) <= step + np.abs(y64) * 2.0 ** -20)
+        whole = o.qk_rmsnorm_fwd(q, qw, k, kw, 1e-6, 1e-5, group_size=hq, q_residual=r)
+        per_row = o.rmsnorm_fp8_fwd(q, qw, 1e-6, residual=r)
+        assert np.array_equal(whole["q_out"], per_row[0])
+        assert np.array_equal(whole["q_scale"][:, 0], per_row[1])
+        bf = o.qk_rmsnorm_fwd(q, qw, k, kw, 1e-6, 1e-5, group_size=0, q_residual=r)
+        if with_res:
+            out, ro = o.add_rmsnorm_fwd(q, r, qw, 1e-6)
+            assert np.array_equal(bf["q_residual_out"], ro)
+            assert np.array_equal(res["q_residual_out"], ro)
+        else:
+            out = o.rmsnorm_fwd(q, qw, 1e-6)
+        assert np.array_equal(bf["q_out"], out)
+        assert np.array_equal(bf["k_out"], o.rmsnorm_fwd(k, kw, 1e-5))
+        assert np.array_equal(res["k_out"], bf["k_out"])
+
+    # zero groups inside a nonzero row; an empty side
+    q = np.zeros((2, 64), np.uint16)
+    q[:, 16:32] = refs.u16(inputs.normal_bf16(g, (2, 16), 0.0, 1.0))
+    one = np.full(64, 0x3F80, np.uint16)
+    res = o.qk_rmsnorm_fwd(q, one, np.zeros((0, 8), np.uint16), np.full(8, 0x3F80, np.uint16),
+                           1e-6, 1e-6, group_size=16)
+    assert np.all(res["q_scale"][:, [0, 2, 3]] == 0) and np.all(res["q_scale"][:, 1] > 0)
+    assert np.all(res["q_out"][:, :16] == 0) and np.all(res["q_out"][:, 32:] == 0)
+    assert res["k_out"].shape == (0, 8)
+    res = o.qk_rmsnorm_fwd(np.zeros((0, 64), np.uint16), one, q, one, 1e-6, 1e-6, group_size=16)
+    assert res["q_out"].shape == (0, 64) and np.array_equal(res["k_out"], o.rmsnorm_fwd(q, one, 1e-6))
+
+
 FAST_PINS = [
     pin_rne_edge_table,
     pin_tree_worked_examples,
@@ -532,4 +605,5 @@ FAST_PINS = [
     pin_fp8_rows,
     pin_e2m1_encoder,
     pin_fp4_rows,
+    pin_qk_rows,
 ]

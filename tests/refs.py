@@ -246,6 +246,30 @@ def e4m3_row_exact(x_bits, r_bits, w_bits, eps: float, quant_op: str = "div"):
     xs = list(x_bits)
     rs = list(r_bits) if r_bits is not None else [0] * len(xs)
     ys = row_exact(xs, rs, w_bits, eps)["y"] if r_bits is not None else _plain_row_y(xs, w_bits, eps)
+    return _e4m3_codes(ys, quant_op)
+
+
+def e4m3_group_exact(x_bits, r_bits, w_bits, eps: float, group: int):
+    """Exact-rational per-group e4m3 quantisation of one row: y as in
+    e4m3_row_exact, then every run of `group` consecutive elements gets its
+    own scale = RN32(amax / 448) over that run.  Returns (codes, scales)."""
+    xs = list(x_bits)
+    rs = list(r_bits) if r_bits is not None else [0] * len(xs)
+    ys = row_exact(xs, rs, w_bits, eps)["y"] if r_bits is not None else _plain_row_y(xs, w_bits, eps)
+    codes, scales = [], []
+    for lo in range(0, len(ys), group):
+        c, s = _e4m3_codes(ys[lo:lo + group], "div")
+        codes += c
+        scales.append(s)
+    return codes, scales
+
+
+def plain_bf16_exact(x_bits, w_bits, eps: float):
+    """bf16 bit patterns of plain RMSNorm of one row by exact rational steps."""
+    return [rne_bf16_exact(y) for y in _plain_row_y(list(x_bits), w_bits, eps)]
+
+
+def _e4m3_codes(ys, quant_op):
     amax = max((abs(frac(y)) for y in ys), default=Fraction(0))
     scale = rn32(amax / 448)
     if scale == 0:

@@ -62,6 +62,25 @@ MUTANTS = {
     "e2m1_nibbles_swapped": ("q_out[i / 2] = (uint8_t)(c0 | (c1 << 4));", "q_out[i / 2] = (uint8_t)(c1 | (c0 << 4));"),
     "e4m3_quotient_by_reciprocal": ("q_out[i] = s != 0.0f ? oracle_e4m3_rne(y[i] / s) : 0;",
                                     "q_out[i] = s != 0.0f ? oracle_e4m3_rne(y[i] * (1.0f / s)) : 0;"),
+    "qk_group_scale_index_by_group_only": ("q_scale + r * groups + g,", "q_scale + g,"),
+    "qk_group_codes_offset_by_group_index": ("(uint8_t*)q_out + base + g * group_size,",
+                                             "(uint8_t*)q_out + base + g,"),
+    "qk_group_values_not_offset": ("q_scale + r * groups + g, y + g * group_size, group_size);",
+                                   "q_scale + r * groups + g, y, group_size);"),
+    "qk_group_scale_over_whole_row": (
+        "for (int64_t g = 0; g < groups; ++g)\n                quantize_row_e4m3(",
+        "float am = 0.0f;\n"
+        "            for (int64_t i = 0; i < hidden; ++i) am = fmaxf(am, fabsf(y[i]));\n"
+        "            for (int64_t g = 0; g < groups; ++g)\n"
+        "                for (int64_t i = 0; i < group_size; ++i) {\n"
+        "                    float s = am / E4M3_MAX; q_scale[r * groups + g] = s;\n"
+        "                    ((uint8_t*)q_out)[base + g * group_size + i] =\n"
+        "                        s != 0.0f ? oracle_e4m3_rne(y[g * group_size + i] / s) : 0; }\n"
+        "            if (0) for (int64_t g = 0; g < groups; ++g)\n                quantize_row_e4m3("),
+    "qk_k_uses_q_eps": ("k_weight, k_eps, n_k_rows", "k_weight, q_eps, n_k_rows"),
+    "qk_k_uses_q_weight": ("k_weight, k_eps, n_k_rows", "q_weight, k_eps, n_k_rows"),
+    "qk_q_residual_ignored": ("residual ? residual + base : NULL, weight, eps, hidden, padded,\n                        ORACLE_STORE_RNE, NULL, NULL);\n        if (group_size == 0)",
+                              "NULL, weight, eps, hidden, padded,\n                        ORACLE_STORE_RNE, NULL, NULL);\n        if (group_size == 0)"),
 }
 
 
