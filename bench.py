@@ -20,6 +20,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import dataclasses
 import hashlib
 import json
 import os
@@ -39,6 +40,7 @@ import deterministic_residual_add_gb300 as dr  # noqa: E402
 from deterministic_residual_add_gb300 import inputs  # noqa: E402
 
 METRIC = "add+RMSNorm GB/s and % of HBM peak at 4096×4096 bf16; bit-exact vs oracle"
+QK_METRIC = "fused q/k RMSNorm GB/s and % of HBM peak; bit-exact vs oracle"
 N_SETS = 4
 KERNEL_SOURCES = ["csrc/dradd_kernels.cuh", "csrc/dradd_device.cuh"]
 TRAFFIC_FILE = ROOT / "profiles" / "add_rmsnorm_fwd_4096x4096_ncu.md"
@@ -458,6 +460,187 @@ def run_ours(args):
         tdist.destroy_process_group()
 
 
+# ------------------------------------------------------- fused q/k RMSNorm
+def qk_algorithmic_bytes(w, n_tokens: int) -> int:
+    """q: bf16 read, residual read + residual_out write (with a residual),
+    e4m3 codes (1 byte) + a 4-byte scale per group, or a bf16 store; k: bf16
+    read and store; both weights once."""
+    eq = n_tokens * w.q_heads * w.q_head
+    ek = n_tokens * w.k_heads * w.k_head
+    q_bytes = 2 * eq + (4 * eq if w.residual else 0)
+    q_bytes += (eq + 4 * eq // w.group_size) if w.group_size else 2 * eq
+    return q_bytes + 4 * ek + 2 * (w.q_head + w.k_head)
+
+
+def qk_oracle_fn(o, w):
+    def fn(d):
+        return o.qk_rmsnorm_fwd(d["q"], d["q_weight"], d["k"], d["k_weight"], inputs.EPS, inputs.EPS,
+                                group_size=w.group_size, q_residual=d["residual"])
+    return fn
+
+
+def qk_slice(d, w, lo, hi):
+    """Tokens [lo, hi) of a q/k input dict."""
+    out = dict(d)
+    out["q"] = d["q"][lo * w.q_heads:hi * w.q_heads]
+    out["k"] = d["k"][lo * w.k_heads:hi * w.k_heads]
+    if d["residual"] is not None:
+        out["residual"] = d["residual"][lo * w.q_heads:hi * w.q_heads]
+    return out
+
+
+def run_qk(args):
+    """The fused q/k RMSNorm workloads: same timing rules as the main op,
+    with enough rotating buffer sets to exceed L2 four times over."""
+    import numpy as np
+    world, rank, local = dist_setup()
+    device = torch.device("cuda", local)
+    w = inputs.QK_WORKLOADS[args.workload]
+    L = dr.lib()
+    stream = torch.cuda.Stream(device)
+    d0 = w.make()
+    bytes_step = qk_algorithmic_bytes(w, w.n_tokens)
+    n_sets = max(N_SETS, -(-(4 * 129 * 2**20) // bytes_step))
+    nq, nk = d0["q"].shape[0], d0["k"].shape[0]
+    qw, kw = d0["q_weight"].to(device), d0["k_weight"].to(device)
+    sets = []
+    for i in range(n_sets):
+        g = inputs.generator(2000 + i)
+        q = d0["q"] if i == 0 else inputs.normal_bf16(g, tuple(d0["q"].shape), 0.0, 1.0)
+        k = d0["k"] if i == 0 else inputs.normal_bf16(g, tuple(d0["k"].shape), 0.0, 1.0)
+        s = {"q": q.to(device), "k": k.to(device), "k_out": torch.empty(tuple(k.shape), dtype=torch.bfloat16,
+                                                                          device=device)}
+        s["r"] = d0["residual"].to(device) if w.residual else None
+        s["ro"] = torch.empty_like(s["q"]) if w.residual else None
+        if w.group_size:
+            s["q_out"] = torch.empty(tuple(q.shape), dtype=torch.uint8, device=device)
+            s["q_scale"] = torch.empty(nq, w.q_head // w.group_size, dtype=torch.float32, device=device)
+        else:
+            s["q_out"] = torch.empty_like(s["q"])
+            s["q_scale"] = None
+        sets.append(s)
+    torch.cuda.synchronize()
+    eps = ctypes.c_float(inputs.EPS)
+    st = stream.cuda_stream
+    argv = []
+    for s in sets:
+        argv.append((s["q_out"].data_ptr(), s["q_scale"].data_ptr() if s["q_scale"] is not None else None,
+                     s["ro"].data_ptr() if s["ro"] is not None else None, s["k_out"].data_ptr(),
+                     s["q"].data_ptr(), s["r"].data_ptr() if s["r"] is not None else None, qw.data_ptr(),
+                     s["k"].data_ptr(), kw.data_ptr(), eps, eps, nq, w.q_head, nk, w.k_head, w.group_size, st))
+    fn = L.fused_qk_rmsnorm_group_quant_fwd
+
+    def call(i):
+        rc = fn(*argv[i % n_sets])
+        if rc != 0:
+            raise dr.DraddError(rc, "fused_qk_rmsnorm_group_quant_fwd")
+
+    with torch.cuda.stream(stream):
+        sampler = ClockSampler(local)
+        with sampler:
+            ms = time_device(call, args.steps, args.warmup, stream, world, args.graph)
+    ms = max_over_ranks(ms, world)
+    ms_per_step = ms / args.steps
+    per_launch_gbs = bytes_step / (ms_per_step / 1e3) / 1e9
+    peak = measured_peaks().get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    if not peak:
+        peak = 6800.0
+    sm_count = torch.cuda.get_device_properties(device).multi_processor_count
+    plan = dr.qk_resolve_config(nq, w.q_head, nk, w.k_head, w.group_size, sm_count=sm_count)
+    qdesc = (f"q {w.q_heads}x{w.q_head}" + (" + residual" if w.residual else "") +
+             (f" -> e4m3 groups of {w.group_size}" if w.group_size else " -> bf16"))
+    line = {
+        "metric": QK_METRIC, "value": round(world * bytes_step * args.steps / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"fused_qk_rmsnorm_group_quant_fwd {w.n_tokens} tokens: {qdesc}; "
+                               f"k {w.k_heads}x{w.k_head} -> bf16",
+                   "n_q_rows": nq, "q_hidden": w.q_head, "n_k_rows": nk, "k_hidden": w.k_head,
+                   "group_size": w.group_size, "io_dtype": "bf16",
+                   "l2": f"{n_sets} rotating buffer sets ({n_sets * bytes_step // 2**20} MiB) > L2",
+                   "launch": dataclasses.asdict(plan), "cuda_graph": bool(args.graph),
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": round(world * w.n_tokens * args.steps / (ms / 1e3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(per_launch_gbs, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(per_launch_gbs / peak, 4), "peak_source": f"{peak_src} hbm_gbs",
+                     "traffic": None, "algorithmic_bytes_per_launch": bytes_step},
+        "gpu_launches": args.steps,
+        "e2e": None,
+    }
+    if rank == 0:
+        line["clocks"] = sampler.summary()
+        if not args.no_cpu:
+            import oracle
+            fn_o = qk_oracle_fn(oracle.lib(), w)
+            chunk = 16
+            tokens, first = 0, None
+            t0 = time.perf_counter()
+            while True:
+                lo = tokens % w.n_tokens
+                hi = min(w.n_tokens, lo + chunk)
+                res = fn_o(qk_slice(d0, w, lo, hi))
+                first = first or res
+                tokens += hi - lo
+                if time.perf_counter() - t0 >= args.cpu_seconds:
+                    break
+            dt = time.perf_counter() - t0
+            s0 = sets[0]
+            got = {"q_out": s0["q_out"][:chunk * w.q_heads], "k_out": s0["k_out"][:chunk * w.k_heads]}
+            if w.group_size:
+                got["q_scale"] = s0["q_scale"][:chunk * w.q_heads]
+            if w.residual:
+                got["q_residual_out"] = s0["ro"][:chunk * w.q_heads]
+
+            def raw(t):
+                t = t.detach().cpu().contiguous()
+                return t.view(torch.uint8).numpy() if t.dtype != torch.uint8 else t.numpy()
+            exact = all(np.array_equal(raw(got[k]), np.ascontiguousarray(first[k]).view(np.uint8))
+                        for k in got)
+            line["cpu_baseline"] = {
+                "value": round(qk_algorithmic_bytes(w, tokens) / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+                "kind": "oracle", "sample": f"{tokens} tokens of the {w.n_tokens}-token workload in {dt:.1f} s, "
+                                            "single thread", "seconds": round(dt, 3),
+                "parity_rows_checked": chunk, "parity_bit_exact": bool(exact)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+
+
+def run_qk_reference(args):
+    """The oracle on the host cores for a fused q/k workload."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    import oracle
+    w = inputs.QK_WORKLOADS[args.workload]
+    fn = qk_oracle_fn(oracle.lib(), w)
+    d0 = w.make()
+    t0 = time.perf_counter()
+    fn(qk_slice(d0, w, 0, 4))
+    t_tok = max(1e-6, (time.perf_counter() - t0) / 4)
+    total = args.warmup + args.steps
+    tokens = int(max(1, min(w.n_tokens, args.reference_seconds / total / t_tok)))
+    for _ in range(args.warmup):
+        fn(qk_slice(d0, w, 0, tokens))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        lo = (i * tokens) % (w.n_tokens - tokens + 1)
+        fn(qk_slice(d0, w, lo, lo + tokens))
+    dt = time.perf_counter() - t0
+    value = qk_algorithmic_bytes(w, tokens) * args.steps / dt / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": QK_METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"fused_qk_rmsnorm_group_quant_fwd {args.workload} (CPU oracle)",
+                   "tokens_per_step": tokens},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{tokens} of {w.n_tokens} tokens per step, single thread"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0}), flush=True)
+
+
 def run_reference(args):
     """The oracle on the host cores, on the same metric, unit and workload:
     each step runs a bounded sample of rows of the batch."""
@@ -512,7 +695,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(WORKLOADS), default="4096x4096")
+    ap.add_argument("--workload", choices=list(WORKLOADS) + list(inputs.QK_WORKLOADS), default="4096x4096")
     ap.add_argument("--graph", type=int, default=1, help="replay the timed steps from CUDA graphs")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-e2e", action="store_true")
@@ -522,10 +705,11 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    qk = args.workload in inputs.QK_WORKLOADS
     if args.impl == "reference":
-        run_reference(args)
+        (run_qk_reference if qk else run_reference)(args)
     else:
-        run_ours(args)
+        (run_qk if qk else run_ours)(args)
 
 
 if __name__ == "__main__":

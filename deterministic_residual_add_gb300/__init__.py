@@ -78,6 +78,24 @@ class LaunchConfig:
                             c.fault_inject, c.wait_limit_us, c.serialize)
 
 
+class _QkPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "threads_per_cta", "q_threads_per_row", "q_rows_per_cta", "q_ctas", "k_threads_per_row",
+        "k_rows_per_cta", "k_ctas")]
+
+
+@dataclass
+class QkPlan:
+    """Mirror of dradd_qk_plan: how a fused q/k call spreads its rows."""
+    threads_per_cta: int
+    q_threads_per_row: int
+    q_rows_per_cta: int
+    q_ctas: int
+    k_threads_per_row: int
+    k_rows_per_cta: int
+    k_ctas: int
+
+
 _lib = None
 _vp, _i64, _f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float
 
@@ -99,6 +117,7 @@ def lib() -> ctypes.CDLL:
     bf16_args = [_vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp]
     quant_args = [_vp, _vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp]
     cfgp = ctypes.POINTER(_LaunchCfg)
+    qk_args = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _f32, _i64, _i64, _i64, _i64, _i64, _vp]
     for name, args in [("add_rmsnorm_fwd", bf16_args),
                        ("add_rmsnorm_quant_fwd", quant_args),
                        ("add_rmsnorm_fwd_with_config", bf16_args + [cfgp]),
@@ -117,6 +136,10 @@ def lib() -> ctypes.CDLL:
                        ("rmsnorm_fp4_fwd", [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp]),
                        ("rmsnorm_fp4_fwd_with_config", [_vp, _vp, _vp, _vp, _f32, _i64, _i64, _vp, cfgp]),
                        ("dradd_resolve_config", [_i64, _i64, ctypes.c_int, ctypes.c_int, cfgp]),
+                       ("fused_qk_rmsnorm_group_quant_fwd", qk_args),
+                       ("fused_qk_rmsnorm_group_quant_fwd_with_config", qk_args + [cfgp]),
+                       ("dradd_qk_resolve_config", [_i64, _i64, _i64, _i64, _i64, ctypes.c_int, cfgp,
+                                                    ctypes.POINTER(_QkPlan)]),
                        ("dradd_device_status", [_vp, ctypes.c_int]),
                        ("dradd_bf16_convert_range", [_vp, ctypes.c_uint64, _i64, ctypes.c_int, _vp])]:
         f = getattr(L, name)
@@ -435,6 +458,62 @@ def residual_add_fwd(x, residual, *, residual_out=None, stream=None):
     with torch.cuda.device(x.device):
         _check(lib().residual_add_fwd(*args), "residual_add_fwd")
     return residual_out
+
+
+def fused_qk_rmsnorm_group_quant_fwd(q, q_weight, k, k_weight, q_eps: float = 1e-6, k_eps: float = 1e-6, *,
+                                     group_size: int = 0, q_residual=None, q_out=None, q_scale=None,
+                                     q_residual_out=None, k_out=None, stream=None,
+                                     config: LaunchConfig | None = None):
+    """Fused q/k RMSNorm in one launch: q rows (optionally + q_residual) with
+    bf16 out (group_size 0) or per-group e4m3 out, k rows plain with bf16
+    out.  Returns (q_out, q_scale, q_residual_out, k_out); q_scale is None
+    for bf16 out, q_residual_out None without a q residual."""
+    torch = _torch()
+    n_q, hq = _shape(q, None)
+    n_k, hk = _shape(k, None)
+    nq, nk = n_q * hq, n_k * hk
+    g = int(group_size)
+    if q_out is None:
+        q_out = torch.empty(q.shape, dtype=torch.uint8 if g else torch.bfloat16, device=q.device)
+    if g:
+        if q_out.dtype != torch.uint8:
+            raise ValueError("q_out must hold uint8 e4m3 codes")
+        if q_scale is None:
+            q_scale = torch.empty((*q.shape[:-1], hq // g if hq % g == 0 else 0), dtype=torch.float32,
+                                  device=q.device)
+        _check_quant_outs(q_out.view(torch.int8), q_scale.view(-1), nq, n_q * (hq // g) if hq % g == 0 else 0)
+        q_out_ptr, scale_ptr = q_out.data_ptr(), q_scale.data_ptr()
+    else:
+        q_out_ptr, scale_ptr = _bf16_ptr(q_out, "q_out", nq), 0
+    if q_residual is not None and q_residual_out is None:
+        q_residual_out = torch.empty_like(q)
+    if k_out is None:
+        k_out = torch.empty_like(k)
+    args = (q_out_ptr, scale_ptr,
+            _bf16_ptr(q_residual_out, "q_residual_out", nq) if q_residual is not None else 0,
+            _bf16_ptr(k_out, "k_out", nk), _bf16_ptr(q, "q", nq),
+            _bf16_ptr(q_residual, "q_residual", nq) if q_residual is not None else 0,
+            _bf16_ptr(q_weight, "q_weight", hq), _bf16_ptr(k, "k", nk), _bf16_ptr(k_weight, "k_weight", hk),
+            float(q_eps), float(k_eps), n_q, hq, n_k, hk, g, _stream_handle(stream, q.device))
+    with torch.cuda.device(q.device):
+        if config is None:
+            _check(lib().fused_qk_rmsnorm_group_quant_fwd(*args), "fused_qk_rmsnorm_group_quant_fwd")
+        else:
+            c = config._c()
+            _check(lib().fused_qk_rmsnorm_group_quant_fwd_with_config(*args, ctypes.byref(c)),
+                   "fused_qk_rmsnorm_group_quant_fwd_with_config")
+    return q_out, (q_scale if g else None), (q_residual_out if q_residual is not None else None), k_out
+
+
+def qk_resolve_config(n_q_rows: int, q_hidden: int, n_k_rows: int, k_hidden: int, group_size: int = 0,
+                      sm_count: int = 152, config: LaunchConfig | None = None) -> QkPlan:
+    """The plan the fused q/k call would use (no GPU needed for sm_count > 0)."""
+    plan = _QkPlan()
+    c = config._c() if config is not None else None
+    _check(lib().dradd_qk_resolve_config(int(n_q_rows), int(q_hidden), int(n_k_rows), int(k_hidden),
+                                         int(group_size), int(sm_count), ctypes.byref(c) if c is not None else None,
+                                         ctypes.byref(plan)), "dradd_qk_resolve_config")
+    return QkPlan(*(getattr(plan, f) for f, _ in _QkPlan._fields_))
 
 
 def device_status(stream=None, clear: bool = True, device=None) -> int:

@@ -361,6 +361,228 @@ dradd_status run(int out_kind, bool add, dradd_bf16* out, int8_t* out_q, float* 
     return e == cudaSuccess ? DRADD_OK : DRADD_ERR_CUDA;
 }
 
+// ---------------------------------------------------------- fused q/k RMSNorm
+struct QkSide {
+    bool active = false;
+    int64_t n_rows = 0, hidden = 0;
+    int K = 0, T = 0, R = 0;
+    int64_t ctas = 0;
+};
+
+dradd_status qk_check_side(int64_t n_rows, int64_t hidden)
+{
+    if (hidden <= 0)
+        return DRADD_ERR_BAD_SHAPE;
+    if (hidden % 8 != 0 || hidden > DRADD_QK_MAX_HIDDEN)
+        return DRADD_ERR_UNSUPPORTED_HIDDEN;
+    if (n_rows > (INT64_MAX / 4) / hidden)
+        return DRADD_ERR_BAD_SHAPE;
+    return DRADD_OK;
+}
+
+// Shapes and the launch plan of the fused q/k call.  A side with no rows
+// takes no part.  Threads per CTA B (cfg->threads_per_row): automatic
+// max(128, P / 32) over the active sides, at most 512 (so K <= 4).  Each side then takes the smallest K with P / 8 / K <= B,
+// T = P / 8 / K threads per row and R = B / T rows per CTA.  CTAs
+// (cfg->grid_ctas): automatic SMs x 2048 / B; when the two sides need more,
+// they share them in proportion to their elements.
+dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t group_size, int sm_count,
+                     const dradd_launch_cfg* cfg_in, QkSide* q, QkSide* k, int* threads, bool* serialize)
+{
+    if (n_q < 0 || n_k < 0 || group_size < 0)
+        return DRADD_ERR_BAD_SHAPE;
+    q->active = n_q > 0;
+    k->active = n_k > 0;
+    q->n_rows = n_q;
+    k->n_rows = n_k;
+    q->hidden = hq;
+    k->hidden = hk;
+    dradd_status st;
+    if (q->active && (st = qk_check_side(n_q, hq)) != DRADD_OK)
+        return st;
+    if (k->active && (st = qk_check_side(n_k, hk)) != DRADD_OK)
+        return st;
+    if (q->active && group_size != 0 && (!is_pow2(group_size) || group_size < 8 || group_size > 256 ||
+                                         hq % group_size != 0))
+        return DRADD_ERR_BAD_SHAPE;
+    dradd_launch_cfg cfg = {};
+    if (cfg_in)
+        cfg = *cfg_in;
+    if ((cfg.variant != DRADD_VARIANT_AUTO && cfg.variant != DRADD_VARIANT_ROWS) || cfg.rows_per_cta != 0 ||
+        cfg.stages != 0 || cfg.fault_inject != 0 || cfg.wait_limit_us < 0 || cfg.grid_ctas < 0 ||
+        (cfg.serialize != 0 && cfg.serialize != 1))
+        return DRADD_ERR_BAD_CONFIG;
+    *serialize = cfg.serialize != 0;
+    if (!q->active && !k->active) {
+        *threads = 0;
+        return DRADD_OK;
+    }
+    int64_t B = cfg.threads_per_row;
+    if (B == 0) {
+        B = 128;
+        for (const QkSide* s : {q, k}) {
+            if (!s->active)
+                continue;
+            const int64_t want = next_pow2(s->hidden) / 32;
+            if (want > B)
+                B = want;
+        }
+        if (B > 512)
+            B = 512;
+    }
+    if (!is_pow2(B) || B < 32 || B > 1024)
+        return DRADD_ERR_BAD_CONFIG;
+    int max_k = 1;
+    for (QkSide* s : {q, k}) {
+        if (!s->active)
+            continue;
+        const int64_t blocks = next_pow2(s->hidden) / 8;
+        int64_t K = 1;
+        while (blocks / K > B)
+            K *= 2;
+        if (K > 8)
+            return DRADD_ERR_BAD_CONFIG;
+        s->K = static_cast<int>(K);
+        s->T = static_cast<int>(blocks / K);
+        s->R = static_cast<int>(B / s->T);
+        if (s->K > max_k)
+            max_k = s->K;
+    }
+    if (B > dradd::qk_max_threads(max_k))
+        return DRADD_ERR_BAD_CONFIG;
+    if (q->active && group_size != 0 && group_size / 8 > q->T)
+        return DRADD_ERR_BAD_CONFIG;
+
+    const int64_t need_q = q->active ? (n_q + q->R - 1) / q->R : 0;
+    const int64_t need_k = k->active ? (n_k + k->R - 1) / k->R : 0;
+    int64_t C = cfg.grid_ctas;
+    if (C == 0)
+        C = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * (2048 / B);
+    if (C < (q->active ? 1 : 0) + (k->active ? 1 : 0))
+        return DRADD_ERR_BAD_CONFIG;
+    if (need_q + need_k <= C) {
+        q->ctas = need_q;
+        k->ctas = need_k;
+    } else {
+        const double wq = q->active ? static_cast<double>(n_q) * static_cast<double>(hq) : 0.0;
+        const double wk = k->active ? static_cast<double>(n_k) * static_cast<double>(hk) : 0.0;
+        int64_t cq = q->active ? static_cast<int64_t>(static_cast<double>(C) * wq / (wq + wk) + 0.5) : 0;
+        if (q->active && cq < 1)
+            cq = 1;
+        if (k->active && cq > C - 1)
+            cq = C - 1;
+        if (cq > need_q)
+            cq = need_q;
+        int64_t ck = C - cq;
+        if (ck > need_k)
+            ck = need_k;
+        q->ctas = cq;
+        k->ctas = ck;
+    }
+    if (q->ctas + k->ctas > 0x7FFFFFFF)
+        return DRADD_ERR_BAD_CONFIG;
+    *threads = static_cast<int>(B);
+    return DRADD_OK;
+}
+
+dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dradd_bf16* k_out,
+                    const dradd_bf16* q, const dradd_bf16* q_residual, const dradd_bf16* q_weight,
+                    const dradd_bf16* k, const dradd_bf16* k_weight, float q_eps, float k_eps, int64_t n_q,
+                    int64_t hq, int64_t n_k, int64_t hk, int64_t group_size, cudaStream_t stream,
+                    const dradd_launch_cfg* cfg)
+{
+    QkSide sq, sk;
+    int threads = 0;
+    bool serialize = false;
+    // shapes first, with the default SM count; the plan is redone below
+    dradd_status st = qk_plan(n_q, hq, n_k, hk, group_size, 152, cfg, &sq, &sk, &threads, &serialize);
+    if (st != DRADD_OK || threads == 0)
+        return st;
+    const bool quant = group_size != 0;
+    const bool add = q_residual != nullptr;
+    if (sq.active) {
+        if (!q_out || !q || !q_weight || (quant && !q_scale) || (add && !q_residual_out))
+            return DRADD_ERR_NULL_PTR;
+        if (!aligned(q_out, 16) || !aligned(q, 16) || !aligned(q_weight, 16) || (quant && !aligned(q_scale, 4)) ||
+            (add && (!aligned(q_residual, 16) || !aligned(q_residual_out, 16))))
+            return DRADD_ERR_MISALIGNED;
+        if (!std::isfinite(q_eps) || q_eps < 0.0f)
+            return DRADD_ERR_BAD_EPS;
+    }
+    if (sk.active) {
+        if (!k_out || !k || !k_weight)
+            return DRADD_ERR_NULL_PTR;
+        if (!aligned(k_out, 16) || !aligned(k, 16) || !aligned(k_weight, 16))
+            return DRADD_ERR_MISALIGNED;
+        if (!std::isfinite(k_eps) || k_eps < 0.0f)
+            return DRADD_ERR_BAD_EPS;
+    }
+    // Overlaps: outputs never overlap one another; an output may coincide
+    // exactly with the input it replaces (q_out with q when bf16,
+    // q_residual_out with q_residual, k_out with k) and overlap nothing else.
+    const int64_t eq = sq.active ? n_q * hq : 0, ek = sk.active ? n_k * hk : 0;
+    const Range in[5] = {sq.active ? range_of(q, eq * 2) : Range{},
+                         sq.active ? range_of(q_weight, hq * 2) : Range{},
+                         sq.active && add ? range_of(q_residual, eq * 2) : Range{},
+                         sk.active ? range_of(k, ek * 2) : Range{},
+                         sk.active ? range_of(k_weight, hk * 2) : Range{}};
+    const Range out[4] = {sq.active ? range_of(q_out, quant ? eq : eq * 2) : Range{},
+                          sq.active && quant ? range_of(q_scale, n_q * (hq / group_size) * 4) : Range{},
+                          sq.active && add ? range_of(q_residual_out, eq * 2) : Range{},
+                          sk.active ? range_of(k_out, ek * 2) : Range{}};
+    const int may_equal[4] = {quant ? -1 : 0, -1, 2, 3};  // input index each output may equal
+    for (int a = 0; a < 4; ++a) {
+        for (int b = a + 1; b < 4; ++b)
+            if (out[a].overlaps(out[b]))
+                return DRADD_ERR_ALIAS;
+        for (int b = 0; b < 5; ++b)
+            if (out[a].overlaps(in[b]) && !(b == may_equal[a] && out[a].same(in[b])))
+                return DRADD_ERR_ALIAS;
+    }
+    DeviceLimits L;
+    st = query_limits(&L);
+    if (st != DRADD_OK)
+        return st;
+    st = qk_plan(n_q, hq, n_k, hk, group_size, L.sm_count, cfg, &sq, &sk, &threads, &serialize);
+    if (st != DRADD_OK)
+        return st;
+
+    unsigned* status = nullptr;
+    if (dradd::device_status_ptr(&status) != cudaSuccess)
+        return DRADD_ERR_CUDA;
+    auto params = [&](const QkSide& s, const dradd_bf16* x, const dradd_bf16* res, const dradd_bf16* w,
+                      float eps) {
+        Params p = {};
+        p.x = x;
+        p.residual = res;
+        p.weight = w;
+        p.eps = eps;
+        p.hidden = static_cast<int>(s.hidden);
+        p.inv_hidden = is_pow2(s.hidden) ? 1.0f / static_cast<float>(s.hidden) : 0.0f;
+        p.n_rows = s.n_rows;
+        p.threads_per_row = s.T;
+        p.rows_per_cta = s.R;
+        p.wait_limit_ns = kDefaultWaitLimitNs;
+        p.status = status;
+        return p;
+    };
+    Params pq = params(sq, q, q_residual, q_weight, q_eps);
+    if (quant) {
+        pq.out_q = static_cast<int8_t*>(q_out);
+        pq.scale = q_scale;
+        pq.group_blocks = static_cast<int>(group_size / 8);
+    } else {
+        pq.out = static_cast<uint16_t*>(q_out);
+    }
+    pq.residual_out = q_residual_out;
+    Params pk = params(sk, k, nullptr, k_weight, k_eps);
+    pk.out = k_out;
+    const cudaError_t e = dradd::launch_qk(pq, pk, sq.active ? sq.K : 1, sk.active ? sk.K : 1, quant, add,
+                                           static_cast<int>(sq.ctas), static_cast<int>(sk.ctas), threads,
+                                           serialize, stream);
+    return e == cudaSuccess ? DRADD_OK : DRADD_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -566,6 +788,60 @@ dradd_status residual_add_fwd(dradd_bf16* residual_out, const dradd_bf16* x, con
                    cudaSuccess
                ? DRADD_OK
                : DRADD_ERR_CUDA;
+}
+
+dradd_status fused_qk_rmsnorm_group_quant_fwd(void* q_out, float* q_scale, dradd_bf16* q_residual_out,
+                                              dradd_bf16* k_out, const dradd_bf16* q,
+                                              const dradd_bf16* q_residual, const dradd_bf16* q_weight,
+                                              const dradd_bf16* k, const dradd_bf16* k_weight, float q_eps,
+                                              float k_eps, int64_t n_q_rows, int64_t q_hidden, int64_t n_k_rows,
+                                              int64_t k_hidden, int64_t group_size, cudaStream_t stream)
+{
+    return qk_run(q_out, q_scale, q_residual_out, k_out, q, q_residual, q_weight, k, k_weight, q_eps, k_eps,
+                  n_q_rows, q_hidden, n_k_rows, k_hidden, group_size, stream, nullptr);
+}
+
+dradd_status fused_qk_rmsnorm_group_quant_fwd_with_config(
+    void* q_out, float* q_scale, dradd_bf16* q_residual_out, dradd_bf16* k_out, const dradd_bf16* q,
+    const dradd_bf16* q_residual, const dradd_bf16* q_weight, const dradd_bf16* k, const dradd_bf16* k_weight,
+    float q_eps, float k_eps, int64_t n_q_rows, int64_t q_hidden, int64_t n_k_rows, int64_t k_hidden,
+    int64_t group_size, cudaStream_t stream, const dradd_launch_cfg* cfg)
+{
+    if (!cfg)
+        return DRADD_ERR_NULL_PTR;
+    return qk_run(q_out, q_scale, q_residual_out, k_out, q, q_residual, q_weight, k, k_weight, q_eps, k_eps,
+                  n_q_rows, q_hidden, n_k_rows, k_hidden, group_size, stream, cfg);
+}
+
+dradd_status dradd_qk_resolve_config(int64_t n_q_rows, int64_t q_hidden, int64_t n_k_rows, int64_t k_hidden,
+                                     int64_t group_size, int sm_count, const dradd_launch_cfg* cfg,
+                                     dradd_qk_plan* plan)
+{
+    if (!plan)
+        return DRADD_ERR_NULL_PTR;
+    DeviceLimits L;
+    if (sm_count > 0) {
+        L.sm_count = sm_count;
+    } else {
+        const dradd_status st = query_limits(&L);
+        if (st != DRADD_OK)
+            return st;
+    }
+    QkSide sq, sk;
+    int threads = 0;
+    bool serialize = false;
+    const dradd_status st =
+        qk_plan(n_q_rows, q_hidden, n_k_rows, k_hidden, group_size, L.sm_count, cfg, &sq, &sk, &threads, &serialize);
+    if (st != DRADD_OK)
+        return st;
+    plan->threads_per_cta = threads;
+    plan->q_threads_per_row = sq.T;
+    plan->q_rows_per_cta = sq.R;
+    plan->q_ctas = static_cast<int>(sq.ctas);
+    plan->k_threads_per_row = sk.T;
+    plan->k_rows_per_cta = sk.R;
+    plan->k_ctas = static_cast<int>(sk.ctas);
+    return DRADD_OK;
 }
 
 dradd_status dradd_device_status(cudaStream_t stream, int clear)

@@ -11,7 +11,7 @@ namespace dradd {
 struct Params {
     uint16_t* out;            // bf16 out (bf16 variant)
     int8_t* out_q;            // int8, e4m3 or packed e2m1 codes (quantised variants)
-    float* scale;             // per-row scale (quant variant)
+    float* scale;             // per-row (or per-group) scale (quantised variants)
     uint16_t* residual_out;
     const uint16_t* x;
     const uint16_t* residual;
@@ -26,18 +26,25 @@ struct Params {
     int fault_inject;         // staged kernel only
     uint64_t wait_limit_ns;   // staged kernel only
     unsigned* status;         // device status word (set on an expired wait)
+    int group_blocks;         // per-group e4m3 out: 8-element blocks per group
 };
 
 constexpr unsigned kDeviceStatusTimeout = 1u;
 
 // What a normalised row is stored as.
-enum OutKind : int { kOutBf16 = 0, kOutInt8 = 1, kOutE4m3 = 2, kOutE2m1 = 3 };
+enum OutKind : int { kOutBf16 = 0, kOutInt8 = 1, kOutE4m3 = 2, kOutE2m1 = 3, kOutE4m3Group = 4 };
 
 using KernelFn = void (*)(Params);
+// Fused q/k RMSNorm: (q rows, k rows, number of CTAs given to the q rows).
+using QkKernelFn = void (*)(Params, Params, int);
 
 // Largest CTA for K blocks per thread: the register budget of the bigger
 // tiles (K * 8 accumulators per thread) needs the smaller CTA.
 constexpr int max_threads_for(int K) { return K <= 2 ? 1024 : 512; }
+
+// Largest CTA of the fused q/k kernel whose larger side has K blocks per
+// thread: 128 registers per thread up to K = 4, 255 at K = 8, no spills.
+constexpr int qk_max_threads(int K) { return K <= 4 ? 512 : 256; }
 
 // Resident CTAs per SM the staged kernel with T threads and K blocks per
 // thread is compiled for: the register budget per thread is about 40 for
@@ -70,6 +77,13 @@ KernelFn staged_fn_norm_bf16(int T, int K);
 KernelFn staged_fn_norm_int8(int T, int K);
 KernelFn staged_fn_norm_e4m3(int T, int K);
 KernelFn staged_fn_norm_e2m1(int T, int K);
+// Fused q/k RMSNorm (register kernel): CTAs [0, q_ctas) take the q rows,
+// the next k_ctas the k rows; kq / kk blocks of 8 per thread on each side.
+// quant: per-group e4m3 q out (else bf16); add: q has a residual.
+cudaError_t launch_qk(const Params& pq, const Params& pk, int kq, int kk, bool quant, bool add, int q_ctas,
+                      int k_ctas, int threads, bool serialize, cudaStream_t stream);
+QkKernelFn qk_fn_bf16(int kq, int kk, bool add);
+QkKernelFn qk_fn_e4m3(int kq, int kk, bool add);
 cudaError_t launch_residual_add(uint16_t* residual_out, const uint16_t* x, const uint16_t* residual,
                                 int64_t n_vec, int sm_count, bool serialize, cudaStream_t stream);
 cudaError_t launch_convert(uint16_t* out, uint64_t first, int64_t count, int method, cudaStream_t stream);

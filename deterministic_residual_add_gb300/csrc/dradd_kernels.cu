@@ -2,7 +2,8 @@
 // conversion test kernel, the device status word and every launcher.  The
 // staged kernels are instantiated in dradd_staged_<mode>_<out>.cu (one
 // translation unit per mode and output kind, compiled in parallel) and
-// reached through staged_fn_<mode>_<out>.
+// reached through staged_fn_<mode>_<out>; the fused q/k kernels likewise in
+// dradd_qk_<out>.cu through qk_fn_<out>.
 #include <atomic>
 
 #include "dradd_kernels.cuh"
@@ -240,6 +241,15 @@ size_t staged_static_smem(int K)
 {
     // s_sum[2][32 * K] + s_max[2][32], as declared in staged_kernel
     return sizeof(float) * (2 * 32 * static_cast<size_t>(K) + 2 * 32);
+}
+
+cudaError_t launch_qk(const Params& pq, const Params& pk, int kq, int kk, bool quant, bool add, int q_ctas,
+                      int k_ctas, int threads, bool serialize, cudaStream_t stream)
+{
+    QkKernelFn fn = quant ? qk_fn_e4m3(kq, kk, add) : qk_fn_bf16(kq, kk, add);
+    if (!fn)
+        return cudaErrorInvalidValue;
+    return launch(fn, q_ctas + k_ctas, threads, 0, serialize, stream, pq, pk, q_ctas);
 }
 
 cudaError_t launch_residual_add(uint16_t* residual_out, const uint16_t* x, const uint16_t* residual,

@@ -27,6 +27,8 @@
 //   rows_kernel    rows are loaded straight into registers with streaming
 //                  16-byte loads; a CTA handles rows_per_cta rows side by side
 //                  and loops over the rows with a grid stride.
+//   qk_kernel      two rows_kernel bodies in one launch (fused q/k RMSNorm),
+//                  the q side optionally with per-group e4m3 out.
 //   staged_kernel  persistent CTAs stage whole rows of x (and residual) into
 //                  shared memory with 1-D bulk asynchronous copies (TMA
 //                  engine), `stages` rows ahead of the compute; the copy for
@@ -98,6 +100,31 @@ __device__ __forceinline__ void finish_row(const Params& p, float (&acc)[K][8], 
                 const int b = t + j * T;
                 if (b < nblocks)
                     st_stream(orow + b, pack8_rne(acc[j]));
+            }
+        }
+    } else if constexpr (OUT == kOutE4m3Group) {
+        // A group is gb consecutive blocks, gb a power of two <= min(T, 32)
+        // that divides nblocks.  Block t + jT belongs to group (t + jT) / gb,
+        // and since gb divides T the gb lanes of an aligned lane group hold
+        // one group for every j: its amax is their butterfly max (exact,
+        // so independent of the order).  Padding blocks form whole groups
+        // of their own and are never stored.
+        const int gb = p.group_blocks;
+        const int64_t groups = nblocks / gb;
+        uint2* qrow = reinterpret_cast<uint2*>(p.out_q + row * p.hidden);
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            float m = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                m = fmaxf(m, fabsf(acc[j][e]));
+            m = butterfly_max(m, gb);
+            const float scale = __fdiv_rn(m, 448.0f);
+            const int b = t + j * T;
+            if (active && b < nblocks) {
+                if ((b & (gb - 1)) == 0)
+                    p.scale[row * groups + b / gb] = scale;
+                st_stream(qrow + b, quantize8_e4m3(acc[j], make_e4m3_scale(scale)));
             }
         }
     } else {
@@ -199,8 +226,9 @@ __device__ __forceinline__ void record_timeout(const Params& p)
 }
 
 // ---------------------------------------------------------------- rows_kernel
+// The CTA numbered `cta` of `n_ctas` handles row groups cta, cta + n_ctas, ...
 template <int K, int OUT, bool ADD>
-__global__ void __launch_bounds__(max_threads_for(K)) rows_kernel(const Params p)
+__device__ __forceinline__ void rows_body(const Params& p, int64_t cta, int64_t n_ctas)
 {
     __shared__ float s_sum[2][32 * K];
     __shared__ float s_max[2][32];
@@ -218,9 +246,9 @@ __global__ void __launch_bounds__(max_threads_for(K)) rows_kernel(const Params p
     uint4 w[K];
     load_weights<K>(p, w, t, T, nblocks);
 
-    const int64_t rows_per_step = static_cast<int64_t>(gridDim.x) * p.rows_per_cta;
+    const int64_t rows_per_step = n_ctas * p.rows_per_cta;
     int buf = 0;
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * p.rows_per_cta; base < p.n_rows;
+    for (int64_t base = cta * p.rows_per_cta; base < p.n_rows;
          base += rows_per_step) {
         const int64_t row = base + r_local;
         const bool active = row < p.n_rows;
@@ -250,6 +278,51 @@ __global__ void __launch_bounds__(max_threads_for(K)) rows_kernel(const Params p
         finish_row<K, OUT>(p, acc, w, inv, row, active, t, T, lane, warp_in_row, nblocks,
                              &s_max[buf][r_local * warps_per_row]);
         buf ^= 1;
+    }
+}
+
+template <int K, int OUT, bool ADD>
+__global__ void __launch_bounds__(max_threads_for(K)) rows_kernel(const Params p)
+{
+    rows_body<K, OUT, ADD>(p, blockIdx.x, gridDim.x);
+}
+
+// ------------------------------------------------------------------ qk_kernel
+// Fused q/k RMSNorm in one launch: CTAs [0, q_ctas) run the q rows (residual
+// add with QADD; per-group e4m3 out with QQUANT, else bf16), the rest the k
+// rows (plain, bf16).  Both sides use the CTA's threads, each with its own
+// split into threads per row, rows per CTA and blocks per thread.
+template <int KQ, int KK, bool QQUANT, bool QADD>
+__global__ void __launch_bounds__(qk_max_threads(KQ > KK ? KQ : KK)) qk_kernel(const Params pq, const Params pk, int q_ctas)
+{
+    const int cta = static_cast<int>(blockIdx.x);
+    if (cta < q_ctas)
+        rows_body<KQ, QQUANT ? kOutE4m3Group : kOutBf16, QADD>(pq, cta, q_ctas);
+    else
+        rows_body<KK, kOutBf16, false>(pk, cta - q_ctas, static_cast<int>(gridDim.x) - q_ctas);
+}
+
+template <int KQ, bool QQUANT, bool QADD>
+QkKernelFn qk_by_kk(int kk)
+{
+    switch (kk) {
+    case 1: return qk_kernel<KQ, 1, QQUANT, QADD>;
+    case 2: return qk_kernel<KQ, 2, QQUANT, QADD>;
+    case 4: return qk_kernel<KQ, 4, QQUANT, QADD>;
+    case 8: return qk_kernel<KQ, 8, QQUANT, QADD>;
+    default: return nullptr;
+    }
+}
+
+template <bool QQUANT, bool QADD>
+QkKernelFn qk_table(int kq, int kk)
+{
+    switch (kq) {
+    case 1: return qk_by_kk<1, QQUANT, QADD>(kk);
+    case 2: return qk_by_kk<2, QQUANT, QADD>(kk);
+    case 4: return qk_by_kk<4, QQUANT, QADD>(kk);
+    case 8: return qk_by_kk<8, QQUANT, QADD>(kk);
+    default: return nullptr;
     }
 }
 

@@ -19,6 +19,17 @@ Workloads (n_rows x hidden, distributions as N(mean, std)):
 
 Within one workload the draws come from one generator in the order
 x, residual, weight.  eps is 1e-6 everywhere.
+
+Fused q/k RMSNorm workloads (QK_WORKLOADS; the page names the kernel but
+gives no shapes, so these are the two common layouts, with the main
+workloads' distributions): per token, q rows N(0,1) with a residual
+N(0,4), k rows N(0,1); both weights N(1,0.1); draws in the order q,
+residual, q weight, k, k weight.
+
+  qk_lowrank4096  4096 tokens: q 1 x 1536 (+ residual, e4m3 groups of 128),
+                  k 1 x 512                                           seed 5
+  qk_heads4096    4096 tokens: q 32 heads x 128, k 8 heads x 128, bf16 out,
+                  no residual                                         seed 6
 """
 from __future__ import annotations
 
@@ -158,6 +169,44 @@ def edge_rows(n_rows: int = 16, hidden: int = 1024, seed: int = 0):
 def bits(t: torch.Tensor) -> torch.Tensor:
     """bf16 tensor -> int16 view of its bits (no arithmetic)."""
     return t.view(torch.int16)
+
+
+@dataclass(frozen=True)
+class QkWorkload:
+    """Fused q/k RMSNorm inputs: q is n_tokens * q_heads rows of q_head
+    elements, k is n_tokens * k_heads rows of k_head."""
+    name: str
+    n_tokens: int
+    q_heads: int
+    q_head: int
+    k_heads: int
+    k_head: int
+    group_size: int
+    residual: bool
+    seed: int
+    residual_std: float = 4.0
+
+    def make(self, n_tokens: int | None = None):
+        """dict(q, residual (or None), q_weight, k, k_weight) as CPU bf16
+        tensors; n_tokens < self.n_tokens keeps the leading tokens."""
+        g = generator(self.seed)
+        nq, nk = self.n_tokens * self.q_heads, self.n_tokens * self.k_heads
+        q = normal_bf16(g, (nq, self.q_head), 0.0, 1.0)
+        r = normal_bf16(g, (nq, self.q_head), 0.0, self.residual_std) if self.residual else None
+        qw = normal_bf16(g, (self.q_head,), 1.0, 0.1)
+        k = normal_bf16(g, (nk, self.k_head), 0.0, 1.0)
+        kw = normal_bf16(g, (self.k_head,), 1.0, 0.1)
+        if n_tokens is not None:
+            q = q[:n_tokens * self.q_heads].contiguous()
+            k = k[:n_tokens * self.k_heads].contiguous()
+            r = r[:n_tokens * self.q_heads].contiguous() if r is not None else None
+        return {"q": q, "residual": r, "q_weight": qw, "k": k, "k_weight": kw}
+
+
+QK_WORKLOADS = {
+    "qk_lowrank4096": QkWorkload("qk_lowrank4096", 4096, 1, 1536, 1, 512, group_size=128, residual=True, seed=5),
+    "qk_heads4096": QkWorkload("qk_heads4096", 4096, 32, 128, 8, 128, group_size=0, residual=False, seed=6),
+}
 
 
 def hashed_bf16_rows(rows: torch.Tensor, hidden: int, salt: int) -> torch.Tensor:

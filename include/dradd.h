@@ -61,6 +61,7 @@ extern "C" {
 
 #define DRADD_ABI_VERSION 1
 #define DRADD_MAX_HIDDEN 32768
+#define DRADD_QK_MAX_HIDDEN 16384  /* q_hidden, k_hidden of the fused q/k call */
 
 typedef uint16_t dradd_bf16;  /* raw bf16 bit pattern */
 typedef int dradd_status;
@@ -328,6 +329,76 @@ dradd_status rmsnorm_fp4_fwd_with_config(uint8_t* out_q, float* scale, const dra
 dradd_status residual_add_fwd(dradd_bf16* residual_out, const dradd_bf16* x,
                               const dradd_bf16* residual, int64_t n_rows, int64_t hidden,
                               cudaStream_t stream);
+
+/*
+ * fused_qk_rmsnorm_group_quant_fwd -- two independent RMSNorms in one launch
+ * ("q" and "k" rows), q optionally with a residual add and a per-group e4m3
+ * output.  Page: ROCm/aiter issue #5151, section "Notes", which names the
+ * fused q/k RMSNorm + group quant kernel among those whose bf16 residual
+ * stores were not audited; the page prints no formula for it, and this is
+ * the plainest reading of the name on top of the row function above:
+ *   q rows (n_q_rows x q_hidden): with q_residual != NULL, acc = fp32(q) +
+ *     fp32(q_residual) and q_residual_out = bf16_rne(acc) (the residual
+ *     store, round to nearest even); else acc = fp32(q).  y = the row
+ *     function of add_rmsnorm_fwd with q_weight and q_eps.
+ *       group_size == 0: q_out = bf16_rne(y), [n_q_rows x q_hidden] bf16.
+ *       group_size  > 0: y is cut into consecutive groups of group_size
+ *         elements; each group gets scale = amax / 448 and codes
+ *         e4m3(y / scale) exactly as a row of add_rmsnorm_fp8_fwd.
+ *         q_out: [n_q_rows x q_hidden] e4m3 codes (uint8);
+ *         q_scale: [n_q_rows x (q_hidden / group_size)] fp32, row-major.
+ *         group_size: a power of two, 8 <= group_size <= 256, dividing
+ *         q_hidden (else DRADD_ERR_BAD_SHAPE).
+ *   k rows (n_k_rows x k_hidden): plain RMSNorm with k_weight and k_eps,
+ *     k_out = bf16_rne(y).
+ * q_hidden and k_hidden: multiples of 8, at most DRADD_QK_MAX_HIDDEN
+ * (else DRADD_ERR_UNSUPPORTED_HIDDEN).  A per-head q/k norm is the same
+ * call with rows = tokens x heads and hidden = the head size.  Either row count may be 0: that side is then
+ * ignored (its pointers, hidden and eps are not inspected); both 0 is a
+ * no-op.  q_residual_out is written only when q_residual is non-NULL.
+ * Every result is bit-identical to two separate calls of the single-set
+ * entry points and independent of the launch configuration.
+ * Aliasing: q_out may be exactly q (bf16 out only), q_residual_out exactly
+ * q_residual, k_out exactly k; no other overlap.  Alignment: every array
+ * 16 bytes, q_scale 4 bytes.  Other conventions as for add_rmsnorm_fwd.
+ */
+dradd_status fused_qk_rmsnorm_group_quant_fwd(void* q_out, float* q_scale, dradd_bf16* q_residual_out,
+                                              dradd_bf16* k_out, const dradd_bf16* q,
+                                              const dradd_bf16* q_residual, const dradd_bf16* q_weight,
+                                              const dradd_bf16* k, const dradd_bf16* k_weight, float q_eps,
+                                              float k_eps, int64_t n_q_rows, int64_t q_hidden, int64_t n_k_rows,
+                                              int64_t k_hidden, int64_t group_size, cudaStream_t stream);
+
+/*
+ * Test hook: the fused q/k call with an explicit configuration.  Only
+ * variant (AUTO or ROWS), threads_per_row (read here as the threads of a
+ * CTA: a power of two 32..512, at most 256 when a side needs 8 blocks of
+ * 8 per thread, i.e. when P / 8 > 4 x threads), grid_ctas (total CTAs,
+ * shared by the two sides) and serialize are used; rows_per_cta, stages
+ * and fault_inject must be 0.  Results never depend on it.
+ */
+dradd_status fused_qk_rmsnorm_group_quant_fwd_with_config(
+    void* q_out, float* q_scale, dradd_bf16* q_residual_out, dradd_bf16* k_out, const dradd_bf16* q,
+    const dradd_bf16* q_residual, const dradd_bf16* q_weight, const dradd_bf16* k, const dradd_bf16* k_weight,
+    float q_eps, float k_eps, int64_t n_q_rows, int64_t q_hidden, int64_t n_k_rows, int64_t k_hidden,
+    int64_t group_size, cudaStream_t stream, const dradd_launch_cfg* cfg);
+
+/* The launch plan of a fused q/k call (for tests and reports). */
+typedef struct dradd_qk_plan {
+    int threads_per_cta;
+    int q_threads_per_row, q_rows_per_cta, q_ctas;  /* 0 when n_q_rows == 0 */
+    int k_threads_per_row, k_rows_per_cta, k_ctas;  /* 0 when n_k_rows == 0 */
+} dradd_qk_plan;
+
+/*
+ * dradd_qk_resolve_config -- the plan the fused q/k call would use, without
+ * launching.  sm_count > 0 stands in for the device's SM count (no GPU
+ * needed); sm_count <= 0 asks the current device.  cfg may be NULL
+ * (automatic).  Returns the shape and configuration errors of the call.
+ */
+dradd_status dradd_qk_resolve_config(int64_t n_q_rows, int64_t q_hidden, int64_t n_k_rows, int64_t k_hidden,
+                                     int64_t group_size, int sm_count, const dradd_launch_cfg* cfg,
+                                     dradd_qk_plan* plan);
 
 /*
  * dradd_device_status -- synchronise `stream`, then return DRADD_OK or the

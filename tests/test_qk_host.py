@@ -1,0 +1,136 @@
+"""The fused q/k RMSNorm entry points on the host, without a GPU: argument
+checks and the launch plan.  Every call made here returns before any CUDA
+runtime call; nothing is launched."""
+import pytest
+
+import deterministic_residual_add_gb300 as dr
+from deterministic_residual_add_gb300 import build as drbuild
+
+MB = 1 << 20
+BASE = 1 << 41
+Q, QR, QW, K, KW, QO, QS, QRO, KO = (BASE + i * 256 * MB for i in range(9))
+
+
+@pytest.fixture(scope="module")
+def L():
+    drbuild.build()
+    return dr.lib()
+
+
+def call(L, qo=QO, qs=QS, qro=QRO, ko=KO, q=Q, qr=QR, qw=QW, k=K, kw=KW, q_eps=1e-6, k_eps=1e-6,
+         nq=4, hq=1536, nk=4, hk=512, g=128):
+    return L.fused_qk_rmsnorm_group_quant_fwd(qo, qs, qro, ko, q, qr, qw, k, kw, q_eps, k_eps, nq, hq, nk, hk,
+                                              g, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(nq=-1), 2), (dict(nk=-1), 2), (dict(g=-8), 2), (dict(hq=0), 2), (dict(hk=-8), 2),
+    (dict(hq=12), 3), (dict(hk=1001), 3), (dict(hq=16392), 3), (dict(hq=32768), 3),
+    (dict(nq=1 << 62, hq=8), 2),
+    (dict(g=96), 2), (dict(g=4), 2), (dict(g=512), 2), (dict(hq=200, g=16), 2),
+    (dict(qo=0), 1), (dict(qs=0), 1), (dict(qro=0), 1), (dict(ko=0), 1), (dict(q=0), 1),
+    (dict(qw=0), 1), (dict(k=0), 1), (dict(kw=0), 1),
+    (dict(qo=QO + 8), 4), (dict(q=Q + 2), 4), (dict(qs=QS + 2), 4), (dict(qr=QR + 8), 4),
+    (dict(qro=QRO + 4), 4), (dict(ko=KO + 8), 4), (dict(kw=KW + 2), 4),
+    (dict(q_eps=float("nan")), 5), (dict(k_eps=-1.0), 5), (dict(k_eps=float("inf")), 5),
+    (dict(qo=Q), 6),               # e4m3 codes may not overwrite q
+    (dict(ko=Q), 6),               # k out over q
+    (dict(qro=QR + 16), 6),        # shifted alias of the residual
+    (dict(qs=QO + 1024), 6),       # scales inside the codes
+    (dict(ko=KW), 6),              # output over a weight
+    (dict(qro=KO), 6),             # two outputs the same buffer
+])
+def test_argument_errors(L, kw, code):
+    assert call(L, **kw) == code
+
+
+@pytest.mark.parametrize("kw", [
+    dict(nq=0, nk=0),                                   # nothing to do
+])
+def test_noop(L, kw):
+    assert call(L, **kw) == 0
+
+
+def test_inactive_side_is_not_inspected(L):
+    # with no k rows, k's pointers, hidden and eps are ignored: the q checks
+    # still run (a NULL q_out is reported) ...
+    assert call(L, nk=0, k=0, kw=0, ko=0, hk=-5, k_eps=float("nan"), qo=0) == 1
+    # ... and with no q rows, q's
+    assert call(L, nq=0, q=0, qw=0, qo=0, qs=0, hq=12, g=96, q_eps=-1.0, k=0) == 1
+
+
+def test_bf16_q_may_be_updated_in_place_but_not_codes(L):
+    # group_size 0: q_out == q is allowed (reaches the device query, which
+    # fails without a GPU); with codes it is an alias error
+    assert call(L, qo=Q, g=128) == 6
+    assert call(L, qo=Q, g=0) not in (1, 2, 3, 4, 5, 6, 9)
+    assert call(L, qro=QR, ko=K) not in (1, 2, 3, 4, 5, 6, 9)
+
+
+def test_residual_out_unused_without_residual(L):
+    # q_residual NULL: q_residual_out is neither required nor checked
+    assert call(L, qr=0, qro=0, qo=0) == 1
+    assert call(L, qr=0, qro=QO, qo=0) == 1
+
+
+def test_with_config_needs_config(L):
+    assert L.fused_qk_rmsnorm_group_quant_fwd_with_config(QO, QS, QRO, KO, Q, QR, QW, K, KW, 1e-6, 1e-6, 4,
+                                                          1536, 4, 512, 128, None, None) == 1
+
+
+# ------------------------------------------------------------------ the plan
+@pytest.mark.parametrize("nq,hq,nk,hk,g", [
+    (4096, 1536, 4096, 512, 128), (64 * 32, 128, 64 * 8, 128, 0), (8, 16384, 8, 512, 256),
+    (1, 8, 1, 16, 8), (100000, 1536, 0, 512, 64), (0, 1536, 7, 4096, 0), (3, 200, 5, 24, 8),
+    (2048, 8192, 2048, 1024, 32),
+])
+def test_plan_rules(nq, hq, nk, hk, g):
+    p = dr.qk_resolve_config(nq, hq, nk, hk, g, sm_count=152)
+    B = p.threads_per_cta
+    assert B & (B - 1) == 0 and 128 <= B <= 512
+    for n, h, T, R, C in ((nq, hq, p.q_threads_per_row, p.q_rows_per_cta, p.q_ctas),
+                          (nk, hk, p.k_threads_per_row, p.k_rows_per_cta, p.k_ctas)):
+        if n == 0:
+            assert (T, R, C) == (0, 0, 0)
+            continue
+        P = 1 << (h - 1).bit_length()
+        K = P // 8 // T
+        assert T * R == B and K * T == P // 8 and K in (1, 2, 4)
+        assert 1 <= C <= -(-n // R)
+    assert p.q_ctas + p.k_ctas <= 152 * 2048 // B
+    if nq and g:
+        assert g // 8 <= p.q_threads_per_row
+
+
+def test_plan_explicit_threads_and_grid():
+    for B in (64, 128, 256, 512):
+        p = dr.qk_resolve_config(64, 4096, 64, 512, 128, config=dr.LaunchConfig(threads_per_row=B))
+        assert p.threads_per_cta == B
+    p = dr.qk_resolve_config(64, 4096, 64, 512, 128, config=dr.LaunchConfig(threads_per_row=256, grid_ctas=7))
+    assert p.q_ctas + p.k_ctas == 7 and p.q_ctas >= 1 and p.k_ctas >= 1
+    p = dr.qk_resolve_config(64, 4096, 0, 512, 128, config=dr.LaunchConfig(grid_ctas=1))
+    assert (p.q_ctas, p.k_ctas) == (1, 0)
+    # K = 8 needs at most 256 threads; 1024 is never allowed; 32 cannot hold
+    # a 4096-element row with K <= 8
+    p = dr.qk_resolve_config(64, 8192, 0, 0, 0, config=dr.LaunchConfig(threads_per_row=128))
+    assert p.q_threads_per_row == 128
+    for cfg in (dr.LaunchConfig(threads_per_row=1024), dr.LaunchConfig(threads_per_row=32),
+                dr.LaunchConfig(threads_per_row=96), dr.LaunchConfig(variant=2),
+                dr.LaunchConfig(rows_per_cta=2), dr.LaunchConfig(stages=1), dr.LaunchConfig(fault_inject=1),
+                dr.LaunchConfig(grid_ctas=1), dr.LaunchConfig(serialize=2)):
+        with pytest.raises(dr.DraddError) as e:
+            dr.qk_resolve_config(64, 4096, 64, 512, 128, config=cfg)
+        assert e.value.status == 9
+    with pytest.raises(dr.DraddError) as e:
+        dr.qk_resolve_config(64, 16384, 0, 0, 0, config=dr.LaunchConfig(threads_per_row=512 // 2 // 2))
+    assert e.value.status == 9
+    # a group never spans more lanes than a row has threads: with K > 1,
+    # T > B / 2 >= 16, and a group is at most 32 blocks
+    for B in (32, 64, 128, 256, 512):
+        for hq in (256, 512, 2048, 8192):
+            try:
+                p = dr.qk_resolve_config(4, hq, 0, 0, 256, config=dr.LaunchConfig(threads_per_row=B))
+            except dr.DraddError as e:
+                assert e.status == 9
+                continue
+            assert p.q_threads_per_row >= 32
