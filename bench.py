@@ -547,7 +547,8 @@ def run_qk(args):
     if not peak:
         peak = 6800.0
     sm_count = torch.cuda.get_device_properties(device).multi_processor_count
-    plan = dr.qk_resolve_config(nq, w.q_head, nk, w.k_head, w.group_size, sm_count=sm_count)
+    plan = dr.qk_resolve_config(nq, w.q_head, nk, w.k_head, w.group_size, q_residual=w.residual,
+                                sm_count=sm_count)
     qdesc = (f"q {w.q_heads}x{w.q_head}" + (" + residual" if w.residual else "") +
              (f" -> e4m3 groups of {w.group_size}" if w.group_size else " -> bf16"))
     line = {

@@ -53,7 +53,7 @@ class DraddError(RuntimeError):
 class _LaunchCfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "variant", "threads_per_row", "rows_per_cta", "grid_ctas", "stages", "fault_inject",
-        "wait_limit_us", "serialize")]
+        "wait_limit_us", "serialize", "blocks_per_thread")]
 
 
 @dataclass
@@ -67,32 +67,38 @@ class LaunchConfig:
     fault_inject: int = 0
     wait_limit_us: int = 0
     serialize: int = 0
+    blocks_per_thread: int = 0
 
     def _c(self) -> _LaunchCfg:
         return _LaunchCfg(self.variant, self.threads_per_row, self.rows_per_cta, self.grid_ctas,
-                          self.stages, self.fault_inject, self.wait_limit_us, self.serialize)
+                          self.stages, self.fault_inject, self.wait_limit_us, self.serialize,
+                          self.blocks_per_thread)
 
     @staticmethod
     def _from_c(c: _LaunchCfg) -> "LaunchConfig":
         return LaunchConfig(c.variant, c.threads_per_row, c.rows_per_cta, c.grid_ctas, c.stages,
-                            c.fault_inject, c.wait_limit_us, c.serialize)
+                            c.fault_inject, c.wait_limit_us, c.serialize, c.blocks_per_thread)
 
 
 class _QkPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
-        "threads_per_cta", "q_threads_per_row", "q_rows_per_cta", "q_ctas", "k_threads_per_row",
-        "k_rows_per_cta", "k_ctas")]
+        "variant", "threads_per_cta", "dyn_smem_bytes", "q_threads_per_row", "q_rows_per_cta", "q_stages",
+        "q_ctas", "k_threads_per_row", "k_rows_per_cta", "k_stages", "k_ctas")]
 
 
 @dataclass
 class QkPlan:
     """Mirror of dradd_qk_plan: how a fused q/k call spreads its rows."""
+    variant: int
     threads_per_cta: int
+    dyn_smem_bytes: int
     q_threads_per_row: int
     q_rows_per_cta: int
+    q_stages: int
     q_ctas: int
     k_threads_per_row: int
     k_rows_per_cta: int
+    k_stages: int
     k_ctas: int
 
 
@@ -138,8 +144,8 @@ def lib() -> ctypes.CDLL:
                        ("dradd_resolve_config", [_i64, _i64, ctypes.c_int, ctypes.c_int, cfgp]),
                        ("fused_qk_rmsnorm_group_quant_fwd", qk_args),
                        ("fused_qk_rmsnorm_group_quant_fwd_with_config", qk_args + [cfgp]),
-                       ("dradd_qk_resolve_config", [_i64, _i64, _i64, _i64, _i64, ctypes.c_int, cfgp,
-                                                    ctypes.POINTER(_QkPlan)]),
+                       ("dradd_qk_resolve_config", [_i64, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int,
+                                                    cfgp, ctypes.POINTER(_QkPlan)]),
                        ("dradd_device_status", [_vp, ctypes.c_int]),
                        ("dradd_bf16_convert_range", [_vp, ctypes.c_uint64, _i64, ctypes.c_int, _vp])]:
         f = getattr(L, name)
@@ -506,13 +512,16 @@ def fused_qk_rmsnorm_group_quant_fwd(q, q_weight, k, k_weight, q_eps: float = 1e
 
 
 def qk_resolve_config(n_q_rows: int, q_hidden: int, n_k_rows: int, k_hidden: int, group_size: int = 0,
-                      sm_count: int = 152, config: LaunchConfig | None = None) -> QkPlan:
-    """The plan the fused q/k call would use (no GPU needed for sm_count > 0)."""
+                      q_residual: bool = False, sm_count: int = 152,
+                      config: LaunchConfig | None = None) -> QkPlan:
+    """The plan the fused q/k call would use (no GPU needed for sm_count > 0;
+    the real call then sizes the automatic grid by the device's occupancy)."""
     plan = _QkPlan()
     c = config._c() if config is not None else None
     _check(lib().dradd_qk_resolve_config(int(n_q_rows), int(q_hidden), int(n_k_rows), int(k_hidden),
-                                         int(group_size), int(sm_count), ctypes.byref(c) if c is not None else None,
-                                         ctypes.byref(plan)), "dradd_qk_resolve_config")
+                                         int(group_size), int(bool(q_residual)), int(sm_count),
+                                         ctypes.byref(c) if c is not None else None, ctypes.byref(plan)),
+           "dradd_qk_resolve_config")
     return QkPlan(*(getattr(plan, f) for f, _ in _QkPlan._fields_))
 
 

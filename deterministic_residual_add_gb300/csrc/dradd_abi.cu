@@ -195,6 +195,11 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     const bool staged = cfg->variant == DRADD_VARIANT_STAGED;
 
     int auto_stages = 2;
+    if (cfg->threads_per_row == 0 && cfg->blocks_per_thread != 0) {
+        if (!is_pow2(cfg->blocks_per_thread) || cfg->blocks_per_thread > 8 || blocks % cfg->blocks_per_thread != 0)
+            return DRADD_ERR_BAD_CONFIG;
+        cfg->threads_per_row = static_cast<int>(blocks / cfg->blocks_per_thread);
+    }
     if (cfg->threads_per_row == 0) {
         int64_t T;
         if (!staged) {
@@ -231,8 +236,9 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     if (!is_pow2(T) || T > 1024 || blocks % T != 0)
         return DRADD_ERR_BAD_CONFIG;
     const int64_t K = blocks / T;
-    if (K != 1 && K != 2 && K != 4 && K != 8)
+    if ((K != 1 && K != 2 && K != 4 && K != 8) || (cfg->blocks_per_thread != 0 && cfg->blocks_per_thread != K))
         return DRADD_ERR_BAD_CONFIG;
+    cfg->blocks_per_thread = static_cast<int>(K);
     if (staged && T < 32)
         return DRADD_ERR_BAD_CONFIG;
 
@@ -365,9 +371,18 @@ dradd_status run(int out_kind, bool add, dradd_bf16* out, int8_t* out_q, float* 
 struct QkSide {
     bool active = false;
     int64_t n_rows = 0, hidden = 0;
-    int K = 0, T = 0, R = 0;
-    int64_t ctas = 0;
+    int K = 0, T = 0, R = 0, stages = 0;
+    int64_t ctas = 0, stage_bytes = 0;
 };
+
+struct QkLaunch {
+    QkSide q, k;
+    int threads = 0;
+    bool staged = false, serialize = false;
+    int64_t dyn_smem = 0;
+};
+
+constexpr int64_t kQkStageBudget = 96 * 1024;  // automatic stages: bytes per CTA
 
 dradd_status qk_check_side(int64_t n_rows, int64_t hidden)
 {
@@ -381,14 +396,24 @@ dradd_status qk_check_side(int64_t n_rows, int64_t hidden)
 }
 
 // Shapes and the launch plan of the fused q/k call.  A side with no rows
-// takes no part.  Threads per CTA B (cfg->threads_per_row): automatic
-// max(128, P / 32) over the active sides, at most 512 (so K <= 4).  Each side then takes the smallest K with P / 8 / K <= B,
-// T = P / 8 / K threads per row and R = B / T rows per CTA.  CTAs
-// (cfg->grid_ctas): automatic SMs x 2048 / B; when the two sides need more,
-// they share them in proportion to their elements.
-dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t group_size, int sm_count,
-                     const dradd_launch_cfg* cfg_in, QkSide* q, QkSide* k, int* threads, bool* serialize)
+// takes no part.  Variant, threads per CTA B (cfg->threads_per_row) and a
+// least K (cfg->blocks_per_thread) default to the table below.  Each side
+// takes K = the smallest power of two with P / 8 / K <= B, raised to the
+// least K if that is larger (at most P / 8 and 8); then T = P / 8 / K
+// threads per row and R = B / T rows per CTA.  The staged variant gives
+// each side min(2, 96 KiB / stage) stages of R rows (cfg->stages: the same
+// count for both).  CTAs (cfg->grid_ctas):
+// automatic SMs x ctas_per_sm (ctas_per_sm <= 0: 2048 / B); when the two
+// sides need more, they share them in proportion to their elements.
+dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t group_size, bool add,
+                     int sm_count, int ctas_per_sm, int smem_optin, const dradd_launch_cfg* cfg_in, QkLaunch* out)
 {
+    QkSide* q = &out->q;
+    QkSide* k = &out->k;
+    *q = QkSide{};
+    *k = QkSide{};
+    out->threads = 0;
+    out->dyn_smem = 0;
     if (n_q < 0 || n_k < 0 || group_size < 0)
         return DRADD_ERR_BAD_SHAPE;
     q->active = n_q > 0;
@@ -408,56 +433,101 @@ dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t g
     dradd_launch_cfg cfg = {};
     if (cfg_in)
         cfg = *cfg_in;
-    if ((cfg.variant != DRADD_VARIANT_AUTO && cfg.variant != DRADD_VARIANT_ROWS) || cfg.rows_per_cta != 0 ||
-        cfg.stages != 0 || cfg.fault_inject != 0 || cfg.wait_limit_us < 0 || cfg.grid_ctas < 0 ||
-        (cfg.serialize != 0 && cfg.serialize != 1))
+    if (cfg.variant < DRADD_VARIANT_AUTO || cfg.variant > DRADD_VARIANT_STAGED || cfg.rows_per_cta != 0 ||
+        cfg.stages < 0 || cfg.stages > 8 || cfg.fault_inject < 0 || cfg.wait_limit_us < 0 || cfg.grid_ctas < 0 ||
+        (cfg.serialize != 0 && cfg.serialize != 1) ||
+        (cfg.blocks_per_thread != 0 && (!is_pow2(cfg.blocks_per_thread) || cfg.blocks_per_thread > 8)))
         return DRADD_ERR_BAD_CONFIG;
-    *serialize = cfg.serialize != 0;
-    if (!q->active && !k->active) {
-        *threads = 0;
+    out->serialize = cfg.serialize != 0;
+    int64_t max_p = 0;
+    for (const QkSide* side : {q, k})
+        if (side->active && next_pow2(side->hidden) > max_p)
+            max_p = next_pow2(side->hidden);
+    // Automatic choice by the longer side's P, measured on GB300 (CUDA-graph
+    // replays over buffers larger than L2, median of interleaved rounds):
+    //   P <= 256           staged, 64 threads, K >= 4 (4 threads a row)
+    //   256 < P <= 2048    rows kernel, 128 threads, K >= 2
+    //   P > 2048           staged, max(128, P / 8) threads up to 512
+    // with 2 stages per side.
+    int auto_variant = DRADD_VARIANT_STAGED, auto_k = 1;
+    int64_t auto_b = max_p / 8 < 128 ? 128 : (max_p / 8 > 512 ? 512 : max_p / 8);
+    if (max_p <= 256) {
+        auto_b = 64;
+        auto_k = 4;
+    } else if (max_p <= 2048) {
+        auto_variant = DRADD_VARIANT_ROWS;
+        auto_b = 128;
+        auto_k = 2;
+    }
+    // an explicit stage count or the fault hook asks for the staged variant
+    if (cfg.variant == DRADD_VARIANT_AUTO && (cfg.stages != 0 || cfg.fault_inject != 0))
+        auto_variant = DRADD_VARIANT_STAGED;
+    out->staged = (cfg.variant == DRADD_VARIANT_AUTO ? auto_variant : cfg.variant) != DRADD_VARIANT_ROWS;
+    if (!out->staged && (cfg.stages != 0 || cfg.fault_inject != 0))
+        return DRADD_ERR_BAD_CONFIG;
+    if (!q->active && !k->active)
         return DRADD_OK;
-    }
-    int64_t B = cfg.threads_per_row;
-    if (B == 0) {
-        B = 128;
-        for (const QkSide* s : {q, k}) {
-            if (!s->active)
-                continue;
-            const int64_t want = next_pow2(s->hidden) / 32;
-            if (want > B)
-                B = want;
-        }
-        if (B > 512)
-            B = 512;
-    }
+    int64_t B = cfg.threads_per_row != 0 ? cfg.threads_per_row : auto_b;
+    const int64_t k_pref = cfg.blocks_per_thread != 0 ? cfg.blocks_per_thread : auto_k;
     if (!is_pow2(B) || B < 32 || B > 1024)
         return DRADD_ERR_BAD_CONFIG;
     int max_k = 1;
-    for (QkSide* s : {q, k}) {
-        if (!s->active)
+    for (QkSide* side : {q, k}) {
+        if (!side->active)
             continue;
-        const int64_t blocks = next_pow2(s->hidden) / 8;
+        const int64_t blocks = next_pow2(side->hidden) / 8;
         int64_t K = 1;
         while (blocks / K > B)
             K *= 2;
+        int64_t pref = k_pref < blocks ? k_pref : blocks;
+        if (side == q && group_size != 0 && pref > blocks / (group_size / 8))
+            pref = blocks / (group_size / 8);  // a group's lanes stay within one row's threads
+        if (pref > K)
+            K = pref;
         if (K > 8)
             return DRADD_ERR_BAD_CONFIG;
-        s->K = static_cast<int>(K);
-        s->T = static_cast<int>(blocks / K);
-        s->R = static_cast<int>(B / s->T);
-        if (s->K > max_k)
-            max_k = s->K;
+        side->K = static_cast<int>(K);
+        side->T = static_cast<int>(blocks / K);
+        side->R = static_cast<int>(B / side->T);
+        if (side->K > max_k)
+            max_k = side->K;
     }
     if (B > dradd::qk_max_threads(max_k))
         return DRADD_ERR_BAD_CONFIG;
     if (q->active && group_size != 0 && group_size / 8 > q->T)
         return DRADD_ERR_BAD_CONFIG;
 
+    if (out->staged) {
+        const int64_t avail =
+            static_cast<int64_t>(smem_optin) -
+            static_cast<int64_t>(dradd::qk_static_smem(q->active ? q->K : 1, k->active ? k->K : 1)) - 1024;
+        for (QkSide* side : {q, k}) {
+            if (!side->active)
+                continue;
+            const bool side_add = side == q && add;
+            side->stage_bytes = (side_add ? 4 : 2) * side->hidden * side->R;
+            int64_t S = cfg.stages;
+            if (S == 0) {
+                S = kQkStageBudget / side->stage_bytes;
+                if (S > 2)
+                    S = 2;
+                if (S < 1)
+                    S = 1;
+            }
+            if (S * (side->stage_bytes + 8) > avail)
+                return DRADD_ERR_BAD_CONFIG;
+            side->stages = static_cast<int>(S);
+            const int64_t need = S * (side->stage_bytes + 8);
+            if (need > out->dyn_smem)
+                out->dyn_smem = need;
+        }
+    }
+
     const int64_t need_q = q->active ? (n_q + q->R - 1) / q->R : 0;
     const int64_t need_k = k->active ? (n_k + k->R - 1) / k->R : 0;
     int64_t C = cfg.grid_ctas;
     if (C == 0)
-        C = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * (2048 / B);
+        C = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * (ctas_per_sm > 0 ? ctas_per_sm : 2048 / B);
     if (C < (q->active ? 1 : 0) + (k->active ? 1 : 0))
         return DRADD_ERR_BAD_CONFIG;
     if (need_q + need_k <= C) {
@@ -481,7 +551,7 @@ dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t g
     }
     if (q->ctas + k->ctas > 0x7FFFFFFF)
         return DRADD_ERR_BAD_CONFIG;
-    *threads = static_cast<int>(B);
+    out->threads = static_cast<int>(B);
     return DRADD_OK;
 }
 
@@ -491,16 +561,16 @@ dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dra
                     int64_t hq, int64_t n_k, int64_t hk, int64_t group_size, cudaStream_t stream,
                     const dradd_launch_cfg* cfg)
 {
-    QkSide sq, sk;
-    int threads = 0;
-    bool serialize = false;
-    // shapes first, with the default SM count; the plan is redone below
-    dradd_status st = qk_plan(n_q, hq, n_k, hk, group_size, 152, cfg, &sq, &sk, &threads, &serialize);
-    if (st != DRADD_OK || threads == 0)
-        return st;
     const bool quant = group_size != 0;
     const bool add = q_residual != nullptr;
-    if (sq.active) {
+    DeviceLimits defaults;
+    QkLaunch plan;
+    // shapes and configuration first, with GB300's limits; redone below
+    dradd_status st = qk_plan(n_q, hq, n_k, hk, group_size, add, defaults.sm_count, 0,
+                              defaults.smem_per_block_optin, cfg, &plan);
+    if (st != DRADD_OK || plan.threads == 0)
+        return st;
+    if (plan.q.active) {
         if (!q_out || !q || !q_weight || (quant && !q_scale) || (add && !q_residual_out))
             return DRADD_ERR_NULL_PTR;
         if (!aligned(q_out, 16) || !aligned(q, 16) || !aligned(q_weight, 16) || (quant && !aligned(q_scale, 4)) ||
@@ -509,7 +579,7 @@ dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dra
         if (!std::isfinite(q_eps) || q_eps < 0.0f)
             return DRADD_ERR_BAD_EPS;
     }
-    if (sk.active) {
+    if (plan.k.active) {
         if (!k_out || !k || !k_weight)
             return DRADD_ERR_NULL_PTR;
         if (!aligned(k_out, 16) || !aligned(k, 16) || !aligned(k_weight, 16))
@@ -520,16 +590,15 @@ dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dra
     // Overlaps: outputs never overlap one another; an output may coincide
     // exactly with the input it replaces (q_out with q when bf16,
     // q_residual_out with q_residual, k_out with k) and overlap nothing else.
-    const int64_t eq = sq.active ? n_q * hq : 0, ek = sk.active ? n_k * hk : 0;
-    const Range in[5] = {sq.active ? range_of(q, eq * 2) : Range{},
-                         sq.active ? range_of(q_weight, hq * 2) : Range{},
-                         sq.active && add ? range_of(q_residual, eq * 2) : Range{},
-                         sk.active ? range_of(k, ek * 2) : Range{},
-                         sk.active ? range_of(k_weight, hk * 2) : Range{}};
-    const Range out[4] = {sq.active ? range_of(q_out, quant ? eq : eq * 2) : Range{},
-                          sq.active && quant ? range_of(q_scale, n_q * (hq / group_size) * 4) : Range{},
-                          sq.active && add ? range_of(q_residual_out, eq * 2) : Range{},
-                          sk.active ? range_of(k_out, ek * 2) : Range{}};
+    const bool qa = plan.q.active, ka = plan.k.active;
+    const int64_t eq = qa ? n_q * hq : 0, ek = ka ? n_k * hk : 0;
+    const Range in[5] = {qa ? range_of(q, eq * 2) : Range{}, qa ? range_of(q_weight, hq * 2) : Range{},
+                         qa && add ? range_of(q_residual, eq * 2) : Range{}, ka ? range_of(k, ek * 2) : Range{},
+                         ka ? range_of(k_weight, hk * 2) : Range{}};
+    const Range out[4] = {qa ? range_of(q_out, quant ? eq : eq * 2) : Range{},
+                          qa && quant ? range_of(q_scale, n_q * (hq / group_size) * 4) : Range{},
+                          qa && add ? range_of(q_residual_out, eq * 2) : Range{},
+                          ka ? range_of(k_out, ek * 2) : Range{}};
     const int may_equal[4] = {quant ? -1 : 0, -1, 2, 3};  // input index each output may equal
     for (int a = 0; a < 4; ++a) {
         for (int b = a + 1; b < 4; ++b)
@@ -543,43 +612,62 @@ dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dra
     st = query_limits(&L);
     if (st != DRADD_OK)
         return st;
-    st = qk_plan(n_q, hq, n_k, hk, group_size, L.sm_count, cfg, &sq, &sk, &threads, &serialize);
+    st = qk_plan(n_q, hq, n_k, hk, group_size, add, L.sm_count, 0, L.smem_per_block_optin, cfg, &plan);
     if (st != DRADD_OK)
         return st;
+    const int kq = qa ? plan.q.K : 1, kk = ka ? plan.k.K : 1;
+    if (plan.staged && (!cfg || cfg->grid_ctas == 0)) {
+        // persistent grid: as many CTAs as fit on the device at once
+        int per_sm = 0;
+        if (dradd::qk_occupancy(kq, kk, quant, add, true, plan.threads, static_cast<size_t>(plan.dyn_smem),
+                                &per_sm) != cudaSuccess)
+            return DRADD_ERR_CUDA;
+        st = qk_plan(n_q, hq, n_k, hk, group_size, add, L.sm_count, per_sm > 0 ? per_sm : 1,
+                     L.smem_per_block_optin, cfg, &plan);
+        if (st != DRADD_OK)
+            return st;
+    }
 
     unsigned* status = nullptr;
     if (dradd::device_status_ptr(&status) != cudaSuccess)
         return DRADD_ERR_CUDA;
-    auto params = [&](const QkSide& s, const dradd_bf16* x, const dradd_bf16* res, const dradd_bf16* w,
+    const uint64_t wait_ns = cfg && cfg->wait_limit_us > 0 ? static_cast<uint64_t>(cfg->wait_limit_us) * 1000ull
+                                                          : kDefaultWaitLimitNs;
+    auto params = [&](const QkSide& side, const dradd_bf16* x, const dradd_bf16* res, const dradd_bf16* w,
                       float eps) {
         Params p = {};
         p.x = x;
         p.residual = res;
         p.weight = w;
         p.eps = eps;
-        p.hidden = static_cast<int>(s.hidden);
-        p.inv_hidden = is_pow2(s.hidden) ? 1.0f / static_cast<float>(s.hidden) : 0.0f;
-        p.n_rows = s.n_rows;
-        p.threads_per_row = s.T;
-        p.rows_per_cta = s.R;
-        p.wait_limit_ns = kDefaultWaitLimitNs;
+        p.hidden = static_cast<int>(side.hidden);
+        p.inv_hidden = is_pow2(side.hidden) ? 1.0f / static_cast<float>(side.hidden) : 0.0f;
+        p.n_rows = side.n_rows;
+        p.threads_per_row = side.T;
+        p.rows_per_cta = side.R;
+        p.stages = side.stages;
+        p.fault_inject = cfg ? cfg->fault_inject : 0;
+        p.wait_limit_ns = wait_ns;
         p.status = status;
         return p;
     };
-    Params pq = params(sq, q, q_residual, q_weight, q_eps);
+    Params pq = params(plan.q, q, q_residual, q_weight, q_eps);
     if (quant) {
         pq.out_q = static_cast<int8_t*>(q_out);
         pq.scale = q_scale;
         pq.group_blocks = static_cast<int>(group_size / 8);
+        while ((1 << pq.group_shift) < pq.group_blocks)
+            ++pq.group_shift;
     } else {
         pq.out = static_cast<uint16_t*>(q_out);
     }
     pq.residual_out = q_residual_out;
-    Params pk = params(sk, k, nullptr, k_weight, k_eps);
+    Params pk = params(plan.k, k, nullptr, k_weight, k_eps);
     pk.out = k_out;
-    const cudaError_t e = dradd::launch_qk(pq, pk, sq.active ? sq.K : 1, sk.active ? sk.K : 1, quant, add,
-                                           static_cast<int>(sq.ctas), static_cast<int>(sk.ctas), threads,
-                                           serialize, stream);
+    const cudaError_t e =
+        dradd::launch_qk(pq, pk, kq, kk, quant, add, plan.staged, static_cast<int>(plan.q.ctas),
+                         static_cast<int>(plan.k.ctas), plan.threads, static_cast<size_t>(plan.dyn_smem),
+                         plan.serialize, stream);
     return e == cudaSuccess ? DRADD_OK : DRADD_ERR_CUDA;
 }
 
@@ -814,7 +902,7 @@ dradd_status fused_qk_rmsnorm_group_quant_fwd_with_config(
 }
 
 dradd_status dradd_qk_resolve_config(int64_t n_q_rows, int64_t q_hidden, int64_t n_k_rows, int64_t k_hidden,
-                                     int64_t group_size, int sm_count, const dradd_launch_cfg* cfg,
+                                     int64_t group_size, int q_residual, int sm_count, const dradd_launch_cfg* cfg,
                                      dradd_qk_plan* plan)
 {
     if (!plan)
@@ -827,20 +915,22 @@ dradd_status dradd_qk_resolve_config(int64_t n_q_rows, int64_t q_hidden, int64_t
         if (st != DRADD_OK)
             return st;
     }
-    QkSide sq, sk;
-    int threads = 0;
-    bool serialize = false;
-    const dradd_status st =
-        qk_plan(n_q_rows, q_hidden, n_k_rows, k_hidden, group_size, L.sm_count, cfg, &sq, &sk, &threads, &serialize);
+    QkLaunch r;
+    const dradd_status st = qk_plan(n_q_rows, q_hidden, n_k_rows, k_hidden, group_size, q_residual != 0,
+                                    L.sm_count, 0, L.smem_per_block_optin, cfg, &r);
     if (st != DRADD_OK)
         return st;
-    plan->threads_per_cta = threads;
-    plan->q_threads_per_row = sq.T;
-    plan->q_rows_per_cta = sq.R;
-    plan->q_ctas = static_cast<int>(sq.ctas);
-    plan->k_threads_per_row = sk.T;
-    plan->k_rows_per_cta = sk.R;
-    plan->k_ctas = static_cast<int>(sk.ctas);
+    plan->variant = r.threads == 0 ? 0 : (r.staged ? DRADD_VARIANT_STAGED : DRADD_VARIANT_ROWS);
+    plan->threads_per_cta = r.threads;
+    plan->dyn_smem_bytes = static_cast<int>(r.dyn_smem);
+    plan->q_threads_per_row = r.q.T;
+    plan->q_rows_per_cta = r.q.R;
+    plan->q_stages = r.q.stages;
+    plan->q_ctas = static_cast<int>(r.q.ctas);
+    plan->k_threads_per_row = r.k.T;
+    plan->k_rows_per_cta = r.k.R;
+    plan->k_stages = r.k.stages;
+    plan->k_ctas = static_cast<int>(r.k.ctas);
     return DRADD_OK;
 }
 

@@ -251,9 +251,39 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
     return d;
 }
 
-// Per-row fp8 / fp4 scale (scale = RN(amax / 448) or RN(amax / 6)) and the
-// two multipliers that bracket 1 / scale, c_lo = RN(RN(1/scale) * (1 - 2^-20))
-// and c_hi likewise with 1 + 2^-20.
+// RN(m / 448) for an amax m >= 0, by division with one correction step
+// (Markstein): q0 = RN(m * RN(1/448)); the remainder m - q0 * 448 is exact
+// in one fused multiply-add; q = RN(q0 + remainder * RN(1/448)).  Every
+// operation scales exactly with m by powers of two while q0 and the
+// remainder stay normal, so checking every significand in a few binades
+// proves the identity for all m in [2^-100, 2^128): the test suite does
+// that against the correctly rounded quotient.  Anything else (0,
+// subnormal or tiny m, Inf, NaN) takes the IEEE division.
+__device__ __forceinline__ float div448_rn(float m)
+{
+    constexpr float kInv448 = 0x1.24924ap-9f;  // RN(1 / 448)
+    if (!(m >= 0x1p-100f && m <= 3.40282347e38f))
+        return __fdiv_rn(m, 448.0f);
+    const float q0 = __fmul_rn(m, kInv448);
+    const float r = __fmaf_rn(-q0, 448.0f, m);
+    return __fmaf_rn(r, kInv448, q0);
+}
+
+// An approximation of 1 / x with relative error below 2^-22 for normal x
+// whose reciprocal is normal: the hardware reciprocal, documented to be
+// within 1 ulp.
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// Per-row (or per-group) fp8 / fp4 scale (scale = RN(amax / 448) or
+// RN(amax / 6)) and two multipliers that bracket 1 / scale:
+// c_lo = RN(c * (1 - 2^-20)) and c_hi = RN(c * (1 + 2^-20)), where c is
+// 1 / scale to within a relative 2^-22.  fast: scale is a normal number
+// below 2^120 (so 1 / scale is normal too); else quantisation divides.
 struct E4m3Scale {
     float scale;
     float c_lo, c_hi;
@@ -264,17 +294,18 @@ __device__ __forceinline__ E4m3Scale make_e4m3_scale(float scale)
 {
     E4m3Scale s;
     s.scale = scale;
-    s.fast = scale >= 0x1p-126f && scale <= 3.40282347e38f;
-    const float c = s.fast ? __frcp_rn(scale) : 0.0f;
+    s.fast = scale >= 0x1p-126f && scale < 0x1p120f;
+    const float c = s.fast ? rcp_approx(scale) : 0.0f;
     s.c_lo = __fmul_rn(c, 1.0f - 0x1p-20f);
     s.c_hi = __fmul_rn(c, 1.0f + 0x1p-20f);
     return s;
 }
 
 // Eight e4m3 codes for eight consecutive y values: e4m3(RN(y / scale)).
-// Fast path: with every rounding relative and at most 2^-24, for y >= 0
-// RN(y * c_lo) <= y/scale * (1 - 2^-20 + 3 * 2^-24) < y/scale * (1 - 2^-24)
-// <= RN(y / scale), and likewise RN(y / scale) <= RN(y * c_hi) (mirrored for
+// Fast path: c is within a relative 2^-22 of 1 / scale and every rounding
+// is relative and at most 2^-24, so for y >= 0 RN(y * c_lo) <=
+// y/scale * (1 - 2^-20 + 2^-22 + 3 * 2^-24) < y/scale * (1 - 2^-24) <=
+// RN(y / scale), and likewise RN(y / scale) <= RN(y * c_hi) (mirrored for
 // y < 0; values too small for a relative bound are below half the smallest
 // e4m3 step and give code 0 at both ends).  Rounding to e4m3 is monotone, so when
 // both ends give the same code, RN(y / scale) gives it too.  A block where

@@ -26,7 +26,8 @@ struct Params {
     int fault_inject;         // staged kernel only
     uint64_t wait_limit_ns;   // staged kernel only
     unsigned* status;         // device status word (set on an expired wait)
-    int group_blocks;         // per-group e4m3 out: 8-element blocks per group
+    int group_blocks;         // per-group e4m3 out: 8-element blocks per group (a power of two)
+    int group_shift;          // log2(group_blocks)
 };
 
 constexpr unsigned kDeviceStatusTimeout = 1u;
@@ -77,13 +78,20 @@ KernelFn staged_fn_norm_bf16(int T, int K);
 KernelFn staged_fn_norm_int8(int T, int K);
 KernelFn staged_fn_norm_e4m3(int T, int K);
 KernelFn staged_fn_norm_e2m1(int T, int K);
-// Fused q/k RMSNorm (register kernel): CTAs [0, q_ctas) take the q rows,
-// the next k_ctas the k rows; kq / kk blocks of 8 per thread on each side.
-// quant: per-group e4m3 q out (else bf16); add: q has a residual.
-cudaError_t launch_qk(const Params& pq, const Params& pk, int kq, int kk, bool quant, bool add, int q_ctas,
-                      int k_ctas, int threads, bool serialize, cudaStream_t stream);
-QkKernelFn qk_fn_bf16(int kq, int kk, bool add);
-QkKernelFn qk_fn_e4m3(int kq, int kk, bool add);
+// Fused q/k RMSNorm: CTAs [0, q_ctas) take the q rows, the next k_ctas the
+// k rows; kq / kk blocks of 8 per thread on each side.  quant: per-group
+// e4m3 q out (else bf16); add: q has a residual; staged: rows staged
+// through dyn_smem bytes of shared memory (else loaded into registers).
+cudaError_t launch_qk(const Params& pq, const Params& pk, int kq, int kk, bool quant, bool add, bool staged,
+                      int q_ctas, int k_ctas, int threads, size_t dyn_smem, bool serialize, cudaStream_t stream);
+cudaError_t qk_occupancy(int kq, int kk, bool quant, bool add, bool staged, int threads, size_t dyn_smem,
+                         int* blocks_per_sm);
+QkKernelFn qk_fn_bf16_rows(int kq, int kk, bool add);
+QkKernelFn qk_fn_bf16_staged(int kq, int kk, bool add);
+QkKernelFn qk_fn_e4m3_rows(int kq, int kk, bool add);
+QkKernelFn qk_fn_e4m3_staged(int kq, int kk, bool add);
+// Static shared memory of a qk kernel whose sides have kq / kk blocks per thread.
+size_t qk_static_smem(int kq, int kk);
 cudaError_t launch_residual_add(uint16_t* residual_out, const uint16_t* x, const uint16_t* residual,
                                 int64_t n_vec, int sm_count, bool serialize, cudaStream_t stream);
 cudaError_t launch_convert(uint16_t* out, uint64_t first, int64_t count, int method, cudaStream_t stream);

@@ -3,7 +3,7 @@
 // staged kernels are instantiated in dradd_staged_<mode>_<out>.cu (one
 // translation unit per mode and output kind, compiled in parallel) and
 // reached through staged_fn_<mode>_<out>; the fused q/k kernels likewise in
-// dradd_qk_<out>.cu through qk_fn_<out>.
+// dradd_qk_<out>_<variant>.cu through qk_fn_<out>_<variant>.
 #include <atomic>
 
 #include "dradd_kernels.cuh"
@@ -243,13 +243,78 @@ size_t staged_static_smem(int K)
     return sizeof(float) * (2 * 32 * static_cast<size_t>(K) + 2 * 32);
 }
 
-cudaError_t launch_qk(const Params& pq, const Params& pk, int kq, int kk, bool quant, bool add, int q_ctas,
-                      int k_ctas, int threads, bool serialize, cudaStream_t stream)
+namespace {
+
+QkKernelFn qk_fn(int kq, int kk, bool quant, bool add, bool staged)
 {
-    QkKernelFn fn = quant ? qk_fn_e4m3(kq, kk, add) : qk_fn_bf16(kq, kk, add);
+    if (quant)
+        return staged ? qk_fn_e4m3_staged(kq, kk, add) : qk_fn_e4m3_rows(kq, kk, add);
+    return staged ? qk_fn_bf16_staged(kq, kk, add) : qk_fn_bf16_rows(kq, kk, add);
+}
+
+// One bit per staged qk kernel (kq, kk, quant, add): its dynamic shared
+// memory limit has been raised to the device's opt-in maximum.
+std::atomic<uint64_t> g_qk_smem_done[kMaxDevices];
+
+cudaError_t qk_prepare(QkKernelFn fn, int kq, int kk, bool quant, bool add, bool staged)
+{
+    if (!staged)
+        return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const uint64_t bit = 1ull << (((log2i(kq) * 4 + log2i(kk)) * 2 + (quant ? 1 : 0)) * 2 + (add ? 1 : 0));
+    std::atomic<uint64_t>* word = dev >= 0 && dev < kMaxDevices ? &g_qk_smem_done[dev] : nullptr;
+    if (word && (word->load(std::memory_order_acquire) & bit))
+        return cudaSuccess;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess)
+        return e;
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, fn);
+    if (e != cudaSuccess)
+        return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - static_cast<int>(attr.sharedSizeBytes));
+    if (e != cudaSuccess)
+        return e;
+    if (word)
+        word->fetch_or(bit, std::memory_order_acq_rel);
+    return cudaSuccess;
+}
+
+}  // namespace
+
+size_t qk_static_smem(int kq, int kk)
+{
+    // s_sum[2][32 * K] + s_max[2][32] of each side's body, as declared
+    return sizeof(float) * (2 * 32 * static_cast<size_t>(kq + kk) + 4 * 32);
+}
+
+cudaError_t launch_qk(const Params& pq, const Params& pk, int kq, int kk, bool quant, bool add, bool staged,
+                      int q_ctas, int k_ctas, int threads, size_t dyn_smem, bool serialize, cudaStream_t stream)
+{
+    QkKernelFn fn = qk_fn(kq, kk, quant, add, staged);
     if (!fn)
         return cudaErrorInvalidValue;
-    return launch(fn, q_ctas + k_ctas, threads, 0, serialize, stream, pq, pk, q_ctas);
+    cudaError_t e = qk_prepare(fn, kq, kk, quant, add, staged);
+    if (e != cudaSuccess)
+        return e;
+    return launch(fn, q_ctas + k_ctas, threads, dyn_smem, serialize, stream, pq, pk, q_ctas);
+}
+
+cudaError_t qk_occupancy(int kq, int kk, bool quant, bool add, bool staged, int threads, size_t dyn_smem,
+                         int* blocks_per_sm)
+{
+    QkKernelFn fn = qk_fn(kq, kk, quant, add, staged);
+    if (!fn)
+        return cudaErrorInvalidValue;
+    cudaError_t e = qk_prepare(fn, kq, kk, quant, add, staged);
+    if (e != cudaSuccess)
+        return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, threads, dyn_smem);
 }
 
 cudaError_t launch_residual_add(uint16_t* residual_out, const uint16_t* x, const uint16_t* residual,

@@ -27,8 +27,11 @@
 //   rows_kernel    rows are loaded straight into registers with streaming
 //                  16-byte loads; a CTA handles rows_per_cta rows side by side
 //                  and loops over the rows with a grid stride.
-//   qk_kernel      two rows_kernel bodies in one launch (fused q/k RMSNorm),
-//                  the q side optionally with per-group e4m3 out.
+//   qk_kernel      fused q/k RMSNorm: two row sets in one launch, the q side
+//                  optionally with per-group e4m3 out; each side runs either
+//                  the rows_kernel body or tile_body, which stages groups of
+//                  rows_per_cta adjacent rows into shared memory with one
+//                  bulk copy per tensor.
 //   staged_kernel  persistent CTAs stage whole rows of x (and residual) into
 //                  shared memory with 1-D bulk asynchronous copies (TMA
 //                  engine), `stages` rows ahead of the compute; the copy for
@@ -84,8 +87,12 @@ __device__ __forceinline__ void finish_row(const Params& p, float (&acc)[K][8], 
                                            float inv, int64_t row, bool active, int t, int T, int lane,
                                            int warp_in_row, int nblocks, float* red_max)
 {
+    // Padding blocks (t + jT >= nblocks) keep acc = 0 and are never stored;
+    // a warp whose blocks for some j are all padding skips that j.
 #pragma unroll
     for (int j = 0; j < K; ++j) {
+        if (t + j * T >= nblocks)
+            continue;
         float wf[8];
         unpack8(w[j], wf);
 #pragma unroll
@@ -110,20 +117,24 @@ __device__ __forceinline__ void finish_row(const Params& p, float (&acc)[K][8], 
         // so independent of the order).  Padding blocks form whole groups
         // of their own and are never stored.
         const int gb = p.group_blocks;
-        const int64_t groups = nblocks / gb;
+        const int gshift = p.group_shift;
+        const int64_t groups = nblocks >> gshift;
         uint2* qrow = reinterpret_cast<uint2*>(p.out_q + row * p.hidden);
 #pragma unroll
         for (int j = 0; j < K; ++j) {
+            // with T >= 32 a warp lies inside one row: warp-uniform skip
+            if (T >= 32 && (t & ~31) + j * T >= nblocks)
+                continue;
             float m = 0.0f;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 m = fmaxf(m, fabsf(acc[j][e]));
             m = butterfly_max(m, gb);
-            const float scale = __fdiv_rn(m, 448.0f);
+            const float scale = div448_rn(m);
             const int b = t + j * T;
             if (active && b < nblocks) {
                 if ((b & (gb - 1)) == 0)
-                    p.scale[row * groups + b / gb] = scale;
+                    p.scale[row * groups + (b >> gshift)] = scale;
                 st_stream(qrow + b, quantize8_e4m3(acc[j], make_e4m3_scale(scale)));
             }
         }
@@ -287,45 +298,6 @@ __global__ void __launch_bounds__(max_threads_for(K)) rows_kernel(const Params p
     rows_body<K, OUT, ADD>(p, blockIdx.x, gridDim.x);
 }
 
-// ------------------------------------------------------------------ qk_kernel
-// Fused q/k RMSNorm in one launch: CTAs [0, q_ctas) run the q rows (residual
-// add with QADD; per-group e4m3 out with QQUANT, else bf16), the rest the k
-// rows (plain, bf16).  Both sides use the CTA's threads, each with its own
-// split into threads per row, rows per CTA and blocks per thread.
-template <int KQ, int KK, bool QQUANT, bool QADD>
-__global__ void __launch_bounds__(qk_max_threads(KQ > KK ? KQ : KK)) qk_kernel(const Params pq, const Params pk, int q_ctas)
-{
-    const int cta = static_cast<int>(blockIdx.x);
-    if (cta < q_ctas)
-        rows_body<KQ, QQUANT ? kOutE4m3Group : kOutBf16, QADD>(pq, cta, q_ctas);
-    else
-        rows_body<KK, kOutBf16, false>(pk, cta - q_ctas, static_cast<int>(gridDim.x) - q_ctas);
-}
-
-template <int KQ, bool QQUANT, bool QADD>
-QkKernelFn qk_by_kk(int kk)
-{
-    switch (kk) {
-    case 1: return qk_kernel<KQ, 1, QQUANT, QADD>;
-    case 2: return qk_kernel<KQ, 2, QQUANT, QADD>;
-    case 4: return qk_kernel<KQ, 4, QQUANT, QADD>;
-    case 8: return qk_kernel<KQ, 8, QQUANT, QADD>;
-    default: return nullptr;
-    }
-}
-
-template <bool QQUANT, bool QADD>
-QkKernelFn qk_table(int kq, int kk)
-{
-    switch (kq) {
-    case 1: return qk_by_kk<1, QQUANT, QADD>(kk);
-    case 2: return qk_by_kk<2, QQUANT, QADD>(kk);
-    case 4: return qk_by_kk<4, QQUANT, QADD>(kk);
-    case 8: return qk_by_kk<8, QQUANT, QADD>(kk);
-    default: return nullptr;
-    }
-}
-
 // -------------------------------------------------------------- staged_kernel
 // T (threads per row = threads per CTA) is a compile-time constant so that
 // every (T, K) pair gets its own register budget (staged_min_blocks) and the
@@ -482,6 +454,193 @@ KernelFn staged_table(int T, int K)
     case 256: return staged_by_k<256, OUT, ADD>(K);
     case 512: return staged_by_k<512, OUT, ADD>(K);
     case 1024: return staged_by_k<1024, OUT, ADD>(K);
+    default: return nullptr;
+    }
+}
+
+// ----------------------------------------------------------------- tile_body
+// Staged body for rows of any width: R = rows_per_cta consecutive rows form
+// a group, T = threads_per_row threads per row (T x R = the CTA), K blocks
+// of 8 per thread.  A stage holds one group: its R rows of x (and then its
+// R rows of residual) arrive by one 1-D bulk copy each, since the rows of
+// a group are adjacent in memory; the last group of the tensor may be
+// short, and its copies carry only the rows that exist.  Groups cta,
+// cta + n_ctas, ... are this CTA's; the copy for the group `stages` ahead
+// is issued as soon as every thread has read the current stage.  Waits are
+// bounded as in staged_kernel.
+template <int K, int OUT, bool ADD>
+__device__ __forceinline__ void tile_body(const Params& p, int64_t cta, int64_t n_ctas,
+                                          unsigned char* stage_mem)
+{
+    __shared__ float s_sum[2][32 * K];
+    __shared__ float s_max[2][32];
+    const int T = p.threads_per_row;
+    const int R = p.rows_per_cta;
+    const int tid = threadIdx.x;
+    const int r_local = tid / T;
+    const int t = tid - r_local * T;
+    const int lane = tid & 31;
+    const int warp_in_row = t >> 5;
+    const int warps_per_row = T > 32 ? T >> 5 : 1;
+    const int nblocks = p.hidden >> 3;
+    const int stages = p.stages;
+    const uint32_t row_bytes = static_cast<uint32_t>(p.hidden) * 2u;
+    const uint32_t tile_bytes = row_bytes * static_cast<uint32_t>(R);
+    const uint32_t stage_bytes = (ADD ? 2u : 1u) * tile_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stage_mem + static_cast<size_t>(stages) * stage_bytes);
+    const int64_t n_groups = (p.n_rows + R - 1) / R;
+
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s)
+            mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    wait_prior_grids();
+    allow_next_grid();
+
+    const uint64_t policy = l2_policy_evict_first();
+    auto issue = [&](int s, int64_t g) {
+        const int64_t row0 = g * R;
+        const int64_t left = p.n_rows - row0;
+        const uint32_t bytes = row_bytes * static_cast<uint32_t>(left < R ? left : R);
+        unsigned char* dst = stage_mem + static_cast<size_t>(s) * stage_bytes;
+        mbar_arrive_expect_tx(&bars[s], (ADD ? 2u : 1u) * bytes);
+        bulk_copy_g2s(dst, p.x + row0 * p.hidden, bytes, &bars[s], policy);
+        if constexpr (ADD)
+            bulk_copy_g2s(dst + tile_bytes, p.residual + row0 * p.hidden, bytes, &bars[s], policy);
+    };
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) {
+            const int64_t g = cta + s * n_ctas;
+            if (g >= n_groups)
+                break;
+            if (p.fault_inject && s == 0)
+                continue;  // test hook: this copy never comes, so its wait expires
+            issue(s, g);
+        }
+    }
+
+    uint4 w[K];
+    load_weights<K>(p, w, t, T, nblocks);
+
+    int buf = 0;
+    int64_t i = 0;
+    int s = 0;
+    uint32_t parity = 0;
+    for (int64_t g = cta; g < n_groups; g += n_ctas, ++i) {
+        const bool ok = mbar_wait_bounded(&bars[s], parity, p.wait_limit_ns);
+        const int64_t row = g * R + r_local;
+        const bool active = row < p.n_rows;
+        const unsigned char* sbase =
+            stage_mem + static_cast<size_t>(s) * stage_bytes + static_cast<size_t>(r_local) * row_bytes;
+        const uint4* xs = reinterpret_cast<const uint4*>(sbase);
+        const uint4* rs = reinterpret_cast<const uint4*>(sbase + tile_bytes);
+        uint4 xv[K], rv[K];
+        if (active) {
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const int b = t + j * T;
+                if (b < nblocks) {
+                    xv[j] = xs[b];
+                    if constexpr (ADD)
+                        rv[j] = rs[b];
+                }
+            }
+        }
+        float acc[K][8], part[K];
+        row_accumulate<K, ADD>(p, xv, rv, acc, part, row, active, t, T, nblocks);
+
+        float* red = &s_sum[buf][r_local * warps_per_row * K];
+        lanes_then_publish<K>(part, T, lane, warp_in_row, red);
+        // Every thread has read stage s and published its warp's partial
+        // sums; any expired wait ends the CTA here.
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                record_timeout(p);
+                // Copies already issued must land before shared memory is released.
+                int s2 = s;
+                uint32_t parity2 = parity;
+                for (int64_t i2 = i; i2 < i + stages; ++i2) {
+                    if (cta + i2 * n_ctas >= n_groups)
+                        break;
+                    if (!(p.fault_inject && i2 == 0))
+                        mbar_wait_bounded(&bars[s2], parity2, p.wait_limit_ns);
+                    if (++s2 == stages) {
+                        s2 = 0;
+                        parity2 ^= 1u;
+                    }
+                }
+            }
+            return;
+        }
+        if (tid == 0) {
+            const int64_t next = g + static_cast<int64_t>(stages) * n_ctas;
+            if (next < n_groups) {
+                fence_proxy_async_smem();
+                issue(s, next);
+            }
+        }
+        gather_warps<K>(part, T, lane, red);
+        const float inv = inv_rms(fold_k<K>(part), p.hidden, p.inv_hidden, p.eps);
+        finish_row<K, OUT>(p, acc, w, inv, row, active, t, T, lane, warp_in_row, nblocks,
+                             &s_max[buf][r_local * warps_per_row]);
+        buf ^= 1;
+        if (++s == stages) {
+            s = 0;
+            parity ^= 1u;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ qk_kernel
+// Fused q/k RMSNorm in one launch: CTAs [0, q_ctas) run the q rows (residual
+// add with QADD; per-group e4m3 out with QQUANT, else bf16), the rest the k
+// rows (plain, bf16).  Both sides use the CTA's threads, each with its own
+// threads per row, rows per CTA and blocks per thread; STAGED selects
+// tile_body (bulk copies into shared memory, `stages` groups ahead) over
+// rows_body (loads straight into registers).
+template <int KQ, int KK, bool QQUANT, bool QADD, bool STAGED>
+__global__ void __launch_bounds__(qk_max_threads(KQ > KK ? KQ : KK))
+    qk_kernel(const Params pq, const Params pk, int q_ctas)
+{
+    extern __shared__ __align__(128) unsigned char stage_mem[];
+    constexpr int QOUT = QQUANT ? kOutE4m3Group : kOutBf16;
+    const int cta = static_cast<int>(blockIdx.x);
+    const int k_ctas = static_cast<int>(gridDim.x) - q_ctas;
+    if constexpr (STAGED) {
+        if (cta < q_ctas)
+            tile_body<KQ, QOUT, QADD>(pq, cta, q_ctas, stage_mem);
+        else
+            tile_body<KK, kOutBf16, false>(pk, cta - q_ctas, k_ctas, stage_mem);
+    } else {
+        if (cta < q_ctas)
+            rows_body<KQ, QOUT, QADD>(pq, cta, q_ctas);
+        else
+            rows_body<KK, kOutBf16, false>(pk, cta - q_ctas, k_ctas);
+    }
+}
+
+template <int KQ, bool QQUANT, bool QADD, bool STAGED>
+QkKernelFn qk_by_kk(int kk)
+{
+    switch (kk) {
+    case 1: return qk_kernel<KQ, 1, QQUANT, QADD, STAGED>;
+    case 2: return qk_kernel<KQ, 2, QQUANT, QADD, STAGED>;
+    case 4: return qk_kernel<KQ, 4, QQUANT, QADD, STAGED>;
+    case 8: return qk_kernel<KQ, 8, QQUANT, QADD, STAGED>;
+    default: return nullptr;
+    }
+}
+
+template <bool QQUANT, bool QADD, bool STAGED>
+QkKernelFn qk_table(int kq, int kk)
+{
+    switch (kq) {
+    case 1: return qk_by_kk<1, QQUANT, QADD, STAGED>(kk);
+    case 2: return qk_by_kk<2, QQUANT, QADD, STAGED>(kk);
+    case 4: return qk_by_kk<4, QQUANT, QADD, STAGED>(kk);
+    case 8: return qk_by_kk<8, QQUANT, QADD, STAGED>(kk);
     default: return nullptr;
     }
 }

@@ -154,6 +154,10 @@ dradd_status add_rmsnorm_quant_fwd(int8_t* out_q, float* scale, dradd_bf16* resi
  *                    in the stream drains; they wait for it to complete (and
  *                    its writes to be visible) before any global memory
  *                    access.  1: plain launch.
+ *   blocks_per_thread K (1, 2, 4 or 8): 8-element blocks per thread.  With
+ *                    threads_per_row given it must agree (K = P / 8 / T);
+ *                    alone it sets T = P / 8 / K (the automatic stage count
+ *                    is then 2).
  */
 enum { DRADD_VARIANT_AUTO = 0, DRADD_VARIANT_ROWS = 1, DRADD_VARIANT_STAGED = 2 };
 
@@ -166,6 +170,7 @@ typedef struct dradd_launch_cfg {
     int fault_inject;
     int wait_limit_us;
     int serialize;
+    int blocks_per_thread;
 } dradd_launch_cfg;
 
 dradd_status add_rmsnorm_fwd_with_config(dradd_bf16* out, dradd_bf16* residual_out,
@@ -370,12 +375,19 @@ dradd_status fused_qk_rmsnorm_group_quant_fwd(void* q_out, float* q_scale, dradd
                                               int64_t k_hidden, int64_t group_size, cudaStream_t stream);
 
 /*
- * Test hook: the fused q/k call with an explicit configuration.  Only
- * variant (AUTO or ROWS), threads_per_row (read here as the threads of a
- * CTA: a power of two 32..512, at most 256 when a side needs 8 blocks of
- * 8 per thread, i.e. when P / 8 > 4 x threads), grid_ctas (total CTAs,
- * shared by the two sides) and serialize are used; rows_per_cta, stages
- * and fault_inject must be 0.  Results never depend on it.
+ * Test hook: the fused q/k call with an explicit configuration.  variant:
+ * STAGED (rows staged through shared memory by bulk copies) or ROWS (rows
+ * loaded straight into registers); AUTO picks by the longer side's padded
+ * width P: staged for P <= 256 and P > 2048, rows in between, and staged
+ * whenever stages or fault_inject is set.
+ * threads_per_row is read here as the threads of a CTA: a power of two
+ * 32..512, at most 256 when a side needs 8 blocks of 8 per thread.
+ * blocks_per_thread: the least K both sides use (each side raises it to
+ * what the CTA size needs; at most P / 8 and 8).  grid_ctas: total CTAs,
+ * shared by the two sides.  stages (staged only): stages per side, 1..8.
+ * fault_inject, wait_limit_us and serialize as for
+ * add_rmsnorm_fwd_with_config (staged only for the first two);
+ * rows_per_cta must be 0.  Results never depend on it.
  */
 dradd_status fused_qk_rmsnorm_group_quant_fwd_with_config(
     void* q_out, float* q_scale, dradd_bf16* q_residual_out, dradd_bf16* k_out, const dradd_bf16* q,
@@ -385,20 +397,25 @@ dradd_status fused_qk_rmsnorm_group_quant_fwd_with_config(
 
 /* The launch plan of a fused q/k call (for tests and reports). */
 typedef struct dradd_qk_plan {
+    int variant;          /* DRADD_VARIANT_ROWS or _STAGED (0 for an empty call) */
     int threads_per_cta;
-    int q_threads_per_row, q_rows_per_cta, q_ctas;  /* 0 when n_q_rows == 0 */
-    int k_threads_per_row, k_rows_per_cta, k_ctas;  /* 0 when n_k_rows == 0 */
+    int dyn_smem_bytes;   /* staged: shared memory for the stages */
+    int q_threads_per_row, q_rows_per_cta, q_stages, q_ctas;  /* 0 when n_q_rows == 0 */
+    int k_threads_per_row, k_rows_per_cta, k_stages, k_ctas;  /* 0 when n_k_rows == 0 */
 } dradd_qk_plan;
 
 /*
  * dradd_qk_resolve_config -- the plan the fused q/k call would use, without
- * launching.  sm_count > 0 stands in for the device's SM count (no GPU
- * needed); sm_count <= 0 asks the current device.  cfg may be NULL
- * (automatic).  Returns the shape and configuration errors of the call.
+ * launching.  q_residual != 0: the call has a q residual (its stages hold
+ * both tensors).  sm_count > 0 stands in for the device's SM count (no GPU
+ * needed; the automatic grid then assumes 2048 / threads CTAs per SM, where
+ * the real call asks the occupancy calculator); sm_count <= 0 asks the
+ * current device.  cfg may be NULL (automatic).  Returns the shape and
+ * configuration errors of the call.
  */
 dradd_status dradd_qk_resolve_config(int64_t n_q_rows, int64_t q_hidden, int64_t n_k_rows, int64_t k_hidden,
-                                     int64_t group_size, int sm_count, const dradd_launch_cfg* cfg,
-                                     dradd_qk_plan* plan);
+                                     int64_t group_size, int q_residual, int sm_count,
+                                     const dradd_launch_cfg* cfg, dradd_qk_plan* plan);
 
 /*
  * dradd_device_status -- synchronise `stream`, then return DRADD_OK or the

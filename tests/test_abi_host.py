@@ -241,3 +241,15 @@ def test_fp4_argument_errors(L):
     assert L.rmsnorm_fp4_fwd_with_config(Q, SC, X, W, 1e-6, 4, 1024, None, None) == 1
     c = dr.resolve_config(2048, 16384, add=True, fp4=True)
     assert c.variant == dr.VARIANT_STAGED and c.threads_per_row == 512
+
+
+def test_blocks_per_thread_sets_or_checks_threads():
+    c = dr.resolve_config(4096, 4096, sm_count=152, config=dr.LaunchConfig(blocks_per_thread=2))
+    assert c.threads_per_row == 256 and c.blocks_per_thread == 2
+    c = dr.resolve_config(4096, 4096, sm_count=152)
+    assert c.threads_per_row * c.blocks_per_thread * 8 == 4096
+    for bad in (dr.LaunchConfig(threads_per_row=128, blocks_per_thread=2), dr.LaunchConfig(blocks_per_thread=3),
+                dr.LaunchConfig(blocks_per_thread=16)):
+        with pytest.raises(dr.DraddError) as e:
+            dr.resolve_config(4096, 4096, sm_count=152, config=bad)
+        assert e.value.status == 9

@@ -79,9 +79,14 @@ def test_parity(orc, case):
     assert dr.device_status() == 0
 
 
-CONFIGS = [None] + [dr.LaunchConfig(threads_per_row=B, grid_ctas=G)
-                    for B in (64, 128, 256, 512) for G in (0, 2, 3, 7, 1000)] + \
-          [dr.LaunchConfig(serialize=1), dr.LaunchConfig(variant=1, threads_per_row=256, grid_ctas=3)]
+CONFIGS = ([None] +
+           [dr.LaunchConfig(variant=1, threads_per_row=B, grid_ctas=G)
+            for B in (64, 128, 256, 512) for G in (0, 2, 7, 1000)] +
+           [dr.LaunchConfig(variant=2, threads_per_row=B, grid_ctas=G, stages=S)
+            for B, G, S in ((64, 0, 1), (128, 2, 2), (256, 7, 3), (512, 0, 4), (128, 1000, 8), (256, 3, 1))] +
+           [dr.LaunchConfig(variant=v, threads_per_row=128, blocks_per_thread=K)
+            for v in (1, 2) for K in (2, 4, 8)] +
+           [dr.LaunchConfig(serialize=1), dr.LaunchConfig(variant=1, serialize=1)])
 
 
 @pytest.mark.parametrize("group,with_res", [(128, True), (0, False), (16, False)])
@@ -152,3 +157,21 @@ def test_zero_groups_and_tiny_scales(orc):
         compare(orc, q, None, qw, k, kw, group, 1e-6, 1e-6, got, what=f"group {group}")
         s = got[1].cpu().numpy()
         assert np.all(s[5] == 0)
+
+
+def test_bounded_wait_expires_and_recovers(orc):
+    """fault_inject withholds each CTA's first staged copy on both sides:
+    every wait runs out after wait_limit_us, the kernel records
+    DRADD_ERR_TIMEOUT, drains its other copies and returns; the context
+    stays usable."""
+    d = dev()
+    assert dr.device_status(clear=True) == 0
+    q, r, qw, k, kw = make(15, 64, 1536, 64, 512, True)
+    qd, rd, qwd, kd, kwd = (t.to(d) for t in (q, r, qw, k, kw))
+    cfg = dr.LaunchConfig(variant=2, stages=3, grid_ctas=8, fault_inject=1, wait_limit_us=20000)
+    dr.fused_qk_rmsnorm_group_quant_fwd(qd, qwd, kd, kwd, 1e-6, 1e-6, group_size=128, q_residual=rd, config=cfg)
+    assert dr.device_status(clear=True) == 8
+    assert dr.device_status(clear=True) == 0
+    got = run_gpu(q, r, qw, k, kw, 128, 1e-6, 1e-6)
+    compare(orc, q, r, qw, k, kw, 128, 1e-6, 1e-6, got, what="after timeout")
+    assert dr.device_status(clear=True) == 0

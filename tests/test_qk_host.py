@@ -82,24 +82,79 @@ def test_with_config_needs_config(L):
 @pytest.mark.parametrize("nq,hq,nk,hk,g", [
     (4096, 1536, 4096, 512, 128), (64 * 32, 128, 64 * 8, 128, 0), (8, 16384, 8, 512, 256),
     (1, 8, 1, 16, 8), (100000, 1536, 0, 512, 64), (0, 1536, 7, 4096, 0), (3, 200, 5, 24, 8),
-    (2048, 8192, 2048, 1024, 32),
+    (2048, 8192, 2048, 1024, 32), (50, 256, 3, 64, 256), (7, 128, 7, 128, 128),
 ])
 def test_plan_rules(nq, hq, nk, hk, g):
-    p = dr.qk_resolve_config(nq, hq, nk, hk, g, sm_count=152)
+    p = dr.qk_resolve_config(nq, hq, nk, hk, g, q_residual=True, sm_count=152)
     B = p.threads_per_cta
-    assert B & (B - 1) == 0 and 128 <= B <= 512
-    for n, h, T, R, C in ((nq, hq, p.q_threads_per_row, p.q_rows_per_cta, p.q_ctas),
-                          (nk, hk, p.k_threads_per_row, p.k_rows_per_cta, p.k_ctas)):
+    max_p = max(1 << (h - 1).bit_length() for n, h in ((nq, hq), (nk, hk)) if n)
+    if max_p <= 256:
+        assert (p.variant, B) == (2, 64)
+    elif max_p <= 2048:
+        assert (p.variant, B) == (1, 128)
+    else:
+        assert p.variant == 2 and B == min(512, max(128, max_p // 8))
+    least_k = 4 if max_p <= 256 else 2 if max_p <= 2048 else 1
+    for side, n, h, T, R, C in (("q", nq, hq, p.q_threads_per_row, p.q_rows_per_cta, p.q_ctas),
+                                ("k", nk, hk, p.k_threads_per_row, p.k_rows_per_cta, p.k_ctas)):
         if n == 0:
             assert (T, R, C) == (0, 0, 0)
             continue
         P = 1 << (h - 1).bit_length()
         K = P // 8 // T
-        assert T * R == B and K * T == P // 8 and K in (1, 2, 4)
+        assert T * R == B and K * T == P // 8 and K in (1, 2, 4, 8)
+        kmin = 1
+        while P // 8 // kmin > B:
+            kmin *= 2
+        pref = min(least_k, P // 8)
+        if side == "q" and g:
+            pref = min(pref, P // 8 // (g // 8))
+        assert K == max(kmin, pref)
         assert 1 <= C <= -(-n // R)
     assert p.q_ctas + p.k_ctas <= 152 * 2048 // B
     if nq and g:
         assert g // 8 <= p.q_threads_per_row
+    # staged: up to 2 stages of R rows per side, within 96 KiB unless one
+    # stage alone is larger
+    for n, h, R, S, res in ((nq, hq, p.q_rows_per_cta, p.q_stages, True),
+                            (nk, hk, p.k_rows_per_cta, p.k_stages, False)):
+        if n == 0 or p.variant == 1:
+            assert S == 0
+            continue
+        stage = (4 if res else 2) * h * R
+        assert 1 <= S <= 2 and (S * stage <= 96 * 1024 or S == 1)
+        assert p.dyn_smem_bytes >= S * (stage + 8)
+
+
+def test_plan_rows_variant_and_stage_limits():
+    p = dr.qk_resolve_config(64, 1536, 64, 512, 128, q_residual=True, config=dr.LaunchConfig(variant=1))
+    assert p.variant == 1 and p.q_stages == 0 and p.k_stages == 0 and p.dyn_smem_bytes == 0
+    p = dr.qk_resolve_config(64, 1536, 64, 512, 128, q_residual=True, config=dr.LaunchConfig(stages=8))
+    assert p.q_stages == 8 and p.k_stages == 8 and p.dyn_smem_bytes == 8 * (4 * 1536 + 8)
+    # 16384-element q rows with a residual: 64 KiB a stage; 3 stages fit in
+    # 227 KiB, 4 do not
+    p = dr.qk_resolve_config(8, 16384, 0, 0, 0, q_residual=True, config=dr.LaunchConfig(stages=3))
+    assert p.q_stages == 3
+    with pytest.raises(dr.DraddError) as e:
+        dr.qk_resolve_config(8, 16384, 0, 0, 0, q_residual=True, config=dr.LaunchConfig(stages=4))
+    assert e.value.status == 9
+    assert dr.qk_resolve_config(8, 16384, 0, 0, 0, q_residual=True).q_stages == 1
+    assert dr.qk_resolve_config(0, 16384, 0, 0, 0).variant == 0
+    p = dr.qk_resolve_config(64, 1536, 64, 512, 128, q_residual=True, config=dr.LaunchConfig(variant=2))
+    assert p.variant == 2 and p.q_stages == 2
+
+
+def test_plan_blocks_per_thread():
+    # a preferred K is raised where the CTA size needs more, capped at P / 8
+    for K in (1, 2, 4, 8):
+        p = dr.qk_resolve_config(64, 1536, 64, 512, 128, config=dr.LaunchConfig(threads_per_row=128,
+                                                                               blocks_per_thread=K))
+        kq = 256 // p.q_threads_per_row
+        kk = 64 // p.k_threads_per_row
+        assert kq == max(K, 2) and kk == K
+        assert p.q_threads_per_row * p.q_rows_per_cta == 128 == p.k_threads_per_row * p.k_rows_per_cta
+    p = dr.qk_resolve_config(64, 16, 0, 0, 0, config=dr.LaunchConfig(blocks_per_thread=8))
+    assert p.q_threads_per_row == 1
 
 
 def test_plan_explicit_threads_and_grid():
@@ -115,9 +170,11 @@ def test_plan_explicit_threads_and_grid():
     p = dr.qk_resolve_config(64, 8192, 0, 0, 0, config=dr.LaunchConfig(threads_per_row=128))
     assert p.q_threads_per_row == 128
     for cfg in (dr.LaunchConfig(threads_per_row=1024), dr.LaunchConfig(threads_per_row=32),
-                dr.LaunchConfig(threads_per_row=96), dr.LaunchConfig(variant=2),
-                dr.LaunchConfig(rows_per_cta=2), dr.LaunchConfig(stages=1), dr.LaunchConfig(fault_inject=1),
-                dr.LaunchConfig(grid_ctas=1), dr.LaunchConfig(serialize=2)):
+                dr.LaunchConfig(threads_per_row=96), dr.LaunchConfig(variant=3),
+                dr.LaunchConfig(rows_per_cta=2), dr.LaunchConfig(stages=9), dr.LaunchConfig(stages=-1),
+                dr.LaunchConfig(variant=1, stages=1), dr.LaunchConfig(variant=1, fault_inject=1),
+                dr.LaunchConfig(grid_ctas=1), dr.LaunchConfig(serialize=2), dr.LaunchConfig(wait_limit_us=-1),
+                dr.LaunchConfig(blocks_per_thread=3), dr.LaunchConfig(blocks_per_thread=16)):
         with pytest.raises(dr.DraddError) as e:
             dr.qk_resolve_config(64, 4096, 64, 512, 128, config=cfg)
         assert e.value.status == 9
