@@ -6,7 +6,8 @@ never imports, links or calls it, and the two share no code.
 
 The arithmetic lives in ``dradd_oracle.c`` (plain C, single-threaded,
 ``-ffp-contract=off``); this module compiles it with the host C compiler and
-wraps it with ctypes.  Arrays of bf16 values are numpy ``uint16`` bit
+wraps it with ctypes.  ``lse_oracle.c`` / ``oracle.lse`` hold the log-sum-exp
+merge and the launch-invariant elementwise functions.  Arrays of bf16 values are numpy ``uint16`` bit
 patterns.  See the C file's header for the page and sections it follows.
 
 parity pins: every function here is pinned by ``tests/test_oracle_*.py``.
@@ -54,12 +55,15 @@ def compile_source(src: Path, out: Path) -> Path:
 
 
 def build(force: bool = False) -> Path:
-    """Build ``liboracle.so`` next to the source if missing or stale."""
+    """Build ``liboracle.so`` (and the log-sum-exp oracle's library) next to
+    the sources if missing or stale."""
     with _lock:
         stale = (not LIB_PATH.exists()
                  or LIB_PATH.stat().st_mtime < SOURCE.stat().st_mtime)
         if force or stale:
             compile_source(SOURCE, LIB_PATH)
+    from . import lse
+    lse.build(force)
     return LIB_PATH
 
 
