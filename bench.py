@@ -609,6 +609,174 @@ def run_qk(args):
         tdist.destroy_process_group()
 
 
+# ------------------------------------------- log-sum-exp merge and log1p
+ELEM_METRIC = "launch-invariant LSE merge / log1p GB/s and % of HBM peak; within the stated bound of the oracle"
+
+
+def elem_bytes(w) -> int:
+    """merge: read the running lse and the step lse, write the merged lse
+    (12 B per merged element); log1p: 8 B per element."""
+    return 12 * w.rows * w.step_cols if w.kind == "merge" else 8 * w.rows * w.cols
+
+
+def run_elem(args):
+    import numpy as np
+    world, rank, local = dist_setup()
+    device = torch.device("cuda", local)
+    w = inputs.ELEM_WORKLOADS[args.workload]
+    L = dr.lib()
+    stream = torch.cuda.Stream(device)
+    d0 = w.make()
+    bytes_step = elem_bytes(w)
+    n_sets = max(N_SETS, -(-(4 * 129 * 2**20) // bytes_step))
+    st = stream.cuda_stream
+    sets, argv = [], []
+    for i in range(n_sets):
+        if w.kind == "merge":
+            run = (d0["lse"] if i == 0 else d0["lse"].roll(i, 0)).to(device).contiguous()
+            step = d0["step"].to(device)
+            off = w.cols - w.step_cols
+            half = run[:, off:]
+            sets.append((run, step))
+            argv.append((half.data_ptr(), w.cols, half.data_ptr(), w.cols, step.data_ptr(), w.step_cols,
+                         w.rows, w.step_cols, st))
+        else:
+            x = d0["x"].to(device)
+            y = torch.empty_like(x)
+            sets.append((x, y))
+            argv.append((y.data_ptr(), x.data_ptr(), x.numel(), 0, st))
+    fn = L.lse_merge_2d_fwd if w.kind == "merge" else L.invariant_unary_fwd
+    torch.cuda.synchronize()
+
+    def call(i):
+        rc = fn(*argv[i % n_sets])
+        if rc != 0:
+            raise dr.DraddError(rc, fn.__name__)
+
+    with torch.cuda.stream(stream):
+        sampler = ClockSampler(local)
+        with sampler:
+            ms = time_device(call, args.steps, args.warmup, stream, world, args.graph)
+    ms = max_over_ranks(ms, world)
+    ms_per_step = ms / args.steps
+    per_launch = bytes_step / (ms_per_step / 1e3) / 1e9
+    peak = measured_peaks().get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    if not peak:
+        peak = 6800.0
+    desc = (f"lse_merge_2d_fwd: [{w.rows} x {w.cols}] running fp32 lse, last {w.step_cols} columns of each row "
+            f"merged in place with a [{w.rows} x {w.step_cols}] step lse" if w.kind == "merge"
+            else f"invariant_unary_fwd log1p of {w.rows * w.cols} fp32 values")
+    line = {
+        "metric": ELEM_METRIC, "value": round(world * bytes_step * args.steps / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": desc, "io_dtype": "f32",
+                   "l2": f"{n_sets} rotating buffer sets ({n_sets * bytes_step // 2**20} MiB)"
+                         + (" > L2" if n_sets * bytes_step > 129e6 else " (fits in L2: latency-bound size)"),
+                   "launch": {"threads_per_cta": 128, "elements_per_thread": 8}, "cuda_graph": bool(args.graph),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(per_launch, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(per_launch / peak, 4), "peak_source": f"{peak_src} hbm_gbs", "traffic": None,
+                     "algorithmic_bytes_per_launch": bytes_step},
+        "gpu_launches": args.steps,
+        "e2e": None,
+    }
+    if rank == 0:
+        line["clocks"] = sampler.summary()
+        if not args.no_cpu:
+            import oracle.lse as lse_oracle
+            o = lse_oracle.lib()
+            t0 = time.perf_counter()
+            done = 0
+            if w.kind == "merge":
+                run_np, step_np = d0["lse"].numpy(), d0["step"].numpy()
+                off = w.cols - w.step_cols
+                while time.perf_counter() - t0 < args.cpu_seconds:
+                    r = done % w.rows
+                    o.merge(run_np[r, off:], step_np[r])
+                    done += 1
+                units, elems = "rows", done * w.step_cols
+                cpu_bytes = 12 * elems
+                # the timed steps merged in place repeatedly: check a fresh call
+                fresh = d0["lse"].to(device)
+                half = fresh[:, off:]
+                dr.lse_merge_fwd(half, d0["step"].to(device), out=half)
+                torch.cuda.synchronize()
+                got = fresh[0, off:].cpu().numpy()
+                ref = o.merge(run_np[0, off:], step_np[0])
+            else:
+                x_np = d0["x"].numpy()
+                chunk = 1 << 16
+                while time.perf_counter() - t0 < args.cpu_seconds:
+                    lo = (done * chunk) % (x_np.size - chunk + 1) if x_np.size > chunk else 0
+                    o.unary(x_np[lo:lo + chunk], "log1p")
+                    done += 1
+                units, elems = "chunks", done * min(chunk, x_np.size)
+                cpu_bytes = 8 * elems
+                got = sets[0][1][:4096].cpu().numpy()
+                ref = o.unary(x_np[:4096], "log1p")
+            dt = time.perf_counter() - t0
+            a = np.abs(ref)
+            ulp = 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -126))) - 23)
+            bound = ulp + (2.0 ** -22 if w.kind == "merge" else 0.0)
+            line["cpu_baseline"] = {
+                "value": round(cpu_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"{done} {units} ({elems} elements) of the workload in {dt:.1f} s, single thread, double",
+                "seconds": round(dt, 3), "parity_elements_checked": int(ref.size),
+                "parity_within_bound": bool(np.all(np.abs(got.astype(np.float64) - ref) <= bound))}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+
+
+def run_elem_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    import oracle.lse as lse_oracle
+    o = lse_oracle.lib()
+    w = inputs.ELEM_WORKLOADS[args.workload]
+    d0 = w.make()
+    if w.kind == "merge":
+        run_np, step_np = d0["lse"].numpy(), d0["step"].numpy()
+        off = w.cols - w.step_cols
+        t0 = time.perf_counter()
+        o.merge(run_np[0, off:], step_np[0])
+        t_row = max(1e-6, time.perf_counter() - t0)
+        rows = int(max(1, min(w.rows, args.reference_seconds / (args.warmup + args.steps) / t_row)))
+        def fn(i):
+            lo = (i * rows) % (w.rows - rows + 1)
+            o.merge(run_np[lo:lo + rows, off:], step_np[lo:lo + rows])
+        per_step = 12 * rows * w.step_cols
+        sample = f"{rows} of {w.rows} rows per step"
+    else:
+        x_np = d0["x"].numpy()
+        t0 = time.perf_counter()
+        o.unary(x_np[:4096], "log1p")
+        t_el = max(1e-9, (time.perf_counter() - t0) / 4096)
+        n = int(max(1, min(x_np.size, args.reference_seconds / (args.warmup + args.steps) / t_el)))
+        fn = lambda i: o.unary(x_np[:n], "log1p")
+        per_step = 8 * n
+        sample = f"{n} of {x_np.size} values per step"
+    for i in range(args.warmup):
+        fn(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        fn(i)
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": ELEM_METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload} (CPU oracle)", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{sample}, single thread"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0}), flush=True)
+
+
 def run_qk_reference(args):
     """The oracle on the host cores for a fused q/k workload."""
     if int(os.environ.get("RANK", "0")) != 0:
@@ -696,7 +864,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(WORKLOADS) + list(inputs.QK_WORKLOADS), default="4096x4096")
+    ap.add_argument("--workload", choices=list(WORKLOADS) + list(inputs.QK_WORKLOADS) + list(inputs.ELEM_WORKLOADS),
+                    default="4096x4096")
     ap.add_argument("--graph", type=int, default=1, help="replay the timed steps from CUDA graphs")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-e2e", action="store_true")
@@ -706,11 +875,12 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    qk = args.workload in inputs.QK_WORKLOADS
-    if args.impl == "reference":
-        (run_qk_reference if qk else run_reference)(args)
+    if args.workload in inputs.QK_WORKLOADS:
+        (run_qk_reference if args.impl == "reference" else run_qk)(args)
+    elif args.workload in inputs.ELEM_WORKLOADS:
+        (run_elem_reference if args.impl == "reference" else run_elem)(args)
     else:
-        (run_qk if qk else run_ours)(args)
+        (run_reference if args.impl == "reference" else run_ours)(args)
 
 
 if __name__ == "__main__":

@@ -146,6 +146,11 @@ def lib() -> ctypes.CDLL:
                        ("fused_qk_rmsnorm_group_quant_fwd_with_config", qk_args + [cfgp]),
                        ("dradd_qk_resolve_config", [_i64, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int,
                                                     cfgp, ctypes.POINTER(_QkPlan)]),
+                       ("lse_merge_fwd", [_vp, _vp, _vp, _i64, _vp]),
+                       ("lse_merge_2d_fwd", [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _vp]),
+                       ("lse_merge_2d_fwd_with_config", [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _vp, cfgp]),
+                       ("invariant_unary_fwd", [_vp, _vp, _i64, ctypes.c_int, _vp]),
+                       ("invariant_unary_fwd_with_config", [_vp, _vp, _i64, ctypes.c_int, _vp, cfgp]),
                        ("dradd_device_status", [_vp, ctypes.c_int]),
                        ("dradd_bf16_convert_range", [_vp, ctypes.c_uint64, _i64, ctypes.c_int, _vp])]:
         f = getattr(L, name)
@@ -523,6 +528,69 @@ def qk_resolve_config(n_q_rows: int, q_hidden: int, n_k_rows: int, k_hidden: int
                                          ctypes.byref(c) if c is not None else None, ctypes.byref(plan)),
            "dradd_qk_resolve_config")
     return QkPlan(*(getattr(plan, f) for f, _ in _QkPlan._fields_))
+
+
+UNARY_OPS = {"log1p": 0, "cosh": 1, "exp": 2}
+
+
+def _f32_ptr(t, name: str) -> int:
+    torch = _torch()
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32 (got {t.dtype})")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return t.data_ptr()
+
+
+def _elem_stride(t, name: str) -> tuple[int, int, int]:
+    """(rows, cols, row stride) of a 1-D or 2-D tensor with unit column stride."""
+    if t.dim() == 1:
+        if t.numel() > 1 and t.stride(0) != 1:
+            raise ValueError(f"{name} must have unit stride")
+        return (1 if t.numel() else 0), t.numel(), t.numel()
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError(f"{name} must be 1-D, or 2-D with unit column stride")
+    return t.shape[0], t.shape[1], t.stride(0) if t.shape[0] > 1 else t.shape[1]
+
+
+def lse_merge_fwd(lse_a, lse_b, *, out=None, stream=None, config: LaunchConfig | None = None):
+    """log(e^a + e^b) elementwise (fp32): 1-D tensors, or 2-D views with any
+    row stride (e.g. the second half of each row of a running lse).  out may
+    be lse_a or lse_b (in place)."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(lse_a.shape, dtype=torch.float32, device=lse_a.device)
+    ra, ca, sa = _elem_stride(lse_a, "lse_a")
+    rb, cb, sb = _elem_stride(lse_b, "lse_b")
+    ro, co, so = _elem_stride(out, "out")
+    if (ra, ca) != (rb, cb) or (ra, ca) != (ro, co):
+        raise ValueError("lse_a, lse_b and out must have the same shape")
+    args = (_f32_ptr(out, "out"), so, _f32_ptr(lse_a, "lse_a"), sa, _f32_ptr(lse_b, "lse_b"), sb, ra, ca,
+            _stream_handle(stream, lse_a.device))
+    with torch.cuda.device(lse_a.device):
+        if config is None:
+            _check(lib().lse_merge_2d_fwd(*args), "lse_merge_2d_fwd")
+        else:
+            c = config._c()
+            _check(lib().lse_merge_2d_fwd_with_config(*args, ctypes.byref(c)), "lse_merge_2d_fwd_with_config")
+    return out
+
+
+def invariant_unary_fwd(x, op: str = "log1p", *, out=None, stream=None, config: LaunchConfig | None = None):
+    """log1p / cosh / exp of a contiguous fp32 tensor, launch-invariant."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty_like(x)
+    if not x.is_contiguous() or not out.is_contiguous() or out.numel() != x.numel():
+        raise ValueError("x and out must be contiguous and the same size")
+    args = (_f32_ptr(out, "out"), _f32_ptr(x, "x"), x.numel(), UNARY_OPS[op], _stream_handle(stream, x.device))
+    with torch.cuda.device(x.device):
+        if config is None:
+            _check(lib().invariant_unary_fwd(*args), "invariant_unary_fwd")
+        else:
+            c = config._c()
+            _check(lib().invariant_unary_fwd_with_config(*args, ctypes.byref(c)), "invariant_unary_fwd_with_config")
+    return out
 
 
 def device_status(stream=None, clear: bool = True, device=None) -> int:

@@ -671,6 +671,128 @@ dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dra
     return e == cudaSuccess ? DRADD_OK : DRADD_ERR_CUDA;
 }
 
+// ------------------------------------------- log-sum-exp merge, unary math
+// Threads per CTA (cfg->threads_per_row, default 128), elements per thread
+// per pass (cfg->blocks_per_thread, default 8) and CTAs (cfg->grid_ctas,
+// default: two waves, 2 x SMs x 2048 / threads, at most one per unit).
+// The defaults are the fastest of a sweep on GB300 (CTA sizes 128-512, 2-8
+// elements per thread, grids of 2, 16 and 32 CTAs per SM).
+dradd_status elementwise_plan(int64_t n_rows, int64_t n_cols, const dradd_launch_cfg* cfg_in, int sm_count,
+                              int* threads, int* vec, int* grid, bool* serialize)
+{
+    dradd_launch_cfg cfg = {};
+    if (cfg_in)
+        cfg = *cfg_in;
+    if (cfg.variant != DRADD_VARIANT_AUTO || cfg.rows_per_cta != 0 || cfg.stages != 0 || cfg.fault_inject != 0 ||
+        cfg.wait_limit_us != 0 || cfg.grid_ctas < 0 || (cfg.serialize != 0 && cfg.serialize != 1))
+        return DRADD_ERR_BAD_CONFIG;
+    const int T = cfg.threads_per_row ? cfg.threads_per_row : 128;
+    const int V = cfg.blocks_per_thread ? cfg.blocks_per_thread : 8;
+    if (!is_pow2(T) || T < 32 || T > 1024 || (V != 1 && V != 2 && V != 4 && V != 8))
+        return DRADD_ERR_BAD_CONFIG;
+    const int64_t span = static_cast<int64_t>(T) * V;
+    const int64_t units = n_rows * ((n_cols + span - 1) / span);
+    int64_t G = cfg.grid_ctas;
+    if (G == 0) {
+        G = 2 * static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * (2048 / T);
+        if (G > units)
+            G = units;
+        if (G < 1)
+            G = 1;
+    }
+    if (G > 0x7FFFFFFF)
+        return DRADD_ERR_BAD_CONFIG;
+    *threads = T;
+    *vec = V;
+    *grid = static_cast<int>(G);
+    *serialize = cfg.serialize != 0;
+    return DRADD_OK;
+}
+
+// Byte range of a row-strided fp32 tensor.
+Range strided_range(const float* p, int64_t stride, int64_t n_rows, int64_t n_cols)
+{
+    return range_of(p, ((n_rows - 1) * stride + n_cols) * 4);
+}
+
+dradd_status lse_run(float* out, int64_t out_stride, const float* a, int64_t a_stride, const float* b,
+                     int64_t b_stride, int64_t n_rows, int64_t n_cols, cudaStream_t stream,
+                     const dradd_launch_cfg* cfg)
+{
+    if (n_rows < 0 || n_cols < 0)
+        return DRADD_ERR_BAD_SHAPE;
+    if (n_rows > 0 && n_cols > 0 && (out_stride < n_cols || a_stride < n_cols || b_stride < n_cols))
+        return DRADD_ERR_BAD_SHAPE;
+    for (int64_t stride : {out_stride, a_stride, b_stride})
+        if (n_rows > 0 && n_cols > 0 && n_rows - 1 > (INT64_MAX / 8 - n_cols) / (stride > 0 ? stride : 1))
+            return DRADD_ERR_BAD_SHAPE;
+    int threads = 0, vec = 0, grid = 0;
+    bool serialize = false;
+    dradd_status st = elementwise_plan(n_rows, n_cols, cfg, 152, &threads, &vec, &grid, &serialize);
+    if (st != DRADD_OK)
+        return st;
+    if (n_rows == 0 || n_cols == 0)
+        return DRADD_OK;
+    if (!out || !a || !b)
+        return DRADD_ERR_NULL_PTR;
+    if (!aligned(out, 4) || !aligned(a, 4) || !aligned(b, 4))
+        return DRADD_ERR_MISALIGNED;
+    // out may be exactly a or b (same address and stride: each element is
+    // read by the thread that then writes it); no other overlap
+    const Range ro = strided_range(out, out_stride, n_rows, n_cols);
+    const Range ra = strided_range(a, a_stride, n_rows, n_cols);
+    const Range rb = strided_range(b, b_stride, n_rows, n_cols);
+    if (ro.overlaps(ra) && !(out == a && out_stride == a_stride))
+        return DRADD_ERR_ALIAS;
+    if (ro.overlaps(rb) && !(out == b && out_stride == b_stride))
+        return DRADD_ERR_ALIAS;
+    DeviceLimits L;
+    st = query_limits(&L);
+    if (st != DRADD_OK)
+        return st;
+    st = elementwise_plan(n_rows, n_cols, cfg, L.sm_count, &threads, &vec, &grid, &serialize);
+    if (st != DRADD_OK)
+        return st;
+    return dradd::launch_lse_merge(out, out_stride, a, a_stride, b, b_stride, n_rows, n_cols, vec, grid, threads,
+                                   serialize, stream) == cudaSuccess
+               ? DRADD_OK
+               : DRADD_ERR_CUDA;
+}
+
+dradd_status unary_run(float* out, const float* x, int64_t n, int op, cudaStream_t stream,
+                       const dradd_launch_cfg* cfg)
+{
+    if (n < 0)
+        return DRADD_ERR_BAD_SHAPE;
+    if (n > INT64_MAX / 8)
+        return DRADD_ERR_BAD_SHAPE;
+    if (op < DRADD_UNARY_LOG1P || op > DRADD_UNARY_EXP)
+        return DRADD_ERR_BAD_CONFIG;
+    int threads = 0, vec = 0, grid = 0;
+    bool serialize = false;
+    dradd_status st = elementwise_plan(1, n, cfg, 152, &threads, &vec, &grid, &serialize);
+    if (st != DRADD_OK)
+        return st;
+    if (n == 0)
+        return DRADD_OK;
+    if (!out || !x)
+        return DRADD_ERR_NULL_PTR;
+    if (!aligned(out, 4) || !aligned(x, 4))
+        return DRADD_ERR_MISALIGNED;
+    if (range_of(out, n * 4).overlaps(range_of(x, n * 4)) && out != x)
+        return DRADD_ERR_ALIAS;
+    DeviceLimits L;
+    st = query_limits(&L);
+    if (st != DRADD_OK)
+        return st;
+    st = elementwise_plan(1, n, cfg, L.sm_count, &threads, &vec, &grid, &serialize);
+    if (st != DRADD_OK)
+        return st;
+    return dradd::launch_unary(out, x, n, op, vec, grid, threads, serialize, stream) == cudaSuccess
+               ? DRADD_OK
+               : DRADD_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -932,6 +1054,40 @@ dradd_status dradd_qk_resolve_config(int64_t n_q_rows, int64_t q_hidden, int64_t
     plan->k_stages = r.k.stages;
     plan->k_ctas = static_cast<int>(r.k.ctas);
     return DRADD_OK;
+}
+
+dradd_status lse_merge_fwd(float* out, const float* lse_a, const float* lse_b, int64_t n, cudaStream_t stream)
+{
+    return lse_run(out, n, lse_a, n, lse_b, n, n > 0 ? 1 : 0, n, stream, nullptr);
+}
+
+dradd_status lse_merge_2d_fwd(float* out, int64_t out_stride, const float* lse_a, int64_t a_stride,
+                              const float* lse_b, int64_t b_stride, int64_t n_rows, int64_t n_cols,
+                              cudaStream_t stream)
+{
+    return lse_run(out, out_stride, lse_a, a_stride, lse_b, b_stride, n_rows, n_cols, stream, nullptr);
+}
+
+dradd_status lse_merge_2d_fwd_with_config(float* out, int64_t out_stride, const float* lse_a, int64_t a_stride,
+                                          const float* lse_b, int64_t b_stride, int64_t n_rows, int64_t n_cols,
+                                          cudaStream_t stream, const dradd_launch_cfg* cfg)
+{
+    if (!cfg)
+        return DRADD_ERR_NULL_PTR;
+    return lse_run(out, out_stride, lse_a, a_stride, lse_b, b_stride, n_rows, n_cols, stream, cfg);
+}
+
+dradd_status invariant_unary_fwd(float* out, const float* x, int64_t n, int op, cudaStream_t stream)
+{
+    return unary_run(out, x, n, op, stream, nullptr);
+}
+
+dradd_status invariant_unary_fwd_with_config(float* out, const float* x, int64_t n, int op, cudaStream_t stream,
+                                             const dradd_launch_cfg* cfg)
+{
+    if (!cfg)
+        return DRADD_ERR_NULL_PTR;
+    return unary_run(out, x, n, op, stream, cfg);
 }
 
 dradd_status dradd_device_status(cudaStream_t stream, int clear)

@@ -98,4 +98,34 @@ cudaError_t launch_convert(uint16_t* out, uint64_t first, int64_t count, int met
 cudaError_t read_device_status(unsigned* status, bool clear, cudaStream_t stream);
 cudaError_t device_status_ptr(unsigned** ptr);
 
+// Launch with programmatic stream serialization unless `serialize`: the
+// kernel may then be scheduled while the previous kernel in the stream is
+// still draining, and waits for it (griddepcontrol.wait) before touching
+// global memory.
+template <typename... Args>
+inline cudaError_t launch(void (*fn)(Args...), int grid, int threads, size_t dyn_smem, bool serialize,
+                          cudaStream_t stream, Args... args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = dyn_smem;
+    cfg.stream = stream;
+    cfg.attrs = serialize ? nullptr : attr;
+    cfg.numAttrs = serialize ? 0 : 1;
+    return cudaLaunchKernelEx(&cfg, fn, args...);
+}
+
+// Log-sum-exp merge and launch-invariant elementwise functions
+// (dradd_lse.cu).  Rows of n_cols elements, row strides in elements; a flat
+// array is one row.  vec: elements per thread per pass (1, 2, 4, 8).
+cudaError_t launch_lse_merge(float* out, int64_t out_stride, const float* a, int64_t a_stride, const float* b,
+                             int64_t b_stride, int64_t n_rows, int64_t n_cols, int vec, int grid, int threads,
+                             bool serialize, cudaStream_t stream);
+cudaError_t launch_unary(float* out, const float* x, int64_t n, int op, int vec, int grid, int threads,
+                         bool serialize, cudaStream_t stream);
+
 }  // namespace dradd

@@ -176,27 +176,6 @@ cudaError_t device_status_ptr(unsigned** ptr)
     return cudaSuccess;
 }
 
-// Launch with programmatic stream serialization unless `serialize`: the
-// kernel may then be scheduled while the previous kernel in the stream is
-// still draining, and waits for it (griddepcontrol.wait) before touching
-// global memory.
-template <typename... Args>
-static cudaError_t launch(void (*fn)(Args...), int grid, int threads, size_t dyn_smem, bool serialize,
-                          cudaStream_t stream, Args... args)
-{
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(static_cast<unsigned>(threads));
-    cfg.dynamicSmemBytes = dyn_smem;
-    cfg.stream = stream;
-    cfg.attrs = serialize ? nullptr : attr;
-    cfg.numAttrs = serialize ? 0 : 1;
-    return cudaLaunchKernelEx(&cfg, fn, args...);
-}
-
 cudaError_t launch_rows(const Params& p, int K, int out, bool add, int grid, int threads, bool serialize,
                         cudaStream_t stream)
 {

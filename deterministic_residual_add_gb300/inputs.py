@@ -30,6 +30,12 @@ residual, q weight, k, k weight.
                   k 1 x 512                                           seed 5
   qk_heads4096    4096 tokens: q 32 heads x 128, k 8 heads x 128, bf16 out,
                   no residual                                         seed 6
+
+Log-sum-exp merge and elementwise workloads (ELEM_WORKLOADS; fp32):
+softmax log-sum-exps of attention rows are values of about log(S) plus a
+score scale, drawn as N(8, 3) for the running lse and the step lse (seed 7);
+log1p inputs are uniform in [0, 1) as in the TransformerEngine page's
+reproducer (N = 225,280; seed 0), plus a 16M-element case.
 """
 from __future__ import annotations
 
@@ -224,3 +230,32 @@ def hashed_bf16_rows(rows: torch.Tensor, hidden: int, salt: int) -> torch.Tensor
     expo = 0x7B + ((hsh >> 7) & 0x7)
     sign = ((hsh >> 10) & 1) << 15
     return (sign | (expo << 7) | mant).to(torch.int16)
+
+
+@dataclass(frozen=True)
+class ElemWorkload:
+    """fp32 elementwise workloads: kind "merge" (rows x cols running lse and
+    a step lse of rows x step_cols, merged into the last step_cols columns
+    of each row, in place) or "log1p" (n values)."""
+    name: str
+    kind: str
+    rows: int
+    cols: int
+    step_cols: int
+    seed: int
+
+    def make(self):
+        g = generator(self.seed)
+        if self.kind == "log1p":
+            return {"x": torch.rand((self.rows * self.cols,), generator=g, dtype=torch.float32)}
+        run = torch.randn((self.rows, self.cols), generator=g, dtype=torch.float32) * 3.0 + 8.0
+        step = torch.randn((self.rows, self.step_cols), generator=g, dtype=torch.float32) * 3.0 + 8.0
+        return {"lse": run, "step": step}
+
+
+ELEM_WORKLOADS = {
+    "lse_merge8x32x32768": ElemWorkload("lse_merge8x32x32768", "merge", 8 * 32, 32768, 32768, seed=7),
+    "lse_merge_half8x32x32768": ElemWorkload("lse_merge_half8x32x32768", "merge", 8 * 32, 32768, 16384, seed=7),
+    "log1p225280": ElemWorkload("log1p225280", "log1p", 1, 225280, 0, seed=0),
+    "log1p16M": ElemWorkload("log1p16M", "log1p", 1, 1 << 24, 0, seed=0),
+}

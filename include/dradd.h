@@ -418,6 +418,69 @@ dradd_status dradd_qk_resolve_config(int64_t n_q_rows, int64_t q_hidden, int64_t
                                      const dradd_launch_cfg* cfg, dradd_qk_plan* plan);
 
 /*
+ * Log-sum-exp merge and launch-invariant elementwise functions.
+ * Page: ROCm/TransformerEngine issue #693, "CP LSE merge switches compiled
+ * variants on ROCm, breaking forward reproducibility".  Context-parallel
+ * attention merges the softmax log-sum-exp of blocks computed on different
+ * ranks ("Summary"; one merge function is for the second half of the
+ * sequence), and the page traces a forward mismatch to log1p (and cosh)
+ * giving different bits under different launch configurations of the same
+ * compiled function ("Root cause", "Minimal reproducer").  Here every
+ * element is computed by one fixed sequence of fp32 operations whatever
+ * the launch configuration: the results below depend on the inputs only.
+ *
+ * lse_merge_fwd -- out[i] = log(e^a[i] + e^b[i]), evaluated as
+ *   hi + log1p(exp(lo - hi)) with hi = max(a, b), lo = min(a, b), in fp32
+ *   with the CUDA math library's expf and log1pf (documented to within 2
+ *   and 1 ulp).  Both -inf (two empty blocks) gives -inf; a +inf operand
+ *   gives +inf; NaN gives NaN.  Within 1 ulp(result) + 2^-22 of the exact
+ *   value (the bound the tests use).
+ *   out, lse_a, lse_b: n fp32 values, 4-byte aligned; out may be exactly
+ *   lse_a or lse_b (an in-place running merge); no other overlap.
+ */
+dradd_status lse_merge_fwd(float* out, const float* lse_a, const float* lse_b, int64_t n, cudaStream_t stream);
+
+/*
+ * lse_merge_2d_fwd -- the same merge over n_rows rows of n_cols elements
+ * with a row stride (in elements, >= n_cols) per operand:
+ *   out[r * out_stride + c] = merge(lse_a[r * a_stride + c],
+ *                                   lse_b[r * b_stride + c]).
+ * The second-half merge of a [rows x S] running lse with a [rows x S/2]
+ * per-step lse is lse_merge_2d_fwd(lse + S/2, S, lse + S/2, S, step, S/2,
+ * rows, S/2).  out may be exactly lse_a or lse_b (same address and stride);
+ * no other overlap of the spans the three operands cover.
+ */
+dradd_status lse_merge_2d_fwd(float* out, int64_t out_stride, const float* lse_a, int64_t a_stride,
+                              const float* lse_b, int64_t b_stride, int64_t n_rows, int64_t n_cols,
+                              cudaStream_t stream);
+
+/*
+ * Test hook: the merge with an explicit configuration.  threads_per_row is
+ * read as the threads of a CTA (a power of two, 32..1024), blocks_per_thread
+ * as the elements a thread handles per pass (1, 2, 4, 8), grid_ctas as the
+ * CTAs; serialize as above; every other field must be 0.  Results never
+ * depend on it.
+ */
+dradd_status lse_merge_2d_fwd_with_config(float* out, int64_t out_stride, const float* lse_a, int64_t a_stride,
+                                          const float* lse_b, int64_t b_stride, int64_t n_rows, int64_t n_cols,
+                                          cudaStream_t stream, const dradd_launch_cfg* cfg);
+
+enum { DRADD_UNARY_LOG1P = 0, DRADD_UNARY_COSH = 1, DRADD_UNARY_EXP = 2 };
+
+/*
+ * invariant_unary_fwd -- out[i] = f(x[i]) for f = log1pf, coshf or expf
+ * (DRADD_UNARY_*; CUDA math library: within 1, 3 and 2 ulp in the tests),
+ * the same bits under every launch configuration.  n fp32 values, 4-byte
+ * aligned; out may be exactly x; an unknown op is DRADD_ERR_BAD_CONFIG.
+ */
+dradd_status invariant_unary_fwd(float* out, const float* x, int64_t n, int op, cudaStream_t stream);
+
+/* Test hook: invariant_unary_fwd with an explicit configuration (fields as
+ * for lse_merge_2d_fwd_with_config). */
+dradd_status invariant_unary_fwd_with_config(float* out, const float* x, int64_t n, int op, cudaStream_t stream,
+                                             const dradd_launch_cfg* cfg);
+
+/*
  * dradd_device_status -- synchronise `stream`, then return DRADD_OK or the
  * error a kernel recorded on the current device since the last clear
  * (DRADD_ERR_TIMEOUT).  clear != 0 resets the word afterwards.
