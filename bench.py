@@ -298,11 +298,13 @@ def time_device(call, steps, warmup, stream, world, use_graph):
     return start.elapsed_time(end)  # ms
 
 
-def time_e2e(steps, device, stream, name, chunk_rows=1024):
-    """Public API with host data: per step, the inputs (x, residual, weight)
-    go from pinned host memory to the device and the outputs come back, with
-    the copies overlapped with the kernels chunk by chunk (host.HostPipeline)."""
-    from deterministic_residual_add_gb300.host import HostPipeline
+def time_e2e(steps, device, stream, name):
+    """Public API with host data: per step, the kernel reads that step's
+    inputs (x, residual, weight) from pinned host memory over the host link
+    and writes out and residual_out back to pinned host memory
+    (host.add_rmsnorm_fwd_host, zero copy); the step ends when the stream
+    has finished, i.e. when the results are in host memory."""
+    from deterministic_residual_add_gb300.host import add_rmsnorm_fwd_host
     n, h, op, _ = WORKLOADS[name]
     quant = op == "add_rmsnorm_quant"
     xs, r0, w = workload_inputs(name)
@@ -313,14 +315,13 @@ def time_e2e(steps, device, stream, name, chunk_rows=1024):
                 torch.empty(n, dtype=torch.float32).pin_memory(), ro_h)
     else:
         outs = (torch.empty_like(x_h).pin_memory(), ro_h)
-    pipe = HostPipeline(n, h, device, chunk_rows=chunk_rows, quant=quant)
     with torch.cuda.stream(stream):
-        for _ in range(2):
-            pipe(x_h, r_h, w_h, inputs.EPS, outs)
+        for _ in range(3):
+            add_rmsnorm_fwd_host(x_h, r_h, w_h, inputs.EPS, outs, stream=stream, quant=quant)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(steps):
-            pipe(x_h, r_h, w_h, inputs.EPS, outs)
+            add_rmsnorm_fwd_host(x_h, r_h, w_h, inputs.EPS, outs, stream=stream, quant=quant)
         torch.cuda.synchronize()
         dt = time.perf_counter() - t0
     bi = (x_h.numel() + r_h.numel() + w_h.numel()) * 2
@@ -414,7 +415,7 @@ def run_ours(args):
         e2e = {"value": round(world * bytes_step * e2e_steps / dt / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
                "ms_per_step": round(dt / e2e_steps * 1e3, 4),
-               "pipeline": "1024-row chunks, upload / kernel / download on 3 streams"}
+               "pipeline": "zero copy: the kernel reads and writes pinned host memory over the host link"}
 
     sm_count = torch.cuda.get_device_properties(device).multi_processor_count
     if op == "residual_add":

@@ -6,6 +6,7 @@
 // the partial sums in the same canonical pairwise order for every choice.
 #include <atomic>
 #include <cmath>
+#include <initializer_list>
 #include <cstdint>
 #include <cstring>
 
@@ -58,6 +59,26 @@ dradd_status query_limits(DeviceLimits* out)
     }
     *out = L;
     return DRADD_OK;
+}
+
+// True when every non-NULL pointer is device memory.  Other memory the GPU
+// can address (pinned or registered host memory, memory the GPU reaches
+// through the host link, managed memory) is served by the register-load
+// variant only: the staged variant's bulk copies are used on device memory.
+bool all_device_memory(std::initializer_list<const void*> ptrs)
+{
+    for (const void* p : ptrs) {
+        if (!p)
+            continue;
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+            cudaGetLastError();  // not a sticky error; the pointer is simply not device memory
+            return false;
+        }
+        if (a.type != cudaMemoryTypeDevice)
+            return false;
+    }
+    return true;
 }
 
 bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
@@ -317,6 +338,11 @@ dradd_status run(int out_kind, bool add, dradd_bf16* out, int8_t* out_q, float* 
     if (user_cfg)
         cfg = *user_cfg;
     const bool auto_grid = cfg.grid_ctas == 0;
+    if (!all_device_memory({out, out_q, scale, residual_out, x, residual, weight})) {
+        if (cfg.variant == DRADD_VARIANT_STAGED)
+            return DRADD_ERR_BAD_CONFIG;
+        cfg.variant = DRADD_VARIANT_ROWS;
+    }
     st = resolve(n_rows, hidden, quant, add, L, &cfg);
     if (st != DRADD_OK)
         return st;
@@ -612,6 +638,15 @@ dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dra
     st = query_limits(&L);
     if (st != DRADD_OK)
         return st;
+    dradd_launch_cfg eff = {};
+    if (cfg)
+        eff = *cfg;
+    if (!all_device_memory({q_out, q_scale, q_residual_out, k_out, q, q_residual, q_weight, k, k_weight})) {
+        if (eff.variant == DRADD_VARIANT_STAGED || eff.stages != 0 || eff.fault_inject != 0)
+            return DRADD_ERR_BAD_CONFIG;
+        eff.variant = DRADD_VARIANT_ROWS;
+    }
+    cfg = &eff;
     st = qk_plan(n_q, hq, n_k, hk, group_size, add, L.sm_count, 0, L.smem_per_block_optin, cfg, &plan);
     if (st != DRADD_OK)
         return st;

@@ -1,5 +1,15 @@
-"""Host-buffer driver: run the forward on tensors that live in (pinned) host
-memory, overlapping the copies with the kernels.
+"""Host-buffer drivers: run the forward on tensors that live in pinned host
+memory.
+
+``add_rmsnorm_fwd_host`` (the fast path on Grace-Blackwell): the kernel
+reads x, residual and weight from pinned host memory and writes out and
+residual_out back to it directly over the host link (zero copy); no device
+buffers, no copies.  The C library sees host pointers and uses its
+register-load variant, so the results are the same bits as a device call.
+
+``HostPipeline`` (copy engines): the rows are cut into chunks and each chunk
+is copied to the device, processed and copied back, with the copies
+overlapped with the kernels.
 
 The rows are cut into chunks.  Chunk c is copied host-to-device on one
 stream, processed by the library's kernel on a second stream once its copy
@@ -16,7 +26,48 @@ from __future__ import annotations
 
 import torch
 
-from . import add_rmsnorm_fwd, add_rmsnorm_quant_fwd
+from . import DraddError, add_rmsnorm_fwd, add_rmsnorm_quant_fwd, lib
+
+
+def _pinned_ptr(t, name: str, numel: int, dtypes) -> int:
+    if t.device.type != "cpu" or not t.is_pinned():
+        raise ValueError(f"{name} must be a pinned host tensor")
+    if t.dtype not in dtypes or not t.is_contiguous() or t.numel() != numel:
+        raise ValueError(f"{name}: expected a contiguous {dtypes[0]} tensor of {numel} elements")
+    return t.data_ptr()
+
+
+def add_rmsnorm_fwd_host(x_h, r_h, w_h, eps: float, outs_h, stream=None, quant: bool = False):
+    """Residual-add + RMSNorm of pinned host tensors, read and written by the
+    kernel directly over the host link.  x_h, r_h: [n_rows, hidden] bf16;
+    w_h: [hidden] bf16; outs_h: (out, residual_out), or for quant
+    (out_q int8, scale fp32 [n_rows], residual_out).  Enqueues on `stream`
+    (default: the current stream of cuda:0 or the current device) and
+    returns; synchronise the stream before reading the outputs."""
+    import ctypes
+    import torch
+    bf16 = (torch.bfloat16, torch.int16)
+    hidden = int(x_h.shape[-1])
+    n_rows = x_h.numel() // hidden if hidden else 0
+    n = n_rows * hidden
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    args_in = (_pinned_ptr(x_h, "x", n, bf16), _pinned_ptr(r_h, "residual", n, bf16),
+               _pinned_ptr(w_h, "weight", hidden, bf16), ctypes.c_float(eps), n_rows, hidden, stream.cuda_stream)
+    if quant:
+        q_h, s_h, ro_h = outs_h
+        st = lib().add_rmsnorm_quant_fwd(_pinned_ptr(q_h, "out_q", n, (torch.int8,)),
+                                         _pinned_ptr(s_h, "scale", n_rows, (torch.float32,)),
+                                         _pinned_ptr(ro_h, "residual_out", n, bf16), *args_in)
+        where = "add_rmsnorm_quant_fwd"
+    else:
+        out_h, ro_h = outs_h
+        st = lib().add_rmsnorm_fwd(_pinned_ptr(out_h, "out", n, bf16), _pinned_ptr(ro_h, "residual_out", n, bf16),
+                                   *args_in)
+        where = "add_rmsnorm_fwd"
+    if st != 0:
+        raise DraddError(st, where)
+    return outs_h
 
 
 class HostPipeline:

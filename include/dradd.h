@@ -30,9 +30,16 @@
  *   - x, residual, out, residual_out: row-major, n_rows x hidden, contiguous
  *     (row stride = hidden elements).  weight: hidden elements, shared by
  *     all rows.
- *   - All pointers are DEVICE pointers (cudaMalloc'd or otherwise addressable
- *     by the current device).  The caller allocates and owns every buffer;
- *     the library allocates no device memory and keeps no per-call state.
+ *   - All pointers are addressable by the current device: device memory
+ *     (cudaMalloc'd), or host memory the device can reach (pinned or
+ *     registered host memory, memory behind the Grace-Blackwell host link,
+ *     managed memory).  With any non-device buffer the kernels read and
+ *     write it directly over the host link (zero copy) and the register-load
+ *     variant is used; an explicit DRADD_VARIANT_STAGED configuration (or a
+ *     stage count or fault hook for the fused q/k call) with such a buffer
+ *     is rejected with DRADD_ERR_BAD_CONFIG.  The caller allocates and owns
+ *     every buffer; the library allocates no device memory and keeps no
+ *     per-call state.
  *   - Every array pointer must be 16-byte aligned (scale: 4-byte aligned).
  *   - 1 <= hidden <= DRADD_MAX_HIDDEN and hidden % 8 == 0.  n_rows >= 0;
  *     n_rows == 0 is a successful no-op (pointers are not inspected).
