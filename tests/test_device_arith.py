@@ -4,7 +4,10 @@ IEEE fp32 operations (the same operations the kernels issue):
 - the group scale RN(amax / 448) of the per-group fp8 output is computed by
   one multiplication and two fused multiply-adds (a division with one
   correction step); tests/div448_check.c compares it with the correctly
-  rounded quotient for every fp32 amax in [2^-100, 2^128)."""
+  rounded quotient for every fp32 amax in [2^-100, 2^128);
+- the LSE merge's log1p(u) on [0, 1] by the atanh series;
+  tests/log1p_series_check.c compares it with log1p in double for every
+  fp32 u in [0, 1]."""
 import os
 import subprocess
 from concurrent.futures import ThreadPoolExecutor
@@ -33,3 +36,27 @@ def test_div448_correction_step_is_correctly_rounded(tmp_path):
         assert r.returncode == 0, r.stdout + r.stderr
         checked += int(r.stdout.split()[1])
     assert checked == len(exps) << 23
+
+
+def test_log1p_series_on_unit_interval(tmp_path):
+    """The LSE merge's log1p(u), u in [0, 1] (tests/log1p_series_check.c runs
+    the kernel's fp32 operations): every fp32 u within 3 x 2^-24 relative
+    (plus 2^-148 absolute for subnormal u) of log1p in double."""
+    exe = tmp_path / "log1p_series_check"
+    subprocess.run([oracle._compiler(), "-O2", "-std=c11", "-ffp-contract=off", "-o", str(exe),
+                    str(HERE / "log1p_series_check.c"), "-lm"], check=True)
+    last = 0x3F800000
+    parts = 32
+    step = (last + 1) // parts
+    ranges = [(k * step, last if k == parts - 1 else (k + 1) * step - 1) for k in range(parts)]
+
+    def run(r):
+        return subprocess.run([str(exe), hex(r[0]), hex(r[1])], capture_output=True, text=True)
+
+    with ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1))) as ex:
+        results = list(ex.map(run, ranges))
+    checked = 0
+    for r in results:
+        assert r.returncode == 0, r.stdout + r.stderr
+        checked += int(r.stdout.split()[1])
+    assert checked == last + 1

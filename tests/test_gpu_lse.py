@@ -1,7 +1,8 @@
 """Log-sum-exp merge and launch-invariant unary functions on the GPU,
 through the C ABI, against the double-precision oracle: within
 ulp(result) + 2^-22 for the merge (the bound the merge's arithmetic gives:
-the fp32 expf and log1pf errors scaled by at most 1/2, plus the final
+expf's error scaled by at most 1/2, the series log1p's 2.95 x 2^-24
+relative of a value below ln 2, the rounding of lo - hi, and the final
 rounding) and within the CUDA math library's documented ulp bounds for the
 unary functions (coshf: its measured maximum, below 3 ulp); special
 values exactly; and one result, bit for bit, under
