@@ -25,13 +25,13 @@ __all__ = [
     "add_rmsnorm_fp8_fwd", "rmsnorm_fp8_fwd", "add_rmsnorm_fp4_fwd", "rmsnorm_fp4_fwd",
     "LaunchConfig", "DraddError", "resolve_config",
     "device_status", "bf16_convert_range", "status_string", "abi_version", "lib", "library_path",
-    "VARIANT_AUTO", "VARIANT_ROWS", "VARIANT_STAGED", "MAX_HIDDEN",
+    "VARIANT_AUTO", "VARIANT_ROWS", "VARIANT_STAGED", "VARIANT_SPLIT", "MAX_HIDDEN",
 ]
 
 PKG = Path(__file__).resolve().parent
 LIB_PATH = PKG / "libdradd.so"
 MAX_HIDDEN = 32768
-VARIANT_AUTO, VARIANT_ROWS, VARIANT_STAGED = 0, 1, 2
+VARIANT_AUTO, VARIANT_ROWS, VARIANT_STAGED, VARIANT_SPLIT = 0, 1, 2, 3
 OP_ADD_RMSNORM, OP_ADD_RMSNORM_QUANT, OP_RMSNORM, OP_RMSNORM_QUANT = 0, 1, 2, 3
 OP_ADD_RMSNORM_FP8, OP_RMSNORM_FP8 = 4, 5
 OP_ADD_RMSNORM_FP4, OP_RMSNORM_FP4 = 6, 7
@@ -53,7 +53,7 @@ class DraddError(RuntimeError):
 class _LaunchCfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "variant", "threads_per_row", "rows_per_cta", "grid_ctas", "stages", "fault_inject",
-        "wait_limit_us", "serialize", "blocks_per_thread")]
+        "wait_limit_us", "serialize", "blocks_per_thread", "cluster_ctas")]
 
 
 @dataclass
@@ -68,16 +68,17 @@ class LaunchConfig:
     wait_limit_us: int = 0
     serialize: int = 0
     blocks_per_thread: int = 0
+    cluster_ctas: int = 0
 
     def _c(self) -> _LaunchCfg:
         return _LaunchCfg(self.variant, self.threads_per_row, self.rows_per_cta, self.grid_ctas,
                           self.stages, self.fault_inject, self.wait_limit_us, self.serialize,
-                          self.blocks_per_thread)
+                          self.blocks_per_thread, self.cluster_ctas)
 
     @staticmethod
     def _from_c(c: _LaunchCfg) -> "LaunchConfig":
         return LaunchConfig(c.variant, c.threads_per_row, c.rows_per_cta, c.grid_ctas, c.stages,
-                            c.fault_inject, c.wait_limit_us, c.serialize, c.blocks_per_thread)
+                            c.fault_inject, c.wait_limit_us, c.serialize, c.blocks_per_thread, c.cluster_ctas)
 
 
 class _QkPlan(ctypes.Structure):

@@ -185,6 +185,82 @@ dradd_status validate(int out_kind, bool add, const void* out, const void* out_q
     return check_overlaps(inputs, n_in, outs, bf16_out, n_out);
 }
 
+// The split-row variant: a cluster of C CTAs per row (bf16 out only), each
+// CTA a slice of P / C elements with T threads and K blocks of 8 per thread.
+// Automatic: C = 2, T = slice blocks / 4 (at least 32, K at most 8), 2
+// stages, as many clusters as fit.
+dradd_status resolve_split(int64_t n_rows, int64_t hidden, bool quant, bool add, const DeviceLimits& L,
+                           dradd_launch_cfg* cfg)
+{
+    const int64_t P = next_pow2(hidden);
+    if (quant)
+        return DRADD_ERR_BAD_CONFIG;
+    const int C = cfg->cluster_ctas ? cfg->cluster_ctas : 2;
+    if (C != 2 && C != 4)
+        return DRADD_ERR_BAD_CONFIG;
+    const int64_t slice_blocks = P / 8 / C;
+    if (slice_blocks < 32)
+        return DRADD_ERR_BAD_CONFIG;
+    if (cfg->threads_per_row == 0) {
+        int64_t T;
+        if (cfg->blocks_per_thread != 0) {
+            if (!is_pow2(cfg->blocks_per_thread) || slice_blocks % cfg->blocks_per_thread != 0)
+                return DRADD_ERR_BAD_CONFIG;
+            T = slice_blocks / cfg->blocks_per_thread;
+        } else {
+            T = slice_blocks / 4 < 32 ? 32 : slice_blocks / 4;
+            while (slice_blocks / T > 8)
+                T *= 2;
+            if (T > slice_blocks)
+                T = slice_blocks;
+        }
+        cfg->threads_per_row = static_cast<int>(T);
+    }
+    const int T = cfg->threads_per_row;
+    if (!is_pow2(T) || T < 32 || T > 1024 || slice_blocks % T != 0)
+        return DRADD_ERR_BAD_CONFIG;
+    const int64_t K = slice_blocks / T;
+    if ((K != 1 && K != 2 && K != 4 && K != 8) || T > dradd::max_threads_for(static_cast<int>(K)) ||
+        (cfg->blocks_per_thread != 0 && cfg->blocks_per_thread != K))
+        return DRADD_ERR_BAD_CONFIG;
+    cfg->blocks_per_thread = static_cast<int>(K);
+    if (cfg->rows_per_cta == 0)
+        cfg->rows_per_cta = 1;
+    if (cfg->rows_per_cta != 1 || cfg->wait_limit_us < 0 || (cfg->serialize != 0 && cfg->serialize != 1) ||
+        cfg->fault_inject < 0)
+        return DRADD_ERR_BAD_CONFIG;
+    const int64_t stage_bytes = (add ? 4 : 2) * (P / C);
+    const int64_t static_smem = static_cast<int64_t>(dradd::split_static_smem(static_cast<int>(K)));
+    const int64_t avail = L.smem_per_block_optin - static_smem - 8 * 8;
+    if (cfg->stages == 0) {
+        const int64_t S = avail / stage_bytes;
+        cfg->stages = static_cast<int>(S > 2 ? 2 : S);
+    }
+    const int S = cfg->stages;
+    if (S < 1 || S > 8 || S * stage_bytes > avail)
+        return DRADD_ERR_BAD_CONFIG;
+    if (cfg->grid_ctas == 0) {
+        int ctas_per_sm = L.max_threads_per_sm / T;
+        if (ctas_per_sm > L.max_blocks_per_sm)
+            ctas_per_sm = L.max_blocks_per_sm;
+        const int64_t per_cta = S * stage_bytes + static_smem + 8 * S + 1024;
+        if (L.smem_per_sm / per_cta < ctas_per_sm)
+            ctas_per_sm = static_cast<int>(L.smem_per_sm / per_cta);
+        int64_t clusters = static_cast<int64_t>(L.sm_count) * (ctas_per_sm > 0 ? ctas_per_sm : 1) / C;
+        if (clusters > n_rows)
+            clusters = n_rows;
+        if (clusters < 1)
+            clusters = 1;
+        if (clusters * C > 0x7FFFFFFF)
+            clusters = 0x7FFFFFFF / C;
+        cfg->grid_ctas = static_cast<int>(clusters * C);
+    }
+    if (cfg->grid_ctas < C || cfg->grid_ctas % C != 0)
+        return DRADD_ERR_BAD_CONFIG;
+    cfg->cluster_ctas = C;
+    return DRADD_OK;
+}
+
 // Fill the automatic fields of *cfg and check the explicit ones.
 dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const DeviceLimits& L,
                      dradd_launch_cfg* cfg)
@@ -211,6 +287,10 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     const bool auto_variant = cfg->variant == DRADD_VARIANT_AUTO;
     if (auto_variant)
         cfg->variant = hidden > 256 ? DRADD_VARIANT_STAGED : DRADD_VARIANT_ROWS;
+    if (cfg->variant == DRADD_VARIANT_SPLIT)
+        return resolve_split(n_rows, hidden, quant, add, L, cfg);
+    if (cfg->cluster_ctas != 0)
+        return DRADD_ERR_BAD_CONFIG;
     if (cfg->variant != DRADD_VARIANT_ROWS && cfg->variant != DRADD_VARIANT_STAGED)
         return DRADD_ERR_BAD_CONFIG;
     const bool staged = cfg->variant == DRADD_VARIANT_STAGED;
@@ -339,13 +419,51 @@ dradd_status run(int out_kind, bool add, dradd_bf16* out, int8_t* out_q, float* 
         cfg = *user_cfg;
     const bool auto_grid = cfg.grid_ctas == 0;
     if (!all_device_memory({out, out_q, scale, residual_out, x, residual, weight})) {
-        if (cfg.variant == DRADD_VARIANT_STAGED)
+        if (cfg.variant == DRADD_VARIANT_STAGED || cfg.variant == DRADD_VARIANT_SPLIT)
             return DRADD_ERR_BAD_CONFIG;
         cfg.variant = DRADD_VARIANT_ROWS;
     }
     st = resolve(n_rows, hidden, quant, add, L, &cfg);
     if (st != DRADD_OK)
         return st;
+    if (cfg.variant == DRADD_VARIANT_SPLIT) {
+        const int C = cfg.cluster_ctas;
+        const int Ks = cfg.blocks_per_thread;
+        const size_t dyn_s = static_cast<size_t>(cfg.stages) *
+                                 ((add ? 4 : 2) * static_cast<size_t>(next_pow2(hidden) / C) + 8);
+        int grid = cfg.grid_ctas;
+        if (auto_grid) {
+            int clusters = 0;
+            if (dradd::split_max_clusters(Ks, C, add, cfg.threads_per_row, dyn_s, &clusters) != cudaSuccess)
+                return DRADD_ERR_CUDA;
+            int64_t c = clusters > 0 ? clusters : 1;
+            if (c > n_rows)
+                c = n_rows;
+            grid = static_cast<int>(c * C);
+        }
+        Params p = {};
+        p.out = out;
+        p.residual_out = residual_out;
+        p.x = x;
+        p.residual = residual;
+        p.weight = weight;
+        p.eps = eps;
+        p.hidden = static_cast<int>(hidden);
+        p.inv_hidden = is_pow2(hidden) ? 1.0f / static_cast<float>(hidden) : 0.0f;
+        p.n_rows = n_rows;
+        p.threads_per_row = cfg.threads_per_row;
+        p.rows_per_cta = 1;
+        p.stages = cfg.stages;
+        p.fault_inject = cfg.fault_inject;
+        p.wait_limit_ns = cfg.wait_limit_us > 0 ? static_cast<uint64_t>(cfg.wait_limit_us) * 1000ull
+                                                : kDefaultWaitLimitNs;
+        if (dradd::device_status_ptr(&p.status) != cudaSuccess)
+            return DRADD_ERR_CUDA;
+        return dradd::launch_split(p, Ks, C, add, grid, cfg.threads_per_row, dyn_s, cfg.serialize != 0, stream) ==
+                       cudaSuccess
+                   ? DRADD_OK
+                   : DRADD_ERR_CUDA;
+    }
     const int K = static_cast<int>(next_pow2(hidden) / 8 / cfg.threads_per_row);
     const size_t dyn = cfg.variant == DRADD_VARIANT_STAGED
                            ? static_cast<size_t>(cfg.stages) * (add ? 4 : 2) * static_cast<size_t>(hidden) +
@@ -462,7 +580,8 @@ dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t g
     if (cfg.variant < DRADD_VARIANT_AUTO || cfg.variant > DRADD_VARIANT_STAGED || cfg.rows_per_cta != 0 ||
         cfg.stages < 0 || cfg.stages > 8 || cfg.fault_inject < 0 || cfg.wait_limit_us < 0 || cfg.grid_ctas < 0 ||
         (cfg.serialize != 0 && cfg.serialize != 1) ||
-        (cfg.blocks_per_thread != 0 && (!is_pow2(cfg.blocks_per_thread) || cfg.blocks_per_thread > 8)))
+        (cfg.blocks_per_thread != 0 && (!is_pow2(cfg.blocks_per_thread) || cfg.blocks_per_thread > 8)) ||
+        cfg.cluster_ctas != 0)
         return DRADD_ERR_BAD_CONFIG;
     out->serialize = cfg.serialize != 0;
     int64_t max_p = 0;
@@ -719,7 +838,8 @@ dradd_status elementwise_plan(int64_t n_rows, int64_t n_cols, const dradd_launch
     if (cfg_in)
         cfg = *cfg_in;
     if (cfg.variant != DRADD_VARIANT_AUTO || cfg.rows_per_cta != 0 || cfg.stages != 0 || cfg.fault_inject != 0 ||
-        cfg.wait_limit_us != 0 || cfg.grid_ctas < 0 || (cfg.serialize != 0 && cfg.serialize != 1))
+        cfg.wait_limit_us != 0 || cfg.grid_ctas < 0 || (cfg.serialize != 0 && cfg.serialize != 1) ||
+        cfg.cluster_ctas != 0)
         return DRADD_ERR_BAD_CONFIG;
     const int T = cfg.threads_per_row ? cfg.threads_per_row : 128;
     const int V = cfg.blocks_per_thread ? cfg.blocks_per_thread : 8;

@@ -78,6 +78,14 @@ KernelFn staged_fn_norm_bf16(int T, int K);
 KernelFn staged_fn_norm_int8(int T, int K);
 KernelFn staged_fn_norm_e4m3(int T, int K);
 KernelFn staged_fn_norm_e2m1(int T, int K);
+// Split-row kernels (bf16 out): clusters of C CTAs (2 or 4), each CTA a
+// slice of every row of its cluster; grid a multiple of C.
+KernelFn split_fn_add(int T, int K, int C);
+KernelFn split_fn_norm(int T, int K, int C);
+cudaError_t launch_split(const Params& p, int K, int C, bool add, int grid, int threads, size_t dyn_smem,
+                         bool serialize, cudaStream_t stream);
+cudaError_t split_max_clusters(int K, int C, bool add, int threads, size_t dyn_smem, int* clusters);
+size_t split_static_smem(int K);
 // Fused q/k RMSNorm: CTAs [0, q_ctas) take the q rows, the next k_ctas the
 // k rows; kq / kk blocks of 8 per thread on each side.  quant: per-group
 // e4m3 q out (else bf16); add: q has a residual; staged: rows staged

@@ -123,9 +123,10 @@ int staged_index(int T, int K, int out, bool add)
 }
 
 constexpr int kMaxDevices = 64;
-// Per device: bit k of word k / 64 set once staged kernel k has been allowed
-// its full dynamic shared memory (8 x 24 kernels).
-std::atomic<uint64_t> g_smem_attr_done[kMaxDevices][3];
+// Per device: bit k of word k / 64 set once staged kernel k (8 x 24 of them)
+// or split kernel k - 192 (4 x 24) has been allowed its full dynamic shared
+// memory.
+std::atomic<uint64_t> g_smem_attr_done[kMaxDevices][5];
 std::atomic<unsigned*> g_status_ptr[kMaxDevices];
 
 cudaError_t ensure_smem_attr(KernelFn fn, int index, int dev)
@@ -201,6 +202,74 @@ cudaError_t launch_staged(const Params& p, int K, int out, bool add, int grid, i
     return launch(fn, grid, threads, dyn_smem, serialize, stream, p);
 }
 
+namespace {
+
+KernelFn split_fn(int T, int K, int C, bool add)
+{
+    return add ? split_fn_add(T, K, C) : split_fn_norm(T, K, C);
+}
+
+int split_index(int T, int K, int C, bool add)
+{
+    return 192 + ((add ? 2 : 0) + (C == 4 ? 1 : 0)) * 24 + (log2i(T) - 5) * 4 + log2i(K);
+}
+
+cudaLaunchConfig_t split_config(int grid, int threads, size_t dyn_smem, bool serialize, cudaStream_t stream,
+                                int C, cudaLaunchAttribute (&attr)[2])
+{
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = dyn_smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = serialize ? 1 : 2;
+    return cfg;
+}
+
+}  // namespace
+
+cudaError_t launch_split(const Params& p, int K, int C, bool add, int grid, int threads, size_t dyn_smem,
+                         bool serialize, cudaStream_t stream)
+{
+    KernelFn fn = split_fn(threads, K, C, add);
+    if (!fn || grid % C != 0)
+        return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    e = ensure_smem_attr(fn, split_index(threads, K, C, add), dev);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = split_config(grid, threads, dyn_smem, serialize, stream, C, attr);
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+cudaError_t split_max_clusters(int K, int C, bool add, int threads, size_t dyn_smem, int* clusters)
+{
+    KernelFn fn = split_fn(threads, K, C, add);
+    if (!fn)
+        return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    e = ensure_smem_attr(fn, split_index(threads, K, C, add), dev);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = split_config(C, threads, dyn_smem, true, 0, C, attr);
+    return cudaOccupancyMaxActiveClusters(clusters, fn, &cfg);
+}
+
 cudaError_t staged_occupancy(int K, int out, bool add, int threads, size_t dyn_smem, int* blocks_per_sm)
 {
     KernelFn fn = staged_fn(threads, K, out, add);
@@ -214,6 +283,12 @@ cudaError_t staged_occupancy(int K, int out, bool add, int threads, size_t dyn_s
     if (e != cudaSuccess)
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, threads, dyn_smem);
+}
+
+size_t split_static_smem(int K)
+{
+    // s_sum[2][32 * K] + s_max[2][32] + s_part[2][2], as declared in split_kernel
+    return sizeof(float) * (2 * 32 * static_cast<size_t>(K) + 2 * 32 + 4);
 }
 
 size_t staged_static_smem(int K)

@@ -165,8 +165,18 @@ dradd_status add_rmsnorm_quant_fwd(int8_t* out_q, float* scale, dradd_bf16* resi
  *                    threads_per_row given it must agree (K = P / 8 / T);
  *                    alone it sets T = P / 8 / K (the automatic stage count
  *                    is then 2).
+ *   cluster_ctas     DRADD_VARIANT_SPLIT only (2 or 4, 0 = 2): each row is
+ *                    shared by a thread-block cluster of this many CTAs,
+ *                    CTA r of the cluster staging and reducing the r-th of
+ *                    that many equal slices of the padded row (P / C
+ *                    elements, threads_per_row T and K blocks per thread
+ *                    within the slice, T * K * 8 * C == P, T >= 32); the
+ *                    slice sums meet through distributed shared memory and
+ *                    are added in the same tree order.  bf16 output only
+ *                    (the quantised entry points reject it); grid_ctas a
+ *                    multiple of C.
  */
-enum { DRADD_VARIANT_AUTO = 0, DRADD_VARIANT_ROWS = 1, DRADD_VARIANT_STAGED = 2 };
+enum { DRADD_VARIANT_AUTO = 0, DRADD_VARIANT_ROWS = 1, DRADD_VARIANT_STAGED = 2, DRADD_VARIANT_SPLIT = 3 };
 
 typedef struct dradd_launch_cfg {
     int variant;
@@ -178,6 +188,7 @@ typedef struct dradd_launch_cfg {
     int wait_limit_us;
     int serialize;
     int blocks_per_thread;
+    int cluster_ctas;
 } dradd_launch_cfg;
 
 dradd_status add_rmsnorm_fwd_with_config(dradd_bf16* out, dradd_bf16* residual_out,

@@ -144,7 +144,7 @@ def test_auto_grid(L):
 
 
 @pytest.mark.parametrize("cfg", [
-    dict(variant=3),
+    dict(variant=4),
     dict(threads_per_row=384),              # not a power of two
     dict(threads_per_row=2048),
     dict(threads_per_row=64),               # K = 16 for P = 8192
@@ -252,4 +252,26 @@ def test_blocks_per_thread_sets_or_checks_threads():
                 dr.LaunchConfig(blocks_per_thread=16)):
         with pytest.raises(dr.DraddError) as e:
             dr.resolve_config(4096, 4096, sm_count=152, config=bad)
+        assert e.value.status == 9
+
+
+def test_split_variant_rules():
+    split = dict(variant=dr.VARIANT_SPLIT)
+    c = dr.resolve_config(1024, 8192, sm_count=152, config=dr.LaunchConfig(**split))
+    assert (c.cluster_ctas, c.threads_per_row, c.blocks_per_thread, c.stages) == (2, 128, 4, 2)
+    assert c.grid_ctas % 2 == 0 and c.grid_ctas <= 2 * 1024
+    c = dr.resolve_config(3, 8192, sm_count=152, config=dr.LaunchConfig(**split, cluster_ctas=4))
+    assert c.grid_ctas == 12 and c.threads_per_row * c.blocks_per_thread * 8 * 4 == 8192
+    for bad in (dict(cluster_ctas=3), dict(cluster_ctas=8), dict(grid_ctas=3), dict(rows_per_cta=2),
+                dict(threads_per_row=16), dict(threads_per_row=2048), dict(stages=9)):
+        with pytest.raises(dr.DraddError) as e:
+            dr.resolve_config(1024, 8192, sm_count=152, config=dr.LaunchConfig(**split, **bad))
+        assert e.value.status == 9
+    # slices narrower than 256 elements, quantised outputs, a cluster size
+    # on another variant
+    for h, q, cfg in ((256, False, dr.LaunchConfig(**split)), (512, False, dr.LaunchConfig(**split, cluster_ctas=4)),
+                      (4096, True, dr.LaunchConfig(**split)),
+                      (4096, False, dr.LaunchConfig(variant=dr.VARIANT_STAGED, cluster_ctas=2))):
+        with pytest.raises(dr.DraddError) as e:
+            dr.resolve_config(64, h, quant=q, sm_count=152, config=cfg)
         assert e.value.status == 9
