@@ -380,7 +380,31 @@ def cpu_baseline(seconds: float, name: str, first_inputs, gpu_set0=None):
         out["parity_bit_exact"] = bool(all(
             np.array_equal(np.ascontiguousarray(g).view(np.uint8), np.ascontiguousarray(e).view(np.uint8))
             for g, e in zip(got, first)))
+        if op == "add_rmsnorm":
+            out["numerics"] = spot_numerics(x0[:chunk], r0[:chunk], w, got[0], got[1])
     return out
+
+
+def spot_numerics(x, r, w, out_bits, ro_bits) -> dict:
+    """On the spot-checked rows: the largest error of out against the fp64
+    evaluation of the page's formula, in bf16 ulps of the exact value, and
+    the mean signed magnitude error of residual_out against the exact fp32
+    sum (the page's bias metric; truncation gives about -1.5e-3 here)."""
+    import numpy as np
+
+    def val(bits):
+        return (np.ascontiguousarray(bits).view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    xf = x.float().numpy().astype(np.float64)
+    rf = r.float().numpy().astype(np.float64)
+    wf = w.float().numpy().astype(np.float64)
+    acc = xf + rf
+    y = acc / np.sqrt((acc * acc).mean(axis=1, keepdims=True) + np.float64(np.float32(inputs.EPS))) * wf
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** -133))) - 7)
+    acc32 = (x.float() + r.float()).numpy().astype(np.float64)
+    nz = acc32 != 0
+    bias = float(((np.abs(val(ro_bits)) - np.abs(acc32))[nz] / np.abs(acc32)[nz]).mean())
+    return {"rows": int(x.shape[0]), "out_max_ulp_vs_f64": round(float((np.abs(val(out_bits) - y) / ulp).max()), 4),
+            "residual_out_magnitude_bias": float(f"{bias:.3e}")}
 
 
 def run_ours(args):

@@ -1264,7 +1264,7 @@ dradd_status dradd_bf16_convert_range(dradd_bf16* out, uint64_t first, int64_t c
         return DRADD_ERR_NULL_PTR;
     if (!aligned(out, 2))
         return DRADD_ERR_MISALIGNED;
-    if (method < 0 || method > 4)
+    if (method < 0 || method > 5)
         return DRADD_ERR_BAD_CONFIG;
     return dradd::launch_convert(out, first, count, method, stream) == cudaSuccess ? DRADD_OK
                                                                                   : DRADD_ERR_CUDA;

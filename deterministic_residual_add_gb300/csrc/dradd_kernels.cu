@@ -6,6 +6,8 @@
 // dradd_qk_<out>_<variant>.cu through qk_fn_<out>_<variant>.
 #include <atomic>
 
+#include <cuda_bf16.h>
+
 #include "dradd_kernels.cuh"
 
 namespace dradd {
@@ -65,6 +67,8 @@ __global__ void convert_kernel(uint16_t* out, uint64_t first, int64_t count, int
             b = e4m3x2(f, f) & 0xFFu;
         else if (method == 4)
             b = e2m1x2(f, f) & 0xFu;
+        else if (method == 5)
+            b = __bfloat16_as_ushort(__float2bfloat16_rn(f));
         else
             b = pack_rne(f, f) & 0xFFFFu;
         out[i] = static_cast<uint16_t>(b);

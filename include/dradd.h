@@ -512,7 +512,8 @@ dradd_status dradd_device_status(cudaStream_t stream, int clear);
  * 0 = the bf16 conversion the kernels use, 1 = integer round-half-even bit
  * arithmetic to bf16, 2 = the hardware cvt.rn.bf16x2.f32 instruction,
  * 3 = the e4m3 conversion the fp8 kernels use (code in the low byte),
- * 4 = the e2m1 conversion the fp4 kernels use (code in the low nibble).
+ * 4 = the e2m1 conversion the fp4 kernels use (code in the low nibble),
+ * 5 = CUDA's own __float2bfloat16_rn (a library reference for method 0).
  * `out` is a device array of `count` 16-bit words (2-byte aligned).
  */
 dradd_status dradd_bf16_convert_range(dradd_bf16* out, uint64_t first, int64_t count,

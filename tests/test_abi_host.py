@@ -104,7 +104,7 @@ def test_convert_hook_argument_errors(L):
     assert L.dradd_bf16_convert_range(None, 0, 16, 0, None) == 1
     assert L.dradd_bf16_convert_range(OUT, 0, -1, 0, None) == 2
     assert L.dradd_bf16_convert_range(OUT + 1, 0, 16, 0, None) == 4
-    assert L.dradd_bf16_convert_range(OUT, 0, 16, 5, None) == 9
+    assert L.dradd_bf16_convert_range(OUT, 0, 16, 6, None) == 9
     assert L.dradd_bf16_convert_range(OUT, 0, 0, 0, None) == 0
 
 
