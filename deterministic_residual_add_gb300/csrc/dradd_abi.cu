@@ -625,10 +625,22 @@ dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t g
         while (blocks / K > B)
             K *= 2;
         int64_t pref = k_pref < blocks ? k_pref : blocks;
-        if (side == q && group_size != 0 && pref > blocks / (group_size / 8))
-            pref = blocks / (group_size / 8);  // a group's lanes stay within one row's threads
+        if (side == q && group_size != 0) {
+            if (pref > blocks / (group_size / 8))
+                pref = blocks / (group_size / 8);  // a group's lanes stay within one row's threads
+            if (!out->staged && pref > group_size / 8)
+                pref = group_size / 8;  // register variant: a thread's blocks stay within one group
+        }
         if (pref > K)
             K = pref;
+        if (!out->staged && side == q && group_size != 0 && K > group_size / 8) {
+            // the register variant cannot place this split; the staged one can
+            if (cfg.variant != DRADD_VARIANT_AUTO)
+                return DRADD_ERR_BAD_CONFIG;
+            dradd_launch_cfg forced = cfg;
+            forced.variant = DRADD_VARIANT_STAGED;
+            return qk_plan(n_q, hq, n_k, hk, group_size, add, sm_count, ctas_per_sm, smem_optin, &forced, out);
+        }
         if (K > 8)
             return DRADD_ERR_BAD_CONFIG;
         side->K = static_cast<int>(K);

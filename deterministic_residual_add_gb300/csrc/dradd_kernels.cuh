@@ -792,13 +792,141 @@ __device__ __forceinline__ void tile_body(const Params& p, int64_t cta, int64_t 
     }
 }
 
+// ----------------------------------------------------------- rows_body_contig
+// The register-load body with the contiguous mapping: thread t of a row owns
+// the K adjacent blocks tK .. tK + K - 1, an aligned subtree of 8K elements
+// of the canonical tree.  The thread folds its K block sums first (fold_k
+// pairs adjacent blocks), then one butterfly over the row's lanes and, past
+// 32 threads, one over its warps: the same tree, so the same bits as the
+// strided mapping.  A lane's 16-byte loads stride K x 16 bytes across the
+// warp; the neighbouring halves of each 32-byte sector arrive with the
+// thread's next block.  For the per-group e4m3 output a group (gb blocks,
+// gb >= K, both powers of two) is held whole by gb / K adjacent lanes, so
+// its max takes log2(gb / K) shuffles and its scale is computed once per
+// thread rather than once per block.  bf16 or per-group e4m3 out.
+template <int K, int OUT, bool ADD>
+__device__ __forceinline__ void rows_body_contig(const Params& p, int64_t cta, int64_t n_ctas)
+{
+    static_assert(OUT == kOutBf16 || OUT == kOutE4m3Group, "bf16 or per-group e4m3 out");
+    __shared__ float s_sum[2][32];
+    const int T = p.threads_per_row;
+    const int tid = threadIdx.x;
+    const int r_local = tid / T;
+    const int t = tid - r_local * T;
+    const int lane = tid & 31;
+    const int warp_in_row = t >> 5;
+    const int warps_per_row = T > 32 ? T >> 5 : 1;
+    const int nblocks = p.hidden >> 3;
+    const int b0 = t * K;
+
+    wait_prior_grids();
+    allow_next_grid();
+    uint4 w[K];
+    {
+        const uint4* wrow = reinterpret_cast<const uint4*>(p.weight);
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+            w[j] = b0 + j < nblocks ? __ldg(wrow + b0 + j) : make_uint4(0u, 0u, 0u, 0u);
+    }
+
+    const int64_t rows_per_step = n_ctas * p.rows_per_cta;
+    int buf = 0;
+    for (int64_t base = cta * p.rows_per_cta; base < p.n_rows; base += rows_per_step) {
+        const int64_t row = base + r_local;
+        const bool active = row < p.n_rows;
+        uint4 xv[K], rv[K];
+        if (active) {
+            const uint4* xrow = reinterpret_cast<const uint4*>(p.x + row * p.hidden);
+            const uint4* rrow = ADD ? reinterpret_cast<const uint4*>(p.residual + row * p.hidden) : nullptr;
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                if (b0 + j < nblocks) {
+                    xv[j] = ld_stream(xrow + b0 + j);
+                    if constexpr (ADD)
+                        rv[j] = ld_stream(rrow + b0 + j);
+                }
+            }
+        }
+        float acc[K][8], part[K];
+        uint4* rorow = ADD ? reinterpret_cast<uint4*>(p.residual_out + row * p.hidden) : nullptr;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            if (active && b0 + j < nblocks) {
+                if constexpr (ADD) {
+                    add8(xv[j], rv[j], acc[j]);
+                    st_stream(rorow + b0 + j, pack8_rne(acc[j]));
+                } else {
+                    unpack8(xv[j], acc[j]);
+                }
+                part[j] = fold8_squares(acc[j]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    acc[j][e] = 0.0f;
+                part[j] = 0.0f;
+            }
+        }
+        float sum = butterfly_sum(fold_k<K>(part), T < 32 ? T : 32);
+        if (T > 32) {
+            float* red = &s_sum[buf][r_local * warps_per_row];
+            if (lane == 0)
+                red[warp_in_row] = sum;
+            __syncthreads();
+            sum = butterfly_sum(red[lane & (warps_per_row - 1)], warps_per_row);
+        }
+        const float inv = inv_rms(sum, p.hidden, p.inv_hidden, p.eps);
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            if (b0 + j >= nblocks)
+                continue;
+            float wf[8];
+            unpack8(w[j], wf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[j][e] = __fmul_rn(__fmul_rn(acc[j][e], inv), wf[e]);
+        }
+        if constexpr (OUT == kOutBf16) {
+            if (active) {
+                uint4* orow = reinterpret_cast<uint4*>(p.out + row * p.hidden);
+#pragma unroll
+                for (int j = 0; j < K; ++j)
+                    if (b0 + j < nblocks)
+                        st_stream(orow + b0 + j, pack8_rne(acc[j]));
+            }
+        } else {
+            const int lanes = p.group_blocks / K;  // lanes per group, a power of two >= 1
+            float m = 0.0f;
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    m = fmaxf(m, fabsf(acc[j][e]));
+            }
+            m = butterfly_max(m, lanes);
+            const float scale = div448_rn(m);
+            if (active && b0 < nblocks) {
+                const int64_t groups = nblocks >> p.group_shift;
+                if ((t & (lanes - 1)) == 0)
+                    p.scale[row * groups + (b0 >> p.group_shift)] = scale;
+                const E4m3Scale qs = make_e4m3_scale(scale);
+                uint2* qrow = reinterpret_cast<uint2*>(p.out_q + row * p.hidden);
+#pragma unroll
+                for (int j = 0; j < K; ++j)
+                    if (b0 + j < nblocks)
+                        st_stream(qrow + b0 + j, quantize8_e4m3(acc[j], qs));
+            }
+        }
+        buf ^= 1;
+    }
+}
+
 // ------------------------------------------------------------------ qk_kernel
 // Fused q/k RMSNorm in one launch: CTAs [0, q_ctas) run the q rows (residual
 // add with QADD; per-group e4m3 out with QQUANT, else bf16), the rest the k
 // rows (plain, bf16).  Both sides use the CTA's threads, each with its own
 // threads per row, rows per CTA and blocks per thread; STAGED selects
 // tile_body (bulk copies into shared memory, `stages` groups ahead) over
-// rows_body (loads straight into registers).
+// rows_body_contig (loads straight into registers, contiguous mapping).
 template <int KQ, int KK, bool QQUANT, bool QADD, bool STAGED>
 __global__ void __launch_bounds__(qk_max_threads(KQ > KK ? KQ : KK))
     qk_kernel(const Params pq, const Params pk, int q_ctas)
@@ -814,9 +942,9 @@ __global__ void __launch_bounds__(qk_max_threads(KQ > KK ? KQ : KK))
             tile_body<KK, kOutBf16, false>(pk, cta - q_ctas, k_ctas, stage_mem);
     } else {
         if (cta < q_ctas)
-            rows_body<KQ, QOUT, QADD>(pq, cta, q_ctas);
+            rows_body_contig<KQ, QOUT, QADD>(pq, cta, q_ctas);
         else
-            rows_body<KK, kOutBf16, false>(pk, cta - q_ctas, k_ctas);
+            rows_body_contig<KK, kOutBf16, false>(pk, cta - q_ctas, k_ctas);
     }
 }
 

@@ -94,7 +94,15 @@ def test_launch_configuration_invariance(orc, group, with_res):
     q, r, qw, k, kw = make(7, 123, 1536, 77, 512, with_res)
     exp = orc.qk_rmsnorm_fwd(q, qw, k, kw, 1e-6, 1e-6, group_size=group, q_residual=r)
     digests = set()
+    ran = 0
     for cfg in CONFIGS:
+        try:
+            dr.qk_resolve_config(123, 1536, 77, 512, group, q_residual=with_res, config=cfg)
+        except dr.DraddError as e:
+            # a register-variant split whose threads would straddle groups
+            assert e.status == 9 and cfg is not None and cfg.variant == 1 and group
+            continue
+        ran += 1
         qo, qs, qro, ko = run_gpu(q, r, qw, k, kw, group, 1e-6, 1e-6, config=cfg)
         parts = [(qo.cpu().numpy() if group else refs.u16(qo)).tobytes(), refs.u16(ko).tobytes()]
         if group:
@@ -103,7 +111,7 @@ def test_launch_configuration_invariance(orc, group, with_res):
             parts.append(refs.u16(qro).tobytes())
         digests.add(hash(b"".join(parts)))
         compare(orc, q, r, qw, k, kw, group, 1e-6, 1e-6, (qo, qs, qro, ko), what=str(cfg))
-    assert len(digests) == 1
+    assert len(digests) == 1 and ran >= 20
     assert exp["k_out"].size > 0
 
 

@@ -82,7 +82,8 @@ def test_with_config_needs_config(L):
 @pytest.mark.parametrize("nq,hq,nk,hk,g", [
     (4096, 1536, 4096, 512, 128), (64 * 32, 128, 64 * 8, 128, 0), (8, 16384, 8, 512, 256),
     (1, 8, 1, 16, 8), (100000, 1536, 0, 512, 64), (0, 1536, 7, 4096, 0), (3, 200, 5, 24, 8),
-    (2048, 8192, 2048, 1024, 32), (50, 256, 3, 64, 256), (7, 128, 7, 128, 128),
+    (2048, 8192, 2048, 1024, 32), (50, 256, 3, 64, 256), (7, 128, 7, 128, 128), (64, 2048, 64, 512, 8),
+    (64, 1536, 64, 512, 16),
 ])
 def test_plan_rules(nq, hq, nk, hk, g):
     p = dr.qk_resolve_config(nq, hq, nk, hk, g, q_residual=True, sm_count=152)
@@ -91,7 +92,9 @@ def test_plan_rules(nq, hq, nk, hk, g):
     if max_p <= 256:
         assert (p.variant, B) == (2, 64)
     elif max_p <= 2048:
-        assert (p.variant, B) == (1, 128)
+        assert B == 128
+        # the register variant, unless its q split would span groups
+        assert p.variant == 1 or (g and (1 << (hq - 1).bit_length()) // 8 // 128 > g // 8)
     else:
         assert p.variant == 2 and B == min(512, max(128, max_p // 8))
     least_k = 4 if max_p <= 256 else 2 if max_p <= 2048 else 1
@@ -109,6 +112,9 @@ def test_plan_rules(nq, hq, nk, hk, g):
         pref = min(least_k, P // 8)
         if side == "q" and g:
             pref = min(pref, P // 8 // (g // 8))
+            if p.variant == 1:
+                pref = min(pref, g // 8)
+                assert max(kmin, pref) <= g // 8  # else the plan takes the staged variant
         assert K == max(kmin, pref)
         assert 1 <= C <= -(-n // R)
     assert p.q_ctas + p.k_ctas <= 152 * 2048 // B
