@@ -281,7 +281,9 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     //   1024   64    2  1                             2
     //   2048   64    4  3                             2
     //   4096   128   4  1 (bf16, >= 24 rows/SM) else 2  3 (bf16), 1 (int8)
+    //          (bf16 residual-add batches of up to 256 rows: T = 256, K = 2)
     //   8192   1024  1  2                             T = 512, K = 2: 3
+    //          (bf16 residual-add batches of 65..512 rows: T = 512, K = 2)
     //   16384  512   4  2                             4
     //   32768  512   8  1                             2
     const bool auto_variant = cfg->variant == DRADD_VARIANT_AUTO;
@@ -315,13 +317,15 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
             T = 64;
             auto_stages = add ? 3 : 2;
         } else if (P == 4096) {
-            T = 128;
+            // small bf16 batches (up to 256 rows): 256 threads, K = 2
+            T = add && !quant && n_rows <= 256 ? 256 : 128;
             if (add)
                 auto_stages = (!quant && n_rows >= 24 * static_cast<int64_t>(L.sm_count)) ? 1 : 2;
             else
                 auto_stages = quant ? 1 : 3;
         } else if (P == 8192) {
-            T = add ? 1024 : 512;
+            // 65..512-row bf16 batches: 512 threads, K = 2
+            T = add && !(quant || n_rows <= 64 || n_rows > 512) ? 512 : (add ? 1024 : 512);
             auto_stages = add ? 2 : 3;
         } else {
             T = 512;
@@ -588,15 +592,17 @@ dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t g
     for (const QkSide* side : {q, k})
         if (side->active && next_pow2(side->hidden) > max_p)
             max_p = next_pow2(side->hidden);
-    // Automatic choice by the longer side's P, measured on GB300 (CUDA-graph
-    // replays over buffers larger than L2, median of interleaved rounds):
-    //   P <= 256           staged, 64 threads, K >= 4 (4 threads a row)
-    //   256 < P <= 2048    rows kernel, 128 threads, K >= 2
-    //   P > 2048           staged, max(128, P / 8) threads up to 512
+    // Automatic choice by the longer side's P (and, for short rows, the row
+    // count), measured on GB300 (CUDA-graph replays over rotating buffers,
+    // median of interleaved rounds):
+    //   P <= 256, more than 4096 rows   staged, 64 threads, K >= 4 (4 threads a row)
+    //   P <= 256, up to 4096 rows       register variant, 128 threads, K >= 2
+    //   256 < P <= 2048                 register variant, 128 threads, K >= 2
+    //   P > 2048                        staged, max(128, P / 8) threads up to 512
     // with 2 stages per side.
     int auto_variant = DRADD_VARIANT_STAGED, auto_k = 1;
     int64_t auto_b = max_p / 8 < 128 ? 128 : (max_p / 8 > 512 ? 512 : max_p / 8);
-    if (max_p <= 256) {
+    if (max_p <= 256 && n_q + n_k > 4096) {
         auto_b = 64;
         auto_k = 4;
     } else if (max_p <= 2048) {

@@ -275,3 +275,13 @@ def test_split_variant_rules():
         with pytest.raises(dr.DraddError) as e:
             dr.resolve_config(64, h, quant=q, sm_count=152, config=cfg)
         assert e.value.status == 9
+
+
+def test_small_batch_choices():
+    """Measured on GB300: small bf16 residual-add batches take wider CTAs."""
+    assert dr.resolve_config(64, 4096, sm_count=152).threads_per_row == 256
+    assert dr.resolve_config(257, 4096, sm_count=152).threads_per_row == 128
+    assert dr.resolve_config(64, 4096, quant=True, sm_count=152).threads_per_row == 128
+    assert dr.resolve_config(256, 8192, sm_count=152).threads_per_row == 512
+    assert dr.resolve_config(64, 8192, sm_count=152).threads_per_row == 1024
+    assert dr.resolve_config(1024, 8192, sm_count=152).threads_per_row == 1024
