@@ -185,10 +185,12 @@ def barrier(world):
 
 
 def max_over_ranks(v: float, world: int) -> float:
+    """The largest of every rank's value (the slowest rank's time)."""
     if world == 1:
         return v
     import torch.distributed as tdist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    device = "cuda" if tdist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
     return float(t.item())
 

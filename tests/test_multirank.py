@@ -62,3 +62,28 @@ def test_two_ranks_match_one(tmp_path, orc):
     out, ro = orc.add_rmsnorm_fwd(c["x"], c["residual"], c["weight"], c["eps"])
     assert np.array_equal(np.load(tmp_path / "out.npy"), out)
     assert np.array_equal(np.load(tmp_path / "ro.npy"), ro)
+
+
+def _bench_rank_main(rank, world, port, result_dir):
+    import sys
+    from pathlib import Path
+    root = Path(__file__).resolve().parents[1]
+    sys.path.insert(0, str(root))
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    tdist.init_process_group("gloo", rank=rank, world_size=world)
+    bench.barrier(world)
+    # each rank reports its own elapsed time; every rank must get the slowest
+    got = bench.max_over_ranks(1.5 + rank * 2.25, world)
+    np.save(os.path.join(result_dir, f"max{rank}.npy"), np.array([got]))
+    bench.barrier(world)
+    tdist.destroy_process_group()
+
+
+def test_bench_reduces_to_the_slowest_rank(tmp_path):
+    """The bench's timing reduction over ranks (gloo stands in for nccl)."""
+    world = 2
+    mp.start_processes(_bench_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world,
+                       join=True, start_method="spawn")
+    for r in range(world):
+        assert float(np.load(tmp_path / f"max{r}.npy")[0]) == 1.5 + (world - 1) * 2.25
