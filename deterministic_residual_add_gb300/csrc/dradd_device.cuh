@@ -61,6 +61,60 @@ __device__ __forceinline__ uint32_t pack_rne(float lo, float hi)
 #endif
 }
 
+// ------------------------------------------------------- packed fp32 pairs
+// Blackwell issues add, sub, mul and fma on two fp32 values per instruction
+// (the .f32x2 forms); each lane is the IEEE operation rounded to nearest
+// with subnormals kept, so the results equal the scalar forms' bit for bit
+// (the parity tests hold every kernel to the oracle).  Half the
+// floating-point instructions of the element-wise steps.  Never feed a
+// packed multiply straight into a packed add: the pair can come out fused
+// (see fold8_squares).
+__device__ __forceinline__ void add2_rn(float a0, float a1, float b0, float b1, float& d0, float& d1)
+{
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void sub2_rn(float a0, float a1, float b0, float b1, float& d0, float& d1)
+{
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void mul2_rn(float a0, float a1, float b0, float b1, float& d0, float& d1)
+{
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void fma2_rn(float a0, float a1, float b0, float b1, float c0, float c1, float& d0,
+                                        float& d1)
+{
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 // 8 consecutive bf16 elements = one 16-byte vector.
 __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8])
 {
@@ -87,21 +141,38 @@ __device__ __forceinline__ void add8(const uint4& xv, const uint4& rv, float (&a
     unpack8(xv, xf);
     unpack8(rv, rf);
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-        acc[e] = __fadd_rn(xf[e], rf[e]);
+    for (int e = 0; e < 8; e += 2)
+        add2_rn(xf[e], xf[e + 1], rf[e], rf[e + 1], acc[e], acc[e + 1]);
 }
 
 // The lowest three levels of the pairwise tree: squares of one aligned
 // 8-element block, summed as ((s0+s1)+(s2+s3)) + ((s4+s5)+(s6+s7)).
 __device__ __forceinline__ float fold8_squares(const float (&a)[8])
 {
+    // The squares stay scalar: a packed multiply whose only use is a packed
+    // add was found fused into one packed fma by the code generator (a
+    // different rounding), which the scalar mul.rn never is.  The first
+    // level adds are packed: (s0 + s1, s2 + s3) and (s4 + s5, s6 + s7).
     float s[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e)
         s[e] = __fmul_rn(a[e], a[e]);
-    const float l0 = __fadd_rn(s[0], s[1]), l1 = __fadd_rn(s[2], s[3]);
-    const float l2 = __fadd_rn(s[4], s[5]), l3 = __fadd_rn(s[6], s[7]);
+    float l0, l1, l2, l3;
+    add2_rn(s[0], s[2], s[1], s[3], l0, l1);
+    add2_rn(s[4], s[6], s[5], s[7], l2, l3);
     return __fadd_rn(__fadd_rn(l0, l1), __fadd_rn(l2, l3));
+}
+
+// y = (acc * inv) * w for one block, the two products rounded in that order.
+__device__ __forceinline__ void scale8(float (&a)[8], float inv, const uint4& w)
+{
+    float wf[8];
+    unpack8(w, wf);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        mul2_rn(a[e], a[e + 1], inv, inv, a[e], a[e + 1]);
+        mul2_rn(a[e], a[e + 1], wf[e], wf[e + 1], a[e], a[e + 1]);
+    }
 }
 
 // Pairwise fold of K partial sums held by one thread (K a power of two,
@@ -221,11 +292,14 @@ __device__ __forceinline__ uint2 quantize8(const float (&y)[8], const QuantScale
     uint32_t bits[8];
     bool near_tie = !s.fast;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const float m = __fmaf_rn(y[e], s.recip, kRound);
-        const float t = __fsub_rn(m, kRound);
-        near_tie |= !(fabsf(__fmaf_rn(y[e], s.recip, -t)) <= 0.5f - 0x1p-15f);
-        bits[e] = __float_as_uint(m);
+    for (int e = 0; e < 8; e += 2) {
+        float m0, m1, nt0, nt1, d0, d1;
+        fma2_rn(y[e], y[e + 1], s.recip, s.recip, kRound, kRound, m0, m1);
+        sub2_rn(kRound, kRound, m0, m1, nt0, nt1);  // -t, exactly
+        fma2_rn(y[e], y[e + 1], s.recip, s.recip, nt0, nt1, d0, d1);
+        near_tie |= !(fabsf(d0) <= 0.5f - 0x1p-15f) || !(fabsf(d1) <= 0.5f - 0x1p-15f);
+        bits[e] = __float_as_uint(m0);
+        bits[e + 1] = __float_as_uint(m1);
     }
     if (near_tie) {
 #pragma unroll
@@ -318,8 +392,11 @@ __device__ __forceinline__ uint2 quantize8_e4m3(const float (&y)[8], const E4m3S
     bool boundary = !s.fast;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        lo[p] = e4m3x2(__fmul_rn(y[2 * p], s.c_lo), __fmul_rn(y[2 * p + 1], s.c_lo));
-        hi[p] = e4m3x2(__fmul_rn(y[2 * p], s.c_hi), __fmul_rn(y[2 * p + 1], s.c_hi));
+        float l0, l1, h0, h1;
+        mul2_rn(y[2 * p], y[2 * p + 1], s.c_lo, s.c_lo, l0, l1);
+        mul2_rn(y[2 * p], y[2 * p + 1], s.c_hi, s.c_hi, h0, h1);
+        lo[p] = e4m3x2(l0, l1);
+        hi[p] = e4m3x2(h0, h1);
         boundary |= lo[p] != hi[p];
     }
     if (boundary) {
@@ -363,8 +440,11 @@ __device__ __forceinline__ uint32_t quantize8_e2m1(const float (&y)[8], const E4
     bool boundary = !s.fast;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        lo[p] = e2m1x2(__fmul_rn(y[2 * p], s.c_lo), __fmul_rn(y[2 * p + 1], s.c_lo));
-        hi[p] = e2m1x2(__fmul_rn(y[2 * p], s.c_hi), __fmul_rn(y[2 * p + 1], s.c_hi));
+        float l0, l1, h0, h1;
+        mul2_rn(y[2 * p], y[2 * p + 1], s.c_lo, s.c_lo, l0, l1);
+        mul2_rn(y[2 * p], y[2 * p + 1], s.c_hi, s.c_hi, h0, h1);
+        lo[p] = e2m1x2(l0, l1);
+        hi[p] = e2m1x2(h0, h1);
         boundary |= lo[p] != hi[p];
     }
     if (boundary) {

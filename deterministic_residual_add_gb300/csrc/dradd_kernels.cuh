@@ -93,11 +93,7 @@ __device__ __forceinline__ void finish_row(const Params& p, float (&acc)[K][8], 
     for (int j = 0; j < K; ++j) {
         if (t + j * T >= nblocks)
             continue;
-        float wf[8];
-        unpack8(w[j], wf);
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            acc[j][e] = __fmul_rn(__fmul_rn(acc[j][e], inv), wf[e]);
+        scale8(acc[j], inv, w[j]);
     }
     if constexpr (OUT == kOutBf16) {
         if (active) {
@@ -879,11 +875,7 @@ __device__ __forceinline__ void rows_body_contig(const Params& p, int64_t cta, i
         for (int j = 0; j < K; ++j) {
             if (b0 + j >= nblocks)
                 continue;
-            float wf[8];
-            unpack8(w[j], wf);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                acc[j][e] = __fmul_rn(__fmul_rn(acc[j][e], inv), wf[e]);
+            scale8(acc[j], inv, w[j]);
         }
         if constexpr (OUT == kOutBf16) {
             if (active) {
