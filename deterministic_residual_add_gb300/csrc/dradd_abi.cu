@@ -595,20 +595,27 @@ dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t g
     // Automatic choice by the longer side's P (and, for short rows, the row
     // count), measured on GB300 (CUDA-graph replays over rotating buffers,
     // median of interleaved rounds):
-    //   P <= 256, more than 4096 rows   staged, 64 threads, K >= 4 (4 threads a row)
-    //   P <= 256, up to 4096 rows       register variant, 128 threads, K >= 2
-    //   256 < P <= 2048                 register variant, 128 threads, K >= 2
-    //   P > 2048                        staged, max(128, P / 8) threads up to 512
+    //   P <= 256, more than 16384 rows    staged, 64 threads, K >= 4 (4 threads a row)
+    //   P <= 256, 4097..16384 rows        register variant, 128 threads, K >= 1
+    //   P <= 256, up to 4096 rows         register variant, 128 threads, K >= 2
+    //   256 < P <= 2048, 8192 rows or more  register variant, 256 threads, K >= 1
+    //   256 < P <= 2048, fewer rows       register variant, 128 threads, K >= 2
+    //   P > 2048                          staged, max(128, P / 8) threads up to 512
     // with 2 stages per side.
     int auto_variant = DRADD_VARIANT_STAGED, auto_k = 1;
     int64_t auto_b = max_p / 8 < 128 ? 128 : (max_p / 8 > 512 ? 512 : max_p / 8);
-    if (max_p <= 256 && n_q + n_k > 4096) {
+    const int64_t rows = n_q + n_k;
+    if (max_p <= 256 && rows > 16384) {
         auto_b = 64;
         auto_k = 4;
-    } else if (max_p <= 2048) {
+    } else if (max_p <= 256) {
         auto_variant = DRADD_VARIANT_ROWS;
         auto_b = 128;
-        auto_k = 2;
+        auto_k = rows > 4096 ? 1 : 2;
+    } else if (max_p <= 2048) {
+        auto_variant = DRADD_VARIANT_ROWS;
+        auto_b = rows >= 8192 ? 256 : 128;
+        auto_k = rows >= 8192 ? 1 : 2;
     }
     // an explicit stage count or the fault hook asks for the staged variant
     if (cfg.variant == DRADD_VARIANT_AUTO && (cfg.stages != 0 || cfg.fault_inject != 0))

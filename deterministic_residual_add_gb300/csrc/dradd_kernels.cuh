@@ -796,7 +796,8 @@ __device__ __forceinline__ void tile_body(const Params& p, int64_t cta, int64_t 
 // 32 threads, one over its warps: the same tree, so the same bits as the
 // strided mapping.  A lane's 16-byte loads stride K x 16 bytes across the
 // warp; the neighbouring halves of each 32-byte sector arrive with the
-// thread's next block.  For the per-group e4m3 output a group (gb blocks,
+// thread's next block.  Each thread loads its blocks of the next row while
+// it computes the current one.  For the per-group e4m3 output a group (gb blocks,
 // gb >= K, both powers of two) is held whole by gb / K adjacent lanes, so
 // its max takes log2(gb / K) shuffles and its scale is computed once per
 // thread rather than once per block.  bf16 or per-group e4m3 out.
@@ -826,23 +827,34 @@ __device__ __forceinline__ void rows_body_contig(const Params& p, int64_t cta, i
     }
 
     const int64_t rows_per_step = n_ctas * p.rows_per_cta;
+    // The next row's vectors are loaded while this row is computed (one
+    // row of prefetch in registers).
+    auto load_row = [&](int64_t row, uint4 (&xv)[K], uint4 (&rv)[K]) {
+        if (row >= p.n_rows)
+            return;
+        const uint4* xrow = reinterpret_cast<const uint4*>(p.x + row * p.hidden);
+        const uint4* rrow = ADD ? reinterpret_cast<const uint4*>(p.residual + row * p.hidden) : nullptr;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            if (b0 + j < nblocks) {
+                xv[j] = ld_stream(xrow + b0 + j);
+                if constexpr (ADD)
+                    rv[j] = ld_stream(rrow + b0 + j);
+            }
+        }
+    };
+    uint4 xv[K], rv[K], nxv[K], nrv[K];
+    load_row(cta * p.rows_per_cta + r_local, nxv, nrv);
     int buf = 0;
     for (int64_t base = cta * p.rows_per_cta; base < p.n_rows; base += rows_per_step) {
         const int64_t row = base + r_local;
         const bool active = row < p.n_rows;
-        uint4 xv[K], rv[K];
-        if (active) {
-            const uint4* xrow = reinterpret_cast<const uint4*>(p.x + row * p.hidden);
-            const uint4* rrow = ADD ? reinterpret_cast<const uint4*>(p.residual + row * p.hidden) : nullptr;
 #pragma unroll
-            for (int j = 0; j < K; ++j) {
-                if (b0 + j < nblocks) {
-                    xv[j] = ld_stream(xrow + b0 + j);
-                    if constexpr (ADD)
-                        rv[j] = ld_stream(rrow + b0 + j);
-                }
-            }
+        for (int j = 0; j < K; ++j) {
+            xv[j] = nxv[j];
+            rv[j] = nrv[j];
         }
+        load_row(row + rows_per_step, nxv, nrv);
         float acc[K][8], part[K];
         uint4* rorow = ADD ? reinterpret_cast<uint4*>(p.residual_out + row * p.hidden) : nullptr;
 #pragma unroll

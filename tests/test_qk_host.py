@@ -83,21 +83,27 @@ def test_with_config_needs_config(L):
     (4096, 1536, 4096, 512, 128), (64 * 32, 128, 64 * 8, 128, 0), (8, 16384, 8, 512, 256),
     (1, 8, 1, 16, 8), (100000, 1536, 0, 512, 64), (0, 1536, 7, 4096, 0), (3, 200, 5, 24, 8),
     (2048, 8192, 2048, 1024, 32), (50, 256, 3, 64, 256), (7, 128, 7, 128, 128), (64, 2048, 64, 512, 8),
-    (64, 1536, 64, 512, 16), (4096 * 32, 128, 4096 * 8, 128, 0),
+    (64, 1536, 64, 512, 16), (4096 * 32, 128, 4096 * 8, 128, 0), (256 * 32, 128, 256 * 8, 128, 0),
 ])
 def test_plan_rules(nq, hq, nk, hk, g):
     p = dr.qk_resolve_config(nq, hq, nk, hk, g, q_residual=True, sm_count=152)
     B = p.threads_per_cta
     max_p = max(1 << (h - 1).bit_length() for n, h in ((nq, hq), (nk, hk)) if n)
-    if max_p <= 256 and nq + nk > 4096:
+    rows = nq + nk
+    if max_p <= 256 and rows > 16384:
         assert (p.variant, B) == (2, 64)
+        least_k = 4
+    elif max_p <= 256:
+        assert (p.variant, B) == (1, 128)
+        least_k = 1 if rows > 4096 else 2
     elif max_p <= 2048:
-        assert B == 128
+        assert B == (256 if rows >= 8192 else 128)
+        least_k = 1 if rows >= 8192 else 2
         # the register variant, unless its q split would span groups
-        assert p.variant == 1 or (g and (1 << (hq - 1).bit_length()) // 8 // 128 > g // 8)
+        assert p.variant == 1 or (g and (1 << (hq - 1).bit_length()) // 8 // B > g // 8)
     else:
         assert p.variant == 2 and B == min(512, max(128, max_p // 8))
-    least_k = 4 if max_p <= 256 and nq + nk > 4096 else 2 if max_p <= 2048 else 1
+        least_k = 1
     for side, n, h, T, R, C in (("q", nq, hq, p.q_threads_per_row, p.q_rows_per_cta, p.q_ctas),
                                 ("k", nk, hk, p.k_threads_per_row, p.k_rows_per_cta, p.k_ctas)):
         if n == 0:
