@@ -27,11 +27,8 @@
 //   rows_kernel    rows are loaded straight into registers with streaming
 //                  16-byte loads; a CTA handles rows_per_cta rows side by side
 //                  and loops over the rows with a grid stride.
-//   qk_kernel      fused q/k RMSNorm: two row sets in one launch, the q side
-//                  optionally with per-group e4m3 out; each side runs either
-//                  the rows_kernel body or tile_body, which stages groups of
-//                  rows_per_cta adjacent rows into shared memory with one
-//                  bulk copy per tensor.
+// The fused q/k kernels (dradd_qk.cuh) and the split-row cluster kernel
+// (dradd_split.cuh) build on the helpers here.
 //   staged_kernel  persistent CTAs stage whole rows of x (and residual) into
 //                  shared memory with 1-D bulk asynchronous copies (TMA
 //                  engine), `stages` rows ahead of the compute; the copy for
@@ -450,528 +447,6 @@ KernelFn staged_table(int T, int K)
     case 256: return staged_by_k<256, OUT, ADD>(K);
     case 512: return staged_by_k<512, OUT, ADD>(K);
     case 1024: return staged_by_k<1024, OUT, ADD>(K);
-    default: return nullptr;
-    }
-}
-
-// --------------------------------------------------------------- split_kernel
-// A cluster of C CTAs shares each row: CTA rank r of the cluster owns the
-// r-th of C equal slices of the padded row (P / C elements, an aligned
-// subtree of the canonical tree), stages its slice of x (and residual) with
-// 1-D bulk copies `stages` rows ahead, and reduces it as staged_kernel
-// reduces a whole row (T threads, K blocks of 8 per thread).  The C slice
-// sums meet through distributed shared memory after a cluster barrier and
-// are folded as the top levels of the tree ((S0 + S1) for C = 2,
-// (S0 + S1) + (S2 + S3) for C = 4), so the bits equal every other variant's.
-// Rows go round-robin over the clusters.  A timed-out wait is made known to
-// the whole cluster at that barrier, and every CTA then drains its copies
-// and leaves after one more cluster barrier: every CTA of a cluster always
-// runs the same number of cluster barriers.  bf16 output.
-template <int T, int K, int C, bool ADD>
-__global__ void __launch_bounds__(T, staged_min_blocks(T, K)) split_kernel(const Params p)
-{
-    static_assert(C == 2 || C == 4, "cluster of 2 or 4 CTAs");
-    extern __shared__ __align__(128) unsigned char stage_mem[];
-    __shared__ float s_sum[2][32 * K];
-    __shared__ float s_max[2][32];
-    __shared__ float s_part[2][2];  // [buffer][slice sum, timeout flag]
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp_in_row = tid >> 5;
-    const uint32_t rank = cluster_ctarank();
-    const int64_t first_row = cluster_id_x();
-    const int64_t n_clusters = cluster_count_x();
-    constexpr int kSliceElems = 8 * T * K;
-    const int slice_off = static_cast<int>(rank) * kSliceElems;
-    int valid = p.hidden - slice_off;
-    valid = valid < 0 ? 0 : (valid > kSliceElems ? kSliceElems : valid);
-    const int nblocks = valid >> 3;
-    const int stages = p.stages;
-    const uint32_t slice_bytes = static_cast<uint32_t>(valid) * 2u;
-    constexpr uint32_t kStageBytes = (ADD ? 2u : 1u) * kSliceElems * 2u;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(stage_mem + static_cast<size_t>(stages) * kStageBytes);
-    // this slice's view of the outputs and the weight
-    Params ps = p;
-    ps.out = p.out + slice_off;
-    ps.weight = p.weight + slice_off;
-    if constexpr (ADD)
-        ps.residual_out = p.residual_out + slice_off;
-
-    if (tid == 0) {
-        for (int s = 0; s < stages; ++s)
-            mbar_init(&bars[s], 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    wait_prior_grids();
-    allow_next_grid();
-
-    const uint64_t policy = l2_policy_evict_first();
-    auto issue = [&](int s, int64_t row) {
-        unsigned char* dst = stage_mem + static_cast<size_t>(s) * kStageBytes;
-        mbar_arrive_expect_tx(&bars[s], (ADD ? 2u : 1u) * slice_bytes);
-        if (slice_bytes) {
-            bulk_copy_g2s(dst, p.x + row * p.hidden + slice_off, slice_bytes, &bars[s], policy);
-            if constexpr (ADD)
-                bulk_copy_g2s(dst + kSliceElems * 2, p.residual + row * p.hidden + slice_off, slice_bytes, &bars[s],
-                              policy);
-        }
-    };
-    if (tid == 0) {
-        for (int s = 0; s < stages; ++s) {
-            const int64_t row = first_row + s * n_clusters;
-            if (row >= p.n_rows)
-                break;
-            if (p.fault_inject && s == 0)
-                continue;  // test hook: this copy never comes, so its wait expires
-            issue(s, row);
-        }
-    }
-
-    uint4 w[K];
-    load_weights<K>(ps, w, tid, T, nblocks);
-
-    int buf = 0;
-    int64_t i = 0;
-    int s = 0;
-    uint32_t parity = 0;
-    for (int64_t row = first_row; row < p.n_rows; row += n_clusters, ++i) {
-        const bool ok = mbar_wait_bounded(&bars[s], parity, p.wait_limit_ns);
-        const unsigned char* sbase = stage_mem + static_cast<size_t>(s) * kStageBytes;
-        const uint4* xs = reinterpret_cast<const uint4*>(sbase);
-        const uint4* rs = reinterpret_cast<const uint4*>(sbase + kSliceElems * 2);
-        uint4 xv[K], rv[K];
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            const int b = tid + j * T;
-            if (b < nblocks) {
-                xv[j] = xs[b];
-                if constexpr (ADD)
-                    rv[j] = rs[b];
-            }
-        }
-        float acc[K][8], part[K];
-        row_accumulate<K, ADD>(ps, xv, rv, acc, part, row, true, tid, T, nblocks);
-
-        float* red = &s_sum[buf][0];
-        lanes_then_publish<K>(part, T, lane, warp_in_row, red);
-        const bool bad = __syncthreads_or(!ok);
-        gather_warps<K>(part, T, lane, red);
-        const float slice_sum = fold_k<K>(part);
-        if (tid == 0) {
-            s_part[buf][0] = slice_sum;
-            s_part[buf][1] = bad ? 1.0f : 0.0f;
-        }
-        cluster_sync_all();
-        float sums[C];
-        float flags = 0.0f;
-#pragma unroll
-        for (int r = 0; r < C; ++r) {
-            sums[r] = ld_cluster_f32(&s_part[buf][0], static_cast<uint32_t>(r));
-            flags = __fadd_rn(flags, ld_cluster_f32(&s_part[buf][1], static_cast<uint32_t>(r)));
-        }
-        if (flags != 0.0f) {
-            // some CTA of the cluster gave up waiting: all of them leave here
-            if (tid == 0) {
-                if (bad)
-                    record_timeout(p);
-                // Copies already issued (rows i .. i + stages - 1; none was
-                // issued for a stage after its wait) must land before shared
-                // memory is released.
-                int s2 = s;
-                uint32_t parity2 = parity;
-                for (int64_t i2 = i; i2 < i + stages; ++i2) {
-                    if (first_row + i2 * n_clusters >= p.n_rows)
-                        break;
-                    if (!(p.fault_inject && i2 == 0))
-                        mbar_wait_bounded(&bars[s2], parity2, p.wait_limit_ns);
-                    if (++s2 == stages) {
-                        s2 = 0;
-                        parity2 ^= 1u;
-                    }
-                }
-            }
-            cluster_sync_all();  // no CTA leaves while another may read its shared memory
-            return;
-        }
-        // every CTA has read stage s and every wait succeeded: refill it
-        if (tid == 0) {
-            const int64_t next = row + static_cast<int64_t>(stages) * n_clusters;
-            if (next < p.n_rows) {
-                fence_proxy_async_smem();
-                issue(s, next);
-            }
-        }
-        float total;
-        if constexpr (C == 2)
-            total = __fadd_rn(sums[0], sums[1]);
-        else
-            total = __fadd_rn(__fadd_rn(sums[0], sums[1]), __fadd_rn(sums[2], sums[3]));
-        const float inv = inv_rms(total, p.hidden, p.inv_hidden, p.eps);
-        finish_row<K, kOutBf16>(ps, acc, w, inv, row, true, tid, T, lane, warp_in_row, nblocks, &s_max[buf][0]);
-        buf ^= 1;
-        if (++s == stages) {
-            s = 0;
-            parity ^= 1u;
-        }
-    }
-    cluster_sync_all();  // the last row's slice sums may still be read by other CTAs
-}
-
-template <int T, int K, int C, bool ADD>
-KernelFn split_pick()
-{
-    if constexpr (T <= max_threads_for(K))
-        return split_kernel<T, K, C, ADD>;
-    else
-        return nullptr;
-}
-
-template <int T, int C, bool ADD>
-KernelFn split_by_k(int K)
-{
-    switch (K) {
-    case 1: return split_pick<T, 1, C, ADD>();
-    case 2: return split_pick<T, 2, C, ADD>();
-    case 4: return split_pick<T, 4, C, ADD>();
-    case 8: return split_pick<T, 8, C, ADD>();
-    default: return nullptr;
-    }
-}
-
-template <int C, bool ADD>
-KernelFn split_table(int T, int K)
-{
-    switch (T) {
-    case 32: return split_by_k<32, C, ADD>(K);
-    case 64: return split_by_k<64, C, ADD>(K);
-    case 128: return split_by_k<128, C, ADD>(K);
-    case 256: return split_by_k<256, C, ADD>(K);
-    case 512: return split_by_k<512, C, ADD>(K);
-    case 1024: return split_by_k<1024, C, ADD>(K);
-    default: return nullptr;
-    }
-}
-
-// ----------------------------------------------------------------- tile_body
-// Staged body for rows of any width: R = rows_per_cta consecutive rows form
-// a group, T = threads_per_row threads per row (T x R = the CTA), K blocks
-// of 8 per thread.  A stage holds one group: its R rows of x (and then its
-// R rows of residual) arrive by one 1-D bulk copy each, since the rows of
-// a group are adjacent in memory; the last group of the tensor may be
-// short, and its copies carry only the rows that exist.  Groups cta,
-// cta + n_ctas, ... are this CTA's; the copy for the group `stages` ahead
-// is issued as soon as every thread has read the current stage.  Waits are
-// bounded as in staged_kernel.
-template <int K, int OUT, bool ADD>
-__device__ __forceinline__ void tile_body(const Params& p, int64_t cta, int64_t n_ctas,
-                                          unsigned char* stage_mem)
-{
-    __shared__ float s_sum[2][32 * K];
-    __shared__ float s_max[2][32];
-    const int T = p.threads_per_row;
-    const int R = p.rows_per_cta;
-    const int tid = threadIdx.x;
-    const int r_local = tid / T;
-    const int t = tid - r_local * T;
-    const int lane = tid & 31;
-    const int warp_in_row = t >> 5;
-    const int warps_per_row = T > 32 ? T >> 5 : 1;
-    const int nblocks = p.hidden >> 3;
-    const int stages = p.stages;
-    const uint32_t row_bytes = static_cast<uint32_t>(p.hidden) * 2u;
-    const uint32_t tile_bytes = row_bytes * static_cast<uint32_t>(R);
-    const uint32_t stage_bytes = (ADD ? 2u : 1u) * tile_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(stage_mem + static_cast<size_t>(stages) * stage_bytes);
-    const int64_t n_groups = (p.n_rows + R - 1) / R;
-
-    if (tid == 0) {
-        for (int s = 0; s < stages; ++s)
-            mbar_init(&bars[s], 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    wait_prior_grids();
-    allow_next_grid();
-
-    const uint64_t policy = l2_policy_evict_first();
-    auto issue = [&](int s, int64_t g) {
-        const int64_t row0 = g * R;
-        const int64_t left = p.n_rows - row0;
-        const uint32_t bytes = row_bytes * static_cast<uint32_t>(left < R ? left : R);
-        unsigned char* dst = stage_mem + static_cast<size_t>(s) * stage_bytes;
-        mbar_arrive_expect_tx(&bars[s], (ADD ? 2u : 1u) * bytes);
-        bulk_copy_g2s(dst, p.x + row0 * p.hidden, bytes, &bars[s], policy);
-        if constexpr (ADD)
-            bulk_copy_g2s(dst + tile_bytes, p.residual + row0 * p.hidden, bytes, &bars[s], policy);
-    };
-    if (tid == 0) {
-        for (int s = 0; s < stages; ++s) {
-            const int64_t g = cta + s * n_ctas;
-            if (g >= n_groups)
-                break;
-            if (p.fault_inject && s == 0)
-                continue;  // test hook: this copy never comes, so its wait expires
-            issue(s, g);
-        }
-    }
-
-    uint4 w[K];
-    load_weights<K>(p, w, t, T, nblocks);
-
-    int buf = 0;
-    int64_t i = 0;
-    int s = 0;
-    uint32_t parity = 0;
-    for (int64_t g = cta; g < n_groups; g += n_ctas, ++i) {
-        const bool ok = mbar_wait_bounded(&bars[s], parity, p.wait_limit_ns);
-        const int64_t row = g * R + r_local;
-        const bool active = row < p.n_rows;
-        const unsigned char* sbase =
-            stage_mem + static_cast<size_t>(s) * stage_bytes + static_cast<size_t>(r_local) * row_bytes;
-        const uint4* xs = reinterpret_cast<const uint4*>(sbase);
-        const uint4* rs = reinterpret_cast<const uint4*>(sbase + tile_bytes);
-        uint4 xv[K], rv[K];
-        if (active) {
-#pragma unroll
-            for (int j = 0; j < K; ++j) {
-                const int b = t + j * T;
-                if (b < nblocks) {
-                    xv[j] = xs[b];
-                    if constexpr (ADD)
-                        rv[j] = rs[b];
-                }
-            }
-        }
-        float acc[K][8], part[K];
-        row_accumulate<K, ADD>(p, xv, rv, acc, part, row, active, t, T, nblocks);
-
-        float* red = &s_sum[buf][r_local * warps_per_row * K];
-        lanes_then_publish<K>(part, T, lane, warp_in_row, red);
-        // Every thread has read stage s and published its warp's partial
-        // sums; any expired wait ends the CTA here.
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) {
-                record_timeout(p);
-                // Copies already issued must land before shared memory is released.
-                int s2 = s;
-                uint32_t parity2 = parity;
-                for (int64_t i2 = i; i2 < i + stages; ++i2) {
-                    if (cta + i2 * n_ctas >= n_groups)
-                        break;
-                    if (!(p.fault_inject && i2 == 0))
-                        mbar_wait_bounded(&bars[s2], parity2, p.wait_limit_ns);
-                    if (++s2 == stages) {
-                        s2 = 0;
-                        parity2 ^= 1u;
-                    }
-                }
-            }
-            return;
-        }
-        if (tid == 0) {
-            const int64_t next = g + static_cast<int64_t>(stages) * n_ctas;
-            if (next < n_groups) {
-                fence_proxy_async_smem();
-                issue(s, next);
-            }
-        }
-        gather_warps<K>(part, T, lane, red);
-        const float inv = inv_rms(fold_k<K>(part), p.hidden, p.inv_hidden, p.eps);
-        finish_row<K, OUT>(p, acc, w, inv, row, active, t, T, lane, warp_in_row, nblocks,
-                             &s_max[buf][r_local * warps_per_row]);
-        buf ^= 1;
-        if (++s == stages) {
-            s = 0;
-            parity ^= 1u;
-        }
-    }
-}
-
-// ----------------------------------------------------------- rows_body_contig
-// The register-load body with the contiguous mapping: thread t of a row owns
-// the K adjacent blocks tK .. tK + K - 1, an aligned subtree of 8K elements
-// of the canonical tree.  The thread folds its K block sums first (fold_k
-// pairs adjacent blocks), then one butterfly over the row's lanes and, past
-// 32 threads, one over its warps: the same tree, so the same bits as the
-// strided mapping.  A lane's 16-byte loads stride K x 16 bytes across the
-// warp; the neighbouring halves of each 32-byte sector arrive with the
-// thread's next block.  Each thread loads its blocks of the next row while
-// it computes the current one.  For the per-group e4m3 output a group (gb blocks,
-// gb >= K, both powers of two) is held whole by gb / K adjacent lanes, so
-// its max takes log2(gb / K) shuffles and its scale is computed once per
-// thread rather than once per block.  bf16 or per-group e4m3 out.
-template <int K, int OUT, bool ADD>
-__device__ __forceinline__ void rows_body_contig(const Params& p, int64_t cta, int64_t n_ctas)
-{
-    static_assert(OUT == kOutBf16 || OUT == kOutE4m3Group, "bf16 or per-group e4m3 out");
-    __shared__ float s_sum[2][32];
-    const int T = p.threads_per_row;
-    const int tid = threadIdx.x;
-    const int r_local = tid / T;
-    const int t = tid - r_local * T;
-    const int lane = tid & 31;
-    const int warp_in_row = t >> 5;
-    const int warps_per_row = T > 32 ? T >> 5 : 1;
-    const int nblocks = p.hidden >> 3;
-    const int b0 = t * K;
-
-    wait_prior_grids();
-    allow_next_grid();
-    uint4 w[K];
-    {
-        const uint4* wrow = reinterpret_cast<const uint4*>(p.weight);
-#pragma unroll
-        for (int j = 0; j < K; ++j)
-            w[j] = b0 + j < nblocks ? __ldg(wrow + b0 + j) : make_uint4(0u, 0u, 0u, 0u);
-    }
-
-    const int64_t rows_per_step = n_ctas * p.rows_per_cta;
-    // The next row's vectors are loaded while this row is computed (one
-    // row of prefetch in registers).
-    auto load_row = [&](int64_t row, uint4 (&xv)[K], uint4 (&rv)[K]) {
-        if (row >= p.n_rows)
-            return;
-        const uint4* xrow = reinterpret_cast<const uint4*>(p.x + row * p.hidden);
-        const uint4* rrow = ADD ? reinterpret_cast<const uint4*>(p.residual + row * p.hidden) : nullptr;
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            if (b0 + j < nblocks) {
-                xv[j] = ld_stream(xrow + b0 + j);
-                if constexpr (ADD)
-                    rv[j] = ld_stream(rrow + b0 + j);
-            }
-        }
-    };
-    uint4 xv[K], rv[K], nxv[K], nrv[K];
-    load_row(cta * p.rows_per_cta + r_local, nxv, nrv);
-    int buf = 0;
-    for (int64_t base = cta * p.rows_per_cta; base < p.n_rows; base += rows_per_step) {
-        const int64_t row = base + r_local;
-        const bool active = row < p.n_rows;
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            xv[j] = nxv[j];
-            rv[j] = nrv[j];
-        }
-        load_row(row + rows_per_step, nxv, nrv);
-        float acc[K][8], part[K];
-        uint4* rorow = ADD ? reinterpret_cast<uint4*>(p.residual_out + row * p.hidden) : nullptr;
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            if (active && b0 + j < nblocks) {
-                if constexpr (ADD) {
-                    add8(xv[j], rv[j], acc[j]);
-                    st_stream(rorow + b0 + j, pack8_rne(acc[j]));
-                } else {
-                    unpack8(xv[j], acc[j]);
-                }
-                part[j] = fold8_squares(acc[j]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    acc[j][e] = 0.0f;
-                part[j] = 0.0f;
-            }
-        }
-        float sum = butterfly_sum(fold_k<K>(part), T < 32 ? T : 32);
-        if (T > 32) {
-            float* red = &s_sum[buf][r_local * warps_per_row];
-            if (lane == 0)
-                red[warp_in_row] = sum;
-            __syncthreads();
-            sum = butterfly_sum(red[lane & (warps_per_row - 1)], warps_per_row);
-        }
-        const float inv = inv_rms(sum, p.hidden, p.inv_hidden, p.eps);
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            if (b0 + j >= nblocks)
-                continue;
-            scale8(acc[j], inv, w[j]);
-        }
-        if constexpr (OUT == kOutBf16) {
-            if (active) {
-                uint4* orow = reinterpret_cast<uint4*>(p.out + row * p.hidden);
-#pragma unroll
-                for (int j = 0; j < K; ++j)
-                    if (b0 + j < nblocks)
-                        st_stream(orow + b0 + j, pack8_rne(acc[j]));
-            }
-        } else {
-            const int lanes = p.group_blocks / K;  // lanes per group, a power of two >= 1
-            float m = 0.0f;
-#pragma unroll
-            for (int j = 0; j < K; ++j) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    m = fmaxf(m, fabsf(acc[j][e]));
-            }
-            m = butterfly_max(m, lanes);
-            const float scale = div448_rn(m);
-            if (active && b0 < nblocks) {
-                const int64_t groups = nblocks >> p.group_shift;
-                if ((t & (lanes - 1)) == 0)
-                    p.scale[row * groups + (b0 >> p.group_shift)] = scale;
-                const E4m3Scale qs = make_e4m3_scale(scale);
-                uint2* qrow = reinterpret_cast<uint2*>(p.out_q + row * p.hidden);
-#pragma unroll
-                for (int j = 0; j < K; ++j)
-                    if (b0 + j < nblocks)
-                        st_stream(qrow + b0 + j, quantize8_e4m3(acc[j], qs));
-            }
-        }
-        buf ^= 1;
-    }
-}
-
-// ------------------------------------------------------------------ qk_kernel
-// Fused q/k RMSNorm in one launch: CTAs [0, q_ctas) run the q rows (residual
-// add with QADD; per-group e4m3 out with QQUANT, else bf16), the rest the k
-// rows (plain, bf16).  Both sides use the CTA's threads, each with its own
-// threads per row, rows per CTA and blocks per thread; STAGED selects
-// tile_body (bulk copies into shared memory, `stages` groups ahead) over
-// rows_body_contig (loads straight into registers, contiguous mapping).
-template <int KQ, int KK, bool QQUANT, bool QADD, bool STAGED>
-__global__ void __launch_bounds__(qk_max_threads(KQ > KK ? KQ : KK))
-    qk_kernel(const Params pq, const Params pk, int q_ctas)
-{
-    extern __shared__ __align__(128) unsigned char stage_mem[];
-    constexpr int QOUT = QQUANT ? kOutE4m3Group : kOutBf16;
-    const int cta = static_cast<int>(blockIdx.x);
-    const int k_ctas = static_cast<int>(gridDim.x) - q_ctas;
-    if constexpr (STAGED) {
-        if (cta < q_ctas)
-            tile_body<KQ, QOUT, QADD>(pq, cta, q_ctas, stage_mem);
-        else
-            tile_body<KK, kOutBf16, false>(pk, cta - q_ctas, k_ctas, stage_mem);
-    } else {
-        if (cta < q_ctas)
-            rows_body_contig<KQ, QOUT, QADD>(pq, cta, q_ctas);
-        else
-            rows_body_contig<KK, kOutBf16, false>(pk, cta - q_ctas, k_ctas);
-    }
-}
-
-template <int KQ, bool QQUANT, bool QADD, bool STAGED>
-QkKernelFn qk_by_kk(int kk)
-{
-    switch (kk) {
-    case 1: return qk_kernel<KQ, 1, QQUANT, QADD, STAGED>;
-    case 2: return qk_kernel<KQ, 2, QQUANT, QADD, STAGED>;
-    case 4: return qk_kernel<KQ, 4, QQUANT, QADD, STAGED>;
-    case 8: return qk_kernel<KQ, 8, QQUANT, QADD, STAGED>;
-    default: return nullptr;
-    }
-}
-
-template <bool QQUANT, bool QADD, bool STAGED>
-QkKernelFn qk_table(int kq, int kk)
-{
-    switch (kq) {
-    case 1: return qk_by_kk<1, QQUANT, QADD, STAGED>(kk);
-    case 2: return qk_by_kk<2, QQUANT, QADD, STAGED>(kk);
-    case 4: return qk_by_kk<4, QQUANT, QADD, STAGED>(kk);
-    case 8: return qk_by_kk<8, QQUANT, QADD, STAGED>(kk);
     default: return nullptr;
     }
 }

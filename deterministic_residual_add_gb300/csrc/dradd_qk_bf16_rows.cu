@@ -1,6 +1,6 @@
 // Fused q/k RMSNorm kernels with bf16 q out, rows loaded into registers: every
 // (KQ, KK) pair, q with and without a residual.
-#include "dradd_kernels.cuh"
+#include "dradd_qk.cuh"
 
 namespace dradd {
 

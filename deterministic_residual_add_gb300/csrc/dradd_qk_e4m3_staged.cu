@@ -1,6 +1,6 @@
 // Fused q/k RMSNorm kernels with per-group e4m3 q out, rows staged through
 // shared memory: every (KQ, KK) pair, q with and without a residual.
-#include "dradd_kernels.cuh"
+#include "dradd_qk.cuh"
 
 namespace dradd {
 

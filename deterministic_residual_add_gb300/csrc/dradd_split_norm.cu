@@ -1,5 +1,5 @@
 // Split-row kernels (a cluster of 2 or 4 CTAs per row), bf16 out, plain RMSNorm.
-#include "dradd_kernels.cuh"
+#include "dradd_split.cuh"
 
 namespace dradd {
 
