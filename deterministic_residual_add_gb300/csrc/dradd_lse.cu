@@ -58,6 +58,40 @@ __device__ __forceinline__ float lse_merge1(float a, float b)
     return __fadd_rn(hi, log1p_unit(expf(__fsub_rn(lo, hi))));
 }
 
+// Two merges at once: the same operations as lse_merge1 for each element,
+// the subtraction, the series and the final addition on packed pairs (each
+// lane the IEEE operation, so each element's bits are lse_merge1's).
+__device__ __forceinline__ void lse_merge2(float a0, float a1, float b0, float b1, float& r0, float& r1)
+{
+    const float hi0 = a0 > b0 ? a0 : b0, lo0 = a0 > b0 ? b0 : a0;
+    const float hi1 = a1 > b1 ? a1 : b1, lo1 = a1 > b1 ? b1 : a1;
+    float d0, d1;
+    sub2_rn(lo0, lo1, hi0, hi1, d0, d1);
+    const float u0 = expf(d0), u1 = expf(d1);
+    float t0, t1;
+    add2_rn(2.0f, 2.0f, u0, u1, t0, t1);
+    const float s0 = __fdiv_rn(u0, t0), s1 = __fdiv_rn(u1, t1);
+    float z0, z1;
+    mul2_rn(s0, s1, s0, s1, z0, z1);
+    float p0 = 0x1.e1e1e2p-5f, p1 = 0x1.e1e1e2p-5f;
+    fma2_rn(p0, p1, z0, z1, 0x1.111112p-4f, 0x1.111112p-4f, p0, p1);
+    fma2_rn(p0, p1, z0, z1, 0x1.3b13b2p-4f, 0x1.3b13b2p-4f, p0, p1);
+    fma2_rn(p0, p1, z0, z1, 0x1.745d18p-4f, 0x1.745d18p-4f, p0, p1);
+    fma2_rn(p0, p1, z0, z1, 0x1.c71c72p-4f, 0x1.c71c72p-4f, p0, p1);
+    fma2_rn(p0, p1, z0, z1, 0x1.24924ap-3f, 0x1.24924ap-3f, p0, p1);
+    fma2_rn(p0, p1, z0, z1, 0x1.99999ap-3f, 0x1.99999ap-3f, p0, p1);
+    fma2_rn(p0, p1, z0, z1, 0x1.555556p-2f, 0x1.555556p-2f, p0, p1);
+    float w0, w1, q0, q1, l0, l1;
+    mul2_rn(2.0f, 2.0f, s0, s1, w0, w1);
+    mul2_rn(w0, w1, z0, z1, q0, q1);
+    fma2_rn(q0, q1, p0, p1, w0, w1, l0, l1);
+    add2_rn(hi0, hi1, l0, l1, r0, r1);
+    if (!(isfinite(a0) && isfinite(b0)))
+        r0 = lse_merge1(a0, b0);
+    if (!(isfinite(a1) && isfinite(b1)))
+        r1 = lse_merge1(a1, b1);
+}
+
 __device__ __forceinline__ float unary1(float x, int op)
 {
     return op == 0 ? log1pf(x) : op == 1 ? coshf(x) : expf(x);
@@ -97,11 +131,21 @@ __global__ void __launch_bounds__(1024) lse_merge_kernel(float* out, int64_t out
                 vb[v] = __ldcs(br + c);
             }
         }
+        if constexpr (VEC == 1) {
+            if (c0 < n_cols)
+                __stcs(orow + c0, lse_merge1(va[0], vb[0]));
+        } else {
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            const int64_t c = c0 + static_cast<int64_t>(v) * blockDim.x;
-            if (c < n_cols)
-                __stcs(orow + c, lse_merge1(va[v], vb[v]));
+            for (int v = 0; v < VEC; v += 2) {
+                const int64_t c = c0 + static_cast<int64_t>(v) * blockDim.x;
+                const int64_t c1 = c + blockDim.x;
+                float r0, r1;
+                lse_merge2(va[v], va[v + 1], vb[v], vb[v + 1], r0, r1);
+                if (c < n_cols)
+                    __stcs(orow + c, r0);
+                if (c1 < n_cols)
+                    __stcs(orow + c1, r1);
+            }
         }
         cb += step_cb;
         if (cb >= units_per_row) {
