@@ -367,6 +367,24 @@ def cpu_baseline(seconds: float, name: str, first_inputs, gpu_set0=None):
            "sample": f"{rows} rows of the {n}x{h} workload ({rows * h} elements) in "
                      f"{dt:.1f} s, single thread",
            "seconds": round(dt, 3)}
+    # The same per-row code with the rows split over every host core (rows
+    # are independent, so the bits are the single-threaded run's).
+    threaded = {"add_rmsnorm": o.add_rmsnorm_fwd, "add_rmsnorm_quant": o.add_rmsnorm_quant_fwd}.get(op)
+    if threaded is not None:
+        cores = oracle.default_threads()
+        tchunk = min(n, chunk * cores)
+        trows = 0
+        t0 = time.perf_counter()
+        while True:
+            lo = trows % n
+            hi = min(n, lo + tchunk)
+            threaded(x0[lo:hi], r0[lo:hi], w, inputs.EPS, threads=cores)
+            trows += hi - lo
+            if time.perf_counter() - t0 >= max(1.0, seconds / 3):
+                break
+        tdt = time.perf_counter() - t0
+        out["all_cores"] = {"value": round(algorithmic_bytes(trows, h, op) / tdt / 1e9, 4), "cores": cores,
+                            "sample": f"{trows} rows in {tdt:.1f} s, rows split over {cores} threads"}
     if gpu_set0 is not None:
         def host(t):
             t = t[:chunk].cpu()
