@@ -933,8 +933,10 @@ dradd_status lse_run(float* out, int64_t out_stride, const float* a, int64_t a_s
     st = elementwise_plan(n_rows, n_cols, cfg, L.sm_count, &threads, &vec, &grid, &serialize);
     if (st != DRADD_OK)
         return st;
-    return dradd::launch_lse_merge(out, out_stride, a, a_stride, b, b_stride, n_rows, n_cols, vec, grid, threads,
-                                   serialize, stream) == cudaSuccess
+    const bool vec4 = aligned(out, 16) && aligned(a, 16) && aligned(b, 16) &&
+                      (n_rows == 1 || (out_stride % 4 == 0 && a_stride % 4 == 0 && b_stride % 4 == 0));
+    return dradd::launch_lse_merge(out, out_stride, a, a_stride, b, b_stride, n_rows, n_cols, vec, vec4, grid,
+                                   threads, serialize, stream) == cudaSuccess
                ? DRADD_OK
                : DRADD_ERR_CUDA;
 }
@@ -968,7 +970,8 @@ dradd_status unary_run(float* out, const float* x, int64_t n, int op, cudaStream
     st = elementwise_plan(1, n, cfg, L.sm_count, &threads, &vec, &grid, &serialize);
     if (st != DRADD_OK)
         return st;
-    return dradd::launch_unary(out, x, n, op, vec, grid, threads, serialize, stream) == cudaSuccess
+    const bool vec4 = aligned(out, 16) && aligned(x, 16);
+    return dradd::launch_unary(out, x, n, op, vec, vec4, grid, threads, serialize, stream) == cudaSuccess
                ? DRADD_OK
                : DRADD_ERR_CUDA;
 }

@@ -129,11 +129,13 @@ inline cudaError_t launch(void (*fn)(Args...), int grid, int threads, size_t dyn
 
 // Log-sum-exp merge and launch-invariant elementwise functions
 // (dradd_lse.cu).  Rows of n_cols elements, row strides in elements; a flat
-// array is one row.  vec: elements per thread per pass (1, 2, 4, 8).
+// array is one row.  vec: elements per thread per pass (1, 2, 4, 8); vec4:
+// every base address is 16-byte aligned and every row stride a multiple of
+// 4 elements (whole units then move as 16-byte vectors).
 cudaError_t launch_lse_merge(float* out, int64_t out_stride, const float* a, int64_t a_stride, const float* b,
-                             int64_t b_stride, int64_t n_rows, int64_t n_cols, int vec, int grid, int threads,
-                             bool serialize, cudaStream_t stream);
-cudaError_t launch_unary(float* out, const float* x, int64_t n, int op, int vec, int grid, int threads,
+                             int64_t b_stride, int64_t n_rows, int64_t n_cols, int vec, bool vec4, int grid,
+                             int threads, bool serialize, cudaStream_t stream);
+cudaError_t launch_unary(float* out, const float* x, int64_t n, int op, int vec, bool vec4, int grid, int threads,
                          bool serialize, cudaStream_t stream);
 
 }  // namespace dradd

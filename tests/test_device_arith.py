@@ -5,9 +5,9 @@ IEEE fp32 operations (the same operations the kernels issue):
   one multiplication and two fused multiply-adds (a division with one
   correction step); tests/div448_check.c compares it with the correctly
   rounded quotient for every fp32 amax in [2^-100, 2^128);
-- the LSE merge's log1p(u) on [0, 1] by the atanh series;
-  tests/log1p_series_check.c compares it with log1p in double for every
-  fp32 u in [0, 1]."""
+- the LSE merge's log1p(u) on [0, 1] by the atanh series after a division
+  with one correction step; tests/log1p_series_check.c compares it with
+  log1p in double for every fp32 u in [0, 1]."""
 import os
 import subprocess
 from concurrent.futures import ThreadPoolExecutor
@@ -40,8 +40,9 @@ def test_div448_correction_step_is_correctly_rounded(tmp_path):
 
 def test_log1p_series_on_unit_interval(tmp_path):
     """The LSE merge's log1p(u), u in [0, 1] (tests/log1p_series_check.c runs
-    the kernel's fp32 operations): every fp32 u within 3 x 2^-24 relative
-    (plus 2^-148 absolute for subnormal u) of log1p in double."""
+    the kernel's fp32 operations, with every quotient its reciprocal-based
+    division can give): every fp32 u within 3 x 2^-24 relative (plus 2^-146
+    absolute where the quotient is subnormal) of log1p in double."""
     exe = tmp_path / "log1p_series_check"
     subprocess.run([oracle._compiler(), "-O2", "-std=c11", "-ffp-contract=off", "-o", str(exe),
                     str(HERE / "log1p_series_check.c"), "-lm"], check=True)

@@ -95,6 +95,58 @@ def test_merge_launch_invariance(lo):
     check_merge(np.frombuffer(digests.pop(), np.float32), a, b, lo)
 
 
+def test_merge_every_difference(lo):
+    """merge(0, d) for every fp32 d in [-104, 0] (below -104, e^d is under
+    2^-150 and the correction is 0): the exp, the division and the series on
+    every argument they can meet with the larger operand 0, where the final
+    addition is exact.  The bound there is 2^-22 absolute: the series'
+    2.95 x 2^-24 relative of a value below ln 2, plus the exp's error
+    (at most 2 + floor(1.173 |d|) ulp of u = e^d) scaled by 1 / (1 + u)."""
+    from concurrent.futures import ThreadPoolExecutor
+    first, last = 0x80000000, 0xC2D00000
+    chunk = 1 << 26
+    d = dev()
+    worst = 0.0
+    with ThreadPoolExecutor(8) as ex:
+        for c0 in range(first, last + 1, chunk):
+            c1 = min(last + 1, c0 + chunk)
+            bits = np.arange(c0, c1, dtype=np.uint64).astype(np.uint32)
+            x = bits.view(np.float32)
+            zeros = np.zeros_like(x)
+            got = dr.lse_merge_fwd(torch.zeros(x.size, device=d), torch.from_numpy(x).to(d)).cpu().numpy()
+            parts = np.array_split(np.arange(x.size), 8)
+            ref = np.concatenate(list(ex.map(lambda ix: lo.merge(zeros[ix], x[ix]), parts)))
+            err = np.abs(got.astype(np.float64) - ref)
+            bad = np.flatnonzero(err > 2.0 ** -22)
+            assert bad.size == 0, (x[bad[:3]], got[bad[:3]], ref[bad[:3]])
+            worst = max(worst, float(err.max()))
+    assert worst > 0.0
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_merge_alignment_invariance(lo, offset):
+    """Views that start off a 16-byte boundary, or whose row stride is not
+    a multiple of 4 elements, take the element-at-a-time path; the bits
+    equal those of the aligned (16-byte vector) path on the same values."""
+    rows, cols, stride = 33, 3000, 3001 + offset
+    a, b = lse_pairs(rows * cols, 40 + offset)
+    a, b = a.reshape(rows, cols), b.reshape(rows, cols)
+    d = dev()
+    ref = dr.lse_merge_fwd(torch.from_numpy(a).to(d), torch.from_numpy(b).to(d)).cpu().numpy()
+    flat_a = torch.zeros(offset + rows * stride, device=d)
+    flat_b = torch.zeros(offset + rows * stride, device=d)
+    va = flat_a[offset:].view(rows, stride)[:, :cols]
+    vb = flat_b[offset:].view(rows, stride)[:, :cols]
+    va.copy_(torch.from_numpy(a))
+    vb.copy_(torch.from_numpy(b))
+    got = dr.lse_merge_fwd(va, vb).cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    out = torch.zeros(offset + rows * stride, device=d)[offset:].view(rows, stride)[:, :cols]
+    dr.lse_merge_fwd(torch.from_numpy(a).to(d), torch.from_numpy(b).to(d), out=out)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    check_merge(ref, a, b, lo)
+
+
 def test_second_half_in_place(lo):
     """A running [rows x S] lse merged, in place, with a [rows x S/2] step
     lse on the second half of each row; the first half is untouched."""
@@ -153,6 +205,18 @@ def test_unary_bounds_and_invariance(lo, op):
     err_ulp = np.abs(got - ref) / ulp32(np.maximum(np.abs(ref), np.abs(got)))
     worst = int(np.argmax(err_ulp))
     assert err_ulp.max() <= UNARY_BOUND_ULP[op], (op, err_ulp.max(), x[worst], got[worst], ref[worst])
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_unary_alignment_invariance(offset):
+    x = np.random.default_rng(offset).uniform(-0.9, 50, 100003).astype(np.float32)
+    d = dev()
+    ref = dr.invariant_unary_fwd(torch.from_numpy(x).to(d), "log1p").cpu().numpy()
+    buf = torch.zeros(offset + x.size, device=d)
+    view = buf[offset:]
+    view.copy_(torch.from_numpy(x))
+    got = dr.invariant_unary_fwd(view, "log1p").cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
 def test_unary_in_place(lo):
