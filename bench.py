@@ -82,6 +82,11 @@ def algorithmic_bytes(n_rows: int, hidden: int, op: str = "add_rmsnorm") -> int:
             "residual_add": 6 * e}[op])
 
 
+# GB300 HBM3e nominal bandwidth (about 8 TB/s), reported beside the measured
+# copy bandwidth that the roofline fraction uses.
+NOMINAL_HBM_GBS = 8000.0
+
+
 def measured_peaks() -> dict:
     p = ROOT / "MEASURED_PEAKS.json"
     return json.loads(p.read_text()) if p.exists() else {}
@@ -490,6 +495,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(per_launch_gbs, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(per_launch_gbs / peak, 4),
                      "peak_source": f"{peak_src} hbm_gbs",
+                     "frac_of_nominal": round(per_launch_gbs / NOMINAL_HBM_GBS, 4),
                      "traffic": recorded_traffic() if args.workload == "4096x4096" else None,
                      "algorithmic_bytes_per_launch": bytes_step},
         "gpu_launches": args.steps,
@@ -610,6 +616,7 @@ def run_qk(args):
         "tokens_per_s": round(world * w.n_tokens * args.steps / (ms / 1e3), 1),
         "roofline": {"bound": "hbm", "achieved": round(per_launch_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(per_launch_gbs / peak, 4), "peak_source": f"{peak_src} hbm_gbs",
+                     "frac_of_nominal": round(per_launch_gbs / NOMINAL_HBM_GBS, 4),
                      "traffic": None, "algorithmic_bytes_per_launch": bytes_step},
         "gpu_launches": args.steps,
         "e2e": None,
@@ -723,6 +730,7 @@ def run_elem(args):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(per_launch, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(per_launch / peak, 4), "peak_source": f"{peak_src} hbm_gbs", "traffic": None,
+                     "frac_of_nominal": round(per_launch / NOMINAL_HBM_GBS, 4),
                      "algorithmic_bytes_per_launch": bytes_step},
         "gpu_launches": args.steps,
         "e2e": None,
