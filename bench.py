@@ -53,6 +53,8 @@ WORKLOADS = {
     "4096x4096": (4096, 4096, "add_rmsnorm", "chain4096"),
     "2048x4096": (2048, 4096, "add_rmsnorm", "2048x4096"),
     "4096x8192": (4096, 8192, "add_rmsnorm", "4096x8192"),
+    "8192x4096": (8192, 4096, "add_rmsnorm", "8192x4096"),
+    "16384x4096": (16384, 4096, "add_rmsnorm", "16384x4096"),
     "2048x16384": (2048, 16384, "add_rmsnorm", "quant2048x16384"),
     "quant2048x16384": (2048, 16384, "add_rmsnorm_quant", "quant2048x16384"),
     "quant4096x4096": (4096, 4096, "add_rmsnorm_quant", "chain4096"),

@@ -89,6 +89,9 @@ class Workload:
 WORKLOADS = {
     "tiny": Workload("tiny", 64, 1024, 1.0, 1.0, seed=0),
     "2048x4096": Workload("2048x4096", 2048, 4096, 1.0, 4.0, seed=1),
+    # the same distributions and seed over more rows (the launch-boundary fit)
+    "8192x4096": Workload("8192x4096", 8192, 4096, 1.0, 4.0, seed=1),
+    "16384x4096": Workload("16384x4096", 16384, 4096, 1.0, 4.0, seed=1),
     "4096x8192": Workload("4096x8192", 4096, 8192, 1.0, 4.0, seed=2),
     "quant2048x16384": Workload("quant2048x16384", 2048, 16384, 1.0, 4.0, seed=4, quant=True),
 }

@@ -13,7 +13,7 @@ from gpu_util import THREADS, assert_bits_equal, gpu_fwd, gpu_quant, max_ulp_vs_
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name", ["tiny", "2048x4096", "4096x8192"])
+@pytest.mark.parametrize("name", ["tiny", "2048x4096", "4096x8192", "16384x4096"])
 def test_bf16_workloads_bit_exact(orc, name):
     c = inputs.WORKLOADS[name].make()
     out, ro = gpu_fwd(c["x"], c["residual"], c["weight"], c["eps"])
