@@ -273,14 +273,18 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     const int64_t blocks = P / 8;
 
     // Automatic choice, measured on GB300 (back-to-back launches over buffers
-    // larger than L2, median of interleaved rounds).  Rows of up to 256
+    // larger than L2, median of interleaved rounds, with the staged
+    // kernel's L2 prefetch of its first rows).  Rows of up to 256
     // elements go several to a CTA in registers; longer rows are staged
     // through shared memory, mostly with K = 4 blocks of 8 per thread:
     //   P      T     K  stages (residual-add forms)   stages (plain RMSNorm)
     //   512    32    2  4                             4
-    //   1024   64    2  1                             2
-    //   2048   64    4  3                             2
-    //   4096   128   4  1 (bf16, >= 24 rows/SM) else 2  3 (bf16), 1 (int8)
+    //   1024   64    2  3                             2
+    //   2048   128   2  4 (64 rows per SM or more:    T = 64, K = 4: 2
+    //                      T = 64, K = 4, 3 stages)
+    //   4096   128   4  bf16: 3 below 24 rows per SM,  bf16: 4 from 20 to 63
+    //                   2 below 64, else 1;           rows per SM, else 2;
+    //                   int8: 2 below 64, else 1      int8: 1
     //          (bf16 residual-add batches of up to 256 rows: T = 256, K = 2)
     //   8192   1024  1  2                             T = 512, K = 2: 3
     //          (bf16 residual-add batches of 65..512 rows: T = 512, K = 2)
@@ -298,6 +302,7 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     const bool staged = cfg->variant == DRADD_VARIANT_STAGED;
 
     int auto_stages = 2;
+    const int64_t per_sm = n_rows / (L.sm_count > 0 ? L.sm_count : 1);  // rows per SM
     if (cfg->threads_per_row == 0 && cfg->blocks_per_thread != 0) {
         if (!is_pow2(cfg->blocks_per_thread) || cfg->blocks_per_thread > 8 || blocks % cfg->blocks_per_thread != 0)
             return DRADD_ERR_BAD_CONFIG;
@@ -312,17 +317,22 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
             auto_stages = 4;
         } else if (P == 1024) {
             T = 64;
-            auto_stages = add ? 1 : 2;
-        } else if (P == 2048) {
-            T = 64;
             auto_stages = add ? 3 : 2;
+        } else if (P == 2048) {
+            const bool wide = add && per_sm < 64;
+            T = wide ? 128 : 64;
+            auto_stages = wide ? 4 : (add ? 3 : 2);
         } else if (P == 4096) {
             // small bf16 batches (up to 256 rows): 256 threads, K = 2
             T = add && !quant && n_rows <= 256 ? 256 : 128;
-            if (add)
-                auto_stages = (!quant && n_rows >= 24 * static_cast<int64_t>(L.sm_count)) ? 1 : 2;
+            if (add && !quant)
+                auto_stages = per_sm < 24 ? 3 : (per_sm < 64 ? 2 : 1);
+            else if (add)
+                auto_stages = per_sm < 64 ? 2 : 1;
+            else if (!quant)
+                auto_stages = per_sm < 20 || per_sm >= 64 ? 2 : 4;
             else
-                auto_stages = quant ? 1 : 3;
+                auto_stages = 1;
         } else if (P == 8192) {
             // 65..512-row bf16 batches: 512 threads, K = 2
             T = add && !(quant || n_rows <= 64 || n_rows > 512) ? 512 : (add ? 1024 : 512);

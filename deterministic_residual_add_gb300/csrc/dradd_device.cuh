@@ -548,6 +548,14 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst_smem, const void* src_gm
         : "memory");
 }
 
+// An L2 prefetch of `bytes` bytes at `src` (16-byte aligned, a multiple of
+// 16 bytes).  A hint only: it brings lines into L2 and moves nothing to the
+// SM, so a load issued later still reads what the memory holds then.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------- thread-block clusters
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {

@@ -125,10 +125,14 @@ def test_auto_config_covers_every_supported_hidden(L):
 
 def test_auto_grid(L):
     c = dr.resolve_config(4096, 4096, sm_count=152)
-    assert (c.variant, c.threads_per_row, c.rows_per_cta, c.stages) == (dr.VARIANT_STAGED, 128, 1, 1)
+    assert (c.variant, c.threads_per_row, c.rows_per_cta, c.stages) == (dr.VARIANT_STAGED, 128, 1, 2)
     assert c.grid_ctas % 152 == 0
     c = dr.resolve_config(2048, 4096, sm_count=152)
-    assert (c.threads_per_row, c.stages) == (128, 2)
+    assert (c.threads_per_row, c.stages) == (128, 3)
+    c = dr.resolve_config(16384, 4096, sm_count=152)
+    assert (c.threads_per_row, c.stages) == (128, 1)
+    c = dr.resolve_config(16384, 4096, quant=True, sm_count=152)
+    assert (c.threads_per_row, c.stages) == (128, 1)
     c = dr.resolve_config(4096, 4096, quant=True, sm_count=152)
     assert (c.threads_per_row, c.stages) == (128, 2)
     c = dr.resolve_config(2048, 16384, quant=True, sm_count=152)
@@ -136,9 +140,15 @@ def test_auto_grid(L):
     assert c.grid_ctas % 152 == 0 or c.grid_ctas == 2048
     c = dr.resolve_config(4096, 8192, sm_count=152)
     assert (c.variant, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 1024, 2)
-    for h, T, S in [(264, 32, 4), (512, 32, 4), (1024, 64, 1), (2048, 64, 3)]:
+    for h, T, S in [(264, 32, 4), (512, 32, 4), (1024, 64, 3), (2048, 128, 4)]:
         c = dr.resolve_config(4096, h, sm_count=152)
         assert (c.threads_per_row, c.stages) == (T, S), h
+    c = dr.resolve_config(16384, 2048, sm_count=152)
+    assert (c.threads_per_row, c.stages) == (64, 3)
+    c = dr.resolve_config(4096, 4096, add=False, sm_count=152)
+    assert c.stages == 4
+    c = dr.resolve_config(2048, 4096, add=False, sm_count=152)
+    assert c.stages == 2
     c = dr.resolve_config(3, 64, sm_count=152)
     assert c.threads_per_row == 8 and c.rows_per_cta == 16 and c.grid_ctas == 1
 
