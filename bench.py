@@ -203,24 +203,36 @@ def max_over_ranks(v: float, world: int) -> float:
 
 
 # ---------------------------------------------------------------- workload
-def workload_inputs(name: str):
+def n_sets_for(name: str) -> int:
+    """Buffer sets the timed loop rotates through: the smallest power of two
+    >= N_SETS whose sets together hold at least 512 MiB of the op's
+    algorithmic bytes (about four times the 129 MB L2), at most 64."""
+    n, h, op, _ = WORKLOADS[name]
+    b = algorithmic_bytes(n, h, op)
+    k = N_SETS
+    while k * b < 512 * 2**20 and k < 64:
+        k *= 2
+    return k
+
+
+def workload_inputs(name: str, n_sets: int = N_SETS):
     """(one x per buffer set, residual, weight) as CPU bf16 tensors."""
     n, h, _, recipe = WORKLOADS[name]
     if recipe == "chain4096":
         ch = inputs.CHAIN4096
         r0, w = ch.initial()
-        return [ch.delta(k) for k in range(N_SETS)], r0, w
+        return [ch.delta(k) for k in range(n_sets)], r0, w
     c = inputs.WORKLOADS[recipe].make(n_rows=n)
     xs = [c["x"]] + [inputs.normal_bf16(inputs.generator(1000 + k), (n, h), 0.0, 1.0)
-                     for k in range(1, N_SETS)]
+                     for k in range(1, n_sets)]
     return xs, c["residual"], c["weight"]
 
 
 def make_sets(device, name: str):
-    """N_SETS independent buffer sets; set 0 holds the workload's own first
-    draw (used by the parity spot check)."""
+    """n_sets_for(name) independent buffer sets; set 0 holds the workload's
+    own first draw (used by the parity spot check)."""
     n, h, op, _ = WORKLOADS[name]
-    xs, r0, w = workload_inputs(name)
+    xs, r0, w = workload_inputs(name, n_sets_for(name))
     sets = []
     for x_cpu in xs:
         x = x_cpu.to(device)
@@ -267,7 +279,7 @@ class RawCall:
             raise dr.DraddError(st, self.name)
 
 
-GRAPH_CHUNK = 256  # launches per captured graph (a multiple of N_SETS)
+GRAPH_CHUNK = 256  # launches per captured graph (a multiple of every set count)
 
 
 def time_device(call, steps, warmup, stream, world, use_graph):
@@ -490,7 +502,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": f"{op}_fwd {n_rows}x{hidden} {io}", "n_rows": n_rows, "hidden": hidden,
                    "io_dtype": "bf16",
-                   "l2": f"{N_SETS} rotating buffer sets ({N_SETS * bytes_step // 2**20} MiB) > L2",
+                   "l2": f"{len(sets)} rotating buffer sets ({len(sets) * bytes_step // 2**20} MiB) > L2",
                    "launch": launch,
                    "cuda_graph": bool(args.graph), "parallelism": f"replicas x{world}"},
         "rows_per_s": round(world * n_rows * args.steps / (ms / 1e3), 1),

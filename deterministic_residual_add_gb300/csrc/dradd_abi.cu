@@ -432,7 +432,8 @@ dradd_status run(int out_kind, bool add, dradd_bf16* out, int8_t* out_q, float* 
     if (user_cfg)
         cfg = *user_cfg;
     const bool auto_grid = cfg.grid_ctas == 0;
-    if (!all_device_memory({out, out_q, scale, residual_out, x, residual, weight})) {
+    const bool device_memory = all_device_memory({out, out_q, scale, residual_out, x, residual, weight});
+    if (!device_memory) {
         if (cfg.variant == DRADD_VARIANT_STAGED || cfg.variant == DRADD_VARIANT_SPLIT)
             return DRADD_ERR_BAD_CONFIG;
         cfg.variant = DRADD_VARIANT_ROWS;
@@ -512,6 +513,7 @@ dradd_status run(int out_kind, bool add, dradd_bf16* out, int8_t* out_q, float* 
     p.fault_inject = cfg.fault_inject;
     p.wait_limit_ns = cfg.wait_limit_us > 0 ? static_cast<uint64_t>(cfg.wait_limit_us) * 1000ull
                                             : kDefaultWaitLimitNs;
+    p.l2_prefetch = device_memory ? 1 : 0;
     if (dradd::device_status_ptr(&p.status) != cudaSuccess)
         return DRADD_ERR_CUDA;
     cudaError_t e;
@@ -795,7 +797,9 @@ dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dra
     dradd_launch_cfg eff = {};
     if (cfg)
         eff = *cfg;
-    if (!all_device_memory({q_out, q_scale, q_residual_out, k_out, q, q_residual, q_weight, k, k_weight})) {
+    const bool device_memory =
+        all_device_memory({q_out, q_scale, q_residual_out, k_out, q, q_residual, q_weight, k, k_weight});
+    if (!device_memory) {
         if (eff.variant == DRADD_VARIANT_STAGED || eff.stages != 0 || eff.fault_inject != 0)
             return DRADD_ERR_BAD_CONFIG;
         eff.variant = DRADD_VARIANT_ROWS;
@@ -838,6 +842,7 @@ dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dra
         p.fault_inject = cfg ? cfg->fault_inject : 0;
         p.wait_limit_ns = wait_ns;
         p.status = status;
+        p.l2_prefetch = device_memory ? 1 : 0;
         return p;
     };
     Params pq = params(plan.q, q, q_residual, q_weight, q_eps);
@@ -945,8 +950,9 @@ dradd_status lse_run(float* out, int64_t out_stride, const float* a, int64_t a_s
         return st;
     const bool vec4 = aligned(out, 16) && aligned(a, 16) && aligned(b, 16) &&
                       (n_rows == 1 || (out_stride % 4 == 0 && a_stride % 4 == 0 && b_stride % 4 == 0));
-    return dradd::launch_lse_merge(out, out_stride, a, a_stride, b, b_stride, n_rows, n_cols, vec, vec4, grid,
-                                   threads, serialize, stream) == cudaSuccess
+    const bool dev = all_device_memory({out, a, b});
+    return dradd::launch_lse_merge(out, out_stride, a, a_stride, b, b_stride, n_rows, n_cols, vec, vec4, dev,
+                                   grid, threads, serialize, stream) == cudaSuccess
                ? DRADD_OK
                : DRADD_ERR_CUDA;
 }
@@ -981,7 +987,8 @@ dradd_status unary_run(float* out, const float* x, int64_t n, int op, cudaStream
     if (st != DRADD_OK)
         return st;
     const bool vec4 = aligned(out, 16) && aligned(x, 16);
-    return dradd::launch_unary(out, x, n, op, vec, vec4, grid, threads, serialize, stream) == cudaSuccess
+    const bool dev = all_device_memory({out, x});
+    return dradd::launch_unary(out, x, n, op, vec, vec4, dev, grid, threads, serialize, stream) == cudaSuccess
                ? DRADD_OK
                : DRADD_ERR_CUDA;
 }
@@ -1187,7 +1194,8 @@ dradd_status residual_add_fwd(dradd_bf16* residual_out, const dradd_bf16* x, con
     st = query_limits(&L);
     if (st != DRADD_OK)
         return st;
-    return dradd::launch_residual_add(residual_out, x, residual, elems / 8, L.sm_count, false, stream) ==
+    const bool dev = all_device_memory({residual_out, x, residual});
+    return dradd::launch_residual_add(residual_out, x, residual, elems / 8, L.sm_count, dev, false, stream) ==
                    cudaSuccess
                ? DRADD_OK
                : DRADD_ERR_CUDA;

@@ -28,6 +28,7 @@ struct Params {
     unsigned* status;         // device status word (set on an expired wait)
     int group_blocks;         // per-group e4m3 out: 8-element blocks per group (a power of two)
     int group_shift;          // log2(group_blocks)
+    int l2_prefetch;          // 1: device memory; first rows may be prefetched into L2 before the dependency wait
 };
 
 constexpr unsigned kDeviceStatusTimeout = 1u;
@@ -100,8 +101,11 @@ QkKernelFn qk_fn_e4m3_rows(int kq, int kk, bool add);
 QkKernelFn qk_fn_e4m3_staged(int kq, int kk, bool add);
 // Static shared memory of a qk kernel whose sides have kq / kk blocks per thread.
 size_t qk_static_smem(int kq, int kk);
+// l2_prefetch: all three are device memory (each CTA's first vectors are
+// then prefetched into L2 before the dependency wait).
 cudaError_t launch_residual_add(uint16_t* residual_out, const uint16_t* x, const uint16_t* residual,
-                                int64_t n_vec, int sm_count, bool serialize, cudaStream_t stream);
+                                int64_t n_vec, int sm_count, bool l2_prefetch, bool serialize,
+                                cudaStream_t stream);
 cudaError_t launch_convert(uint16_t* out, uint64_t first, int64_t count, int method, cudaStream_t stream);
 cudaError_t read_device_status(unsigned* status, bool clear, cudaStream_t stream);
 cudaError_t device_status_ptr(unsigned** ptr);
@@ -131,11 +135,13 @@ inline cudaError_t launch(void (*fn)(Args...), int grid, int threads, size_t dyn
 // (dradd_lse.cu).  Rows of n_cols elements, row strides in elements; a flat
 // array is one row.  vec: elements per thread per pass (1, 2, 4, 8); vec4:
 // every base address is 16-byte aligned and every row stride a multiple of
-// 4 elements (whole units then move as 16-byte vectors).
+// 4 elements (whole units then move as 16-byte vectors); l2_prefetch (with
+// vec4): the inputs are device memory, and each CTA's first unit is
+// prefetched into L2 before the dependency wait.
 cudaError_t launch_lse_merge(float* out, int64_t out_stride, const float* a, int64_t a_stride, const float* b,
-                             int64_t b_stride, int64_t n_rows, int64_t n_cols, int vec, bool vec4, int grid,
-                             int threads, bool serialize, cudaStream_t stream);
-cudaError_t launch_unary(float* out, const float* x, int64_t n, int op, int vec, bool vec4, int grid, int threads,
-                         bool serialize, cudaStream_t stream);
+                             int64_t b_stride, int64_t n_rows, int64_t n_cols, int vec, bool vec4,
+                             bool l2_prefetch, int grid, int threads, bool serialize, cudaStream_t stream);
+cudaError_t launch_unary(float* out, const float* x, int64_t n, int op, int vec, bool vec4, bool l2_prefetch,
+                         int grid, int threads, bool serialize, cudaStream_t stream);
 
 }  // namespace dradd

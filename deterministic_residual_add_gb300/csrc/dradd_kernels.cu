@@ -21,15 +21,25 @@ __device__ unsigned int g_device_status;
 // residual_out = bf16_rne(fp32(x) + fp32(residual)) over n_vec 16-byte
 // vectors (8 elements each), four vectors per thread in flight.
 __global__ void __launch_bounds__(256) residual_add_kernel(uint16_t* residual_out, const uint16_t* x,
-                                                           const uint16_t* residual, int64_t n_vec)
+                                                           const uint16_t* residual, int64_t n_vec,
+                                                           int l2_prefetch)
 {
-    wait_prior_grids();
-    allow_next_grid();
     const uint4* xv = reinterpret_cast<const uint4*>(x);
     const uint4* rv = reinterpret_cast<const uint4*>(residual);
     uint4* ov = reinterpret_cast<uint4*>(residual_out);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x;
+    if (l2_prefetch && threadIdx.x == 0 && first < n_vec) {
+        // the CTA's first vectors of x and residual, into L2 while the
+        // previous grid finishes (a hint; the loads come after the wait)
+        const int64_t left = n_vec - first;
+        const uint32_t bytes = 16u * static_cast<uint32_t>(left < blockDim.x ? left : blockDim.x);
+        prefetch_l2(xv + first, bytes);
+        prefetch_l2(rv + first, bytes);
+    }
+    wait_prior_grids();
+    allow_next_grid();
+    int64_t i = first + threadIdx.x;
     for (; i + 3 * stride < n_vec; i += 4 * stride) {
         uint4 a[4], b[4];
 #pragma unroll
@@ -376,7 +386,8 @@ cudaError_t qk_occupancy(int kq, int kk, bool quant, bool add, bool staged, int 
 }
 
 cudaError_t launch_residual_add(uint16_t* residual_out, const uint16_t* x, const uint16_t* residual,
-                                int64_t n_vec, int sm_count, bool serialize, cudaStream_t stream)
+                                int64_t n_vec, int sm_count, bool l2_prefetch, bool serialize,
+                                cudaStream_t stream)
 {
     const int threads = 256;
     int64_t blocks = (n_vec + threads - 1) / threads;
@@ -386,7 +397,7 @@ cudaError_t launch_residual_add(uint16_t* residual_out, const uint16_t* x, const
     if (blocks < 1)
         blocks = 1;
     return launch(residual_add_kernel, static_cast<int>(blocks), threads, 0, serialize, stream, residual_out, x,
-                  residual, n_vec);
+                  residual, n_vec, l2_prefetch ? 1 : 0);
 }
 
 cudaError_t launch_convert(uint16_t* out, uint64_t first, int64_t count, int method, cudaStream_t stream)

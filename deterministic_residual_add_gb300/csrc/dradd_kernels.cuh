@@ -325,7 +325,8 @@ __global__ void __launch_bounds__(T, staged_min_blocks(T, K)) staged_kernel(cons
         // While the previous grid finishes: L2 prefetches of this CTA's
         // first rows.  The copies that consume them are issued after the
         // wait below, and read what the memory holds then.
-        const uint32_t ahead = stage_bytes < kL2PrefetchBytes ? kL2PrefetchBytes / stage_bytes : 1u;
+        const uint32_t ahead =
+            !p.l2_prefetch ? 0u : (stage_bytes < kL2PrefetchBytes ? kL2PrefetchBytes / stage_bytes : 1u);
         for (uint32_t s = 0; s < ahead; ++s) {
             const int64_t row = blockIdx.x + static_cast<int64_t>(s) * stride;
             if (row >= p.n_rows)

@@ -133,12 +133,26 @@ __device__ __forceinline__ float unary1(float x, int op)
 template <int VEC>
 __global__ void __launch_bounds__(1024) lse_merge_kernel(float* out, int64_t out_stride, const float* a,
                                                          int64_t a_stride, const float* b, int64_t b_stride,
-                                                         int64_t n_rows, int64_t n_cols, int vec4)
+                                                         int64_t n_rows, int64_t n_cols, int vec4,
+                                                         int l2_prefetch)
 {
-    wait_prior_grids();
-    allow_next_grid();
     const int64_t span = static_cast<int64_t>(blockDim.x) * VEC;
     const int64_t units_per_row = (n_cols + span - 1) / span;
+    if (l2_prefetch && vec4 && threadIdx.x == 0) {
+        // The CTA's first unit of a and b, into L2 while the previous grid
+        // finishes (a hint; the loads come after the wait).  Whole 16-byte
+        // pieces inside the row only.
+        const int64_t row = blockIdx.x / units_per_row;
+        const int64_t base = (blockIdx.x - row * units_per_row) * span;
+        const int64_t end = base + span < n_cols ? base + span : n_cols;
+        const uint32_t bytes = static_cast<uint32_t>(((end - base) * 4) & ~int64_t{15});
+        if (row < n_rows && bytes > 0) {
+            prefetch_l2(a + row * a_stride + base, bytes);
+            prefetch_l2(b + row * b_stride + base, bytes);
+        }
+    }
+    wait_prior_grids();
+    allow_next_grid();
     // unit u = row * units_per_row + cb, walked with a stride of gridDim.x:
     // (row, cb) advances by (gridDim.x / units_per_row, gridDim.x %
     // units_per_row) with a carry, so the loop divides only once here
@@ -205,11 +219,21 @@ __global__ void __launch_bounds__(1024) lse_merge_kernel(float* out, int64_t out
 // The same unit walk over one flat array (vec4: both base addresses 16-byte
 // aligned).
 template <int VEC>
-__global__ void __launch_bounds__(1024) unary_kernel(float* out, const float* x, int64_t n, int op, int vec4)
+__global__ void __launch_bounds__(1024) unary_kernel(float* out, const float* x, int64_t n, int op, int vec4,
+                                                     int l2_prefetch)
 {
+    const int64_t span = static_cast<int64_t>(blockDim.x) * VEC;
+    if (l2_prefetch && vec4 && threadIdx.x == 0) {
+        const int64_t base = static_cast<int64_t>(blockIdx.x) * span;
+        const int64_t end = base + span < n ? base + span : n;
+        if (base < n) {
+            const uint32_t bytes = static_cast<uint32_t>(((end - base) * 4) & ~int64_t{15});
+            if (bytes > 0)
+                prefetch_l2(x + base, bytes);
+        }
+    }
     wait_prior_grids();
     allow_next_grid();
-    const int64_t span = static_cast<int64_t>(blockDim.x) * VEC;
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * span; base < n;
          base += static_cast<int64_t>(gridDim.x) * span) {
         const float* xr = x + base;
@@ -246,27 +270,27 @@ __global__ void __launch_bounds__(1024) unary_kernel(float* out, const float* x,
 }
 
 cudaError_t launch_lse_merge(float* out, int64_t out_stride, const float* a, int64_t a_stride, const float* b,
-                             int64_t b_stride, int64_t n_rows, int64_t n_cols, int vec, bool vec4, int grid,
-                             int threads, bool serialize, cudaStream_t stream)
+                             int64_t b_stride, int64_t n_rows, int64_t n_cols, int vec, bool vec4,
+                             bool l2_prefetch, int grid, int threads, bool serialize, cudaStream_t stream)
 {
-    void (*fn)(float*, int64_t, const float*, int64_t, const float*, int64_t, int64_t, int64_t, int) =
+    void (*fn)(float*, int64_t, const float*, int64_t, const float*, int64_t, int64_t, int64_t, int, int) =
         vec == 1 ? lse_merge_kernel<1> : vec == 2 ? lse_merge_kernel<2> : vec == 4 ? lse_merge_kernel<4>
         : vec == 8 ? lse_merge_kernel<8> : nullptr;
     if (!fn)
         return cudaErrorInvalidValue;
     return launch(fn, grid, threads, 0, serialize, stream, out, out_stride, a, a_stride, b, b_stride, n_rows,
-                  n_cols, vec4 ? 1 : 0);
+                  n_cols, vec4 ? 1 : 0, l2_prefetch ? 1 : 0);
 }
 
-cudaError_t launch_unary(float* out, const float* x, int64_t n, int op, int vec, bool vec4, int grid, int threads,
-                         bool serialize, cudaStream_t stream)
+cudaError_t launch_unary(float* out, const float* x, int64_t n, int op, int vec, bool vec4, bool l2_prefetch,
+                         int grid, int threads, bool serialize, cudaStream_t stream)
 {
-    void (*fn)(float*, const float*, int64_t, int, int) = vec == 1 ? unary_kernel<1> : vec == 2 ? unary_kernel<2>
+    void (*fn)(float*, const float*, int64_t, int, int, int) = vec == 1 ? unary_kernel<1> : vec == 2 ? unary_kernel<2>
                                                      : vec == 4 ? unary_kernel<4> : vec == 8 ? unary_kernel<8>
                                                                                              : nullptr;
     if (!fn)
         return cudaErrorInvalidValue;
-    return launch(fn, grid, threads, 0, serialize, stream, out, x, n, op, vec4 ? 1 : 0);
+    return launch(fn, grid, threads, 0, serialize, stream, out, x, n, op, vec4 ? 1 : 0, l2_prefetch ? 1 : 0);
 }
 
 }  // namespace dradd

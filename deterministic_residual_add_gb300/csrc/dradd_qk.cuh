@@ -44,6 +44,22 @@ __device__ __forceinline__ void tile_body(const Params& p, int64_t cta, int64_t 
     const int64_t n_groups = (p.n_rows + R - 1) / R;
 
     if (tid == 0) {
+        // While the previous grid finishes: L2 prefetches of this CTA's
+        // first groups (about 16 KiB of input); the copies that consume
+        // them come after the wait and read what the memory holds then.
+        if (p.l2_prefetch) {
+            const uint32_t ahead = stage_bytes < kL2PrefetchBytes ? kL2PrefetchBytes / stage_bytes : 1u;
+            for (uint32_t a = 0; a < ahead; ++a) {
+                const int64_t row0 = (cta + static_cast<int64_t>(a) * n_ctas) * R;
+                if (row0 >= p.n_rows)
+                    break;
+                const int64_t left = p.n_rows - row0;
+                const uint32_t bytes = row_bytes * static_cast<uint32_t>(left < R ? left : R);
+                prefetch_l2(p.x + row0 * p.hidden, bytes);
+                if constexpr (ADD)
+                    prefetch_l2(p.residual + row0 * p.hidden, bytes);
+            }
+        }
         for (int s = 0; s < stages; ++s)
             mbar_init(&bars[s], 1);
         fence_mbar_init();
@@ -174,6 +190,23 @@ __device__ __forceinline__ void rows_body_contig(const Params& p, int64_t cta, i
     const int nblocks = p.hidden >> 3;
     const int b0 = t * K;
 
+    if (p.l2_prefetch && tid == 0) {
+        // The CTA's first rows (about 16 KiB of input; adjacent rows), into
+        // L2 while the previous grid finishes; the loads come after the wait.
+        const uint32_t row_bytes = static_cast<uint32_t>(p.hidden) * 2u;
+        const uint32_t step_bytes = (ADD ? 2u : 1u) * row_bytes * static_cast<uint32_t>(p.rows_per_cta);
+        const uint32_t ahead = step_bytes < kL2PrefetchBytes ? kL2PrefetchBytes / step_bytes : 1u;
+        for (uint32_t a = 0; a < ahead; ++a) {
+            const int64_t row0 = (cta + static_cast<int64_t>(a) * n_ctas) * p.rows_per_cta;
+            if (row0 >= p.n_rows)
+                break;
+            const int64_t left = p.n_rows - row0;
+            const uint32_t bytes = row_bytes * static_cast<uint32_t>(left < p.rows_per_cta ? left : p.rows_per_cta);
+            prefetch_l2(p.x + row0 * p.hidden, bytes);
+            if constexpr (ADD)
+                prefetch_l2(p.residual + row0 * p.hidden, bytes);
+        }
+    }
     wait_prior_grids();
     allow_next_grid();
     uint4 w[K];
