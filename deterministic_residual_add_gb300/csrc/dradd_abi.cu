@@ -561,7 +561,8 @@ dradd_status qk_check_side(int64_t n_rows, int64_t hidden)
 // takes K = the smallest power of two with P / 8 / K <= B, raised to the
 // least K if that is larger (at most P / 8 and 8); then T = P / 8 / K
 // threads per row and R = B / T rows per CTA.  The staged variant gives
-// each side min(2, 96 KiB / stage) stages of R rows (cfg->stages: the same
+// each side min(S, 96 KiB / stage) stages of R rows, S = 3 for short rows
+// in large batches and 2 otherwise (cfg->stages: the same
 // count for both).  CTAs (cfg->grid_ctas):
 // automatic SMs x ctas_per_sm (ctas_per_sm <= 0: 2048 / B); when the two
 // sides need more, they share them in proportion to their elements.
@@ -607,19 +608,21 @@ dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t g
     // Automatic choice by the longer side's P (and, for short rows, the row
     // count), measured on GB300 (CUDA-graph replays over rotating buffers,
     // median of interleaved rounds):
-    //   P <= 256, more than 16384 rows    staged, 64 threads, K >= 4 (4 threads a row)
+    //   P <= 256, more than 16384 rows    staged, 128 threads, K >= 4 (4 threads a row), 3 stages
     //   P <= 256, 4097..16384 rows        register variant, 128 threads, K >= 1
     //   P <= 256, up to 4096 rows         register variant, 128 threads, K >= 2
     //   256 < P <= 2048, 8192 rows or more  register variant, 256 threads, K >= 1
     //   256 < P <= 2048, fewer rows       register variant, 128 threads, K >= 2
     //   P > 2048                          staged, max(128, P / 8) threads up to 512
-    // with 2 stages per side.
-    int auto_variant = DRADD_VARIANT_STAGED, auto_k = 1;
+    // with 2 stages per side unless stated (with the L2 prefetch of each
+    // CTA's first rows before the dependency wait).
+    int auto_variant = DRADD_VARIANT_STAGED, auto_k = 1, auto_stages = 2;
     int64_t auto_b = max_p / 8 < 128 ? 128 : (max_p / 8 > 512 ? 512 : max_p / 8);
     const int64_t rows = n_q + n_k;
     if (max_p <= 256 && rows > 16384) {
-        auto_b = 64;
+        auto_b = 128;
         auto_k = 4;
+        auto_stages = 3;
     } else if (max_p <= 256) {
         auto_variant = DRADD_VARIANT_ROWS;
         auto_b = 128;
@@ -691,8 +694,8 @@ dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t g
             int64_t S = cfg.stages;
             if (S == 0) {
                 S = kQkStageBudget / side->stage_bytes;
-                if (S > 2)
-                    S = 2;
+                if (S > auto_stages)
+                    S = auto_stages;
                 if (S < 1)
                     S = 1;
             }

@@ -90,9 +90,11 @@ def test_plan_rules(nq, hq, nk, hk, g):
     B = p.threads_per_cta
     max_p = max(1 << (h - 1).bit_length() for n, h in ((nq, hq), (nk, hk)) if n)
     rows = nq + nk
+    max_stages = 2
     if max_p <= 256 and rows > 16384:
-        assert (p.variant, B) == (2, 64)
+        assert (p.variant, B) == (2, 128)
         least_k = 4
+        max_stages = 3
     elif max_p <= 256:
         assert (p.variant, B) == (1, 128)
         least_k = 1 if rows > 4096 else 2
@@ -126,15 +128,15 @@ def test_plan_rules(nq, hq, nk, hk, g):
     assert p.q_ctas + p.k_ctas <= 152 * 2048 // B
     if nq and g:
         assert g // 8 <= p.q_threads_per_row
-    # staged: up to 2 stages of R rows per side, within 96 KiB unless one
-    # stage alone is larger
+    # staged: up to 2 stages of R rows per side (3 for short rows in large
+    # batches), within 96 KiB unless one stage alone is larger
     for n, h, R, S, res in ((nq, hq, p.q_rows_per_cta, p.q_stages, True),
                             (nk, hk, p.k_rows_per_cta, p.k_stages, False)):
         if n == 0 or p.variant == 1:
             assert S == 0
             continue
         stage = (4 if res else 2) * h * R
-        assert 1 <= S <= 2 and (S * stage <= 96 * 1024 or S == 1)
+        assert 1 <= S <= max_stages and (S * stage <= 96 * 1024 or S == 1)
         assert p.dyn_smem_bytes >= S * (stage + 8)
 
 
