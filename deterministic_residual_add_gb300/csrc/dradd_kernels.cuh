@@ -291,11 +291,6 @@ __global__ void __launch_bounds__(max_threads_for(K)) rows_kernel(const Params p
     rows_body<K, OUT, ADD>(p, blockIdx.x, gridDim.x);
 }
 
-// -------------------------------------------------------------- staged_kernel
-// T (threads per row = threads per CTA) is a compile-time constant so that
-// every (T, K) pair gets its own register budget (staged_min_blocks) and the
-// reduction widths fold away.  A stage holds one row of x, then (with ADD)
-// one row of residual.
 // Input bytes per CTA prefetched into L2 before the wait for the previous
 // grid (whole rows, at least one): with 4 CTAs per SM about 10 MB per
 // launch, what the previous grid's last rows leave room for.  Measured on
@@ -304,6 +299,11 @@ __global__ void __launch_bounds__(max_threads_for(K)) rows_kernel(const Params p
 // plain RMSNorm with two rows of x; deeper prefetches slowed the calls.
 constexpr uint32_t kL2PrefetchBytes = 16384;
 
+// -------------------------------------------------------------- staged_kernel
+// T (threads per row = threads per CTA) is a compile-time constant so that
+// every (T, K) pair gets its own register budget (staged_min_blocks) and the
+// reduction widths fold away.  A stage holds one row of x, then (with ADD)
+// one row of residual.
 template <int T, int K, int OUT, bool ADD>
 __global__ void __launch_bounds__(T, staged_min_blocks(T, K)) staged_kernel(const Params p)
 {
