@@ -203,6 +203,33 @@ def max_over_ranks(v: float, world: int) -> float:
 
 
 # ---------------------------------------------------------------- workload
+IO_DESC = {"add_rmsnorm": "bf16 in/out", "add_rmsnorm_quant": "bf16 in, int8 + fp32 scale + bf16 residual_out out",
+           "rmsnorm": "bf16 in/out", "rmsnorm_quant": "bf16 in, int8 + fp32 scale out",
+           "residual_add": "bf16 in/out",
+           "add_rmsnorm_fp8": "bf16 in, e4m3 + fp32 scale + bf16 residual_out out",
+           "rmsnorm_fp8": "bf16 in, e4m3 + fp32 scale out",
+           "add_rmsnorm_fp4": "bf16 in, packed e2m1 + fp32 scale + bf16 residual_out out"}
+
+
+def workload_desc(name: str) -> str:
+    """config.workload of a main-op workload (the same on both arms)."""
+    n, h, op, _ = WORKLOADS[name]
+    return f"{op}_fwd {n}x{h} {IO_DESC[op]}"
+
+
+def qk_workload_desc(w) -> str:
+    qdesc = (f"q {w.q_heads}x{w.q_head}" + (" + residual" if w.residual else "") +
+             (f" -> e4m3 groups of {w.group_size}" if w.group_size else " -> bf16"))
+    return f"fused_qk_rmsnorm_group_quant_fwd {w.n_tokens} tokens: {qdesc}; k {w.k_heads}x{w.k_head} -> bf16"
+
+
+def elem_workload_desc(w) -> str:
+    if w.kind == "merge":
+        return (f"lse_merge_2d_fwd: [{w.rows} x {w.cols}] running fp32 lse, last {w.step_cols} columns of each "
+                f"row merged in place with a [{w.rows} x {w.step_cols}] step lse")
+    return f"invariant_unary_fwd log1p of {w.rows * w.cols} fp32 values"
+
+
 def n_sets_for(name: str) -> int:
     """Buffer sets the timed loop rotates through: the smallest power of two
     >= N_SETS whose sets together hold at least 512 MiB of the op's
@@ -489,18 +516,12 @@ def run_ours(args):
         launch = {"variant": "rows" if cfg.variant == 1 else "staged",
                   "threads_per_row": cfg.threads_per_row, "rows_per_cta": cfg.rows_per_cta,
                   "stages": cfg.stages}
-    io = {"add_rmsnorm": "bf16 in/out", "add_rmsnorm_quant": "bf16 in, int8 + fp32 scale + bf16 residual_out out",
-          "rmsnorm": "bf16 in/out", "rmsnorm_quant": "bf16 in, int8 + fp32 scale out",
-          "residual_add": "bf16 in/out",
-          "add_rmsnorm_fp8": "bf16 in, e4m3 + fp32 scale + bf16 residual_out out",
-          "rmsnorm_fp8": "bf16 in, e4m3 + fp32 scale out",
-          "add_rmsnorm_fp4": "bf16 in, packed e2m1 + fp32 scale + bf16 residual_out out"}[op]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"{op}_fwd {n_rows}x{hidden} {io}", "n_rows": n_rows, "hidden": hidden,
+        "config": {"workload": workload_desc(args.workload), "n_rows": n_rows, "hidden": hidden,
                    "io_dtype": "bf16",
                    "l2": f"{len(sets)} rotating buffer sets ({len(sets) * bytes_step // 2**20} MiB) > L2",
                    "launch": launch,
@@ -614,14 +635,11 @@ def run_qk(args):
     sm_count = torch.cuda.get_device_properties(device).multi_processor_count
     plan = dr.qk_resolve_config(nq, w.q_head, nk, w.k_head, w.group_size, q_residual=w.residual,
                                 sm_count=sm_count)
-    qdesc = (f"q {w.q_heads}x{w.q_head}" + (" + residual" if w.residual else "") +
-             (f" -> e4m3 groups of {w.group_size}" if w.group_size else " -> bf16"))
     line = {
         "metric": QK_METRIC, "value": round(world * bytes_step * args.steps / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"fused_qk_rmsnorm_group_quant_fwd {w.n_tokens} tokens: {qdesc}; "
-                               f"k {w.k_heads}x{w.k_head} -> bf16",
+        "config": {"workload": qk_workload_desc(w),
                    "n_q_rows": nq, "q_hidden": w.q_head, "n_k_rows": nk, "k_hidden": w.k_head,
                    "group_size": w.group_size, "io_dtype": "bf16",
                    "l2": f"{n_sets} rotating buffer sets ({n_sets * bytes_step // 2**20} MiB) > L2",
@@ -730,9 +748,7 @@ def run_elem(args):
     peak_src = "measured" if peak else "fallback"
     if not peak:
         peak = 6800.0
-    desc = (f"lse_merge_2d_fwd: [{w.rows} x {w.cols}] running fp32 lse, last {w.step_cols} columns of each row "
-            f"merged in place with a [{w.rows} x {w.step_cols}] step lse" if w.kind == "merge"
-            else f"invariant_unary_fwd log1p of {w.rows * w.cols} fp32 values")
+    desc = elem_workload_desc(w)
     line = {
         "metric": ELEM_METRIC, "value": round(world * bytes_step * args.steps / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
@@ -837,7 +853,7 @@ def run_elem_reference(args):
         "impl": "reference", "metric": ELEM_METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload} (CPU oracle)", "sample": sample},
+        "config": {"workload": elem_workload_desc(w), "engine": "CPU oracle", "sample": sample},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{sample}, single thread"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -869,8 +885,7 @@ def run_qk_reference(args):
         "impl": "reference", "metric": QK_METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"fused_qk_rmsnorm_group_quant_fwd {args.workload} (CPU oracle)",
-                   "tokens_per_step": tokens},
+        "config": {"workload": qk_workload_desc(w), "engine": "CPU oracle", "tokens_per_step": tokens},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{tokens} of {w.n_tokens} tokens per step, single thread"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -914,7 +929,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"{op}_fwd {n}x{h} (CPU oracle)", "n_rows": n, "hidden": h,
+        "config": {"workload": workload_desc(args.workload), "engine": "CPU oracle", "n_rows": n, "hidden": h,
                    "io_dtype": "bf16", "rows_per_step": rows},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{rows} of {n} rows per step, single thread"},
