@@ -159,8 +159,12 @@ dradd_status add_rmsnorm_quant_fwd(int8_t* out_q, float* scale, dradd_bf16* resi
  *   serialize        0: launch with programmatic stream serialization, so the
  *                    kernel's CTAs may be scheduled while the previous kernel
  *                    in the stream drains; they wait for it to complete (and
- *                    its writes to be visible) before any global memory
- *                    access.  1: plain launch.
+ *                    its writes to be visible) before any global load or
+ *                    store.  Before that wait, with every buffer in device
+ *                    memory, a CTA may only prefetch its first input rows
+ *                    into L2 (a hint that moves no data to the SM, so the
+ *                    loads after the wait read what memory then holds).
+ *                    1: plain launch.
  *   blocks_per_thread K (1, 2, 4 or 8): 8-element blocks per thread.  With
  *                    threads_per_row given it must agree (K = P / 8 / T);
  *                    alone it sets T = P / 8 / K (the automatic stage count
