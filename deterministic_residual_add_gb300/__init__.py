@@ -153,6 +153,7 @@ def lib() -> ctypes.CDLL:
                        ("invariant_unary_fwd", [_vp, _vp, _i64, ctypes.c_int, _vp]),
                        ("invariant_unary_fwd_with_config", [_vp, _vp, _i64, ctypes.c_int, _vp, cfgp]),
                        ("dradd_device_status", [_vp, ctypes.c_int]),
+                       ("dradd_last_device_status", [_vp]),
                        ("dradd_bf16_convert_range", [_vp, ctypes.c_uint64, _i64, ctypes.c_int, _vp])]:
         f = getattr(L, name)
         f.argtypes = args
@@ -600,6 +601,15 @@ def device_status(stream=None, clear: bool = True, device=None) -> int:
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     with torch.cuda.device(device):
         return int(lib().dradd_device_status(_stream_handle(stream, device), int(clear)))
+
+
+def last_device_status(stream=None, device=None) -> int:
+    """Synchronise the stream, return the device status (0 or TIMEOUT=8)
+    recorded since the last read, and reset it."""
+    torch = _torch()
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(device):
+        return int(lib().dradd_last_device_status(_stream_handle(stream, device)))
 
 
 def bf16_convert_range(out, first: int, count: int, method: int = 0, stream=None):

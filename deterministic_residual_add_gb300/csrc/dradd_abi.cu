@@ -1302,6 +1302,11 @@ dradd_status dradd_device_status(cudaStream_t stream, int clear)
     return word ? DRADD_ERR_TIMEOUT : DRADD_OK;
 }
 
+dradd_status dradd_last_device_status(cudaStream_t stream)
+{
+    return dradd_device_status(stream, 1);
+}
+
 dradd_status dradd_bf16_convert_range(dradd_bf16* out, uint64_t first, int64_t count, int method,
                                       cudaStream_t stream)
 {

@@ -511,6 +511,15 @@ dradd_status invariant_unary_fwd_with_config(float* out, const float* x, int64_t
 dradd_status dradd_device_status(cudaStream_t stream, int clear);
 
 /*
+ * dradd_last_device_status -- the optional check after a call: synchronise
+ * `stream`, return DRADD_OK or the error a kernel recorded on the current
+ * device since the last read (DRADD_ERR_TIMEOUT: a bounded wait for a
+ * staged row expired, and that call's outputs are unspecified), and reset
+ * the word.  Equal to dradd_device_status(stream, 1).
+ */
+dradd_status dradd_last_device_status(cudaStream_t stream);
+
+/*
  * dradd_bf16_convert_range -- test hook: convert the `count` fp32 bit
  * patterns first, first+1, ... (mod 2^32) on the device, with method
  * 0 = the bf16 conversion the kernels use, 1 = integer round-half-even bit

@@ -121,3 +121,7 @@ def test_bounded_wait_expires_and_recovers(orc):
     eo, ero = orc.add_rmsnorm_fwd(x, r, w, 1e-6)
     assert_bits_equal(refs.u16(out), eo, "after timeout")
     assert dr.device_status(clear=True) == 0
+    # the one-argument form reads and resets in one call
+    dr.add_rmsnorm_fwd(dx, drs, dw, 1e-6, config=cfg)
+    assert dr.last_device_status() == 8
+    assert dr.last_device_status() == 0
