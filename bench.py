@@ -230,6 +230,22 @@ def elem_workload_desc(w) -> str:
     return f"invariant_unary_fwd log1p of {w.rows * w.cols} fp32 values"
 
 
+def host_cpu() -> str:
+    """The host CPU the oracle runs on: architecture, model and logical CPUs
+    (from lscpu where it is present)."""
+    import platform
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return f"{platform.machine()}, {model or 'model not reported'}, {os.cpu_count()} logical CPUs"
+
+
 def n_sets_for(name: str) -> int:
     """Buffer sets the timed loop rotates through: the smallest power of two
     >= N_SETS whose sets together hold at least 512 MiB of the op's
@@ -409,7 +425,7 @@ def cpu_baseline(seconds: float, name: str, first_inputs, gpu_set0=None):
             break
     dt = time.perf_counter() - t0
     out = {"value": algorithmic_bytes(rows, h, op) / dt / 1e9, "unit": "GB/s", "cores": 1,
-           "kind": "oracle",
+           "host": host_cpu(), "kind": "oracle",
            "sample": f"{rows} rows of the {n}x{h} workload ({rows * h} elements) in "
                      f"{dt:.1f} s, single thread",
            "seconds": round(dt, 3)}
@@ -684,6 +700,7 @@ def run_qk(args):
                         for k in got)
             line["cpu_baseline"] = {
                 "value": round(qk_algorithmic_bytes(w, tokens) / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+                "host": host_cpu(),
                 "kind": "oracle", "sample": f"{tokens} tokens of the {w.n_tokens}-token workload in {dt:.1f} s, "
                                             "single thread", "seconds": round(dt, 3),
                 "parity_rows_checked": chunk, "parity_bit_exact": bool(exact)}
@@ -804,7 +821,8 @@ def run_elem(args):
             ulp = 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -126))) - 23)
             bound = ulp + (2.0 ** -22 if w.kind == "merge" else 0.0)
             line["cpu_baseline"] = {
-                "value": round(cpu_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "value": round(cpu_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+                "host": host_cpu(), "kind": "oracle",
                 "sample": f"{done} {units} ({elems} elements) of the workload in {dt:.1f} s, single thread, double",
                 "seconds": round(dt, 3), "parity_elements_checked": int(ref.size),
                 "parity_within_bound": bool(np.all(np.abs(got.astype(np.float64) - ref) <= bound))}
@@ -854,7 +872,8 @@ def run_elem_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": elem_workload_desc(w), "engine": "CPU oracle", "sample": sample},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                         "host": host_cpu(), "kind": "oracle",
                          "sample": f"{sample}, single thread"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0}), flush=True)
@@ -886,7 +905,8 @@ def run_qk_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": qk_workload_desc(w), "engine": "CPU oracle", "tokens_per_step": tokens},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                         "host": host_cpu(), "kind": "oracle",
                          "sample": f"{tokens} of {w.n_tokens} tokens per step, single thread"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0}), flush=True)
@@ -931,7 +951,8 @@ def run_reference(args):
         "data": "synthetic",
         "config": {"workload": workload_desc(args.workload), "engine": "CPU oracle", "n_rows": n, "hidden": h,
                    "io_dtype": "bf16", "rows_per_step": rows},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                         "host": host_cpu(), "kind": "oracle",
                          "sample": f"{rows} of {n} rows per step, single thread"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
