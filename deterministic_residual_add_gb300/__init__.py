@@ -23,9 +23,11 @@ __all__ = [
     "add_rmsnorm_fwd", "add_rmsnorm_quant_fwd", "add_rmsnorm_fwd_with_config",
     "add_rmsnorm_quant_fwd_with_config", "rmsnorm_fwd", "rmsnorm_quant_fwd", "residual_add_fwd",
     "add_rmsnorm_fp8_fwd", "rmsnorm_fp8_fwd", "add_rmsnorm_fp4_fwd", "rmsnorm_fp4_fwd",
+    "fused_qk_rmsnorm_group_quant_fwd", "qk_resolve_config", "QkPlan",
+    "lse_merge_fwd", "invariant_unary_fwd", "UNARY_OPS",
     "LaunchConfig", "DraddError", "resolve_config",
-    "device_status", "bf16_convert_range", "status_string", "abi_version", "lib", "library_path",
-    "VARIANT_AUTO", "VARIANT_ROWS", "VARIANT_STAGED", "VARIANT_SPLIT", "MAX_HIDDEN",
+    "device_status", "last_device_status", "bf16_convert_range", "status_string", "abi_version", "lib",
+    "library_path", "VARIANT_AUTO", "VARIANT_ROWS", "VARIANT_STAGED", "VARIANT_SPLIT", "MAX_HIDDEN",
 ]
 
 PKG = Path(__file__).resolve().parent
