@@ -6,8 +6,8 @@ and out.  One step = one call over one 4096 x 4096 batch (x and residual
 read, residual_out and out written: 8 bytes per element, plus the weight
 once).  Inputs follow the chained-depth workload's distributions (x ~
 N(0, 0.05), residual ~ N(0, 1), weight ~ N(1, 0.1)).  Timed steps run back
-to back over 4 rotating buffer sets (512 MiB, four times the L2), so every
-step streams from HBM.  Other workloads (--workload) exist for profiling.
+to back over 8 rotating buffer sets (1 GiB, about eight times the L2), so
+every step streams from HBM.  Other workloads (--workload) exist for profiling.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -24,7 +24,6 @@ import dataclasses
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -42,8 +41,10 @@ from deterministic_residual_add_gb300 import inputs  # noqa: E402
 METRIC = "add+RMSNorm GB/s and % of HBM peak at 4096×4096 bf16; bit-exact vs oracle"
 QK_METRIC = "fused q/k RMSNorm GB/s and % of HBM peak; bit-exact vs oracle"
 N_SETS = 4
-KERNEL_SOURCES = ["csrc/dradd_kernels.cuh", "csrc/dradd_device.cuh"]
-TRAFFIC_FILE = ROOT / "profiles" / "add_rmsnorm_fwd_4096x4096_ncu.md"
+# Bytes the rotating buffer sets of a timed loop hold together: 1 GiB,
+# about eight times the 129 MB L2, so a set has left L2 before it comes round.
+ROTATION_BYTES = 2**30
+PROFILES = ROOT / "profiles"
 
 # name -> (n_rows, hidden, op, input recipe).  The first is the headline
 # workload; the others are for profiling and context.  op is one of
@@ -51,6 +52,7 @@ TRAFFIC_FILE = ROOT / "profiles" / "add_rmsnorm_fwd_4096x4096_ncu.md"
 # rmsnorm_quant, rmsnorm_fp8, residual_add.
 WORKLOADS = {
     "4096x4096": (4096, 4096, "add_rmsnorm", "chain4096"),
+    "tiny": (64, 1024, "add_rmsnorm", "tiny"),
     "2048x4096": (2048, 4096, "add_rmsnorm", "2048x4096"),
     "4096x8192": (4096, 8192, "add_rmsnorm", "4096x8192"),
     "8192x4096": (8192, 4096, "add_rmsnorm", "8192x4096"),
@@ -94,24 +96,186 @@ def measured_peaks() -> dict:
     return json.loads(p.read_text()) if p.exists() else {}
 
 
-def kernel_source_hash() -> str:
+# ------------------------------------------------------------ ncu records
+# DRAM traffic per launch comes from one ncu capture of the workload's own
+# bench command (one pass: gpu__time_duration and the two dram byte
+# counters), stored as profiles/ncu_<workload>.json by `--ncu-record`.  A
+# record is used only while the sources its kernels are built from hash to
+# the value it was taken on; otherwise the line's traffic is null.
+SOURCE_FAMILIES = {
+    "main": ["dradd_device.cuh", "dradd_kernels.cuh", "dradd_internal.h", "dradd_kernels.cu",
+             "dradd_staged_*.cu", "dradd_abi.cu"],
+    "qk": ["dradd_device.cuh", "dradd_kernels.cuh", "dradd_internal.h", "dradd_qk.cuh", "dradd_qk_*.cu",
+           "dradd_abi.cu"],
+    "elem": ["dradd_device.cuh", "dradd_internal.h", "dradd_lse.cu", "dradd_abi.cu"],
+}
+NCU_METRICS = "dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum"
+NCU_KERNELS = "regex:staged_kernel|rows_kernel|split_kernel|qk_kernel|lse_merge_kernel|unary_kernel|residual_add_kernel"
+NCU_WARMUP = 5
+
+
+def workload_family(name: str) -> str:
+    if name in inputs.QK_WORKLOADS:
+        return "qk"
+    if name in inputs.ELEM_WORKLOADS:
+        return "elem"
+    return "main"
+
+
+def source_files(family: str):
+    csrc = ROOT / "deterministic_residual_add_gb300" / "csrc"
+    files = []
+    for pat in SOURCE_FAMILIES[family]:
+        files += sorted(csrc.glob(pat))
+    return files + [ROOT / "include" / "dradd.h"]
+
+
+def source_hash(family: str) -> str:
+    """First 16 hex digits of the SHA-256 over the family's kernel sources
+    (names and contents, in a fixed order)."""
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
-        h.update((ROOT / "deterministic_residual_add_gb300" / rel).read_bytes())
+    for f in source_files(family):
+        h.update(f.name.encode() + b"\0" + f.read_bytes())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
-    if not TRAFFIC_FILE.exists():
-        return None
-    text = TRAFFIC_FILE.read_text()
-    m_src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
-    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not m_src or not m_b or m_src.group(1) != kernel_source_hash():
-        return None
-    return int(m_b.group(1))
+def workload_n_sets(name: str) -> int:
+    """Buffer sets the timed loop rotates through for any workload."""
+    if name in inputs.QK_WORKLOADS:
+        w = inputs.QK_WORKLOADS[name]
+        return max(N_SETS, -(-ROTATION_BYTES // qk_algorithmic_bytes(w, w.n_tokens)))
+    if name in inputs.ELEM_WORKLOADS:
+        return max(N_SETS, -(-ROTATION_BYTES // elem_bytes(inputs.ELEM_WORKLOADS[name])))
+    return n_sets_for(name)
+
+
+def workload_bytes(name: str) -> int:
+    if name in inputs.QK_WORKLOADS:
+        w = inputs.QK_WORKLOADS[name]
+        return qk_algorithmic_bytes(w, w.n_tokens)
+    if name in inputs.ELEM_WORKLOADS:
+        return elem_bytes(inputs.ELEM_WORKLOADS[name])
+    n, h, op, _ = WORKLOADS[name]
+    return algorithmic_bytes(n, h, op)
+
+
+def ncu_plan(name: str):
+    """(skip, count, steps): the capture skips the warm-up launches and one
+    full rotation of the buffer sets, then takes one full rotation (at least
+    4 launches), so each set's outputs are written back once in the window."""
+    k = workload_n_sets(name)
+    count = max(4, k)
+    skip = NCU_WARMUP + k
+    return skip, count, k + count + 2
+
+
+def ncu_capture_command(name: str) -> str:
+    """The capture behind profiles/ncu_<name>.json, run from the repository
+    root after the same bench command has exited 0 without ncu."""
+    skip, count, steps = ncu_plan(name)
+    return (f"ncu --metrics {NCU_METRICS} --print-units base --cache-control none --clock-control none "
+            f"-k '{NCU_KERNELS}' -s {skip} -c {count} --csv --log-file gpurun_out/ncu_{name}.csv "
+            f"python bench.py --workload {name} {ncu_bench_args(name)}")
+
+
+def ncu_bench_args(name: str) -> str:
+    _, _, steps = ncu_plan(name)
+    return f"--steps {steps} --warmup {NCU_WARMUP} --graph 0 --no-e2e --no-cpu"
+
+
+_UNIT = {"byte": 1.0, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9,
+         "nsecond": 1.0, "usecond": 1e3, "msecond": 1e6, "second": 1e9}
+
+
+def parse_ncu_csv(text: str):
+    """Launches of an ncu --csv metric log: [{kernel, grid, block, device,
+    metrics: {name: value in bytes or ns}}] in capture order."""
+    import csv
+    import io
+    lines = text.splitlines()
+    start = next((i for i, ln in enumerate(lines) if ln.startswith('"ID"')), None)
+    if start is None:
+        raise ValueError("no ncu CSV header in the log")
+    launches = {}
+    for row in csv.DictReader(io.StringIO("\n".join(lines[start:]))):
+        if not row.get("ID") or not row.get("Metric Name"):
+            continue
+        lid = int(row["ID"])
+        rec = launches.setdefault(lid, {"kernel": row.get("Kernel Name", ""), "grid": row.get("Grid Size", ""),
+                                        "block": row.get("Block Size", ""), "device": row.get("Device", ""),
+                                        "metrics": {}})
+        unit = (row.get("Metric Unit") or "").strip().lower()
+        val = float(row["Metric Value"].replace(",", ""))
+        rec["metrics"][row["Metric Name"]] = val * _UNIT.get(unit, 1.0)
+    return [launches[k] for k in sorted(launches)]
+
+
+def make_ncu_record(name: str, csv_text: str) -> dict:
+    launches = parse_ncu_csv(csv_text)
+    if not launches:
+        raise ValueError("the ncu log holds no launch")
+    kernels = sorted({ln["kernel"] for ln in launches})
+    if len(kernels) != 1:
+        raise ValueError(f"expected one kernel in the capture, found {kernels}")
+
+    def mean(metric):
+        return statistics.fmean(ln["metrics"][metric] for ln in launches)
+    rd, wr = mean("dram__bytes_read.sum"), mean("dram__bytes_write.sum")
+    alg = workload_bytes(name)
+    fam = workload_family(name)
+    return {
+        "workload": name, "kernel": kernels[0], "grid": launches[0]["grid"], "block": launches[0]["block"],
+        "launches_captured": len(launches), "rotating_sets": workload_n_sets(name),
+        "dram_bytes_read_per_launch": round(rd), "dram_bytes_write_per_launch": round(wr),
+        "dram_bytes_per_launch": round(rd + wr),
+        "gpu_time_duration_ns_mean": round(mean("gpu__time_duration.sum"), 1),
+        "algorithmic_bytes_per_launch": alg, "traffic_over_algorithmic": round((rd + wr) / alg, 4),
+        "note": "means over consecutive launches of the back-to-back bench loop, caches not flushed: "
+                "outputs left dirty in L2 are written back during later launches; under ncu each launch "
+                "is serialised, so the duration is not the bench's",
+        "source_family": fam, "source_sha256_16": source_hash(fam),
+        "sources": [str(f.relative_to(ROOT)) for f in source_files(fam)],
+        "command": ncu_capture_command(name),
+    }
+
+
+def ncu_record_path(name: str) -> Path:
+    return PROFILES / f"ncu_{name}.json"
+
+
+def recorded_traffic(name: str):
+    """(DRAM bytes per launch, record file) from profiles/ncu_<name>.json if
+    the record was taken on the current sources, else (None, reason)."""
+    p = ncu_record_path(name)
+    if not p.exists():
+        return None, "no ncu record"
+    rec = json.loads(p.read_text())
+    if rec.get("source_sha256_16") != source_hash(workload_family(name)):
+        return None, f"{p.name} was taken on other sources"
+    return int(rec["dram_bytes_per_launch"]), p.name
+
+
+L2_BYTES = 129 * 10**6
+
+
+def l2_desc(n_sets: int, bytes_step: int) -> str:
+    """config.l2: how the timed loop keeps its inputs out of L2."""
+    total = n_sets * bytes_step
+    where = ("more than L2 (129 MB): every step streams from HBM; roofline.traffic_over_algorithmic "
+             "gives the share of DRAM bytes measured" if total > L2_BYTES
+             else "fits in L2 (129 MB): a latency-bound size, not an HBM figure")
+    return f"{n_sets} rotating buffer sets ({total // 2**20} MiB), {where}"
+
+
+def traffic_fields(name: str, ms_per_step: float, peak: float) -> dict:
+    """roofline.traffic and what it says: the measured DRAM bytes over the
+    algorithmic bytes, and the DRAM-only fraction (traffic / time / peak)."""
+    traffic, src = recorded_traffic(name)
+    out = {"traffic": traffic, "traffic_source": src}
+    if traffic is not None:
+        out["traffic_over_algorithmic"] = round(traffic / workload_bytes(name), 4)
+        out["frac_dram"] = round(traffic / (ms_per_step / 1e3) / 1e9 / peak, 4)
+    return out
 
 
 # ------------------------------------------------------------------ clocks
@@ -248,12 +412,12 @@ def host_cpu() -> str:
 
 def n_sets_for(name: str) -> int:
     """Buffer sets the timed loop rotates through: the smallest power of two
-    >= N_SETS whose sets together hold at least 512 MiB of the op's
-    algorithmic bytes (about four times the 129 MB L2), at most 64."""
+    >= N_SETS whose sets together hold at least ROTATION_BYTES of the op's
+    algorithmic bytes, at most 64."""
     n, h, op, _ = WORKLOADS[name]
     b = algorithmic_bytes(n, h, op)
     k = N_SETS
-    while k * b < 512 * 2**20 and k < 64:
+    while k * b < ROTATION_BYTES and k < 64:
         k *= 2
     return k
 
@@ -322,36 +486,57 @@ class RawCall:
             raise dr.DraddError(st, self.name)
 
 
-GRAPH_CHUNK = 256  # launches per captured graph (a multiple of every set count)
+GRAPH_CHUNK = 256  # most launches captured in one CUDA graph
+PREROLL_CYCLES = 1_000_000
 
 
-def time_device(call, steps, warmup, stream, world, use_graph):
+def graph_plan(steps: int, n_sets: int, chunk: int = GRAPH_CHUNK):
+    """The CUDA graphs that replay `steps` launches, in order: a list of
+    (launches, first buffer set).  Launch k of the timed run (k = 0 ..
+    steps - 1) uses buffer set k mod n_sets whatever the split, so a graph
+    starts its rotation where the previous one stopped; graphs with the same
+    (launches, first set) are one captured graph replayed again."""
+    if steps < 0 or n_sets < 1 or chunk < 1:
+        raise ValueError("graph_plan: steps >= 0, n_sets >= 1, chunk >= 1")
+    plan, k = [], 0
+    while k < steps:
+        n = min(chunk, steps - k)
+        plan.append((n, k % n_sets))
+        k += n
+    return plan
+
+
+def time_device(call, steps, warmup, stream, world, use_graph, n_sets):
     """Exactly `steps` launches back to back on `stream`, timed with CUDA
-    events; with use_graph the launches are replayed from CUDA graphs of
-    GRAPH_CHUNK launches (plus one graph for the remainder)."""
+    events; launch k uses buffer set k mod n_sets (call(k)).  With use_graph
+    the launches are replayed from CUDA graphs of at most GRAPH_CHUNK
+    launches (graph_plan)."""
     for i in range(warmup):
         call(i)
     torch.cuda.synchronize()
-    plan = []
+    plan, graphs = graph_plan(steps, n_sets), {}
     if use_graph:
-        full, rest = divmod(steps, GRAPH_CHUNK)
-        graphs = {}
-        for n in {GRAPH_CHUNK if full else 0, rest} - {0}:
+        for key in dict.fromkeys(plan):
+            n, first = key
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for i in range(n):
-                    call(i)
+                    call(first + i)
             g.replay()  # untimed
-            graphs[n] = g
-        plan = [graphs[GRAPH_CHUNK]] * full + ([graphs[rest]] if rest else [])
+            graphs[key] = g
         torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
+    # Keep the stream busy (about half a millisecond, untimed) while the
+    # host enqueues the start event and the first launches, so the timed
+    # region holds the launches themselves and no host submission gap.
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(PREROLL_CYCLES)
     start.record(stream)
     if use_graph:
-        for g in plan:
-            g.replay()
+        for key in plan:
+            graphs[key].replay()
     else:
         for i in range(steps):
             call(i)
@@ -502,7 +687,7 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         sampler = ClockSampler(local)
         with sampler:
-            ms = time_device(call, args.steps, args.warmup, stream, world, args.graph)
+            ms = time_device(call, args.steps, args.warmup, stream, world, args.graph, len(sets))
     ms = max_over_ranks(ms, world)
     bytes_step = algorithmic_bytes(n_rows, hidden, op)
     ms_per_step = ms / args.steps
@@ -539,7 +724,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": workload_desc(args.workload), "n_rows": n_rows, "hidden": hidden,
                    "io_dtype": "bf16",
-                   "l2": f"{len(sets)} rotating buffer sets ({len(sets) * bytes_step // 2**20} MiB) > L2",
+                   "l2": l2_desc(len(sets), bytes_step),
                    "launch": launch,
                    "cuda_graph": bool(args.graph), "parallelism": f"replicas x{world}"},
         "rows_per_s": round(world * n_rows * args.steps / (ms / 1e3), 1),
@@ -547,7 +732,7 @@ def run_ours(args):
                      "unit": "GB/s", "frac": round(per_launch_gbs / peak, 4),
                      "peak_source": f"{peak_src} hbm_gbs",
                      "frac_of_nominal": round(per_launch_gbs / NOMINAL_HBM_GBS, 4),
-                     "traffic": recorded_traffic() if args.workload == "4096x4096" else None,
+                     **traffic_fields(args.workload, ms_per_step, peak),
                      "algorithmic_bytes_per_launch": bytes_step},
         "gpu_launches": args.steps,
         "e2e": e2e,
@@ -602,7 +787,7 @@ def run_qk(args):
     stream = torch.cuda.Stream(device)
     d0 = w.make()
     bytes_step = qk_algorithmic_bytes(w, w.n_tokens)
-    n_sets = max(N_SETS, -(-(4 * 129 * 2**20) // bytes_step))
+    n_sets = workload_n_sets(args.workload)
     nq, nk = d0["q"].shape[0], d0["k"].shape[0]
     qw, kw = d0["q_weight"].to(device), d0["k_weight"].to(device)
     sets = []
@@ -640,7 +825,7 @@ def run_qk(args):
     with torch.cuda.stream(stream):
         sampler = ClockSampler(local)
         with sampler:
-            ms = time_device(call, args.steps, args.warmup, stream, world, args.graph)
+            ms = time_device(call, args.steps, args.warmup, stream, world, args.graph, n_sets)
     ms = max_over_ranks(ms, world)
     ms_per_step = ms / args.steps
     per_launch_gbs = bytes_step / (ms_per_step / 1e3) / 1e9
@@ -658,14 +843,15 @@ def run_qk(args):
         "config": {"workload": qk_workload_desc(w),
                    "n_q_rows": nq, "q_hidden": w.q_head, "n_k_rows": nk, "k_hidden": w.k_head,
                    "group_size": w.group_size, "io_dtype": "bf16",
-                   "l2": f"{n_sets} rotating buffer sets ({n_sets * bytes_step // 2**20} MiB) > L2",
+                   "l2": l2_desc(n_sets, bytes_step),
                    "launch": dataclasses.asdict(plan), "cuda_graph": bool(args.graph),
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": round(world * w.n_tokens * args.steps / (ms / 1e3), 1),
         "roofline": {"bound": "hbm", "achieved": round(per_launch_gbs, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(per_launch_gbs / peak, 4), "peak_source": f"{peak_src} hbm_gbs",
                      "frac_of_nominal": round(per_launch_gbs / NOMINAL_HBM_GBS, 4),
-                     "traffic": None, "algorithmic_bytes_per_launch": bytes_step},
+                     **traffic_fields(args.workload, ms_per_step, peak),
+                     "algorithmic_bytes_per_launch": bytes_step},
         "gpu_launches": args.steps,
         "e2e": None,
     }
@@ -729,7 +915,7 @@ def run_elem(args):
     stream = torch.cuda.Stream(device)
     d0 = w.make()
     bytes_step = elem_bytes(w)
-    n_sets = max(N_SETS, -(-(4 * 129 * 2**20) // bytes_step))
+    n_sets = workload_n_sets(args.workload)
     st = stream.cuda_stream
     sets, argv = [], []
     for i in range(n_sets):
@@ -757,7 +943,7 @@ def run_elem(args):
     with torch.cuda.stream(stream):
         sampler = ClockSampler(local)
         with sampler:
-            ms = time_device(call, args.steps, args.warmup, stream, world, args.graph)
+            ms = time_device(call, args.steps, args.warmup, stream, world, args.graph, n_sets)
     ms = max_over_ranks(ms, world)
     ms_per_step = ms / args.steps
     per_launch = bytes_step / (ms_per_step / 1e3) / 1e9
@@ -771,12 +957,12 @@ def run_elem(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": desc, "io_dtype": "f32",
-                   "l2": f"{n_sets} rotating buffer sets ({n_sets * bytes_step // 2**20} MiB)"
-                         + (" > L2" if n_sets * bytes_step > 129e6 else " (fits in L2: latency-bound size)"),
+                   "l2": l2_desc(n_sets, bytes_step),
                    "launch": {"threads_per_cta": 128, "elements_per_thread": 8}, "cuda_graph": bool(args.graph),
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(per_launch, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(per_launch / peak, 4), "peak_source": f"{peak_src} hbm_gbs", "traffic": None,
+                     "frac": round(per_launch / peak, 4), "peak_source": f"{peak_src} hbm_gbs",
+                     **traffic_fields(args.workload, ms_per_step, peak),
                      "frac_of_nominal": round(per_launch / NOMINAL_HBM_GBS, 4),
                      "algorithmic_bytes_per_launch": bytes_step},
         "gpu_launches": args.steps,
@@ -975,7 +1161,20 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
+    ap.add_argument("--ncu-command", action="store_true",
+                    help="print the ncu capture command behind the workload's traffic record and exit")
+    ap.add_argument("--ncu-record", metavar="CSV",
+                    help="write profiles/ncu_<workload>.json from the log of that capture and exit")
     args = ap.parse_args()
+    if args.ncu_command:
+        print(f"python bench.py --workload {args.workload} {ncu_bench_args(args.workload)}")
+        print(ncu_capture_command(args.workload))
+        return
+    if args.ncu_record:
+        rec = make_ncu_record(args.workload, Path(args.ncu_record).read_text())
+        ncu_record_path(args.workload).write_text(json.dumps(rec, indent=1) + "\n")
+        print(json.dumps(rec))
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.workload in inputs.QK_WORKLOADS:
