@@ -40,7 +40,7 @@ OP_ADD_RMSNORM_FP4, OP_RMSNORM_FP4 = 6, 7
 
 STATUS_NAMES = {
     0: "OK", 1: "NULL_PTR", 2: "BAD_SHAPE", 3: "UNSUPPORTED_HIDDEN", 4: "MISALIGNED",
-    5: "BAD_EPS", 6: "ALIAS", 7: "CUDA", 8: "TIMEOUT", 9: "BAD_CONFIG",
+    5: "BAD_EPS", 6: "ALIAS", 7: "CUDA", 8: "TIMEOUT", 9: "BAD_CONFIG", 10: "UNDRAINED",
 }
 
 
@@ -598,7 +598,8 @@ def invariant_unary_fwd(x, op: str = "log1p", *, out=None, stream=None, config: 
 
 
 def device_status(stream=None, clear: bool = True, device=None) -> int:
-    """Synchronise the stream and return the device status (0 or TIMEOUT=8)."""
+    """Synchronise the stream and return the device status (0, TIMEOUT=8 or
+    UNDRAINED=10)."""
     torch = _torch()
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     with torch.cuda.device(device):
@@ -606,8 +607,8 @@ def device_status(stream=None, clear: bool = True, device=None) -> int:
 
 
 def last_device_status(stream=None, device=None) -> int:
-    """Synchronise the stream, return the device status (0 or TIMEOUT=8)
-    recorded since the last read, and reset it."""
+    """Synchronise the stream, return the device status (0, TIMEOUT=8 or
+    UNDRAINED=10) recorded since the last read, and reset it."""
     torch = _torch()
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     with torch.cuda.device(device):

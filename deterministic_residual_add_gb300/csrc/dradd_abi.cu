@@ -371,7 +371,17 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     if (staged) {
         const int64_t stage_bytes = (add ? 4 : 2) * hidden;
         const int64_t static_smem = static_cast<int64_t>(dradd::staged_static_smem(static_cast<int>(K)));
-        const int64_t avail = L.smem_per_block_optin - static_smem - 8 * 8;
+        // the quantised outputs keep the row's weights in fp32 beside the stages
+        const int64_t weight_bytes = quant ? 4 * hidden : 0;
+        const int64_t avail = L.smem_per_block_optin - static_smem - weight_bytes - 8 * 8;
+        if (auto_variant && avail < stage_bytes) {
+            // not even one stage fits beside the weights: registers instead
+            cfg->variant = DRADD_VARIANT_ROWS;
+            cfg->threads_per_row = 0;
+            cfg->blocks_per_thread = 0;
+            cfg->stages = 0;
+            return resolve(n_rows, hidden, quant, add, L, cfg);
+        }
         if (cfg->stages == 0) {
             int64_t S = avail / stage_bytes;
             cfg->stages = static_cast<int>(S > auto_stages ? auto_stages : S);
@@ -379,7 +389,7 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
         const int S = cfg->stages;
         if (S < 1 || S > 8 || S * stage_bytes > avail)
             return DRADD_ERR_BAD_CONFIG;
-        const int64_t per_cta = S * stage_bytes + static_smem + 8 * S + 1024;  // 1 KiB reserved per CTA
+        const int64_t per_cta = S * stage_bytes + weight_bytes + static_smem + 8 * S + 1024;  // 1 KiB reserved per CTA
         const int64_t by_smem = L.smem_per_sm / per_cta;
         if (by_smem < ctas_per_sm)
             ctas_per_sm = static_cast<int>(by_smem);
@@ -482,6 +492,7 @@ dradd_status run(int out_kind, bool add, dradd_bf16* out, int8_t* out_q, float* 
     const int K = static_cast<int>(next_pow2(hidden) / 8 / cfg.threads_per_row);
     const size_t dyn = cfg.variant == DRADD_VARIANT_STAGED
                            ? static_cast<size_t>(cfg.stages) * (add ? 4 : 2) * static_cast<size_t>(hidden) +
+                                 dradd::staged_weight_bytes(out_kind, static_cast<int>(hidden)) +
                                  8 * static_cast<size_t>(cfg.stages)
                            : 0;
     if (auto_grid && cfg.variant == DRADD_VARIANT_STAGED) {
@@ -1299,6 +1310,8 @@ dradd_status dradd_device_status(cudaStream_t stream, int clear)
     unsigned word = 0;
     if (dradd::read_device_status(&word, clear != 0, stream) != cudaSuccess)
         return DRADD_ERR_CUDA;
+    if (word & dradd::kDeviceStatusUndrained)
+        return DRADD_ERR_UNDRAINED;
     return word ? DRADD_ERR_TIMEOUT : DRADD_OK;
 }
 
@@ -1338,6 +1351,8 @@ const char* dradd_status_string(dradd_status status)
     case DRADD_ERR_CUDA: return "DRADD_ERR_CUDA: a CUDA runtime call failed";
     case DRADD_ERR_TIMEOUT: return "DRADD_ERR_TIMEOUT: a kernel's bounded wait expired";
     case DRADD_ERR_BAD_CONFIG: return "DRADD_ERR_BAD_CONFIG: invalid launch configuration";
+    case DRADD_ERR_UNDRAINED:
+        return "DRADD_ERR_UNDRAINED: a bounded wait expired and an issued copy had not landed";
     default: return "DRADD_ERR_UNKNOWN";
     }
 }

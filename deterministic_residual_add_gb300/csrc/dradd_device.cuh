@@ -214,6 +214,118 @@ __device__ __forceinline__ float butterfly_max(float v, int width)
     return v;
 }
 
+// The K per-block partial sums of every lane of a full warp, reduced over
+// the warp's 32 lanes by recursive halving: at the level with offset d
+// (d = 1, 2, ..., K / 2) a lane keeps one half of its current list of
+// subtree sums (the upper half if lane bit d is set) and sends the other
+// half to lane ^ d, which keeps the opposite half, and adds what it
+// receives to what it keeps; past K the single remaining sum goes through
+// the ordinary butterfly.  Both partners of a level hold the sums of the
+// same subtrees j over their aligned d-lane groups, so each addition is
+// (lower group) + (upper group) of the canonical tree, as in
+// butterfly_sum, with K / 2 + K / 4 + ... + 1 + (5 - log2 K) shuffles
+// instead of 5 K.  Returns the sum over the warp of subtree j_out, where
+// j_out is lane bit 0 -> K / 2, bit 1 -> K / 4, ... (the lane's low
+// log2 K bits reversed).
+template <int K>
+__device__ __forceinline__ float warp_halving_sum(float (&p)[K], int lane, int& j_out)
+{
+    static_assert(K >= 1 && K <= 32 && (K & (K - 1)) == 0, "K: a power of two up to 32");
+    int j = 0;
+#pragma unroll
+    for (int d = 1, c = K; d < K; d <<= 1, c >>= 1) {
+        const bool upper = (lane & d) != 0;
+        const int h = c >> 1;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float keep = upper ? p[h + i] : p[i];
+            const float send = upper ? p[i] : p[h + i];
+            p[i] = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, send, d));
+        }
+        j += upper ? h : 0;
+    }
+    float v = p[0];
+#pragma unroll
+    for (int d = K; d < 32; d <<= 1)
+        v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, d));
+    j_out = j;
+    return v;
+}
+
+// After warp_halving_sum in a one-warp row: the top log2 K levels of the
+// tree, across the lanes that hold the K subtree sums.  Subtree j ^ 1 sits
+// on lane ^ (K / 2), j ^ 2 on lane ^ (K / 4), ...; every lane ends with the
+// row's sum.
+template <int K>
+__device__ __forceinline__ float fold_lane_subtrees(float v)
+{
+#pragma unroll
+    for (int d = K >> 1; d >= 1; d >>= 1)
+        v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, d));
+    return v;
+}
+
+// The rest of the tree from red[j * W + w] = the sum of subtree j over warp
+// w (W = T / 32 warps of a row, published by lanes 0 .. K - 1 after
+// warp_halving_sum): over the warps of each subtree, then over the
+// subtrees, adjacent pairs first at every level.  Every lane returns the
+// row's sum.
+template <int K, int W>
+__device__ __forceinline__ float cross_warp_sum(const float* red, int lane)
+{
+    if constexpr (K * W <= 32) {
+        // one value per lane: index j * W + w, so offsets below W join
+        // warps and offsets W, 2W, ... join adjacent subtrees
+        float v = red[lane & (K * W - 1)];
+#pragma unroll
+        for (int d = 1; d < K * W; d <<= 1)
+            v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, d));
+        return v;
+    } else {
+        float q[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+            q[j] = butterfly_sum(red[j * W + (lane & (W - 1))], W);
+        return fold_k<K>(q);
+    }
+}
+
+// max(a, |b|), NaN if either is NaN (a NaN y anywhere in a row shows in its
+// amax, so the row can take the exact path).
+__device__ __forceinline__ float max_abs_nan(float a, float b)
+{
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(fabsf(b)));
+    return d;
+}
+
+// y = (acc * inv) * w for one block, with its 8 weights already in fp32
+// (w_lo: elements 0-3, w_hi: 4-7).
+__device__ __forceinline__ void scale8_f32(float (&a)[8], float inv, const float4& w_lo, const float4& w_hi)
+{
+    mul2_rn(a[0], a[1], inv, inv, a[0], a[1]);
+    mul2_rn(a[2], a[3], inv, inv, a[2], a[3]);
+    mul2_rn(a[4], a[5], inv, inv, a[4], a[5]);
+    mul2_rn(a[6], a[7], inv, inv, a[6], a[7]);
+    mul2_rn(a[0], a[1], w_lo.x, w_lo.y, a[0], a[1]);
+    mul2_rn(a[2], a[3], w_lo.z, w_lo.w, a[2], a[3]);
+    mul2_rn(a[4], a[5], w_hi.x, w_hi.y, a[4], a[5]);
+    mul2_rn(a[6], a[7], w_hi.z, w_hi.w, a[6], a[7]);
+}
+
+// butterfly_max with NaN propagation: NaN in any lane gives NaN in all.
+__device__ __forceinline__ float butterfly_max_nan(float v, int width)
+{
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        if (d < width) {
+            const float o = __shfl_xor_sync(0xFFFFFFFFu, v, d);
+            asm("max.NaN.f32 %0, %1, %2;" : "=f"(v) : "f"(v), "f"(o));
+        }
+    }
+    return v;
+}
+
 // inv = 1 / sqrt(S / hidden + eps), each operation rounded once.
 // inv_hidden is 1 / hidden when hidden is a power of two (else 0): S / hidden
 // and S * 2^-k are then the same real number, so rounding the product gives
@@ -309,6 +421,71 @@ __device__ __forceinline__ uint2 quantize8(const float (&y)[8], const QuantScale
     uint2 u;
     u.x = pack4_low_bytes(bits[0], bits[1], bits[2], bits[3]);
     u.y = pack4_low_bytes(bits[4], bits[5], bits[6], bits[7]);
+    return u;
+}
+
+// Int8 codes by a bracket of the quotient.  With c = RN(1 / scale) (relative
+// error at most 2^-24), c_lo = RN(c (1 - 2^-22)) and c_hi = RN(c (1 + 2^-22))
+// satisfy, for y >= 0 and a normal quotient,
+//   y c_lo <= y/scale (1 + 2^-24)(1 - 2^-22)(1 + 2^-24) < y/scale (1 - 2^-24)
+//          <= RN(y / scale) <= y/scale (1 + 2^-24)
+//          < y/scale (1 - 2^-24)(1 + 2^-22)(1 - 2^-24) <= y c_hi
+// (mirrored for y < 0; a subnormal quotient is below 2^-126 and every
+// candidate then rounds to 0).  fma(y, c, 1.5 * 2^23) is 1.5 * 2^23 plus
+// the exact product rounded to an integer, ties to even (|y c| < 2^22 here),
+// and rounding to an integer is monotone, so when the two ends give the
+// same bits, rint(RN(y / scale)) is that integer; |y / scale| <= 127.00001,
+// so no clamp is needed.  The low byte of those bits is the int8 code.
+// fast: scale normal and below 2^120; rows with a NaN y or another scale
+// take quantize_exact.
+struct Int8Bracket {
+    float scale;
+    float c_lo, c_hi;
+    bool fast;
+};
+
+__device__ __forceinline__ Int8Bracket make_int8_bracket(float scale)
+{
+    Int8Bracket s;
+    s.scale = scale;
+    s.fast = scale >= 0x1p-126f && scale < 0x1p120f;
+    const float c = s.fast ? __frcp_rn(scale) : 0.0f;
+    s.c_lo = __fmul_rn(c, 1.0f - 0x1p-22f);
+    s.c_hi = __fmul_rn(c, 1.0f + 0x1p-22f);
+    return s;
+}
+
+// Eight codes; `differ` collects the bits in which any pair of ends
+// differs (nonzero: redo the block with quantize_exact).
+__device__ __forceinline__ uint2 quantize8_bracket(const float (&y)[8], const Int8Bracket& s, uint32_t& differ)
+{
+    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+    uint32_t lo[8];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        float l0, l1, h0, h1;
+        fma2_rn(y[e], y[e + 1], s.c_lo, s.c_lo, kRound, kRound, l0, l1);
+        fma2_rn(y[e], y[e + 1], s.c_hi, s.c_hi, kRound, kRound, h0, h1);
+        lo[e] = __float_as_uint(l0);
+        lo[e + 1] = __float_as_uint(l1);
+        differ |= lo[e] ^ __float_as_uint(h0);
+        differ |= lo[e + 1] ^ __float_as_uint(h1);
+    }
+    uint2 u;
+    u.x = pack4_low_bytes(lo[0], lo[1], lo[2], lo[3]);
+    u.y = pack4_low_bytes(lo[4], lo[5], lo[6], lo[7]);
+    return u;
+}
+
+__device__ __forceinline__ uint2 quantize8_exact(const float (&y)[8], float scale)
+{
+    uint32_t q[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        q[e] = static_cast<uint32_t>(quantize_exact(y[e], scale));
+    uint2 u;
+    u.x = pack4_low_bytes(q[0], q[1], q[2], q[3]);
+    u.y = pack4_low_bytes(q[4], q[5], q[6], q[7]);
     return u;
 }
 

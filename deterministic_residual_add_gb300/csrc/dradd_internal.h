@@ -32,9 +32,20 @@ struct Params {
 };
 
 constexpr unsigned kDeviceStatusTimeout = 1u;
+// A bulk copy issued before a timeout had still not landed when the CTA gave
+// up waiting for it (after several wait limits).
+constexpr unsigned kDeviceStatusUndrained = 2u;
 
 // What a normalised row is stored as.
 enum OutKind : int { kOutBf16 = 0, kOutInt8 = 1, kOutE4m3 = 2, kOutE2m1 = 3, kOutE4m3Group = 4 };
+
+// Shared memory the staged kernel keeps besides its stages: for the
+// quantised outputs the row's weights, widened to fp32 once per CTA (4
+// bytes per element of the row, 16-byte aligned).
+__host__ __device__ constexpr uint32_t staged_weight_bytes(int out, int hidden)
+{
+    return out == kOutBf16 ? 0u : 4u * static_cast<uint32_t>(hidden);
+}
 
 using KernelFn = void (*)(Params);
 // Fused q/k RMSNorm: (q rows, k rows, number of CTAs given to the q rows).

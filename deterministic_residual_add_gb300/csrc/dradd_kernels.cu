@@ -307,8 +307,9 @@ size_t split_static_smem(int K)
 
 size_t staged_static_smem(int K)
 {
-    // s_sum[2][32 * K] + s_max[2][32], as declared in staged_kernel
-    return sizeof(float) * (2 * 32 * static_cast<size_t>(K) + 2 * 32);
+    // at most s_sum[2][K * 32] + s_max[2][32] + s_max2[32] (32 warps), as
+    // declared in staged_kernel
+    return sizeof(float) * (2 * 32 * static_cast<size_t>(K) + 3 * 32);
 }
 
 namespace {
@@ -412,18 +413,37 @@ cudaError_t launch_convert(uint16_t* out, uint64_t first, int64_t count, int met
     return cudaGetLastError();
 }
 
+// The status word is read (and with `clear` reset) by one atomic exchange in
+// a one-thread kernel on the caller's stream, so a timeout that a kernel on
+// another stream records at the same moment is either in the value read or
+// stays in the word for the next read; never lost.  The value travels back
+// through a result slot of its own per call (a ring of kStatusSlots, picked
+// by a host counter), so reads from several host threads at once do not
+// overwrite each other's results.
+constexpr unsigned kStatusSlots = 64;
+__device__ unsigned int g_status_taken[kStatusSlots];
+
+__global__ void status_take_kernel(unsigned slot, int clear)
+{
+    g_status_taken[slot] = clear ? atomicExch(&g_device_status, 0u) : atomicOr(&g_device_status, 0u);
+}
+
 cudaError_t read_device_status(unsigned* status, bool clear, cudaStream_t stream)
 {
-    cudaError_t e = cudaStreamSynchronize(stream);
+    static std::atomic<unsigned> next_slot{0};
+    const unsigned slot = next_slot.fetch_add(1, std::memory_order_relaxed) % kStatusSlots;
+    status_take_kernel<<<1, 1, 0, stream>>>(slot, clear ? 1 : 0);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
-    e = cudaMemcpyFromSymbol(status, g_device_status, sizeof(unsigned));
+    unsigned value = 0;
+    e = cudaMemcpyFromSymbolAsync(&value, g_status_taken, sizeof(unsigned), slot * sizeof(unsigned),
+                                  cudaMemcpyDeviceToHost, stream);
     if (e != cudaSuccess)
         return e;
-    if (clear) {
-        const unsigned zero = 0;
-        e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(unsigned));
-    }
+    e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess)
+        *status = value;
     return e;
 }
 

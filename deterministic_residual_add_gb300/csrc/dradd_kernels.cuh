@@ -229,6 +229,37 @@ __device__ __forceinline__ void record_timeout(const Params& p)
     atomicOr(p.status, kDeviceStatusTimeout);
 }
 
+// After an expired wait, thread 0 of a staged CTA waits for every bulk copy
+// the CTA has issued and not yet consumed: iterations i .. i + stages - 1
+// (stage s onwards, phase parity `parity`) whose unit first + i2 * stride
+// is below n_units; with fault_inject the copy of iteration 0 was never
+// issued.  A copy that has not landed within the wait limit gets up to
+// kDrainRounds limits in all, so that none lands in shared memory after
+// the CTA has exited; one still missing then is recorded as
+// kDeviceStatusUndrained (every wait stays bounded).
+constexpr int kDrainRounds = 8;
+
+__device__ __forceinline__ void drain_issued_copies(const Params& p, uint64_t* bars, int s, uint32_t parity,
+                                                    int64_t i, int stages, int64_t first, int64_t stride,
+                                                    int64_t n_units)
+{
+    for (int64_t i2 = i; i2 < i + stages; ++i2) {
+        if (first + i2 * stride >= n_units)
+            break;
+        if (!(p.fault_inject && i2 == 0)) {
+            bool landed = false;
+            for (int r = 0; r < kDrainRounds && !landed; ++r)
+                landed = mbar_wait_bounded(&bars[s], parity, p.wait_limit_ns);
+            if (!landed)
+                atomicOr(p.status, kDeviceStatusUndrained);
+        }
+        if (++s == stages) {
+            s = 0;
+            parity ^= 1u;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- rows_kernel
 // The CTA numbered `cta` of `n_ctas` handles row groups cta, cta + n_ctas, ...
 template <int K, int OUT, bool ADD>
@@ -300,25 +331,143 @@ __global__ void __launch_bounds__(max_threads_for(K)) rows_kernel(const Params p
 constexpr uint32_t kL2PrefetchBytes = 16384;
 
 // -------------------------------------------------------------- staged_kernel
+// Per-row scale and codes of the quantised outputs in the staged kernel
+// (one row per CTA, T threads, compile-time): the row's amax over the CTA,
+// then the codes of each of the thread's blocks.
+template <int T, int K, int OUT>
+__device__ __forceinline__ void staged_quant_row(const Params& p, const float (&y)[K][8], int64_t row, int tid,
+                                                 int lane, int warp, int nblocks, float* red_max,
+                                                 float* red_max2)
+{
+    constexpr int W = T / 32;
+    if constexpr (OUT == kOutInt8) {
+        // amax with NaN propagation: a row holding a NaN y shows as a NaN
+        // amax and takes the exact path (whose amax ignores NaN).
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                m = max_abs_nan(m, y[j][e]);
+        m = butterfly_max_nan(m, 32);
+        if constexpr (W > 1) {
+            if (lane == 0)
+                red_max[warp] = m;
+            __syncthreads();
+            m = butterfly_max_nan(red_max[lane & (W - 1)], W);
+        }
+        uint2* qrow = reinterpret_cast<uint2*>(p.out_q + row * p.hidden);
+        if (!isnan(m)) {
+            const float scale = __fdiv_rn(m, 127.0f);
+            if (tid == 0)
+                p.scale[row] = scale;
+            const Int8Bracket qs = make_int8_bracket(scale);
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const int b = tid + j * T;
+                if (b < nblocks) {
+                    uint32_t differ = 0u;
+                    uint2 code = quantize8_bracket(y[j], qs, differ);
+                    if (!qs.fast || differ != 0u)
+                        code = quantize8_exact(y[j], scale);
+                    st_stream(qrow + b, code);
+                }
+            }
+        } else {
+            // uniform over the CTA: every thread holds the same m
+            float m2 = 0.0f;
+#pragma unroll
+            for (int j = 0; j < K; ++j)
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    m2 = fmaxf(m2, fabsf(y[j][e]));
+            m2 = butterfly_max(m2, 32);
+            if constexpr (W > 1) {
+                if (lane == 0)
+                    red_max2[warp] = m2;
+                __syncthreads();
+                m2 = butterfly_max(red_max2[lane & (W - 1)], W);
+            }
+            const float scale = __fdiv_rn(m2, 127.0f);
+            if (tid == 0)
+                p.scale[row] = scale;
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const int b = tid + j * T;
+                if (b < nblocks)
+                    st_stream(qrow + b, quantize8_exact(y[j], scale));
+            }
+        }
+    } else {
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                m = fmaxf(m, fabsf(y[j][e]));
+        m = butterfly_max(m, 32);
+        if constexpr (W > 1) {
+            if (lane == 0)
+                red_max[warp] = m;
+            __syncthreads();
+            m = butterfly_max(red_max[lane & (W - 1)], W);
+        }
+        const float scale = __fdiv_rn(m, OUT == kOutE4m3 ? 448.0f : 6.0f);
+        if (tid == 0)
+            p.scale[row] = scale;
+        const E4m3Scale qs = make_e4m3_scale(scale);
+        if constexpr (OUT == kOutE2m1) {
+            // two codes per byte: a row is hidden / 2 bytes, a block 4 bytes
+            uint32_t* prow = reinterpret_cast<uint32_t*>(p.out_q + row * (p.hidden / 2));
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const int b = tid + j * T;
+                if (b < nblocks)
+                    __stcs(prow + b, quantize8_e2m1(y[j], qs));
+            }
+        } else {
+            uint2* qrow = reinterpret_cast<uint2*>(p.out_q + row * p.hidden);
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const int b = tid + j * T;
+                if (b < nblocks)
+                    st_stream(qrow + b, quantize8_e4m3(y[j], qs));
+            }
+        }
+    }
+}
+
 // T (threads per row = threads per CTA) is a compile-time constant so that
 // every (T, K) pair gets its own register budget (staged_min_blocks) and the
 // reduction widths fold away.  A stage holds one row of x, then (with ADD)
-// one row of residual.
+// one row of residual.  The row's sum of squares: each thread's K block sums
+// go through warp_halving_sum, then (T > 32) lanes 0 .. K - 1 of each warp
+// publish their subtree sums and cross_warp_sum finishes the tree.  The
+// quantised outputs read their weights as fp32 from shared memory (widened
+// once per CTA, each thread its own blocks: w_lo holds elements 0-3 of
+// every block, w_hi elements 4-7, so a warp's 16-byte reads are
+// consecutive); bf16 out keeps them packed in registers.
 template <int T, int K, int OUT, bool ADD>
 __global__ void __launch_bounds__(T, staged_min_blocks(T, K)) staged_kernel(const Params p)
 {
     static_assert(T >= 32 && T <= 1024 && (T & (T - 1)) == 0, "T: a power of two, 32..1024");
+    constexpr int W = T / 32;
+    constexpr bool kWsm = OUT != kOutBf16;
     extern __shared__ __align__(128) unsigned char stage_mem[];
-    __shared__ float s_sum[2][32 * K];
-    __shared__ float s_max[2][32];
+    __shared__ float s_sum[2][K * W];
+    __shared__ float s_max[2][W];
+    __shared__ float s_max2[W];
     const int tid = threadIdx.x;
     const int lane = tid & 31;
-    const int warp_in_row = tid >> 5;
+    const int warp = tid >> 5;
     const int nblocks = p.hidden >> 3;
     const int stages = p.stages;
     const uint32_t row_bytes = static_cast<uint32_t>(p.hidden) * 2u;
     const uint32_t stage_bytes = (ADD ? 2u : 1u) * row_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(stage_mem + static_cast<size_t>(stages) * stage_bytes);
+    unsigned char* const after_stages = stage_mem + static_cast<size_t>(stages) * stage_bytes;
+    float4* const w_lo = reinterpret_cast<float4*>(after_stages);
+    float4* const w_hi = w_lo + nblocks;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(after_stages + staged_weight_bytes(OUT, p.hidden));
     const int64_t stride = gridDim.x;
 
     if (tid == 0) {
@@ -362,8 +511,24 @@ __global__ void __launch_bounds__(T, staged_min_blocks(T, K)) staged_kernel(cons
         }
     }
 
-    uint4 w[K];
-    load_weights<K>(p, w, tid, T, nblocks);
+    uint4 w[kWsm ? 1 : K];
+    if constexpr (kWsm) {
+        // each thread widens the weights of its own blocks (and only it
+        // reads them, so no barrier is needed)
+        const uint4* wrow = reinterpret_cast<const uint4*>(p.weight);
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const int b = tid + j * T;
+            if (b < nblocks) {
+                float f[8];
+                unpack8(__ldg(wrow + b), f);
+                w_lo[b] = make_float4(f[0], f[1], f[2], f[3]);
+                w_hi[b] = make_float4(f[4], f[5], f[6], f[7]);
+            }
+        }
+    } else {
+        load_weights<K>(p, w, tid, T, nblocks);
+    }
 
     int buf = 0;
     // Iteration i of this CTA uses stage s = i mod stages and waits for phase
@@ -392,26 +557,19 @@ __global__ void __launch_bounds__(T, staged_min_blocks(T, K)) staged_kernel(cons
         float acc[K][8], part[K];
         row_accumulate<K, ADD>(p, xv, rv, acc, part, row, true, tid, T, nblocks);
 
-        float* red = &s_sum[buf][0];
-        lanes_then_publish<K>(part, T, lane, warp_in_row, red);
+        int jsub;
+        float v = warp_halving_sum<K>(part, lane, jsub);
+        if constexpr (W > 1) {
+            if (lane < K)
+                s_sum[buf][jsub * W + warp] = v;
+        }
         // Every thread has read stage s (so it can be refilled) and published
-        // its warp's partial sums; any expired wait ends the CTA here.
+        // its warp's subtree sums; any expired wait ends the CTA here.
         if (__syncthreads_or(!ok)) {
             if (tid == 0) {
                 record_timeout(p);
                 // Copies already issued must land before shared memory is released.
-                int s2 = s;
-                uint32_t parity2 = parity;
-                for (int64_t i2 = i; i2 < i + stages; ++i2) {
-                    if (blockIdx.x + i2 * stride >= p.n_rows)
-                        break;
-                    if (!(p.fault_inject && i2 == 0))
-                        mbar_wait_bounded(&bars[s2], parity2, p.wait_limit_ns);
-                    if (++s2 == stages) {
-                        s2 = 0;
-                        parity2 ^= 1u;
-                    }
-                }
+                drain_issued_copies(p, bars, s, parity, i, stages, blockIdx.x, stride, p.n_rows);
             }
             return;
         }
@@ -422,10 +580,23 @@ __global__ void __launch_bounds__(T, staged_min_blocks(T, K)) staged_kernel(cons
                 issue(s, next);
             }
         }
-        gather_warps<K>(part, T, lane, red);
-        const float inv = inv_rms(fold_k<K>(part), p.hidden, p.inv_hidden, p.eps);
-        finish_row<K, OUT>(p, acc, w, inv, row, true, tid, T, lane, warp_in_row, nblocks,
-                             &s_max[buf][0]);
+        float sum;
+        if constexpr (W > 1)
+            sum = cross_warp_sum<K, W>(s_sum[buf], lane);
+        else
+            sum = fold_lane_subtrees<K>(v);
+        const float inv = inv_rms(sum, p.hidden, p.inv_hidden, p.eps);
+        if constexpr (kWsm) {
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const int b = tid + j * T;
+                if (b < nblocks)
+                    scale8_f32(acc[j], inv, w_lo[b], w_hi[b]);
+            }
+            staged_quant_row<T, K, OUT>(p, acc, row, tid, lane, warp, nblocks, s_max[buf], s_max2);
+        } else {
+            finish_row<K, OUT>(p, acc, w, inv, row, true, tid, T, lane, warp, nblocks, &s_max[buf][0]);
+        }
         buf ^= 1;
         if (++s == stages) {
             s = 0;

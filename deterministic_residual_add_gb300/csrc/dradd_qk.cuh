@@ -128,18 +128,7 @@ __device__ __forceinline__ void tile_body(const Params& p, int64_t cta, int64_t 
             if (tid == 0) {
                 record_timeout(p);
                 // Copies already issued must land before shared memory is released.
-                int s2 = s;
-                uint32_t parity2 = parity;
-                for (int64_t i2 = i; i2 < i + stages; ++i2) {
-                    if (cta + i2 * n_ctas >= n_groups)
-                        break;
-                    if (!(p.fault_inject && i2 == 0))
-                        mbar_wait_bounded(&bars[s2], parity2, p.wait_limit_ns);
-                    if (++s2 == stages) {
-                        s2 = 0;
-                        parity2 ^= 1u;
-                    }
-                }
+                drain_issued_copies(p, bars, s, parity, i, stages, cta, n_ctas, n_groups);
             }
             return;
         }

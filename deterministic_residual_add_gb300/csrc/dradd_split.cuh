@@ -131,18 +131,7 @@ __global__ void __launch_bounds__(T, staged_min_blocks(T, K)) split_kernel(const
                 // Copies already issued (rows i .. i + stages - 1; none was
                 // issued for a stage after its wait) must land before shared
                 // memory is released.
-                int s2 = s;
-                uint32_t parity2 = parity;
-                for (int64_t i2 = i; i2 < i + stages; ++i2) {
-                    if (first_row + i2 * n_clusters >= p.n_rows)
-                        break;
-                    if (!(p.fault_inject && i2 == 0))
-                        mbar_wait_bounded(&bars[s2], parity2, p.wait_limit_ns);
-                    if (++s2 == stages) {
-                        s2 = 0;
-                        parity2 ^= 1u;
-                    }
-                }
+                drain_issued_copies(p, bars, s, parity, i, stages, first_row, n_clusters, p.n_rows);
             }
             cluster_sync_all();  // no CTA leaves while another may read its shared memory
             return;

@@ -83,7 +83,9 @@ enum {
     DRADD_ERR_ALIAS = 6,              /* buffers overlap other than as allowed         */
     DRADD_ERR_CUDA = 7,               /* a CUDA runtime call failed                    */
     DRADD_ERR_TIMEOUT = 8,            /* a kernel's bounded wait expired (device)      */
-    DRADD_ERR_BAD_CONFIG = 9          /* an explicit launch configuration is invalid   */
+    DRADD_ERR_BAD_CONFIG = 9,         /* an explicit launch configuration is invalid   */
+    DRADD_ERR_UNDRAINED = 10          /* after a timeout, an issued bulk copy had not
+                                         landed when the kernel stopped waiting (device) */
 };
 
 /*
@@ -505,8 +507,14 @@ dradd_status invariant_unary_fwd_with_config(float* out, const float* x, int64_t
 
 /*
  * dradd_device_status -- synchronise `stream`, then return DRADD_OK or the
- * error a kernel recorded on the current device since the last clear
- * (DRADD_ERR_TIMEOUT).  clear != 0 resets the word afterwards.
+ * error a kernel recorded on the current device since the last clear:
+ * DRADD_ERR_TIMEOUT (a bounded wait expired) or DRADD_ERR_UNDRAINED (it
+ * expired and, after several more wait limits, a bulk copy the kernel had
+ * issued still had not landed in shared memory: the device's state is
+ * suspect and the context should be rebuilt).  The word is read, and with
+ * clear != 0 reset, by one atomic exchange on `stream`: a kernel on another
+ * stream that records an error at the same time is either seen by this read
+ * or left for the next one.
  */
 dradd_status dradd_device_status(cudaStream_t stream, int clear);
 
