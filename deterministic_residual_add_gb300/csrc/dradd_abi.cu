@@ -261,6 +261,41 @@ dradd_status resolve_split(int64_t n_rows, int64_t hidden, bool quant, bool add,
     return DRADD_OK;
 }
 
+// The warp-per-row variant: K = P / 256 blocks per lane, one warp a row,
+// rows_per_cta warps (and rows per stage) per CTA, `stages` stages.
+// Automatic: the most warps (up to kWarpMaxRows) for which 2 stages fit in
+// one CTA's shared memory, 2 stages.
+dradd_status resolve_warp(int64_t hidden, bool add, const DeviceLimits& L, dradd_launch_cfg* cfg)
+{
+    const int64_t blocks = next_pow2(hidden) / 8;
+    if (blocks < 32 || blocks / 32 > 16 || (add && blocks / 32 > 8))
+        return DRADD_ERR_BAD_CONFIG;
+    const int K = static_cast<int>(blocks / 32);
+    if (cfg->threads_per_row == 0)
+        cfg->threads_per_row = 32;
+    if (cfg->blocks_per_thread == 0)
+        cfg->blocks_per_thread = K;
+    if (cfg->threads_per_row != 32 || cfg->blocks_per_thread != K || cfg->cluster_ctas != 0 ||
+        cfg->wait_limit_us < 0 || (cfg->serialize != 0 && cfg->serialize != 1) || cfg->grid_ctas < 0 ||
+        cfg->fault_inject < 0 || cfg->rows_per_cta < 0 || cfg->rows_per_cta > dradd::kWarpMaxRows ||
+        cfg->stages < 0 || cfg->stages > 8)
+        return DRADD_ERR_BAD_CONFIG;
+    const int64_t limit = L.smem_per_block_optin - 1024;
+    const int S0 = cfg->stages != 0 ? cfg->stages : 2;
+    if (cfg->rows_per_cta == 0) {
+        int R = dradd::kWarpMaxRows;
+        while (R > 1 && static_cast<int64_t>(dradd::warp_smem_bytes(S0, R, static_cast<int>(hidden), add)) > limit)
+            --R;
+        cfg->rows_per_cta = R;
+    }
+    if (cfg->stages == 0)
+        cfg->stages = S0;
+    if (static_cast<int64_t>(dradd::warp_smem_bytes(cfg->stages, cfg->rows_per_cta, static_cast<int>(hidden),
+                                                    add)) > limit)
+        return DRADD_ERR_BAD_CONFIG;
+    return DRADD_OK;
+}
+
 // Fill the automatic fields of *cfg and check the explicit ones.
 dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const DeviceLimits& L,
                      dradd_launch_cfg* cfg)
@@ -295,6 +330,8 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
         cfg->variant = hidden > 256 ? DRADD_VARIANT_STAGED : DRADD_VARIANT_ROWS;
     if (cfg->variant == DRADD_VARIANT_SPLIT)
         return resolve_split(n_rows, hidden, quant, add, L, cfg);
+    if (cfg->variant == DRADD_VARIANT_WARP)
+        return resolve_warp(hidden, add, L, cfg);
     if (cfg->cluster_ctas != 0)
         return DRADD_ERR_BAD_CONFIG;
     if (cfg->variant != DRADD_VARIANT_ROWS && cfg->variant != DRADD_VARIANT_STAGED)
@@ -444,13 +481,60 @@ dradd_status run(int out_kind, bool add, dradd_bf16* out, int8_t* out_q, float* 
     const bool auto_grid = cfg.grid_ctas == 0;
     const bool device_memory = all_device_memory({out, out_q, scale, residual_out, x, residual, weight});
     if (!device_memory) {
+        // host memory (read and written over the host link): register loads
+        // only, so no variant that stages rows with bulk copies
         if (cfg.variant == DRADD_VARIANT_STAGED || cfg.variant == DRADD_VARIANT_SPLIT)
+            return DRADD_ERR_BAD_CONFIG;
+        if (cfg.variant == DRADD_VARIANT_WARP)
             return DRADD_ERR_BAD_CONFIG;
         cfg.variant = DRADD_VARIANT_ROWS;
     }
     st = resolve(n_rows, hidden, quant, add, L, &cfg);
     if (st != DRADD_OK)
         return st;
+    if (cfg.variant == DRADD_VARIANT_WARP) {
+        if (!device_memory)
+            return DRADD_ERR_BAD_CONFIG;  // bulk copies read device memory only
+        const int Kw = cfg.blocks_per_thread;
+        const int threads = 32 * cfg.rows_per_cta;
+        const size_t dyn_w = dradd::warp_smem_bytes(cfg.stages, cfg.rows_per_cta, static_cast<int>(hidden), add);
+        int grid = cfg.grid_ctas;
+        const int64_t groups = (n_rows + cfg.rows_per_cta - 1) / cfg.rows_per_cta;
+        if (auto_grid) {
+            int per_sm = 0;
+            if (dradd::warp_occupancy(Kw, out_kind, add, threads, dyn_w, &per_sm) != cudaSuccess)
+                return DRADD_ERR_CUDA;
+            int64_t g = static_cast<int64_t>(L.sm_count) * (per_sm > 0 ? per_sm : 1);
+            if (g > groups)
+                g = groups;
+            grid = static_cast<int>(g);
+        }
+        Params p = {};
+        p.out = out;
+        p.out_q = out_q;
+        p.scale = scale;
+        p.residual_out = residual_out;
+        p.x = x;
+        p.residual = residual;
+        p.weight = weight;
+        p.eps = eps;
+        p.hidden = static_cast<int>(hidden);
+        p.inv_hidden = is_pow2(hidden) ? 1.0f / static_cast<float>(hidden) : 0.0f;
+        p.n_rows = n_rows;
+        p.threads_per_row = 32;
+        p.rows_per_cta = cfg.rows_per_cta;
+        p.stages = cfg.stages;
+        p.fault_inject = cfg.fault_inject;
+        p.wait_limit_ns = cfg.wait_limit_us > 0 ? static_cast<uint64_t>(cfg.wait_limit_us) * 1000ull
+                                                : kDefaultWaitLimitNs;
+        p.l2_prefetch = 1;
+        if (dradd::device_status_ptr(&p.status) != cudaSuccess)
+            return DRADD_ERR_CUDA;
+        return dradd::launch_warp(p, Kw, out_kind, add, grid, threads, dyn_w, cfg.serialize != 0, stream) ==
+                       cudaSuccess
+                   ? DRADD_OK
+                   : DRADD_ERR_CUDA;
+    }
     if (cfg.variant == DRADD_VARIANT_SPLIT) {
         const int C = cfg.cluster_ctas;
         const int Ks = cfg.blocks_per_thread;
@@ -549,7 +633,7 @@ struct QkSide {
 struct QkLaunch {
     QkSide q, k;
     int threads = 0;
-    bool staged = false, serialize = false;
+    bool staged = false, warp = false, serialize = false;
     int64_t dyn_smem = 0;
 };
 
@@ -563,6 +647,77 @@ dradd_status qk_check_side(int64_t n_rows, int64_t hidden)
         return DRADD_ERR_UNSUPPORTED_HIDDEN;
     if (n_rows > (INT64_MAX / 4) / hidden)
         return DRADD_ERR_BAD_SHAPE;
+    return DRADD_OK;
+}
+
+// The warp-per-row plan of the fused q/k call (DRADD_VARIANT_WARP): each
+// side one warp a row, K = P / 256 blocks of 8 per lane (1..8, so
+// 256 <= P <= 2048 on both sides), threads_per_row read as the threads of a
+// CTA (a multiple of 32 up to 256, 0 = 256: one row of each side per warp
+// and stage), stages per side (0 = 2); CTAs split between the sides as in
+// qk_plan.  Dynamic shared memory: the larger side's warp_smem_bytes.
+dradd_status qk_plan_warp(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, bool add, int sm_count,
+                          int ctas_per_sm, int smem_optin, const dradd_launch_cfg& cfg, QkLaunch* out)
+{
+    QkSide* q = &out->q;
+    QkSide* k = &out->k;
+    if (cfg.rows_per_cta != 0 || cfg.fault_inject < 0 || cfg.blocks_per_thread != 0 || cfg.cluster_ctas != 0 ||
+        cfg.grid_ctas < 0 || cfg.wait_limit_us < 0 || cfg.stages < 0 || cfg.stages > 8 ||
+        (cfg.serialize != 0 && cfg.serialize != 1))
+        return DRADD_ERR_BAD_CONFIG;
+    const int64_t B = cfg.threads_per_row != 0 ? cfg.threads_per_row : 256;
+    if (B < 32 || B > 256 || B % 32 != 0)
+        return DRADD_ERR_BAD_CONFIG;
+    out->warp = true;
+    out->staged = false;
+    out->serialize = cfg.serialize != 0;
+    const int S = cfg.stages != 0 ? cfg.stages : 2;
+    for (QkSide* side : {q, k}) {
+        if (!side->active)
+            continue;
+        const int64_t blocks = next_pow2(side->hidden) / 8;
+        if (blocks < 32 || blocks / 32 > 8)
+            return DRADD_ERR_BAD_CONFIG;
+        side->K = static_cast<int>(blocks / 32);
+        side->T = 32;
+        side->R = static_cast<int>(B / 32);
+        side->stages = S;
+        const int64_t need = static_cast<int64_t>(
+            dradd::warp_smem_bytes(S, side->R, static_cast<int>(side->hidden), side == q && add));
+        if (need > smem_optin - 1024)
+            return DRADD_ERR_BAD_CONFIG;
+        if (need > out->dyn_smem)
+            out->dyn_smem = need;
+    }
+    const int64_t need_q = q->active ? (n_q + q->R - 1) / q->R : 0;
+    const int64_t need_k = k->active ? (n_k + k->R - 1) / k->R : 0;
+    int64_t C = cfg.grid_ctas;
+    if (C == 0)
+        C = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * (ctas_per_sm > 0 ? ctas_per_sm : 2048 / B);
+    if (C < (q->active ? 1 : 0) + (k->active ? 1 : 0))
+        return DRADD_ERR_BAD_CONFIG;
+    if (need_q + need_k <= C) {
+        q->ctas = need_q;
+        k->ctas = need_k;
+    } else {
+        const double wq = q->active ? static_cast<double>(n_q) * static_cast<double>(hq) : 0.0;
+        const double wk = k->active ? static_cast<double>(n_k) * static_cast<double>(hk) : 0.0;
+        int64_t cq = q->active ? static_cast<int64_t>(static_cast<double>(C) * wq / (wq + wk) + 0.5) : 0;
+        if (q->active && cq < 1)
+            cq = 1;
+        if (k->active && cq > C - 1)
+            cq = C - 1;
+        if (cq > need_q)
+            cq = need_q;
+        int64_t ck = C - cq;
+        if (ck > need_k)
+            ck = need_k;
+        q->ctas = cq;
+        k->ctas = ck;
+    }
+    if (q->ctas + k->ctas > 0x7FFFFFFF)
+        return DRADD_ERR_BAD_CONFIG;
+    out->threads = static_cast<int>(B);
     return DRADD_OK;
 }
 
@@ -605,6 +760,10 @@ dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t g
     dradd_launch_cfg cfg = {};
     if (cfg_in)
         cfg = *cfg_in;
+    if (cfg.variant == DRADD_VARIANT_WARP)
+        return (q->active || k->active)
+                   ? qk_plan_warp(n_q, hq, n_k, hk, add, sm_count, ctas_per_sm, smem_optin, cfg, out)
+                   : DRADD_OK;
     if (cfg.variant < DRADD_VARIANT_AUTO || cfg.variant > DRADD_VARIANT_STAGED || cfg.rows_per_cta != 0 ||
         cfg.stages < 0 || cfg.stages > 8 || cfg.fault_inject < 0 || cfg.wait_limit_us < 0 || cfg.grid_ctas < 0 ||
         (cfg.serialize != 0 && cfg.serialize != 1) ||
@@ -816,6 +975,8 @@ dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dra
     if (!device_memory) {
         if (eff.variant == DRADD_VARIANT_STAGED || eff.stages != 0 || eff.fault_inject != 0)
             return DRADD_ERR_BAD_CONFIG;
+        if (eff.variant == DRADD_VARIANT_WARP)
+            return DRADD_ERR_BAD_CONFIG;  // bulk copies read device memory only
         eff.variant = DRADD_VARIANT_ROWS;
     }
     cfg = &eff;
@@ -823,10 +984,11 @@ dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dra
     if (st != DRADD_OK)
         return st;
     const int kq = qa ? plan.q.K : 1, kk = ka ? plan.k.K : 1;
-    if (plan.staged && (!cfg || cfg->grid_ctas == 0)) {
+    const int mode = plan.warp ? dradd::kQkWarp : plan.staged ? dradd::kQkStaged : dradd::kQkRows;
+    if ((plan.staged || plan.warp) && (!cfg || cfg->grid_ctas == 0)) {
         // persistent grid: as many CTAs as fit on the device at once
         int per_sm = 0;
-        if (dradd::qk_occupancy(kq, kk, quant, add, true, plan.threads, static_cast<size_t>(plan.dyn_smem),
+        if (dradd::qk_occupancy(kq, kk, quant, add, mode, plan.threads, static_cast<size_t>(plan.dyn_smem),
                                 &per_sm) != cudaSuccess)
             return DRADD_ERR_CUDA;
         st = qk_plan(n_q, hq, n_k, hk, group_size, add, L.sm_count, per_sm > 0 ? per_sm : 1,
@@ -873,7 +1035,7 @@ dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dra
     Params pk = params(plan.k, k, nullptr, k_weight, k_eps);
     pk.out = k_out;
     const cudaError_t e =
-        dradd::launch_qk(pq, pk, kq, kk, quant, add, plan.staged, static_cast<int>(plan.q.ctas),
+        dradd::launch_qk(pq, pk, kq, kk, quant, add, mode, static_cast<int>(plan.q.ctas),
                          static_cast<int>(plan.k.ctas), plan.threads, static_cast<size_t>(plan.dyn_smem),
                          plan.serialize, stream);
     return e == cudaSuccess ? DRADD_OK : DRADD_ERR_CUDA;
@@ -1257,7 +1419,8 @@ dradd_status dradd_qk_resolve_config(int64_t n_q_rows, int64_t q_hidden, int64_t
                                     L.sm_count, 0, L.smem_per_block_optin, cfg, &r);
     if (st != DRADD_OK)
         return st;
-    plan->variant = r.threads == 0 ? 0 : (r.staged ? DRADD_VARIANT_STAGED : DRADD_VARIANT_ROWS);
+    plan->variant = r.threads == 0 ? 0
+                    : (r.warp ? DRADD_VARIANT_WARP : r.staged ? DRADD_VARIANT_STAGED : DRADD_VARIANT_ROWS);
     plan->threads_per_cta = r.threads;
     plan->dyn_smem_bytes = static_cast<int>(r.dyn_smem);
     plan->q_threads_per_row = r.q.T;

@@ -299,6 +299,50 @@ __device__ __forceinline__ float max_abs_nan(float a, float b)
     return d;
 }
 
+// max |y| over K blocks of 8 as a balanced tree (the maximum is exact, so
+// any order gives the same value; the tree keeps the dependent chain short).
+// NAN_PROP: a NaN anywhere gives NaN (max.NaN), else NaN is ignored.
+template <bool NAN_PROP>
+__device__ __forceinline__ float max2_abs(float a, float b)
+{
+    float d;
+    if constexpr (NAN_PROP)
+        asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(fabsf(a)), "f"(fabsf(b)));
+    else
+        d = fmaxf(fabsf(a), fabsf(b));
+    return d;
+}
+
+template <bool NAN_PROP>
+__device__ __forceinline__ float max2(float a, float b)
+{
+    float d;
+    if constexpr (NAN_PROP)
+        asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    else
+        d = fmaxf(a, b);
+    return d;
+}
+
+template <int K, bool NAN_PROP>
+__device__ __forceinline__ float tree_max_abs(const float (&y)[K][8])
+{
+    float m[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        const float a = max2<NAN_PROP>(max2_abs<NAN_PROP>(y[j][0], y[j][1]), max2_abs<NAN_PROP>(y[j][2], y[j][3]));
+        const float b = max2<NAN_PROP>(max2_abs<NAN_PROP>(y[j][4], y[j][5]), max2_abs<NAN_PROP>(y[j][6], y[j][7]));
+        m[j] = max2<NAN_PROP>(a, b);
+    }
+#pragma unroll
+    for (int width = 1; width < K; width *= 2) {
+#pragma unroll
+        for (int j = 0; j < K; j += 2 * width)
+            m[j] = max2<NAN_PROP>(m[j], m[j + width]);
+    }
+    return m[0];
+}
+
 // y = (acc * inv) * w for one block, with its 8 weights already in fp32
 // (w_lo: elements 0-3, w_hi: 4-7).
 __device__ __forceinline__ void scale8_f32(float (&a)[8], float inv, const float4& w_lo, const float4& w_hi)
@@ -460,7 +504,7 @@ __device__ __forceinline__ Int8Bracket make_int8_bracket(float scale)
 __device__ __forceinline__ uint2 quantize8_bracket(const float (&y)[8], const Int8Bracket& s, uint32_t& differ)
 {
     constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-    uint32_t lo[8];
+    uint32_t lo[8], d[4];
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
         float l0, l1, h0, h1;
@@ -468,9 +512,9 @@ __device__ __forceinline__ uint2 quantize8_bracket(const float (&y)[8], const In
         fma2_rn(y[e], y[e + 1], s.c_hi, s.c_hi, kRound, kRound, h0, h1);
         lo[e] = __float_as_uint(l0);
         lo[e + 1] = __float_as_uint(l1);
-        differ |= lo[e] ^ __float_as_uint(h0);
-        differ |= lo[e + 1] ^ __float_as_uint(h1);
+        d[e / 2] = (lo[e] ^ __float_as_uint(h0)) | (lo[e + 1] ^ __float_as_uint(h1));
     }
+    differ |= (d[0] | d[1]) | (d[2] | d[3]);
     uint2 u;
     u.x = pack4_low_bytes(lo[0], lo[1], lo[2], lo[3]);
     u.y = pack4_low_bytes(lo[4], lo[5], lo[6], lo[7]);

@@ -90,6 +90,22 @@ KernelFn staged_fn_norm_bf16(int T, int K);
 KernelFn staged_fn_norm_int8(int T, int K);
 KernelFn staged_fn_norm_e4m3(int T, int K);
 KernelFn staged_fn_norm_e2m1(int T, int K);
+// Warp-per-row kernels: K = P / 256 blocks of 8 per lane (1..16; with a
+// residual 1..8), one warp per row, R warps per CTA (R adjacent rows per
+// stage; at most kWarpMaxRows), `stages` stages.  Dynamic shared memory:
+// the stages, the fp32 weights and one mbarrier per stage.
+constexpr int kWarpMaxRows = 16;
+constexpr size_t warp_smem_bytes(int stages, int rows, int hidden, bool add)
+{
+    return static_cast<size_t>(stages) * (add ? 2u : 1u) * static_cast<size_t>(rows) * 2u *
+               static_cast<size_t>(hidden) +
+           4u * static_cast<size_t>(hidden) + 8u * static_cast<size_t>(stages);
+}
+KernelFn warp_fn_add(int out, int K);
+KernelFn warp_fn_norm(int out, int K);
+cudaError_t launch_warp(const Params& p, int K, int out, bool add, int grid, int threads, size_t dyn_smem,
+                        bool serialize, cudaStream_t stream);
+cudaError_t warp_occupancy(int K, int out, bool add, int threads, size_t dyn_smem, int* blocks_per_sm);
 // Split-row kernels (bf16 out): clusters of C CTAs (2 or 4), each CTA a
 // slice of every row of its cluster; grid a multiple of C.
 KernelFn split_fn_add(int T, int K, int C);
@@ -102,14 +118,18 @@ size_t split_static_smem(int K);
 // k rows; kq / kk blocks of 8 per thread on each side.  quant: per-group
 // e4m3 q out (else bf16); add: q has a residual; staged: rows staged
 // through dyn_smem bytes of shared memory (else loaded into registers).
-cudaError_t launch_qk(const Params& pq, const Params& pk, int kq, int kk, bool quant, bool add, bool staged,
+// mode: how each side's rows reach the registers.
+enum QkMode : int { kQkRows = 0, kQkStaged = 1, kQkWarp = 2 };
+cudaError_t launch_qk(const Params& pq, const Params& pk, int kq, int kk, bool quant, bool add, int mode,
                       int q_ctas, int k_ctas, int threads, size_t dyn_smem, bool serialize, cudaStream_t stream);
-cudaError_t qk_occupancy(int kq, int kk, bool quant, bool add, bool staged, int threads, size_t dyn_smem,
+cudaError_t qk_occupancy(int kq, int kk, bool quant, bool add, int mode, int threads, size_t dyn_smem,
                          int* blocks_per_sm);
 QkKernelFn qk_fn_bf16_rows(int kq, int kk, bool add);
 QkKernelFn qk_fn_bf16_staged(int kq, int kk, bool add);
 QkKernelFn qk_fn_e4m3_rows(int kq, int kk, bool add);
 QkKernelFn qk_fn_e4m3_staged(int kq, int kk, bool add);
+QkKernelFn qk_fn_bf16_warp(int kq, int kk, bool add);
+QkKernelFn qk_fn_e4m3_warp(int kq, int kk, bool add);
 // Static shared memory of a qk kernel whose sides have kq / kk blocks per thread.
 size_t qk_static_smem(int kq, int kk);
 // l2_prefetch: all three are device memory (each CTA's first vectors are

@@ -284,6 +284,60 @@ cudaError_t split_max_clusters(int K, int C, bool add, int threads, size_t dyn_s
     return cudaOccupancyMaxActiveClusters(clusters, fn, &cfg);
 }
 
+// One bit per warp kernel (add, out = 0..3, K = 1..16): its dynamic shared
+// memory limit has been raised to the device's opt-in maximum.
+std::atomic<uint64_t> g_warp_smem_done[kMaxDevices];
+
+cudaError_t warp_prepare(KernelFn fn, int K, int out, bool add)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const uint64_t bit = 1ull << (((add ? 4 : 0) + out) * 5 + log2i(K));
+    std::atomic<uint64_t>* word = dev >= 0 && dev < kMaxDevices ? &g_warp_smem_done[dev] : nullptr;
+    if (word && (word->load(std::memory_order_acquire) & bit))
+        return cudaSuccess;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess)
+        return e;
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, fn);
+    if (e != cudaSuccess)
+        return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - static_cast<int>(attr.sharedSizeBytes));
+    if (e != cudaSuccess)
+        return e;
+    if (word)
+        word->fetch_or(bit, std::memory_order_acq_rel);
+    return cudaSuccess;
+}
+
+cudaError_t launch_warp(const Params& p, int K, int out, bool add, int grid, int threads, size_t dyn_smem,
+                        bool serialize, cudaStream_t stream)
+{
+    KernelFn fn = add ? warp_fn_add(out, K) : warp_fn_norm(out, K);
+    if (!fn)
+        return cudaErrorInvalidValue;
+    cudaError_t e = warp_prepare(fn, K, out, add);
+    if (e != cudaSuccess)
+        return e;
+    return launch(fn, grid, threads, dyn_smem, serialize, stream, p);
+}
+
+cudaError_t warp_occupancy(int K, int out, bool add, int threads, size_t dyn_smem, int* blocks_per_sm)
+{
+    KernelFn fn = add ? warp_fn_add(out, K) : warp_fn_norm(out, K);
+    if (!fn)
+        return cudaErrorInvalidValue;
+    cudaError_t e = warp_prepare(fn, K, out, add);
+    if (e != cudaSuccess)
+        return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, threads, dyn_smem);
+}
+
 cudaError_t staged_occupancy(int K, int out, bool add, int threads, size_t dyn_smem, int* blocks_per_sm)
 {
     KernelFn fn = staged_fn(threads, K, out, add);
@@ -314,27 +368,32 @@ size_t staged_static_smem(int K)
 
 namespace {
 
-QkKernelFn qk_fn(int kq, int kk, bool quant, bool add, bool staged)
+QkKernelFn qk_fn(int kq, int kk, bool quant, bool add, int mode)
 {
+    if (mode == kQkWarp)
+        return quant ? qk_fn_e4m3_warp(kq, kk, add) : qk_fn_bf16_warp(kq, kk, add);
+    const bool staged = mode == kQkStaged;
     if (quant)
         return staged ? qk_fn_e4m3_staged(kq, kk, add) : qk_fn_e4m3_rows(kq, kk, add);
     return staged ? qk_fn_bf16_staged(kq, kk, add) : qk_fn_bf16_rows(kq, kk, add);
 }
 
-// One bit per staged qk kernel (kq, kk, quant, add): its dynamic shared
-// memory limit has been raised to the device's opt-in maximum.
-std::atomic<uint64_t> g_qk_smem_done[kMaxDevices];
+// One bit per staged (word 0) or warp-per-row (word 1) qk kernel (kq, kk,
+// quant, add): its dynamic shared memory limit has been raised to the
+// device's opt-in maximum.
+std::atomic<uint64_t> g_qk_smem_done[kMaxDevices][2];
 
-cudaError_t qk_prepare(QkKernelFn fn, int kq, int kk, bool quant, bool add, bool staged)
+cudaError_t qk_prepare(QkKernelFn fn, int kq, int kk, bool quant, bool add, int mode)
 {
-    if (!staged)
+    if (mode == kQkRows)
         return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     const uint64_t bit = 1ull << (((log2i(kq) * 4 + log2i(kk)) * 2 + (quant ? 1 : 0)) * 2 + (add ? 1 : 0));
-    std::atomic<uint64_t>* word = dev >= 0 && dev < kMaxDevices ? &g_qk_smem_done[dev] : nullptr;
+    std::atomic<uint64_t>* word =
+        dev >= 0 && dev < kMaxDevices ? &g_qk_smem_done[dev][mode == kQkWarp ? 1 : 0] : nullptr;
     if (word && (word->load(std::memory_order_acquire) & bit))
         return cudaSuccess;
     int optin = 0;
@@ -362,25 +421,25 @@ size_t qk_static_smem(int kq, int kk)
     return sizeof(float) * (2 * 32 * static_cast<size_t>(kq + kk) + 4 * 32);
 }
 
-cudaError_t launch_qk(const Params& pq, const Params& pk, int kq, int kk, bool quant, bool add, bool staged,
+cudaError_t launch_qk(const Params& pq, const Params& pk, int kq, int kk, bool quant, bool add, int mode,
                       int q_ctas, int k_ctas, int threads, size_t dyn_smem, bool serialize, cudaStream_t stream)
 {
-    QkKernelFn fn = qk_fn(kq, kk, quant, add, staged);
+    QkKernelFn fn = qk_fn(kq, kk, quant, add, mode);
     if (!fn)
         return cudaErrorInvalidValue;
-    cudaError_t e = qk_prepare(fn, kq, kk, quant, add, staged);
+    cudaError_t e = qk_prepare(fn, kq, kk, quant, add, mode);
     if (e != cudaSuccess)
         return e;
     return launch(fn, q_ctas + k_ctas, threads, dyn_smem, serialize, stream, pq, pk, q_ctas);
 }
 
-cudaError_t qk_occupancy(int kq, int kk, bool quant, bool add, bool staged, int threads, size_t dyn_smem,
+cudaError_t qk_occupancy(int kq, int kk, bool quant, bool add, int mode, int threads, size_t dyn_smem,
                          int* blocks_per_sm)
 {
-    QkKernelFn fn = qk_fn(kq, kk, quant, add, staged);
+    QkKernelFn fn = qk_fn(kq, kk, quant, add, mode);
     if (!fn)
         return cudaErrorInvalidValue;
-    cudaError_t e = qk_prepare(fn, kq, kk, quant, add, staged);
+    cudaError_t e = qk_prepare(fn, kq, kk, quant, add, mode);
     if (e != cudaSuccess)
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, threads, dyn_smem);

@@ -343,12 +343,7 @@ __device__ __forceinline__ void staged_quant_row(const Params& p, const float (&
     if constexpr (OUT == kOutInt8) {
         // amax with NaN propagation: a row holding a NaN y shows as a NaN
         // amax and takes the exact path (whose amax ignores NaN).
-        float m = 0.0f;
-#pragma unroll
-        for (int j = 0; j < K; ++j)
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                m = max_abs_nan(m, y[j][e]);
+        float m = tree_max_abs<K, true>(y);
         m = butterfly_max_nan(m, 32);
         if constexpr (W > 1) {
             if (lane == 0)
@@ -375,12 +370,7 @@ __device__ __forceinline__ void staged_quant_row(const Params& p, const float (&
             }
         } else {
             // uniform over the CTA: every thread holds the same m
-            float m2 = 0.0f;
-#pragma unroll
-            for (int j = 0; j < K; ++j)
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    m2 = fmaxf(m2, fabsf(y[j][e]));
+            float m2 = fmaxf(0.0f, tree_max_abs<K, false>(y));  // NaN ignored, as a running max from 0
             m2 = butterfly_max(m2, 32);
             if constexpr (W > 1) {
                 if (lane == 0)
@@ -399,12 +389,7 @@ __device__ __forceinline__ void staged_quant_row(const Params& p, const float (&
             }
         }
     } else {
-        float m = 0.0f;
-#pragma unroll
-        for (int j = 0; j < K; ++j)
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                m = fmaxf(m, fabsf(y[j][e]));
+        float m = fmaxf(0.0f, tree_max_abs<K, false>(y));  // NaN ignored, as a running max from 0
         m = butterfly_max(m, 32);
         if constexpr (W > 1) {
             if (lane == 0)

@@ -8,6 +8,7 @@
 #pragma once
 
 #include "dradd_kernels.cuh"
+#include "dradd_warp.cuh"
 
 namespace dradd {
 
@@ -330,6 +331,43 @@ __global__ void __launch_bounds__(qk_max_threads(KQ > KK ? KQ : KK))
         else
             rows_body_contig<KK, kOutBf16, false>(pk, cta - q_ctas, k_ctas);
     }
+}
+
+// ------------------------------------------------------------- qk_warp_kernel
+// Fused q/k RMSNorm, one warp per row (warp_body): CTAs [0, q_ctas) take the
+// q rows, the rest the k rows, each side with its own stages and weights
+// (dynamic shared memory: the larger side's warp_smem_bytes).
+template <int KQ, int KK, bool QQUANT, bool QADD>
+__global__ void __launch_bounds__(256, 1) qk_warp_kernel(const Params pq, const Params pk, int q_ctas)
+{
+    extern __shared__ __align__(128) unsigned char wsm[];
+    constexpr int QOUT = QQUANT ? kOutE4m3Group : kOutBf16;
+    const int cta = static_cast<int>(blockIdx.x);
+    if (cta < q_ctas)
+        warp_body<KQ, QOUT, QADD>(pq, cta, q_ctas, wsm);
+    else
+        warp_body<KK, kOutBf16, false>(pk, cta - q_ctas, static_cast<int64_t>(gridDim.x) - q_ctas, wsm);
+}
+
+template <bool QQUANT, bool QADD>
+QkKernelFn qk_warp_table(int kq, int kk)
+{
+#define DRADD_QK_WARP_KK(KQV)                                         \
+    switch (kk) {                                                     \
+    case 1: return qk_warp_kernel<KQV, 1, QQUANT, QADD>;              \
+    case 2: return qk_warp_kernel<KQV, 2, QQUANT, QADD>;              \
+    case 4: return qk_warp_kernel<KQV, 4, QQUANT, QADD>;              \
+    case 8: return qk_warp_kernel<KQV, 8, QQUANT, QADD>;              \
+    default: return nullptr;                                          \
+    }
+    switch (kq) {
+    case 1: DRADD_QK_WARP_KK(1)
+    case 2: DRADD_QK_WARP_KK(2)
+    case 4: DRADD_QK_WARP_KK(4)
+    case 8: DRADD_QK_WARP_KK(8)
+    default: return nullptr;
+    }
+#undef DRADD_QK_WARP_KK
 }
 
 template <int KQ, bool QQUANT, bool QADD, bool STAGED>

@@ -181,8 +181,22 @@ dradd_status add_rmsnorm_quant_fwd(int8_t* out_q, float* scale, dradd_bf16* resi
  *                    are added in the same tree order.  bf16 output only
  *                    (the quantised entry points reject it); grid_ctas a
  *                    multiple of C.
+ *
+ * DRADD_VARIANT_WARP: one warp per row (threads_per_row 32, or 0), lane l
+ * owning blocks l, l + 32, ... (K = P / 256, so 256 <= P <= 4096, and with
+ * a residual P <= 2048); rows loaded straight into registers, the row's
+ * reductions within the warp, the weights widened once per CTA into shared
+ * memory.  rows_per_cta: warps per CTA (0 = 8, or 4 at P = 4096; at most
+ * that); grid_ctas: 0 = as many CTAs as fit on the device at once (at most
+ * one per rows_per_cta rows).  stages and fault_inject must be 0.
  */
-enum { DRADD_VARIANT_AUTO = 0, DRADD_VARIANT_ROWS = 1, DRADD_VARIANT_STAGED = 2, DRADD_VARIANT_SPLIT = 3 };
+enum {
+    DRADD_VARIANT_AUTO = 0,
+    DRADD_VARIANT_ROWS = 1,
+    DRADD_VARIANT_STAGED = 2,
+    DRADD_VARIANT_SPLIT = 3,
+    DRADD_VARIANT_WARP = 4
+};
 
 typedef struct dradd_launch_cfg {
     int variant;
@@ -411,7 +425,11 @@ dradd_status fused_qk_rmsnorm_group_quant_fwd(void* q_out, float* q_scale, dradd
  * shared by the two sides.  stages (staged only): stages per side, 1..8.
  * fault_inject, wait_limit_us and serialize as for
  * add_rmsnorm_fwd_with_config (staged only for the first two);
- * rows_per_cta must be 0.  Results never depend on it.
+ * rows_per_cta must be 0.  WARP: one warp per row on both sides, each lane
+ * owning blocks l, l + 32, ... of its row (both sides 256 <= P <= 2048),
+ * threads_per_row read as the threads of a CTA (a multiple of 32 up to 256,
+ * 0 = 256), blocks_per_thread, stages and fault_inject 0.  Results never
+ * depend on it.
  */
 dradd_status fused_qk_rmsnorm_group_quant_fwd_with_config(
     void* q_out, float* q_scale, dradd_bf16* q_residual_out, dradd_bf16* k_out, const dradd_bf16* q,
@@ -421,9 +439,9 @@ dradd_status fused_qk_rmsnorm_group_quant_fwd_with_config(
 
 /* The launch plan of a fused q/k call (for tests and reports). */
 typedef struct dradd_qk_plan {
-    int variant;          /* DRADD_VARIANT_ROWS or _STAGED (0 for an empty call) */
+    int variant;          /* DRADD_VARIANT_ROWS, _STAGED or _WARP (0 for an empty call) */
     int threads_per_cta;
-    int dyn_smem_bytes;   /* staged: shared memory for the stages */
+    int dyn_smem_bytes;   /* staged: shared memory for the stages; warp: for the fp32 weights */
     int q_threads_per_row, q_rows_per_cta, q_stages, q_ctas;  /* 0 when n_q_rows == 0 */
     int k_threads_per_row, k_rows_per_cta, k_stages, k_ctas;  /* 0 when n_k_rows == 0 */
 } dradd_qk_plan;

@@ -79,6 +79,23 @@ def test_parity(orc, case):
     assert dr.device_status() == 0
 
 
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:5])) + ("r" if c[5] else ""))
+def test_parity_warp_rows(orc, case):
+    """The warp-per-row mode on every case whose two sides it takes (both
+    256 <= P <= 2048)."""
+    nq, hq, nk, hk, group, with_res, qe, ke = case
+    cfg = dr.LaunchConfig(variant=dr.VARIANT_WARP)
+    try:
+        dr.qk_resolve_config(nq, hq, nk, hk, group, q_residual=with_res, config=cfg)
+    except dr.DraddError as e:
+        assert e.status == 9
+        pytest.skip("a side outside 256 <= P <= 2048")
+    q, r, qw, k, kw = make(hash(case) % 1000 + 1, nq, hq, nk, hk, with_res)
+    got = run_gpu(q, r, qw, k, kw, group, qe, ke, config=cfg)
+    compare(orc, q, r, qw, k, kw, group, qe, ke, got, what="warp")
+    assert dr.device_status() == 0
+
+
 CONFIGS = ([None] +
            [dr.LaunchConfig(variant=1, threads_per_row=B, grid_ctas=G)
             for B in (64, 128, 256, 512) for G in (0, 2, 7, 1000)] +
@@ -86,6 +103,8 @@ CONFIGS = ([None] +
             for B, G, S in ((64, 0, 1), (128, 2, 2), (256, 7, 3), (512, 0, 4), (128, 1000, 8), (256, 3, 1))] +
            [dr.LaunchConfig(variant=v, threads_per_row=128, blocks_per_thread=K)
             for v in (1, 2) for K in (2, 4, 8)] +
+           [dr.LaunchConfig(variant=dr.VARIANT_WARP, threads_per_row=B, grid_ctas=G)
+            for B in (64, 256) for G in (0, 3)] +
            [dr.LaunchConfig(serialize=1), dr.LaunchConfig(variant=1, serialize=1)])
 
 
@@ -167,7 +186,8 @@ def test_zero_groups_and_tiny_scales(orc):
         assert np.all(s[5] == 0)
 
 
-def test_bounded_wait_expires_and_recovers(orc):
+@pytest.mark.parametrize("variant", [2, dr.VARIANT_WARP])
+def test_bounded_wait_expires_and_recovers(orc, variant):
     """fault_inject withholds each CTA's first staged copy on both sides:
     every wait runs out after wait_limit_us, the kernel records
     DRADD_ERR_TIMEOUT, drains its other copies and returns; the context
@@ -176,7 +196,7 @@ def test_bounded_wait_expires_and_recovers(orc):
     assert dr.device_status(clear=True) == 0
     q, r, qw, k, kw = make(15, 64, 1536, 64, 512, True)
     qd, rd, qwd, kd, kwd = (t.to(d) for t in (q, r, qw, k, kw))
-    cfg = dr.LaunchConfig(variant=2, stages=3, grid_ctas=8, fault_inject=1, wait_limit_us=20000)
+    cfg = dr.LaunchConfig(variant=variant, stages=3, grid_ctas=8, fault_inject=1, wait_limit_us=20000)
     dr.fused_qk_rmsnorm_group_quant_fwd(qd, qwd, kd, kwd, 1e-6, 1e-6, group_size=128, q_residual=rd, config=cfg)
     assert dr.device_status(clear=True) == 8
     assert dr.device_status(clear=True) == 0
