@@ -265,7 +265,8 @@ dradd_status resolve_split(int64_t n_rows, int64_t hidden, bool quant, bool add,
 // rows_per_cta warps (and rows per stage) per CTA, `stages` stages.
 // Automatic: the most warps (up to kWarpMaxRows) for which 2 stages fit in
 // one CTA's shared memory, 2 stages.
-dradd_status resolve_warp(int64_t hidden, bool add, const DeviceLimits& L, dradd_launch_cfg* cfg)
+dradd_status resolve_warp(int64_t n_rows, int64_t hidden, bool add, const DeviceLimits& L,
+                           dradd_launch_cfg* cfg)
 {
     const int64_t blocks = next_pow2(hidden) / 8;
     if (blocks < 32 || blocks / 32 > 16 || (add && blocks / 32 > 8))
@@ -290,9 +291,23 @@ dradd_status resolve_warp(int64_t hidden, bool add, const DeviceLimits& L, dradd
     }
     if (cfg->stages == 0)
         cfg->stages = S0;
-    if (static_cast<int64_t>(dradd::warp_smem_bytes(cfg->stages, cfg->rows_per_cta, static_cast<int>(hidden),
-                                                    add)) > limit)
+    const int64_t smem = static_cast<int64_t>(
+        dradd::warp_smem_bytes(cfg->stages, cfg->rows_per_cta, static_cast<int>(hidden), add));
+    if (smem > limit)
         return DRADD_ERR_BAD_CONFIG;
+    if (cfg->grid_ctas == 0) {
+        // as many CTAs as fit at once (the launch refines this with the
+        // kernel's occupancy), at most one per group of rows
+        int64_t per_sm = L.smem_per_sm / (smem + 1024);
+        const int64_t by_threads = L.max_threads_per_sm / (32 * cfg->rows_per_cta);
+        if (by_threads < per_sm)
+            per_sm = by_threads;
+        const int64_t groups = (n_rows + cfg->rows_per_cta - 1) / cfg->rows_per_cta;
+        int64_t grid = static_cast<int64_t>(L.sm_count) * (per_sm > 0 ? per_sm : 1);
+        if (grid > groups)
+            grid = groups;
+        cfg->grid_ctas = static_cast<int>(grid < 1 ? 1 : grid);
+    }
     return DRADD_OK;
 }
 
@@ -325,13 +340,51 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     //          (bf16 residual-add batches of 65..512 rows: T = 512, K = 2)
     //   16384  512   4  2                             4
     //   32768  512   8  1                             2
+    //
+    // Two shapes go elsewhere (same measurements):
+    //   - bf16 out, P = 32768 and at most 160 rows: the split-row cluster
+    //     variant, 4 CTAs a row up to 64 rows, else 2 (one row: 3.2 us
+    //     against 8.8 us staged; 152 rows: 10.5 against 11.4);
+    //   - 512 <= P <= 2048 with enough rows: the warp-per-row variant
+    //     (residual-add bf16 from 1024 rows, 4 warps and 3 stages: 4096 x
+    //     1024 in 5.27 us against 6.83; quantised residual-add from 2048
+    //     rows, up to 8192 at P = 2048, 4 warps and 2 stages; plain bf16
+    //     from 16384 rows, 8 warps and 3 stages; plain quantised at P <= 1024
+    //     from 8192 rows, 4 warps and 2 stages).
     const bool auto_variant = cfg->variant == DRADD_VARIANT_AUTO;
-    if (auto_variant)
+    if (auto_variant) {
         cfg->variant = hidden > 256 ? DRADD_VARIANT_STAGED : DRADD_VARIANT_ROWS;
+        const bool no_explicit = cfg->threads_per_row == 0 && cfg->rows_per_cta == 0 && cfg->stages == 0 &&
+                                 cfg->blocks_per_thread == 0 && cfg->fault_inject == 0 && cfg->cluster_ctas == 0;
+        if (no_explicit && !quant && P >= 32768 && n_rows <= 160) {
+            cfg->variant = DRADD_VARIANT_SPLIT;
+            cfg->cluster_ctas = n_rows <= 64 ? 4 : 2;
+        } else if (no_explicit && P >= 512 && P <= 2048) {
+            int R = 0, S = 0;
+            if (add && !quant && n_rows >= 1024) {
+                R = 4;
+                S = 3;
+            } else if (add && quant && n_rows >= 2048 && (P < 2048 || n_rows <= 8192)) {
+                R = 4;
+                S = 2;
+            } else if (!add && !quant && n_rows >= 16384) {
+                R = 8;
+                S = 3;
+            } else if (!add && quant && P <= 1024 && n_rows >= 8192) {
+                R = 4;
+                S = 2;
+            }
+            if (R != 0) {
+                cfg->variant = DRADD_VARIANT_WARP;
+                cfg->rows_per_cta = R;
+                cfg->stages = S;
+            }
+        }
+    }
     if (cfg->variant == DRADD_VARIANT_SPLIT)
         return resolve_split(n_rows, hidden, quant, add, L, cfg);
     if (cfg->variant == DRADD_VARIANT_WARP)
-        return resolve_warp(hidden, add, L, cfg);
+        return resolve_warp(n_rows, hidden, add, L, cfg);
     if (cfg->cluster_ctas != 0)
         return DRADD_ERR_BAD_CONFIG;
     if (cfg->variant != DRADD_VARIANT_ROWS && cfg->variant != DRADD_VARIANT_STAGED)

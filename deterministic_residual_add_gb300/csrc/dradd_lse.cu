@@ -122,6 +122,10 @@ __device__ __forceinline__ float unary1(float x, int op)
     return op == 0 ? log1pf(x) : op == 1 ? coshf(x) : expf(x);
 }
 
+// Grid strides ahead of its loads at which a merge CTA prefetches a unit
+// into L2.
+constexpr int64_t kLseL2Ahead = 1;
+
 // Rows of n_cols elements; a unit is `blockDim.x * VEC` consecutive columns
 // of one row, units_per_row of them per row; the grid strides over units
 // (in row-major unit order).  In a whole unit of 16-byte aligned rows
@@ -160,7 +164,31 @@ __global__ void __launch_bounds__(1024) lse_merge_kernel(float* out, int64_t out
     const int64_t step_cb = gridDim.x - step_rows * units_per_row;
     int64_t row = blockIdx.x / units_per_row;
     int64_t cb = blockIdx.x - row * units_per_row;
+    // The unit kLseL2Ahead grid strides ahead, walked the same way: thread 0
+    // prefetches it into L2 (a hint; whole 16-byte units of device memory
+    // only), so more bytes are on their way than the registers hold.  Only
+    // thread 0 pays for locating it.
+    const int64_t first_ahead = static_cast<int64_t>(blockIdx.x) + kLseL2Ahead * static_cast<int64_t>(gridDim.x);
+    const bool ahead_on =
+        l2_prefetch && vec4 && threadIdx.x == 0 && kLseL2Ahead > 0 && first_ahead < n_rows * units_per_row;
+    int64_t ahead_row = n_rows, ahead_cb = 0;
+    if (ahead_on) {
+        ahead_row = first_ahead / units_per_row;
+        ahead_cb = first_ahead - ahead_row * units_per_row;
+    }
     for (; row < n_rows; row += step_rows) {
+        if (ahead_on) {
+            if (ahead_row < n_rows && ahead_cb * span + span <= n_cols) {
+                prefetch_l2(a + ahead_row * a_stride + ahead_cb * span, static_cast<uint32_t>(span * 4));
+                prefetch_l2(b + ahead_row * b_stride + ahead_cb * span, static_cast<uint32_t>(span * 4));
+            }
+            ahead_row += step_rows;
+            ahead_cb += step_cb;
+            if (ahead_cb >= units_per_row) {
+                ahead_cb -= units_per_row;
+                ++ahead_row;
+            }
+        }
         const int64_t base = cb * span;
         const float* ar = a + row * a_stride + base;
         const float* br = b + row * b_stride + base;

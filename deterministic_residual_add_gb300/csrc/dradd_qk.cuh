@@ -152,6 +152,10 @@ __device__ __forceinline__ void tile_body(const Params& p, int64_t cta, int64_t 
     }
 }
 
+// Row steps ahead of its loads at which a register-variant CTA prefetches
+// its rows into L2.
+constexpr int64_t kQkL2Ahead = 4;
+
 // ----------------------------------------------------------- rows_body_contig
 // The register-load body with the contiguous mapping: thread t of a row owns
 // the K adjacent blocks tK .. tK + K - 1, an aligned subtree of 8K elements
@@ -228,6 +232,19 @@ __device__ __forceinline__ void rows_body_contig(const Params& p, int64_t cta, i
     load_row(cta * p.rows_per_cta + r_local, nxv, nrv);
     int buf = 0;
     for (int64_t base = cta * p.rows_per_cta; base < p.n_rows; base += rows_per_step) {
+        if (p.l2_prefetch && tid == 0) {
+            // the CTA's rows kQkL2Ahead steps ahead, into L2 (a hint: the
+            // registers already hold the next step's rows)
+            const int64_t ahead = base + kQkL2Ahead * rows_per_step;
+            if (ahead < p.n_rows) {
+                const int64_t left = p.n_rows - ahead;
+                const uint32_t bytes = static_cast<uint32_t>(p.hidden) * 2u *
+                                       static_cast<uint32_t>(left < p.rows_per_cta ? left : p.rows_per_cta);
+                prefetch_l2(p.x + ahead * p.hidden, bytes);
+                if constexpr (ADD)
+                    prefetch_l2(p.residual + ahead * p.hidden, bytes);
+            }
+        }
         const int64_t row = base + r_local;
         const bool active = row < p.n_rows;
 #pragma unroll

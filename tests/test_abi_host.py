@@ -117,7 +117,12 @@ def test_auto_config_covers_every_supported_hidden(L):
         K = P // 8 // T
         assert T * K * 8 == P and K in (1, 2, 4, 8)
         assert (T * R) % 32 == 0 and T * R <= (1024 if K <= 2 else 512)
-        assert c.variant == (dr.VARIANT_STAGED if h > 256 else dr.VARIANT_ROWS)
+        # 512 <= P <= 2048 with 4096 rows: the warp-per-row variant (one warp
+        # a row); longer rows staged, shorter ones in registers
+        assert c.variant == (dr.VARIANT_WARP if 256 < h <= 2048 else
+                             dr.VARIANT_STAGED if h > 256 else dr.VARIANT_ROWS)
+        if c.variant == dr.VARIANT_WARP:
+            assert (T, R, c.stages, c.blocks_per_thread) == (32, 4, 3, P // 256)
         if c.variant == dr.VARIANT_STAGED:
             assert 1 <= c.stages <= 8 and c.stages * 4 * h <= 232448
         assert c.grid_ctas >= 1
@@ -140,11 +145,20 @@ def test_auto_grid(L):
     assert c.grid_ctas % 152 == 0 or c.grid_ctas == 2048
     c = dr.resolve_config(4096, 8192, sm_count=152)
     assert (c.variant, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 1024, 2)
-    for h, T, S in [(264, 32, 4), (512, 32, 4), (1024, 64, 3), (2048, 128, 4)]:
+    for h in (264, 512, 1024, 2048):
         c = dr.resolve_config(4096, h, sm_count=152)
-        assert (c.threads_per_row, c.stages) == (T, S), h
-    c = dr.resolve_config(16384, 2048, sm_count=152)
-    assert (c.threads_per_row, c.stages) == (64, 3)
+        assert (c.variant, c.threads_per_row, c.rows_per_cta, c.stages) == (dr.VARIANT_WARP, 32, 4, 3), h
+    for h, T, S in [(264, 32, 4), (512, 32, 4), (1024, 64, 3), (2048, 128, 4)]:
+        c = dr.resolve_config(512, h, sm_count=152)  # fewer rows: staged
+        assert (c.variant, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, T, S), h
+    c = dr.resolve_config(16384, 2048, quant=True, sm_count=152)
+    assert (c.variant, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 64, 3)
+    # few rows of 32768: the split-row cluster variant (bf16 out only)
+    for n, C in ((1, 4), (64, 4), (65, 2), (160, 2)):
+        c = dr.resolve_config(n, 32768, sm_count=152)
+        assert (c.variant, c.cluster_ctas) == (dr.VARIANT_SPLIT, C), n
+    assert dr.resolve_config(161, 32768, sm_count=152).variant == dr.VARIANT_STAGED
+    assert dr.resolve_config(8, 32768, quant=True, sm_count=152).variant != dr.VARIANT_SPLIT
     c = dr.resolve_config(4096, 4096, add=False, sm_count=152)
     assert c.stages == 4
     c = dr.resolve_config(2048, 4096, add=False, sm_count=152)
@@ -179,8 +193,8 @@ def test_staged_stages_limited_by_shared_memory(L):
         dr.resolve_config(16, 32768, sm_count=152, config=dr.LaunchConfig(variant=2, stages=2))
     c = dr.resolve_config(16, 32768, sm_count=152, config=dr.LaunchConfig(variant=2))
     assert c.stages == 1
-    c = dr.resolve_config(16, 32768, sm_count=152)
-    assert c.stages == 1 and c.threads_per_row == 512
+    c = dr.resolve_config(200, 32768, sm_count=152)  # (16 rows would take the split variant)
+    assert c.variant == dr.VARIANT_STAGED and c.stages == 1 and c.threads_per_row == 512
 
 
 def test_binding_refuses_cpu_tensors():
