@@ -91,15 +91,16 @@ KernelFn staged_fn_norm_int8(int T, int K);
 KernelFn staged_fn_norm_e4m3(int T, int K);
 KernelFn staged_fn_norm_e2m1(int T, int K);
 // Warp-per-row kernels: K = P / 256 blocks of 8 per lane (1..16; with a
-// residual 1..8), one warp per row, R warps per CTA (R adjacent rows per
-// stage; at most kWarpMaxRows), `stages` stages.  Dynamic shared memory:
-// the stages, the fp32 weights and one mbarrier per stage.
+// residual 1..8), one warp per row, R warps per CTA (at most kWarpMaxRows),
+// `stages` groups of R rows (the main op) or a ring of `stages` row slots
+// per warp (the fused q/k call).  Dynamic shared memory: the row slots, the
+// fp32 weights and the mbarriers (one per slot at most).
 constexpr int kWarpMaxRows = 16;
 constexpr size_t warp_smem_bytes(int stages, int rows, int hidden, bool add)
 {
     return static_cast<size_t>(stages) * (add ? 2u : 1u) * static_cast<size_t>(rows) * 2u *
                static_cast<size_t>(hidden) +
-           4u * static_cast<size_t>(hidden) + 8u * static_cast<size_t>(stages);
+           4u * static_cast<size_t>(hidden) + 8u * static_cast<size_t>(stages) * static_cast<size_t>(rows);
 }
 KernelFn warp_fn_add(int out, int K);
 KernelFn warp_fn_norm(int out, int K);

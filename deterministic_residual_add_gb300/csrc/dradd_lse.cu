@@ -45,10 +45,20 @@ __device__ __forceinline__ float series_tail(float z)
     return __fmaf_rn(p, z, 0x1.555556p-2f); // 1/3
 }
 
+// The reciprocal approximation for an argument in [2, 3] (t = 2 + u): the
+// flush-to-zero form of rcp.approx, without the subnormal handling of the
+// plain form that a normal argument with a normal reciprocal never needs.
+__device__ __forceinline__ float rcp_approx_normal(float x)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 __device__ __forceinline__ float log1p_unit(float u)
 {
     const float t = __fadd_rn(2.0f, u);
-    const float r = rcp_approx(t);
+    const float r = rcp_approx_normal(t);
     const float q0 = __fmul_rn(u, r);
     const float s = __fmaf_rn(__fmaf_rn(-q0, t, u), r, q0);
     const float z = __fmul_rn(s, s);
@@ -92,7 +102,7 @@ __device__ __forceinline__ void lse_merge2(float a0, float a1, float b0, float b
     const float u0 = __expf(d0), u1 = __expf(d1);
     float t0, t1, q0, q1, s0, s1;
     add2_rn(2.0f, 2.0f, u0, u1, t0, t1);
-    const float c0 = rcp_approx(t0), c1 = rcp_approx(t1);
+    const float c0 = rcp_approx_normal(t0), c1 = rcp_approx_normal(t1);
     mul2_rn(u0, u1, c0, c1, q0, q1);
     const float e0 = __fmaf_rn(-q0, t0, u0), e1 = __fmaf_rn(-q1, t1, u1);
     fma2_rn(e0, e1, c0, c1, q0, q1, s0, s1);

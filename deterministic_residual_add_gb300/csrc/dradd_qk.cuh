@@ -351,9 +351,9 @@ __global__ void __launch_bounds__(qk_max_threads(KQ > KK ? KQ : KK))
 }
 
 // ------------------------------------------------------------- qk_warp_kernel
-// Fused q/k RMSNorm, one warp per row (warp_body): CTAs [0, q_ctas) take the
-// q rows, the rest the k rows, each side with its own stages and weights
-// (dynamic shared memory: the larger side's warp_smem_bytes).
+// Fused q/k RMSNorm, one warp per row (warp_ring_body): CTAs [0, q_ctas)
+// take the q rows, the rest the k rows, each side with its own rings and
+// weights (dynamic shared memory: the larger side's warp_smem_bytes).
 template <int KQ, int KK, bool QQUANT, bool QADD>
 __global__ void __launch_bounds__(256, 1) qk_warp_kernel(const Params pq, const Params pk, int q_ctas)
 {
@@ -361,9 +361,9 @@ __global__ void __launch_bounds__(256, 1) qk_warp_kernel(const Params pq, const 
     constexpr int QOUT = QQUANT ? kOutE4m3Group : kOutBf16;
     const int cta = static_cast<int>(blockIdx.x);
     if (cta < q_ctas)
-        warp_body<KQ, QOUT, QADD>(pq, cta, q_ctas, wsm);
+        warp_ring_body<KQ, QOUT, QADD>(pq, cta, q_ctas, wsm);
     else
-        warp_body<KK, kOutBf16, false>(pk, cta - q_ctas, static_cast<int64_t>(gridDim.x) - q_ctas, wsm);
+        warp_ring_body<KK, kOutBf16, false>(pk, cta - q_ctas, static_cast<int64_t>(gridDim.x) - q_ctas, wsm);
 }
 
 template <bool QQUANT, bool QADD>

@@ -26,9 +26,11 @@
 // makes the scale infinite, which the bracket does not take).  Other rows,
 // and blocks whose bracket ends differ, use the correctly rounded division.
 //
-// The CTA meets at a barrier once per group, after every warp has finished
-// with the stage, and thread 0 then refills that stage with the group
-// `stages` ahead.  Every wait on a copy is bounded, as in staged_kernel.
+// warp_body's CTA meets at a barrier once per group, after every warp has
+// finished with the stage, and thread 0 then refills that stage with the
+// group `stages` ahead; warp_ring_body's warps share only the weights and
+// never wait for one another.  Every wait on a copy is bounded, as in
+// staged_kernel.
 #pragma once
 
 #include "dradd_kernels.cuh"
@@ -304,6 +306,100 @@ __device__ __forceinline__ void warp_body(const Params& p, int64_t cta, int64_t 
         if (tid == 0) {
             const int64_t next = g + static_cast<int64_t>(stages) * n_ctas;
             if (next < n_groups) {
+                fence_proxy_async_smem();
+                issue(s, next);
+            }
+        }
+        if (++s == stages) {
+            s = 0;
+            parity ^= 1u;
+        }
+    }
+}
+
+// Rows of p for the warps of CTAs cta, cta + n_ctas, ...: warp w of the CTA
+// (W warps) takes rows gw, gw + GW, ... with gw = cta * W + w and GW =
+// n_ctas * W, each through a ring of `stages` row slots of its own in shared
+// memory, filled by bulk copies that its lane 0 issues `stages` rows ahead
+// and waited on through the warp's own mbarriers.  No barrier joins the
+// warps once the weights are widened, so a warp never waits for another.
+template <int K, int OUT, bool ADD>
+__device__ __forceinline__ void warp_ring_body(const Params& p, int64_t cta, int64_t n_ctas, unsigned char* smem)
+{
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int W = blockDim.x >> 5;
+    const int nblocks = p.hidden >> 3;
+    const int stages = p.stages;
+    const uint32_t row_bytes = static_cast<uint32_t>(p.hidden) * 2u;
+    const uint32_t slot_bytes = (ADD ? 2u : 1u) * row_bytes;
+    unsigned char* const ring = smem + static_cast<size_t>(warp) * stages * slot_bytes;
+    unsigned char* const after_rings = smem + static_cast<size_t>(W) * stages * slot_bytes;
+    float4* const w_lo = reinterpret_cast<float4*>(after_rings);
+    float4* const w_hi = w_lo + nblocks;
+    uint64_t* const bars =
+        reinterpret_cast<uint64_t*>(after_rings + 4u * static_cast<uint32_t>(p.hidden)) + warp * stages;
+    const int64_t first = cta * W + warp;
+    const int64_t stride = n_ctas * W;
+
+    if (lane == 0) {
+        // While the previous grid finishes: an L2 prefetch of this warp's
+        // first row (the copy that consumes it is issued after the wait
+        // below, and reads what the memory holds then).
+        if (p.l2_prefetch && first < p.n_rows) {
+            prefetch_l2(p.x + first * p.hidden, row_bytes);
+            if constexpr (ADD)
+                prefetch_l2(p.residual + first * p.hidden, row_bytes);
+        }
+        for (int s = 0; s < stages; ++s)
+            mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    wait_prior_grids();
+    allow_next_grid();
+
+    const uint64_t policy = l2_policy_evict_first();
+    auto issue = [&](int s, int64_t row) {
+        unsigned char* dst = ring + static_cast<size_t>(s) * slot_bytes;
+        mbar_arrive_expect_tx(&bars[s], slot_bytes);
+        bulk_copy_g2s(dst, p.x + row * p.hidden, row_bytes, &bars[s], policy);
+        if constexpr (ADD)
+            bulk_copy_g2s(dst + row_bytes, p.residual + row * p.hidden, row_bytes, &bars[s], policy);
+    };
+    if (lane == 0) {
+        for (int s = 0; s < stages; ++s) {
+            const int64_t row = first + s * stride;
+            if (row >= p.n_rows)
+                break;
+            if (p.fault_inject && s == 0)
+                continue;  // test hook: this copy never comes, so its wait expires
+            issue(s, row);
+        }
+    }
+    const bool w_finite = widen_weights_to_smem(p.weight, nblocks, w_lo, w_hi);
+
+    int64_t i = 0;
+    int s = 0;
+    uint32_t parity = 0;
+    for (int64_t row = first; row < p.n_rows; row += stride, ++i) {
+        const bool ok = mbar_wait_bounded(&bars[s], parity, p.wait_limit_ns);
+        if (__any_sync(0xFFFFFFFFu, !ok)) {
+            // this warp stops; its issued copies land before it leaves
+            if (lane == 0) {
+                record_timeout(p);
+                drain_issued_copies(p, bars, s, parity, i, stages, first, stride, p.n_rows);
+            }
+            return;
+        }
+        const unsigned char* slot = ring + static_cast<size_t>(s) * slot_bytes;
+        warp_row<K, OUT, ADD>(p, row, reinterpret_cast<const uint4*>(slot),
+                              reinterpret_cast<const uint4*>(slot + row_bytes), w_lo, w_hi, w_finite);
+        __syncwarp();  // every lane is done with the slot
+        if (lane == 0) {
+            const int64_t next = row + static_cast<int64_t>(stages) * stride;
+            if (next < p.n_rows) {
                 fence_proxy_async_smem();
                 issue(s, next);
             }

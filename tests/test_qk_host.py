@@ -91,6 +91,15 @@ def test_plan_rules(nq, hq, nk, hk, g):
     max_p = max(1 << (h - 1).bit_length() for n, h in ((nq, hq), (nk, hk)) if n)
     rows = nq + nk
     max_stages = 2
+    min_p = min(1 << (h - 1).bit_length() for n, h in ((nq, hq), (nk, hk)) if n)
+    if 256 < min_p and max_p <= 2048 and rows >= 8192:
+        # the low-rank q / kv class: one warp a row, rings of 2 slots, 128 threads
+        assert (p.variant, B) == (dr.VARIANT_WARP, 128)
+        for n, h, T, R, S, C in ((nq, hq, p.q_threads_per_row, p.q_rows_per_cta, p.q_stages, p.q_ctas),
+                                 (nk, hk, p.k_threads_per_row, p.k_rows_per_cta, p.k_stages, p.k_ctas)):
+            if n:
+                assert (T, R, S) == (32, 4, 2) and 1 <= C <= -(-n // R)
+        return
     if max_p <= 256 and rows > 16384:
         assert (p.variant, B) == (2, 128)
         least_k = 4
