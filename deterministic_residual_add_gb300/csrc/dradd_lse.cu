@@ -80,11 +80,13 @@ __device__ __forceinline__ float lse_merge_nan_d(float a, float b)
 // __expf (at most 2 + floor(1.173 |d|) ulp from e^d; scaled by
 // e^d / (1 + e^d), an absolute error below 2^-23 in the sum, like the
 // accurate expf's); both -inf gives -inf, +inf wins, NaN propagates.
+// d = lo - hi is taken as -|RN(a - b)|: rounding is symmetric, so that is
+// RN(lo - hi) (up to the sign of a zero difference, which only exp sees);
+// hi = max(a, b).  A NaN operand or two equal infinities make d NaN.
 __device__ __forceinline__ float lse_merge1(float a, float b)
 {
-    const float hi = a > b ? a : b;
-    const float lo = a > b ? b : a;
-    const float d = __fsub_rn(lo, hi);
+    const float hi = fmaxf(a, b);
+    const float d = -fabsf(__fsub_rn(a, b));
     if (isnan(d))
         return lse_merge_nan_d(a, b);
     return __fadd_rn(hi, log1p_unit(__expf(d)));
@@ -95,10 +97,10 @@ __device__ __forceinline__ float lse_merge1(float a, float b)
 // each element's bits are lse_merge1's).
 __device__ __forceinline__ void lse_merge2(float a0, float a1, float b0, float b1, float& r0, float& r1)
 {
-    const float hi0 = a0 > b0 ? a0 : b0, lo0 = a0 > b0 ? b0 : a0;
-    const float hi1 = a1 > b1 ? a1 : b1, lo1 = a1 > b1 ? b1 : a1;
-    float d0, d1;
-    sub2_rn(lo0, lo1, hi0, hi1, d0, d1);
+    const float hi0 = fmaxf(a0, b0), hi1 = fmaxf(a1, b1);
+    float e0d, e1d;
+    sub2_rn(a0, a1, b0, b1, e0d, e1d);
+    const float d0 = -fabsf(e0d), d1 = -fabsf(e1d);
     const float u0 = __expf(d0), u1 = __expf(d1);
     float t0, t1, q0, q1, s0, s1;
     add2_rn(2.0f, 2.0f, u0, u1, t0, t1);
