@@ -590,7 +590,11 @@ __device__ __forceinline__ E4m3Scale make_e4m3_scale(float scale)
     E4m3Scale s;
     s.scale = scale;
     s.fast = scale >= 0x1p-126f && scale < 0x1p120f;
-    const float c = s.fast ? rcp_approx(scale) : 0.0f;
+    // a normal scale below 2^120 has a normal reciprocal: the flush-to-zero
+    // form of rcp.approx gives the same value without subnormal handling
+    float c = 0.0f;
+    if (s.fast)
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(c) : "f"(scale));
     s.c_lo = __fmul_rn(c, 1.0f - 0x1p-20f);
     s.c_hi = __fmul_rn(c, 1.0f + 0x1p-20f);
     return s;

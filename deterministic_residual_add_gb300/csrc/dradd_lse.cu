@@ -123,10 +123,13 @@ __device__ __forceinline__ void lse_merge2(float a0, float a1, float b0, float b
     mul2_rn(w0, w1, z0, z1, v0, v1);
     fma2_rn(v0, v1, p0, p1, w0, w1, l0, l1);
     add2_rn(hi0, hi1, l0, l1, r0, r1);
-    if (isnan(d0))
-        r0 = lse_merge_nan_d(a0, b0);
-    if (isnan(d1))
-        r1 = lse_merge_nan_d(a1, b1);
+    // d0, d1 <= 0 (or NaN), so their sum is NaN exactly when one of them is
+    if (isnan(__fadd_rn(d0, d1))) {
+        if (isnan(d0))
+            r0 = lse_merge_nan_d(a0, b0);
+        if (isnan(d1))
+            r1 = lse_merge_nan_d(a1, b1);
+    }
 }
 
 __device__ __forceinline__ float unary1(float x, int op)
