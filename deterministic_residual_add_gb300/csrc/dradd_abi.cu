@@ -1115,11 +1115,18 @@ dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dra
 // ------------------------------------------- log-sum-exp merge, unary math
 // Threads per CTA (cfg->threads_per_row, default 128), elements per thread
 // per pass (cfg->blocks_per_thread, default 8) and CTAs (cfg->grid_ctas,
-// default: two waves, 2 x SMs x 2048 / threads, at most one per unit).
-// The defaults are the fastest of a sweep on GB300 (CTA sizes 128-512, 2-8
-// elements per thread, grids of 2, 16 and 32 CTAs per SM).
+// default: threads_per_sm threads on every SM in whole CTAs, at most one
+// CTA per unit).  The defaults are the fastest of sweeps on GB300 (CTA
+// sizes 128-1024, 4-8 elements per thread, 1-32 CTAs per SM): the merge of
+// 256 x 32768 (and of the last 16384 columns in place) with 1024 threads
+// per SM, a few units per CTA (15.99 -> 15.39 and 9.45 -> 8.25 us against
+// two full waves, 4096 threads per SM); log1p of 2^24 values with two full
+// waves (21.2 us; 1024 threads per SM: 25.6 us).
+constexpr int kMergeThreadsPerSm = 1024;
+constexpr int kUnaryThreadsPerSm = 4096;
+
 dradd_status elementwise_plan(int64_t n_rows, int64_t n_cols, const dradd_launch_cfg* cfg_in, int sm_count,
-                              int* threads, int* vec, int* grid, bool* serialize)
+                              int threads_per_sm, int* threads, int* vec, int* grid, bool* serialize)
 {
     dradd_launch_cfg cfg = {};
     if (cfg_in)
@@ -1136,7 +1143,8 @@ dradd_status elementwise_plan(int64_t n_rows, int64_t n_cols, const dradd_launch
     const int64_t units = n_rows * ((n_cols + span - 1) / span);
     int64_t G = cfg.grid_ctas;
     if (G == 0) {
-        G = 2 * static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * (2048 / T);
+        const int per_sm = threads_per_sm > T ? threads_per_sm / T : 1;
+        G = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * per_sm;
         if (G > units)
             G = units;
         if (G < 1)
@@ -1170,7 +1178,8 @@ dradd_status lse_run(float* out, int64_t out_stride, const float* a, int64_t a_s
             return DRADD_ERR_BAD_SHAPE;
     int threads = 0, vec = 0, grid = 0;
     bool serialize = false;
-    dradd_status st = elementwise_plan(n_rows, n_cols, cfg, 152, &threads, &vec, &grid, &serialize);
+    dradd_status st = elementwise_plan(n_rows, n_cols, cfg, 152, kMergeThreadsPerSm, &threads, &vec, &grid,
+                                       &serialize);
     if (st != DRADD_OK)
         return st;
     if (n_rows == 0 || n_cols == 0)
@@ -1192,7 +1201,8 @@ dradd_status lse_run(float* out, int64_t out_stride, const float* a, int64_t a_s
     st = query_limits(&L);
     if (st != DRADD_OK)
         return st;
-    st = elementwise_plan(n_rows, n_cols, cfg, L.sm_count, &threads, &vec, &grid, &serialize);
+    st = elementwise_plan(n_rows, n_cols, cfg, L.sm_count, kMergeThreadsPerSm, &threads, &vec, &grid,
+                          &serialize);
     if (st != DRADD_OK)
         return st;
     const bool vec4 = aligned(out, 16) && aligned(a, 16) && aligned(b, 16) &&
@@ -1215,7 +1225,7 @@ dradd_status unary_run(float* out, const float* x, int64_t n, int op, cudaStream
         return DRADD_ERR_BAD_CONFIG;
     int threads = 0, vec = 0, grid = 0;
     bool serialize = false;
-    dradd_status st = elementwise_plan(1, n, cfg, 152, &threads, &vec, &grid, &serialize);
+    dradd_status st = elementwise_plan(1, n, cfg, 152, kUnaryThreadsPerSm, &threads, &vec, &grid, &serialize);
     if (st != DRADD_OK)
         return st;
     if (n == 0)
@@ -1230,7 +1240,7 @@ dradd_status unary_run(float* out, const float* x, int64_t n, int op, cudaStream
     st = query_limits(&L);
     if (st != DRADD_OK)
         return st;
-    st = elementwise_plan(1, n, cfg, L.sm_count, &threads, &vec, &grid, &serialize);
+    st = elementwise_plan(1, n, cfg, L.sm_count, kUnaryThreadsPerSm, &threads, &vec, &grid, &serialize);
     if (st != DRADD_OK)
         return st;
     const bool vec4 = aligned(out, 16) && aligned(x, 16);

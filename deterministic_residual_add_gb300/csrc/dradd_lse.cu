@@ -277,8 +277,16 @@ __global__ void __launch_bounds__(1024) unary_kernel(float* out, const float* x,
     }
     wait_prior_grids();
     allow_next_grid();
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * span; base < n;
-         base += static_cast<int64_t>(gridDim.x) * span) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * span;
+    // As in the merge: thread 0 prefetches the whole unit kLseL2Ahead grid
+    // strides ahead into L2.
+    const bool ahead_on = l2_prefetch && vec4 && threadIdx.x == 0 && kLseL2Ahead > 0;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * span; base < n; base += stride) {
+        if (ahead_on) {
+            const int64_t ahead = base + kLseL2Ahead * stride;
+            if (ahead < n && span <= n - ahead)
+                prefetch_l2(x + ahead, static_cast<uint32_t>(span * 4));
+        }
         const float* xr = x + base;
         float* orow = out + base;
         if (VEC >= 4 && vec4 && base + span <= n) {
