@@ -204,8 +204,16 @@ __device__ __forceinline__ float butterfly_sum(float v, int width)
     return v;
 }
 
+// The maximum over `width` lanes (a power of two <= 32; all 32 lanes of
+// the warp take part), in every lane: a butterfly, or for the whole warp
+// one redux.sync.  The maximum is exact, so every form gives the same value.
 __device__ __forceinline__ float butterfly_max(float v, int width)
 {
+    if (width >= 32) {
+        float r;
+        asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+        return r;
+    }
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         if (d < width)
@@ -290,29 +298,11 @@ __device__ __forceinline__ float cross_warp_sum(const float* red, int lane)
     }
 }
 
-// max(a, |b|), NaN if either is NaN (a NaN y anywhere in a row shows in its
-// amax, so the row can take the exact path).
-__device__ __forceinline__ float max_abs_nan(float a, float b)
-{
-    float d;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(fabsf(b)));
-    return d;
-}
-
-// max |y| over K blocks of 8 as a balanced tree (the maximum is exact, so
-// any order gives the same value; the tree keeps the dependent chain short).
-// NAN_PROP: a NaN anywhere gives NaN (max.NaN), else NaN is ignored.
-template <bool NAN_PROP>
-__device__ __forceinline__ float max2_abs(float a, float b)
-{
-    float d;
-    if constexpr (NAN_PROP)
-        asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(fabsf(a)), "f"(fabsf(b)));
-    else
-        d = fmaxf(fabsf(a), fabsf(b));
-    return d;
-}
-
+// max |y| over K blocks of 8 as a tree of max instructions (the maximum is
+// exact, so any order gives the same value; the tree keeps the dependent
+// chain short).  NAN_PROP: a NaN anywhere gives NaN (max.NaN, so a NaN y in
+// a row shows in its amax and the row can take the exact path), else NaN is
+// ignored (NaN only if every value is NaN).
 template <bool NAN_PROP>
 __device__ __forceinline__ float max2(float a, float b)
 {
@@ -324,23 +314,54 @@ __device__ __forceinline__ float max2(float a, float b)
     return d;
 }
 
+// max(a, b, c) in one three-input instruction, NaN propagating as in max2.
+template <bool NAN_PROP>
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    if constexpr (NAN_PROP)
+        asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    else
+        asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Level by level: each level replaces consecutive triples of the N values
+// by their max3 (a last pair by max2, a last single value passes), so N
+// values take about N / 2 instructions.
+template <int N, bool NAN_PROP>
+__device__ __forceinline__ float max_tree(float (&v)[N])
+{
+    if constexpr (N == 1) {
+        return v[0];
+    } else {
+        constexpr int M = (N + 2) / 3;
+        float u[M];
+#pragma unroll
+        for (int i = 0; i < M; ++i) {
+            const int k = 3 * i;
+            if (k + 2 < N)
+                u[i] = max3<NAN_PROP>(v[k], v[k + 1], v[k + 2]);
+            else if (k + 1 < N)
+                u[i] = max2<NAN_PROP>(v[k], v[k + 1]);
+            else
+                u[i] = v[k];
+        }
+        return max_tree<M, NAN_PROP>(u);
+    }
+}
+
 template <int K, bool NAN_PROP>
 __device__ __forceinline__ float tree_max_abs(const float (&y)[K][8])
 {
-    float m[K];
+    float a[K * 8];
 #pragma unroll
     for (int j = 0; j < K; ++j) {
-        const float a = max2<NAN_PROP>(max2_abs<NAN_PROP>(y[j][0], y[j][1]), max2_abs<NAN_PROP>(y[j][2], y[j][3]));
-        const float b = max2<NAN_PROP>(max2_abs<NAN_PROP>(y[j][4], y[j][5]), max2_abs<NAN_PROP>(y[j][6], y[j][7]));
-        m[j] = max2<NAN_PROP>(a, b);
-    }
 #pragma unroll
-    for (int width = 1; width < K; width *= 2) {
-#pragma unroll
-        for (int j = 0; j < K; j += 2 * width)
-            m[j] = max2<NAN_PROP>(m[j], m[j + width]);
+        for (int e = 0; e < 8; ++e)
+            a[j * 8 + e] = fabsf(y[j][e]);
     }
-    return m[0];
+    return max_tree<K * 8, NAN_PROP>(a);
 }
 
 // y = (acc * inv) * w for one block, with its 8 weights already in fp32
@@ -360,6 +381,11 @@ __device__ __forceinline__ void scale8_f32(float (&a)[8], float inv, const float
 // butterfly_max with NaN propagation: NaN in any lane gives NaN in all.
 __device__ __forceinline__ float butterfly_max_nan(float v, int width)
 {
+    if (width >= 32) {
+        float r;
+        asm volatile("redux.sync.max.NaN.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+        return r;
+    }
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         if (d < width) {
@@ -468,12 +494,13 @@ __device__ __forceinline__ uint2 quantize8(const float (&y)[8], const QuantScale
     return u;
 }
 
-// Int8 codes by a bracket of the quotient.  With c = RN(1 / scale) (relative
-// error at most 2^-24), c_lo = RN(c (1 - 2^-22)) and c_hi = RN(c (1 + 2^-22))
-// satisfy, for y >= 0 and a normal quotient,
-//   y c_lo <= y/scale (1 + 2^-24)(1 - 2^-22)(1 + 2^-24) < y/scale (1 - 2^-24)
+// Int8 codes by a bracket of the quotient.  With c the hardware reciprocal
+// of scale (rcp.approx, documented to be within 1 ulp, so a relative error
+// below 2^-22 where scale and 1 / scale are normal), c_lo = RN(c (1 - 2^-21)) and
+// c_hi = RN(c (1 + 2^-21)) satisfy, for y >= 0 and a normal quotient,
+//   y c_lo <= y/scale (1 + 2^-22)(1 - 2^-21)(1 + 2^-24) < y/scale (1 - 2^-24)
 //          <= RN(y / scale) <= y/scale (1 + 2^-24)
-//          < y/scale (1 - 2^-24)(1 + 2^-22)(1 - 2^-24) <= y c_hi
+//          < y/scale (1 - 2^-22)(1 + 2^-21)(1 - 2^-24) <= y c_hi
 // (mirrored for y < 0; a subnormal quotient is below 2^-126 and every
 // candidate then rounds to 0).  fma(y, c, 1.5 * 2^23) is 1.5 * 2^23 plus
 // the exact product rounded to an integer, ties to even (|y c| < 2^22 here),
@@ -493,9 +520,13 @@ __device__ __forceinline__ Int8Bracket make_int8_bracket(float scale)
     Int8Bracket s;
     s.scale = scale;
     s.fast = scale >= 0x1p-126f && scale < 0x1p120f;
-    const float c = s.fast ? __frcp_rn(scale) : 0.0f;
-    s.c_lo = __fmul_rn(c, 1.0f - 0x1p-22f);
-    s.c_hi = __fmul_rn(c, 1.0f + 0x1p-22f);
+    // a normal scale below 2^120 has a normal reciprocal: the flush-to-zero
+    // form of rcp.approx gives the same value without subnormal handling
+    float c = 0.0f;
+    if (s.fast)
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(c) : "f"(scale));
+    s.c_lo = __fmul_rn(c, 1.0f - 0x1p-21f);
+    s.c_hi = __fmul_rn(c, 1.0f + 0x1p-21f);
     return s;
 }
 
@@ -546,32 +577,32 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
     return d;
 }
 
-// RN(m / 448) for an amax m >= 0, by division with one correction step
-// (Markstein): q0 = RN(m * RN(1/448)); the remainder m - q0 * 448 is exact
-// in one fused multiply-add; q = RN(q0 + remainder * RN(1/448)).  Every
-// operation scales exactly with m by powers of two while q0 and the
-// remainder stay normal, so checking every significand in a few binades
-// proves the identity for all m in [2^-100, 2^128): the test suite does
-// that against the correctly rounded quotient.  Anything else (0,
-// subnormal or tiny m, Inf, NaN) takes the IEEE division.
-__device__ __forceinline__ float div448_rn(float m)
+// RN(m / d) for an amax m >= 0 and the divisor d of a quantised format
+// (127 for int8, 448 for fp8 e4m3, 6 for fp4 e2m1), by division with one
+// correction step (Markstein): q0 = RN(m * c) with c = RN(1 / d); the
+// remainder m - q0 * d is exact in one fused multiply-add; q = RN(q0 +
+// remainder * c).  Every operation scales exactly with m by powers of two
+// while q0 and the remainder stay normal, so checking every significand in
+// a few binades proves the identity for all m in [2^-100, 2^128): the test
+// suite checks every m in that range against the correctly rounded
+// quotient, for each of the three divisors and constants.  Anything else
+// (0, subnormal or tiny m, Inf, NaN) takes the IEEE division.
+template <int D>
+__device__ __forceinline__ float div_const_rn(float m)
 {
-    constexpr float kInv448 = 0x1.24924ap-9f;  // RN(1 / 448)
+    static_assert(D == 127 || D == 448 || D == 6, "divisor: 127, 448 or 6");
+    constexpr float kInv = D == 127 ? 0x1.020408p-7f : D == 448 ? 0x1.24924ap-9f : 0x1.555556p-3f;  // RN(1 / D)
+    constexpr float kD = static_cast<float>(D);
     if (!(m >= 0x1p-100f && m <= 3.40282347e38f))
-        return __fdiv_rn(m, 448.0f);
-    const float q0 = __fmul_rn(m, kInv448);
-    const float r = __fmaf_rn(-q0, 448.0f, m);
-    return __fmaf_rn(r, kInv448, q0);
+        return __fdiv_rn(m, kD);
+    const float q0 = __fmul_rn(m, kInv);
+    const float r = __fmaf_rn(-q0, kD, m);
+    return __fmaf_rn(r, kInv, q0);
 }
 
-// An approximation of 1 / x with relative error below 2^-22 for normal x
-// whose reciprocal is normal: the hardware reciprocal, documented to be
-// within 1 ulp.
-__device__ __forceinline__ float rcp_approx(float x)
+__device__ __forceinline__ float div448_rn(float m)
 {
-    float r;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
-    return r;
+    return div_const_rn<448>(m);
 }
 
 // Per-row (or per-group) fp8 / fp4 scale (scale = RN(amax / 448) or

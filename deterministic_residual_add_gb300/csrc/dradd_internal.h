@@ -39,6 +39,13 @@ constexpr unsigned kDeviceStatusUndrained = 2u;
 // What a normalised row is stored as.
 enum OutKind : int { kOutBf16 = 0, kOutInt8 = 1, kOutE4m3 = 2, kOutE2m1 = 3, kOutE4m3Group = 4 };
 
+// The largest code magnitude of a quantised output: its scale is
+// RN(amax / quant_divisor(out)).
+__host__ __device__ constexpr int quant_divisor(int out)
+{
+    return out == kOutInt8 ? 127 : out == kOutE2m1 ? 6 : 448;
+}
+
 // Shared memory the staged kernel keeps besides its stages: for the
 // quantised outputs the row's weights, widened to fp32 once per CTA (4
 // bytes per element of the row, 16-byte aligned).

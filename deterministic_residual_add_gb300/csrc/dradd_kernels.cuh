@@ -144,9 +144,10 @@ __device__ __forceinline__ void finish_row(const Params& p, float (&acc)[K][8], 
             if (lane == 0)
                 red_max[warp_in_row] = m;
             __syncthreads();
-            m = butterfly_max(red_max[lane & ((T >> 5) - 1)], T >> 5);
+            // every lane reads one warp's max (replicated): one warp-wide max
+            m = butterfly_max(red_max[lane & ((T >> 5) - 1)], 32);
         }
-        const float scale = __fdiv_rn(m, OUT == kOutInt8 ? 127.0f : OUT == kOutE4m3 ? 448.0f : 6.0f);
+        const float scale = div_const_rn<quant_divisor(OUT)>(m);
         if (active) {
             if (t == 0)
                 p.scale[row] = scale;
@@ -349,11 +350,11 @@ __device__ __forceinline__ void staged_quant_row(const Params& p, const float (&
             if (lane == 0)
                 red_max[warp] = m;
             __syncthreads();
-            m = butterfly_max_nan(red_max[lane & (W - 1)], W);
+            m = butterfly_max_nan(red_max[lane & (W - 1)], 32);  // replicated lanes
         }
         uint2* qrow = reinterpret_cast<uint2*>(p.out_q + row * p.hidden);
         if (!isnan(m)) {
-            const float scale = __fdiv_rn(m, 127.0f);
+            const float scale = div_const_rn<127>(m);
             if (tid == 0)
                 p.scale[row] = scale;
             const Int8Bracket qs = make_int8_bracket(scale);
@@ -376,9 +377,9 @@ __device__ __forceinline__ void staged_quant_row(const Params& p, const float (&
                 if (lane == 0)
                     red_max2[warp] = m2;
                 __syncthreads();
-                m2 = butterfly_max(red_max2[lane & (W - 1)], W);
+                m2 = butterfly_max(red_max2[lane & (W - 1)], 32);
             }
-            const float scale = __fdiv_rn(m2, 127.0f);
+            const float scale = div_const_rn<127>(m2);
             if (tid == 0)
                 p.scale[row] = scale;
 #pragma unroll
@@ -395,9 +396,9 @@ __device__ __forceinline__ void staged_quant_row(const Params& p, const float (&
             if (lane == 0)
                 red_max[warp] = m;
             __syncthreads();
-            m = butterfly_max(red_max[lane & (W - 1)], W);
+            m = butterfly_max(red_max[lane & (W - 1)], 32);
         }
-        const float scale = __fdiv_rn(m, OUT == kOutE4m3 ? 448.0f : 6.0f);
+        const float scale = div_const_rn<quant_divisor(OUT)>(m);
         if (tid == 0)
             p.scale[row] = scale;
         const E4m3Scale qs = make_e4m3_scale(scale);

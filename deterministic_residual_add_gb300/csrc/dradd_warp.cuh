@@ -61,9 +61,11 @@ __device__ __forceinline__ bool widen_weights_to_smem(const uint16_t* weight, in
 // max |y| of one block as a balanced tree (exact; NaN ignored).
 __device__ __forceinline__ float block_max_abs(const float (&y)[8])
 {
-    const float a = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
-    const float b = fmaxf(fmaxf(fabsf(y[4]), fabsf(y[5])), fmaxf(fabsf(y[6]), fabsf(y[7])));
-    return fmaxf(a, b);
+    float a[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        a[e] = fabsf(y[e]);
+    return max_tree<8, false>(a);
 }
 
 // One row by one warp: xs (and rs) its x (and residual) in shared memory.
@@ -170,7 +172,7 @@ __device__ __forceinline__ void warp_row(const Params& p, int64_t row, const uin
             }
         }
         m = butterfly_max(m, 32);
-        const float scale = __fdiv_rn(m, OUT == kOutInt8 ? 127.0f : OUT == kOutE4m3 ? 448.0f : 6.0f);
+        const float scale = div_const_rn<quant_divisor(OUT)>(m);
         if (lane == 0)
             p.scale[row] = scale;
         if constexpr (OUT == kOutInt8) {

@@ -1,10 +1,11 @@
 """Arithmetic identities the CUDA kernels rely on, checked on the CPU with
 IEEE fp32 operations (the same operations the kernels issue):
 
-- the group scale RN(amax / 448) of the per-group fp8 output is computed by
-  one multiplication and two fused multiply-adds (a division with one
-  correction step); tests/div448_check.c compares it with the correctly
-  rounded quotient for every fp32 amax in [2^-100, 2^128);
+- the scales RN(amax / 127), RN(amax / 448) and RN(amax / 6) of the int8,
+  fp8 and fp4 outputs are computed by one multiplication and two fused
+  multiply-adds (a division with one correction step);
+  tests/div_const_check.c compares each with the correctly rounded quotient
+  for every fp32 amax in [2^-100, 2^128);
 - the LSE merge's log1p(u) on [0, 1] by the atanh series after a division
   with one correction step; tests/log1p_series_check.c compares it with
   log1p in double for every fp32 u in [0, 1]."""
@@ -13,21 +14,25 @@ import subprocess
 from concurrent.futures import ThreadPoolExecutor
 from pathlib import Path
 
+import pytest
+
 import oracle
 
 HERE = Path(__file__).resolve().parent
 
 
-def test_div448_correction_step_is_correctly_rounded(tmp_path):
-    exe = tmp_path / "div448_check"
+@pytest.mark.parametrize("divisor", [127, 448, 6])
+def test_division_by_constant_is_correctly_rounded(tmp_path, divisor):
+    exe = tmp_path / "div_const_check"
     subprocess.run([oracle._compiler(), "-O2", "-std=c11", "-ffp-contract=off", "-o", str(exe),
-                    str(HERE / "div448_check.c"), "-lm"], check=True)
+                    str(HERE / "div_const_check.c"), "-lm"], check=True)
     exps = list(range(-100, 128))
     parts = max(1, min(16, os.cpu_count() or 1))
     chunks = [exps[i::parts] for i in range(parts)]
 
     def run(ch):
-        return [subprocess.run([str(exe), str(e), str(e)], capture_output=True, text=True) for e in ch]
+        return [subprocess.run([str(exe), str(divisor), str(e), str(e)], capture_output=True, text=True)
+                for e in ch]
 
     with ThreadPoolExecutor(parts) as ex:
         results = [r for rs in ex.map(run, chunks) for r in rs]
