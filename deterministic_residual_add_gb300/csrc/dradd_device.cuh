@@ -205,21 +205,33 @@ __device__ __forceinline__ float butterfly_sum(float v, int width)
 }
 
 // The maximum over `width` lanes (a power of two <= 32; all 32 lanes of
-// the warp take part), in every lane: a butterfly, or for the whole warp
-// one redux.sync.  The maximum is exact, so every form gives the same value.
+// the warp take part), in every lane.
 __device__ __forceinline__ float butterfly_max(float v, int width)
 {
-    if (width >= 32) {
-        float r;
-        asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-        return r;
-    }
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         if (d < width)
             v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, d));
     }
     return v;
+}
+
+// The maximum over all 32 lanes of a warp (every lane active), in every
+// lane, by one redux.sync: NaN is ignored unless every lane holds NaN (as
+// fmaxf), or with warp_max_nan a NaN in any lane gives NaN.  The maximum is
+// exact, so this equals the butterfly.
+__device__ __forceinline__ float warp_max(float v)
+{
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+__device__ __forceinline__ float warp_max_nan(float v)
+{
+    float r;
+    asm volatile("redux.sync.max.NaN.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
 }
 
 // The K per-block partial sums of every lane of a full warp, reduced over
@@ -381,11 +393,6 @@ __device__ __forceinline__ void scale8_f32(float (&a)[8], float inv, const float
 // butterfly_max with NaN propagation: NaN in any lane gives NaN in all.
 __device__ __forceinline__ float butterfly_max_nan(float v, int width)
 {
-    if (width >= 32) {
-        float r;
-        asm volatile("redux.sync.max.NaN.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-        return r;
-    }
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         if (d < width) {

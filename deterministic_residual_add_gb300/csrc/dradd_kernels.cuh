@@ -144,8 +144,7 @@ __device__ __forceinline__ void finish_row(const Params& p, float (&acc)[K][8], 
             if (lane == 0)
                 red_max[warp_in_row] = m;
             __syncthreads();
-            // every lane reads one warp's max (replicated): one warp-wide max
-            m = butterfly_max(red_max[lane & ((T >> 5) - 1)], 32);
+            m = butterfly_max(red_max[lane & ((T >> 5) - 1)], T >> 5);
         }
         const float scale = div_const_rn<quant_divisor(OUT)>(m);
         if (active) {
@@ -345,12 +344,12 @@ __device__ __forceinline__ void staged_quant_row(const Params& p, const float (&
         // amax with NaN propagation: a row holding a NaN y shows as a NaN
         // amax and takes the exact path (whose amax ignores NaN).
         float m = tree_max_abs<K, true>(y);
-        m = butterfly_max_nan(m, 32);
+        m = warp_max_nan(m);
         if constexpr (W > 1) {
             if (lane == 0)
                 red_max[warp] = m;
             __syncthreads();
-            m = butterfly_max_nan(red_max[lane & (W - 1)], 32);  // replicated lanes
+            m = warp_max_nan(red_max[lane & (W - 1)]);  // lane l reads warp l mod W
         }
         uint2* qrow = reinterpret_cast<uint2*>(p.out_q + row * p.hidden);
         if (!isnan(m)) {
@@ -372,12 +371,12 @@ __device__ __forceinline__ void staged_quant_row(const Params& p, const float (&
         } else {
             // uniform over the CTA: every thread holds the same m
             float m2 = fmaxf(0.0f, tree_max_abs<K, false>(y));  // NaN ignored, as a running max from 0
-            m2 = butterfly_max(m2, 32);
+            m2 = warp_max(m2);
             if constexpr (W > 1) {
                 if (lane == 0)
                     red_max2[warp] = m2;
                 __syncthreads();
-                m2 = butterfly_max(red_max2[lane & (W - 1)], 32);
+                m2 = warp_max(red_max2[lane & (W - 1)]);
             }
             const float scale = div_const_rn<127>(m2);
             if (tid == 0)
@@ -391,12 +390,12 @@ __device__ __forceinline__ void staged_quant_row(const Params& p, const float (&
         }
     } else {
         float m = fmaxf(0.0f, tree_max_abs<K, false>(y));  // NaN ignored, as a running max from 0
-        m = butterfly_max(m, 32);
+        m = warp_max(m);
         if constexpr (W > 1) {
             if (lane == 0)
                 red_max[warp] = m;
             __syncthreads();
-            m = butterfly_max(red_max[lane & (W - 1)], 32);
+            m = warp_max(red_max[lane & (W - 1)]);
         }
         const float scale = div_const_rn<quant_divisor(OUT)>(m);
         if (tid == 0)

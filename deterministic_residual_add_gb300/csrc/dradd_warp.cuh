@@ -171,7 +171,7 @@ __device__ __forceinline__ void warp_row(const Params& p, int64_t row, const uin
                 m = fmaxf(m, block_max_abs(y));
             }
         }
-        m = butterfly_max(m, 32);
+        m = warp_max(m);
         const float scale = div_const_rn<quant_divisor(OUT)>(m);
         if (lane == 0)
             p.scale[row] = scale;

@@ -67,6 +67,10 @@ CASES = [
     (100, 1536, 0, 512, 128, True, 1e-6, 1e-6),
     (1, 8, 1, 16, 8, True, 1e-6, 1e-6),
     (3, 64, 2, 64, 16, False, 1e-6, 1e-6),
+    # q rows whose data fill at most three quarters of their warp slices
+    (77, 1280, 45, 512, 128, True, 1e-6, 1e-6),
+    (70, 640, 33, 768, 64, True, 1e-6, 1e-6),
+    (66, 768, 20, 1024, 0, True, 1e-6, 1e-6),
 ]
 
 
