@@ -981,6 +981,30 @@ dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t g
     return DRADD_OK;
 }
 
+int qk_mode(const QkLaunch& plan)
+{
+    return plan.warp ? dradd::kQkWarp : plan.staged ? dradd::kQkStaged : dradd::kQkRows;
+}
+
+// qk_plan on the current device (limits L): the staged and warp-per-row
+// variants with an automatic grid get as many CTAs as fit on the device
+// at once, from the occupancy calculator for the kernel the plan picks.
+dradd_status qk_plan_on_device(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t group_size, bool add,
+                               const DeviceLimits& L, const dradd_launch_cfg* cfg, QkLaunch* plan)
+{
+    dradd_status st = qk_plan(n_q, hq, n_k, hk, group_size, add, L.sm_count, 0, L.smem_per_block_optin, cfg, plan);
+    if (st != DRADD_OK || !(plan->staged || plan->warp) || (cfg && cfg->grid_ctas != 0))
+        return st;
+    const bool quant = group_size != 0;
+    const int kq = plan->q.active ? plan->q.K : 1, kk = plan->k.active ? plan->k.K : 1;
+    int per_sm = 0;
+    if (dradd::qk_occupancy(kq, kk, quant, add, qk_mode(*plan), plan->threads, static_cast<size_t>(plan->dyn_smem),
+                            &per_sm) != cudaSuccess)
+        return DRADD_ERR_CUDA;
+    return qk_plan(n_q, hq, n_k, hk, group_size, add, L.sm_count, per_sm > 0 ? per_sm : 1, L.smem_per_block_optin,
+                   cfg, plan);
+}
+
 dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dradd_bf16* k_out,
                     const dradd_bf16* q, const dradd_bf16* q_residual, const dradd_bf16* q_weight,
                     const dradd_bf16* k, const dradd_bf16* k_weight, float q_eps, float k_eps, int64_t n_q,
@@ -1051,22 +1075,11 @@ dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dra
         eff.variant = DRADD_VARIANT_ROWS;
     }
     cfg = &eff;
-    st = qk_plan(n_q, hq, n_k, hk, group_size, add, L.sm_count, 0, L.smem_per_block_optin, cfg, &plan);
+    st = qk_plan_on_device(n_q, hq, n_k, hk, group_size, add, L, cfg, &plan);
     if (st != DRADD_OK)
         return st;
     const int kq = qa ? plan.q.K : 1, kk = ka ? plan.k.K : 1;
-    const int mode = plan.warp ? dradd::kQkWarp : plan.staged ? dradd::kQkStaged : dradd::kQkRows;
-    if ((plan.staged || plan.warp) && (!cfg || cfg->grid_ctas == 0)) {
-        // persistent grid: as many CTAs as fit on the device at once
-        int per_sm = 0;
-        if (dradd::qk_occupancy(kq, kk, quant, add, mode, plan.threads, static_cast<size_t>(plan.dyn_smem),
-                                &per_sm) != cudaSuccess)
-            return DRADD_ERR_CUDA;
-        st = qk_plan(n_q, hq, n_k, hk, group_size, add, L.sm_count, per_sm > 0 ? per_sm : 1,
-                     L.smem_per_block_optin, cfg, &plan);
-        if (st != DRADD_OK)
-            return st;
-    }
+    const int mode = qk_mode(plan);
 
     unsigned* status = nullptr;
     if (dradd::device_status_ptr(&status) != cudaSuccess)
@@ -1496,8 +1509,11 @@ dradd_status dradd_qk_resolve_config(int64_t n_q_rows, int64_t q_hidden, int64_t
             return st;
     }
     QkLaunch r;
-    const dradd_status st = qk_plan(n_q_rows, q_hidden, n_k_rows, k_hidden, group_size, q_residual != 0,
-                                    L.sm_count, 0, L.smem_per_block_optin, cfg, &r);
+    const dradd_status st =
+        sm_count > 0 ? qk_plan(n_q_rows, q_hidden, n_k_rows, k_hidden, group_size, q_residual != 0, L.sm_count, 0,
+                               L.smem_per_block_optin, cfg, &r)
+                     : qk_plan_on_device(n_q_rows, q_hidden, n_k_rows, k_hidden, group_size, q_residual != 0, L,
+                                         cfg, &r);
     if (st != DRADD_OK)
         return st;
     plan->variant = r.threads == 0 ? 0

@@ -452,7 +452,9 @@ typedef struct dradd_qk_plan {
  * both tensors).  sm_count > 0 stands in for the device's SM count (no GPU
  * needed; the automatic grid then assumes 2048 / threads CTAs per SM, where
  * the real call asks the occupancy calculator); sm_count <= 0 asks the
- * current device.  cfg may be NULL (automatic).  Returns the shape and
+ * current device, and for the staged and warp-per-row variants with an
+ * automatic grid its occupancy calculator, as the call does, so the plan is
+ * the call's.  cfg may be NULL (automatic).  Returns the shape and
  * configuration errors of the call.
  */
 dradd_status dradd_qk_resolve_config(int64_t n_q_rows, int64_t q_hidden, int64_t n_k_rows, int64_t k_hidden,
