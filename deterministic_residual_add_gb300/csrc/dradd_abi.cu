@@ -450,17 +450,24 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     if (cfg->rows_per_cta == 0)
         cfg->rows_per_cta = staged ? 1 : (T < 128 ? static_cast<int>(128 / T) : 1);
     const int R = cfg->rows_per_cta;
-    if (R < 1 || static_cast<int64_t>(T) * R > dradd::max_threads_for(static_cast<int>(K)) ||
-        (T * R) % 32 != 0 || (staged && R != 1))
+    // staged with R = 2: the plain quantised forms' pair kernel (two rows
+    // per thread, T threads a CTA, K <= 4)
+    const bool pair = staged && R == 2;
+    if (pair) {
+        if (add || !quant || K > 4 || T > dradd::max_threads_for(static_cast<int>(2 * K)))
+            return DRADD_ERR_BAD_CONFIG;
+    } else if (R < 1 || static_cast<int64_t>(T) * R > dradd::max_threads_for(static_cast<int>(K)) ||
+               (T * R) % 32 != 0 || (staged && R != 1)) {
         return DRADD_ERR_BAD_CONFIG;
+    }
 
-    const int threads = T * R;
+    const int threads = pair ? T : T * R;
     int ctas_per_sm = L.max_threads_per_sm / threads;
     if (ctas_per_sm > L.max_blocks_per_sm)
         ctas_per_sm = L.max_blocks_per_sm;
     if (staged) {
-        const int64_t stage_bytes = (add ? 4 : 2) * hidden;
-        const int64_t static_smem = static_cast<int64_t>(dradd::staged_static_smem(static_cast<int>(K)));
+        const int64_t stage_bytes = (add ? 4 : 2) * hidden * R;
+        const int64_t static_smem = static_cast<int64_t>(dradd::staged_static_smem(static_cast<int>(K), pair));
         // the quantised outputs keep the row's weights in fp32 beside the stages
         const int64_t weight_bytes = quant ? 4 * hidden : 0;
         const int64_t avail = L.smem_per_block_optin - static_smem - weight_bytes - 8 * 8;
@@ -627,19 +634,23 @@ dradd_status run(int out_kind, bool add, dradd_bf16* out, int8_t* out_q, float* 
                    : DRADD_ERR_CUDA;
     }
     const int K = static_cast<int>(next_pow2(hidden) / 8 / cfg.threads_per_row);
+    const bool pair = cfg.variant == DRADD_VARIANT_STAGED && cfg.rows_per_cta == 2;
     const size_t dyn = cfg.variant == DRADD_VARIANT_STAGED
-                           ? static_cast<size_t>(cfg.stages) * (add ? 4 : 2) * static_cast<size_t>(hidden) +
+                           ? static_cast<size_t>(cfg.stages) * (add ? 4 : 2) * static_cast<size_t>(hidden) *
+                                     static_cast<size_t>(cfg.rows_per_cta) +
                                  dradd::staged_weight_bytes(out_kind, static_cast<int>(hidden)) +
                                  8 * static_cast<size_t>(cfg.stages)
                            : 0;
     if (auto_grid && cfg.variant == DRADD_VARIANT_STAGED) {
-        // persistent grid: as many CTAs as fit on the device at once
+        // persistent grid: as many CTAs as fit on the device at once, at
+        // most one per unit (row, or pair of rows)
         int per_sm = 0;
-        if (dradd::staged_occupancy(K, out_kind, add, cfg.threads_per_row, dyn, &per_sm) != cudaSuccess)
+        if (dradd::staged_occupancy(K, out_kind, add, cfg.threads_per_row, dyn, &per_sm, pair) != cudaSuccess)
             return DRADD_ERR_CUDA;
         int64_t grid = static_cast<int64_t>(L.sm_count) * (per_sm > 0 ? per_sm : 1);
-        if (grid > n_rows)
-            grid = n_rows;
+        const int64_t units = pair ? (n_rows + 1) / 2 : n_rows;
+        if (grid > units)
+            grid = units;
         cfg.grid_ctas = static_cast<int>(grid);
     }
 

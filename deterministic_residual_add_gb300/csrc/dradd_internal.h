@@ -86,8 +86,9 @@ cudaError_t launch_rows(const Params& p, int K, int out, bool add, int grid, int
                         cudaStream_t stream);
 cudaError_t launch_staged(const Params& p, int K, int out, bool add, int grid, int threads,
                           size_t dyn_smem, bool serialize, cudaStream_t stream);
-cudaError_t staged_occupancy(int K, int out, bool add, int threads, size_t dyn_smem, int* blocks_per_sm);
-size_t staged_static_smem(int K);
+cudaError_t staged_occupancy(int K, int out, bool add, int threads, size_t dyn_smem, int* blocks_per_sm,
+                             bool pair = false);
+size_t staged_static_smem(int K, bool pair = false);
 // One function per (mode, output kind), each in its own translation unit.
 KernelFn staged_fn_add_bf16(int T, int K);
 KernelFn staged_fn_add_int8(int T, int K);
@@ -95,6 +96,9 @@ KernelFn staged_fn_add_e4m3(int T, int K);
 KernelFn staged_fn_add_e2m1(int T, int K);
 KernelFn staged_fn_norm_bf16(int T, int K);
 KernelFn staged_fn_norm_int8(int T, int K);
+KernelFn staged_pair_fn_norm_int8(int T, int K);
+KernelFn staged_pair_fn_norm_e4m3(int T, int K);
+KernelFn staged_pair_fn_norm_e2m1(int T, int K);
 KernelFn staged_fn_norm_e4m3(int T, int K);
 KernelFn staged_fn_norm_e2m1(int T, int K);
 // Warp-per-row kernels: K = P / 256 blocks of 8 per lane (1..16; with a

@@ -111,8 +111,18 @@ KernelFn rows_fn(int K, int out, bool add)
 #undef DRADD_ROWS_OUT
 }
 
-KernelFn staged_fn(int T, int K, int out, bool add)
+KernelFn staged_fn(int T, int K, int out, bool add, bool pair = false)
 {
+    if (pair) {
+        if (add)
+            return nullptr;
+        switch (out) {
+        case kOutInt8: return staged_pair_fn_norm_int8(T, K);
+        case kOutE4m3: return staged_pair_fn_norm_e4m3(T, K);
+        case kOutE2m1: return staged_pair_fn_norm_e2m1(T, K);
+        default: return nullptr;
+        }
+    }
     switch (out) {
     case kOutBf16: return add ? staged_fn_add_bf16(T, K) : staged_fn_norm_bf16(T, K);
     case kOutInt8: return add ? staged_fn_add_int8(T, K) : staged_fn_norm_int8(T, K);
@@ -130,17 +140,20 @@ int log2i(int v)
     return l;
 }
 
-// One bit per staged kernel: (add, out = 0..3, T = 32..1024, K = 1..8).
-int staged_index(int T, int K, int out, bool add)
+// One bit per staged kernel: (add, out = 0..3, T = 32..1024, K = 1..8); the
+// plain quantised pair kernels (out = 1..3) follow from 288.
+int staged_index(int T, int K, int out, bool add, bool pair = false)
 {
+    if (pair)
+        return 288 + (out - 1) * 24 + (log2i(T) - 5) * 4 + log2i(K);
     return ((add ? 4 : 0) + out) * 24 + (log2i(T) - 5) * 4 + log2i(K);
 }
 
 constexpr int kMaxDevices = 64;
-// Per device: bit k of word k / 64 set once staged kernel k (8 x 24 of them)
-// or split kernel k - 192 (4 x 24) has been allowed its full dynamic shared
-// memory.
-std::atomic<uint64_t> g_smem_attr_done[kMaxDevices][5];
+// Per device: bit k of word k / 64 set once staged kernel k (8 x 24 of them),
+// split kernel k - 192 (4 x 24) or pair kernel k - 288 (3 x 24) has been
+// allowed its full dynamic shared memory.
+std::atomic<uint64_t> g_smem_attr_done[kMaxDevices][6];
 std::atomic<unsigned*> g_status_ptr[kMaxDevices];
 
 cudaError_t ensure_smem_attr(KernelFn fn, int index, int dev)
@@ -203,14 +216,15 @@ cudaError_t launch_rows(const Params& p, int K, int out, bool add, int grid, int
 cudaError_t launch_staged(const Params& p, int K, int out, bool add, int grid, int threads,
                           size_t dyn_smem, bool serialize, cudaStream_t stream)
 {
-    KernelFn fn = staged_fn(threads, K, out, add);
+    const bool pair = p.rows_per_cta == 2;
+    KernelFn fn = staged_fn(threads, K, out, add, pair);
     if (!fn)
         return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    e = ensure_smem_attr(fn, staged_index(threads, K, out, add), dev);
+    e = ensure_smem_attr(fn, staged_index(threads, K, out, add, pair), dev);
     if (e != cudaSuccess)
         return e;
     return launch(fn, grid, threads, dyn_smem, serialize, stream, p);
@@ -338,16 +352,17 @@ cudaError_t warp_occupancy(int K, int out, bool add, int threads, size_t dyn_sme
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, threads, dyn_smem);
 }
 
-cudaError_t staged_occupancy(int K, int out, bool add, int threads, size_t dyn_smem, int* blocks_per_sm)
+cudaError_t staged_occupancy(int K, int out, bool add, int threads, size_t dyn_smem, int* blocks_per_sm,
+                             bool pair)
 {
-    KernelFn fn = staged_fn(threads, K, out, add);
+    KernelFn fn = staged_fn(threads, K, out, add, pair);
     if (!fn)
         return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    e = ensure_smem_attr(fn, staged_index(threads, K, out, add), dev);
+    e = ensure_smem_attr(fn, staged_index(threads, K, out, add, pair), dev);
     if (e != cudaSuccess)
         return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, threads, dyn_smem);
@@ -359,11 +374,12 @@ size_t split_static_smem(int K)
     return sizeof(float) * (2 * 32 * static_cast<size_t>(K) + 2 * 32 + 4);
 }
 
-size_t staged_static_smem(int K)
+size_t staged_static_smem(int K, bool pair)
 {
     // at most s_sum[2][K * 32] + s_max[2][32] + s_max2[32] (32 warps), as
-    // declared in staged_kernel
-    return sizeof(float) * (2 * 32 * static_cast<size_t>(K) + 3 * 32);
+    // declared in staged_kernel; twice each for staged_pair_kernel
+    const size_t one = 2 * 32 * static_cast<size_t>(K) + 3 * 32;
+    return sizeof(float) * (pair ? 2 * one : one);
 }
 
 namespace {

@@ -331,26 +331,40 @@ __global__ void __launch_bounds__(max_threads_for(K)) rows_kernel(const Params p
 constexpr uint32_t kL2PrefetchBytes = 16384;
 
 // -------------------------------------------------------------- staged_kernel
-// Per-row scale and codes of the quantised outputs in the staged kernel
-// (one row per CTA, T threads, compile-time): the row's amax over the CTA,
-// then the codes of each of the thread's blocks.
+// This thread's part of a row's amax, reduced over its warp: int8 with NaN
+// propagation (a row holding a NaN y shows as a NaN amax and takes the exact
+// path, whose amax ignores NaN); the other formats ignore NaN, as a running
+// max from 0.
+template <int K, int OUT>
+__device__ __forceinline__ float quant_warp_amax(const float (&y)[K][8])
+{
+    if constexpr (OUT == kOutInt8)
+        return warp_max_nan(tree_max_abs<K, true>(y));
+    else
+        return warp_max(fmaxf(0.0f, tree_max_abs<K, false>(y)));
+}
+
+// The CTA-wide amax from the W warps' values in red (lane l reads warp
+// l mod W; with W == 1, m is already the row's).
+template <int W, int OUT>
+__device__ __forceinline__ float quant_cta_amax(float m, const float* red, int lane)
+{
+    if constexpr (W > 1)
+        return OUT == kOutInt8 ? warp_max_nan(red[lane & (W - 1)]) : warp_max(red[lane & (W - 1)]);
+    else
+        return m;
+}
+
+// Per-row scale and codes of the quantised outputs (one row per T threads,
+// compile-time), given the row's amax m over the CTA.  Called by every
+// thread of the CTA: an int8 row whose amax is NaN takes a second,
+// NaN-ignoring amax through red_max2 (W floats of its own) and a barrier.
 template <int T, int K, int OUT>
-__device__ __forceinline__ void staged_quant_row(const Params& p, const float (&y)[K][8], int64_t row, int tid,
-                                                 int lane, int warp, int nblocks, float* red_max,
-                                                 float* red_max2)
+__device__ __forceinline__ void quant_row_finish(const Params& p, const float (&y)[K][8], float m, int64_t row,
+                                                 int tid, int lane, int warp, int nblocks, float* red_max2)
 {
     constexpr int W = T / 32;
     if constexpr (OUT == kOutInt8) {
-        // amax with NaN propagation: a row holding a NaN y shows as a NaN
-        // amax and takes the exact path (whose amax ignores NaN).
-        float m = tree_max_abs<K, true>(y);
-        m = warp_max_nan(m);
-        if constexpr (W > 1) {
-            if (lane == 0)
-                red_max[warp] = m;
-            __syncthreads();
-            m = warp_max_nan(red_max[lane & (W - 1)]);  // lane l reads warp l mod W
-        }
         uint2* qrow = reinterpret_cast<uint2*>(p.out_q + row * p.hidden);
         if (!isnan(m)) {
             const float scale = div_const_rn<127>(m);
@@ -370,8 +384,7 @@ __device__ __forceinline__ void staged_quant_row(const Params& p, const float (&
             }
         } else {
             // uniform over the CTA: every thread holds the same m
-            float m2 = fmaxf(0.0f, tree_max_abs<K, false>(y));  // NaN ignored, as a running max from 0
-            m2 = warp_max(m2);
+            float m2 = warp_max(fmaxf(0.0f, tree_max_abs<K, false>(y)));  // NaN ignored, as a running max from 0
             if constexpr (W > 1) {
                 if (lane == 0)
                     red_max2[warp] = m2;
@@ -389,14 +402,6 @@ __device__ __forceinline__ void staged_quant_row(const Params& p, const float (&
             }
         }
     } else {
-        float m = fmaxf(0.0f, tree_max_abs<K, false>(y));  // NaN ignored, as a running max from 0
-        m = warp_max(m);
-        if constexpr (W > 1) {
-            if (lane == 0)
-                red_max[warp] = m;
-            __syncthreads();
-            m = warp_max(red_max[lane & (W - 1)]);
-        }
         const float scale = div_const_rn<quant_divisor(OUT)>(m);
         if (tid == 0)
             p.scale[row] = scale;
@@ -420,6 +425,25 @@ __device__ __forceinline__ void staged_quant_row(const Params& p, const float (&
             }
         }
     }
+}
+
+// Per-row scale and codes of the quantised outputs in the staged kernel
+// (one row per CTA, T threads, compile-time): the row's amax over the CTA,
+// then the codes of each of the thread's blocks.
+template <int T, int K, int OUT>
+__device__ __forceinline__ void staged_quant_row(const Params& p, const float (&y)[K][8], int64_t row, int tid,
+                                                 int lane, int warp, int nblocks, float* red_max,
+                                                 float* red_max2)
+{
+    constexpr int W = T / 32;
+    float m = quant_warp_amax<K, OUT>(y);
+    if constexpr (W > 1) {
+        if (lane == 0)
+            red_max[warp] = m;
+        __syncthreads();
+    }
+    m = quant_cta_amax<W, OUT>(m, red_max, lane);
+    quant_row_finish<T, K, OUT>(p, y, m, row, tid, lane, warp, nblocks, red_max2);
 }
 
 // T (threads per row = threads per CTA) is a compile-time constant so that
@@ -588,6 +612,218 @@ __global__ void __launch_bounds__(T, staged_min_blocks(T, K)) staged_kernel(cons
             parity ^= 1u;
         }
     }
+}
+
+// ---------------------------------------------------------- staged_pair_kernel
+// The plain RMSNorm with quantised out, two rows per thread: a unit is the
+// pair of adjacent rows 2u, 2u + 1 (the last alone when n_rows is odd),
+// staged by one bulk copy, and every thread carries both rows through the
+// same steps as staged_kernel, so one barrier serves both rows' sums and one
+// both rows' amax, and the two rows' dependent chains interleave.  Each row
+// gets exactly the arithmetic of staged_kernel (same tree, same epilogue).
+template <int T, int K, int OUT>
+__global__ void __launch_bounds__(T, staged_min_blocks(T, 2 * K)) staged_pair_kernel(const Params p)
+{
+    static_assert(T >= 32 && T <= 1024 && (T & (T - 1)) == 0, "T: a power of two, 32..1024");
+    static_assert(OUT != kOutBf16, "quantised outputs only");
+    constexpr int W = T / 32;
+    extern __shared__ __align__(128) unsigned char stage_mem[];
+    __shared__ float s_sum[2][2][K * W];
+    __shared__ float s_max[2][2][W];
+    __shared__ float s_max2[2][W];
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nblocks = p.hidden >> 3;
+    const int stages = p.stages;
+    const uint32_t row_bytes = static_cast<uint32_t>(p.hidden) * 2u;
+    const uint32_t stage_bytes = 2u * row_bytes;
+    unsigned char* const after_stages = stage_mem + static_cast<size_t>(stages) * stage_bytes;
+    float4* const w_lo = reinterpret_cast<float4*>(after_stages);
+    float4* const w_hi = w_lo + nblocks;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(after_stages + staged_weight_bytes(OUT, p.hidden));
+    const int64_t stride = gridDim.x;
+    const int64_t n_units = (p.n_rows + 1) / 2;
+
+    // bytes of unit u: one or two rows
+    auto unit_bytes = [&](int64_t u) -> uint32_t {
+        return 2 * u + 1 < p.n_rows ? stage_bytes : row_bytes;
+    };
+    if (tid == 0) {
+        if (p.l2_prefetch && static_cast<int64_t>(blockIdx.x) < n_units)
+            prefetch_l2(p.x + 2 * static_cast<int64_t>(blockIdx.x) * p.hidden, unit_bytes(blockIdx.x));
+        for (int s = 0; s < stages; ++s)
+            mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    wait_prior_grids();
+    allow_next_grid();
+
+    const uint64_t policy = l2_policy_evict_first();
+    auto issue = [&](int s, int64_t u) {
+        const uint32_t bytes = unit_bytes(u);
+        mbar_arrive_expect_tx(&bars[s], bytes);
+        bulk_copy_g2s(stage_mem + static_cast<size_t>(s) * stage_bytes, p.x + 2 * u * p.hidden, bytes, &bars[s],
+                      policy);
+    };
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) {
+            const int64_t u = blockIdx.x + s * stride;
+            if (u >= n_units)
+                break;
+            if (p.fault_inject && s == 0)
+                continue;  // test hook: this copy never comes, so its wait expires
+            issue(s, u);
+        }
+    }
+    {
+        // each thread widens the weights of its own blocks (only it reads them)
+        const uint4* wrow = reinterpret_cast<const uint4*>(p.weight);
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const int b = tid + j * T;
+            if (b < nblocks) {
+                float f[8];
+                unpack8(__ldg(wrow + b), f);
+                w_lo[b] = make_float4(f[0], f[1], f[2], f[3]);
+                w_hi[b] = make_float4(f[4], f[5], f[6], f[7]);
+            }
+        }
+    }
+
+    int buf = 0;
+    int64_t i = 0;
+    int s = 0;
+    uint32_t parity = 0;
+    for (int64_t u = blockIdx.x; u < n_units; u += stride, ++i) {
+        const bool ok = mbar_wait_bounded(&bars[s], parity, p.wait_limit_ns);
+        const int64_t row0 = 2 * u;
+        const bool two = row0 + 1 < p.n_rows;  // uniform over the CTA
+        const uint4* xs0 = reinterpret_cast<const uint4*>(stage_mem + static_cast<size_t>(s) * stage_bytes);
+        const uint4* xs1 = xs0 + (row_bytes >> 4);
+        float a0[K][8], a1[K][8], part0[K], part1[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const int b = tid + j * T;
+            if (b < nblocks) {
+                unpack8(xs0[b], a0[j]);
+                part0[j] = fold8_squares(a0[j]);
+                if (two) {
+                    unpack8(xs1[b], a1[j]);
+                    part1[j] = fold8_squares(a1[j]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        a1[j][e] = 0.0f;
+                    part1[j] = 0.0f;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    a0[j][e] = 0.0f;
+                    a1[j][e] = 0.0f;
+                }
+                part0[j] = 0.0f;
+                part1[j] = 0.0f;
+            }
+        }
+        int jsub0, jsub1;
+        const float v0 = warp_halving_sum<K>(part0, lane, jsub0);
+        const float v1 = warp_halving_sum<K>(part1, lane, jsub1);
+        if constexpr (W > 1) {
+            if (lane < K) {
+                s_sum[buf][0][jsub0 * W + warp] = v0;
+                s_sum[buf][1][jsub1 * W + warp] = v1;
+            }
+        }
+        // Every thread has read stage s (so it can be refilled) and published
+        // its warps' subtree sums; any expired wait ends the CTA here.
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                record_timeout(p);
+                drain_issued_copies(p, bars, s, parity, i, stages, blockIdx.x, stride, n_units);
+            }
+            return;
+        }
+        if (tid == 0) {
+            const int64_t next = u + static_cast<int64_t>(stages) * stride;
+            if (next < n_units) {
+                fence_proxy_async_smem();
+                issue(s, next);
+            }
+        }
+        float sum0, sum1;
+        if constexpr (W > 1) {
+            sum0 = cross_warp_sum<K, W>(s_sum[buf][0], lane);
+            sum1 = cross_warp_sum<K, W>(s_sum[buf][1], lane);
+        } else {
+            sum0 = fold_lane_subtrees<K>(v0);
+            sum1 = fold_lane_subtrees<K>(v1);
+        }
+        const float inv0 = inv_rms(sum0, p.hidden, p.inv_hidden, p.eps);
+        const float inv1 = inv_rms(sum1, p.hidden, p.inv_hidden, p.eps);
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const int b = tid + j * T;
+            if (b < nblocks) {
+                const float4 wl = w_lo[b], wh = w_hi[b];
+                scale8_f32(a0[j], inv0, wl, wh);
+                scale8_f32(a1[j], inv1, wl, wh);
+            }
+        }
+        float m0 = quant_warp_amax<K, OUT>(a0);
+        float m1 = quant_warp_amax<K, OUT>(a1);
+        if constexpr (W > 1) {
+            if (lane == 0) {
+                s_max[buf][0][warp] = m0;
+                s_max[buf][1][warp] = m1;
+            }
+            __syncthreads();
+        }
+        m0 = quant_cta_amax<W, OUT>(m0, s_max[buf][0], lane);
+        m1 = quant_cta_amax<W, OUT>(m1, s_max[buf][1], lane);
+        quant_row_finish<T, K, OUT>(p, a0, m0, row0, tid, lane, warp, nblocks, s_max2[0]);
+        if (two)
+            quant_row_finish<T, K, OUT>(p, a1, m1, row0 + 1, tid, lane, warp, nblocks, s_max2[1]);
+        buf ^= 1;
+        if (++s == stages) {
+            s = 0;
+            parity ^= 1u;
+        }
+    }
+}
+
+template <int T, int K, int OUT>
+KernelFn staged_pair_pick()
+{
+    if constexpr (T <= max_threads_for(2 * K))
+        return staged_pair_kernel<T, K, OUT>;
+    else
+        return nullptr;
+}
+
+// Pair kernels for T = 32..512 and K in {1, 2, 4} (two rows' accumulators
+// per thread, so the register budget of 2 K blocks).
+template <int OUT>
+KernelFn staged_pair_table(int T, int K)
+{
+#define DRADD_PAIR_K(TT)                                   \
+    switch (K) {                                           \
+    case 1: return staged_pair_pick<TT, 1, OUT>();         \
+    case 2: return staged_pair_pick<TT, 2, OUT>();         \
+    case 4: return staged_pair_pick<TT, 4, OUT>();         \
+    default: return nullptr;                               \
+    }
+    switch (T) {
+    case 32: DRADD_PAIR_K(32)
+    case 64: DRADD_PAIR_K(64)
+    case 128: DRADD_PAIR_K(128)
+    case 256: DRADD_PAIR_K(256)
+    case 512: DRADD_PAIR_K(512)
+    default: return nullptr;
+    }
+#undef DRADD_PAIR_K
 }
 
 // ------------------------------------------------------- staged kernel table

@@ -6,5 +6,6 @@
 namespace dradd {
 
 KernelFn staged_fn_norm_e2m1(int T, int K) { return staged_table<kOutE2m1, false>(T, K); }
+KernelFn staged_pair_fn_norm_e2m1(int T, int K) { return staged_pair_table<kOutE2m1>(T, K); }
 
 }  // namespace dradd

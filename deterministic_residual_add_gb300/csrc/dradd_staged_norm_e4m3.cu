@@ -6,5 +6,6 @@
 namespace dradd {
 
 KernelFn staged_fn_norm_e4m3(int T, int K) { return staged_table<kOutE4m3, false>(T, K); }
+KernelFn staged_pair_fn_norm_e4m3(int T, int K) { return staged_pair_table<kOutE4m3>(T, K); }
 
 }  // namespace dradd

@@ -6,5 +6,6 @@
 namespace dradd {
 
 KernelFn staged_fn_norm_int8(int T, int K) { return staged_table<kOutInt8, false>(T, K); }
+KernelFn staged_pair_fn_norm_int8(int T, int K) { return staged_pair_table<kOutInt8>(T, K); }
 
 }  // namespace dradd

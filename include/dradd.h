@@ -144,9 +144,13 @@ dradd_status add_rmsnorm_quant_fwd(int8_t* out_q, float* scale, dradd_bf16* resi
  *   threads_per_row  power of two T with T * K * 8 == P (P = next power of
  *                    two >= hidden) for some K in {1, 2, 4, 8}: thread t of
  *                    a row owns the 8-element blocks t, t + T, ..., t + (K-1)T.
- *   rows_per_cta     rows processed side by side by one CTA (ROWS only);
+ *   rows_per_cta     ROWS: rows processed side by side by one CTA;
  *                    threads_per_row * rows_per_cta <= 1024 and a multiple
- *                    of 32.
+ *                    of 32.  STAGED: 1, or 2 for the plain RMSNorm with
+ *                    int8, e4m3 or e2m1 out with K <= 4: every thread of a
+ *                    CTA of threads_per_row threads carries two adjacent
+ *                    rows through each step (one bulk copy and one barrier
+ *                    per step serve both; a stage holds both rows).
  *   grid_ctas        number of CTAs; each loops over rows with a stride of
  *                    grid_ctas * rows_per_cta.
  *   stages           STAGED only: rows in flight per CTA (1..8), limited by

@@ -188,6 +188,27 @@ def test_bad_configs_rejected(L, cfg):
     assert e.value.status == 9
 
 
+def test_staged_pair_rule(L):
+    """rows_per_cta = 2 on the staged variant: the plain quantised forms'
+    two-rows-per-thread kernel, K <= 4; refused for bf16 out, the residual
+    forms and K = 8; its grid is at most one CTA per pair of rows."""
+    pair = dr.LaunchConfig(variant=dr.VARIANT_STAGED, rows_per_cta=2)
+    for kw in (dict(), dict(fp8=True), dict(fp4=True)):
+        c = dr.resolve_config(4096, 4096, quant=True, add=False, sm_count=152, config=pair, **kw)
+        assert (c.variant, c.rows_per_cta, c.threads_per_row, c.blocks_per_thread) == (dr.VARIANT_STAGED, 2, 128, 4)
+        assert 1 <= c.grid_ctas <= 2048
+    c = dr.resolve_config(5, 4096, quant=True, add=False, sm_count=152, config=pair)
+    assert c.grid_ctas == 3
+    for kw in (dict(quant=False, add=False), dict(quant=True, add=True)):
+        with pytest.raises(dr.DraddError) as e:
+            dr.resolve_config(4096, 4096, sm_count=152, config=pair, **kw)
+        assert e.value.status == 9
+    with pytest.raises(dr.DraddError) as e:
+        dr.resolve_config(64, 8192, quant=True, add=False, sm_count=152,
+                          config=dr.LaunchConfig(variant=dr.VARIANT_STAGED, rows_per_cta=2, threads_per_row=128))
+    assert e.value.status == 9
+
+
 def test_staged_stages_limited_by_shared_memory(L):
     with pytest.raises(dr.DraddError):
         dr.resolve_config(16, 32768, sm_count=152, config=dr.LaunchConfig(variant=2, stages=2))
