@@ -209,6 +209,24 @@ def test_staged_pair_rule(L):
     assert e.value.status == 9
 
 
+@pytest.mark.parametrize("n,h,T", [(16384, 1024, 64), (8192, 2048, 128), (2048, 8192, 256), (1024, 16384, 512),
+                                   (512, 4096, 512), (608, 4096, 512), (608, 2048, 256), (609, 2048, 128),
+                                   (37, 1000, 128)])
+def test_auto_plain_quantised_takes_the_pair_kernel(L, n, h, T):
+    for kw in (dict(), dict(fp8=True), dict(fp4=True)):
+        c = dr.resolve_config(n, h, quant=True, add=False, sm_count=152, **kw)
+        assert (c.variant, c.rows_per_cta, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 2, T, 1), (n, h, kw)
+        assert c.grid_ctas <= (n + 1) // 2
+    # not for bf16 out, the residual forms, P = 4096 beyond 4 rows per SM, P = 512 or P = 32768
+    assert dr.resolve_config(4096, 4096, add=False, sm_count=152).rows_per_cta == 1
+    for kw in (dict(), dict(fp8=True)):
+        c = dr.resolve_config(609, 4096, quant=True, add=False, sm_count=152, **kw)
+        assert (c.variant, c.rows_per_cta, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 1, 128, 1)
+    assert dr.resolve_config(4096, 4096, quant=True, sm_count=152).rows_per_cta == 1
+    assert dr.resolve_config(8192, 512, quant=True, add=False, sm_count=152).variant == dr.VARIANT_WARP
+    assert dr.resolve_config(64, 32768, quant=True, add=False, sm_count=152).rows_per_cta == 1
+
+
 def test_staged_stages_limited_by_shared_memory(L):
     with pytest.raises(dr.DraddError):
         dr.resolve_config(16, 32768, sm_count=152, config=dr.LaunchConfig(variant=2, stages=2))
