@@ -62,10 +62,13 @@ WORKLOADS = {
     "quant4096x4096": (4096, 4096, "add_rmsnorm_quant", "chain4096"),
     "rmsnorm4096x4096": (4096, 4096, "rmsnorm", "chain4096"),
     "rmsnorm_quant4096x4096": (4096, 4096, "rmsnorm_quant", "chain4096"),
+    "rmsnorm_quant2048x8192": (2048, 8192, "rmsnorm_quant", "4096x8192"),
+    "rmsnorm_quant16384x1024": (16384, 1024, "rmsnorm_quant", "tiny"),
     "residual_add4096x4096": (4096, 4096, "residual_add", "chain4096"),
     "fp8_2048x16384": (2048, 16384, "add_rmsnorm_fp8", "quant2048x16384"),
     "fp8_4096x4096": (4096, 4096, "add_rmsnorm_fp8", "chain4096"),
     "rmsnorm_fp8_4096x4096": (4096, 4096, "rmsnorm_fp8", "chain4096"),
+    "rmsnorm_fp8_2048x8192": (2048, 8192, "rmsnorm_fp8", "4096x8192"),
     "fp4_2048x16384": (2048, 16384, "add_rmsnorm_fp4", "quant2048x16384"),
     "fp4_4096x4096": (4096, 4096, "add_rmsnorm_fp4", "chain4096"),
 }
@@ -432,6 +435,7 @@ def workload_inputs(name: str, n_sets: int = N_SETS):
     c = inputs.WORKLOADS[recipe].make(n_rows=n)
     xs = [c["x"]] + [inputs.normal_bf16(inputs.generator(1000 + k), (n, h), 0.0, 1.0)
                      for k in range(1, n_sets)]
+    assert all(tuple(x.shape) == (n, h) for x in xs) and tuple(c["residual"].shape) == (n, h), name
     return xs, c["residual"], c["weight"]
 
 

@@ -27,13 +27,14 @@ __all__ = [
     "lse_merge_fwd", "invariant_unary_fwd", "UNARY_OPS",
     "LaunchConfig", "DraddError", "resolve_config",
     "device_status", "last_device_status", "bf16_convert_range", "status_string", "abi_version", "lib",
-    "library_path", "VARIANT_AUTO", "VARIANT_ROWS", "VARIANT_STAGED", "VARIANT_SPLIT", "VARIANT_WARP", "MAX_HIDDEN",
+    "library_path", "VARIANT_AUTO", "VARIANT_ROWS", "VARIANT_STAGED", "VARIANT_SPLIT", "VARIANT_WARP",
+    "VARIANT_CHUNK", "MAX_HIDDEN",
 ]
 
 PKG = Path(__file__).resolve().parent
 LIB_PATH = PKG / "libdradd.so"
 MAX_HIDDEN = 32768
-VARIANT_AUTO, VARIANT_ROWS, VARIANT_STAGED, VARIANT_SPLIT, VARIANT_WARP = 0, 1, 2, 3, 4
+VARIANT_AUTO, VARIANT_ROWS, VARIANT_STAGED, VARIANT_SPLIT, VARIANT_WARP, VARIANT_CHUNK = 0, 1, 2, 3, 4, 5
 OP_ADD_RMSNORM, OP_ADD_RMSNORM_QUANT, OP_RMSNORM, OP_RMSNORM_QUANT = 0, 1, 2, 3
 OP_ADD_RMSNORM_FP8, OP_RMSNORM_FP8 = 4, 5
 OP_ADD_RMSNORM_FP4, OP_RMSNORM_FP4 = 6, 7

@@ -717,7 +717,7 @@ struct QkSide {
 struct QkLaunch {
     QkSide q, k;
     int threads = 0;
-    bool staged = false, warp = false, serialize = false;
+    bool staged = false, warp = false, chunk = false, serialize = false;
     int64_t dyn_smem = 0;
 };
 
@@ -805,6 +805,83 @@ dradd_status qk_plan_warp(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, bool
     return DRADD_OK;
 }
 
+// The chunked-q plan (DRADD_VARIANT_CHUNK): the q rows (512 < P <= 4096)
+// in 512-element chunks, one warp a chunk and one CTA a row; the k rows
+// one warp each (256 <= P <= 2048) in CTAs of the same number of warps.
+// Both sides get `stages` ring slots per warp (0 = 2).  CTAs (grid_ctas):
+// automatic SMs x ctas_per_sm (<= 0: 2048 / threads); when the two sides
+// need more, they share them in proportion to their elements.
+dradd_status qk_plan_chunk(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, bool add, int sm_count,
+                           int ctas_per_sm, int smem_optin, const dradd_launch_cfg& cfg, QkLaunch* out)
+{
+    QkSide* q = &out->q;
+    QkSide* k = &out->k;
+    if (cfg.rows_per_cta != 0 || cfg.threads_per_row != 0 || cfg.blocks_per_thread != 0 || cfg.cluster_ctas != 0 ||
+        cfg.fault_inject < 0 || cfg.grid_ctas < 0 || cfg.wait_limit_us < 0 || cfg.stages < 0 || cfg.stages > 8 ||
+        (cfg.serialize != 0 && cfg.serialize != 1))
+        return DRADD_ERR_BAD_CONFIG;
+    if (!q->active)
+        return DRADD_ERR_BAD_CONFIG;  // the variant is defined by its q rows
+    const int64_t pq = next_pow2(hq);
+    if (pq <= 512 || pq > 4096)
+        return DRADD_ERR_BAD_CONFIG;
+    const int nw = static_cast<int>((hq + dradd::kChunkElems - 1) / dradd::kChunkElems);
+    const int S = cfg.stages != 0 ? cfg.stages : 2;
+    out->chunk = true;
+    out->staged = false;
+    out->warp = false;
+    out->serialize = cfg.serialize != 0;
+    out->threads = 32 * nw;
+    q->K = dradd::kChunkBlocks / 32;
+    q->T = 32 * nw;
+    q->R = 1;
+    q->stages = S;
+    out->dyn_smem = static_cast<int64_t>(dradd::chunk_smem_bytes(S, nw, static_cast<int>(hq), add));
+    if (k->active) {
+        const int64_t blocks = next_pow2(hk) / 8;
+        if (blocks < 32 || blocks / 32 > 8)
+            return DRADD_ERR_BAD_CONFIG;
+        k->K = static_cast<int>(blocks / 32);
+        k->T = 32;
+        k->R = nw;
+        k->stages = S;
+        const int64_t need = static_cast<int64_t>(dradd::warp_smem_bytes(S, nw, static_cast<int>(hk), false));
+        if (need > out->dyn_smem)
+            out->dyn_smem = need;
+    }
+    if (out->dyn_smem > smem_optin - 1024)
+        return DRADD_ERR_BAD_CONFIG;
+    const int64_t need_q = n_q;
+    const int64_t need_k = k->active ? (n_k + nw - 1) / nw : 0;
+    int64_t C = cfg.grid_ctas;
+    if (C == 0)
+        C = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * (ctas_per_sm > 0 ? ctas_per_sm : 2048 / out->threads);
+    if (C < 1 + (k->active ? 1 : 0))
+        return DRADD_ERR_BAD_CONFIG;
+    if (need_q + need_k <= C) {
+        q->ctas = need_q;
+        k->ctas = need_k;
+    } else {
+        const double wq = static_cast<double>(n_q) * static_cast<double>(hq);
+        const double wk = k->active ? static_cast<double>(n_k) * static_cast<double>(hk) : 0.0;
+        int64_t cq = static_cast<int64_t>(static_cast<double>(C) * wq / (wq + wk) + 0.5);
+        if (cq < 1)
+            cq = 1;
+        if (k->active && cq > C - 1)
+            cq = C - 1;
+        if (cq > need_q)
+            cq = need_q;
+        int64_t ck = C - cq;
+        if (ck > need_k)
+            ck = need_k;
+        q->ctas = cq;
+        k->ctas = ck;
+    }
+    if (q->ctas + k->ctas > 0x7FFFFFFF)
+        return DRADD_ERR_BAD_CONFIG;
+    return DRADD_OK;
+}
+
 // Shapes and the launch plan of the fused q/k call.  A side with no rows
 // takes no part.  Variant, threads per CTA B (cfg->threads_per_row) and a
 // least K (cfg->blocks_per_thread) default to the table below.  Each side
@@ -848,6 +925,8 @@ dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t g
         return (q->active || k->active)
                    ? qk_plan_warp(n_q, hq, n_k, hk, add, sm_count, ctas_per_sm, smem_optin, cfg, out)
                    : DRADD_OK;
+    if (cfg.variant == DRADD_VARIANT_CHUNK)
+        return qk_plan_chunk(n_q, hq, n_k, hk, add, sm_count, ctas_per_sm, smem_optin, cfg, out);
     if (cfg.variant < DRADD_VARIANT_AUTO || cfg.variant > DRADD_VARIANT_STAGED || cfg.rows_per_cta != 0 ||
         cfg.stages < 0 || cfg.stages > 8 || cfg.fault_inject < 0 || cfg.wait_limit_us < 0 || cfg.grid_ctas < 0 ||
         (cfg.serialize != 0 && cfg.serialize != 1) ||
@@ -889,12 +968,26 @@ dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t g
     // an explicit stage count or the fault hook asks for the staged variant
     if (cfg.variant == DRADD_VARIANT_AUTO && (cfg.stages != 0 || cfg.fault_inject != 0))
         auto_variant = DRADD_VARIANT_STAGED;
+    const bool auto_plain = cfg.variant == DRADD_VARIANT_AUTO && cfg.stages == 0 && cfg.fault_inject == 0 &&
+                            cfg.threads_per_row == 0 && cfg.blocks_per_thread == 0;
+    // q rows wider than 1536 up to P = 4096 (k rows 256 <= P <= 2048, or
+    // none): the q rows in 512-element chunks, one warp each, one stage with
+    // e4m3 groups and two with bf16 out (4096 x 3072 q + 1024 k: 25.3 us
+    // against 33.2 staged; 4096 x 4096 + 512: 29.8 against 32.1; 4096 x
+    // 2048 + 512: 15.4 against 16.2 one warp a row; 2048 x 4096 bf16 +
+    // 1024: 10.0 against 12.9; at 1536, three chunks, it lost).
+    if (auto_plain && q->active && hq > 1536 && next_pow2(hq) <= 4096 &&
+        (!k->active || (next_pow2(hk) >= 256 && next_pow2(hk) <= 2048))) {
+        dradd_launch_cfg c = cfg;
+        c.variant = DRADD_VARIANT_CHUNK;
+        c.stages = group_size != 0 ? 1 : 2;
+        return qk_plan_chunk(n_q, hq, n_k, hk, add, sm_count, ctas_per_sm, smem_optin, c, out);
+    }
     // Both sides 256 < P <= 2048 (the low-rank q / kv layout) with 8192 rows
     // or more: one warp a row with a ring of 2 row slots per warp, 128
     // threads a CTA (4096 tokens of 1536 + 512: 13.41 us against 14.21 for
     // the register variant).
-    if (cfg.variant == DRADD_VARIANT_AUTO && cfg.stages == 0 && cfg.fault_inject == 0 &&
-        cfg.threads_per_row == 0 && cfg.blocks_per_thread == 0 && rows >= 8192 && max_p <= 2048) {
+    if (auto_plain && rows >= 8192 && max_p <= 2048) {
         bool fits = true;
         for (const QkSide* side : {q, k})
             if (side->active && next_pow2(side->hidden) <= 256)
@@ -1014,7 +1107,8 @@ dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t g
 
 int qk_mode(const QkLaunch& plan)
 {
-    return plan.warp ? dradd::kQkWarp : plan.staged ? dradd::kQkStaged : dradd::kQkRows;
+    return plan.chunk ? dradd::kQkChunk : plan.warp ? dradd::kQkWarp : plan.staged ? dradd::kQkStaged
+                                                                                  : dradd::kQkRows;
 }
 
 // qk_plan on the current device (limits L): the staged and warp-per-row
@@ -1024,7 +1118,7 @@ dradd_status qk_plan_on_device(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk,
                                const DeviceLimits& L, const dradd_launch_cfg* cfg, QkLaunch* plan)
 {
     dradd_status st = qk_plan(n_q, hq, n_k, hk, group_size, add, L.sm_count, 0, L.smem_per_block_optin, cfg, plan);
-    if (st != DRADD_OK || !(plan->staged || plan->warp) || (cfg && cfg->grid_ctas != 0))
+    if (st != DRADD_OK || !(plan->staged || plan->warp || plan->chunk) || (cfg && cfg->grid_ctas != 0))
         return st;
     const bool quant = group_size != 0;
     const int kq = plan->q.active ? plan->q.K : 1, kk = plan->k.active ? plan->k.K : 1;
@@ -1101,7 +1195,7 @@ dradd_status qk_run(void* q_out, float* q_scale, dradd_bf16* q_residual_out, dra
     if (!device_memory) {
         if (eff.variant == DRADD_VARIANT_STAGED || eff.stages != 0 || eff.fault_inject != 0)
             return DRADD_ERR_BAD_CONFIG;
-        if (eff.variant == DRADD_VARIANT_WARP)
+        if (eff.variant == DRADD_VARIANT_WARP || eff.variant == DRADD_VARIANT_CHUNK)
             return DRADD_ERR_BAD_CONFIG;  // bulk copies read device memory only
         eff.variant = DRADD_VARIANT_ROWS;
     }
@@ -1548,7 +1642,10 @@ dradd_status dradd_qk_resolve_config(int64_t n_q_rows, int64_t q_hidden, int64_t
     if (st != DRADD_OK)
         return st;
     plan->variant = r.threads == 0 ? 0
-                    : (r.warp ? DRADD_VARIANT_WARP : r.staged ? DRADD_VARIANT_STAGED : DRADD_VARIANT_ROWS);
+                    : (r.chunk  ? DRADD_VARIANT_CHUNK
+                       : r.warp ? DRADD_VARIANT_WARP
+                       : r.staged ? DRADD_VARIANT_STAGED
+                                  : DRADD_VARIANT_ROWS);
     plan->threads_per_cta = r.threads;
     plan->dyn_smem_bytes = static_cast<int>(r.dyn_smem);
     plan->q_threads_per_row = r.q.T;

@@ -113,6 +113,24 @@ constexpr size_t warp_smem_bytes(int stages, int rows, int hidden, bool add)
                static_cast<size_t>(hidden) +
            4u * static_cast<size_t>(hidden) + 8u * static_cast<size_t>(stages) * static_cast<size_t>(rows);
 }
+
+// Chunked rows (the fused q/k call's CHUNK variant): kChunkElems elements
+// a warp.  Dynamic shared memory of a CTA of nw chunk warps: the rings of
+// `stages` chunk slots per warp, the row's fp32 weights, the chunk sums
+// (2 x 8 floats) and the mbarriers.
+constexpr int kChunkElems = 512;
+constexpr int kChunkBlocks = kChunkElems / 8;
+
+__host__ __device__ constexpr uint32_t chunk_slot_bytes(bool add)
+{
+    return (add ? 2u : 1u) * kChunkElems * 2u;
+}
+
+__host__ __device__ constexpr size_t chunk_smem_bytes(int stages, int nw, int hidden, bool add)
+{
+    return static_cast<size_t>(nw) * stages * chunk_slot_bytes(add) + 4u * static_cast<size_t>(hidden) + 64u +
+           8u * static_cast<size_t>(nw) * stages;
+}
 KernelFn warp_fn_add(int out, int K);
 KernelFn warp_fn_norm(int out, int K);
 cudaError_t launch_warp(const Params& p, int K, int out, bool add, int grid, int threads, size_t dyn_smem,
@@ -131,7 +149,7 @@ size_t split_static_smem(int K);
 // e4m3 q out (else bf16); add: q has a residual; staged: rows staged
 // through dyn_smem bytes of shared memory (else loaded into registers).
 // mode: how each side's rows reach the registers.
-enum QkMode : int { kQkRows = 0, kQkStaged = 1, kQkWarp = 2 };
+enum QkMode : int { kQkRows = 0, kQkStaged = 1, kQkWarp = 2, kQkChunk = 3 };
 cudaError_t launch_qk(const Params& pq, const Params& pk, int kq, int kk, bool quant, bool add, int mode,
                       int q_ctas, int k_ctas, int threads, size_t dyn_smem, bool serialize, cudaStream_t stream);
 cudaError_t qk_occupancy(int kq, int kk, bool quant, bool add, int mode, int threads, size_t dyn_smem,
@@ -142,6 +160,8 @@ QkKernelFn qk_fn_e4m3_rows(int kq, int kk, bool add);
 QkKernelFn qk_fn_e4m3_staged(int kq, int kk, bool add);
 QkKernelFn qk_fn_bf16_warp(int kq, int kk, bool add);
 QkKernelFn qk_fn_e4m3_warp(int kq, int kk, bool add);
+QkKernelFn qk_fn_bf16_chunk(int kk, bool add);
+QkKernelFn qk_fn_e4m3_chunk(int kk, bool add);
 // Static shared memory of a qk kernel whose sides have kq / kk blocks per thread.
 size_t qk_static_smem(int kq, int kk);
 // l2_prefetch: all three are device memory (each CTA's first vectors are

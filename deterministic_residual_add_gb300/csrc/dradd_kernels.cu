@@ -386,6 +386,8 @@ namespace {
 
 QkKernelFn qk_fn(int kq, int kk, bool quant, bool add, int mode)
 {
+    if (mode == kQkChunk)
+        return quant ? qk_fn_e4m3_chunk(kk, add) : qk_fn_bf16_chunk(kk, add);
     if (mode == kQkWarp)
         return quant ? qk_fn_e4m3_warp(kq, kk, add) : qk_fn_bf16_warp(kq, kk, add);
     const bool staged = mode == kQkStaged;
@@ -394,10 +396,10 @@ QkKernelFn qk_fn(int kq, int kk, bool quant, bool add, int mode)
     return staged ? qk_fn_bf16_staged(kq, kk, add) : qk_fn_bf16_rows(kq, kk, add);
 }
 
-// One bit per staged (word 0) or warp-per-row (word 1) qk kernel (kq, kk,
-// quant, add): its dynamic shared memory limit has been raised to the
-// device's opt-in maximum.
-std::atomic<uint64_t> g_qk_smem_done[kMaxDevices][2];
+// One bit per staged (word 0), warp-per-row (word 1) or chunked-q (word 2)
+// qk kernel (kq, kk, quant, add): its dynamic shared memory limit has been
+// raised to the device's opt-in maximum.
+std::atomic<uint64_t> g_qk_smem_done[kMaxDevices][3];
 
 cudaError_t qk_prepare(QkKernelFn fn, int kq, int kk, bool quant, bool add, int mode)
 {
@@ -407,9 +409,10 @@ cudaError_t qk_prepare(QkKernelFn fn, int kq, int kk, bool quant, bool add, int 
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    const uint64_t bit = 1ull << (((log2i(kq) * 4 + log2i(kk)) * 2 + (quant ? 1 : 0)) * 2 + (add ? 1 : 0));
-    std::atomic<uint64_t>* word =
-        dev >= 0 && dev < kMaxDevices ? &g_qk_smem_done[dev][mode == kQkWarp ? 1 : 0] : nullptr;
+    const int kq_bits = mode == kQkChunk ? 0 : log2i(kq);  // the chunked kernels have no kq
+    const uint64_t bit = 1ull << (((kq_bits * 4 + log2i(kk)) * 2 + (quant ? 1 : 0)) * 2 + (add ? 1 : 0));
+    const int w = mode == kQkChunk ? 2 : mode == kQkWarp ? 1 : 0;
+    std::atomic<uint64_t>* word = dev >= 0 && dev < kMaxDevices ? &g_qk_smem_done[dev][w] : nullptr;
     if (word && (word->load(std::memory_order_acquire) & bit))
         return cudaSuccess;
     int optin = 0;

@@ -387,6 +387,35 @@ QkKernelFn qk_warp_table(int kq, int kk)
 #undef DRADD_QK_WARP_KK
 }
 
+// ----------------------------------------------------------- qk_chunk_kernel
+// Fused q/k RMSNorm with the q rows in 512-element chunks (chunk_row_body,
+// one warp a chunk, a CTA a row) and the k rows one warp each
+// (warp_ring_body): CTAs [0, q_ctas) take the q rows, the rest the k rows;
+// both kinds have the q row's chunk count of warps.
+template <int KK, bool QQUANT, bool QADD>
+__global__ void __launch_bounds__(256, 1) qk_chunk_kernel(const Params pq, const Params pk, int q_ctas)
+{
+    extern __shared__ __align__(128) unsigned char wsm[];
+    constexpr int QOUT = QQUANT ? kOutE4m3Group : kOutBf16;
+    const int cta = static_cast<int>(blockIdx.x);
+    if (cta < q_ctas)
+        chunk_row_body<QOUT, QADD>(pq, cta, q_ctas, wsm);
+    else
+        warp_ring_body<KK, kOutBf16, false>(pk, cta - q_ctas, static_cast<int64_t>(gridDim.x) - q_ctas, wsm);
+}
+
+template <bool QQUANT, bool QADD>
+QkKernelFn qk_chunk_table(int kk)
+{
+    switch (kk) {
+    case 1: return qk_chunk_kernel<1, QQUANT, QADD>;
+    case 2: return qk_chunk_kernel<2, QQUANT, QADD>;
+    case 4: return qk_chunk_kernel<4, QQUANT, QADD>;
+    case 8: return qk_chunk_kernel<8, QQUANT, QADD>;
+    default: return nullptr;
+    }
+}
+
 template <int KQ, bool QQUANT, bool QADD, bool STAGED>
 QkKernelFn qk_by_kk(int kk)
 {

@@ -413,6 +413,231 @@ __device__ __forceinline__ void warp_ring_body(const Params& p, int64_t cta, int
     }
 }
 
+// ------------------------------------------------------------ chunked rows
+// Rows of kChunkElems-element chunks, one warp per chunk: a CTA of NW
+// warps (NW = the chunks that hold data, hidden / kChunkElems rounded up)
+// takes whole rows, rows cta, cta + n_ctas, ...  Warp c owns the blocks
+// 64 c .. 64 c + 63 of every row, lane l the blocks 64 c + l and 64 c + l
+// + 32, so within its chunk the warp computes exactly what warp_row
+// computes for a 512-element row: the chunk's subtree of the canonical
+// tree.  The P / 512 chunk sums (zero for the chunks past the data) then
+// fold pairwise, adjacent first: the top levels of the same tree, so the
+// row's sum is bit for bit the one-warp (and the oracle's) value.  One CTA
+// barrier per row exchanges the chunk sums; each warp has its own ring of
+// `stages` chunk slots in shared memory, filled by bulk copies that its
+// lane 0 issues `stages` rows ahead.  The chunk's fp32 weights are widened
+// into shared memory once by the warp that reads them.  Outputs: bf16, or
+// per-group e4m3 (a group, gb <= 32 aligned blocks, lies inside one
+// j-slice of a chunk).
+template <int OUT, bool ADD>
+__device__ __forceinline__ void chunk_row_body(const Params& p, int64_t cta, int64_t n_ctas, unsigned char* smem)
+{
+    static_assert(OUT == kOutBf16 || OUT == kOutE4m3Group, "bf16 or per-group e4m3 out");
+    constexpr int K = kChunkBlocks / 32;  // blocks per lane in a chunk
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int NW = blockDim.x >> 5;
+    const int nblocks = p.hidden >> 3;
+    int Q = 1;  // chunks of the padded row (P / 512)
+    while (Q * kChunkBlocks < nblocks)
+        Q <<= 1;
+    const int stages = p.stages;
+    const int first_block = warp * kChunkBlocks;
+    const int cblocks = nblocks - first_block < kChunkBlocks ? nblocks - first_block : kChunkBlocks;
+    const uint32_t chunk_bytes = static_cast<uint32_t>(cblocks) * 16u;
+    constexpr uint32_t slot_bytes = chunk_slot_bytes(ADD);
+    unsigned char* const ring = smem + static_cast<size_t>(warp) * stages * slot_bytes;
+    unsigned char* const after_rings = smem + static_cast<size_t>(NW) * stages * slot_bytes;
+    float4* const w_lo = reinterpret_cast<float4*>(after_rings);
+    float4* const w_hi = w_lo + nblocks;
+    float* const s_chunk = reinterpret_cast<float*>(after_rings + 4u * static_cast<uint32_t>(p.hidden));  // [2][8]
+    uint64_t* const bars = reinterpret_cast<uint64_t*>(s_chunk + 16) + warp * stages;
+
+    if (lane == 0) {
+        if (p.l2_prefetch && cta < p.n_rows) {
+            prefetch_l2(p.x + cta * p.hidden + first_block * 8, chunk_bytes);
+            if constexpr (ADD)
+                prefetch_l2(p.residual + cta * p.hidden + first_block * 8, chunk_bytes);
+        }
+        for (int s = 0; s < stages; ++s)
+            mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    wait_prior_grids();
+    allow_next_grid();
+
+    const uint64_t policy = l2_policy_evict_first();
+    auto issue = [&](int s, int64_t row) {
+        unsigned char* dst = ring + static_cast<size_t>(s) * slot_bytes;
+        const int64_t off = row * p.hidden + first_block * 8;
+        mbar_arrive_expect_tx(&bars[s], (ADD ? 2u : 1u) * chunk_bytes);
+        bulk_copy_g2s(dst, p.x + off, chunk_bytes, &bars[s], policy);
+        if constexpr (ADD)
+            bulk_copy_g2s(dst + kChunkElems * 2, p.residual + off, chunk_bytes, &bars[s], policy);
+    };
+    if (lane == 0) {
+        for (int s = 0; s < stages; ++s) {
+            const int64_t row = cta + s * n_ctas;
+            if (row >= p.n_rows)
+                break;
+            if (p.fault_inject && s == 0)
+                continue;  // test hook: this copy never comes, so its wait expires
+            issue(s, row);
+        }
+    }
+    {
+        // this warp's chunk of the weights, widened once (only this lane reads them)
+        const uint4* wrow = reinterpret_cast<const uint4*>(p.weight);
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const int bl = lane + 32 * j;
+            if (bl < cblocks) {
+                float f[8];
+                unpack8(__ldg(wrow + first_block + bl), f);
+                w_lo[first_block + bl] = make_float4(f[0], f[1], f[2], f[3]);
+                w_hi[first_block + bl] = make_float4(f[4], f[5], f[6], f[7]);
+            }
+        }
+    }
+
+    int buf = 0;
+    int64_t i = 0;
+    int s = 0;
+    uint32_t parity = 0;
+    for (int64_t row = cta; row < p.n_rows; row += n_ctas, ++i) {
+        const bool ok = mbar_wait_bounded(&bars[s], parity, p.wait_limit_ns);
+        const unsigned char* slot = ring + static_cast<size_t>(s) * slot_bytes;
+        const uint4* xs = reinterpret_cast<const uint4*>(slot);
+        const uint4* rs = reinterpret_cast<const uint4*>(slot + kChunkElems * 2);
+        float part[K];
+        float acc[ADD ? K : 1][8];
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const int bl = lane + 32 * j;
+            part[j] = 0.0f;
+            if constexpr (ADD) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    acc[j][e] = 0.0f;
+            }
+            if (bl < cblocks) {
+                if constexpr (ADD) {
+                    add8(xs[bl], rs[bl], acc[j]);
+                    st_stream(reinterpret_cast<uint4*>(p.residual_out + row * p.hidden) + first_block + bl,
+                              pack8_rne(acc[j]));
+                    part[j] = fold8_squares(acc[j]);
+                } else {
+                    float f[8];
+                    unpack8(xs[bl], f);
+                    part[j] = fold8_squares(f);
+                }
+            }
+        }
+        int jsub;
+        const float v = fold_lane_subtrees<K>(warp_halving_sum<K>(part, lane, jsub));
+        if (lane == 0)
+            s_chunk[buf * 8 + warp] = v;
+        // every warp has published its chunk's sum; any expired wait ends
+        // the CTA here (each warp's lane 0 first waits for its own copies)
+        if (__syncthreads_or(!ok)) {
+            if (lane == 0) {
+                record_timeout(p);
+                drain_issued_copies(p, bars, s, parity, i, stages, cta, n_ctas, p.n_rows);
+            }
+            return;
+        }
+        if constexpr (ADD) {
+            // acc holds the row: the slot can be refilled now
+            if (lane == 0) {
+                const int64_t next = row + static_cast<int64_t>(stages) * n_ctas;
+                if (next < p.n_rows) {
+                    fence_proxy_async_smem();
+                    issue(s, next);
+                }
+            }
+        }
+        float c[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            c[q] = q < NW ? s_chunk[buf * 8 + q] : 0.0f;
+        // the chunk sums, adjacent pairs first, up to the Q chunks of P
+#pragma unroll
+        for (int width = 1; width < 8; width *= 2) {
+#pragma unroll
+            for (int q = 0; q < 8; q += 2 * width) {
+                if (width < Q)
+                    c[q] = __fadd_rn(c[q], c[q + width]);
+            }
+        }
+        const float inv = inv_rms(c[0], p.hidden, p.inv_hidden, p.eps);
+
+        auto y_of = [&](int j, float (&y)[8]) {
+            const int bl = lane + 32 * j;
+            if constexpr (ADD) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    y[e] = acc[j][e];
+            } else {
+                unpack8(xs[bl], y);
+            }
+            scale8_f32(y, inv, w_lo[first_block + bl], w_hi[first_block + bl]);
+        };
+        if constexpr (OUT == kOutBf16) {
+            uint4* orow = reinterpret_cast<uint4*>(p.out + row * p.hidden);
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const int bl = lane + 32 * j;
+                if (bl < cblocks) {
+                    float y[8];
+                    y_of(j, y);
+                    st_stream(orow + first_block + bl, pack8_rne(y));
+                }
+            }
+        } else {
+            const int gb = p.group_blocks;
+            const int64_t groups = nblocks >> p.group_shift;
+            uint2* qrow = reinterpret_cast<uint2*>(p.out_q + row * p.hidden);
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                if (32 * j >= cblocks)
+                    continue;  // the whole j-slice is past the data (warp-uniform)
+                const int bl = lane + 32 * j;
+                const int b = first_block + bl;
+                float y[8];
+                float m = 0.0f;
+                if (bl < cblocks) {
+                    y_of(j, y);
+                    m = block_max_abs(y);
+                }
+                m = butterfly_max(m, gb);
+                const float scale = div448_rn(m);
+                if (bl < cblocks) {
+                    if ((b & (gb - 1)) == 0)
+                        p.scale[row * groups + (b >> p.group_shift)] = scale;
+                    st_stream(qrow + b, quantize8_e4m3(y, make_e4m3_scale(scale)));
+                }
+            }
+        }
+        if constexpr (!ADD) {
+            __syncwarp();  // every lane is done with the slot
+            if (lane == 0) {
+                const int64_t next = row + static_cast<int64_t>(stages) * n_ctas;
+                if (next < p.n_rows) {
+                    fence_proxy_async_smem();
+                    issue(s, next);
+                }
+            }
+        }
+        buf ^= 1;
+        if (++s == stages) {
+            s = 0;
+            parity ^= 1u;
+        }
+    }
+}
+
 // The warp-per-row kernel of the main op (up to kWarpMaxRows warps a CTA;
 // shared memory layout as warp_smem_bytes).
 template <int K, int OUT, bool ADD>

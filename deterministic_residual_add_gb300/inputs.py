@@ -76,12 +76,14 @@ class Workload:
         """Return dict(x, residual, weight, eps) as CPU bf16 tensors.
 
         n_rows < self.n_rows draws the full-size tensors' leading rows
-        (same bits as the full workload's first rows)."""
+        (same bits as the full workload's first rows); n_rows > self.n_rows
+        draws that many rows from the same distributions and seed."""
         g = generator(self.seed)
-        x = normal_bf16(g, (self.n_rows, self.hidden), 0.0, self.x_std)
-        r = normal_bf16(g, (self.n_rows, self.hidden), 0.0, self.residual_std)
+        rows = self.n_rows if n_rows is None or n_rows <= self.n_rows else n_rows
+        x = normal_bf16(g, (rows, self.hidden), 0.0, self.x_std)
+        r = normal_bf16(g, (rows, self.hidden), 0.0, self.residual_std)
         w = normal_bf16(g, (self.hidden,), self.weight_mean, self.weight_std)
-        if n_rows is not None:
+        if n_rows is not None and n_rows < rows:
             x, r = x[:n_rows].contiguous(), r[:n_rows].contiguous()
         return {"x": x, "residual": r, "weight": w, "eps": self.eps}
 

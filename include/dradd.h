@@ -193,13 +193,17 @@ dradd_status add_rmsnorm_quant_fwd(int8_t* out_q, float* scale, dradd_bf16* resi
  * memory.  rows_per_cta: warps per CTA (0 = 8, or 4 at P = 4096; at most
  * that); grid_ctas: 0 = as many CTAs as fit on the device at once (at most
  * one per rows_per_cta rows).  stages and fault_inject must be 0.
+ *
+ * DRADD_VARIANT_CHUNK: the fused q/k call only (see there); the other entry
+ * points reject it.
  */
 enum {
     DRADD_VARIANT_AUTO = 0,
     DRADD_VARIANT_ROWS = 1,
     DRADD_VARIANT_STAGED = 2,
     DRADD_VARIANT_SPLIT = 3,
-    DRADD_VARIANT_WARP = 4
+    DRADD_VARIANT_WARP = 4,
+    DRADD_VARIANT_CHUNK = 5
 };
 
 typedef struct dradd_launch_cfg {
@@ -432,7 +436,15 @@ dradd_status fused_qk_rmsnorm_group_quant_fwd(void* q_out, float* q_scale, dradd
  * rows_per_cta must be 0.  WARP: one warp per row on both sides, each lane
  * owning blocks l, l + 32, ... of its row (both sides 256 <= P <= 2048),
  * threads_per_row read as the threads of a CTA (a multiple of 32 up to 256,
- * 0 = 256), blocks_per_thread, stages and fault_inject 0.  Results never
+ * 0 = 256), stages per warp ring (0 = 2), fault_inject and wait_limit_us
+ * as for the staged variant, blocks_per_thread 0.  CHUNK: the q
+ * rows in 512-element chunks, one warp a chunk and one CTA a row (the CTA
+ * has hidden / 512 warps rounded up, 2..8: 512 < q P <= 4096), each warp
+ * computing its chunk's subtree of the row's sum, the chunk sums folded in
+ * the same tree order after one barrier; the k rows one warp each as in
+ * WARP, in CTAs of the same size (256 <= k P <= 2048); stages per warp
+ * ring (0 = 2), fault_inject and wait_limit_us as for the staged variant,
+ * threads_per_row, blocks_per_thread and rows_per_cta 0.  Results never
  * depend on it.
  */
 dradd_status fused_qk_rmsnorm_group_quant_fwd_with_config(

@@ -100,6 +100,23 @@ def test_parity_warp_rows(orc, case):
     assert dr.device_status() == 0
 
 
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:5])) + ("r" if c[5] else ""))
+def test_parity_chunk_rows(orc, case):
+    """The chunked-q mode on every case it takes (q 512 < P <= 4096, k
+    256 <= P <= 2048 or no k rows)."""
+    nq, hq, nk, hk, group, with_res, qe, ke = case
+    cfg = dr.LaunchConfig(variant=dr.VARIANT_CHUNK)
+    try:
+        dr.qk_resolve_config(nq, hq, nk, hk, group, q_residual=with_res, config=cfg)
+    except dr.DraddError as e:
+        assert e.status == 9
+        pytest.skip("a side outside the chunked mode's widths")
+    q, r, qw, k, kw = make(hash(case) % 1000 + 2, nq, hq, nk, hk, with_res)
+    got = run_gpu(q, r, qw, k, kw, group, qe, ke, config=cfg)
+    compare(orc, q, r, qw, k, kw, group, qe, ke, got, what="chunk")
+    assert dr.device_status() == 0
+
+
 CONFIGS = ([None] +
            [dr.LaunchConfig(variant=1, threads_per_row=B, grid_ctas=G)
             for B in (64, 128, 256, 512) for G in (0, 2, 7, 1000)] +
@@ -109,6 +126,7 @@ CONFIGS = ([None] +
             for v in (1, 2) for K in (2, 4, 8)] +
            [dr.LaunchConfig(variant=dr.VARIANT_WARP, threads_per_row=B, grid_ctas=G)
             for B in (64, 256) for G in (0, 3)] +
+           [dr.LaunchConfig(variant=dr.VARIANT_CHUNK, stages=S, grid_ctas=G) for S, G in ((1, 0), (3, 5), (2, 2))] +
            [dr.LaunchConfig(serialize=1), dr.LaunchConfig(variant=1, serialize=1)])
 
 
@@ -190,7 +208,7 @@ def test_zero_groups_and_tiny_scales(orc):
         assert np.all(s[5] == 0)
 
 
-@pytest.mark.parametrize("variant", [2, dr.VARIANT_WARP])
+@pytest.mark.parametrize("variant", [2, dr.VARIANT_WARP, dr.VARIANT_CHUNK])
 def test_bounded_wait_expires_and_recovers(orc, variant):
     """fault_inject withholds each CTA's first staged copy on both sides:
     every wait runs out after wait_limit_us, the kernel records

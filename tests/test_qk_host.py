@@ -84,6 +84,7 @@ def test_with_config_needs_config(L):
     (1, 8, 1, 16, 8), (100000, 1536, 0, 512, 64), (0, 1536, 7, 4096, 0), (3, 200, 5, 24, 8),
     (2048, 8192, 2048, 1024, 32), (50, 256, 3, 64, 256), (7, 128, 7, 128, 128), (64, 2048, 64, 512, 8),
     (64, 1536, 64, 512, 16), (4096 * 32, 128, 4096 * 8, 128, 0), (256 * 32, 128, 256 * 8, 128, 0),
+    (4096, 3072, 4096, 1024, 128), (2048, 4096, 2048, 1024, 0), (4096, 4096, 0, 512, 128), (9, 2000, 3, 4096, 0),
 ])
 def test_plan_rules(nq, hq, nk, hk, g):
     p = dr.qk_resolve_config(nq, hq, nk, hk, g, q_residual=True, sm_count=152)
@@ -92,6 +93,14 @@ def test_plan_rules(nq, hq, nk, hk, g):
     rows = nq + nk
     max_stages = 2
     min_p = min(1 << (h - 1).bit_length() for n, h in ((nq, hq), (nk, hk)) if n)
+    pq = 1 << (hq - 1).bit_length()
+    pk = 1 << (hk - 1).bit_length()
+    if nq and 1536 < hq and pq <= 4096 and (not nk or 256 <= pk <= 2048):
+        # wide q rows: 512-element chunks, one warp each
+        nw = -(-hq // 512)
+        assert (p.variant, B) == (dr.VARIANT_CHUNK, 32 * nw)
+        assert (p.q_threads_per_row, p.q_rows_per_cta, p.q_stages) == (32 * nw, 1, 1 if g else 2)
+        return
     if 256 < min_p and max_p <= 2048 and rows >= 8192:
         # the low-rank q / kv class: one warp a row, rings of 2 slots, 128 threads
         assert (p.variant, B) == (dr.VARIANT_WARP, 128)
@@ -214,3 +223,46 @@ def test_plan_explicit_threads_and_grid():
                 assert e.status == 9
                 continue
             assert p.q_threads_per_row >= 32
+
+
+CHUNK = dr.LaunchConfig(variant=dr.VARIANT_CHUNK)
+
+
+@pytest.mark.parametrize("nq,hq,nk,hk,nw", [(4096, 1536, 4096, 512, 3), (100, 1280, 0, 512, 3), (7, 600, 9, 256, 2),
+                                            (33, 4096, 12, 2048, 8), (5, 3000, 5, 1024, 6)])
+def test_chunk_plan(nq, hq, nk, hk, nw):
+    """CHUNK: a q row is one CTA of ceil(hq / 512) warps, a chunk each; the k
+    rows one warp each in CTAs of as many warps; 2 ring slots per warp; the
+    CTAs at most one per q row and one per nw k rows."""
+    p = dr.qk_resolve_config(nq, hq, nk, hk, 0, q_residual=True, sm_count=152, config=CHUNK)
+    assert p.variant == dr.VARIANT_CHUNK and p.threads_per_cta == 32 * nw
+    assert (p.q_threads_per_row, p.q_rows_per_cta, p.q_stages) == (32 * nw, 1, 2)
+    assert 1 <= p.q_ctas <= nq
+    if nk:
+        assert (p.k_threads_per_row, p.k_rows_per_cta, p.k_stages) == (32, nw, 2)
+        assert 1 <= p.k_ctas <= -(-nk // nw)
+    else:
+        assert p.k_ctas == 0
+
+
+@pytest.mark.parametrize("nq,hq,nk,hk,kw", [
+    (64, 512, 64, 512, {}),                   # q P = 512: one warp a row already
+    (64, 8192, 64, 512, {}),                  # q P > 4096
+    (0, 1536, 64, 512, {}),                   # no q rows
+    (64, 1536, 64, 4096, {}),                 # k P > 2048
+    (64, 1536, 64, 128, {}),                  # k P < 256
+    (64, 1536, 64, 512, {"threads_per_row": 128}),
+    (64, 1536, 64, 512, {"blocks_per_thread": 2}),
+    (64, 1536, 64, 512, {"rows_per_cta": 2}),
+    (64, 1536, 64, 512, {"stages": 9}),
+])
+def test_chunk_plan_refusals(nq, hq, nk, hk, kw):
+    with pytest.raises(dr.DraddError) as e:
+        dr.qk_resolve_config(nq, hq, nk, hk, 0, sm_count=152, config=dr.LaunchConfig(variant=dr.VARIANT_CHUNK, **kw))
+    assert e.value.status == 9
+
+
+def test_chunk_variant_is_the_fused_calls_only():
+    with pytest.raises(dr.DraddError) as e:
+        dr.resolve_config(4096, 4096, sm_count=152, config=CHUNK)
+    assert e.value.status == 9
