@@ -837,9 +837,8 @@ def run_qk(args):
     peak_src = "measured" if peak else "fallback"
     if not peak:
         peak = 6800.0
-    sm_count = torch.cuda.get_device_properties(device).multi_processor_count
-    plan = dr.qk_resolve_config(nq, w.q_head, nk, w.k_head, w.group_size, q_residual=w.residual,
-                                sm_count=sm_count)
+    # sm_count 0: the device's plan, with the grid the call launches
+    plan = dr.qk_resolve_config(nq, w.q_head, nk, w.k_head, w.group_size, q_residual=w.residual, sm_count=0)
     line = {
         "metric": QK_METRIC, "value": round(world * bytes_step * args.steps / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),

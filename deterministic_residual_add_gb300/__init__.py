@@ -524,8 +524,9 @@ def fused_qk_rmsnorm_group_quant_fwd(q, q_weight, k, k_weight, q_eps: float = 1e
 def qk_resolve_config(n_q_rows: int, q_hidden: int, n_k_rows: int, k_hidden: int, group_size: int = 0,
                       q_residual: bool = False, sm_count: int = 152,
                       config: LaunchConfig | None = None) -> QkPlan:
-    """The plan the fused q/k call would use (no GPU needed for sm_count > 0;
-    the real call then sizes the automatic grid by the device's occupancy)."""
+    """The plan the fused q/k call would use.  sm_count > 0: no GPU needed
+    (the real call then sizes the automatic grid by the device's
+    occupancy); sm_count <= 0: the current device's plan, grid included."""
     plan = _QkPlan()
     c = config._c() if config is not None else None
     _check(lib().dradd_qk_resolve_config(int(n_q_rows), int(q_hidden), int(n_k_rows), int(k_hidden),
