@@ -19,7 +19,12 @@ __device__ unsigned int g_device_status;
 
 // ------------------------------------------------------------ residual add
 // residual_out = bf16_rne(fp32(x) + fp32(residual)) over n_vec 16-byte
-// vectors (8 elements each), four vectors per thread in flight.
+// vectors (8 elements each).  Thread t handles vectors t, t + stride, ...
+// (stride = the grid's threads), kResidualAddInFlight of them per pass with
+// all their loads issued before the first use, the last pass masked, so a
+// thread's vectors are never fetched one round trip at a time.
+constexpr int kResidualAddInFlight = 4;
+
 __global__ void __launch_bounds__(256) residual_add_kernel(uint16_t* residual_out, const uint16_t* x,
                                                            const uint16_t* residual, int64_t n_vec,
                                                            int l2_prefetch)
@@ -39,25 +44,24 @@ __global__ void __launch_bounds__(256) residual_add_kernel(uint16_t* residual_ou
     }
     wait_prior_grids();
     allow_next_grid();
-    int64_t i = first + threadIdx.x;
-    for (; i + 3 * stride < n_vec; i += 4 * stride) {
-        uint4 a[4], b[4];
+    constexpr int U = kResidualAddInFlight;
+    for (int64_t i = first + threadIdx.x; i < n_vec; i += U * stride) {
+        uint4 a[U], b[U];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            a[u] = ld_stream(xv + i + u * stride);
-            b[u] = ld_stream(rv + i + u * stride);
+        for (int u = 0; u < U; ++u) {
+            if (i + u * stride < n_vec) {
+                a[u] = ld_stream(xv + i + u * stride);
+                b[u] = ld_stream(rv + i + u * stride);
+            }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            float acc[8];
-            add8(a[u], b[u], acc);
-            st_stream(ov + i + u * stride, pack8_rne(acc));
+        for (int u = 0; u < U; ++u) {
+            if (i + u * stride < n_vec) {
+                float acc[8];
+                add8(a[u], b[u], acc);
+                st_stream(ov + i + u * stride, pack8_rne(acc));
+            }
         }
-    }
-    for (; i < n_vec; i += stride) {
-        float acc[8];
-        add8(ld_stream(xv + i), ld_stream(rv + i), acc);
-        st_stream(ov + i, pack8_rne(acc));
     }
 }
 
