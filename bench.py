@@ -107,13 +107,15 @@ def measured_peaks() -> dict:
 # the value it was taken on; otherwise the line's traffic is null.
 SOURCE_FAMILIES = {
     "main": ["dradd_device.cuh", "dradd_kernels.cuh", "dradd_internal.h", "dradd_kernels.cu",
-             "dradd_staged_*.cu", "dradd_abi.cu"],
-    "qk": ["dradd_device.cuh", "dradd_kernels.cuh", "dradd_internal.h", "dradd_qk.cuh", "dradd_qk_*.cu",
-           "dradd_abi.cu"],
+             "dradd_staged_*.cu", "dradd_warp.cuh", "dradd_warp_*.cu", "dradd_split.cuh", "dradd_split_*.cu",
+             "dradd_abi.cu"],
+    "qk": ["dradd_device.cuh", "dradd_kernels.cuh", "dradd_internal.h", "dradd_warp.cuh", "dradd_qk.cuh",
+           "dradd_qk_*.cu", "dradd_abi.cu"],
     "elem": ["dradd_device.cuh", "dradd_internal.h", "dradd_lse.cu", "dradd_abi.cu"],
 }
 NCU_METRICS = "dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum"
-NCU_KERNELS = "regex:staged_kernel|rows_kernel|split_kernel|qk_kernel|lse_merge_kernel|unary_kernel|residual_add_kernel"
+NCU_KERNELS = ("regex:staged_kernel|staged_pair_kernel|rows_kernel|split_kernel|warp_kernel|qk_kernel|qk_chunk_kernel|"
+               "lse_merge_kernel|unary_kernel|residual_add_kernel")
 NCU_WARMUP = 5
 
 
@@ -230,7 +232,7 @@ def make_ncu_record(name: str, csv_text: str) -> dict:
         "workload": name, "kernel": kernels[0], "grid": launches[0]["grid"], "block": launches[0]["block"],
         "launches_captured": len(launches), "rotating_sets": workload_n_sets(name),
         "dram_bytes_read_per_launch": round(rd), "dram_bytes_write_per_launch": round(wr),
-        "dram_bytes_per_launch": round(rd + wr),
+        "dram_bytes_per_launch": round(rd) + round(wr),
         "gpu_time_duration_ns_mean": round(mean("gpu__time_duration.sum"), 1),
         "algorithmic_bytes_per_launch": alg, "traffic_over_algorithmic": round((rd + wr) / alg, 4),
         "note": "means over consecutive launches of the back-to-back bench loop, caches not flushed: "
