@@ -221,7 +221,7 @@ def test_auto_plain_quantised_takes_the_pair_kernel(L, n, h, T):
     assert dr.resolve_config(4096, 4096, add=False, sm_count=152).rows_per_cta == 1
     for kw in (dict(), dict(fp8=True)):
         c = dr.resolve_config(609, 4096, quant=True, add=False, sm_count=152, **kw)
-        assert (c.variant, c.rows_per_cta, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 1, 128, 1)
+        assert (c.variant, c.rows_per_cta, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 1, 128, 2)
     assert dr.resolve_config(4096, 4096, quant=True, sm_count=152).rows_per_cta == 1
     assert dr.resolve_config(8192, 512, quant=True, add=False, sm_count=152).variant == dr.VARIANT_WARP
     assert dr.resolve_config(64, 32768, quant=True, add=False, sm_count=152).rows_per_cta == 1
@@ -292,7 +292,7 @@ def test_fp8_argument_errors(L):
     c = dr.resolve_config(4096, 4096, add=True, fp8=True)
     assert c.variant == dr.VARIANT_STAGED and c.stages == 2
     c = dr.resolve_config(4096, 4096, add=False, fp8=True)
-    assert c.stages == 1
+    assert c.stages == 2
 
 
 def test_fp4_argument_errors(L):
