@@ -21,9 +21,10 @@
 namespace dradd {
 
 // log1p(u) for u in [0, 1]: 2 atanh(s) with s = u / t, t = RN(2 + u), s <=
-// 1/3, by the atanh series 2 s (1 + s^2/3 + s^4/5 + ... + s^16/17), whose
-// truncation is below 2^-28 of the value; the series in fused
-// multiply-adds.  The division is a reciprocal approximation with one
+// 1/3, by the atanh series 2 s (1 + s^2/3 + s^4/5 + ... + s^12/13), whose
+// truncation is below (1/9)^7 / 15 < 2^-26 of the value (the two further
+// terms the series once carried change no worst case below); the series
+// in fused multiply-adds.  The division is a reciprocal approximation with one
 // correction step (Markstein): r = rcp.approx(t) (within 1 ulp),
 // q0 = RN(u r), the remainder u - q0 t exact in one fused multiply-add,
 // s = RN(q0 + rem r).  Before its last rounding that value is within
@@ -35,9 +36,7 @@ namespace dradd {
 // 2.95 x 2^-24 relative, and every smaller u within 2^-146 absolute.
 __device__ __forceinline__ float series_tail(float z)
 {
-    float p = 0x1.e1e1e2p-5f;              // 1/17
-    p = __fmaf_rn(p, z, 0x1.111112p-4f);   // 1/15
-    p = __fmaf_rn(p, z, 0x1.3b13b2p-4f);   // 1/13
+    float p = 0x1.3b13b2p-4f;              // 1/13
     p = __fmaf_rn(p, z, 0x1.745d18p-4f);   // 1/11
     p = __fmaf_rn(p, z, 0x1.c71c72p-4f);   // 1/9
     p = __fmaf_rn(p, z, 0x1.24924ap-3f);   // 1/7
@@ -110,9 +109,7 @@ __device__ __forceinline__ void lse_merge2(float a0, float a1, float b0, float b
     fma2_rn(e0, e1, c0, c1, q0, q1, s0, s1);
     float z0, z1;
     mul2_rn(s0, s1, s0, s1, z0, z1);
-    float p0 = 0x1.e1e1e2p-5f, p1 = 0x1.e1e1e2p-5f;
-    fma2_rn(p0, p1, z0, z1, 0x1.111112p-4f, 0x1.111112p-4f, p0, p1);
-    fma2_rn(p0, p1, z0, z1, 0x1.3b13b2p-4f, 0x1.3b13b2p-4f, p0, p1);
+    float p0 = 0x1.3b13b2p-4f, p1 = 0x1.3b13b2p-4f;
     fma2_rn(p0, p1, z0, z1, 0x1.745d18p-4f, 0x1.745d18p-4f, p0, p1);
     fma2_rn(p0, p1, z0, z1, 0x1.c71c72p-4f, 0x1.c71c72p-4f, p0, p1);
     fma2_rn(p0, p1, z0, z1, 0x1.24924ap-3f, 0x1.24924ap-3f, p0, p1);

@@ -3,11 +3,11 @@
  * that the LSE merge kernel uses:
  *   t = RN(2 + u), s = u / t by a reciprocal approximation and one
  *       correction step, z = RN(s * s),
- *   p = Horner over z of RN(1/17), RN(1/15), ..., RN(1/3) with fused
+ *   p = Horner over z of RN(1/13), RN(1/11), ..., RN(1/3) with fused
  *       multiply-adds,
  *   log1p(u) ~ fma(RN(RN(2 s) * z), p, RN(2 s))
- * (2 atanh(s) by its series, truncated after s^16 / 17: below 2^-28 of the
- * value for s <= 1/3).  The kernel's quotient is RN(u / t) except where
+ * (2 atanh(s) by its series, truncated after s^12 / 13: below
+ * (1/9)^7 / 15 < 2^-26 of the value for s <= 1/3).  The kernel's quotient is RN(u / t) except where
  * u / t lies within 1.5 x 2^-46 (relative) of a rounding midpoint, where it
  * may be the other neighbour (the correction step leaves the value before
  * its last rounding that close to u / t; the reciprocal instruction itself
@@ -46,11 +46,11 @@ static float from_bits(uint32_t u)
 
 static float series_from(float s)
 {
-    const float c[8] = {0x1.555556p-2f, 0x1.99999ap-3f, 0x1.24924ap-3f, 0x1.c71c72p-4f,
-                        0x1.745d18p-4f, 0x1.3b13b2p-4f, 0x1.111112p-4f, 0x1.e1e1e2p-5f};
+    const float c[6] = {0x1.555556p-2f, 0x1.99999ap-3f, 0x1.24924ap-3f, 0x1.c71c72p-4f,
+                        0x1.745d18p-4f, 0x1.3b13b2p-4f};
     const float z = s * s;
-    float p = c[7];
-    for (int k = 6; k >= 0; --k)
+    float p = c[5];
+    for (int k = 4; k >= 0; --k)
         p = fmaf(p, z, c[k]);
     const float two_s = 2.0f * s;
     return fmaf(two_s * z, p, two_s);
