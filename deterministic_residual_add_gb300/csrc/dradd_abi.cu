@@ -334,10 +334,12 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     //                      T = 64, K = 4, 3 stages)
     //   4096   128   4  bf16: 3 below 24 rows per SM,  bf16: 4 from 20 to 63
     //                   2 below 64, else 1;           rows per SM, else 2;
-    //                   int8: 2 below 64, else 1      quantised: 2 (4096 x 4096
-    //                                                 int8 13.51 us against 13.85
-    //                                                 with 1; e4m3 14.91 / 15.04)
-    //          (bf16 residual-add batches of up to 256 rows: T = 256, K = 2)
+    //                   quantised: 2 below 44, else 1 quantised: 2
+    //          (bf16 residual-add batches of up to 256 rows: T = 256, K = 2;
+    //          quantised residual-add, int8: 48 rows per SM 33.87 us with 1
+    //          stage against 34.63 with 2, 32 rows per SM 23.14 with 2 against
+    //          23.62 with 1; plain quantised, 4096 x 4096: int8 13.51 us with 2
+    //          stages against 13.85 with 1, e4m3 14.91 against 15.04)
     //   8192   1024  1  2                             T = 512, K = 2: 3
     //          (bf16 residual-add batches of 65..512 rows: T = 512, K = 2)
     //   16384  512   4  2                             4
@@ -440,7 +442,7 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
             if (add && !quant)
                 auto_stages = per_sm < 24 ? 3 : (per_sm < 64 ? 2 : 1);
             else if (add)
-                auto_stages = per_sm < 64 ? 2 : 1;
+                auto_stages = per_sm < 44 ? 2 : 1;
             else if (!quant)
                 auto_stages = per_sm < 20 || per_sm >= 64 ? 2 : 4;
             else
