@@ -350,10 +350,10 @@ def test_small_batch_choices():
     assert dr.resolve_config(1024, 8192, sm_count=152).threads_per_row == 1024
 
 
-@pytest.mark.parametrize("n,stages", [(4096, 2), (6144, 2), (6687, 1), (7296, 1), (12288, 1)])
+@pytest.mark.parametrize("n,stages", [(4096, 2), (6144, 2), (6687, 2), (6688, 1), (7296, 1), (12288, 1)])
 def test_quantised_residual_add_stages_at_4096(L, n, stages):
     """Residual-add with quantised out at P = 4096: two stages below 44 rows
-    per SM, else one (152 SMs: 6687 rows is 44 a SM)."""
+    per SM (whole rows: 152 SMs x 44 = 6688), else one."""
     for kw in (dict(), dict(fp8=True), dict(fp4=True)):
         c = dr.resolve_config(n, 4096, quant=True, sm_count=152, **kw)
         assert (c.variant, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 128, stages), (n, kw)
