@@ -60,6 +60,7 @@ WORKLOADS = {
     "2048x16384": (2048, 16384, "add_rmsnorm", "quant2048x16384"),
     "quant2048x16384": (2048, 16384, "add_rmsnorm_quant", "quant2048x16384"),
     "quant4096x4096": (4096, 4096, "add_rmsnorm_quant", "chain4096"),
+    "quant4096x8192": (4096, 8192, "add_rmsnorm_quant", "4096x8192"),
     "rmsnorm4096x4096": (4096, 4096, "rmsnorm", "chain4096"),
     "rmsnorm_quant4096x4096": (4096, 4096, "rmsnorm_quant", "chain4096"),
     "rmsnorm_quant2048x8192": (2048, 8192, "rmsnorm_quant", "4096x8192"),

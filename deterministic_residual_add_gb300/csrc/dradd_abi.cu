@@ -341,7 +341,8 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     //          23.62 with 1; plain quantised, 4096 x 4096: int8 13.51 us with 2
     //          stages against 13.85 with 1, e4m3 14.91 against 15.04)
     //   8192   1024  1  2                             T = 512, K = 2: 3
-    //          (bf16 residual-add batches of 65..512 rows: T = 512, K = 2)
+    //          (bf16 residual-add batches of 65..512 rows, and the quantised
+    //          residual-add forms: T = 512, K = 2)
     //   16384  512   4  2                             4
     //   32768  512   8  1                             2
     //
@@ -448,8 +449,11 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
             else
                 auto_stages = 2;
         } else if (P == 8192) {
-            // 65..512-row bf16 batches: 512 threads, K = 2
-            T = add && !(quant || n_rows <= 64 || n_rows > 512) ? 512 : (add ? 1024 : 512);
+            // bf16 residual-add: 1024 threads, K = 1 (65..512-row batches:
+            // 512 threads, K = 2); quantised residual-add and plain: 512
+            // threads, K = 2 (int8 4096 x 8192: 38.27 us against 42.67 with
+            // 1024 threads; 2048 x 8192: 19.55 against 23.04)
+            T = add && !quant && (n_rows <= 64 || n_rows > 512) ? 1024 : 512;
             auto_stages = add ? 2 : 3;
         } else {
             T = 512;

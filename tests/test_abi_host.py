@@ -357,3 +357,14 @@ def test_quantised_residual_add_stages_at_4096(L, n, stages):
     for kw in (dict(), dict(fp8=True), dict(fp4=True)):
         c = dr.resolve_config(n, 4096, quant=True, sm_count=152, **kw)
         assert (c.variant, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 128, stages), (n, kw)
+
+
+def test_threads_at_8192():
+    """P = 8192: the bf16 residual-add takes 1024 threads (K = 1; 512 for
+    batches of 65..512 rows), the quantised residual-add forms and the plain
+    forms 512 (K = 2)."""
+    assert dr.resolve_config(4096, 8192, sm_count=152).threads_per_row == 1024
+    assert dr.resolve_config(256, 8192, sm_count=152).threads_per_row == 512
+    for kw in (dict(), dict(fp8=True), dict(fp4=True)):
+        c = dr.resolve_config(4096, 8192, quant=True, sm_count=152, **kw)
+        assert (c.variant, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 512, 2), kw
