@@ -331,7 +331,10 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     //   512    32    2  4                             4
     //   1024   64    2  3                             2
     //   2048   128   2  4 (64 rows per SM or more:    T = 64, K = 4: 2
-    //                      T = 64, K = 4, 3 stages)
+    //                      T = 64, K = 4, 3 stages;
+    //                      quantised: T = 64, K = 4,
+    //                      1 stage below 32 rows per
+    //                      SM, else 3)
     //   4096   128   4  bf16: 3 below 24 rows per SM,  bf16: 4 from 20 to 63
     //                   2 below 64, else 1;           rows per SM, else 2;
     //                   quantised: 2 below 44, else 1 quantised: 2
@@ -360,8 +363,8 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     //     13.74, and e4m3 slower, 15.47 against 14.95);
     //   - 512 <= P <= 2048 with enough rows: the warp-per-row variant
     //     (residual-add bf16 from 1024 rows, 4 warps and 3 stages: 4096 x
-    //     1024 in 5.27 us against 6.83; quantised residual-add from 2048
-    //     rows, up to 8192 at P = 2048, 4 warps and 2 stages; plain bf16
+    //     1024 in 5.27 us against 6.83; quantised residual-add at P <= 1024
+    //     from 2048 rows, 4 warps and 2 stages; plain bf16
     //     from 16384 rows, 8 warps and 3 stages; plain quantised at P = 512
     //     from 8192 rows, 4 warps and 2 stages).
     const bool auto_variant = cfg->variant == DRADD_VARIANT_AUTO;
@@ -389,7 +392,7 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
             if (add && !quant && n_rows >= 1024) {
                 R = 4;
                 S = 3;
-            } else if (add && quant && n_rows >= 2048 && (P < 2048 || n_rows <= 8192)) {
+            } else if (add && quant && n_rows >= 2048 && P < 2048) {
                 R = 4;
                 S = 2;
             } else if (!add && !quant && n_rows >= 16384) {
@@ -437,6 +440,13 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
             const bool wide = add && per_sm < 64;
             T = wide ? 128 : 64;
             auto_stages = wide ? 4 : (add ? 3 : 2);
+            if (add && quant) {
+                // quantised residual-add: 64 threads, K = 4 (2048 rows, 1
+                // stage: 6.63 us against 8.37 one warp a row; 8192 rows, 3
+                // stages: 19.20 against 20.72)
+                T = 64;
+                auto_stages = per_sm < 32 ? 1 : 3;
+            }
         } else if (P == 4096) {
             // small bf16 batches (up to 256 rows): 256 threads, K = 2
             T = add && !quant && n_rows <= 256 ? 256 : 128;

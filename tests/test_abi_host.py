@@ -368,3 +368,14 @@ def test_threads_at_8192():
     for kw in (dict(), dict(fp8=True), dict(fp4=True)):
         c = dr.resolve_config(4096, 8192, quant=True, sm_count=152, **kw)
         assert (c.variant, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 512, 2), kw
+
+
+@pytest.mark.parametrize("n,stages", [(2048, 1), (4863, 1), (4864, 3), (8192, 3), (20000, 3)])
+def test_quantised_residual_add_at_2048(n, stages):
+    """P = 2048, quantised residual-add: staged, 64 threads (K = 4), one
+    stage below 32 rows per SM, else three (no longer one warp a row)."""
+    for kw in (dict(), dict(fp8=True)):
+        c = dr.resolve_config(n, 2048, quant=True, sm_count=152, **kw)
+        assert (c.variant, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 64, stages), (n, kw)
+    # at P = 1024 the one-warp variant stays
+    assert dr.resolve_config(4096, 1024, quant=True, sm_count=152).variant == dr.VARIANT_WARP
