@@ -349,7 +349,7 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     //   16384  512   4  2                             4
     //   32768  512   8  1                             2
     //
-    // Three shapes go elsewhere (same measurements):
+    // These shapes go elsewhere (same measurements):
     //   - bf16 out, P = 32768 and at most 160 rows: the split-row cluster
     //     variant, 4 CTAs a row up to 64 rows, else 2 (one row: 3.2 us
     //     against 8.8 us staged; 152 rows: 10.5 against 11.4);
@@ -360,13 +360,14 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
     //     against 14.61 us, 8192 x 2048 12.72 against 13.47, 2048 x 8192
     //     14.61 against 16.52, 1024 x 16384 17.51 against 17.95, 512 x 4096
     //     3.84 against 4.87; at 4096 x 4096 int8 a tie, 13.73 against
-    //     13.74, and e4m3 slower, 15.47 against 14.95);
+    //     13.74, and e4m3 slower, 15.47 against 14.95); at P = 512 one
+    //     stage, the pair kernel with K = 1 below 8192 rows, else one row
+    //     a CTA with K = 2 (below);
     //   - 512 <= P <= 2048 with enough rows: the warp-per-row variant
     //     (residual-add bf16 from 1024 rows, 4 warps and 3 stages: 4096 x
     //     1024 in 5.27 us against 6.83; quantised residual-add at P <= 1024
-    //     from 2048 rows, 4 warps and 2 stages; plain bf16
-    //     from 16384 rows, 8 warps and 3 stages; plain quantised at P = 512
-    //     from 8192 rows, 4 warps and 2 stages).
+    //     from 2048 rows, 4 warps and 2 stages; plain bf16 from 16384 rows,
+    //     8 warps and 3 stages).
     const bool auto_variant = cfg->variant == DRADD_VARIANT_AUTO;
     if (auto_variant) {
         cfg->variant = hidden > 256 ? DRADD_VARIANT_STAGED : DRADD_VARIANT_ROWS;
@@ -375,6 +376,19 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
         if (no_explicit && !quant && P >= 32768 && n_rows <= 160) {
             cfg->variant = DRADD_VARIANT_SPLIT;
             cfg->cluster_ctas = n_rows <= 64 ? 4 : 2;
+        } else if (no_explicit && !add && quant && P == 512) {
+            // one stage; below 8192 rows the pair kernel with K = 1, else
+            // one row a CTA with K = 2 (4096 rows: 4.29 us against 4.85 for
+            // 4 stages of single rows; 16384 rows: 7.57 against 9.40 for
+            // one warp a row)
+            cfg->variant = DRADD_VARIANT_STAGED;
+            cfg->stages = 1;
+            if (n_rows < 8192) {
+                cfg->rows_per_cta = 2;
+                cfg->threads_per_row = 64;
+            } else {
+                cfg->threads_per_row = 32;
+            }
         } else if (no_explicit && !add && quant && P >= 1024 && P <= 16384 &&
                    (P != 4096 || n_rows <= 4 * static_cast<int64_t>(L.sm_count))) {
             // the pair kernel, one stage: K = 1 for batches of at most 4
@@ -398,9 +412,6 @@ dradd_status resolve(int64_t n_rows, int64_t hidden, bool quant, bool add, const
             } else if (!add && !quant && n_rows >= 16384) {
                 R = 8;
                 S = 3;
-            } else if (!add && quant && P <= 512 && n_rows >= 8192) {
-                R = 4;
-                S = 2;
             }
             if (R != 0) {
                 cfg->variant = DRADD_VARIANT_WARP;

@@ -217,13 +217,14 @@ def test_auto_plain_quantised_takes_the_pair_kernel(L, n, h, T):
         c = dr.resolve_config(n, h, quant=True, add=False, sm_count=152, **kw)
         assert (c.variant, c.rows_per_cta, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 2, T, 1), (n, h, kw)
         assert c.grid_ctas <= (n + 1) // 2
-    # not for bf16 out, the residual forms, P = 4096 beyond 4 rows per SM, P = 512 or P = 32768
+    # not for bf16 out, the residual forms, P = 4096 beyond 4 rows per SM, P = 512 from 8192 rows or P = 32768
     assert dr.resolve_config(4096, 4096, add=False, sm_count=152).rows_per_cta == 1
     for kw in (dict(), dict(fp8=True)):
         c = dr.resolve_config(609, 4096, quant=True, add=False, sm_count=152, **kw)
         assert (c.variant, c.rows_per_cta, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 1, 128, 2)
     assert dr.resolve_config(4096, 4096, quant=True, sm_count=152).rows_per_cta == 1
-    assert dr.resolve_config(8192, 512, quant=True, add=False, sm_count=152).variant == dr.VARIANT_WARP
+    c = dr.resolve_config(8192, 512, quant=True, add=False, sm_count=152)  # P = 512: one row a CTA from 8192 rows
+    assert (c.variant, c.rows_per_cta, c.threads_per_row) == (dr.VARIANT_STAGED, 1, 32)
     assert dr.resolve_config(64, 32768, quant=True, add=False, sm_count=152).rows_per_cta == 1
 
 
@@ -379,3 +380,13 @@ def test_quantised_residual_add_at_2048(n, stages):
         assert (c.variant, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 64, stages), (n, kw)
     # at P = 1024 the one-warp variant stays
     assert dr.resolve_config(4096, 1024, quant=True, sm_count=152).variant == dr.VARIANT_WARP
+
+
+def test_plain_quantised_at_512():
+    """P = 512, plain quantised: one stage; the pair kernel (64 threads,
+    K = 1) below 8192 rows, else one row a CTA (32 threads, K = 2)."""
+    for kw in (dict(), dict(fp8=True), dict(fp4=True)):
+        c = dr.resolve_config(4096, 512, quant=True, add=False, sm_count=152, **kw)
+        assert (c.variant, c.rows_per_cta, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 2, 64, 1), kw
+        c = dr.resolve_config(16384, 512, quant=True, add=False, sm_count=152, **kw)
+        assert (c.variant, c.rows_per_cta, c.threads_per_row, c.stages) == (dr.VARIANT_STAGED, 1, 32, 1), kw
