@@ -149,3 +149,11 @@ def test_bounded_wait_expires_and_recovers(orc):
     eq, es = orc.rmsnorm_quant_fwd(x, w, 1e-6)
     assert_bits_equal(u8(q), eq.view(np.uint8), "after timeout")
     assert dr.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("n,h", [(4096, 512), (16384, 512), (9001, 400), (301, 480)])
+def test_plain_quantised_at_512_in_the_automatic_plan(orc, n, h):
+    """P = 512 in the automatic plan: the pair kernel with K = 1 below 8192
+    rows, one row a CTA with K = 2 beyond; bit for bit either way."""
+    x, w = case(n, h, n + h)
+    run_quant(orc, x, w, 1e-6, None)
