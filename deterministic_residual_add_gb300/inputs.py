@@ -21,15 +21,17 @@ Within one workload the draws come from one generator in the order
 x, residual, weight.  eps is 1e-6 everywhere.
 
 Fused q/k RMSNorm workloads (QK_WORKLOADS; the page names the kernel but
-gives no shapes, so these are the two common layouts, with the main
-workloads' distributions): per token, q rows N(0,1) with a residual
-N(0,4), k rows N(0,1); both weights N(1,0.1); draws in the order q,
-residual, q weight, k, k weight.
+gives no shapes, so these are the two common layouts and a wider
+low-rank one, with the main workloads' distributions): per token, q rows
+N(0,1) with a residual N(0,4), k rows N(0,1); both weights N(1,0.1);
+draws in the order q, residual, q weight, k, k weight.
 
   qk_lowrank4096  4096 tokens: q 1 x 1536 (+ residual, e4m3 groups of 128),
                   k 1 x 512                                           seed 5
   qk_heads4096    4096 tokens: q 32 heads x 128, k 8 heads x 128, bf16 out,
                   no residual                                         seed 6
+  qk_wide4096     4096 tokens: q 1 x 3072 (+ residual, e4m3 groups of 128),
+                  k 1 x 1024                                          seed 8
 
 Log-sum-exp merge and elementwise workloads (ELEM_WORKLOADS; fp32):
 softmax log-sum-exps of attention rows are values of about log(S) plus a
@@ -217,6 +219,8 @@ class QkWorkload:
 QK_WORKLOADS = {
     "qk_lowrank4096": QkWorkload("qk_lowrank4096", 4096, 1, 1536, 1, 512, group_size=128, residual=True, seed=5),
     "qk_heads4096": QkWorkload("qk_heads4096", 4096, 32, 128, 8, 128, group_size=0, residual=False, seed=6),
+    # a wider low-rank layout (q rows wider than one warp takes well)
+    "qk_wide4096": QkWorkload("qk_wide4096", 4096, 1, 3072, 1, 1024, group_size=128, residual=True, seed=8),
 }
 
 
