@@ -999,17 +999,17 @@ dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t g
         auto_variant = DRADD_VARIANT_STAGED;
     const bool auto_plain = cfg.variant == DRADD_VARIANT_AUTO && cfg.stages == 0 && cfg.fault_inject == 0 &&
                             cfg.threads_per_row == 0 && cfg.blocks_per_thread == 0;
-    // q rows wider than 1536 up to P = 4096 (k rows 256 <= P <= 2048, or
-    // none): the q rows in 512-element chunks, one warp each, one stage with
-    // e4m3 groups and two with bf16 out (4096 x 3072 q + 1024 k: 25.3 us
-    // against 33.2 staged; 4096 x 4096 + 512: 29.8 against 32.1; 4096 x
-    // 2048 + 512: 15.4 against 16.2 one warp a row; 2048 x 4096 bf16 +
-    // 1024: 10.0 against 12.9; at 1536, three chunks, it lost).
-    if (auto_plain && q->active && hq > 1536 && next_pow2(hq) <= 4096 &&
+    // q rows with 512 < P <= 4096 (k rows 256 <= P <= 2048, or none): the
+    // q rows in 512-element chunks, one warp each, one stage (4096 tokens
+    // of 1536 + 512: 12.41 us against 12.73 one warp a row; 2048 tokens:
+    // 6.99 against 7.63; 4096 x 3072 q + 1024 k: 23.1 against 33.2 staged;
+    // 4096 x 1280 q alone: 9.10 against 11.75; 16384 tokens of 1536 + 512:
+    // 43.98 against 43.78, a tie).
+    if (auto_plain && q->active && next_pow2(hq) > 512 && next_pow2(hq) <= 4096 &&
         (!k->active || (next_pow2(hk) >= 256 && next_pow2(hk) <= 2048))) {
         dradd_launch_cfg c = cfg;
         c.variant = DRADD_VARIANT_CHUNK;
-        c.stages = group_size != 0 ? 1 : 2;
+        c.stages = 1;
         return qk_plan_chunk(n_q, hq, n_k, hk, add, sm_count, ctas_per_sm, smem_optin, c, out);
     }
     // Both sides 256 < P <= 2048 (the low-rank q / kv layout) with 8192 rows

@@ -391,9 +391,11 @@ QkKernelFn qk_warp_table(int kq, int kk)
 // Fused q/k RMSNorm with the q rows in 512-element chunks (chunk_row_body,
 // one warp a chunk, a CTA a row) and the k rows one warp each
 // (warp_ring_body): CTAs [0, q_ctas) take the q rows, the rest the k rows;
-// both kinds have the q row's chunk count of warps.
+// both kinds have the q row's chunk count of warps.  Compiled for at least
+// three resident CTAs of up to 256 threads (72 registers, no spills:
+// 4096 x 3072 q + 1024 k 25.39 -> 23.13 us against the unbounded 86).
 template <int KK, bool QQUANT, bool QADD>
-__global__ void __launch_bounds__(256, 1) qk_chunk_kernel(const Params pq, const Params pk, int q_ctas)
+__global__ void __launch_bounds__(256, 3) qk_chunk_kernel(const Params pq, const Params pk, int q_ctas)
 {
     extern __shared__ __align__(128) unsigned char wsm[];
     constexpr int QOUT = QQUANT ? kOutE4m3Group : kOutBf16;

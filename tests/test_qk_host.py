@@ -95,11 +95,11 @@ def test_plan_rules(nq, hq, nk, hk, g):
     min_p = min(1 << (h - 1).bit_length() for n, h in ((nq, hq), (nk, hk)) if n)
     pq = 1 << (hq - 1).bit_length()
     pk = 1 << (hk - 1).bit_length()
-    if nq and 1536 < hq and pq <= 4096 and (not nk or 256 <= pk <= 2048):
-        # wide q rows: 512-element chunks, one warp each
+    if nq and 512 < pq <= 4096 and (not nk or 256 <= pk <= 2048):
+        # q rows of 512 < P <= 4096: 512-element chunks, one warp each, one stage
         nw = -(-hq // 512)
         assert (p.variant, B) == (dr.VARIANT_CHUNK, 32 * nw)
-        assert (p.q_threads_per_row, p.q_rows_per_cta, p.q_stages) == (32 * nw, 1, 1 if g else 2)
+        assert (p.q_threads_per_row, p.q_rows_per_cta, p.q_stages) == (32 * nw, 1, 1)
         return
     if 256 < min_p and max_p <= 2048 and rows >= 8192:
         # the low-rank q / kv class: one warp a row, rings of 2 slots, 128 threads
