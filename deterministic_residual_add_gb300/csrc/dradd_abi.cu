@@ -1012,10 +1012,11 @@ dradd_status qk_plan(int64_t n_q, int64_t hq, int64_t n_k, int64_t hk, int64_t g
         c.stages = 1;
         return qk_plan_chunk(n_q, hq, n_k, hk, add, sm_count, ctas_per_sm, smem_optin, c, out);
     }
-    // Both sides 256 < P <= 2048 (the low-rank q / kv layout) with 8192 rows
-    // or more: one warp a row with a ring of 2 row slots per warp, 128
-    // threads a CTA (4096 tokens of 1536 + 512: 13.41 us against 14.21 for
-    // the register variant).
+    // Both sides 256 < P <= 2048 with 8192 rows or more, where the rule
+    // above did not apply (q rows of P = 512): one warp a row with a ring of
+    // 2 row slots per warp, 128 threads a CTA (on the low-rank layout, 4096
+    // tokens of 1536 + 512, before the chunked-q kernel took it: 13.41 us
+    // against 14.21 for the register variant).
     if (auto_plain && rows >= 8192 && max_p <= 2048) {
         bool fits = true;
         for (const QkSide* side : {q, k})
