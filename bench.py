@@ -72,7 +72,18 @@ WORKLOADS = {
     "rmsnorm_fp8_2048x8192": (2048, 8192, "rmsnorm_fp8", "4096x8192"),
     "fp4_2048x16384": (2048, 16384, "add_rmsnorm_fp4", "quant2048x16384"),
     "fp4_4096x4096": (4096, 4096, "add_rmsnorm_fp4", "chain4096"),
+    # the shapes of the aiter page's "Cost of fixing" table, bf16 and int8 out
+    "8192x2048": (8192, 2048, "add_rmsnorm", "8192x2048"),
+    "quant2048x4096": (2048, 4096, "add_rmsnorm_quant", "2048x4096"),
+    "quant8192x2048": (8192, 2048, "add_rmsnorm_quant", "8192x2048"),
+    "quant8192x4096": (8192, 4096, "add_rmsnorm_quant", "8192x4096"),
 }
+
+
+# Launch variants of the main op as config.launch names them (the resolved
+# plan; "staged" with rows_per_cta 2 is the two-rows-per-thread kernel).
+VARIANT_NAMES = {dr.VARIANT_ROWS: "rows", dr.VARIANT_STAGED: "staged", dr.VARIANT_SPLIT: "split",
+                 dr.VARIANT_WARP: "warp"}
 
 
 def algorithmic_bytes(n_rows: int, hidden: int, op: str = "add_rmsnorm") -> int:
@@ -721,7 +732,7 @@ def run_ours(args):
     else:
         cfg = dr.resolve_config(n_rows, hidden, quant=quant, sm_count=sm_count, add=op.startswith("add"),
                                 fp8=op.endswith("fp8"), fp4=op.endswith("fp4"))
-        launch = {"variant": "rows" if cfg.variant == 1 else "staged",
+        launch = {"variant": VARIANT_NAMES[cfg.variant],
                   "threads_per_row": cfg.threads_per_row, "rows_per_cta": cfg.rows_per_cta,
                   "stages": cfg.stages}
     line = {

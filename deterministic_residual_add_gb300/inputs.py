@@ -97,6 +97,8 @@ WORKLOADS = {
     "8192x4096": Workload("8192x4096", 8192, 4096, 1.0, 4.0, seed=1),
     "16384x4096": Workload("16384x4096", 16384, 4096, 1.0, 4.0, seed=1),
     "4096x8192": Workload("4096x8192", 4096, 8192, 1.0, 4.0, seed=2),
+    # the remaining shape of the aiter page's "Cost of fixing" table
+    "8192x2048": Workload("8192x2048", 8192, 2048, 1.0, 4.0, seed=1),
     "quant2048x16384": Workload("quant2048x16384", 2048, 16384, 1.0, 4.0, seed=4, quant=True),
 }
 

@@ -32,6 +32,21 @@ def test_workload_descriptions():
     assert bench.elem_workload_desc(inputs.ELEM_WORKLOADS["log1p16M"]).startswith("invariant_unary_fwd log1p")
 
 
+def test_launch_variant_names():
+    """config.launch names the variant the automatic plan resolves to, for
+    every main-op workload (152 SMs)."""
+    import deterministic_residual_add_gb300 as dr
+    names = {}
+    for name, (n, h, op, _) in bench.WORKLOADS.items():
+        if op == "residual_add":
+            continue
+        cfg = dr.resolve_config(n, h, quant=op not in ("add_rmsnorm", "rmsnorm"), sm_count=152,
+                                add=op.startswith("add"), fp8=op.endswith("fp8"), fp4=op.endswith("fp4"))
+        names[name] = bench.VARIANT_NAMES[cfg.variant]
+    assert names["4096x4096"] == "staged"
+    assert names["8192x2048"] == "warp"
+
+
 def test_graph_plan_covers_every_launch_once():
     for steps in (0, 1, 3, 20, 255, 256, 257, 600, 50000):
         for n_sets in (1, 3, 4, 7, 16, 64):
