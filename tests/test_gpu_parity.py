@@ -13,7 +13,7 @@ from gpu_util import THREADS, assert_bits_equal, gpu_fwd, gpu_quant, max_ulp_vs_
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name", ["tiny", "2048x4096", "4096x8192", "16384x4096"])
+@pytest.mark.parametrize("name", ["tiny", "2048x4096", "4096x8192", "16384x4096", "8192x2048"])
 def test_bf16_workloads_bit_exact(orc, name):
     c = inputs.WORKLOADS[name].make()
     out, ro = gpu_fwd(c["x"], c["residual"], c["weight"], c["eps"])
@@ -34,8 +34,9 @@ def test_chain_shape_first_call_bit_exact(orc):
     assert_bits_equal(out, eo, "4096x4096 out")
 
 
-def test_quant_workload_bit_exact(orc):
-    c = inputs.WORKLOADS["quant2048x16384"].make()
+@pytest.mark.parametrize("name", ["quant2048x16384", "2048x4096", "8192x2048", "8192x4096"])
+def test_quant_workload_bit_exact(orc, name):
+    c = inputs.WORKLOADS[name].make()
     q, scale, ro = gpu_quant(c["x"], c["residual"], c["weight"], c["eps"])
     eq, escale, ero = orc.add_rmsnorm_quant_fwd(c["x"], c["residual"], c["weight"], c["eps"],
                                                threads=THREADS)
