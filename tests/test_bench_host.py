@@ -2,6 +2,8 @@
 the rotating buffer sets (together at least 1 GiB, about eight times the L2, so
 no step reads its inputs from L2), and the workload descriptions that both
 arms print."""
+import torch
+
 import bench
 from deterministic_residual_add_gb300 import inputs
 
@@ -30,6 +32,25 @@ def test_workload_descriptions():
     w = inputs.QK_WORKLOADS["qk_lowrank4096"]
     assert bench.qk_workload_desc(w).startswith("fused_qk_rmsnorm_group_quant_fwd 4096 tokens")
     assert bench.elem_workload_desc(inputs.ELEM_WORKLOADS["log1p16M"]).startswith("invariant_unary_fwd log1p")
+
+
+def test_input_recipes_draw_the_stated_distributions():
+    """x ~ N(0, x_std), residual ~ N(0, residual_std), weight ~ N(1, 0.1),
+    bf16, at the stated shapes; the first rows of a full draw equal a draw
+    of those rows alone."""
+    for name, (mx, sx, sr) in {"tiny": (0.0, 1.0, 1.0), "2048x4096": (0.0, 1.0, 4.0),
+                               "8192x2048": (0.0, 1.0, 4.0)}.items():
+        w = inputs.WORKLOADS[name]
+        c = w.make()
+        assert tuple(c["x"].shape) == (w.n_rows, w.hidden) and c["x"].dtype == torch.bfloat16
+        assert tuple(c["residual"].shape) == (w.n_rows, w.hidden) and tuple(c["weight"].shape) == (w.hidden,)
+        x, r, wt = (c[k].float() for k in ("x", "residual", "weight"))
+        tol = 6.0 / (w.n_rows * w.hidden) ** 0.5
+        assert abs(x.mean().item() - mx) < tol * sx and abs(x.std().item() / sx - 1) < 0.01, name
+        assert abs(r.mean().item()) < tol * sr and abs(r.std().item() / sr - 1) < 0.01, name
+        assert abs(wt.mean().item() - 1.0) < 0.02 and abs(wt.std().item() / 0.1 - 1) < 0.1, name
+        head = w.make(n_rows=5)
+        assert torch.equal(head["x"], c["x"][:5]) and torch.equal(head["residual"], c["residual"][:5])
 
 
 def test_launch_variant_names():
