@@ -195,10 +195,22 @@ __device__ __forceinline__ void load_weights(const Params& p, uint4 (&w)[K], int
     }
 }
 
+// Whether block b = t + j * T (j unrolled) of a thread lies in the row, for
+// a kernel whose T threads of K blocks cover the padded row exactly (T * K =
+// P / 8 blocks).  P is the next power of two >= hidden, so nblocks > P / 16
+// = T * K / 2: blocks j < K / 2 (b <= T * K / 2 - 1) always lie in the row
+// and only the others need the test (with K = 1, every block does).
+template <int K>
+__device__ __forceinline__ bool block_in_row(int j, int b, int nblocks)
+{
+    return 2 * (j + 1) <= K || b < nblocks;
+}
+
 // acc for K blocks from already loaded vectors (x + residual with ADD, x
 // alone otherwise); with ADD residual_out is stored in the same pass.
-// Returns the per-block partial sums of squares.
-template <int K, bool ADD>
+// Returns the per-block partial sums of squares.  COVERS: the caller's T
+// threads of K blocks cover the padded row exactly (block_in_row applies).
+template <int K, bool ADD, bool COVERS = false>
 __device__ __forceinline__ void row_accumulate(const Params& p, const uint4 (&xv)[K], const uint4 (&rv)[K],
                                                float (&acc)[K][8], float (&part)[K], int64_t row,
                                                bool active, int t, int T, int nblocks)
@@ -207,7 +219,7 @@ __device__ __forceinline__ void row_accumulate(const Params& p, const uint4 (&xv
 #pragma unroll
     for (int j = 0; j < K; ++j) {
         const int b = t + j * T;
-        if (active && b < nblocks) {
+        if (active && (COVERS ? block_in_row<K>(j, b, nblocks) : b < nblocks)) {
             if constexpr (ADD) {
                 add8(xv[j], rv[j], acc[j]);
                 st_stream(rorow + b, pack8_rne(acc[j]));
@@ -356,9 +368,10 @@ __device__ __forceinline__ float quant_cta_amax(float m, const float* red, int l
 }
 
 // Per-row scale and codes of the quantised outputs (one row per T threads,
-// compile-time), given the row's amax m over the CTA.  Called by every
-// thread of the CTA: an int8 row whose amax is NaN takes a second,
-// NaN-ignoring amax through red_max2 (W floats of its own) and a barrier.
+// compile-time; T threads of K blocks cover the padded row), given the
+// row's amax m over the CTA.  Called by every thread of the CTA: an int8
+// row whose amax is NaN takes a second, NaN-ignoring amax through red_max2
+// (W floats of its own) and a barrier.
 template <int T, int K, int OUT>
 __device__ __forceinline__ void quant_row_finish(const Params& p, const float (&y)[K][8], float m, int64_t row,
                                                  int tid, int lane, int warp, int nblocks, float* red_max2)
@@ -374,7 +387,7 @@ __device__ __forceinline__ void quant_row_finish(const Params& p, const float (&
 #pragma unroll
             for (int j = 0; j < K; ++j) {
                 const int b = tid + j * T;
-                if (b < nblocks) {
+                if (block_in_row<K>(j, b, nblocks)) {
                     uint32_t differ = 0u;
                     uint2 code = quantize8_bracket(y[j], qs, differ);
                     if (!qs.fast || differ != 0u)
@@ -397,7 +410,7 @@ __device__ __forceinline__ void quant_row_finish(const Params& p, const float (&
 #pragma unroll
             for (int j = 0; j < K; ++j) {
                 const int b = tid + j * T;
-                if (b < nblocks)
+                if (block_in_row<K>(j, b, nblocks))
                     st_stream(qrow + b, quantize8_exact(y[j], scale));
             }
         }
@@ -412,7 +425,7 @@ __device__ __forceinline__ void quant_row_finish(const Params& p, const float (&
 #pragma unroll
             for (int j = 0; j < K; ++j) {
                 const int b = tid + j * T;
-                if (b < nblocks)
+                if (block_in_row<K>(j, b, nblocks))
                     __stcs(prow + b, quantize8_e2m1(y[j], qs));
             }
         } else {
@@ -420,7 +433,7 @@ __device__ __forceinline__ void quant_row_finish(const Params& p, const float (&
 #pragma unroll
             for (int j = 0; j < K; ++j) {
                 const int b = tid + j * T;
-                if (b < nblocks)
+                if (block_in_row<K>(j, b, nblocks))
                     st_stream(qrow + b, quantize8_e4m3(y[j], qs));
             }
         }
@@ -528,7 +541,7 @@ __global__ void __launch_bounds__(T, staged_min_blocks(T, K)) staged_kernel(cons
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             const int b = tid + j * T;
-            if (b < nblocks) {
+            if (block_in_row<K>(j, b, nblocks)) {
                 float f[8];
                 unpack8(__ldg(wrow + b), f);
                 w_lo[b] = make_float4(f[0], f[1], f[2], f[3]);
@@ -557,14 +570,14 @@ __global__ void __launch_bounds__(T, staged_min_blocks(T, K)) staged_kernel(cons
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             const int b = tid + j * T;
-            if (b < nblocks) {
+            if (block_in_row<K>(j, b, nblocks)) {
                 xv[j] = xs[b];
                 if constexpr (ADD)
                     rv[j] = rs[b];
             }
         }
         float acc[K][8], part[K];
-        row_accumulate<K, ADD>(p, xv, rv, acc, part, row, true, tid, T, nblocks);
+        row_accumulate<K, ADD, true>(p, xv, rv, acc, part, row, true, tid, T, nblocks);
 
         int jsub;
         float v = warp_halving_sum<K>(part, lane, jsub);
@@ -599,7 +612,7 @@ __global__ void __launch_bounds__(T, staged_min_blocks(T, K)) staged_kernel(cons
 #pragma unroll
             for (int j = 0; j < K; ++j) {
                 const int b = tid + j * T;
-                if (b < nblocks)
+                if (block_in_row<K>(j, b, nblocks))
                     scale8_f32(acc[j], inv, w_lo[b], w_hi[b]);
             }
             staged_quant_row<T, K, OUT>(p, acc, row, tid, lane, warp, nblocks, s_max[buf], s_max2);
@@ -683,7 +696,7 @@ __global__ void __launch_bounds__(T, staged_min_blocks(T, 2 * K)) staged_pair_ke
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             const int b = tid + j * T;
-            if (b < nblocks) {
+            if (block_in_row<K>(j, b, nblocks)) {
                 float f[8];
                 unpack8(__ldg(wrow + b), f);
                 w_lo[b] = make_float4(f[0], f[1], f[2], f[3]);
@@ -706,7 +719,7 @@ __global__ void __launch_bounds__(T, staged_min_blocks(T, 2 * K)) staged_pair_ke
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             const int b = tid + j * T;
-            if (b < nblocks) {
+            if (block_in_row<K>(j, b, nblocks)) {
                 unpack8(xs0[b], a0[j]);
                 part0[j] = fold8_squares(a0[j]);
                 if (two) {
@@ -766,7 +779,7 @@ __global__ void __launch_bounds__(T, staged_min_blocks(T, 2 * K)) staged_pair_ke
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             const int b = tid + j * T;
-            if (b < nblocks) {
+            if (block_in_row<K>(j, b, nblocks)) {
                 const float4 wl = w_lo[b], wh = w_hi[b];
                 scale8_f32(a0[j], inv0, wl, wh);
                 scale8_f32(a1[j], inv1, wl, wh);
