@@ -228,6 +228,29 @@ def test_auto_plain_quantised_takes_the_pair_kernel(L, n, h, T):
     assert dr.resolve_config(64, 32768, quant=True, add=False, sm_count=152).rows_per_cta == 1
 
 
+def test_staged_threads_cover_the_padded_row(L):
+    """Every staged and pair launch resolve accepts has T threads of K
+    blocks covering the padded row exactly (T * K * 8 = P), so the first
+    K / 2 blocks of every thread lie in the row: the kernels skip the
+    bounds test there."""
+    accepted = 0
+    for h in range(8, dr.MAX_HIDDEN + 1, 8):
+        P = 1 << (h - 1).bit_length()
+        for T in (32, 64, 128, 256, 512, 1024):
+            for rows, kw in ((1, dict(add=True)), (2, dict(quant=True, add=False))):
+                cfg = dr.LaunchConfig(variant=dr.VARIANT_STAGED, threads_per_row=T, rows_per_cta=rows)
+                try:
+                    c = dr.resolve_config(64, h, sm_count=152, config=cfg, **kw)
+                except dr.DraddError:
+                    continue
+                accepted += 1
+                K = c.blocks_per_thread
+                assert c.threads_per_row == T and T * K * 8 == P, (h, T, rows)
+                if K >= 2:
+                    assert (T - 1) + (K // 2 - 1) * T < h // 8, (h, T, K)
+    assert accepted > 10000
+
+
 def test_staged_stages_limited_by_shared_memory(L):
     with pytest.raises(dr.DraddError):
         dr.resolve_config(16, 32768, sm_count=152, config=dr.LaunchConfig(variant=2, stages=2))
