@@ -53,6 +53,28 @@ def test_input_recipes_draw_the_stated_distributions():
         assert torch.equal(head["x"], c["x"][:5]) and torch.equal(head["residual"], c["residual"][:5])
 
 
+def test_reference_arm_line():
+    """`bench.py --impl reference` runs the CPU oracle on the headline
+    workload (no GPU needed) and prints one JSON line with the keys the
+    measurement contract names, on the same metric, unit and workload as
+    the library's arm."""
+    import json
+    import subprocess
+    import sys
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3"],
+                         cwd=bench.ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["higher_is_better"] is True and d["steps"] == 1 and d["warmup"] == 3 and d["value"] > 0
+    assert d["config"]["workload"] == bench.workload_desc("4096x4096")
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
 def test_launch_variant_names():
     """config.launch names the variant the automatic plan resolves to, for
     every main-op workload (152 SMs)."""
